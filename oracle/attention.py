@@ -1,0 +1,88 @@
+"""Oracle for variable-length (cu_seqlens) softmax attention.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+Source: "Variable-length attention and data packing":
+  * "What it is": the packed batch is one concatenated sequence plus
+    cu_seqlens, and attention is computed only within each real sequence;
+  * "How it works": query rows of a sequence see only that sequence's keys,
+    so the cost is the sum of per-sequence len^2 terms;
+  * "Core math" (C): a block-diagonal mask seg[i] == seg[j] applied to the
+    scores with -inf off the diagonal blocks gives zero cross-sample mass and
+    rows that still sum to one.
+"DanLing NestedTensor", section 3.3 "Attention through packed blocks": the
+output adopts the query structure (token-major, static head and feature axes).
+
+Readings: non-causal; scale passed in (d^-1/2 by default); the log-sum-exp is
+natural-log, lse[h, t] = log sum_k exp(scale * q_t . k_k) over t's segment.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+
+def _softmax_rows(S: np.ndarray) -> np.ndarray:
+    S = S - S.max(axis=-1, keepdims=True)
+    E = np.exp(S)
+    return E / E.sum(axis=-1, keepdims=True)
+
+
+def segment_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
+    """Dense attention of one segment: q, k, v are (n, H, d).  Returns O
+    (n, H, d) and lse (H, n)."""
+    n, H, d = q.shape
+    O = np.zeros((n, H, v.shape[2]))
+    lse = np.zeros((H, n))
+    for h in range(H):
+        S = (q[:, h, :] @ k[:, h, :].T) * scale            # (n, n) explicit scores
+        A = _softmax_rows(S)
+        O[:, h, :] = A @ v[:, h, :]
+        mx = S.max(axis=1)
+        lse[h] = mx + np.log(np.exp(S - mx[:, None]).sum(axis=1))
+    return O, lse
+
+
+def varlen_attention(q, k, v, cu_seqlens: Sequence[int], scale: Optional[float] = None,
+                     segments: Optional[Sequence[int]] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Attention restricted to each [cu[b], cu[b+1]) segment, one segment at a
+    time.  ``segments`` limits the work to the listed segment indices (the
+    other rows of O and lse stay zero)."""
+    T, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    O = np.zeros((T, H, v.shape[2]))
+    lse = np.zeros((H, T))
+    B = len(cu_seqlens) - 1
+    for b in (range(B) if segments is None else segments):
+        lo, hi = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        if hi == lo:
+            continue
+        O[lo:hi], lse[:, lo:hi] = segment_attention(q[lo:hi], k[lo:hi], v[lo:hi], scale)
+    return O, lse
+
+
+def masked_full_attention(q, k, v, seg_ids: Sequence[int], scale: Optional[float] = None):
+    """Full T x T attention with scores set to -inf wherever
+    seg[i] != seg[j] ("Core math" (C)).  Tiny inputs only.  Returns O and the
+    attention matrices A (H, T, T)."""
+    T, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    seg = np.asarray(seg_ids)
+    block = seg[:, None] == seg[None, :]
+    O = np.zeros((T, H, v.shape[2]))
+    A_all = np.zeros((H, T, T))
+    for h in range(H):
+        S = (q[:, h, :] @ k[:, h, :].T) * scale
+        A = _softmax_rows(np.where(block, S, -np.inf))
+        A_all[h] = A
+        O[:, h, :] = A @ v[:, h, :]
+    return O, A_all
+
+
+def attention_flops(seqlens: Sequence[int], H: int, d: int) -> int:
+    """Algorithmic flops of non-causal varlen attention: QK^T and PV, each
+    2 * n^2 * d per head and segment."""
+    return int(sum(4 * int(n) * int(n) * H * d for n in seqlens))

@@ -1,0 +1,287 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each pin takes the oracle callables it checks as arguments, so the same pin
+runs against the real oracle (``test_oracle_pins.py``) and against copies
+with a planted mistake (``test_oracle_mutations.py``), which must fail it.
+None of these checks re-types the oracle's own formula: each compares it
+with a printed value, a closed form, a library routine on a special case,
+an invariant or a brute-force enumeration.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from _helpers import golden
+
+
+# ----------------------------------------------------------------------------
+# Partitions ("DanLing NestedTensor" Eq. 2, Eq. 3, Figure 2, Appendix A)
+# ----------------------------------------------------------------------------
+
+def pin_fig2(partition):
+    g = golden("fig2_partition.json")
+    p = partition(g["lengths"])
+    pr, dv = g["printed"], g["derived_from_prose"]
+    assert p.T == pr["single_positions"]
+    assert p.P == pr["pair_cells"]
+    assert list(p.cu_seqlens) == pr["single_offsets"]
+    assert list(p.pair_off) == pr["pair_offsets"]
+    assert len(p.row_start) == pr["second_level_split_entries"]
+    assert list(p.row_start) == dv["second_level_splits"]
+
+
+def pin_partition_invariants(partition, lengths):
+    p = partition(lengths)
+    N = np.asarray(lengths, dtype=np.int64)
+    # Appendix A: o_0 = 0, o_{i+1} - o_i = p_i, o_B = T
+    assert p.cu_seqlens[0] == 0 and p.pair_off[0] == 0
+    assert np.array_equal(np.diff(p.cu_seqlens), N)
+    assert np.array_equal(np.diff(p.pair_off), N * N)
+    assert p.cu_seqlens[-1] == p.T == N.sum()
+    assert p.pair_off[-1] == p.P == (N * N).sum()
+    assert len(p.row_start) == 1 + N.sum()
+    assert p.max_len == (N.max() if len(N) else 0)
+
+
+def pin_partition_bruteforce(partition, lengths):
+    """Walk every (sample, a, b) in order: Eq. 3 must number the cells
+    0, 1, 2, ... consecutively, and each row's first cell is its split."""
+    p = partition(lengths)
+    cell = 0
+    row = 0
+    for i, n in enumerate(lengths):
+        for a in range(n):
+            assert p.row_start[row] == cell
+            assert p.row_sample[row] == i
+            for b in range(n):
+                assert p.pair_off[i] + a * n + b == cell
+                cell += 1
+            row += 1
+    assert row == p.T and cell == p.P and p.row_start[-1] == cell
+
+
+# ----------------------------------------------------------------------------
+# Block ("DanLing NestedTensor" Eq. 1, Eq. 4)
+# ----------------------------------------------------------------------------
+
+def pin_broadcast_onehot(pair_broadcast, rng):
+    """One-hot projections select single features: with W_a picking feature
+    f of X[a] and W_b zero, cell (a, b) holds X[a, f]; swapped, it holds
+    X[b, g].  Fixes the order of a and b and the orientation of W."""
+    lengths = [3, 1, 4, 0, 2]
+    C, C_p = 5, 3
+    T = sum(lengths)
+    s = rng.standard_normal((T, C))
+    Wsel = np.zeros((C_p, C))
+    Wsel[0, 2] = 1.0
+    Wsel[1, 4] = 1.0
+    Wsel[2, 0] = 1.0
+    Z = np.zeros((C_p, C))
+    za = pair_broadcast(lengths, s, s, Wsel, Z)
+    zb = pair_broadcast(lengths, s, s, Z, Wsel)
+    z0 = pair_broadcast(lengths, s, s, Z, Z)
+    assert za.shape == (sum(n * n for n in lengths), C_p)
+    assert np.all(z0 == 0.0)
+    cell, start = 0, 0
+    for n in lengths:
+        for a in range(n):
+            for b in range(n):
+                assert np.array_equal(za[cell], s[start + a, [2, 4, 0]])
+                assert np.array_equal(zb[cell], s[start + b, [2, 4, 0]])
+                cell += 1
+        start += n
+
+
+def pin_broadcast_left_right(pair_broadcast, rng):
+    """Distinct left/right singles: cell (a, b) = X_L[a] W_a^T + X_R[b] W_b^T,
+    checked with torch's linear on each cell (brute force)."""
+    lengths = [2, 3]
+    C, C_p = 4, 3
+    T = sum(lengths)
+    sL, sR = rng.standard_normal((T, C)), rng.standard_normal((T, C))
+    Wa, Wb = rng.standard_normal((C_p, C)), rng.standard_normal((C_p, C))
+    z = pair_broadcast(lengths, sL, sR, Wa, Wb)
+    tL, tR = torch.from_numpy(sL), torch.from_numpy(sR)
+    ta, tb = torch.from_numpy(Wa), torch.from_numpy(Wb)
+    cell, start = 0, 0
+    for n in lengths:
+        for a in range(n):
+            for b in range(n):
+                ref = F.linear(tL[start + a], ta) + F.linear(tR[start + b], tb)
+                assert np.allclose(z[cell], ref.numpy(), rtol=1e-13, atol=1e-13)
+                cell += 1
+        start += n
+
+
+def pin_transition_library(pair_transition, rng, biases=True):
+    """On any cells, LN -> Linear -> ReLU -> Linear plus residual equals
+    torch.nn.functional's layer_norm / linear / relu in float64."""
+    P, C_p, H = 37, 8, 24
+    z = rng.standard_normal((P, C_p)) * 3.0 + 0.5
+    gamma = 1.0 + 0.1 * rng.standard_normal(C_p)
+    beta = 0.1 * rng.standard_normal(C_p)
+    W1, W2 = rng.standard_normal((H, C_p)), rng.standard_normal((C_p, H))
+    b1 = rng.standard_normal(H) if biases else None
+    b2 = rng.standard_normal(C_p) if biases else None
+    got = pair_transition(z, gamma, beta, 1e-5, W1, b1, W2, b2)
+    tz = torch.from_numpy(z)
+    ln = F.layer_norm(tz, (C_p,), torch.from_numpy(gamma), torch.from_numpy(beta), 1e-5)
+    hid = F.relu(F.linear(ln, torch.from_numpy(W1), None if b1 is None else torch.from_numpy(b1)))
+    ref = tz + F.linear(hid, torch.from_numpy(W2), None if b2 is None else torch.from_numpy(b2))
+    assert np.allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_transition_identity(pair_transition, rng):
+    """W2 = 0 and b2 = 0: the update vanishes and z~ = z exactly."""
+    z = rng.standard_normal((11, 6))
+    out = pair_transition(z, np.ones(6), np.zeros(6), 1e-5, rng.standard_normal((10, 6)),
+                          rng.standard_normal(10), np.zeros((6, 10)), None)
+    assert np.array_equal(out, z)
+
+
+def pin_layernorm_constant(layer_norm, rng):
+    """A constant-feature cell normalises to beta exactly."""
+    beta = rng.standard_normal(7)
+    x = np.full((3, 7), 2.5)
+    assert np.array_equal(layer_norm(x, rng.standard_normal(7), beta, 1e-5), np.broadcast_to(beta, (3, 7)))
+
+
+def pin_reduce_closed_form(pair_broadcast, pair_reduce, rng):
+    """Without a transition, mean_b (U[a] + V[b]) = U[a] + mean_b V[b]."""
+    lengths = [4, 1, 0, 3, 6]
+    C, C_p = 5, 4
+    T = sum(lengths)
+    s = rng.standard_normal((T, C))
+    Wa, Wb = rng.standard_normal((C_p, C)), rng.standard_normal((C_p, C))
+    z = pair_broadcast(lengths, s, s, Wa, Wb)
+    m, _ = pair_reduce(lengths, z)
+    U, V = s @ Wa.T, s @ Wb.T
+    start = 0
+    for n in lengths:
+        for a in range(n):
+            ref = U[start + a] + V[start:start + n].sum(axis=0) / n
+            assert np.allclose(m[start + a], ref, rtol=1e-12, atol=1e-12)
+        start += n
+
+
+def pin_reduce_invariants(pair_reduce, rng):
+    """A per-sample constant pair state reduces to that constant; N_i = 1
+    returns the cell itself; sum_a N_i m[a] equals the sample's cell sum."""
+    lengths = [3, 1, 5]
+    C_p = 4
+    consts = rng.standard_normal((3, C_p))
+    z = np.concatenate([np.broadcast_to(consts[i], (n * n, C_p)) for i, n in enumerate(lengths)])
+    m, _ = pair_reduce(lengths, z)
+    assert np.allclose(m[:3], consts[0], rtol=1e-14, atol=1e-14)
+    assert np.array_equal(m[3], consts[1])
+    assert np.allclose(m[4:], consts[2], rtol=1e-14, atol=1e-14)
+    z = rng.standard_normal((sum(n * n for n in lengths), C_p))
+    m, _ = pair_reduce(lengths, z)
+    assert np.array_equal(m[3], z[9])
+    cell, row = 0, 0
+    for n in lengths:
+        assert np.allclose(n * m[row:row + n].sum(axis=0), z[cell:cell + n * n].sum(axis=0),
+                           rtol=1e-12, atol=1e-12)
+        cell += n * n
+        row += n
+
+
+def pin_reduce_bruteforce(pair_reduce, rng):
+    """Eq. 4 walked cell by cell: rows of sample i start at eta_i, cells at
+    o_i + a N_i + b; the g projection and residual via torch."""
+    lengths = [2, 3, 1]
+    C_p, C = 3, 4
+    z = rng.standard_normal((sum(n * n for n in lengths), C_p))
+    s_in = rng.standard_normal((sum(lengths), C))
+    Wg, bg = rng.standard_normal((C, C_p)), rng.standard_normal(C)
+    m, s_out = pair_reduce(lengths, z, Wg, bg, s_in)
+    o, eta = 0, 0
+    for n in lengths:
+        for a in range(n):
+            acc = np.zeros(C_p)
+            for b in range(n):
+                acc = acc + z[o + a * n + b]
+            assert np.allclose(m[eta + a], acc / n, rtol=1e-13, atol=1e-13)
+            ref = torch.from_numpy(s_in[eta + a]) + F.linear(torch.from_numpy(acc / n),
+                                                             torch.from_numpy(Wg), torch.from_numpy(bg))
+            assert np.allclose(s_out[eta + a], ref.numpy(), rtol=1e-12, atol=1e-12)
+        o += n * n
+        eta += n
+
+
+def pin_packed_equals_padded(block_packed, block_padded_gathered, weights, lengths, s):
+    """Packed results equal the padded-then-gathered ones on valid cells
+    ("DanLing NestedTensor" Appendix A, reference semantics)."""
+    a = block_packed(lengths, s, weights)
+    b = block_padded_gathered(lengths, s, weights)
+    for name in ("z", "z_tilde", "m", "s_out"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert x.shape == y.shape, name
+        assert np.allclose(x, y, rtol=1e-11, atol=1e-11), name
+
+
+# ----------------------------------------------------------------------------
+# Attention ("Variable-length attention and data packing")
+# ----------------------------------------------------------------------------
+
+def pin_attention_single_segment_sdpa(varlen_attention, rng):
+    """One segment is plain dense attention: torch's scaled_dot_product_attention
+    (float64, non-causal, default scale d^-1/2)."""
+    n, H, d = 13, 3, 8
+    q, k, v = (rng.standard_normal((n, H, d)) for _ in range(3))
+    O, lse = varlen_attention(q, k, v, [0, n])
+    tq, tk, tv = (torch.from_numpy(x).permute(1, 0, 2) for x in (q, k, v))
+    ref = F.scaled_dot_product_attention(tq, tk, tv).permute(1, 0, 2).numpy()
+    assert np.allclose(O, ref, rtol=1e-12, atol=1e-12)
+    S = torch.einsum("hnd,hmd->hnm", tq, tk) / np.sqrt(d)
+    assert np.allclose(lse, torch.logsumexp(S, dim=-1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_attention_masked_core_math(masked_full_attention, rng):
+    """The page's nine-token example: masked rows sum to one with zero
+    cross-sample mass; without the mask the softmax leaks above 1e-3."""
+    g = golden("core_math_mask.json")
+    seg = np.asarray(g["segment_ids"])
+    T, H, d = len(seg), 2, 4
+    q, k, v = (rng.standard_normal((T, H, d)) for _ in range(3))
+    _, A = masked_full_attention(q, k, v, seg)
+    block = seg[:, None] == seg[None, :]
+    assert np.all(A[:, ~block] == 0.0)
+    assert np.allclose(A.sum(axis=-1), 1.0, rtol=0, atol=1e-14)
+    _, A_leak = masked_full_attention(q, k, v, np.zeros(T, dtype=int))
+    assert A_leak[:, ~block].max() > g["leak_threshold"]
+
+
+def pin_attention_varlen_equals_masked(varlen_attention, masked_full_attention, rng):
+    """Per-segment attention equals the full T x T block-diagonal masked
+    attention on a tiny stream (brute force)."""
+    g = golden("core_math_mask.json")
+    cu = g["cu_seqlens"] + [12]   # add a fourth segment of 3 tokens
+    seg = np.repeat(np.arange(len(cu) - 1), np.diff(cu))
+    T, H, d = cu[-1], 2, 5
+    q, k, v = (rng.standard_normal((T, H, d)) for _ in range(3))
+    O1, _ = varlen_attention(q, k, v, cu)
+    O2, _ = masked_full_attention(q, k, v, seg)
+    assert np.allclose(O1, O2, rtol=1e-12, atol=1e-12)
+
+
+def pin_attention_special_cases(varlen_attention, rng):
+    """A length-1 segment returns its own v; a segment whose v is constant
+    returns that constant; changing one segment's tokens leaves every other
+    segment's output bit-identical (zero leakage)."""
+    cu = [0, 1, 5, 5, 12]
+    T, H, d = 12, 2, 4
+    q, k, v = (rng.standard_normal((T, H, d)) for _ in range(3))
+    v[5:12] = rng.standard_normal((1, H, d))
+    O, _ = varlen_attention(q, k, v, cu)
+    assert np.allclose(O[0], v[0], rtol=1e-15, atol=1e-15)
+    assert np.allclose(O[5:12], v[5:12], rtol=1e-13, atol=1e-13)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    q2[1:5] += 1.0
+    k2[1:5] *= -2.0
+    v2[1:5] = rng.standard_normal((4, H, d))
+    O2, _ = varlen_attention(q2, k2, v2, cu)
+    assert np.array_equal(O2[:1], O[:1]) and np.array_equal(O2[5:], O[5:])
+    assert not np.allclose(O2[1:5], O[1:5])

@@ -1,0 +1,182 @@
+"""Planted mistakes in copies of the oracle must fail the pins.
+
+Each case builds a wrong variant of one oracle function on the CPU (a dropped
+term, a swapped index, a transposed operand, a wrong divisor) and checks that
+at least one pin rejects it.  The real oracle is never modified.
+"""
+import numpy as np
+import pytest
+
+import _pins as pins
+from oracle import partition as opart
+from oracle import block as oblock
+from oracle import attention as oattn
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def _fails(fn, *args):
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        fn(*args)
+
+
+# --- partitions --------------------------------------------------------------
+
+def inclusive_scan_partition(lengths):
+    p = opart.partition(lengths)
+    p.pair_off = np.concatenate([np.cumsum(p.lengths ** 2), [p.P]])
+    return p
+
+
+def row_major_swap_partition(lengths):
+    p = opart.partition(lengths)           # row splits stride by 1 instead of N_i
+    rs = []
+    for i, n in enumerate(p.lengths):
+        rs += [int(p.pair_off[i]) + a for a in range(int(n))]
+    p.row_start = np.asarray(rs + [p.P])
+    return p
+
+
+def test_inclusive_scan_caught():
+    _fails(pins.pin_fig2, inclusive_scan_partition)
+
+
+def test_row_split_stride_caught():
+    _fails(pins.pin_fig2, row_major_swap_partition)
+    _fails(pins.pin_partition_bruteforce, row_major_swap_partition, [2, 3])
+
+
+# --- broadcast ---------------------------------------------------------------
+
+def broadcast_swapped_ab(lengths, s_left, s_right, W_a, W_b):
+    z = oblock.pair_broadcast(lengths, s_left, s_right, W_a, W_b)
+    part = opart.partition(lengths)
+    out = z.copy()
+    for i, n in enumerate(part.lengths):
+        n = int(n)
+        o = int(part.pair_off[i])
+        out[o:o + n * n] = z[o:o + n * n].reshape(n, n, -1).transpose(1, 0, 2).reshape(n * n, -1)
+    return out
+
+
+def broadcast_transposed_weight(lengths, s_left, s_right, W_a, W_b):
+    # uses W instead of W^T where shapes allow; otherwise the pad makes it fail
+    Wa = W_a.T[: W_a.shape[0], : W_a.shape[1]] if W_a.shape[0] <= W_a.shape[1] else W_a
+    return oblock.pair_broadcast(lengths, s_left, s_right,
+                                 np.pad(Wa, ((0, W_a.shape[0] - Wa.shape[0]), (0, W_a.shape[1] - Wa.shape[1]))),
+                                 W_b)
+
+
+def test_broadcast_swapped_ab_caught():
+    _fails(pins.pin_broadcast_onehot, broadcast_swapped_ab, rng(1))
+
+
+def test_broadcast_transposed_weight_caught():
+    _fails(pins.pin_broadcast_onehot, broadcast_transposed_weight, rng(1))
+
+
+# --- transition --------------------------------------------------------------
+
+def transition_no_residual(z, gamma, beta, eps, W1, b1, W2, b2):
+    return oblock.pair_transition(z, gamma, beta, eps, W1, b1, W2, b2) - z
+
+
+def transition_unbiased_var(z, gamma, beta, eps, W1, b1, W2, b2):
+    mu = z.mean(axis=-1, keepdims=True)
+    var = z.var(axis=-1, ddof=1, keepdims=True)
+    ln = (z - mu) / np.sqrt(var + eps) * gamma + beta
+    return z + oblock.h_theta(ln, W1, b1, W2, b2)
+
+
+def transition_relu_after_second(z, gamma, beta, eps, W1, b1, W2, b2):
+    ln = oblock.layer_norm(z, gamma, beta, eps)
+    return z + np.maximum(oblock.linear(oblock.linear(ln, W1, b1), W2, b2), 0.0)
+
+
+def transition_no_beta(z, gamma, beta, eps, W1, b1, W2, b2):
+    return oblock.pair_transition(z, gamma, np.zeros_like(beta), eps, W1, b1, W2, b2)
+
+
+@pytest.mark.parametrize("bad", [transition_no_residual, transition_unbiased_var,
+                                 transition_relu_after_second, transition_no_beta])
+def test_transition_mistakes_caught(bad):
+    _fails(pins.pin_transition_library, bad, rng(4), True)
+
+
+def test_dropped_residual_caught_by_identity():
+    _fails(pins.pin_transition_identity, transition_no_residual, rng(5))
+
+
+# --- reduce ------------------------------------------------------------------
+
+def reduce_over_rows(lengths, z, W_g=None, b_g=None, s_in=None):
+    part = opart.partition(lengths)
+    zt = z.copy()
+    for i, n in enumerate(part.lengths):
+        n = int(n)
+        o = int(part.pair_off[i])
+        zt[o:o + n * n] = z[o:o + n * n].reshape(n, n, -1).transpose(1, 0, 2).reshape(n * n, -1)
+    return oblock.pair_reduce(lengths, zt, W_g, b_g, s_in)
+
+
+def reduce_divide_by_max(lengths, z, W_g=None, b_g=None, s_in=None):
+    m, s_out = oblock.pair_reduce(lengths, z, W_g, b_g, s_in)
+    part = opart.partition(lengths)
+    for i, n in enumerate(part.lengths):
+        m[part.cu_seqlens[i]:part.cu_seqlens[i + 1]] *= n / max(part.max_len, 1)
+    return m, s_out
+
+
+def reduce_no_residual(lengths, z, W_g=None, b_g=None, s_in=None):
+    return oblock.pair_reduce(lengths, z, W_g, b_g, None)
+
+
+def test_reduce_wrong_axis_caught():
+    _fails(pins.pin_reduce_closed_form, oblock.pair_broadcast, reduce_over_rows, rng(7))
+
+
+def test_reduce_wrong_divisor_caught():
+    _fails(pins.pin_reduce_invariants, reduce_divide_by_max, rng(8))
+
+
+def test_reduce_dropped_residual_caught():
+    _fails(pins.pin_reduce_bruteforce, reduce_no_residual, rng(9))
+
+
+# --- attention ---------------------------------------------------------------
+
+def attention_no_scale(q, k, v, cu, scale=None, segments=None):
+    return oattn.varlen_attention(q, k, v, cu, 1.0, segments)
+
+
+def attention_no_mask(q, k, v, cu, scale=None, segments=None):
+    T = q.shape[0]
+    return oattn.varlen_attention(q, k, v, [0, T], scale)
+
+
+def attention_off_by_one(q, k, v, cu, scale=None, segments=None):
+    cu2 = [cu[0]] + [min(c + 1, cu[-1]) for c in cu[1:-1]] + [cu[-1]]
+    return oattn.varlen_attention(q, k, v, cu2, scale)
+
+
+def masked_leaky(q, k, v, seg, scale=None):
+    return oattn.masked_full_attention(q, k, v, np.zeros(len(seg), dtype=int), scale)
+
+
+def test_attention_scale_caught():
+    _fails(pins.pin_attention_single_segment_sdpa, attention_no_scale, rng(13))
+
+
+def test_attention_mask_caught():
+    _fails(pins.pin_attention_special_cases, attention_no_mask, rng(16))
+    _fails(pins.pin_attention_varlen_equals_masked, attention_no_mask, oattn.masked_full_attention, rng(15))
+
+
+def test_attention_boundary_caught():
+    _fails(pins.pin_attention_varlen_equals_masked, attention_off_by_one, oattn.masked_full_attention, rng(15))
+
+
+def test_masked_without_mask_caught():
+    _fails(pins.pin_attention_masked_core_math, masked_leaky, rng(14))
