@@ -1,0 +1,484 @@
+"""Benchmark of the packed single->pair->single block and varlen attention.
+
+One step is one pass of the whole hot path:
+  * the block on the B=8 Pairformer-style batch (N_i ~ U[64, 256], C_s=384,
+    C_z=128, transition 128->512->128, bf16 I/O, fp32 accumulation):
+    partition build + row splits, pair broadcast, transition, reduce + g;
+  * varlen attention on the packed stream of 65,536 tokens (segments
+    ~ U[16, 512], 12 heads x 64, bf16, non-causal).
+``value`` is packed pair cells per second of the block (the block's P over
+its device time per step); the attention's TFLOPS ride beside it in
+``attn``.  L2 is flushed (a 512 MB write) before every timed step, outside
+the timed events.  ``--impl reference`` times the CPU oracle instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun every rank runs its own replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+os.environ.setdefault("OMP_NUM_THREADS", str(os.cpu_count() or 1))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from variable_length_batching_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "packed pair cells/sec per block and varlen attn TFLOPS; % of HBM/tensor roofline"
+BLOCK_CFG = wl.PAIRFORMER_BF16
+ATTN_CFG = wl.VARLEN_ATTN_BF16
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+# kernels of ours launched per step: partition scan, partition rows,
+# projection, broadcast, transition, reduce, g projection, attention
+LAUNCHES_PER_STEP = 8
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel: str):
+    """Per-launch DRAM bytes from a committed ncu capture, or None when the
+    kernel's source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "variable_length_batching_gb300", "csrc", rec["source"])
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha"]:
+            return None
+    return rec["bytes_per_launch"]
+
+
+# ----------------------------------------------------------------------------
+# Algorithmic work per call (what the method must do, not padded work)
+# ----------------------------------------------------------------------------
+
+def block_work(T, P, C_s, C_z, H_t, es=2):
+    return {
+        "partition": {"bytes": 0, "flops": 0},
+        # writes P*C_z outputs; reads singles and weights; u, v (fp32) written once, read once
+        "broadcast": {"bytes": P * C_z * es + T * C_s * es + 2 * C_z * C_s * es + 2 * 2 * T * C_z * 4,
+                      "flops": 2 * 2 * T * C_s * C_z},
+        # reads and writes every cell once; 2 GEMMs of C_z x H_t per cell
+        "transition": {"bytes": 2 * P * C_z * es + 2 * H_t * C_z * es, "flops": 4 * C_z * H_t * P},
+        # reads every cell once; writes m, reads s_in, writes s_out
+        "reduce": {"bytes": P * C_z * es + T * C_z * es + 2 * T * C_s * es + C_s * C_z * es,
+                   "flops": 2 * T * C_z * C_s},
+    }
+
+
+def attn_work(seqlens, H, d, es=2):
+    n = np.asarray(seqlens, dtype=np.int64)
+    return {"bytes": 4 * int(n.sum()) * H * d * es, "flops": 4 * int((n * n).sum()) * H * d}
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        if self.out:
+            self.out.close()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def _dev_weights(w, dev):
+    from types import SimpleNamespace
+    g = lambda t: None if t is None else t.to(dev)
+    return SimpleNamespace(W_a=g(w.W_a), W_b=g(w.W_b), ln_gamma=g(w.ln_gamma), ln_beta=g(w.ln_beta),
+                           W1=g(w.W1), b1=g(w.b1), W2=g(w.W2), b2=g(w.b2), W_g=g(w.W_g), b_g=g(w.b_g))
+
+
+def run_gpu(args, rank, world, local_rank):
+    from variable_length_batching_gb300 import build, nt
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs, resident in HBM before the timed region ----
+    binp = wl.make_block_inputs(BLOCK_CFG)
+    w = _dev_weights(binp.blocks[0], dev)
+    lengths_d = torch.as_tensor(binp.lengths).to(dev)
+    s_d = binp.s.to(dev)
+    ainp = wl.make_attn_inputs(ATTN_CFG)
+    cu_host = np.concatenate([[0], np.cumsum(ainp.seqlens)]).astype(np.int32)
+    cu_d = torch.as_tensor(cu_host).to(dev)
+    q_d, k_d, v_d = ainp.q.to(dev), ainp.k.to(dev), ainp.v.to(dev)
+    max_len = int(ainp.seqlens.max())
+    o_d = torch.empty_like(q_d)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    part = nt.nt_partition_build(lengths_d)
+    T, P = part.T, part.P
+    C_s, C_z, H_t = BLOCK_CFG.C_s, BLOCK_CFG.C_z, BLOCK_CFG.H_t
+    z_d = torch.empty(P, C_z, dtype=torch.bfloat16, device=dev)
+    ws_d = torch.empty(nt.nt_pair_broadcast_workspace_bytes(T, C_z), dtype=torch.uint8, device=dev)
+    m_d = torch.empty(T, C_z, dtype=torch.bfloat16, device=dev)
+    sout_d = torch.empty(T, C_s, dtype=torch.bfloat16, device=dev)
+
+    names = ("partition", "broadcast", "transition", "reduce", "attention")
+
+    def step(ev):
+        ev[0].record(stream)
+        p = nt.nt_partition_build(lengths_d, stream=stream)
+        ev[1].record(stream)
+        nt.nt_pair_broadcast(p, s_d, s_d, w.W_a, w.W_b, z=z_d, workspace=ws_d, stream=stream)
+        ev[2].record(stream)
+        nt.nt_pair_transition(p, z_d, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2, out=z_d,
+                              stream=stream)
+        ev[3].record(stream)
+        nt.nt_pair_reduce(p, z_d, w.W_g, w.b_g, s_in=s_d, m=m_d, s_out=sout_d, stream=stream)
+        ev[4].record(stream)
+        nt.nt_varlen_attn(q_d, k_d, v_d, cu_d, max_len, out=o_d, stream=stream)
+        ev[5].record(stream)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step(new_events())
+    nt.nt_device_status(stream)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    with ClockSampler(local_rank) as clk:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush.fill_(float(len(evs)))     # L2 flush, outside the step's events
+            ev = new_events()
+            step(ev)
+            evs.append(ev)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    nt.nt_device_status(stream)
+
+    per = {n: [] for n in names}
+    for ev in evs:
+        for i, n in enumerate(names):
+            per[n].append(ev[i].elapsed_time(ev[i + 1]))
+    ms = {n: float(np.mean(v)) for n, v in per.items()}
+    block_ms = ms["partition"] + ms["broadcast"] + ms["transition"] + ms["reduce"]
+    step_ms = block_ms + ms["attention"]
+    if world > 1:
+        t = torch.tensor([block_ms, ms["attention"], step_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        block_ms_max, attn_ms_max, step_ms_max = (float(x) for x in t.tolist())
+    else:
+        block_ms_max, attn_ms_max, step_ms_max = block_ms, ms["attention"], step_ms
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = run_e2e(nt, binp, ainp, cu_host, dev, stream, args)
+
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    work = block_work(T, P, C_s, C_z, H_t)
+    aw = attn_work(ainp.seqlens, ATTN_CFG.H, ATTN_CFG.d)
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
+
+    def kstat(name, w_bytes, w_flops, bound):
+        t = ms[name] * 1e-3
+        if bound == "tensor":
+            a = w_flops / t / 1e12
+            return {"bound": "tensor", "achieved": a, "peak": tc, "unit": "TFLOP/s", "frac": a / tc,
+                    "ms": ms[name]}
+        a = w_bytes / t / 1e9
+        return {"bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s", "frac": a / hbm, "ms": ms[name]}
+
+    kernels = {
+        "broadcast": kstat("broadcast", work["broadcast"]["bytes"], 0, "hbm"),
+        "transition": kstat("transition", work["transition"]["bytes"], work["transition"]["flops"], "tensor"),
+        "reduce": kstat("reduce", work["reduce"]["bytes"], 0, "hbm"),
+        "attention": kstat("attention", aw["bytes"], aw["flops"], "tensor"),
+        "partition": {"ms": ms["partition"], "note": "scan + row splits + one totals readback"},
+    }
+    block_names = ("broadcast", "transition", "reduce")
+    dom = max(block_names, key=lambda n: ms[n])
+    roof = dict(kernels[dom])
+    roof.pop("ms")
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} ({'burst copy' if roof['bound'] == 'hbm' else 'cuBLAS bf16 burst'})"
+    tr = traffic_record(dom)
+    roof["traffic"] = tr
+    cells_per_s = world * P / (block_ms_max * 1e-3)
+    attn_tflops = world * aw["flops"] / (attn_ms_max * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": cells_per_s,
+        "unit": "pair cells/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy draws of the pages' workload shapes; random-init weights)",
+        "config": {"workload": f"block: {BLOCK_CFG.name} (T={T}, P={P} packed cells vs "
+                               f"{BLOCK_CFG.B * int(binp.lengths.max()) ** 2} padded); "
+                               f"attention: {ATTN_CFG.name} ({len(ainp.seqlens)} segments)",
+                   "B": BLOCK_CFG.B, "T": T, "P": P, "C_s": C_s, "C_z": C_z, "H_t": H_t,
+                   "attn_T": int(ainp.seqlens.sum()), "attn_segments": int(len(ainp.seqlens)),
+                   "heads": ATTN_CFG.H, "head_dim": ATTN_CFG.d,
+                   "l2": "flushed before every timed step (512 MB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "block_ms": block_ms_max,
+        "attn": {"tflops": attn_tflops, "ms": attn_ms_max, "flops_per_step": aw["flops"],
+                 "roofline": {k: v for k, v in kernels["attention"].items() if k != "ms"}},
+        "kernels": kernels,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    return line
+
+
+def run_e2e(nt, binp, ainp, cu_host, dev, stream, args):
+    """The block through the binding with inputs in pinned host memory: every
+    step copies lengths, singles and weights in and reads z~ and s_out back."""
+    def pin(t):
+        return None if t is None else t.pin_memory()
+    w = binp.blocks[0]
+    host = {"lengths": torch.as_tensor(binp.lengths).pin_memory(), "s": binp.s.pin_memory()}
+    hw = {k: pin(getattr(w, k)) for k in ("W_a", "W_b", "ln_gamma", "ln_beta", "W1", "b1", "W2", "b2",
+                                         "W_g", "b_g")}
+    T = int(binp.lengths.sum())
+    P = int((binp.lengths.astype(np.int64) ** 2).sum())
+    z_host = torch.empty(P, BLOCK_CFG.C_z, dtype=torch.bfloat16).pin_memory()
+    s_host = torch.empty(T, BLOCK_CFG.C_s, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + [t for t in hw.values() if t is not None])
+    d2h = z_host.numel() * 2 + s_host.numel() * 2
+
+    from types import SimpleNamespace
+
+    def one():
+        lengths = host["lengths"].to(dev, non_blocking=True)
+        s = host["s"].to(dev, non_blocking=True)
+        wd = SimpleNamespace(**{k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in hw.items()})
+        part = nt.nt_partition_build(lengths, stream=stream)
+        z, m, s_out = nt.block_forward(part, s, wd, stream=stream)
+        z_host.copy_(z, non_blocking=True)
+        s_host.copy_(s_out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(args.warmup, 1)):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.steps
+    return {"value": P / dt, "unit": "pair cells/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3,
+            "path": "pinned host -> H2D -> nt_partition_build/broadcast/transition/reduce -> D2H of z~ and s_out"}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle: the baseline beside the GPU number, and the reference arm
+# ----------------------------------------------------------------------------
+
+def oracle_block_sample(budget_s=12.0):
+    """The oracle on the same block workload, whole batches repeated until
+    ``budget_s`` of CPU time; returns cells/s."""
+    from oracle import block as oblock
+    binp = wl.make_block_inputs(BLOCK_CFG)
+    w = binp.blocks[0]
+    f = wl.io_bits_to_f64
+    ow = oblock.Weights(f(w.W_a), f(w.W_b), f(w.ln_gamma), f(w.ln_beta), 1e-5, f(w.W1), None, f(w.W2),
+                        None, f(w.W_g), None)
+    s = f(binp.s)
+    P = int((binp.lengths.astype(np.int64) ** 2).sum())
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oblock.block_packed(binp.lengths, s, ow)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n * P / dt, f"{n} full pass(es) of the block on the B=8 batch ({P} cells), {dt:.1f} s"
+
+
+def oracle_attn_sample(budget_s=8.0):
+    from oracle import attention as oattn
+    a = wl.make_attn_inputs(ATTN_CFG)
+    f = wl.io_bits_to_f64
+    q, k, v = f(a.q), f(a.k), f(a.v)
+    cu = np.concatenate([[0], np.cumsum(a.seqlens)])
+    flops, t0, seg = 0, time.perf_counter(), 0
+    while time.perf_counter() - t0 < budget_s and seg < len(a.seqlens):
+        oattn.varlen_attention(q, k, v, cu, segments=[seg])
+        flops += 4 * int(a.seqlens[seg]) ** 2 * ATTN_CFG.H * ATTN_CFG.d
+        seg += 1
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, f"first {seg} of {len(a.seqlens)} segments, {dt:.1f} s"
+
+
+def cpu_cores():
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    vals = []
+    samples = []
+    for _ in range(args.warmup):
+        oracle_block_sample(budget_s=0.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, smp = oracle_block_sample(budget_s=4.0)
+        vals.append(v)
+        samples.append(smp)
+    wall = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    P = int((wl.make_block_inputs(BLOCK_CFG).lengths.astype(np.int64) ** 2).sum())
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "pair cells/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * P / value,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded numpy draws of the pages' workload shapes; random-init weights)",
+        "config": {"workload": f"block: {BLOCK_CFG.name} (CPU oracle, float64)", "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "pair cells/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": samples[-1] if samples else ""},
+        "e2e": {"value": value, "unit": "pair cells/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_gpu(args, rank, world, local_rank)
+    if line is not None:
+        if not args.no_cpu_baseline:
+            v, smp = oracle_block_sample()
+            av, asmp = oracle_attn_sample()
+            line["cpu_baseline"] = {"value": v, "unit": "pair cells/s", "cores": cpu_cores(), "kind": "oracle",
+                                    "sample": smp, "attn_tflops": av, "attn_sample": asmp}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

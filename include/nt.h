@@ -1,0 +1,203 @@
+/*
+ * nt.h -- C ABI of libnt: the packed multi-ragged single->pair->single block
+ * and variable-length (cu_seqlens) attention, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations:
+ *   [DL]  "DanLing NestedTensor: Composable Multi-Ragged Tensors for Deep
+ *         Learning" -- section 3 Eq. 1 (the block), section 3.1 Eq. 2 and
+ *         Figure 2 (packed storage, offsets, row splits), section 3.2 Eq. 3
+ *         (packed row of ragged coordinates) and Eq. 4 (reduction consuming a
+ *         pair axis), section 3.3 (dense work on packed rows; projections are
+ *         V W^T + b), Appendix A (structural invariants).
+ *   [VA]  "Variable-length attention and data packing" -- sections "What it
+ *         is", "How it works" and "Core math" (C) (attention restricted to
+ *         each cu_seqlens segment, block-diagonal mask).
+ *
+ * Conventions shared by every call
+ *   - Ownership: the caller owns every buffer and the stream.  The library
+ *     never allocates or frees device memory.  Pointers named d_* and every
+ *     tensor argument are DEVICE pointers; nt_partition lives in HOST memory.
+ *   - Layout: row-major, features innermost.  Weights are (out, in) so that
+ *     y = x W^T + b ([DL] section 3.3).  Packed singles are (T, C_s); packed
+ *     pair cells are (P, C_z) with cell (a, b) of sample i at row
+ *     pair_off[i] + a * N_i + b ([DL] Eq. 3).
+ *   - dtype: NT_BF16 -- activations and weights bf16, LayerNorm parameters and
+ *     biases fp32, all accumulation fp32.  NT_F32 -- every operand fp32.
+ *   - Alignment: every pointer 16-byte aligned; feature widths multiples of
+ *     8 (bf16) or 4 (fp32).  Otherwise NT_ERR_INVALID / NT_ERR_UNSUPPORTED.
+ *   - Asynchrony: calls enqueue work on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and return.  nt_partition_build is the one call
+ *     that synchronises the stream, once, to return the totals.
+ *   - Errors: argument errors are detected on the host before anything is
+ *     enqueued; the call then writes nothing.  NT_ERR_CUDA reports a launch
+ *     failure (outputs undefined).  Device-side checks (bounded waits, data
+ *     checks) set a device status word that nt_device_status() reads.
+ *     nt_last_error() gives a one-line detail of the last failure on the
+ *     calling thread.
+ */
+#ifndef NT_H_
+#define NT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NT_OK = 0,
+  NT_ERR_INVALID = 1,      /* bad argument: null, negative, misaligned, mismatched */
+  NT_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement */
+  NT_ERR_OVERFLOW = 3,     /* a total does not fit its index type */
+  NT_ERR_CUDA = 4,         /* CUDA runtime/launch error */
+  NT_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
+  NT_ERR_DEVICE_CHECK = 6  /* a device-side data check failed */
+} nt_status;
+
+typedef enum { NT_F32 = 0, NT_BF16 = 1 } nt_dtype;
+
+/*
+ * Partitions of a packed batch of B samples with lengths N_i ([DL] section
+ * 3.1, Figure 2; Appendix A "Structural invariants").
+ *   cu_seqlens[B+1]  sample offsets of the singles, o_i = sum_{k<i} N_k
+ *                    (= eta_i of Eq. 4); int32 (the cu_seqlens convention).
+ *   pair_off[B+1]    sample offsets of the square pairs, sum_{k<i} N_k^2.
+ *   row_start[T+1]   second-level splits: first cell of every pair row,
+ *                    row_start[cu_seqlens[i] + a] = pair_off[i] + a * N_i,
+ *                    row_start[T] = P.
+ *   row_sample[T]    sample index owning each single row / pair row.
+ * T = sum N_i, P = sum N_i^2, max_len = max N_i.  All pointers are device
+ * pointers owned by the caller; the struct itself is host memory.
+ */
+typedef struct nt_partition {
+  int32_t B;
+  int64_t T;
+  int64_t P;
+  int32_t max_len;
+  const int32_t* lengths;
+  const int32_t* cu_seqlens;
+  const int64_t* pair_off;
+  const int64_t* row_start;   /* NULL until nt_partition_rows */
+  const int32_t* row_sample;  /* NULL until nt_partition_rows */
+} nt_partition;
+
+/*
+ * nt_partition_build -- exact sizes to tensor-backed offsets ([DL] Eq. 2,
+ * Figure 2, Appendix A): exclusive scans of N_i and of N_i^2 on the device.
+ *   d_lengths     [B] int32, N_i >= 0 (zero-length samples allowed).
+ *   B             number of samples, >= 1.
+ *   d_cu_seqlens  [B+1] int32 out.   d_pair_off [B+1] int64 out.
+ *   d_totals      [4] int64 device scratch: T, P, max_len, check word.
+ *   out           host struct filled with B, T, P, max_len and the pointers;
+ *                 row_start / row_sample are set to NULL.
+ * Synchronises `stream` once to read the totals.  Returns NT_ERR_INVALID if
+ * some N_i < 0 and NT_ERR_OVERFLOW if T does not fit int32 (out->T, out->P
+ * are still filled).  Integer-exact.
+ */
+nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_seqlens,
+                             int64_t* d_pair_off, int64_t* d_totals, nt_partition* out,
+                             void* stream);
+
+/*
+ * nt_partition_rows -- second-level row splits of the square pair state
+ * ([DL] Figure 2: 1 + sum N_i entries; Eq. 3 with b = 0).
+ *   part          a partition from nt_partition_build (T, P known).
+ *   d_row_start   [T+1] int64 out.   d_row_sample [T] int32 out.
+ * Sets part->row_start and part->row_sample.  Asynchronous.
+ */
+nt_status nt_partition_rows(nt_partition* part, int64_t* d_row_start, int32_t* d_row_sample,
+                            void* stream);
+
+/* Bytes of device workspace nt_pair_broadcast needs: the two projected
+ * single representations u and v in fp32, 2 * T * C_z * 4. */
+size_t nt_pair_broadcast_workspace_bytes(int64_t T, int32_t C_z);
+
+/*
+ * nt_pair_broadcast -- pair construction of [DL] Eq. 1, first line, with the
+ * broadcast of section 3.2 "Creating axes through broadcasting":
+ *     u = s_left W_a^T,  v = s_right W_b^T            (T x C_z, fp32)
+ *     z[pair_off[i] + a N_i + b, :] = u[cu_i + a] + v[cu_i + b]
+ * over the P = sum N_i^2 cells only; no activation at construction ([DL]
+ * Appendix A.1).
+ *   part          partition with row splits (nt_partition_rows done).
+ *   s_left, s_right  [T, C_s] singles (the same pointer for square pairs).
+ *   W_a, W_b      [C_z, C_s].        z [P, C_z] out.
+ *   workspace     >= nt_pair_broadcast_workspace_bytes(T, C_z) device bytes,
+ *                 16-byte aligned; holds u and v while the call runs.
+ * Asynchronous.  Rounds z once to the I/O dtype (round-to-nearest-even).
+ */
+nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void* s_left,
+                            const void* s_right, int32_t C_s, const void* W_a, const void* W_b,
+                            int32_t C_z, void* z, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * nt_pair_transition -- residual feature update of [DL] Eq. 1, second line,
+ * on every packed cell (section 3.2 "Retaining structure through feature
+ * transformations"; section 3.3 "Dense work across valid positions"):
+ *     x  = LN(z) = (z - mean) / sqrt(var + ln_eps) * ln_gamma + ln_beta
+ *     z~ = z + W2 ReLU(W1 x + b1) + b2
+ * LayerNorm over the C_z features of one cell, biased variance.
+ *   z_in, z_out   [P, C_z]; z_out may equal z_in (in place).
+ *   ln_gamma, ln_beta [C_z] fp32.  W1 [H_t, C_z].  b1 [H_t] fp32 or NULL.
+ *   W2 [C_z, H_t].  b2 [C_z] fp32 or NULL.
+ * bf16 with C_z = 128 and H_t a multiple of 128 runs on the tcgen05 tensor
+ * cores (hidden activations rounded to bf16 before the second GEMM); other
+ * shapes and NT_F32 run on fp32 CUDA cores.  Asynchronous.
+ */
+nt_status nt_pair_transition(const nt_partition* part, nt_dtype dtype, const void* z_in,
+                             void* z_out, int32_t C_z, int32_t H_t, const float* ln_gamma,
+                             const float* ln_beta, float ln_eps, const void* W1,
+                             const float* b1, const void* W2, const float* b2, void* stream);
+
+/*
+ * nt_pair_reduce -- the column mean of [DL] Eq. 1, third line, as the
+ * segmented sum of Eq. 4 divided by N_i:
+ *     m[cu_i + a, :] = (1/N_i) sum_b z[pair_off[i] + a N_i + b, :]
+ * then, if W_g is not NULL:  s_out = s_in + m W_g^T + b_g.
+ *   z [P, C_z].  m [T, C_z] out (fp32 accumulation, stored in the I/O dtype).
+ *   W_g [C_s, C_z] or NULL.  b_g [C_s] fp32 or NULL.  s_in [T, C_s] or NULL
+ *   (no residual).  s_out [T, C_s] out (required when W_g is given; may
+ *   equal s_in).
+ * Asynchronous.
+ */
+nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z, int32_t C_z,
+                         void* m, const void* W_g, const float* b_g, const void* s_in,
+                         void* s_out, int32_t C_s, void* stream);
+
+/*
+ * nt_varlen_attn -- softmax attention restricted to each cu_seqlens segment
+ * ([VA] "What it is", "How it works"; [DL] section 3.3 "Attention through
+ * packed blocks"): for token t of segment i and head h,
+ *     O[t, h, :] = sum_{k in [cu_i, cu_{i+1})} softmax_k(scale q_t.k_k) v_k
+ * non-causal; equivalent to the block-diagonal mask seg(t) == seg(k) of
+ * [VA] "Core math" (C) with no padded rectangle formed.
+ *   q, k, v, o    [T, H, d] token-major, contiguous.
+ *   d_cu_seqlens  [B+1] int32, non-decreasing, cu[0] = 0, cu[B] = T.
+ *   max_len       max segment length (>= every cu[i+1] - cu[i]).
+ *   scale         score scale (d^-1/2 for the usual attention).
+ *   lse           [H, T] fp32 natural-log log-sum-exp, or NULL.
+ * bf16 with d = 64 runs on the tcgen05 tensor cores; NT_F32 and other head
+ * widths (32, 64, 128) run on fp32 CUDA cores.  Asynchronous.
+ */
+nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const void* v,
+                         const int32_t* d_cu_seqlens, int32_t B, int64_t T, int32_t max_len,
+                         int32_t H, int32_t d, float scale, void* o, float* lse, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device status word set by
+ * device-side checks (bounded waits that ran out: NT_ERR_TIMEOUT; failed data
+ * checks: NT_ERR_DEVICE_CHECK).  NT_OK if nothing was flagged. */
+nt_status nt_device_status(void* stream);
+
+/* Static string naming a status code. */
+const char* nt_status_str(nt_status s);
+
+/* One-line detail of the last non-OK status returned on this thread. */
+const char* nt_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NT_H_ */

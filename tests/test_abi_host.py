@@ -1,0 +1,99 @@
+"""The C-ABI library loads here (no GPU) and exports every symbol the header
+declares; host-side argument checks reject bad calls before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from variable_length_batching_gb300 import build as nt_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nt.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nt_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    path = nt_build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ("nt_partition_build", "nt_partition_rows", "nt_pair_broadcast", "nt_pair_transition",
+              "nt_pair_reduce", "nt_varlen_attn", "nt_device_status", "nt_status_str", "nt_last_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_binding_covers_every_declaration():
+    from variable_length_batching_gb300 import nt
+    assert set(nt.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings(L):
+    L.nt_status_str.restype = ctypes.c_char_p
+    assert L.nt_status_str(0) == b"NT_OK"
+    assert L.nt_status_str(1) == b"NT_ERR_INVALID"
+    assert L.nt_status_str(5) == b"NT_ERR_TIMEOUT"
+    assert L.nt_status_str(99) == b"NT_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(L):
+    L.nt_pair_broadcast_workspace_bytes.restype = ctypes.c_size_t
+    L.nt_pair_broadcast_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32]
+    assert L.nt_pair_broadcast_workspace_bytes(1031, 128) == 2 * 1031 * 128 * 4
+    assert L.nt_pair_broadcast_workspace_bytes(-1, 128) == 0
+
+
+def test_host_side_rejections(L):
+    """Calls that must fail on argument checks alone (nothing reaches CUDA)."""
+    from variable_length_batching_gb300 import nt
+    lib = nt.lib()
+    part = nt.nt_partition()
+    P = ctypes.byref(part)
+    fake = ctypes.c_void_p(0x1000)       # never dereferenced: the checks fire first
+    odd = ctypes.c_void_p(0x1008)
+    # NULL output struct / negative B
+    assert lib.nt_partition_build(fake, 4, fake, fake, fake, None, None) == 1
+    assert lib.nt_partition_build(fake, -1, fake, fake, fake, P, None) == 1
+    # NULL partition
+    assert lib.nt_pair_transition(None, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None,
+                                  fake, None, None) == 1
+    # partition without row splits
+    part.B, part.T, part.P, part.max_len = 2, 5, 13, 3
+    part.lengths = part.cu_seqlens = part.pair_off = 0x1000
+    assert lib.nt_pair_broadcast(P, 1, fake, fake, 384, fake, fake, 128, fake, fake, 1 << 20, None) == 1
+    part.row_start = part.row_sample = 0x1000
+    # inconsistent totals: P > T * max_len
+    part.P = 100
+    assert lib.nt_pair_reduce(P, 1, fake, 128, fake, None, None, None, None, 0, None) == 1
+    part.P = 13
+    # width not a multiple of 8 in bf16 -> unsupported
+    assert lib.nt_pair_broadcast(P, 1, fake, fake, 384, fake, fake, 12, fake, fake, 1 << 20, None) == 2
+    # misaligned pointer
+    assert lib.nt_pair_broadcast(P, 1, odd, fake, 384, fake, fake, 128, fake, fake, 1 << 20, None) == 1
+    # workspace too small
+    assert lib.nt_pair_broadcast(P, 1, fake, fake, 384, fake, fake, 128, fake, fake, 16, None) == 1
+    # bad dtype
+    assert lib.nt_pair_transition(P, 7, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, fake,
+                                  None, None) == 1
+    # W_g without s_out
+    assert lib.nt_pair_reduce(P, 1, fake, 128, fake, fake, None, None, None, 384, None) == 1
+    # attention: T > 0 without segments; bad head count; T beyond int32
+    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 0, 64, 64, 12, 64, 0.125, fake, None, None) == 1
+    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 64, 64, 0, 64, 0.125, fake, None, None) == 1
+    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 1 << 31, 64, 1, 64, 0.125, fake, None, None) == 3
+    # an empty stream is a no-op success
+    assert lib.nt_varlen_attn(1, None, None, None, None, 0, 0, 0, 12, 64, 0.125, None, None, None) == 0
+    assert lib.nt_last_error()  # a detail string was recorded

@@ -1,0 +1,286 @@
+// The C ABI of libnt (declared in include/nt.h): argument validation on the
+// host, then one batch-level launch per step on the caller's stream -- every
+// call covers the whole packed batch, never one call per sample ("DanLing
+// NestedTensor" section 4.4, "Separating interface cost from execution
+// strategy": segmented calls over the batch).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "nt_common.cuh"
+
+namespace nt {
+
+// Device status word: set by device-side checks, read by nt_device_status.
+__device__ unsigned int g_device_status;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+nt_status fail(nt_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+nt_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(NT_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+// Device address of g_device_status on the current device, looked up once
+// per device with that device current.
+unsigned int* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool width_ok(nt_dtype dt, int64_t w) { return w > 0 && w % (dt == NT_BF16 ? 8 : 4) == 0; }
+bool dtype_ok(nt_dtype dt) { return dt == NT_F32 || dt == NT_BF16; }
+size_t esize(nt_dtype dt) { return dt == NT_BF16 ? 2 : 4; }
+
+nt_status check_partition(const nt_partition* p, bool need_rows) {
+  if (!p) return fail(NT_ERR_INVALID, "partition is NULL");
+  if (p->B < 0 || p->T < 0 || p->P < 0 || p->max_len < 0)
+    return fail(NT_ERR_INVALID, "partition has negative sizes");
+  if (p->T > 0 && (!p->lengths || !p->cu_seqlens || !p->pair_off))
+    return fail(NT_ERR_INVALID, "partition pointers are NULL");
+  if (need_rows && p->T > 0 && (!p->row_start || !p->row_sample))
+    return fail(NT_ERR_INVALID, "partition has no row splits (call nt_partition_rows)");
+  if (p->P < p->T || (p->T > 0 && p->P > p->T * (int64_t)p->max_len))
+    return fail(NT_ERR_INVALID, "partition totals are inconsistent (T=%lld P=%lld max_len=%d)",
+                (long long)p->T, (long long)p->P, p->max_len);
+  return NT_OK;
+}
+
+}  // namespace
+
+int sm_count() {
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace nt
+
+using namespace nt;
+
+extern "C" {
+
+const char* nt_status_str(nt_status s) {
+  switch (s) {
+    case NT_OK: return "NT_OK";
+    case NT_ERR_INVALID: return "NT_ERR_INVALID";
+    case NT_ERR_UNSUPPORTED: return "NT_ERR_UNSUPPORTED";
+    case NT_ERR_OVERFLOW: return "NT_ERR_OVERFLOW";
+    case NT_ERR_CUDA: return "NT_ERR_CUDA";
+    case NT_ERR_TIMEOUT: return "NT_ERR_TIMEOUT";
+    case NT_ERR_DEVICE_CHECK: return "NT_ERR_DEVICE_CHECK";
+  }
+  return "NT_ERR_UNKNOWN";
+}
+
+const char* nt_last_error(void) { return g_last_error; }
+
+nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_seqlens,
+                             int64_t* d_pair_off, int64_t* d_totals, nt_partition* out,
+                             void* stream) {
+  if (!out) return fail(NT_ERR_INVALID, "out is NULL");
+  if (B < 0) return fail(NT_ERR_INVALID, "B = %d < 0", B);
+  if ((B > 0 && !d_lengths) || !d_cu_seqlens || !d_pair_off || !d_totals)
+    return fail(NT_ERR_INVALID, "NULL device pointer");
+  if (!aligned16(d_totals) || !aligned16(d_pair_off) || !aligned16(d_cu_seqlens))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_partition_scan(d_lengths, B, d_cu_seqlens, d_pair_off, d_totals, s);
+  if (e != cudaSuccess) return cuda_fail(e, "partition scan launch");
+  int64_t tot[4] = {0, 0, 0, 0};
+  e = cudaMemcpyAsync(tot, d_totals, sizeof(tot), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
+  out->B = B;
+  out->T = tot[0];
+  out->P = tot[1];
+  out->max_len = (int32_t)tot[2];
+  out->lengths = d_lengths;
+  out->cu_seqlens = d_cu_seqlens;
+  out->pair_off = d_pair_off;
+  out->row_start = nullptr;
+  out->row_sample = nullptr;
+  if (tot[3] & 1) return fail(NT_ERR_INVALID, "a sample length is negative");
+  if (tot[3] & 2) return fail(NT_ERR_OVERFLOW, "T = %lld does not fit int32 cu_seqlens", (long long)tot[0]);
+  return NT_OK;
+}
+
+nt_status nt_partition_rows(nt_partition* part, int64_t* d_row_start, int32_t* d_row_sample,
+                            void* stream) {
+  nt_status st = check_partition(part, false);
+  if (st != NT_OK) return st;
+  if (!d_row_start || (part->T > 0 && !d_row_sample))
+    return fail(NT_ERR_INVALID, "NULL row split pointer");
+  if (!aligned16(d_row_start) || !aligned16(d_row_sample))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  cudaError_t e = launch_partition_rows(part->lengths, part->cu_seqlens, part->pair_off, part->B,
+                                        part->T, part->P, d_row_start, d_row_sample,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "partition rows launch");
+  part->row_start = d_row_start;
+  part->row_sample = d_row_sample;
+  return NT_OK;
+}
+
+size_t nt_pair_broadcast_workspace_bytes(int64_t T, int32_t C_z) {
+  if (T < 0 || C_z < 0) return 0;
+  return (size_t)2 * (size_t)T * (size_t)C_z * sizeof(float);
+}
+
+nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void* s_left,
+                            const void* s_right, int32_t C_s, const void* W_a, const void* W_b,
+                            int32_t C_z, void* z, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  nt_status st = check_partition(part, true);
+  if (st != NT_OK) return st;
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (!width_ok(dtype, C_s) || !width_ok(dtype, C_z))
+    return fail(NT_ERR_UNSUPPORTED, "C_s=%d, C_z=%d must be positive multiples of %d", C_s, C_z,
+                dtype == NT_BF16 ? 8 : 4);
+  if (!s_left || !s_right || !W_a || !W_b || !z || !workspace)
+    return fail(NT_ERR_INVALID, "NULL pointer");
+  if (!aligned16(s_left) || !aligned16(s_right) || !aligned16(W_a) || !aligned16(W_b) ||
+      !aligned16(z) || !aligned16(workspace))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  if (workspace_bytes < nt_pair_broadcast_workspace_bytes(part->T, C_z))
+    return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes,
+                nt_pair_broadcast_workspace_bytes(part->T, C_z));
+  if (part->T == 0) return NT_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* u = static_cast<float*>(workspace);
+  float* v = u + part->T * (int64_t)C_z;
+  LinearProblem probs[2] = {{s_left, W_a, nullptr, nullptr, u}, {s_right, W_b, nullptr, nullptr, v}};
+  cudaError_t e = launch_linear(dtype, 1, probs, 2, part->T, C_z, C_s, s);
+  if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+  e = launch_broadcast(dtype, u, v, part, C_z, z, s);
+  if (e != cudaSuccess) return cuda_fail(e, "broadcast launch");
+  return NT_OK;
+}
+
+nt_status nt_pair_transition(const nt_partition* part, nt_dtype dtype, const void* z_in,
+                             void* z_out, int32_t C_z, int32_t H_t, const float* ln_gamma,
+                             const float* ln_beta, float ln_eps, const void* W1,
+                             const float* b1, const void* W2, const float* b2, void* stream) {
+  nt_status st = check_partition(part, false);
+  if (st != NT_OK) return st;
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (!width_ok(dtype, C_z) || !width_ok(dtype, H_t))
+    return fail(NT_ERR_UNSUPPORTED, "C_z=%d, H_t=%d must be positive multiples of %d", C_z, H_t,
+                dtype == NT_BF16 ? 8 : 4);
+  if (!z_in || !z_out || !ln_gamma || !ln_beta || !W1 || !W2)
+    return fail(NT_ERR_INVALID, "NULL pointer");
+  if (!aligned16(z_in) || !aligned16(z_out) || !aligned16(W1) || !aligned16(W2) ||
+      !aligned16(ln_gamma) || !aligned16(ln_beta) || !aligned16(b1) || !aligned16(b2))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  if (!(ln_eps >= 0.0f)) return fail(NT_ERR_INVALID, "ln_eps must be >= 0");
+  if (part->P == 0) return NT_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (transition_tc_supported(dtype, C_z, H_t)) {
+    e = launch_transition_tc(z_in, z_out, part->P, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W2,
+                             b2, status_word(), s);
+    if (e != cudaSuccess) return cuda_fail(e, "transition (tensor core) launch");
+    return NT_OK;
+  }
+  if (sizeof(float) * 8 * (size_t)(C_z + H_t) > 200 * 1024)
+    return fail(NT_ERR_UNSUPPORTED, "C_z + H_t = %d too wide for the CUDA-core transition", C_z + H_t);
+  e = launch_transition_simt(dtype, z_in, z_out, part->P, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1,
+                             b1, W2, b2, s);
+  if (e != cudaSuccess) return cuda_fail(e, "transition launch");
+  return NT_OK;
+}
+
+nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z, int32_t C_z,
+                         void* m, const void* W_g, const float* b_g, const void* s_in,
+                         void* s_out, int32_t C_s, void* stream) {
+  nt_status st = check_partition(part, true);
+  if (st != NT_OK) return st;
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (!width_ok(dtype, C_z)) return fail(NT_ERR_UNSUPPORTED, "C_z=%d", C_z);
+  if (dtype == NT_BF16 && C_z > 1024) return fail(NT_ERR_UNSUPPORTED, "bf16 C_z=%d > 1024", C_z);
+  if (!z || !m) return fail(NT_ERR_INVALID, "NULL pointer");
+  if (W_g && (!s_out || !width_ok(dtype, C_s)))
+    return fail(NT_ERR_INVALID, "W_g given: s_out must be set and C_s=%d valid", C_s);
+  if (!aligned16(z) || !aligned16(m) || !aligned16(W_g) || !aligned16(b_g) || !aligned16(s_in) ||
+      !aligned16(s_out))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  if (part->T == 0) return NT_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_reduce(dtype, z, part, C_z, m, s);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
+  if (W_g) {
+    LinearProblem prob = {m, W_g, b_g, s_in, s_out};
+    e = launch_linear(dtype, dtype == NT_F32, &prob, 1, part->T, C_s, C_z, s);
+    if (e != cudaSuccess) return cuda_fail(e, "g projection launch");
+  }
+  return NT_OK;
+}
+
+nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const void* v,
+                         const int32_t* d_cu_seqlens, int32_t B, int64_t T, int32_t max_len,
+                         int32_t H, int32_t d, float scale, void* o, float* lse, void* stream) {
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (B < 0 || T < 0 || H <= 0 || d <= 0 || max_len < 0)
+    return fail(NT_ERR_INVALID, "bad sizes B=%d T=%lld H=%d d=%d max_len=%d", B, (long long)T, H, d,
+                max_len);
+  if (T > 0x7fffffffLL) return fail(NT_ERR_OVERFLOW, "T = %lld does not fit int32", (long long)T);
+  if (T > 0 && B == 0) return fail(NT_ERR_INVALID, "T > 0 with no segments");
+  if (T > 0 && (!q || !k || !v || !o || !d_cu_seqlens)) return fail(NT_ERR_INVALID, "NULL pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  if (T == 0) return NT_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (attn_tc_supported(dtype, d)) {
+    e = launch_attn_tc(q, k, v, d_cu_seqlens, B, T, max_len, H, d, scale, o, lse, status_word(), s);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen attention (tensor core) launch");
+    return NT_OK;
+  }
+  if (!attn_simt_supported(d)) return fail(NT_ERR_UNSUPPORTED, "head width d=%d", d);
+  e = launch_attn_simt(dtype, q, k, v, d_cu_seqlens, B, T, H, d, scale, o, lse, status_word(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "varlen attention launch");
+  return NT_OK;
+}
+
+nt_status nt_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned int word = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&word, g_device_status, sizeof(word));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "device status readback");
+  if (word & kDevTimeout) return fail(NT_ERR_TIMEOUT, "a bounded device wait ran out (word 0x%x)", word);
+  if (word & kDevCheck) return fail(NT_ERR_DEVICE_CHECK, "a device-side data check failed (word 0x%x)", word);
+  return NT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// Shared device helpers of libnt: dtype traits, vector loads/stores, the
+// device status word and the internal launcher declarations.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/nt.h"
+
+namespace nt {
+
+// Bits of the device status word (see nt_device_status).
+enum : unsigned int {
+  kDevTimeout = 1u,      // a bounded wait ran out
+  kDevCheck = 2u,        // a data check failed
+};
+
+typedef __nv_bfloat16 bf16;
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// Load 8 consecutive elements (16 bytes of bf16, 32 bytes of fp32) as fp32.
+__device__ __forceinline__ void load8(const bf16* p, float* out) {
+  uint4 raw = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float* out) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  float4 b = *reinterpret_cast<const float4*>(p + 4);
+  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+}
+__device__ __forceinline__ void store8(bf16* p, const float* in) {
+  uint4 raw;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = raw;
+}
+__device__ __forceinline__ void store8(float* p, const float* in) {
+  *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(in[4], in[5], in[6], in[7]);
+}
+// Streaming store (evict-first): output that is not read again soon.
+__device__ __forceinline__ void store8_stream(bf16* p, const float* in) {
+  uint4 raw;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+  __stcs(reinterpret_cast<uint4*>(p), raw);
+}
+__device__ __forceinline__ void store8_stream(float* p, const float* in) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(in[0], in[1], in[2], in[3]));
+  __stcs(reinterpret_cast<float4*>(p + 4), make_float4(in[4], in[5], in[6], in[7]));
+}
+
+__device__ __forceinline__ void flag_device(unsigned int* status, unsigned int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// ----------------------------------------------------------------------------
+// Internal launchers (one per kernel family), called by the ABI layer after
+// argument validation.  Each returns cudaGetLastError() of its launches.
+// ----------------------------------------------------------------------------
+cudaError_t launch_partition_scan(const int32_t* lengths, int32_t B, int32_t* cu, int64_t* pair_off,
+                                  int64_t* totals, cudaStream_t s);
+cudaError_t launch_partition_rows(const int32_t* lengths, const int32_t* cu, const int64_t* pair_off,
+                                  int32_t B, int64_t T, int64_t P, int64_t* row_start,
+                                  int32_t* row_sample, cudaStream_t s);
+
+// Y[M, N] = X[M, K] W[N, K]^T (+ bias[N]) (+ R[M, N]).  Up to two independent
+// problems in one launch (gridDim.z); all row-major, contiguous.
+struct LinearProblem {
+  const void* X; const void* W; const float* bias; const void* R; void* Y;
+};
+cudaError_t launch_linear(int in_dtype /*nt_dtype of X, W, R*/, int out_f32 /*Y fp32?*/,
+                          const LinearProblem* probs, int nprob, int64_t M, int N, int K,
+                          cudaStream_t s);
+
+cudaError_t launch_broadcast(nt_dtype dt, const float* u, const float* v, const nt_partition* p,
+                             int C_z, void* z, cudaStream_t s);
+
+cudaError_t launch_transition_simt(nt_dtype dt, const void* z_in, void* z_out, int64_t P, int C_z,
+                                   int H_t, const float* gamma, const float* beta, float eps,
+                                   const void* W1, const float* b1, const void* W2,
+                                   const float* b2, cudaStream_t s);
+bool transition_tc_supported(nt_dtype dt, int C_z, int H_t);
+cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t,
+                                 const float* gamma, const float* beta, float eps, const void* W1,
+                                 const float* b1, const void* W2, const float* b2,
+                                 unsigned int* status, cudaStream_t s);
+
+cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m,
+                          cudaStream_t s);
+
+bool attn_simt_supported(int d);
+cudaError_t launch_attn_simt(nt_dtype dt, const void* q, const void* k, const void* v,
+                             const int32_t* cu, int32_t B, int64_t T, int H, int d, float scale,
+                             void* o, float* lse, unsigned int* status, cudaStream_t s);
+bool attn_tc_supported(nt_dtype dt, int d);
+cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, const int32_t* cu,
+                           int32_t B, int64_t T, int32_t max_len, int H, int d, float scale,
+                           void* o, float* lse, unsigned int* status, cudaStream_t s);
+
+}  // namespace nt

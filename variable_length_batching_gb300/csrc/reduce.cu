@@ -1,0 +1,104 @@
+// Segmented column mean over the pair state ("DanLing NestedTensor" Eq. 1
+// third line and Eq. 4, "Consuming one logical axis"):
+//     m[cu_i + a] = (1/N_i) sum_b z[pair_off_i + a N_i + b]
+// Every pair row's N_i cells are contiguous, so one CTA owns one pair row:
+// its threads split the row's cells, each keeping a 16-byte feature vector
+// of fp32 sums, then the cell groups are combined through shared memory.
+// HBM-bound: reads P * C_z elements once, writes T * C_z.
+#include "nt_common.cuh"
+
+namespace nt {
+namespace {
+
+constexpr int kThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ lengths,
+              const int32_t* __restrict__ row_sample, const int64_t* __restrict__ row_start,
+              int64_t rows, int C_z, T* __restrict__ m) {
+  extern __shared__ float part[];              // [groups][C_z]
+  const int lanes = C_z / 8;                   // vectors per cell (<= kThreads)
+  const int groups = kThreads / lanes;         // cells summed concurrently
+  const int lane = threadIdx.x % lanes, grp = threadIdx.x / lanes;
+  const bool active = grp < groups;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int64_t n = lengths[row_sample[r]];
+    const T* zr = z + row_start[r] * C_z + lane * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (active) {
+      int64_t b = grp;
+      // two independent loads in flight per iteration
+      for (; b + groups < n; b += 2 * groups) {
+        float x0[8], x1[8];
+        load8(zr + b * C_z, x0);
+        load8(zr + (b + groups) * C_z, x1);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] += x0[t] + x1[t];
+      }
+      for (; b < n; b += groups) {
+        float x0[8];
+        load8(zr + b * C_z, x0);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] += x0[t];
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) part[grp * C_z + lane * 8 + t] = acc[t];
+    }
+    __syncthreads();
+    if (grp == 0) {
+      float tot[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) tot[t] = part[lane * 8 + t];
+      for (int g = 1; g < groups; ++g)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) tot[t] += part[g * C_z + lane * 8 + t];
+      const float inv = 1.0f / (float)n;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) tot[t] *= inv;
+      store8(m + r * C_z + lane * 8, tot);
+    }
+    __syncthreads();
+  }
+}
+
+// fp32 widths that are multiples of 4 but not of 8: one thread per feature.
+__global__ void reduce_kernel_f32_scalar(const float* __restrict__ z, const int32_t* __restrict__ lengths,
+                                         const int32_t* __restrict__ row_sample,
+                                         const int64_t* __restrict__ row_start, int64_t rows, int C_z,
+                                         float* __restrict__ m) {
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int64_t n = lengths[row_sample[r]];
+    const float* zr = z + row_start[r] * C_z;
+    for (int c = threadIdx.x; c < C_z; c += blockDim.x) {
+      float acc = 0.f;
+      for (int64_t b = 0; b < n; ++b) acc += zr[b * C_z + c];
+      m[r * C_z + c] = acc / (float)n;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m,
+                          cudaStream_t s) {
+  if (p->T == 0) return cudaSuccess;
+  const int sms = sm_count();
+  const int grid = (int)min64(p->T, (int64_t)sms * 32);
+  if (C_z % 8 == 0 && C_z / 8 <= kThreads) {
+    const int groups = kThreads / (C_z / 8);
+    const size_t smem = sizeof(float) * groups * C_z;
+    if (dt == NT_BF16)
+      reduce_kernel<bf16><<<grid, kThreads, smem, s>>>((const bf16*)z, p->lengths, p->row_sample,
+                                                       p->row_start, p->T, C_z, (bf16*)m);
+    else
+      reduce_kernel<float><<<grid, kThreads, smem, s>>>((const float*)z, p->lengths, p->row_sample,
+                                                        p->row_start, p->T, C_z, (float*)m);
+  } else {
+    reduce_kernel_f32_scalar<<<grid, 128, 0, s>>>((const float*)z, p->lengths, p->row_sample,
+                                                 p->row_start, p->T, C_z, (float*)m);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace nt

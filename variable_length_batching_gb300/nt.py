@@ -1,0 +1,257 @@
+"""Thin Python binding of libnt (``include/nt.h``).
+
+Argument marshalling only: torch tensors supply device memory and the
+current CUDA stream; every step of the block and of varlen attention runs in
+the library's kernels.  Functions keep the C names.  If ``libnt.so`` is
+missing or a call fails, an exception is raised -- there is no other path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnt.so")
+
+NT_F32, NT_BF16 = 0, 1
+STATUS = {0: "NT_OK", 1: "NT_ERR_INVALID", 2: "NT_ERR_UNSUPPORTED", 3: "NT_ERR_OVERFLOW",
+          4: "NT_ERR_CUDA", 5: "NT_ERR_TIMEOUT", 6: "NT_ERR_DEVICE_CHECK"}
+
+
+class NTError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {detail}")
+        self.status = status
+
+
+class nt_partition(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int64), ("P", ctypes.c_int64),
+                ("max_len", ctypes.c_int32), ("lengths", ctypes.c_void_p),
+                ("cu_seqlens", ctypes.c_void_p), ("pair_off", ctypes.c_void_p),
+                ("row_start", ctypes.c_void_p), ("row_sample", ctypes.c_void_p)]
+
+
+_lib = None
+
+_P, _I32, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_PP = ctypes.POINTER(nt_partition)
+SIGNATURES = {
+    "nt_partition_build": (_I32, [_P, _I32, _P, _P, _P, _PP, _P]),
+    "nt_partition_rows": (_I32, [_PP, _P, _P, _P]),
+    "nt_pair_broadcast_workspace_bytes": (_SZ, [_I64, _I32]),
+    "nt_pair_broadcast": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "nt_pair_transition": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P]),
+    "nt_pair_reduce": (_I32, [_PP, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P]),
+    "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P]),
+    "nt_device_status": (_I32, [_P]),
+    "nt_status_str": (ctypes.c_char_p, [_I32]),
+    "nt_last_error": (ctypes.c_char_p, []),
+}
+
+
+def lib():
+    """Load libnt.so once; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -m variable_length_batching_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise NTError(status, where, lib().nt_last_error().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return NT_BF16
+    if t.dtype == torch.float32:
+        return NT_F32
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def _f32(t: Optional[torch.Tensor]):
+    if t is not None and t.dtype != torch.float32:
+        raise ValueError("LayerNorm parameters and biases are fp32")
+    return t
+
+
+@dataclass
+class Partition:
+    """Device partitions of a packed batch plus the host totals."""
+    lengths: torch.Tensor
+    cu_seqlens: torch.Tensor
+    pair_off: torch.Tensor
+    totals: torch.Tensor
+    row_start: torch.Tensor
+    row_sample: torch.Tensor
+    c: nt_partition
+
+    @property
+    def B(self): return self.c.B
+
+    @property
+    def T(self): return self.c.T
+
+    @property
+    def P(self): return self.c.P
+
+    @property
+    def max_len(self): return self.c.max_len
+
+
+def nt_partition_build(lengths: torch.Tensor, stream=None) -> Partition:
+    """Sizes N_i (int32, on the device) -> cu_seqlens, pair offsets and the
+    second-level row splits (``nt_partition_build`` + ``nt_partition_rows``)."""
+    if lengths.dtype != torch.int32:
+        raise ValueError("lengths must be int32")
+    dev = lengths.device
+    B = lengths.numel()
+    cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    pair_off = torch.empty(B + 1, dtype=torch.int64, device=dev)
+    totals = torch.empty(4, dtype=torch.int64, device=dev)
+    c = nt_partition()
+    st = lib().nt_partition_build(_ptr(lengths) if B else None, B, _ptr(cu), _ptr(pair_off),
+                                  _ptr(totals), ctypes.byref(c), _stream(stream))
+    _check(st, "nt_partition_build")
+    row_start = torch.empty(c.T + 1, dtype=torch.int64, device=dev)
+    row_sample = torch.empty(max(c.T, 1), dtype=torch.int32, device=dev)
+    _check(lib().nt_partition_rows(ctypes.byref(c), _ptr(row_start), _ptr(row_sample), _stream(stream)),
+           "nt_partition_rows")
+    return Partition(lengths, cu, pair_off, totals, row_start, row_sample, c)
+
+
+def nt_pair_broadcast_workspace_bytes(T: int, C_z: int) -> int:
+    return int(lib().nt_pair_broadcast_workspace_bytes(T, C_z))
+
+
+def nt_pair_broadcast(part: Partition, s_left: torch.Tensor, s_right: torch.Tensor,
+                      W_a: torch.Tensor, W_b: torch.Tensor, z: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    T, C_s = s_left.shape
+    C_z = W_a.shape[0]
+    if T != part.T or tuple(s_right.shape) != (T, C_s):
+        raise ValueError(f"singles {tuple(s_left.shape)} do not match the partition (T={part.T})")
+    if tuple(W_a.shape) != (C_z, C_s) or tuple(W_b.shape) != (C_z, C_s):
+        raise ValueError("W_a, W_b must be (C_z, C_s)")
+    if z is None:
+        z = torch.empty(part.P, C_z, dtype=s_left.dtype, device=s_left.device)
+    elif tuple(z.shape) != (part.P, C_z):
+        raise ValueError(f"z {tuple(z.shape)} must be (P={part.P}, C_z={C_z})")
+    need = nt_pair_broadcast_workspace_bytes(T, C_z)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=s_left.device)
+    st = lib().nt_pair_broadcast(ctypes.byref(part.c), _dtype(s_left), _ptr(s_left), _ptr(s_right), C_s,
+                                 _ptr(W_a), _ptr(W_b), C_z, _ptr(z), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nt_pair_broadcast")
+    return z
+
+
+def nt_pair_transition(part: Partition, z: torch.Tensor, ln_gamma: torch.Tensor, ln_beta: torch.Tensor,
+                       W1: torch.Tensor, b1: Optional[torch.Tensor], W2: torch.Tensor,
+                       b2: Optional[torch.Tensor], ln_eps: float = 1e-5,
+                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    P, C_z = z.shape
+    H_t = W1.shape[0]
+    if P != part.P:
+        raise ValueError(f"z has {P} cells, the partition {part.P}")
+    if tuple(W1.shape) != (H_t, C_z) or tuple(W2.shape) != (C_z, H_t):
+        raise ValueError("W1 must be (H_t, C_z) and W2 (C_z, H_t)")
+    if out is None:
+        out = torch.empty_like(z)
+    st = lib().nt_pair_transition(ctypes.byref(part.c), _dtype(z), _ptr(z), _ptr(out), C_z, H_t,
+                                  _ptr(_f32(ln_gamma)), _ptr(_f32(ln_beta)), ln_eps, _ptr(W1),
+                                  _ptr(_f32(b1)), _ptr(W2), _ptr(_f32(b2)), _stream(stream))
+    _check(st, "nt_pair_transition")
+    return out
+
+
+def nt_pair_reduce(part: Partition, z: torch.Tensor, W_g: Optional[torch.Tensor] = None,
+                   b_g: Optional[torch.Tensor] = None, s_in: Optional[torch.Tensor] = None,
+                   m: Optional[torch.Tensor] = None, s_out: Optional[torch.Tensor] = None,
+                   stream=None):
+    P, C_z = z.shape
+    if P != part.P:
+        raise ValueError(f"z has {P} cells, the partition {part.P}")
+    if m is None:
+        m = torch.empty(part.T, C_z, dtype=z.dtype, device=z.device)
+    C_s = 0
+    if W_g is not None:
+        C_s = W_g.shape[0]
+        if tuple(W_g.shape) != (C_s, C_z):
+            raise ValueError("W_g must be (C_s, C_z)")
+        if s_out is None:
+            s_out = torch.empty(part.T, C_s, dtype=z.dtype, device=z.device)
+    st = lib().nt_pair_reduce(ctypes.byref(part.c), _dtype(z), _ptr(z), C_z, _ptr(m), _ptr(W_g),
+                              _ptr(_f32(b_g)), _ptr(s_in), _ptr(s_out), C_s, _stream(stream))
+    _check(st, "nt_pair_reduce")
+    return m, s_out
+
+
+def nt_varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                   max_len: int, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+    T, H, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share the shape (T, H, d)")
+    if cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if want_lse and lse is None:
+        lse = torch.empty(H, T, dtype=torch.float32, device=q.device)
+    st = lib().nt_varlen_attn(_dtype(q), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, T, int(max_len),
+                              H, d, float(scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "nt_varlen_attn")
+    return out, lse
+
+
+def nt_device_status(stream=None) -> int:
+    """Synchronise and return (then clear) the device status word as a
+    status code; raises on a timeout or failed device check."""
+    st = lib().nt_device_status(_stream(stream))
+    _check(st, "nt_device_status")
+    return st
+
+
+def block_forward(part: Partition, s: torch.Tensor, w, ln_eps: float = 1e-5,
+                  z: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  s_out: Optional[torch.Tensor] = None, stream=None):
+    """One single->pair->single block (Eq. 1) as the three pair calls; ``w``
+    holds W_a, W_b, ln_gamma, ln_beta, W1, b1, W2, b2, W_g, b_g on the device.
+    The transition runs in place on z.  Returns (z~, m, s_out)."""
+    z = nt_pair_broadcast(part, s, s, w.W_a, w.W_b, z=z, workspace=workspace, stream=stream)
+    nt_pair_transition(part, z, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2, ln_eps=ln_eps,
+                       out=z, stream=stream)
+    m, s_out = nt_pair_reduce(part, z, w.W_g, w.b_g, s_in=s, s_out=s_out, stream=stream)
+    return z, m, s_out
