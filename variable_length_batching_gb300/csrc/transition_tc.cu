@@ -1,10 +1,433 @@
-// Tensor-core (tcgen05) residual transition -- placeholder until the kernel lands.
-#include "nt_common.cuh"
+// Residual transition on the tcgen05 tensor cores, bf16 in / fp32 accumulate:
+//     z~ = z + W2 ReLU(W1 LN(z) + b1) + b2        (one packed cell per row)
+// "DanLing NestedTensor" Eq. 1 second line; section 3.3 "Dense work across
+// valid positions": the feature transform is a dense contraction over the
+// sum N_i^2 packed rows, so it runs as a GEMM pair with the LayerNorm fused
+// in front and the residual fused behind.
+//
+// Shape: C_z = 128, H_t = 128 * NC.  Persistent CTAs, one per SM; a tile is
+// 256 packed rows handled as two 128-row sub-tiles that share every weight
+// chunk (half the weight traffic of 128-row tiles).
+//
+// Warp roles (14 warps):
+//   warp 0        TMA producer: z tile (4 boxes of 64 x 128) into A; weight
+//                 chunks of 128 x 128 through a 3-stage ring.
+//   warp 1        TMEM owner and MMA issuer (one thread).
+//   warps 2-5     LayerNorm, in place on the TMA-loaded tile in A.
+//   warps 6-9     epilogue of sub-tile 0; warps 10-13 of sub-tile 1: TMEM
+//                 -> +b1, ReLU -> bf16 hidden chunk in H; at the end TMEM ->
+//                 +b2 + residual -> bf16 into H -> TMA store.
+// TMEM (512 columns): acc1[s] = GEMM1 chunk of sub-tile s at 128*s,
+// acc2[s] = output accumulator of sub-tile s at 256 + 128*s.
+// Every operand tile is K-major with the 128-byte swizzle that TMA writes.
+#include <cudaTypedefs.h>
+
+#include "tc_ptx.cuh"
+
 namespace nt {
-bool transition_tc_supported(nt_dtype, int, int) { return false; }
-cudaError_t launch_transition_tc(const void*, void*, int64_t, int, int, const float*, const float*,
-                                 float, const void*, const float*, const void*, const float*,
-                                 unsigned int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+using namespace tc;
+
+constexpr int kSubRows = 128;
+constexpr int kTileRows = 2 * kSubRows;
+constexpr int kCz = 128;
+constexpr int kChunk = 128;
+constexpr int kStages = 3;
+constexpr int kThreads = 14 * 32;
+constexpr uint32_t kBlockBytes = kSubRows * 128;          // one 64-column block: 16 KB
+constexpr uint32_t kSubBytes = 2 * kBlockBytes;           // 128 x 128 bf16: 32 KB
+constexpr uint32_t kABytes = 2 * kSubBytes;               // z / LN(z) tile: 64 KB
+constexpr uint32_t kHBytes = 2 * kSubBytes;               // hidden chunk per sub-tile: 64 KB
+constexpr uint32_t kWBytes = kChunk * kCz * 2;            // one weight chunk: 32 KB
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffH = kOffA + kABytes;
+constexpr uint32_t kOffW = kOffH + kHBytes;
+constexpr uint32_t kOffLN = kOffW + kStages * kWBytes;    // gamma, beta: 1 KB
+constexpr uint32_t kOffBar = kOffLN + 2 * kCz * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;     // + barriers + alignment slack
+
+struct Bars {
+  uint64_t z_full, a_full, a_empty;
+  uint64_t w_full[kStages], w_empty[kStages];
+  uint64_t acc1_full[2], acc1_empty[2];
+  uint64_t h_full[2], h_empty[2];
+  uint64_t acc2_full[2], acc2_empty[2];
+  uint64_t out_ready[2], store_done[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+__device__ __forceinline__ void weight_order(int q, int NC, bool* is_w1, int* c) {
+  // consumption order: W1(0), then for each chunk c: W1(c+1) (if any), W2(c)
+  if (q == 0) { *is_w1 = true; *c = 0; return; }
+  const int qq = q - 1;
+  if (NC == 1) { *is_w1 = false; *c = 0; return; }
+  const int pairs = NC - 1;                 // chunks c = 0..NC-2 bring a W1(c+1)
+  if (qq < 2 * pairs) {
+    *c = qq / 2;
+    if ((qq & 1) == 0) { *is_w1 = true; *c += 1; } else { *is_w1 = false; }
+    return;
+  }
+  *is_w1 = false;
+  *c = NC - 1;
 }
+
+__global__ void __launch_bounds__(kThreads, 1)
+transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_constant__ CUtensorMap tm_zout,
+                     const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
+                     const bf16* z_in, int64_t P, int H_t, const float* __restrict__ gamma,
+                     const float* __restrict__ beta, float eps, const float* __restrict__ b1,
+                     const float* __restrict__ b2, unsigned int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sA = smem + kOffA;
+  uint8_t* sH = smem + kOffH;
+  uint8_t* sW = smem + kOffW;
+  float* sGamma = reinterpret_cast<float*>(smem + kOffLN);
+  float* sBeta = sGamma + kCz;
+  Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort_flag = &bar.abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NC = H_t / kChunk;
+  const int64_t num_tiles = (P + kTileRows - 1) / kTileRows;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.z_full, 1);
+    mbar_init(&bar.a_full, 128);
+    mbar_init(&bar.a_empty, 1);
+    for (int i = 0; i < kStages; ++i) { mbar_init(&bar.w_full[i], 1); mbar_init(&bar.w_empty[i], 1); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar.acc1_full[s], 1); mbar_init(&bar.acc1_empty[s], 128);
+      mbar_init(&bar.h_full[s], 128); mbar_init(&bar.h_empty[s], 1);
+      mbar_init(&bar.acc2_full[s], 1); mbar_init(&bar.acc2_empty[s], 128);
+      mbar_init(&bar.out_ready[s], 128); mbar_init(&bar.store_done[s], 1);
+    }
+    mbar_init(&bar.mma_done, 1);
+    bar.abort = 0;
+    fence_mbar_init();
+    fence_async_shared();
+  }
+  for (int i = threadIdx.x; i < kCz; i += kThreads) { sGamma[i] = gamma[i]; sBeta[i] = beta[i]; }
+  if (warp == 1) tmem_alloc(&bar.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_zin); prefetch_tmap(&tm_w1); prefetch_tmap(&tm_w2); prefetch_tmap(&tm_zout);
+      int load_idx = 0;
+      int last_tile_j = -1;
+      bool ok = true;
+      int j = 0;
+      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
+        if (!(ok = mbar_wait(&bar.a_empty, (j & 1) ^ 1, abort_flag, status))) break;
+        mbar_arrive_expect_tx(&bar.z_full, kABytes);
+        const int row0 = (int)(tile * kTileRows);
+        for (int s = 0; s < 2; ++s)
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_2d(sA + s * kSubBytes + kb * kBlockBytes, &tm_zin, &bar.z_full, kb * 64, row0 + s * kSubRows);
+        last_tile_j = j;
+        for (int q = 0; q < 2 * NC; ++q) {
+          bool w1; int c;
+          weight_order(q, NC, &w1, &c);
+          const int stage = load_idx % kStages, round = load_idx / kStages;
+          if (!(ok = mbar_wait(&bar.w_empty[stage], (round & 1) ^ 1, abort_flag, status))) break;
+          mbar_arrive_expect_tx(&bar.w_full[stage], kWBytes);
+          uint8_t* dst = sW + stage * kWBytes;
+          if (w1) {
+            tma_load_2d(dst, &tm_w1, &bar.w_full[stage], 0, c * kChunk);
+            tma_load_2d(dst + kBlockBytes, &tm_w1, &bar.w_full[stage], 64, c * kChunk);
+          } else {
+            tma_load_2d(dst, &tm_w2, &bar.w_full[stage], c * kChunk, 0);
+            tma_load_2d(dst + kBlockBytes, &tm_w2, &bar.w_full[stage], c * kChunk + 64, 0);
+          }
+          ++load_idx;
+        }
+      }
+      // drain: every copy this thread issued has landed before the CTA exits
+      if (last_tile_j >= 0) mbar_wait(&bar.z_full, last_tile_j & 1, nullptr, status);
+      for (int l = load_idx - kStages; l < load_idx; ++l)
+        if (l >= 0) mbar_wait(&bar.w_full[l % kStages], (l / kStages) & 1, nullptr, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, 128);
+      const uint32_t a_base = smem_u32(sA), h_base = smem_u32(sH), w_base = smem_u32(sW);
+      int load_idx = 0;
+      bool ok = true;
+      int j = 0;
+      auto take_w = [&](uint32_t* wsm) -> bool {
+        const int stage = load_idx % kStages, round = load_idx / kStages;
+        if (!mbar_wait(&bar.w_full[stage], round & 1, abort_flag, status)) return false;
+        tc_fence_after();
+        *wsm = w_base + stage * kWBytes;
+        return true;
+      };
+      auto release_w = [&]() {
+        mma_commit(&bar.w_empty[load_idx % kStages]);
+        ++load_idx;
+      };
+      auto gemm1 = [&](int s, int it, uint32_t wsm) -> bool {
+        if (!mbar_wait(&bar.acc1_empty[s], (it & 1) ^ 1, abort_flag, status)) return false;
+        tc_fence_after();
+        for (int k = 0; k < kCz / 16; ++k) {
+          const uint32_t koff = (k >> 2) * kBlockBytes + (k & 3) * 32;
+          mma_bf16(tmem + 128 * s, sdesc_k128(a_base + s * kSubBytes + koff), sdesc_k128(wsm + koff), idesc,
+                   k > 0);
+        }
+        mma_commit(&bar.acc1_full[s]);
+        return true;
+      };
+      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
+        if (!(ok = mbar_wait(&bar.a_full, j & 1, abort_flag, status))) break;
+        tc_fence_after();
+        uint32_t wsm;
+        if (!(ok = take_w(&wsm))) break;
+        for (int s = 0; s < 2 && ok; ++s) ok = gemm1(s, j * NC, wsm);
+        if (!ok) break;
+        release_w();
+        if (NC == 1) mma_commit(&bar.a_empty);
+        for (int c = 0; c < NC && ok; ++c) {
+          if (c + 1 < NC) {
+            if (!(ok = take_w(&wsm))) break;
+            for (int s = 0; s < 2 && ok; ++s) ok = gemm1(s, j * NC + c + 1, wsm);
+            if (!ok) break;
+            release_w();
+            if (c + 1 == NC - 1) mma_commit(&bar.a_empty);
+          }
+          if (!(ok = take_w(&wsm))) break;
+          const int it = j * NC + c;
+          for (int s = 0; s < 2; ++s) {
+            if (c == 0 && !(ok = mbar_wait(&bar.acc2_empty[s], (j & 1) ^ 1, abort_flag, status))) break;
+            if (!(ok = mbar_wait(&bar.h_full[s], it & 1, abort_flag, status))) break;
+            tc_fence_after();
+            for (int k = 0; k < kChunk / 16; ++k) {
+              const uint32_t koff = (k >> 2) * kBlockBytes + (k & 3) * 32;
+              mma_bf16(tmem + 256 + 128 * s, sdesc_k128(h_base + s * kSubBytes + koff), sdesc_k128(wsm + koff),
+                       idesc, (c > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(&bar.h_empty[s]);
+            if (c == NC - 1) mma_commit(&bar.acc2_full[s]);
+          }
+          if (!ok) break;
+          release_w();
+        }
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      mma_commit(&bar.mma_done);
+      mbar_wait(&bar.mma_done, 0, nullptr, status);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ LayerNorm
+    const int t = threadIdx.x - 64;   // 0..127: row t of each sub-tile
+    int j = 0;
+    for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++j) {
+      if (!mbar_wait(&bar.z_full, j & 1, abort_flag, status)) break;
+#pragma unroll 1
+      for (int s = 0; s < 2; ++s) {
+        uint8_t* base = sA + s * kSubBytes;
+        // statistics in one pass over the row, shifted by its first element
+        // so that E[d^2] - E[d]^2 does not cancel when |mean| >> std
+        const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(base + swz128_offset(t, 0, kSubRows)));
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int ci = 0; ci < 16; ++ci) {
+          const uint4 v = *reinterpret_cast<const uint4*>(base + swz128_offset(t, ci * 8, kSubRows));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float d0 = bf16lo(w[e]) - shift, d1 = bf16hi(w[e]) - shift;
+            s1 += d0 + d1;
+            s2 += d0 * d0 + d1 * d1;
+          }
+        }
+        const float m1 = s1 * (1.0f / kCz);
+        const float mean = shift + m1;
+        const float var = fmaxf(s2 * (1.0f / kCz) - m1 * m1, 0.f);
+        const float rstd = rsqrtf(var + eps);
+#pragma unroll 4
+        for (int ci = 0; ci < 16; ++ci) {
+          uint8_t* p = base + swz128_offset(t, ci * 8, kSubRows);
+          const uint4 v = *reinterpret_cast<const uint4*>(p);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          const float4 g0 = *reinterpret_cast<const float4*>(sGamma + ci * 8);
+          const float4 g1 = *reinterpret_cast<const float4*>(sGamma + ci * 8 + 4);
+          const float4 be0 = *reinterpret_cast<const float4*>(sBeta + ci * 8);
+          const float4 be1 = *reinterpret_cast<const float4*>(sBeta + ci * 8 + 4);
+          const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          const float bt[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            o[e] = pack_bf16x2((bf16lo(w[e]) - mean) * rstd * gg[2 * e] + bt[2 * e],
+                               (bf16hi(w[e]) - mean) * rstd * gg[2 * e + 1] + bt[2 * e + 1]);
+          *reinterpret_cast<uint4*>(p) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_async_shared();
+      mbar_arrive(&bar.a_full);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int s = (warp - 6) >> 2;                 // sub-tile of this warpgroup
+    const int qd = warp & 3;                       // TMEM lane quarter of this warp
+    const int r = qd * 32 + lane;                  // row within the sub-tile
+    const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
+    uint8_t* hs = sH + s * kSubBytes;
+    const bool leader = (warp == 6 + 4 * s) && lane == 0;
+    int it = 0;
+    int j = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
+      for (int c = 0; c < NC; ++c, ++it) {
+        if (!(ok = mbar_wait_warp(&bar.acc1_full[s], it & 1, abort_flag, status))) break;
+        // H[s] is free once the previous GEMM2 read it and any output store drained
+        if (!(ok = mbar_wait_warp(&bar.h_empty[s], (it & 1) ^ 1, abort_flag, status))) break;
+        if (c == 0 && j > 0 && !(ok = mbar_wait_warp(&bar.store_done[s], (j - 1) & 1, abort_flag, status))) break;
+        tc_fence_after();
+        __syncwarp();   // tcgen05.ld is warp-collective: reconverge after the per-lane waits
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float v[32];
+          tmem_ld32(tmem + lane_addr + 128 * s + 32 * g, v);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = c * kChunk + 32 * g + 2 * e;
+            const float bb0 = b1 ? __ldg(b1 + col) : 0.f, bb1 = b1 ? __ldg(b1 + col + 1) : 0.f;
+            packed[e] = pack_bf16x2(fmaxf(v[2 * e] + bb0, 0.f), fmaxf(v[2 * e + 1] + bb1, 0.f));
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(hs + swz128_offset(r, 32 * g + 8 * u, kSubRows)) =
+                make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.acc1_empty[s]);
+        fence_async_shared();
+        mbar_arrive(&bar.h_full[s]);
+      }
+      if (!ok) break;
+      // output: z~ = z + acc2 + b2, staged through H[s] for a TMA store
+      if (!(ok = mbar_wait_warp(&bar.acc2_full[s], j & 1, abort_flag, status))) break;
+      tc_fence_after();
+      __syncwarp();
+      const int64_t row_g = tile * kTileRows + s * kSubRows + r;
+      const bool in_range = row_g < P;
+      const bf16* zr = z_in + row_g * kCz;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float v[32];
+        tmem_ld32(tmem + lane_addr + 256 + 128 * s + 32 * g, v);
+        tmem_ld_wait();
+        uint32_t rw[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 q4 = make_uint4(0, 0, 0, 0);
+          if (in_range) q4 = *reinterpret_cast<const uint4*>(zr + 32 * g + 8 * u);
+          rw[4 * u] = q4.x; rw[4 * u + 1] = q4.y; rw[4 * u + 2] = q4.z; rw[4 * u + 3] = q4.w;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cl = 32 * g + 8 * u + 2 * e;
+            const uint32_t zw = rw[4 * u + e];
+            const float bb0 = b2 ? __ldg(b2 + cl) : 0.f, bb1 = b2 ? __ldg(b2 + cl + 1) : 0.f;
+            o[e] = pack_bf16x2(bf16lo(zw) + v[8 * u + 2 * e] + bb0, bf16hi(zw) + v[8 * u + 2 * e + 1] + bb1);
+          }
+          *reinterpret_cast<uint4*>(hs + swz128_offset(r, 32 * g + 8 * u, kSubRows)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bar.acc2_empty[s]);
+      fence_async_shared();
+      mbar_arrive(&bar.out_ready[s]);
+      if (leader) {
+        const int64_t y = tile * kTileRows + s * kSubRows;
+        if (mbar_wait(&bar.out_ready[s], j & 1, abort_flag, status) && y < P) {
+          tma_store_2d(&tm_zout, hs, 0, (int)y);
+          tma_store_2d(&tm_zout, hs + kBlockBytes, 64, (int)y);
+          tma_store_commit();
+          tma_store_wait_read0();
+        }
+        mbar_arrive(&bar.store_done[s]);
+      }
+      __syncwarp();
+    }
+    if (leader) tma_store_wait0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix, box {64, 128},
+// 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool transition_tc_supported(nt_dtype dt, int C_z, int H_t) {
+  return dt == NT_BF16 && C_z == kCz && H_t >= kChunk && H_t % kChunk == 0 && H_t <= 16384;
+}
+
+cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t,
+                                 const float* gamma, const float* beta, float eps, const void* W1,
+                                 const float* b1, const void* W2, const float* b2,
+                                 unsigned int* status, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  if (P > 0x7fffffffLL - kTileRows) return cudaErrorInvalidValue;
+  CUtensorMap m_zin, m_zout, m_w1, m_w2;
+  if (!make_map(&m_zin, z_in, C_z, (uint64_t)P) || !make_map(&m_zout, z_out, C_z, (uint64_t)P) ||
+      !make_map(&m_w1, W1, C_z, H_t) || !make_map(&m_w2, W2, H_t, C_z))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(transition_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (P + kTileRows - 1) / kTileRows;
+  const int grid = (int)min64(tiles, (int64_t)sm_count());
+  transition_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(m_zin, m_zout, m_w1, m_w2, (const bf16*)z_in, P, H_t,
+                                                          gamma, beta, eps, b1, b2, status);
+  return cudaGetLastError();
+}
+
 }  // namespace nt
