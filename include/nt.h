@@ -86,7 +86,7 @@ typedef struct nt_partition {
  * nt_partition_build -- exact sizes to tensor-backed offsets ([DL] Eq. 2,
  * Figure 2, Appendix A): exclusive scans of N_i and of N_i^2 on the device.
  *   d_lengths     [B] int32, N_i >= 0 (zero-length samples allowed).
- *   B             number of samples, >= 1.
+ *   B             number of samples, >= 0 (an empty batch gives T = P = 0).
  *   d_cu_seqlens  [B+1] int32 out.   d_pair_off [B+1] int64 out.
  *   d_totals      [4] int64 device scratch: T, P, max_len, check word.
  *   out           host struct filled with B, T, P, max_len and the pointers;
@@ -131,6 +131,34 @@ nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void
                             const void* s_right, int32_t C_s, const void* W_a, const void* W_b,
                             int32_t C_z, void* z, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/*
+ * nt_pair_broadcast_noalloc -- nt_pair_broadcast for callers that cannot
+ * allocate device memory.  The pages describe no counterpart: it is a
+ * property of this library, not of the method.
+ *
+ * nt_pair_broadcast needs a caller workspace for u and v.  Some callers
+ * cannot provide one: a plug-in whose host framework owns every device
+ * allocation and hands it none, or a real-time loop that must not pay for
+ * (or risk failing) an allocation on its hot path.  This call takes the same
+ * arguments minus the workspace and keeps u and v in a fixed array that the
+ * library declares in device memory (8 MiB, held on every GPU that loads the
+ * library until the process exits).  It allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *   Limit: 2 * T * C_z <= 2,097,152; larger problems return
+ *   NT_ERR_UNSUPPORTED (see nt_last_error) and enqueue nothing.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture on the device.
+ *   Sharing: every call uses the same array.  Calls that overlap on the GPU
+ *   (other streams, other host threads on the same device) race on it; order
+ *   them on one stream.  The kernels overwrite every element of u and v they
+ *   read, so earlier contents never reach a result and nothing needs clearing.
+ * Other arguments, outputs and errors are those of nt_pair_broadcast.
+ */
+nt_status nt_pair_broadcast_noalloc(const nt_partition* part, nt_dtype dtype, const void* s_left,
+                                    const void* s_right, int32_t C_s, const void* W_a,
+                                    const void* W_b, int32_t C_z, void* z, void* stream);
 
 /*
  * nt_pair_transition -- residual feature update of [DL] Eq. 1, second line,

@@ -71,6 +71,8 @@ nt_status check_partition(const nt_partition* p, bool need_rows) {
 
 }  // namespace
 
+nt_status record_error(nt_status s, const char* msg) { return fail(s, "%s", msg); }
+
 int sm_count() {
   static int cache[kMaxDevices] = {};
   int dev = 0;

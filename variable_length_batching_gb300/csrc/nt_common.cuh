@@ -24,6 +24,9 @@ __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Records a one-line detail for nt_last_error() and returns `s`.
+nt_status record_error(nt_status s, const char* msg);
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
 

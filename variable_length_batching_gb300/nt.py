@@ -44,6 +44,7 @@ SIGNATURES = {
     "nt_partition_rows": (_I32, [_PP, _P, _P, _P]),
     "nt_pair_broadcast_workspace_bytes": (_SZ, [_I64, _I32]),
     "nt_pair_broadcast": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P, _SZ, _P]),
+    "nt_pair_broadcast_noalloc": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P]),
     "nt_pair_transition": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P]),
     "nt_pair_reduce": (_I32, [_PP, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P]),
     "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P]),
@@ -171,6 +172,23 @@ def nt_pair_broadcast(part: Partition, s_left: torch.Tensor, s_right: torch.Tens
                                  _ptr(W_a), _ptr(W_b), C_z, _ptr(z), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nt_pair_broadcast")
+    return z
+
+
+def nt_pair_broadcast_noalloc(part: Partition, s_left: torch.Tensor, s_right: torch.Tensor,
+                              W_a: torch.Tensor, W_b: torch.Tensor, z: Optional[torch.Tensor] = None,
+                              stream=None) -> torch.Tensor:
+    """nt_pair_broadcast without a workspace argument: u and v live in the
+    library's own fixed device array (2 * T * C_z <= 2,097,152), for callers
+    that cannot allocate device memory.  ``z`` must then be supplied by the
+    caller too if the call itself may not allocate."""
+    T, C_s = s_left.shape
+    C_z = W_a.shape[0]
+    if z is None:
+        z = torch.empty(part.P, C_z, dtype=s_left.dtype, device=s_left.device)
+    st = lib().nt_pair_broadcast_noalloc(ctypes.byref(part.c), _dtype(s_left), _ptr(s_left), _ptr(s_right),
+                                         C_s, _ptr(W_a), _ptr(W_b), C_z, _ptr(z), _stream(stream))
+    _check(st, "nt_pair_broadcast_noalloc")
     return z
 
 
