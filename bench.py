@@ -155,6 +155,27 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+# Multi-rank bookkeeping (replicas: no collective on the data path)
+# ----------------------------------------------------------------------------
+
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of per-rank timings (the job is as slow as its
+    slowest rank); a no-op on one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(units_per_rank, world, ms_max):
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
+# ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
 
@@ -178,10 +199,10 @@ def run_gpu(args, rank, world, local_rank):
     lengths_d = torch.as_tensor(binp.lengths).to(dev)
     s_d = binp.s.to(dev)
     ainp = wl.make_attn_inputs(ATTN_CFG)
-    cu_host = np.concatenate([[0], np.cumsum(ainp.seqlens)]).astype(np.int32)
-    cu_d = torch.as_tensor(cu_host).to(dev)
+    apart = nt.nt_partition_build(torch.as_tensor(ainp.seqlens).to(dev))   # cu_seqlens on the device
+    cu_d = apart.cu_seqlens
     q_d, k_d, v_d = ainp.q.to(dev), ainp.k.to(dev), ainp.v.to(dev)
-    max_len = int(ainp.seqlens.max())
+    max_len = apart.max_len
     o_d = torch.empty_like(q_d)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -243,15 +264,10 @@ def run_gpu(args, rank, world, local_rank):
     ms = {n: float(np.mean(v)) for n, v in per.items()}
     block_ms = ms["partition"] + ms["broadcast"] + ms["transition"] + ms["reduce"]
     step_ms = block_ms + ms["attention"]
-    if world > 1:
-        t = torch.tensor([block_ms, ms["attention"], step_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        block_ms_max, attn_ms_max, step_ms_max = (float(x) for x in t.tolist())
-    else:
-        block_ms_max, attn_ms_max, step_ms_max = block_ms, ms["attention"], step_ms
+    block_ms_max, attn_ms_max, step_ms_max = max_over_ranks([block_ms, ms["attention"], step_ms], world, dev)
 
     # ---- end to end through the C ABI with host buffers ----
-    e2e = run_e2e(nt, binp, ainp, cu_host, dev, stream, args)
+    e2e = run_e2e(nt, binp, dev, stream, args)
 
     if rank != 0:
         return None
@@ -284,8 +300,8 @@ def run_gpu(args, rank, world, local_rank):
     roof["peak_source"] = f"{peak_src} ({'burst copy' if roof['bound'] == 'hbm' else 'cuBLAS bf16 burst'})"
     tr = traffic_record(dom)
     roof["traffic"] = tr
-    cells_per_s = world * P / (block_ms_max * 1e-3)
-    attn_tflops = world * aw["flops"] / (attn_ms_max * 1e-3) / 1e12
+    cells_per_s = job_throughput(P, world, block_ms_max)
+    attn_tflops = job_throughput(aw["flops"], world, attn_ms_max) / 1e12
     line = {
         "metric": METRIC,
         "value": cells_per_s,
@@ -320,7 +336,7 @@ def run_gpu(args, rank, world, local_rank):
     return line
 
 
-def run_e2e(nt, binp, ainp, cu_host, dev, stream, args):
+def run_e2e(nt, binp, dev, stream, args):
     """The block through the binding with inputs in pinned host memory: every
     step copies lengths, singles and weights in and reads z~ and s_out back."""
     def pin(t):
@@ -391,7 +407,8 @@ def oracle_attn_sample(budget_s=8.0):
     a = wl.make_attn_inputs(ATTN_CFG)
     f = wl.io_bits_to_f64
     q, k, v = f(a.q), f(a.k), f(a.v)
-    cu = np.concatenate([[0], np.cumsum(a.seqlens)])
+    from oracle.partition import partition
+    cu = partition(a.seqlens).cu_seqlens
     flops, t0, seg = 0, time.perf_counter(), 0
     while time.perf_counter() - t0 < budget_s and seg < len(a.seqlens):
         oattn.varlen_attention(q, k, v, cu, segments=[seg])
@@ -442,6 +459,84 @@ def run_reference(args, rank, world):
     }
 
 
+WORKLOADS = {"pairformer": wl.PAIRFORMER_BF16, "lognormal": wl.LOGNORMAL_BF16,
+             "near_uniform": wl.NEAR_UNIFORM_BF16, "stacked4": wl.STACKED4_BF16, "tiny": wl.TINY_FP32}
+
+
+def run_only(args):
+    """Time one call on one workload (profiling and per-kernel rooflines):
+    ``--only {partition,broadcast,transition,reduce,block,attention}``."""
+    from variable_length_batching_gb300 import build, nt
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.only == "attention":
+        cfg = ATTN_CFG
+        a = wl.make_attn_inputs(cfg)
+        apart = nt.nt_partition_build(torch.as_tensor(a.seqlens).to(dev))
+        cu, ml = apart.cu_seqlens, apart.max_len
+        q, k, v = a.q.to(dev), a.k.to(dev), a.v.to(dev)
+        o = torch.empty_like(q)
+        fn = lambda: nt.nt_varlen_attn(q, k, v, cu, ml, out=o, stream=stream)
+        w = attn_work(a.seqlens, cfg.H, cfg.d)
+        bound, name = "tensor", cfg.name
+    else:
+        cfg = WORKLOADS[args.workload]
+        inp = wl.make_block_inputs(cfg)
+        wd = _dev_weights(inp.blocks[0], dev)
+        lengths = torch.as_tensor(inp.lengths).to(dev)
+        s = inp.s.to(dev)
+        part = nt.nt_partition_build(lengths)
+        z = nt.nt_pair_broadcast(part, s, s, wd.W_a, wd.W_b)
+        ws = torch.empty(nt.nt_pair_broadcast_workspace_bytes(part.T, cfg.C_z), dtype=torch.uint8, device=dev)
+        zt = torch.empty_like(z)
+        m = torch.empty(part.T, cfg.C_z, dtype=z.dtype, device=dev)
+        so = torch.empty(part.T, cfg.C_s, dtype=z.dtype, device=dev)
+        es = 2 if cfg.dtype == wl.BF16 else 4
+        bw = block_work(part.T, part.P, cfg.C_s, cfg.C_z, cfg.H_t, es)
+        fns = {
+            "partition": (lambda: nt.nt_partition_build(lengths, stream=stream), bw["partition"], "latency"),
+            "broadcast": (lambda: nt.nt_pair_broadcast(part, s, s, wd.W_a, wd.W_b, z=z, workspace=ws,
+                                                       stream=stream), bw["broadcast"], "hbm"),
+            "transition": (lambda: nt.nt_pair_transition(part, z, wd.ln_gamma, wd.ln_beta, wd.W1, wd.b1, wd.W2,
+                                                         wd.b2, out=zt, stream=stream), bw["transition"], "tensor"),
+            "reduce": (lambda: nt.nt_pair_reduce(part, zt, wd.W_g, wd.b_g, s_in=s, m=m, s_out=so, stream=stream),
+                       bw["reduce"], "hbm"),
+            "block": (lambda: nt.block_forward(part, s, wd, z=z, workspace=ws, s_out=so, stream=stream),
+                      {k: sum(v[k] for v in bw.values()) for k in ("bytes", "flops")}, "tensor"),
+        }
+        fn, w, bound = fns[args.only]
+        name = cfg.name
+    for _ in range(args.warmup):
+        flush.fill_(0.0)
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    nt.nt_device_status(stream)
+    ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+    out = {"kernel": args.only, "workload": name, "ms": ms, "steps": args.steps}
+    if bound == "tensor":
+        out.update({"bound": "tensor", "achieved": w["flops"] / ms / 1e9, "unit": "TFLOP/s",
+                    "peak": peaks["bf16_tflops"]})
+    elif bound == "hbm":
+        out.update({"bound": "hbm", "achieved": w["bytes"] / ms / 1e6, "unit": "GB/s", "peak": peaks["hbm_gbs"]})
+    if "peak" in out:
+        out["frac"] = out["achieved"] / out["peak"]
+        out["peak_source"] = peak_src
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,7 +544,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    choices=["partition", "broadcast", "transition", "reduce", "block", "attention"],
+                    help="time one call on one workload instead of the whole step")
+    ap.add_argument("--workload", default="pairformer", choices=sorted(WORKLOADS))
     args = ap.parse_args()
+    if args.only:
+        run_only(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -256,7 +256,10 @@ def test_varlen_attention_zero_leakage(nt):
     cu_d = torch.as_tensor(cu.astype(np.int32)).to(DEV)
     o2, _ = nt.nt_varlen_attn(q.to(DEV), k.to(DEV), v.to(DEV), cu_d, 200)
     assert torch.equal(o2[:lo], o[:lo]) and torch.equal(o2[hi:], o[hi:])
-    assert torch.allclose(o2[lo:hi].float(), torch.full_like(o2[lo:hi].float(), 7.0))
+    # a constant V comes back as that constant, within the bf16 tolerance: the
+    # kernel normalises by a running max that may trail the true one, so the
+    # largest probability is not exactly 1 and P's bf16 rounding stays visible
+    assert normwise_err(to_np(o2[lo:hi]), np.full((hi - lo, 2, 64), 7.0)) <= TOL["bf16"]
 
 
 def test_varlen_attention_full_size_sampled(nt):

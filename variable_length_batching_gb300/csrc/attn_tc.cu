@@ -1,23 +1,23 @@
 // Variable-length attention on the tcgen05 tensor cores, bf16 in / fp32
 // accumulate, head width 64 ("Variable-length attention and data packing",
 // "What it is" / "How it works"): queries of segment i attend only to keys
-// in [cu_i, cu_{i+1}), walked in key tiles of 128, with an online softmax.
+// in [cu_i, cu_{i+1}), walked in key tiles of 64, with an online softmax.
 //
 // One CTA per (segment, 128-query tile, head).  The grid is sized from
 // max_len (ceil(max_len / 128) query tiles per segment); CTAs whose tile
 // starts past their segment's end exit at once, so no work list is needed.
-// Warps: 0 = TMA producer (Q once, K and V tiles double-buffered through
-// 3-D tensor maps over the token-major [T, H, d] tensors), 1 = TMEM owner
-// and MMA issuer, 2-5 = softmax, one query row per thread.
-//   S = Q K^T   (M=128, N=128, K=64)  -> TMEM columns [0, 128)
-//   O_j = P V_j (M=128, N=64,  K=128) -> TMEM columns [128, 192); P is the
-//   bf16 probability tile written by the softmax warps into shared memory
-//   (K-major); V is read as an MN-major operand straight from its TMA tile.
-// The running output stays in registers: O = O * exp(m_old - m_new) + O_j.
-// Two CTAs fit on an SM (112 KB shared memory, 256 TMEM columns each), so
-// one CTA's softmax overlaps the other's MMAs.
-#include <cudaTypedefs.h>
-
+// Warps: 0 = TMA producer (Q once; K and V tiles of 64 tokens through a
+// 3-stage ring, 3-D tensor maps over the token-major [T, H, d] tensors),
+// 1 = TMEM owner and MMA issuer, 2-5 = softmax, one query row per thread.
+//   S_j = Q K_j^T  (M=128, N=64, K=64)  -> TMEM S[j & 1] (double-buffered)
+//   O  += P_j V_j   (M=128, N=64, K=64)  -> TMEM O, accumulated by the MMA
+// P_j is the bf16 probability tile, written by the softmax warps into
+// shared memory (K-major, double-buffered); V is read as an MN-major operand
+// straight from its TMA tile.  The running max moves only when a tile's max
+// exceeds it by more than 8 (log2 units), so O in TMEM is rescaled in place
+// on those tiles only.  A quarter of each full tile's exponentials run on the
+// FMA pipe (exp2_fma), the rest on the SFU.
+// Two CTAs fit on an SM (96 KB shared memory, 256 TMEM columns each).
 #include "tc_ptx.cuh"
 
 namespace nt {
@@ -27,22 +27,25 @@ using namespace tc;
 
 constexpr int kD = 64;
 constexpr int kBQ = 128;
-constexpr int kBK = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 3;
 constexpr int kThreads = 6 * 32;
-constexpr uint32_t kTileBytes = 128 * kD * 2;     // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kQBytes = kBQ * kD * 2;          // 16 KB
+constexpr uint32_t kKVBytes = kBK * kD * 2;         // 8 KB
+constexpr uint32_t kPBytes = kBQ * kBK * 2;         // 16 KB
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;     // 2 stages
-constexpr uint32_t kOffV = kOffK + 2 * kTileBytes; // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes; // 128 x 128 bf16 = 32 KB
-constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256;   // two CTAs per SM: 2 x (112 KB + 1 KB reserved) fit
+constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
+constexpr uint32_t kOffP = kOffV + kStages * kKVBytes;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColO = 128;
+constexpr uint32_t kColS = 0, kColO = 128;          // S[b] at 64*b; O at 128
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full, s_empty, p_full, o_full;
+  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_full[2], p_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -71,12 +74,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (qi == QT - 1 && n > QT * kBQ && threadIdx.x == 0 && h == 0) flag_device(status, kDevCheck);
   const int q0 = lo + qi * kBQ;
   if (q0 >= hi) return;                       // CTA-uniform: nothing allocated yet
-  const int nk = (n + kBK - 1) / kBK;
-
-  if (smem_u32(smem_raw) & 1023) {               // the swizzled tiles need 1024-byte alignment
+  if (smem_u32(smem_raw) & 1023) {            // the swizzled tiles need 1024-byte alignment
     if (threadIdx.x == 0) flag_device(status, kDevCheck);
     return;
   }
+  const int nk = (n + kBK - 1) / kBK;
+
   uint8_t* smem = smem_raw;
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
@@ -88,14 +91,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (threadIdx.x == 0) {
     mbar_init(&bar.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar.k_full[i], 1); mbar_init(&bar.k_empty[i], 1);
       mbar_init(&bar.v_full[i], 1); mbar_init(&bar.v_empty[i], 1);
     }
-    mbar_init(&bar.s_full, 1);
-    mbar_init(&bar.s_empty, 128);
-    mbar_init(&bar.p_full, 128);
-    mbar_init(&bar.o_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.s_full[i], 1); mbar_init(&bar.p_full[i], 128); mbar_init(&bar.p_empty[i], 1);
+    }
     mbar_init(&bar.mma_done, 1);
     bar.abort = 0;
     fence_mbar_init();
@@ -111,59 +113,61 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&bar.q_full, kTileBytes);
+      mbar_arrive_expect_tx(&bar.q_full, kQBytes);
       tma_load_3d(sQ, &tm_q, &bar.q_full, 0, h, q0);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nk; ++j) {
-        const int st = j & 1, rd = j >> 1;
+        const int st = j % kStages, rd = j / kStages;
         if (!mbar_wait(&bar.k_empty[st], (rd & 1) ^ 1, abort_flag, status)) break;
-        mbar_arrive_expect_tx(&bar.k_full[st], kTileBytes);
-        tma_load_3d(sK + st * kTileBytes, &tm_k, &bar.k_full[st], 0, h, lo + j * kBK);
+        mbar_arrive_expect_tx(&bar.k_full[st], kKVBytes);
+        tma_load_3d(sK + st * kKVBytes, &tm_k, &bar.k_full[st], 0, h, lo + j * kBK);
         k_issued = j + 1;
         if (!mbar_wait(&bar.v_empty[st], (rd & 1) ^ 1, abort_flag, status)) break;
-        mbar_arrive_expect_tx(&bar.v_full[st], kTileBytes);
-        tma_load_3d(sV + st * kTileBytes, &tm_v, &bar.v_full[st], 0, h, lo + j * kBK);
+        mbar_arrive_expect_tx(&bar.v_full[st], kKVBytes);
+        tma_load_3d(sV + st * kKVBytes, &tm_v, &bar.v_full[st], 0, h, lo + j * kBK);
         v_issued = j + 1;
       }
       // drain the copies this thread issued
       mbar_wait(&bar.q_full, 0, nullptr, status);
-      for (int j = k_issued - 2; j < k_issued; ++j)
-        if (j >= 0) mbar_wait(&bar.k_full[j & 1], (j >> 1) & 1, nullptr, status);
-      for (int j = v_issued - 2; j < v_issued; ++j)
-        if (j >= 0) mbar_wait(&bar.v_full[j & 1], (j >> 1) & 1, nullptr, status);
+      for (int j = k_issued - kStages; j < k_issued; ++j)
+        if (j >= 0) mbar_wait(&bar.k_full[j % kStages], (j / kStages) & 1, nullptr, status);
+      for (int j = v_issued - kStages; j < v_issued; ++j)
+        if (j >= 0) mbar_wait(&bar.v_full[j % kStages], (j / kStages) & 1, nullptr, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, 128);
+      const uint32_t id_s = idesc_bf16_f32(128, kBK);
       const uint32_t id_o = idesc_bf16_f32(128, kD) | (1u << 16);   // B (= V) MN-major
       const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV), p_base = smem_u32(sP);
       bool ok = mbar_wait(&bar.q_full, 0, abort_flag, status);
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(&bar.p_full, j & 1, abort_flag, status)) return false;
-        if (!mbar_wait(&bar.v_full[j & 1], (j >> 1) & 1, abort_flag, status)) return false;
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % kStages;
+        if (!mbar_wait(&bar.k_full[st], (j / kStages) & 1, abort_flag, status)) return false;
         tc_fence_after();
-        const uint32_t vb = v_base + (j & 1) * kTileBytes;
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t pa = p_base + (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_bf16(tmem + kColO, sdesc_k128(pa), sdesc_k128(vb + kk * 2048), id_o, kk > 0);
-        }
-        mma_commit(&bar.o_full);
-        mma_commit(&bar.v_empty[j & 1]);
+        const uint32_t kb = k_base + st * kKVBytes;
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_bf16(tmem + kColS + 64 * (j & 1), sdesc_k128(q_base + kk * 32), sdesc_k128(kb + kk * 32), id_s, kk > 0);
+        mma_commit(&bar.s_full[j & 1]);
+        mma_commit(&bar.k_empty[st]);
         return true;
       };
+      if (ok) ok = issue_s(0);
+      if (ok && nk > 1) ok = issue_s(1);
       for (int j = 0; j < nk && ok; ++j) {
-        if (!(ok = mbar_wait(&bar.k_full[j & 1], (j >> 1) & 1, abort_flag, status))) break;
-        if (j > 0 && !(ok = mbar_wait(&bar.s_empty, (j - 1) & 1, abort_flag, status))) break;
+        // P_j written (and S_j fully read, and O rescaled if needed) by the softmax
+        if (!(ok = mbar_wait(&bar.p_full[j & 1], (j >> 1) & 1, abort_flag, status))) break;
+        const int st = j % kStages;
+        if (!(ok = mbar_wait(&bar.v_full[st], (j / kStages) & 1, abort_flag, status))) break;
         tc_fence_after();
-        const uint32_t kb = k_base + (j & 1) * kTileBytes;
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tmem + kColS, sdesc_k128(q_base + kk * 32), sdesc_k128(kb + kk * 32), id_s, kk > 0);
-        mma_commit(&bar.s_full);
-        mma_commit(&bar.k_empty[j & 1]);
-        if (j > 0 && !(ok = issue_pv(j - 1))) break;
+        const uint32_t pb = p_base + (j & 1) * kPBytes, vb = v_base + st * kKVBytes;
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_bf16(tmem + kColO, sdesc_k128(pb + kk * 32), sdesc_k128(vb + kk * 2048), id_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar.p_empty[j & 1]);     // PV_j done: P[j&1] free, O holds tiles 0..j
+        mma_commit(&bar.v_empty[st]);
+        if (j + 2 < nk && !(ok = issue_s(j + 2))) break;
       }
-      if (ok) issue_pv(nk - 1);
       mma_commit(&bar.mma_done);
       mbar_wait(&bar.mma_done, 0, nullptr, status);
     }
@@ -173,92 +177,121 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int r = qd * 32 + lane;                 // query row within the tile
     const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
     float m = -INFINITY, l = 0.f;
-    float acc[kD];
-#pragma unroll
-    for (int c = 0; c < kD; ++c) acc[c] = 0.f;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
-      if (!(ok = mbar_wait_warp(&bar.s_full, j & 1, abort_flag, status))) break;
+      const int sb = j & 1;
+      if (!(ok = mbar_wait_warp(&bar.s_full[sb], (j >> 1) & 1, abort_flag, status))) break;
       tc_fence_after();
       __syncwarp();
-      const int kvalid = min(kBK, n - j * kBK);    // keys of this tile inside the segment
-      // pass 1 over S in TMEM: the row maximum of the scaled scores
+      const int kvalid = min(kBK, n - j * kBK);   // keys of this tile inside the segment
+      const bool full = kvalid == kBK;
+      const uint32_t s_addr = tmem + lane_addr + kColS + 64 * sb;
+      // pass 1: row maximum of the raw scores (scale > 0)
       float mx = -INFINITY;
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < 2; ++g) {
         float sv[32];
-        tmem_ld32(tmem + lane_addr + kColS + 32 * g, sv);
+        tmem_ld32(s_addr + 32 * g, sv);
         tmem_ld_wait();
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (32 * g + c < kvalid) mx = fmaxf(mx, sv[c] * scale_log2);
+          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, sv[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (32 * g + c < kvalid) mx = fmaxf(mx, sv[c]);
+        }
       }
-      const float m_new = fmaxf(m, mx);
-      const float corr = exp2f(m - m_new);        // 0 on the first tile (m = -inf)
-      if (j > 0) {
-        // fold in O_{j-1} (relative to the previous max), then rescale; after
-        // this wait PV_{j-1} is done, so P may be overwritten
-        if (!(ok = mbar_wait_warp(&bar.o_full, (j - 1) & 1, abort_flag, status))) break;
+      // lazy running max: move it only when it grows by more than 8 (log2 units)
+      const float cand = mx * scale_log2;
+      float corr = 1.0f;
+      const bool move = cand > m + 8.0f;
+      if (move) {
+        corr = ex2_approx(m - cand);              // 0 on the first tile (m = -inf)
+        m = cand;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, move)) {
+        // rescale this warp's rows of O in TMEM once every earlier PV is done.
+        // PV_{j-1} completes phase (j-1)>>1 of p_empty[(j-1)&1]; that barrier
+        // is waited every other tile, so this wait is never two phases behind.
+        if (!(ok = mbar_wait_warp(&bar.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, status))) break;
         tc_fence_after();
         __syncwarp();
-#pragma unroll
+#pragma unroll 1
         for (int g = 0; g < 2; ++g) {
           float ov[32];
           tmem_ld32(tmem + lane_addr + kColO + 32 * g, ov);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) acc[32 * g + c] = (acc[32 * g + c] + ov[c]) * corr;
+          for (int c = 0; c < 32; ++c) ov[c] *= corr;
+          tmem_st32(tmem + lane_addr + kColO + 32 * g, ov);
         }
+        tmem_st_wait();
       }
-      // pass 2: P = exp2(s - m_new) -> bf16 -> shared memory (K-major, two 64-key blocks)
+      l *= corr;
+      // P_j -> P[sb]; PV_{j-2} has finished reading that buffer
+      if (j >= 2 && !(ok = mbar_wait_warp(&bar.p_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag, status))) break;
+      uint8_t* pbuf = sP + sb * kPBytes;
       float rs = 0.f;
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < 2; ++g) {
         float sv[32];
-        tmem_ld32(tmem + lane_addr + kColS + 32 * g, sv);
+        tmem_ld32(s_addr + 32 * g, sv);
         tmem_ld_wait();
         uint32_t pk[16];
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float p0 = (32 * g + c < kvalid) ? exp2f(sv[c] * scale_log2 - m_new) : 0.f;
-          const float p1 = (32 * g + c + 1 < kvalid) ? exp2f(sv[c + 1] * scale_log2 - m_new) : 0.f;
-          rs += p0 + p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+          for (int c = 0; c < 32; c += 2) {
+            const float x0 = fmaf(sv[c], scale_log2, -m), x1 = fmaf(sv[c + 1], scale_log2, -m);
+            // one in four exponentials on the FMA pipe, the rest on the SFU
+            const float p0 = ex2_approx(x0);
+            const float p1 = ((c & 2) == 2) ? exp2_fma(x1) : ex2_approx(x1);
+            rs += p0 + p1;
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float p0 = (32 * g + c < kvalid) ? ex2_approx(fmaf(sv[c], scale_log2, -m)) : 0.f;
+            const float p1 = (32 * g + c + 1 < kvalid) ? ex2_approx(fmaf(sv[c + 1], scale_log2, -m)) : 0.f;
+            rs += p0 + p1;
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(sP + swz128_offset(r, 32 * g + 8 * u, 128)) =
+          *reinterpret_cast<uint4*>(pbuf + swz128_offset(r, 32 * g + 8 * u, 128)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
+      l += rs;
       tc_fence_before();
-      mbar_arrive(&bar.s_empty);
-      l = l * corr + rs;
-      m = m_new;
       fence_async_shared();
-      mbar_arrive(&bar.p_full);
+      mbar_arrive(&bar.p_full[sb]);
     }
-    if (ok && mbar_wait_warp(&bar.o_full, (nk - 1) & 1, abort_flag, status)) {
+    if (ok && mbar_wait_warp(&bar.p_empty[(nk - 1) & 1], ((nk - 1) >> 1) & 1, abort_flag, status)) {
       tc_fence_after();
       __syncwarp();
-      float ov[kD];
-      tmem_ld32(tmem + lane_addr + kColO, ov);
-      tmem_ld32(tmem + lane_addr + kColO + 32, ov + 32);
-      tmem_ld_wait();
       const int t = q0 + r;
-      if (t < hi) {
-        const float inv = 1.0f / l;
-        bf16* op = o + ((int64_t)t * H + h) * kD;
+      const float inv = 1.0f / l;
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        float ov[32];
+        tmem_ld32(tmem + lane_addr + kColO + 32 * g, ov);
+        tmem_ld_wait();
+        if (t < hi) {
+          bf16* op = o + ((int64_t)t * H + h) * kD + 32 * g;
 #pragma unroll
-        for (int u = 0; u < kD / 8; ++u) {
-          uint4 w;
-          w.x = pack_bf16x2((acc[8 * u] + ov[8 * u]) * inv, (acc[8 * u + 1] + ov[8 * u + 1]) * inv);
-          w.y = pack_bf16x2((acc[8 * u + 2] + ov[8 * u + 2]) * inv, (acc[8 * u + 3] + ov[8 * u + 3]) * inv);
-          w.z = pack_bf16x2((acc[8 * u + 4] + ov[8 * u + 4]) * inv, (acc[8 * u + 5] + ov[8 * u + 5]) * inv);
-          w.w = pack_bf16x2((acc[8 * u + 6] + ov[8 * u + 6]) * inv, (acc[8 * u + 7] + ov[8 * u + 7]) * inv);
-          *reinterpret_cast<uint4*>(op + 8 * u) = w;
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(ov[8 * u] * inv, ov[8 * u + 1] * inv);
+            w.y = pack_bf16x2(ov[8 * u + 2] * inv, ov[8 * u + 3] * inv);
+            w.z = pack_bf16x2(ov[8 * u + 4] * inv, ov[8 * u + 5] * inv);
+            w.w = pack_bf16x2(ov[8 * u + 6] * inv, ov[8 * u + 7] * inv);
+            *reinterpret_cast<uint4*>(op + 8 * u) = w;
+          }
         }
-        if (lse) lse[(int64_t)h * T + t] = (m + log2f(l)) * 0.69314718055994531f;
       }
+      if (t < hi && lse) lse[(int64_t)h * T + t] = (m + log2f(l)) * 0.69314718055994531f;
     }
   }
 
@@ -271,31 +304,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 3-D bf16 map over a token-major [T, H, 64] tensor: box {64, 1, 128}
-// (one head, 128 tokens), 128-byte swizzle.
-bool make_map_thd(CUtensorMap* map, const void* ptr, int64_t T, int H) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T};
-  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-  cuuint32_t box[3] = {(cuuint32_t)kD, 1, 128};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// 3-D map over a token-major [T, H, 64] tensor: box {64, 1, rows} (one head,
+// `rows` tokens), 128-byte swizzle.
+bool make_map_thd(CUtensorMap* map, const void* ptr, int64_t T, int H, uint32_t rows) {
+  const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)T};
+  const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};
+  const uint32_t box[3] = {(uint32_t)kD, 1, rows};
+  return make_tmap_bf16(map, ptr, 3, dims, strides, box);
 }
 
 }  // namespace
@@ -307,7 +322,7 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, const in
                            unsigned int* status, cudaStream_t s) {
   if (T == 0 || B == 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
-  if (!make_map_thd(&mq, q, T, H) || !make_map_thd(&mk, k, T, H) || !make_map_thd(&mv, v, T, H))
+  if (!make_map_thd(&mq, q, T, H, kBQ) || !make_map_thd(&mk, k, T, H, kBK) || !make_map_thd(&mv, v, T, H, kBK))
     return cudaErrorInvalidValue;
   const int QT = max(1, (max_len + kBQ - 1) / kBQ);
   const int64_t items = (int64_t)B * QT * H;

@@ -16,6 +16,55 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRows = 4;
 
+// C_z with kThreads % (C_z / 8) == 0: a thread's 8-feature slice f is the
+// same for every cell it writes, so the kRows u-vectors it adds are loaded
+// once per row group and only v is read per cell.
+template <typename TOut>
+__global__ void __launch_bounds__(kThreads)
+broadcast_fixed_slice_kernel(const float* __restrict__ u, const float* __restrict__ v,
+                             const int32_t* __restrict__ lengths, const int32_t* __restrict__ cu,
+                             const int32_t* __restrict__ row_sample, const int64_t* __restrict__ row_start,
+                             int64_t T, int C_z, TOut* __restrict__ z) {
+  const int vecs = C_z / 8;
+  const int f = (threadIdx.x % vecs) * 8;
+  const int b_step = kThreads / vecs;
+  for (int64_t g = blockIdx.x; g * kRows < T; g += gridDim.x) {
+    const int64_t r0 = g * kRows;
+    const int64_t r_end = min(r0 + kRows, T);
+    int64_t r = r0;
+    while (r < r_end) {
+      // the rows [r, r1) of one sample inside this group
+      const int i = row_sample[r];
+      const int64_t n = lengths[i];
+      const int64_t c0 = cu[i];
+      const int64_t r1 = min(r_end, c0 + n);
+      float uu[kRows][8];
+      int64_t rs[kRows];
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        if (r + k < r1) {
+          load8(u + (r + k) * C_z + f, uu[k]);
+          rs[k] = row_start[r + k];
+        }
+      }
+      for (int64_t b = threadIdx.x / vecs; b < n; b += b_step) {
+        float vv[8];
+        load8(v + (c0 + b) * C_z + f, vv);
+#pragma unroll
+        for (int k = 0; k < kRows; ++k) {
+          if (r + k < r1) {
+            float o[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) o[t] = uu[k][t] + vv[t];
+            store8_stream(z + (rs[k] + b) * C_z + f, o);
+          }
+        }
+      }
+      r = r1;
+    }
+  }
+}
+
 template <typename TOut>
 __global__ void __launch_bounds__(kThreads)
 broadcast_kernel(const float* __restrict__ u, const float* __restrict__ v,
@@ -92,7 +141,17 @@ cudaError_t launch_broadcast(nt_dtype dt, const float* u, const float* v, const 
                              int C_z, void* z, cudaStream_t s) {
   if (p->T == 0) return cudaSuccess;
   const int sms = sm_count();
-  if (C_z % 8 == 0) {
+  if (C_z % 8 == 0 && kThreads % (C_z / 8) == 0) {
+    const int64_t groups = (p->T + kRows - 1) / kRows;
+    const int grid = (int)min64(groups, (int64_t)sms * 16);
+    if (dt == NT_BF16)
+      broadcast_fixed_slice_kernel<bf16><<<grid, kThreads, 0, s>>>(u, v, p->lengths, p->cu_seqlens, p->row_sample,
+                                                                   p->row_start, p->T, C_z, (bf16*)z);
+    else
+      broadcast_fixed_slice_kernel<float><<<grid, kThreads, 0, s>>>(u, v, p->lengths, p->cu_seqlens,
+                                                                    p->row_sample, p->row_start, p->T, C_z,
+                                                                    (float*)z);
+  } else if (C_z % 8 == 0) {
     const int64_t groups = (p->T + kRows - 1) / kRows;
     const int grid = (int)min64(groups, (int64_t)sms * 16);
     if (dt == NT_BF16)

@@ -1,0 +1,183 @@
+// Single-side projections Y = X W^T (+ b) (+ R) on the tcgen05 tensor cores,
+// bf16 operands, fp32 accumulation: the u, v and g Linear layers of the
+// block ("DanLing NestedTensor" Eq. 1; projections are V W^T + b, section
+// 3.3 "Dense work across valid positions") over the T packed single rows.
+//
+// One CTA per 128 x 128 output tile (and per problem: u and v run in one
+// launch).  Warp 0 streams 64-wide K blocks of X and W through a 2-stage
+// TMA ring, warp 1 issues the MMAs into a 128-column TMEM accumulator, and
+// all four warps run the epilogue: TMEM -> +bias (+residual) -> global.
+#include "tc_ptx.cuh"
+
+namespace nt {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128, kBN = 128, kBK = 64;
+constexpr int kThreads = 128;
+constexpr uint32_t kOpBytes = 128 * kBK * 2;          // 16 KB per operand block
+constexpr uint32_t kStageBytes = 2 * kOpBytes;        // X block + W block
+constexpr uint32_t kSmemBytes = 2 * kStageBytes + 128;
+
+struct Bars {
+  uint64_t full[2], empty[2], acc_full;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Prob {
+  const float* bias;
+  const bf16* R;     // residual [M, N] or null
+  void* Y;           // [M, N], fp32 or bf16
+};
+
+template <bool kOutF32>
+__global__ void __launch_bounds__(kThreads)
+linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant__ CUtensorMap tw0,
+                 const __grid_constant__ CUtensorMap tx1, const __grid_constant__ CUtensorMap tw1, Prob p0, Prob p1,
+                 int64_t M, int N, int K, unsigned int* status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023) {
+    if (threadIdx.x == 0) flag_device(status, kDevCheck);
+    return;
+  }
+  const CUtensorMap* tx = blockIdx.z == 0 ? &tx0 : &tx1;
+  const CUtensorMap* tw = blockIdx.z == 0 ? &tw0 : &tw1;
+  const Prob& pr = blockIdx.z == 0 ? p0 : p1;
+  Bars& bar = *reinterpret_cast<Bars*>(smem + 2 * kStageBytes);
+  volatile int* abort_flag = &bar.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m0 = (int64_t)blockIdx.x * kBM;
+  const int n0 = blockIdx.y * kBN;
+  const int nkb = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
+    mbar_init(&bar.acc_full, 1);
+    bar.abort = 0;
+    fence_mbar_init();
+    fence_async_shared();
+  }
+  if (warp == 1) tmem_alloc(&bar.tmem_base, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    int issued = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int st = kb & 1;
+      if (!mbar_wait(&bar.empty[st], ((kb >> 1) & 1) ^ 1, abort_flag, status)) break;
+      mbar_arrive_expect_tx(&bar.full[st], kStageBytes);
+      tma_load_2d(smem + st * kStageBytes, tx, &bar.full[st], kb * kBK, (int)m0);
+      tma_load_2d(smem + st * kStageBytes + kOpBytes, tw, &bar.full[st], kb * kBK, n0);
+      issued = kb + 1;
+    }
+    for (int kb = issued - 2; kb < issued; ++kb)
+      if (kb >= 0) mbar_wait(&bar.full[kb & 1], (kb >> 1) & 1, nullptr, status);
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+    const uint32_t base = smem_u32(smem);
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int st = kb & 1;
+      if (!mbar_wait(&bar.full[st], (kb >> 1) & 1, abort_flag, status)) break;
+      tc_fence_after();
+      const uint32_t a = base + st * kStageBytes, b = a + kOpBytes;
+      for (int k = 0; k < kBK / 16; ++k)
+        mma_bf16(tmem, sdesc_k128(a + k * 32), sdesc_k128(b + k * 32), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+      mma_commit(&bar.empty[st]);
+    }
+    mma_commit(&bar.acc_full);
+  }
+  // epilogue: every warp, one accumulator row per thread
+  const int r = warp * 32 + lane;
+  const int64_t row = m0 + r;
+  if (mbar_wait_warp(&bar.acc_full, 0, abort_flag, status)) {
+    tc_fence_after();
+    __syncwarp();
+    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+    for (int g = 0; g < kBN / 32; ++g) {
+      float v[32];
+      tmem_ld32(tmem + lane_addr + 32 * g, v);
+      tmem_ld_wait();
+      if (row < M) {
+        const int c0 = n0 + 32 * g;
+        if (pr.bias) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] += pr.bias[c0 + c];
+        }
+        if (pr.R) {
+          const bf16* rp = pr.R + row * N + c0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 q4 = *reinterpret_cast<const uint4*>(rp + 8 * u);
+            const uint32_t w[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[8 * u + 2 * e] += bf16lo(w[e]);
+              v[8 * u + 2 * e + 1] += bf16hi(w[e]);
+            }
+          }
+        }
+        if (kOutF32) {
+          float* y = static_cast<float*>(pr.Y) + row * N + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(y + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+        } else {
+          bf16* y = static_cast<bf16*>(pr.Y) + row * N + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 8)
+            *reinterpret_cast<uint4*>(y + c) = make_uint4(pack_bf16x2(v[c], v[c + 1]), pack_bf16x2(v[c + 2], v[c + 3]),
+                                                          pack_bf16x2(v[c + 4], v[c + 5]), pack_bf16x2(v[c + 6], v[c + 7]));
+        }
+      }
+    }
+  }
+  if (warp == 1 && lane == 0) {
+    // nothing may still be writing TMEM when it is released
+    mbar_wait(&bar.acc_full, 0, nullptr, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+}  // namespace
+
+bool linear_tc_supported(int in_dtype, int64_t M, int N, int K) {
+  return in_dtype == NT_BF16 && M > 0 && N % kBN == 0 && K % kBK == 0 && K > 0 && M < 0x7fffffffLL - kBM;
+}
+
+cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob, int64_t M, int N, int K,
+                             unsigned int* status, cudaStream_t s) {
+  if (M == 0 || nprob == 0) return cudaSuccess;
+  CUtensorMap tx[2], tw[2];
+  Prob pp[2];
+  for (int i = 0; i < 2; ++i) {
+    const LinearProblem& lp = probs[i < nprob ? i : 0];
+    if (!make_tmap_rows(&tx[i], lp.X, (uint64_t)K, (uint64_t)M) || !make_tmap_rows(&tw[i], lp.W, (uint64_t)K, (uint64_t)N))
+      return cudaErrorInvalidValue;
+    pp[i] = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y};
+  }
+  dim3 grid((unsigned)((M + kBM - 1) / kBM), N / kBN, nprob);
+  cudaError_t e;
+  if (out_f32) {
+    e = cudaFuncSetAttribute(linear_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    linear_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tx[0], tw[0], tx[1], tw[1], pp[0], pp[1], M, N, K, status);
+  } else {
+    e = cudaFuncSetAttribute(linear_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    linear_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tx[0], tw[0], tx[1], tw[1], pp[0], pp[1], M, N, K, status);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace nt

@@ -181,7 +181,9 @@ nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void
   float* u = static_cast<float*>(workspace);
   float* v = u + part->T * (int64_t)C_z;
   LinearProblem probs[2] = {{s_left, W_a, nullptr, nullptr, u}, {s_right, W_b, nullptr, nullptr, v}};
-  cudaError_t e = launch_linear(dtype, 1, probs, 2, part->T, C_z, C_s, s);
+  cudaError_t e = linear_tc_supported(dtype, part->T, C_z, C_s)
+                      ? launch_linear_tc(1, probs, 2, part->T, C_z, C_s, status_word(), s)
+                      : launch_linear(dtype, 1, probs, 2, part->T, C_z, C_s, s);
   if (e != cudaSuccess) return cuda_fail(e, "projection launch");
   e = launch_broadcast(dtype, u, v, part, C_z, z, s);
   if (e != cudaSuccess) return cuda_fail(e, "broadcast launch");
@@ -241,7 +243,9 @@ nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
   if (W_g) {
     LinearProblem prob = {m, W_g, b_g, s_in, s_out};
-    e = launch_linear(dtype, dtype == NT_F32, &prob, 1, part->T, C_s, C_z, s);
+    e = linear_tc_supported(dtype, part->T, C_s, C_z)
+            ? launch_linear_tc(0, &prob, 1, part->T, C_s, C_z, status_word(), s)
+            : launch_linear(dtype, dtype == NT_F32, &prob, 1, part->T, C_s, C_z, s);
     if (e != cudaSuccess) return cuda_fail(e, "g projection launch");
   }
   return NT_OK;

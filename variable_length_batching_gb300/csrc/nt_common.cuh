@@ -98,6 +98,12 @@ cudaError_t launch_linear(int in_dtype /*nt_dtype of X, W, R*/, int out_f32 /*Y 
                           const LinearProblem* probs, int nprob, int64_t M, int N, int K,
                           cudaStream_t s);
 
+// Same problem on the tcgen05 tensor cores: bf16 X and W, N % 128 == 0,
+// K % 64 == 0; Y fp32 (out_f32) or bf16.
+bool linear_tc_supported(int in_dtype, int64_t M, int N, int K);
+cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob, int64_t M, int N, int K,
+                             unsigned int* status, cudaStream_t s);
+
 cudaError_t launch_broadcast(nt_dtype dt, const float* u, const float* v, const nt_partition* p,
                              int C_z, void* z, cudaStream_t s);
 
