@@ -100,43 +100,68 @@ def attn_work(seqlens, H, d, es=2):
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples, each stamped on arrival.
+
+    Started before the warm-up; ``mark(start, end)`` is given the timed
+    region's host clock (perf_counter) bounds, and the summary keeps only the
+    samples that arrived inside it."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.out = None
+        self.samples = []          # (perf_counter at arrival, line)
+        self.window = None
+        self.thread = None
+        self.first = None
+
+    def _reader(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.samples.append((time.perf_counter(), ln.strip()))
+                if self.first is not None:
+                    self.first.set()
 
     def __enter__(self):
+        import threading
         try:
-            self.out = open(os.devnull, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.first = threading.Event()
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+        self.first.wait(timeout=10.0)       # sampling is running before any timed work
         return self
 
+    def mark(self, start, end):
+        self.window = (start, end)
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
-        if self.out:
-            self.out.close()
+                self.proc.wait()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
 
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in getattr(self, "lines", []):
+        lo, hi = self.window if self.window else (-float("inf"), float("inf"))
+        for t, ln in list(self.samples):
+            if not (lo <= t <= hi):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -149,9 +174,10 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "period_ms": self.PERIOD_MS}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "period_ms": self.PERIOD_MS}
 
 
 # ----------------------------------------------------------------------------
@@ -252,7 +278,9 @@ def run_gpu(args, rank, world, local_rank):
             step(ev)
             evs.append(ev)
         torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        wall = t1 - t0
+        clk.mark(t0, t1)
     if world > 1:
         dist.barrier()
     nt.nt_device_status(stream)
@@ -292,8 +320,8 @@ def run_gpu(args, rank, world, local_rank):
         "attention": kstat("attention", aw["bytes"], aw["flops"], "tensor"),
         "partition": {"ms": ms["partition"], "note": "scan + row splits + one totals readback"},
     }
-    block_names = ("broadcast", "transition", "reduce")
-    dom = max(block_names, key=lambda n: ms[n])
+    # the kernel with the largest share of the step's device time
+    dom = max(("broadcast", "transition", "reduce", "attention"), key=lambda n: ms[n])
     roof = dict(kernels[dom])
     roof.pop("ms")
     roof["kernel"] = dom
