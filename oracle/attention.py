@@ -13,8 +13,14 @@ Source: "Variable-length attention and data packing":
 "DanLing NestedTensor", section 3.3 "Attention through packed blocks": the
 output adopts the query structure (token-major, static head and feature axes).
 
-Readings: non-causal; scale passed in (d^-1/2 by default); the log-sum-exp is
-natural-log, lse[h, t] = log sum_k exp(scale * q_t . k_k) over t's segment.
+Readings: non-causal by default; scale passed in (d^-1/2 by default); the
+log-sum-exp is natural-log, lse[h, t] = log sum_k exp(scale * q_t . k_k) over
+t's segment.  Cross-attention ("DanLing NestedTensor" section 3.3: the output
+adopts the query structure, query and key lengths may differ) takes separate
+query and key offsets.  Causal masking ([VA]'s template passes causal=True)
+is aligned to the bottom-right corner when the lengths differ: query i of a
+segment with n_q queries and n_k keys sees keys j <= i + (n_k - n_q); a query
+that sees no key returns zeros with lse = -inf.
 """
 from __future__ import annotations
 
@@ -29,37 +35,49 @@ def _softmax_rows(S: np.ndarray) -> np.ndarray:
     return E / E.sum(axis=-1, keepdims=True)
 
 
-def segment_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
-    """Dense attention of one segment: q, k, v are (n, H, d).  Returns O
-    (n, H, d) and lse (H, n)."""
-    n, H, d = q.shape
-    O = np.zeros((n, H, v.shape[2]))
-    lse = np.zeros((H, n))
+def segment_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool = False):
+    """Dense attention of one segment: q is (n_q, H, d), k and v (n_k, H, d).
+    Returns O (n_q, H, d) and lse (H, n_q)."""
+    nq, H, d = q.shape
+    nk = k.shape[0]
+    O = np.zeros((nq, H, v.shape[2]))
+    lse = np.full((H, nq), -np.inf)
+    allowed = np.ones((nq, nk), dtype=bool)
+    if causal:
+        allowed = np.arange(nk)[None, :] <= np.arange(nq)[:, None] + (nk - nq)
     for h in range(H):
-        S = (q[:, h, :] @ k[:, h, :].T) * scale            # (n, n) explicit scores
-        A = _softmax_rows(S)
-        O[:, h, :] = A @ v[:, h, :]
-        mx = S.max(axis=1)
-        lse[h] = mx + np.log(np.exp(S - mx[:, None]).sum(axis=1))
+        S = (q[:, h, :] @ k[:, h, :].T) * scale            # (n_q, n_k) explicit scores
+        for i in range(nq):
+            if not allowed[i].any():
+                continue                                     # no key: zeros, lse = -inf
+            s = S[i, allowed[i]]
+            mx = s.max()
+            e = np.exp(s - mx)
+            O[i, h, :] = (e / e.sum()) @ v[allowed[i], h, :]
+            lse[h, i] = mx + np.log(e.sum())
     return O, lse
 
 
 def varlen_attention(q, k, v, cu_seqlens: Sequence[int], scale: Optional[float] = None,
-                     segments: Optional[Sequence[int]] = None) -> Tuple[np.ndarray, np.ndarray]:
-    """Attention restricted to each [cu[b], cu[b+1]) segment, one segment at a
-    time.  ``segments`` limits the work to the listed segment indices (the
-    other rows of O and lse stay zero)."""
+                     segments: Optional[Sequence[int]] = None, causal: bool = False,
+                     cu_seqlens_k: Optional[Sequence[int]] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Attention restricted to each segment, one segment at a time: queries
+    [cu[b], cu[b+1]) against keys [cu_k[b], cu_k[b+1]) (cu_k = cu for
+    self-attention).  ``segments`` limits the work to the listed segment
+    indices (the other rows of O and lse stay zero)."""
     T, H, d = q.shape
     if scale is None:
         scale = 1.0 / np.sqrt(d)
+    cu_k = cu_seqlens if cu_seqlens_k is None else cu_seqlens_k
     O = np.zeros((T, H, v.shape[2]))
     lse = np.zeros((H, T))
     B = len(cu_seqlens) - 1
     for b in (range(B) if segments is None else segments):
         lo, hi = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        klo, khi = int(cu_k[b]), int(cu_k[b + 1])
         if hi == lo:
             continue
-        O[lo:hi], lse[:, lo:hi] = segment_attention(q[lo:hi], k[lo:hi], v[lo:hi], scale)
+        O[lo:hi], lse[:, lo:hi] = segment_attention(q[lo:hi], k[klo:khi], v[klo:khi], scale, causal)
     return O, lse
 
 
@@ -80,6 +98,21 @@ def masked_full_attention(q, k, v, seg_ids: Sequence[int], scale: Optional[float
         A_all[h] = A
         O[:, h, :] = A @ v[:, h, :]
     return O, A_all
+
+
+def masked_full_attention_causal(q, k, v, seg_ids: Sequence[int], scale: Optional[float] = None):
+    """Full T x T attention with the block-diagonal mask and, within a block,
+    keys after the query masked too (self-attention, equal lengths)."""
+    T, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    seg = np.asarray(seg_ids)
+    allowed = (seg[:, None] == seg[None, :]) & (np.arange(T)[None, :] <= np.arange(T)[:, None])
+    O = np.zeros((T, H, v.shape[2]))
+    for h in range(H):
+        S = (q[:, h, :] @ k[:, h, :].T) * scale
+        O[:, h, :] = _softmax_rows(np.where(allowed, S, -np.inf)) @ v[:, h, :]
+    return O
 
 
 def attention_flops(seqlens: Sequence[int], H: int, d: int) -> int:

@@ -285,3 +285,49 @@ def pin_attention_special_cases(varlen_attention, rng):
     O2, _ = varlen_attention(q2, k2, v2, cu)
     assert np.array_equal(O2[:1], O[:1]) and np.array_equal(O2[5:], O[5:])
     assert not np.allclose(O2[1:5], O[1:5])
+
+
+def pin_attention_causal_sdpa(varlen_attention, rng):
+    """Causal self-attention of one segment is torch's SDPA with is_causal."""
+    n, H, d = 11, 2, 8
+    q, k, v = (rng.standard_normal((n, H, d)) for _ in range(3))
+    O, _ = varlen_attention(q, k, v, [0, n], causal=True)
+    tq, tk, tv = (torch.from_numpy(x).permute(1, 0, 2) for x in (q, k, v))
+    ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True).permute(1, 0, 2).numpy()
+    assert np.allclose(O, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_attention_cross_sdpa(varlen_attention, rng):
+    """Cross-attention, query and key lengths differ: each segment is SDPA of
+    its queries against its own keys (non-causal), and with the causal flag the
+    mask is torch.ones(n_q, n_k).tril(n_k - n_q) (bottom-right alignment)."""
+    cu_q, cu_k = [0, 3, 9, 9, 13], [0, 7, 10, 12, 20]
+    H, d = 2, 5
+    q = rng.standard_normal((cu_q[-1], H, d))
+    k, v = (rng.standard_normal((cu_k[-1], H, d)) for _ in range(2))
+    for causal in (False, True):
+        O, lse = varlen_attention(q, k, v, cu_q, causal=causal, cu_seqlens_k=cu_k)
+        for b in range(len(cu_q) - 1):
+            ql, qh, kl, kh = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+            if qh == ql:
+                continue
+            tq = torch.from_numpy(q[ql:qh]).permute(1, 0, 2)
+            tk = torch.from_numpy(k[kl:kh]).permute(1, 0, 2)
+            tv = torch.from_numpy(v[kl:kh]).permute(1, 0, 2)
+            mask = None
+            if causal:
+                mask = torch.ones(qh - ql, kh - kl, dtype=torch.bool).tril(kh - kl - (qh - ql))
+            ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask).permute(1, 0, 2).numpy()
+            assert np.allclose(O[ql:qh], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_attention_causal_masked(varlen_attention, masked_full_attention_causal, rng):
+    """Per-segment causal attention equals the full T x T masked form."""
+    cu = [0, 4, 5, 12]
+    seg = np.repeat(np.arange(3), np.diff(cu))
+    q, k, v = (rng.standard_normal((12, 2, 4)) for _ in range(3))
+    O1, _ = varlen_attention(q, k, v, cu, causal=True)
+    assert np.allclose(O1, masked_full_attention_causal(q, k, v, seg), rtol=1e-12, atol=1e-12)
+    # the first query of every segment sees only its own key: O = v
+    for b in range(3):
+        assert np.allclose(O1[cu[b]], v[cu[b]], rtol=1e-14, atol=1e-14)

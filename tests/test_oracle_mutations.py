@@ -180,3 +180,58 @@ def test_attention_boundary_caught():
 
 def test_masked_without_mask_caught():
     _fails(pins.pin_attention_masked_core_math, masked_leaky, rng(14))
+
+
+def _segment_attention_mask(allow_fn):
+    """A copy of the per-segment attention with a different causal mask."""
+    def seg_attn(q, k, v, scale, causal=False):
+        nq, H, _ = q.shape
+        nk = k.shape[0]
+        allowed = allow_fn(nq, nk) if causal else np.ones((nq, nk), dtype=bool)
+        O = np.zeros((nq, H, v.shape[2]))
+        lse = np.full((H, nq), -np.inf)
+        for h in range(H):
+            S = (q[:, h, :] @ k[:, h, :].T) * scale
+            for i in range(nq):
+                if allowed[i].any():
+                    s = S[i, allowed[i]]
+                    e = np.exp(s - s.max())
+                    O[i, h, :] = (e / e.sum()) @ v[allowed[i], h, :]
+                    lse[h, i] = s.max() + np.log(e.sum())
+        return O, lse
+    return seg_attn
+
+
+def _with_segment(seg_attn):
+    def attn(q, k, v, cu, scale=None, segments=None, causal=False, cu_seqlens_k=None):
+        orig = oattn.segment_attention
+        oattn.segment_attention = seg_attn
+        try:
+            return oattn.varlen_attention(q, k, v, cu, scale, segments, causal, cu_seqlens_k)
+        finally:
+            oattn.segment_attention = orig
+    return attn
+
+
+strict_causal = _with_segment(_segment_attention_mask(
+    lambda nq, nk: np.arange(nk)[None, :] < np.arange(nq)[:, None] + (nk - nq)))
+top_left_causal = _with_segment(_segment_attention_mask(
+    lambda nq, nk: np.arange(nk)[None, :] <= np.arange(nq)[:, None]))
+
+
+def test_causal_strict_mask_caught():
+    _fails(pins.pin_attention_causal_sdpa, strict_causal, rng(17))
+    _fails(pins.pin_attention_causal_masked, strict_causal, oattn.masked_full_attention_causal, rng(19))
+
+
+def test_causal_top_left_alignment_caught():
+    _fails(pins.pin_attention_cross_sdpa, top_left_causal, rng(18))
+
+
+def test_cross_uses_query_offsets_for_keys_caught():
+    def same_cu(q, k, v, cu, scale=None, segments=None, causal=False, cu_seqlens_k=None):
+        T = q.shape[0]
+        return oattn.varlen_attention(q, k[:T] if k.shape[0] >= T else np.resize(k, q.shape),
+                                      v[:T] if v.shape[0] >= T else np.resize(v, q.shape),
+                                      cu, scale, segments, causal, None)
+    _fails(pins.pin_attention_cross_sdpa, same_cu, rng(18))

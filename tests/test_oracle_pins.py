@@ -176,3 +176,15 @@ def test_attention_flops_config():
     assert len(lens) == 237 and int(lens.sum()) == 65536
     assert int((lens.astype(np.int64) ** 2).sum()) == 23342596
     assert oattn.attention_flops(lens, 12, 64) == 4 * 23342596 * 12 * 64
+
+
+def test_attention_causal_sdpa():
+    pins.pin_attention_causal_sdpa(oattn.varlen_attention, rng(17))
+
+
+def test_attention_cross_sdpa():
+    pins.pin_attention_cross_sdpa(oattn.varlen_attention, rng(18))
+
+
+def test_attention_causal_masked():
+    pins.pin_attention_causal_masked(oattn.varlen_attention, oattn.masked_full_attention_causal, rng(19))
