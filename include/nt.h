@@ -204,14 +204,49 @@ nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z
  *   q, k, v, o    [T, H, d] token-major, contiguous.
  *   d_cu_seqlens  [B+1] int32, non-decreasing, cu[0] = 0, cu[B] = T.
  *   max_len       max segment length (>= every cu[i+1] - cu[i]).
- *   scale         score scale (d^-1/2 for the usual attention).
+ *   scale         score scale, finite and > 0 (d^-1/2 for the usual
+ *                 attention); anything else is NT_ERR_INVALID.
  *   lse           [H, T] fp32 natural-log log-sum-exp, or NULL.
  * bf16 with d = 64 runs on the tcgen05 tensor cores; NT_F32 and other head
- * widths (32, 64, 128) run on fp32 CUDA cores.  Asynchronous.
+ * widths (32, 64, 128) run on fp32 CUDA cores.  Asynchronous.  Identical to
+ * nt_varlen_attn_qk with d_cu_seqlens_k = d_cu_seqlens, T_k = T, causal = 0.
  */
 nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const void* v,
                          const int32_t* d_cu_seqlens, int32_t B, int64_t T, int32_t max_len,
                          int32_t H, int32_t d, float scale, void* o, float* lse, void* stream);
+
+/*
+ * nt_varlen_attn_qk -- varlen attention with separate query and key
+ * segments, and an optional causal mask.  Query segment b,
+ * [cu_q[b], cu_q[b+1]), attends to key segment b, [cu_k[b], cu_k[b+1]); the
+ * output adopts the query structure ([DL] section 3.3 "Attention through
+ * packed blocks": attention over packed blocks, query and key lengths may
+ * differ).  With causal = 1, query i of a segment with n_q queries and n_k
+ * keys sees the keys j <= i + (n_k - n_q) (the diagonal aligned to the
+ * bottom-right corner; for self-attention, j <= i).  [VA] "How to use it":
+ * the varlen call of the page's template sets the causal flag.  A query that sees no key
+ * (n_k = 0, or causal with i + n_k - n_q < 0) gets O = 0 and lse = -inf.
+ *   q, o          [T_q, H, d] token-major, contiguous.
+ *   k, v          [T_k, H, d] token-major, contiguous (may be NULL if T_k = 0).
+ *   d_cu_seqlens_q, d_cu_seqlens_k
+ *                 [B+1] int32 each, non-decreasing, starting at 0, ending at
+ *                 T_q and T_k.  Offsets inconsistent with T_q / T_k are caught
+ *                 on the device: nothing is written for those segments and
+ *                 nt_device_status reports NT_ERR_DEVICE_CHECK.
+ *   max_len_q     max query segment length (>= every cu_q[b+1] - cu_q[b]).
+ *   scale         finite and > 0.
+ *   causal        0 or 1.
+ *   lse           [H, T_q] fp32 natural-log log-sum-exp, or NULL.
+ * Host errors: NT_ERR_INVALID (bad sizes, flags, scale, NULL or misaligned
+ * pointers), NT_ERR_OVERFLOW (T_q or T_k beyond int32), NT_ERR_UNSUPPORTED
+ * (head width).  bf16 with d = 64 and T_k > 0 runs on the tensor cores;
+ * the rest on CUDA cores.  Asynchronous on `stream`; buffers stay owned by
+ * the caller.
+ */
+nt_status nt_varlen_attn_qk(nt_dtype dtype, const void* q, const void* k, const void* v,
+                            const int32_t* d_cu_seqlens_q, const int32_t* d_cu_seqlens_k, int32_t B,
+                            int64_t T_q, int64_t T_k, int32_t max_len_q, int32_t H, int32_t d, float scale,
+                            int32_t causal, void* o, float* lse, void* stream);
 
 /* Synchronises `stream`, then reads and clears the device status word set by
  * device-side checks (bounded waits that ran out: NT_ERR_TIMEOUT; failed data

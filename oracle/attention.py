@@ -17,8 +17,9 @@ Readings: non-causal by default; scale passed in (d^-1/2 by default); the
 log-sum-exp is natural-log, lse[h, t] = log sum_k exp(scale * q_t . k_k) over
 t's segment.  Cross-attention ("DanLing NestedTensor" section 3.3: the output
 adopts the query structure, query and key lengths may differ) takes separate
-query and key offsets.  Causal masking ([VA]'s template passes causal=True)
-is aligned to the bottom-right corner when the lengths differ: query i of a
+query and key offsets.  Causal masking ("Variable-length attention and data
+packing", "How to use it": the varlen call of its template sets the causal
+flag) is aligned to the bottom-right corner when the lengths differ: query i of a
 segment with n_q queries and n_k keys sees keys j <= i + (n_k - n_q); a query
 that sees no key returns zeros with lse = -inf.
 """

@@ -27,7 +27,8 @@ def L():
 def test_header_declares_the_calls():
     names = declared_functions()
     for n in ("nt_partition_build", "nt_partition_rows", "nt_pair_broadcast", "nt_pair_transition",
-              "nt_pair_reduce", "nt_varlen_attn", "nt_device_status", "nt_status_str", "nt_last_error"):
+              "nt_pair_reduce", "nt_varlen_attn", "nt_varlen_attn_qk", "nt_device_status", "nt_status_str",
+              "nt_last_error"):
         assert n in names
 
 
@@ -96,4 +97,14 @@ def test_host_side_rejections(L):
     assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 1 << 31, 64, 1, 64, 0.125, fake, None, None) == 3
     # an empty stream is a no-op success
     assert lib.nt_varlen_attn(1, None, None, None, None, 0, 0, 0, 12, 64, 0.125, None, None, None) == 0
+    # scale must be finite and > 0
+    for bad in (0.0, -0.125, float("inf"), float("nan")):
+        assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 64, 64, 1, 64, bad, fake, None, None) == 1
+    # qk form: causal flag 0/1 only; T_k beyond int32; key pointers needed when T_k > 0
+    qk = lib.nt_varlen_attn_qk
+    assert qk(1, fake, fake, fake, fake, fake, 1, 64, 64, 64, 1, 64, 0.125, 2, fake, None, None) == 1
+    assert qk(1, fake, fake, fake, fake, fake, 1, 64, 1 << 31, 64, 1, 64, 0.125, 0, fake, None, None) == 3
+    assert qk(1, fake, None, None, fake, fake, 1, 64, 32, 64, 1, 64, 0.125, 0, fake, None, None) == 1
+    assert qk(1, fake, fake, fake, fake, fake, 1, -1, 32, 64, 1, 64, 0.125, 0, fake, None, None) == 1
+    assert qk(1, None, None, None, None, None, 0, 0, 0, 0, 4, 64, 0.125, 1, None, None, None) == 0
     assert lib.nt_last_error()  # a detail string was recorded

@@ -18,6 +18,14 @@
 // on those tiles only.  A quarter of each full tile's exponentials run on the
 // FMA pipe (exp2_fma), the rest on the SFU.
 // Two CTAs fit on an SM (96 KB shared memory, 256 TMEM columns each).
+//
+// Cross-attention takes the keys of query segment b from [cu_k[b], cu_k[b+1])
+// ("DanLing NestedTensor" section 3.3: the output adopts the query
+// structure).  The causal variant (a template flag) masks key j of a segment
+// for query i when j > i + (n_k - n_q), the diagonal aligned to the segment's
+// bottom-right corner: each CTA loads only the key tiles its last query row
+// can see, tiles wholly under every row's diagonal run the unmasked path,
+// and a query that sees no key gets zeros with lse = -inf.
 #include "tc_ptx.cuh"
 
 namespace nt {
@@ -52,33 +60,53 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
+template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 2)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ cu, int B, int64_t T,
-               int H, int QT, float scale_log2, bf16* __restrict__ o, float* __restrict__ lse,
-               unsigned int* status) {
+               const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ cu,
+               const int32_t* __restrict__ cu_k, int B, int64_t T, int64_t T_k, int H, int QT,
+               float scale_log2, bf16* __restrict__ o, float* __restrict__ lse, unsigned int* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // (segment, query tile, head) of this CTA; heads vary fastest
   const int64_t item = blockIdx.x;
   const int h = (int)(item % H);
   const int64_t rest = item / H;
-  const int qi = (int)(rest % QT);
+  // causal: the longest query tiles (largest qi) are launched first
+  const int qi = kCausal ? QT - 1 - (int)(rest % QT) : (int)(rest % QT);
   const int b = (int)(rest / QT);
   if (b >= B) return;
   const int lo = cu[b], hi = cu[b + 1];
-  if (lo < 0 || hi < lo || hi > T) {
+  const int klo = cu_k[b], khi = cu_k[b + 1];
+  if (lo < 0 || hi < lo || hi > T || klo < 0 || khi < klo || khi > T_k) {
     if (threadIdx.x == 0 && qi == 0 && h == 0) flag_device(status, kDevCheck);
     return;
   }
-  const int n = hi - lo;
+  const int n = hi - lo;                      // queries of the segment
+  const int n_k = khi - klo;                  // keys of the segment
   if (qi == QT - 1 && n > QT * kBQ && threadIdx.x == 0 && h == 0) flag_device(status, kDevCheck);
   const int q0 = lo + qi * kBQ;
   if (q0 >= hi) return;                       // CTA-uniform: nothing allocated yet
+  const int diag = n_k - n;                   // causal: query i sees keys j <= i + diag
+  int nk = (n_k + kBK - 1) / kBK;
+  if (kCausal) {
+    const int last = min(qi * kBQ + kBQ - 1, n - 1) + diag;   // furthest key any row here sees
+    nk = last < 0 ? 0 : min(nk, last / kBK + 1);
+  }
+  if (nk == 0) {
+    // no row of this tile sees a key: zeros and lse = -inf, no pipeline
+    const int rows = min(kBQ, hi - q0);
+    for (int e = threadIdx.x; e < rows * (kD / 8); e += kThreads) {
+      const int rr = e / (kD / 8), u = e % (kD / 8);
+      *reinterpret_cast<uint4*>(o + ((int64_t)(q0 + rr) * H + h) * kD + 8 * u) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (lse)
+      for (int rr = threadIdx.x; rr < rows; rr += kThreads) lse[(int64_t)h * T + q0 + rr] = -INFINITY;
+    return;
+  }
   if (smem_u32(smem_raw) & 1023) {            // the swizzled tiles need 1024-byte alignment
     if (threadIdx.x == 0) flag_device(status, kDevCheck);
     return;
   }
-  const int nk = (n + kBK - 1) / kBK;
 
   uint8_t* smem = smem_raw;
   uint8_t* sQ = smem + kOffQ;
@@ -120,11 +148,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int st = j % kStages, rd = j / kStages;
         if (!mbar_wait(&bar.k_empty[st], (rd & 1) ^ 1, abort_flag, status)) break;
         mbar_arrive_expect_tx(&bar.k_full[st], kKVBytes);
-        tma_load_3d(sK + st * kKVBytes, &tm_k, &bar.k_full[st], 0, h, lo + j * kBK);
+        tma_load_3d(sK + st * kKVBytes, &tm_k, &bar.k_full[st], 0, h, klo + j * kBK);
         k_issued = j + 1;
         if (!mbar_wait(&bar.v_empty[st], (rd & 1) ^ 1, abort_flag, status)) break;
         mbar_arrive_expect_tx(&bar.v_full[st], kKVBytes);
-        tma_load_3d(sV + st * kKVBytes, &tm_v, &bar.v_full[st], 0, h, lo + j * kBK);
+        tma_load_3d(sV + st * kKVBytes, &tm_v, &bar.v_full[st], 0, h, klo + j * kBK);
         v_issued = j + 1;
       }
       // drain the copies this thread issued
@@ -183,8 +211,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (!(ok = mbar_wait_warp(&bar.s_full[sb], (j >> 1) & 1, abort_flag, status))) break;
       tc_fence_after();
       __syncwarp();
-      const int kvalid = min(kBK, n - j * kBK);   // keys of this tile inside the segment
-      const bool full = kvalid == kBK;
+      // keys of this tile this row sees: a prefix [0, cnt) of the tile
+      int cnt = min(kBK, n_k - j * kBK);
+      if (kCausal) cnt = max(0, min(cnt, qi * kBQ + r + diag - j * kBK + 1));
+      const bool full = kCausal ? __all_sync(0xffffffffu, cnt == kBK) : cnt == kBK;
       const uint32_t s_addr = tmem + lane_addr + kColS + 64 * sb;
       // pass 1: row maximum of the raw scores (scale > 0)
       float mx = -INFINITY;
@@ -199,7 +229,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (32 * g + c < kvalid) mx = fmaxf(mx, sv[c]);
+            if (32 * g + c < cnt) mx = fmaxf(mx, sv[c]);
         }
       }
       // lazy running max: move it only when it grows by more than 8 (log2 units)
@@ -252,8 +282,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         } else {
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float p0 = (32 * g + c < kvalid) ? ex2_approx(fmaf(sv[c], scale_log2, -m)) : 0.f;
-            const float p1 = (32 * g + c + 1 < kvalid) ? ex2_approx(fmaf(sv[c + 1], scale_log2, -m)) : 0.f;
+            const float p0 = (32 * g + c < cnt) ? ex2_approx(fmaf(sv[c], scale_log2, -m)) : 0.f;
+            const float p1 = (32 * g + c + 1 < cnt) ? ex2_approx(fmaf(sv[c + 1], scale_log2, -m)) : 0.f;
             rs += p0 + p1;
             pk[c / 2] = pack_bf16x2(p0, p1);
           }
@@ -272,7 +302,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc_fence_after();
       __syncwarp();
       const int t = q0 + r;
-      const float inv = 1.0f / l;
+      const float inv = l > 0.f ? 1.0f / l : 0.f;   // causal rows that see no key: zeros
 #pragma unroll 1
       for (int g = 0; g < 2; ++g) {
         float ov[32];
@@ -291,7 +321,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
       }
-      if (t < hi && lse) lse[(int64_t)h * T + t] = (m + log2f(l)) * 0.69314718055994531f;
+      if (t < hi && lse) lse[(int64_t)h * T + t] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -317,21 +347,22 @@ bool make_map_thd(CUtensorMap* map, const void* ptr, int64_t T, int H, uint32_t 
 
 bool attn_tc_supported(nt_dtype dt, int d) { return dt == NT_BF16 && d == kD; }
 
-cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B, int64_t T,
-                           int32_t max_len, int H, int d, float scale, void* o, float* lse,
-                           unsigned int* status, cudaStream_t s) {
-  if (T == 0 || B == 0) return cudaSuccess;
+cudaError_t launch_attn_tc(const AttnProblem& p, unsigned int* status, cudaStream_t s) {
+  if (p.T_q == 0 || p.B == 0) return cudaSuccess;
+  if (p.T_k == 0) return cudaErrorInvalidValue;   // no key tensor to map; the caller routes this case
   CUtensorMap mq, mk, mv;
-  if (!make_map_thd(&mq, q, T, H, kBQ) || !make_map_thd(&mk, k, T, H, kBK) || !make_map_thd(&mv, v, T, H, kBK))
+  if (!make_map_thd(&mq, p.q, p.T_q, p.H, kBQ) || !make_map_thd(&mk, p.k, p.T_k, p.H, kBK) ||
+      !make_map_thd(&mv, p.v, p.T_k, p.H, kBK))
     return cudaErrorInvalidValue;
-  const int QT = max(1, (max_len + kBQ - 1) / kBQ);
-  const int64_t items = (int64_t)B * QT * H;
+  const int QT = max(1, (p.max_len_q + kBQ - 1) / kBQ);
+  const int64_t items = (int64_t)p.B * QT * p.H;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  auto kern = p.causal ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const float scale_log2 = scale * 1.4426950408889634f;
-  attn_tc_kernel<<<(unsigned)items, kThreads, kSmemBytes, s>>>(mq, mk, mv, cu, B, T, H, QT, scale_log2, (bf16*)o,
-                                                               lse, status);
+  const float scale_log2 = p.scale * 1.4426950408889634f;
+  kern<<<(unsigned)items, kThreads, kSmemBytes, s>>>(mq, mk, mv, p.cu_q, p.cu_k, p.B, p.T_q, p.T_k, p.H, QT,
+                                                     scale_log2, (bf16*)p.o, p.lse, status);
   return cudaGetLastError();
 }
 

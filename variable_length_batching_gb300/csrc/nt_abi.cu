@@ -5,6 +5,7 @@
 // strategy": segmented calls over the batch).
 #include <cstdarg>
 #include <cstdio>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -251,30 +252,45 @@ nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z
   return NT_OK;
 }
 
-nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const void* v,
-                         const int32_t* d_cu_seqlens, int32_t B, int64_t T, int32_t max_len,
-                         int32_t H, int32_t d, float scale, void* o, float* lse, void* stream) {
+nt_status nt_varlen_attn_qk(nt_dtype dtype, const void* q, const void* k, const void* v,
+                            const int32_t* d_cu_seqlens_q, const int32_t* d_cu_seqlens_k, int32_t B,
+                            int64_t T_q, int64_t T_k, int32_t max_len_q, int32_t H, int32_t d, float scale,
+                            int32_t causal, void* o, float* lse, void* stream) {
   if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
-  if (B < 0 || T < 0 || H <= 0 || d <= 0 || max_len < 0)
-    return fail(NT_ERR_INVALID, "bad sizes B=%d T=%lld H=%d d=%d max_len=%d", B, (long long)T, H, d,
-                max_len);
-  if (T > 0x7fffffffLL) return fail(NT_ERR_OVERFLOW, "T = %lld does not fit int32", (long long)T);
-  if (T > 0 && B == 0) return fail(NT_ERR_INVALID, "T > 0 with no segments");
-  if (T > 0 && (!q || !k || !v || !o || !d_cu_seqlens)) return fail(NT_ERR_INVALID, "NULL pointer");
+  if (B < 0 || T_q < 0 || T_k < 0 || H <= 0 || d <= 0 || max_len_q < 0)
+    return fail(NT_ERR_INVALID, "bad sizes B=%d T_q=%lld T_k=%lld H=%d d=%d max_len_q=%d", B, (long long)T_q,
+                (long long)T_k, H, d, max_len_q);
+  if (!(scale > 0.f) || std::isinf(scale)) return fail(NT_ERR_INVALID, "scale must be finite and > 0");
+  if (causal != 0 && causal != 1) return fail(NT_ERR_INVALID, "causal must be 0 or 1");
+  if (T_q > 0x7fffffffLL || T_k > 0x7fffffffLL)
+    return fail(NT_ERR_OVERFLOW, "T_q = %lld, T_k = %lld: token counts must fit int32", (long long)T_q,
+                (long long)T_k);
+  if (T_q > 0 && B == 0) return fail(NT_ERR_INVALID, "T_q > 0 with no segments");
+  if (T_q > 0 && (!q || !o || !d_cu_seqlens_q || !d_cu_seqlens_k)) return fail(NT_ERR_INVALID, "NULL pointer");
+  if (T_q > 0 && T_k > 0 && (!k || !v)) return fail(NT_ERR_INVALID, "NULL key or value pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
-  if (T == 0) return NT_OK;
+  if (T_q == 0) return NT_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const AttnProblem prob = {q, k, v, d_cu_seqlens_q, d_cu_seqlens_k, B, T_q, T_k, max_len_q,
+                            H, d, scale, causal != 0, o, lse};
   cudaError_t e;
-  if (attn_tc_supported(dtype, d)) {
-    e = launch_attn_tc(q, k, v, d_cu_seqlens, B, T, max_len, H, d, scale, o, lse, status_word(), s);
+  if (attn_tc_supported(dtype, d) && T_k > 0) {
+    e = launch_attn_tc(prob, status_word(), s);
     if (e != cudaSuccess) return cuda_fail(e, "varlen attention (tensor core) launch");
     return NT_OK;
   }
   if (!attn_simt_supported(d)) return fail(NT_ERR_UNSUPPORTED, "head width d=%d", d);
-  e = launch_attn_simt(dtype, q, k, v, d_cu_seqlens, B, T, H, d, scale, o, lse, status_word(), s);
+  e = launch_attn_simt(dtype, prob, status_word(), s);
   if (e != cudaSuccess) return cuda_fail(e, "varlen attention launch");
   return NT_OK;
+}
+
+nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const void* v,
+                         const int32_t* d_cu_seqlens, int32_t B, int64_t T, int32_t max_len,
+                         int32_t H, int32_t d, float scale, void* o, float* lse, void* stream) {
+  return nt_varlen_attn_qk(dtype, q, k, v, d_cu_seqlens, d_cu_seqlens, B, T, T, max_len, H, d, scale, 0, o,
+                           lse, stream);
 }
 
 nt_status nt_device_status(void* stream) {

@@ -120,13 +120,28 @@ cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C
 cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m,
                           cudaStream_t s);
 
+// One varlen attention problem: queries [cu_q[b], cu_q[b+1]) attend to keys
+// [cu_k[b], cu_k[b+1]) (cu_k == cu_q for self-attention); causal masks key j
+// of a segment for query i when j > i + (n_k - n_q).
+struct AttnProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int32_t B;
+  int64_t T_q, T_k;
+  int32_t max_len_q;
+  int H, d;
+  float scale;
+  bool causal;
+  void* o;
+  float* lse;
+};
+
 bool attn_simt_supported(int d);
-cudaError_t launch_attn_simt(nt_dtype dt, const void* q, const void* k, const void* v,
-                             const int32_t* cu, int32_t B, int64_t T, int H, int d, float scale,
-                             void* o, float* lse, unsigned int* status, cudaStream_t s);
+cudaError_t launch_attn_simt(nt_dtype dt, const AttnProblem& p, unsigned int* status, cudaStream_t s);
 bool attn_tc_supported(nt_dtype dt, int d);
-cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, const int32_t* cu,
-                           int32_t B, int64_t T, int32_t max_len, int H, int d, float scale,
-                           void* o, float* lse, unsigned int* status, cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnProblem& p, unsigned int* status, cudaStream_t s);
 
 }  // namespace nt

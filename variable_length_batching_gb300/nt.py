@@ -48,6 +48,8 @@ SIGNATURES = {
     "nt_pair_transition": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P]),
     "nt_pair_reduce": (_I32, [_PP, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P]),
     "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P]),
+    "nt_varlen_attn_qk": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _F, _I32,
+                                 _P, _P, _P]),
     "nt_device_status": (_I32, [_P]),
     "nt_status_str": (ctypes.c_char_p, [_I32]),
     "nt_last_error": (ctypes.c_char_p, []),
@@ -251,6 +253,34 @@ def nt_varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
     st = lib().nt_varlen_attn(_dtype(q), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, T, int(max_len),
                               H, d, float(scale), _ptr(out), _ptr(lse), _stream(stream))
     _check(st, "nt_varlen_attn")
+    return out, lse
+
+
+def nt_varlen_attn_qk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                      cu_seqlens_k: torch.Tensor, max_len_q: int, scale: Optional[float] = None,
+                      causal: bool = False, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+    """Queries of segment b attend to keys [cu_k[b], cu_k[b+1]); with
+    ``causal`` the diagonal is aligned to each segment's bottom-right corner."""
+    T_q, H, d = q.shape
+    T_k = k.shape[0]
+    if tuple(k.shape[1:]) != (H, d) or v.shape != k.shape:
+        raise ValueError("k and v must be (T_k, H, d) with q's H and d")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel():
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have B+1 entries each")
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if want_lse and lse is None:
+        lse = torch.empty(H, T_q, dtype=torch.float32, device=q.device)
+    st = lib().nt_varlen_attn_qk(_dtype(q), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                 B, T_q, T_k, int(max_len_q), H, d, float(scale), int(bool(causal)),
+                                 _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "nt_varlen_attn_qk")
     return out, lse
 
 

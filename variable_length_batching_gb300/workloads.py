@@ -234,6 +234,30 @@ def make_attn_inputs(cfg: AttnConfig, seqlens: Optional[Sequence[int]] = None,
     return AttnInputs(cfg, lens, q, k, v)
 
 
+@dataclass
+class CrossAttnInputs:
+    seqlens_q: np.ndarray   # int32 (B,)
+    seqlens_k: np.ndarray   # int32 (B,)
+    q: torch.Tensor         # (T_q, H, d) host, I/O dtype
+    k: torch.Tensor         # (T_k, H, d)
+    v: torch.Tensor
+
+
+def make_cross_attn_inputs(seqlens_q: Sequence[int], seqlens_k: Sequence[int], H: int, d: int,
+                           dtype: str = BF16, seed: int = 0) -> CrossAttnInputs:
+    """Queries and keys with their own per-segment lengths, N(0, 1) entries."""
+    rng = np.random.default_rng(seed)
+    lq = np.asarray(seqlens_q, dtype=np.int32)
+    lk = np.asarray(seqlens_k, dtype=np.int32)
+    if lq.shape != lk.shape:
+        raise ValueError("one key length per query segment")
+    Tq, Tk = int(lq.astype(np.int64).sum()), int(lk.astype(np.int64).sum())
+    q = to_io(rng.standard_normal((Tq, H, d)).astype(np.float32), dtype)
+    k = to_io(rng.standard_normal((Tk, H, d)).astype(np.float32), dtype)
+    v = to_io(rng.standard_normal((Tk, H, d)).astype(np.float32), dtype)
+    return CrossAttnInputs(lq, lk, q, k, v)
+
+
 def io_bits_to_f64(t: torch.Tensor) -> np.ndarray:
     """Exact float64 copy of a host tensor in either I/O dtype."""
     return t.detach().to("cpu").to(torch.float64).numpy()
