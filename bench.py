@@ -9,7 +9,9 @@ One step is one pass of the whole hot path:
 ``value`` is packed pair cells per second of the block (the block's P over
 its device time per step); the attention's TFLOPS ride beside it in
 ``attn``.  L2 is flushed (a 512 MB write) before every timed step, outside
-the timed events.  ``--impl reference`` times the CPU oracle instead.
+the timed events.  The partition build ends with a host readback; a short
+device sleep after it (also outside the events) lets the host queue the
+remaining calls ahead of the device, so each call's interval is device time.  ``--impl reference`` times the CPU oracle instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun every rank runs its own replica (weak scaling).
@@ -37,6 +39,7 @@ import torch  # noqa: E402
 from variable_length_batching_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "packed pair cells/sec per block and varlen attn TFLOPS; % of HBM/tensor roofline"
+HOST_LEAD_CYCLES = 400_000     # ~0.2 ms of device sleep at 2 GHz, outside the timed intervals
 BLOCK_CFG = wl.PAIRFORMER_BF16
 ATTN_CFG = wl.VARLEN_ATTN_BF16
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -90,43 +93,98 @@ def block_work(T, P, C_s, C_z, H_t, es=2):
     }
 
 
-def attn_work(seqlens, H, d, es=2):
+def attn_work(seqlens, H, d, es=2, causal=False):
+    """QK^T and PV over the visible (query, key) pairs: n^2 per segment, or
+    n (n + 1) / 2 under the causal mask; q, k, v read and o written once."""
     n = np.asarray(seqlens, dtype=np.int64)
-    return {"bytes": 4 * int(n.sum()) * H * d * es, "flops": 4 * int((n * n).sum()) * H * d}
+    pairs = int((n * (n + 1) // 2).sum()) if causal else int((n * n).sum())
+    return {"bytes": 4 * int(n.sum()) * H * d * es, "flops": 4 * pairs * H * d}
 
 
 # ----------------------------------------------------------------------------
 # Clock sampling during the timed region
 # ----------------------------------------------------------------------------
 
-class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples, each stamped on arrival.
+_REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                "hw_thermal_slowdown": 0x40}
 
-    Started before the warm-up; ``mark(start, end)`` is given the timed
-    region's host clock (perf_counter) bounds, and the summary keeps only the
-    samples that arrived inside it."""
+
+class _NvmlProbe:
+    """SM clock, max SM clock and clock-event reasons of one GPU read through
+    NVML (the library nvidia-smi reads), for sampling faster than nvidia-smi's
+    loop.  Read-only queries."""
+
+    def __init__(self, index):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        getter = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = getter or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def read(self):
+        c = self.c
+        clk, mx, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(clk)) != 0 or      # 1 = NVML_CLOCK_SM
+                self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, c.byref(mx)) != 0 or
+                self.reasons_fn(self.h, c.byref(rs)) != 0):
+            return None
+        return float(clk.value), float(mx.value), int(rs.value)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+class ClockSampler:
+    """Clock and throttle-reason samples stamped on arrival: nvidia-smi's loop
+    (every 20 ms) and, where libnvidia-ml loads, NVML reads every 2 ms, so that
+    a timed region of a few tens of ms still holds samples.  Started before
+    the warm-up; ``mark(start, end)`` is given the timed region's host clock
+    (perf_counter) bounds, and the summary keeps only samples inside it."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     PERIOD_MS = 20
+    NVML_PERIOD_S = 0.002
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.samples = []          # (perf_counter at arrival, line)
+        self.samples = []          # (perf_counter, source, sm_mhz, max_mhz, set of reasons)
         self.window = None
-        self.thread = None
-        self.first = None
+        self.threads = []
+        self.stop = None
 
-    def _reader(self):
+    def _smi_reader(self, first):
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for ln in self.proc.stdout:
-            if ln.strip():
-                self.samples.append((time.perf_counter(), ln.strip()))
-                if self.first is not None:
-                    self.first.set()
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            rs = {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}
+            self.samples.append((time.perf_counter(), "nvidia-smi", sm, mx, rs))
+            first.set()
+
+    def _nvml_loop(self, probe):
+        while not self.stop.is_set():
+            r = probe.read()
+            if r is not None:
+                rs = {n for n, b in _REASON_BITS.items() if r[2] & b}
+                self.samples.append((time.perf_counter(), "nvml", r[0], r[1], rs))
+            self.stop.wait(self.NVML_PERIOD_S)
+        probe.close()
 
     def __enter__(self):
         import threading
+        self.stop = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
@@ -134,17 +192,27 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-            return self
-        self.first = threading.Event()
-        self.thread = threading.Thread(target=self._reader, daemon=True)
-        self.thread.start()
-        self.first.wait(timeout=10.0)       # sampling is running before any timed work
+        if self.proc is not None:
+            first = threading.Event()
+            t = threading.Thread(target=self._smi_reader, args=(first,), daemon=True)
+            t.start()
+            self.threads.append(t)
+            first.wait(timeout=10.0)        # sampling is running before any timed work
+        try:
+            probe = _NvmlProbe(self.gpu)
+        except (OSError, AttributeError):
+            probe = None
+        if probe is not None:
+            t = threading.Thread(target=self._nvml_loop, args=(probe,), daemon=True)
+            t.start()
+            self.threads.append(t)
         return self
 
     def mark(self, start, end):
         self.window = (start, end)
 
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -152,32 +220,22 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 self.proc.wait()
-            if self.thread is not None:
-                self.thread.join(timeout=5)
+        for t in self.threads:
+            t.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         lo, hi = self.window if self.window else (-float("inf"), float("inf"))
-        for t, ln in list(self.samples):
-            if not (lo <= t <= hi):
-                continue
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
-                    "period_ms": self.PERIOD_MS}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "period_ms": self.PERIOD_MS}
+        inside = [s for s in list(self.samples) if lo <= s[0] <= hi]
+        counts = {}
+        for s in inside:
+            counts[s[1]] = counts.get(s[1], 0) + 1
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": counts}
+        reasons = set()
+        for s in inside:
+            reasons |= s[4]
+        return {"sm_mhz": statistics.median(s[2] for s in inside), "sm_max_mhz": max(s[3] for s in inside),
+                "sm_mhz_min": min(s[2] for s in inside), "reasons": sorted(reasons), "samples": counts}
 
 
 # ----------------------------------------------------------------------------
@@ -243,21 +301,29 @@ def run_gpu(args, rank, world, local_rank):
     names = ("partition", "broadcast", "transition", "reduce", "attention")
 
     def step(ev):
+        # ev[0..1] bracket the partition build (it ends with the host reading
+        # the totals back); ev[2..6] bracket the four device-only calls.
         ev[0].record(stream)
         p = nt.nt_partition_build(lengths_d, stream=stream)
         ev[1].record(stream)
-        nt.nt_pair_broadcast(p, s_d, s_d, w.W_a, w.W_b, z=z_d, workspace=ws_d, stream=stream)
+        # The partition's readback left the stream idle.  A short device
+        # sleep, outside every timed interval, lets the host enqueue the next
+        # calls ahead of the device, so their intervals hold device time and
+        # not host launch latency.
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
         ev[2].record(stream)
+        nt.nt_pair_broadcast(p, s_d, s_d, w.W_a, w.W_b, z=z_d, workspace=ws_d, stream=stream)
+        ev[3].record(stream)
         nt.nt_pair_transition(p, z_d, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2, out=z_d,
                               stream=stream)
-        ev[3].record(stream)
-        nt.nt_pair_reduce(p, z_d, w.W_g, w.b_g, s_in=s_d, m=m_d, s_out=sout_d, stream=stream)
         ev[4].record(stream)
-        nt.nt_varlen_attn(q_d, k_d, v_d, cu_d, max_len, out=o_d, stream=stream)
+        nt.nt_pair_reduce(p, z_d, w.W_g, w.b_g, s_in=s_d, m=m_d, s_out=sout_d, stream=stream)
         ev[5].record(stream)
+        nt.nt_varlen_attn(q_d, k_d, v_d, cu_d, max_len, out=o_d, stream=stream)
+        ev[6].record(stream)
 
     def new_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        return [torch.cuda.Event(enable_timing=True) for _ in range(7)]
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -286,9 +352,12 @@ def run_gpu(args, rank, world, local_rank):
     nt.nt_device_status(stream)
 
     per = {n: [] for n in names}
+    spans = {"partition": (0, 1), "broadcast": (2, 3), "transition": (3, 4), "reduce": (4, 5),
+             "attention": (5, 6)}
     for ev in evs:
-        for i, n in enumerate(names):
-            per[n].append(ev[i].elapsed_time(ev[i + 1]))
+        for n in names:
+            a, b = spans[n]
+            per[n].append(ev[a].elapsed_time(ev[b]))
     ms = {n: float(np.mean(v)) for n, v in per.items()}
     block_ms = ms["partition"] + ms["broadcast"] + ms["transition"] + ms["reduce"]
     step_ms = block_ms + ms["attention"]
@@ -306,12 +375,19 @@ def run_gpu(args, rank, world, local_rank):
 
     def kstat(name, w_bytes, w_flops, bound):
         t = ms[name] * 1e-3
+        spread = {"ms": ms[name], "ms_p10_p50_p90": [float(x) for x in np.percentile(per[name], [10, 50, 90])]}
         if bound == "tensor":
             a = w_flops / t / 1e12
-            return {"bound": "tensor", "achieved": a, "peak": tc, "unit": "TFLOP/s", "frac": a / tc,
-                    "ms": ms[name]}
+            out = {"bound": "tensor", "achieved": a, "peak": tc, "unit": "TFLOP/s", "frac": a / tc}
+            # attainable roofline: min(tensor peak, arithmetic intensity x HBM bandwidth)
+            att = min(tc, w_flops / w_bytes * hbm / 1e3)
+            out.update({"attainable": att, "frac_attainable": a / att})
+            out.update(spread)
+            return out
         a = w_bytes / t / 1e9
-        return {"bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s", "frac": a / hbm, "ms": ms[name]}
+        out = {"bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s", "frac": a / hbm}
+        out.update(spread)
+        return out
 
     kernels = {
         "broadcast": kstat("broadcast", work["broadcast"]["bytes"], 0, "hbm"),
@@ -322,8 +398,7 @@ def run_gpu(args, rank, world, local_rank):
     }
     # the kernel with the largest share of the step's device time
     dom = max(("broadcast", "transition", "reduce", "attention"), key=lambda n: ms[n])
-    roof = dict(kernels[dom])
-    roof.pop("ms")
+    roof = {k: v for k, v in kernels[dom].items() if not k.startswith("ms")}
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} ({'burst copy' if roof['bound'] == 'hbm' else 'cuBLAS bf16 burst'})"
     tr = traffic_record(dom)
@@ -353,7 +428,7 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "block_ms": block_ms_max,
         "attn": {"tflops": attn_tflops, "ms": attn_ms_max, "flops_per_step": aw["flops"],
-                 "roofline": {k: v for k, v in kernels["attention"].items() if k != "ms"}},
+                 "roofline": {k: v for k, v in kernels["attention"].items() if not k.startswith("ms")}},
         "kernels": kernels,
         "roofline": roof,
         "e2e": e2e,
@@ -491,6 +566,127 @@ WORKLOADS = {"pairformer": wl.PAIRFORMER_BF16, "lognormal": wl.LOGNORMAL_BF16,
              "near_uniform": wl.NEAR_UNIFORM_BF16, "stacked4": wl.STACKED4_BF16, "tiny": wl.TINY_FP32}
 
 
+def _timed(fn, flush, reps, stream):
+    """Median, p10 and p90 (ms) of ``reps`` runs of ``fn`` with L2 flushed before each."""
+    ts = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    v = [a.elapsed_time(b) for a, b in ts]
+    return [float(x) for x in np.percentile(v, [50, 10, 90])]
+
+
+def run_packing(args):
+    """Packed against padded pair state for every block workload: cells and
+    bytes of the pair tensor, measured peak device allocation of one block
+    (all four chained blocks for the stacked workload, with the pair buffer
+    reused and with every block's pair output retained), and block time.  The
+    padded rows run the same kernels on every sample padded to N_max, the
+    cost a padded layout pays.  One JSON line per workload."""
+    from variable_length_batching_gb300 import build, nt
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for name in ("tiny", "pairformer", "lognormal", "near_uniform", "stacked4"):
+        cfg = WORKLOADS[name]
+        base = wl.make_block_inputs(cfg)
+        nmax = int(base.lengths.max())
+        es = 2 if cfg.dtype == wl.BF16 else 4
+        line = {"report": "packing", "workload": cfg.name, "B": cfg.B, "C_z": cfg.C_z, "blocks": cfg.n_blocks,
+                "lengths": [int(x) for x in base.lengths]}
+        for layout, lens in (("packed", base.lengths), ("padded", np.full(cfg.B, nmax, dtype=np.int32))):
+            inp = wl.make_block_inputs(cfg, lengths=lens)
+            ws = [_dev_weights(b, dev) for b in inp.blocks]
+            lengths_d = torch.as_tensor(inp.lengths).to(dev)
+            s0 = inp.s.to(dev)
+            torch.cuda.synchronize()
+            res = {}
+            for mode in (("reuse", "retain") if cfg.n_blocks > 1 else ("reuse",)):
+                torch.cuda.synchronize()
+                torch.cuda.reset_peak_memory_stats(dev)
+                before = torch.cuda.memory_allocated(dev)
+                keep = []
+                part = nt.nt_partition_build(lengths_d)
+                s_cur, z = s0, None
+                for w in ws:
+                    z_k, _, s_cur = nt.block_forward(part, s_cur, w, z=None if mode == "retain" else z)
+                    z = z_k
+                    if mode == "retain":
+                        keep.append(z_k)
+                torch.cuda.synchronize()
+                res[mode] = torch.cuda.max_memory_allocated(dev) - before
+                del keep, z, z_k, s_cur, part
+            part = nt.nt_partition_build(lengths_d)
+            z = torch.empty(part.P, cfg.C_z, dtype=s0.dtype, device=dev)
+            wsp = torch.empty(nt.nt_pair_broadcast_workspace_bytes(part.T, cfg.C_z), dtype=torch.uint8, device=dev)
+            sos = [torch.empty_like(s0) for _ in ws]
+            m = torch.empty(part.T, cfg.C_z, dtype=s0.dtype, device=dev)
+
+            def chain():
+                s_cur = s0
+                for w, so in zip(ws, sos):
+                    nt.nt_pair_broadcast(part, s_cur, s_cur, w.W_a, w.W_b, z=z, workspace=wsp, stream=stream)
+                    nt.nt_pair_transition(part, z, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2, out=z,
+                                          stream=stream)
+                    nt.nt_pair_reduce(part, z, w.W_g, w.b_g, s_in=s_cur, m=m, s_out=so, stream=stream)
+                    s_cur = so
+            for _ in range(3):
+                chain()
+            med, p10, p90 = _timed(chain, flush, args.steps, stream)
+            line[layout] = {"cells": int(part.P), "pair_bytes": int(part.P) * cfg.C_z * es,
+                            "peak_alloc_bytes": res, "ms": med, "ms_p10_p90": [p10, p90],
+                            "cells_per_s": part.P * cfg.n_blocks / (med * 1e-3)}
+            del z, wsp, sos, m, part
+            torch.cuda.empty_cache()
+        line["pair_bytes_ratio"] = line["padded"]["pair_bytes"] / line["packed"]["pair_bytes"]
+        line["speedup_packed_over_padded"] = line["padded"]["ms"] / line["packed"]["ms"]
+        print(json.dumps(line), flush=True)
+
+
+def run_padsweep(args):
+    """Varlen attention over the packed stream against the same kernel on the
+    same number of segments padded to 512 tokens, at equivalent padding rates
+    from 3% to 90% (65,536 real tokens, 12 heads x 64).  One JSON line per rate."""
+    from variable_length_batching_gb300 import build, nt
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks, _ = load_peaks()
+    for rate in (0.03, 0.10, 0.25, 0.48, 0.75, 0.90):
+        lo, hi = wl.sweep_length_range(rate)
+        rng = np.random.default_rng(0)
+        lens = wl.draw_segments(ATTN_CFG.total_tokens, lo, hi, rng)
+        line = {"report": "padsweep", "target_rate": rate, "len_range": [lo, hi], "segments": int(len(lens)),
+                "pad_to": wl.PAD_TO,
+                "equivalent_pad_rate": 1.0 - float(lens.sum()) / (len(lens) * wl.PAD_TO)}
+        w = attn_work(lens, ATTN_CFG.H, ATTN_CFG.d)
+        for layout, L in (("varlen", lens), ("padded", np.full(len(lens), wl.PAD_TO, dtype=np.int32))):
+            a = wl.make_attn_inputs(ATTN_CFG, seqlens=L)
+            part = nt.nt_partition_build(torch.as_tensor(a.seqlens).to(dev))
+            q, k, v = a.q.to(dev), a.k.to(dev), a.v.to(dev)
+            o = torch.empty_like(q)
+            fn = lambda: nt.nt_varlen_attn(q, k, v, part.cu_seqlens, part.max_len, out=o, stream=stream)
+            for _ in range(3):
+                fn()
+            med, p10, p90 = _timed(fn, flush, args.steps, stream)
+            line[layout] = {"tokens": int(L.sum()), "ms": med, "ms_p10_p90": [p10, p90],
+                            "useful_tflops": w["flops"] / (med * 1e-3) / 1e12}
+            del q, k, v, o, a, part
+            torch.cuda.empty_cache()
+        line["measured_savings"] = 1.0 - line["varlen"]["ms"] / line["padded"]["ms"]
+        line["varlen_frac_of_peak"] = line["varlen"]["useful_tflops"] / peaks["bf16_tflops"]
+        print(json.dumps(line), flush=True)
+
+
 def run_only(args):
     """Time one call on one workload (profiling and per-kernel rooflines):
     ``--only {partition,broadcast,transition,reduce,block,attention}``."""
@@ -508,9 +704,12 @@ def run_only(args):
         cu, ml = apart.cu_seqlens, apart.max_len
         q, k, v = a.q.to(dev), a.k.to(dev), a.v.to(dev)
         o = torch.empty_like(q)
-        fn = lambda: nt.nt_varlen_attn(q, k, v, cu, ml, out=o, stream=stream)
-        w = attn_work(a.seqlens, cfg.H, cfg.d)
-        bound, name = "tensor", cfg.name
+        if args.causal:
+            fn = lambda: nt.nt_varlen_attn_qk(q, k, v, cu, cu, ml, causal=True, out=o, stream=stream)
+        else:
+            fn = lambda: nt.nt_varlen_attn(q, k, v, cu, ml, out=o, stream=stream)
+        w = attn_work(a.seqlens, cfg.H, cfg.d, causal=args.causal)
+        bound, name = "tensor", cfg.name + ("_causal" if args.causal else "")
     else:
         cfg = WORKLOADS[args.workload]
         inp = wl.make_block_inputs(cfg)
@@ -573,10 +772,19 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=["partition", "broadcast", "transition", "reduce", "block", "attention"],
-                    help="time one call on one workload instead of the whole step")
+                    choices=["partition", "broadcast", "transition", "reduce", "block", "attention",
+                             "packing", "padsweep"],
+                    help="time one call on one workload instead of the whole step; 'packing' and "
+                         "'padsweep' print the packed-vs-padded reports")
     ap.add_argument("--workload", default="pairformer", choices=sorted(WORKLOADS))
+    ap.add_argument("--causal", action="store_true", help="with --only attention: the causal mask")
     args = ap.parse_args()
+    if args.only == "packing":
+        run_packing(args)
+        return
+    if args.only == "padsweep":
+        run_padsweep(args)
+        return
     if args.only:
         run_only(args)
         return
