@@ -6,18 +6,25 @@
 // One CTA per (segment, 128-query tile, head).  The grid is sized from
 // max_len (ceil(max_len / 128) query tiles per segment); CTAs whose tile
 // starts past their segment's end exit at once, so no work list is needed.
-// Warps: 0 = TMA producer (Q once; K and V tiles of 64 tokens through a
-// 3-stage ring, 3-D tensor maps over the token-major [T, H, d] tensors),
-// 1 = TMEM owner and MMA issuer, 2-5 = softmax, one query row per thread.
-//   S_j = Q K_j^T  (M=128, N=64, K=64)  -> TMEM S[j & 1] (double-buffered)
-//   O  += P_j V_j   (M=128, N=64, K=64)  -> TMEM O, accumulated by the MMA
-// P_j is the bf16 probability tile, written by the softmax warps into
-// shared memory (K-major, double-buffered); V is read as an MN-major operand
-// straight from its TMA tile.  The running max moves only when a tile's max
-// exceeds it by more than 8 (log2 units), so O in TMEM is rescaled in place
-// on those tiles only.  A quarter of each full tile's exponentials run on the
-// FMA pipe (exp2_fma), the rest on the SFU.
-// Two CTAs fit on an SM (96 KB shared memory, 256 TMEM columns each).
+// Warps: 0 = TMA producer (K and V tiles of 64 tokens through a 3-stage ring,
+// 3-D tensor maps over the token-major [T, H, d] tensors), 1 = TMEM owner and
+// MMA issuer (the warp waits, one elected lane issues), 2-5 = softmax, one
+// query row per thread.
+//
+// Every MMA takes its A operand from tensor memory, so shared memory only
+// feeds the B operand (2 KB per MMA instead of 6 KB; with both operands in
+// shared memory an N = 64 MMA is bound by shared-memory bandwidth):
+//   Q   -> TMEM (the softmax threads load their query rows once)
+//   S_j  = Q K_j^T  (M=128, N=64, K=64)  -> TMEM S (single buffer)
+//   P_j  -> TMEM P[j & 1] (bf16, two per 32-bit column)
+//   O   += P_j V_j   (M=128, N=64, K=64)  -> TMEM O
+// The softmax threads read S_j into registers first and release the S
+// buffer at once, so S_{j+1} is computed while they exponentiate S_j.  The
+// running max moves only when a tile's max exceeds it by more than 8 (log2
+// units), so O in TMEM is rescaled in place on those tiles only.  A quarter
+// of each full tile's exponentials run on the FMA pipe (exp2_fma), the rest
+// on the SFU.  Two CTAs fit on an SM (48 KB shared memory, 256 TMEM columns
+// each, 224 of them used).
 //
 // Cross-attention takes the keys of query segment b from [cu_k[b], cu_k[b+1])
 // ("DanLing NestedTensor" section 3.3: the output adopts the query
@@ -38,22 +45,21 @@ constexpr int kBQ = 128;
 constexpr int kBK = 64;
 constexpr int kStages = 3;
 constexpr int kThreads = 6 * 32;
-constexpr uint32_t kQBytes = kBQ * kD * 2;          // 16 KB
 constexpr uint32_t kKVBytes = kBK * kD * 2;         // 8 KB
-constexpr uint32_t kPBytes = kBQ * kBK * 2;         // 16 KB
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
-constexpr uint32_t kOffP = kOffV + kStages * kKVBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColO = 128;          // S[b] at 64*b; O at 128
+// S at 0 (64 fp32 columns), O at 64 (64 fp32), P[b] at 128 + 32 b (64 keys as
+// bf16 pairs), Q at 192 (64 features as bf16 pairs)
+constexpr uint32_t kColS = 0, kColO = 64, kColP = 128, kColQ = 192;
 
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_full[2], p_empty[2];
+  uint64_t s_full, s_free;
+  uint64_t p_full[2], p_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -62,10 +68,10 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 
 template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 2)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ cu,
-               const int32_t* __restrict__ cu_k, int B, int64_t T, int64_t T_k, int H, int QT,
-               float scale_log2, bf16* __restrict__ o, float* __restrict__ lse, unsigned int* status) {
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+               const bf16* __restrict__ q, const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_k,
+               int B, int64_t T, int64_t T_k, int H, int QT, float scale_log2, bf16* __restrict__ o,
+               float* __restrict__ lse, unsigned int* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // (segment, query tile, head) of this CTA; heads vary fastest
   const int64_t item = blockIdx.x;
@@ -108,24 +114,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     return;
   }
 
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Softmax threads fetch their query row now, so its global-memory latency
+  // overlaps the barrier and TMEM set-up below (zeros past the segment's end).
+  uint32_t qw[32];
+  const int r = (warp & 3) * 32 + lane;       // query row within the tile (softmax warps)
+  if (warp >= 2 && q0 + r < hi) {
+    const uint4* qp = reinterpret_cast<const uint4*>(q + ((int64_t)(q0 + r) * H + h) * kD);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 w = __ldg(qp + u);
+      qw[4 * u] = w.x; qw[4 * u + 1] = w.y; qw[4 * u + 2] = w.z; qw[4 * u + 3] = w.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 32; ++u) qw[u] = 0u;
+  }
+
   uint8_t* smem = smem_raw;
-  uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
-  uint8_t* sP = smem + kOffP;
   Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort_flag = &bar.abort;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar.q_full, 1);
+    mbar_init(&bar.q_full, 128);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bar.k_full[i], 1); mbar_init(&bar.k_empty[i], 1);
       mbar_init(&bar.v_full[i], 1); mbar_init(&bar.v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar.s_full[i], 1); mbar_init(&bar.p_full[i], 128); mbar_init(&bar.p_empty[i], 1);
-    }
+    mbar_init(&bar.s_full, 1);
+    mbar_init(&bar.s_free, 128);
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.p_full[i], 128); mbar_init(&bar.p_empty[i], 1); }
     mbar_init(&bar.mma_done, 1);
     bar.abort = 0;
     fence_mbar_init();
@@ -140,9 +160,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&bar.q_full, kQBytes);
-      tma_load_3d(sQ, &tm_q, &bar.q_full, 0, h, q0);
+      prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nk; ++j) {
         const int st = j % kStages, rd = j / kStages;
@@ -156,7 +174,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         v_issued = j + 1;
       }
       // drain the copies this thread issued
-      mbar_wait(&bar.q_full, 0, nullptr, status);
       for (int j = k_issued - kStages; j < k_issued; ++j)
         if (j >= 0) mbar_wait(&bar.k_full[j % kStages], (j / kStages) & 1, nullptr, status);
       for (int j = v_issued - kStages; j < v_issued; ++j)
@@ -164,73 +181,89 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, kBK);
-      const uint32_t id_o = idesc_bf16_f32(128, kD) | (1u << 16);   // B (= V) MN-major
-      const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV), p_base = smem_u32(sP);
-      bool ok = mbar_wait(&bar.q_full, 0, abort_flag, status);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j % kStages;
-        if (!mbar_wait(&bar.k_full[st], (j / kStages) & 1, abort_flag, status)) return false;
-        tc_fence_after();
+    // The whole warp runs the loop and waits; one elected lane issues.
+    const uint32_t id_s = idesc_bf16_f32(128, kBK);
+    const uint32_t id_o = idesc_bf16_f32(128, kD) | (1u << 16);   // B (= V) MN-major
+    const uint32_t k_base = smem_u32(sK), v_base = smem_u32(sV);
+    const bool leader = elect_one();
+    bool ok = mbar_wait_warp(&bar.q_full, 0, abort_flag, status);
+    // S_j into the single S buffer: needs K_j, and S_{j-1} read out by the softmax
+    auto issue_s = [&](int j) -> bool {
+      const int st = j % kStages;
+      if (!mbar_wait_warp(&bar.k_full[st], (j / kStages) & 1, abort_flag, status)) return false;
+      if (j > 0 && !mbar_wait_warp(&bar.s_free, (j - 1) & 1, abort_flag, status)) return false;
+      tc_fence_after();
+      if (leader) {
         const uint32_t kb = k_base + st * kKVBytes;
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_bf16(tmem + kColS + 64 * (j & 1), sdesc_k128(q_base + kk * 32), sdesc_k128(kb + kk * 32), id_s, kk > 0);
-        mma_commit(&bar.s_full[j & 1]);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)      // 16 features = 8 packed TMEM columns of Q
+          mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * kk, sdesc_k128(kb + kk * 32), id_s, kk > 0);
+        mma_commit(&bar.s_full);
         mma_commit(&bar.k_empty[st]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && nk > 1) ok = issue_s(1);
-      for (int j = 0; j < nk && ok; ++j) {
-        // P_j written (and S_j fully read, and O rescaled if needed) by the softmax
-        if (!(ok = mbar_wait(&bar.p_full[j & 1], (j >> 1) & 1, abort_flag, status))) break;
-        const int st = j % kStages;
-        if (!(ok = mbar_wait(&bar.v_full[st], (j / kStages) & 1, abort_flag, status))) break;
-        tc_fence_after();
-        const uint32_t pb = p_base + (j & 1) * kPBytes, vb = v_base + st * kKVBytes;
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_bf16(tmem + kColO, sdesc_k128(pb + kk * 32), sdesc_k128(vb + kk * 2048), id_o,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar.p_empty[j & 1]);     // PV_j done: P[j&1] free, O holds tiles 0..j
-        mma_commit(&bar.v_empty[st]);
-        if (j + 2 < nk && !(ok = issue_s(j + 2))) break;
       }
-      mma_commit(&bar.mma_done);
-      mbar_wait(&bar.mma_done, 0, nullptr, status);
+      __syncwarp();
+      return true;
+    };
+    if (ok) {
+      tc_fence_after();
+      ok = issue_s(0);
     }
+    for (int j = 0; j < nk && ok; ++j) {
+      if (j + 1 < nk && !(ok = issue_s(j + 1))) break;
+      // P_j written (and O rescaled if needed) by the softmax
+      if (!(ok = mbar_wait_warp(&bar.p_full[j & 1], (j >> 1) & 1, abort_flag, status))) break;
+      const int st = j % kStages;
+      if (!(ok = mbar_wait_warp(&bar.v_full[st], (j / kStages) & 1, abort_flag, status))) break;
+      tc_fence_after();
+      if (leader) {
+        const uint32_t pt = tmem + kColP + 32 * (j & 1), vb = v_base + st * kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)    // 16 keys = 8 packed TMEM columns of P
+          mma_bf16_ts(tmem + kColO, pt + 8 * kk, sdesc_k128(vb + kk * 2048), id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar.p_empty[j & 1]);   // PV_j done: P[j&1] free, O holds tiles 0..j
+        mma_commit(&bar.v_empty[st]);
+      }
+      __syncwarp();
+    }
+    if (leader) mma_commit(&bar.mma_done);
+    __syncwarp();
+    mbar_wait_warp(&bar.mma_done, 0, nullptr, status);
   } else {
     // ------------------------------------------------------------ softmax
     const int qd = warp & 3;
-    const int r = qd * 32 + lane;                 // query row within the tile
     const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
+    // this row of Q -> TMEM
+    tmem_st32_sync(tmem + lane_addr + kColQ, qw);
+    tc_fence_before();
+    mbar_arrive(&bar.q_full);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
       const int sb = j & 1;
-      if (!(ok = mbar_wait_warp(&bar.s_full[sb], (j >> 1) & 1, abort_flag, status))) break;
+      if (!(ok = mbar_wait_warp(&bar.s_full, j & 1, abort_flag, status))) break;
       tc_fence_after();
       __syncwarp();
+      float sv[64];
+      tmem_ld64_sync(tmem + lane_addr + kColS, sv);   // this row of S_j
+      tc_fence_before();
+      mbar_arrive(&bar.s_free);                      // the S buffer may take S_{j+1}
       // keys of this tile this row sees: a prefix [0, cnt) of the tile
       int cnt = min(kBK, n_k - j * kBK);
       if (kCausal) cnt = max(0, min(cnt, qi * kBQ + r + diag - j * kBK + 1));
       const bool full = kCausal ? __all_sync(0xffffffffu, cnt == kBK) : cnt == kBK;
-      const uint32_t s_addr = tmem + lane_addr + kColS + 64 * sb;
-      // pass 1: row maximum of the raw scores (scale > 0)
+      // row maximum of the raw scores (scale > 0)
       float mx = -INFINITY;
-#pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
-        float sv[32];
-        tmem_ld32(s_addr + 32 * g, sv);
-        tmem_ld_wait();
-        if (full) {
+      if (full) {
+        float pm[8];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, sv[c]);
-        } else {
+        for (int u = 0; u < 8; ++u) pm[u] = sv[u];
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (32 * g + c < cnt) mx = fmaxf(mx, sv[c]);
-        }
+        for (int c = 8; c < 64; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
+        mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < cnt) mx = fmaxf(mx, sv[c]);
       }
       // lazy running max: move it only when it grows by more than 8 (log2 units)
       const float cand = mx * scale_log2;
@@ -247,55 +280,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!(ok = mbar_wait_warp(&bar.p_empty[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, status))) break;
         tc_fence_after();
         __syncwarp();
-#pragma unroll 1
-        for (int g = 0; g < 2; ++g) {
-          float ov[32];
-          tmem_ld32(tmem + lane_addr + kColO + 32 * g, ov);
-          tmem_ld_wait();
+        float ov[64];
+        tmem_ld64_sync(tmem + lane_addr + kColO, ov);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] *= corr;
-          tmem_st32(tmem + lane_addr + kColO + 32 * g, ov);
-        }
+        for (int c = 0; c < 64; ++c) ov[c] *= corr;
+        tmem_st32(tmem + lane_addr + kColO, ov);
+        tmem_st32(tmem + lane_addr + kColO + 32, ov + 32);
         tmem_st_wait();
       }
       l *= corr;
       // P_j -> P[sb]; PV_{j-2} has finished reading that buffer
       if (j >= 2 && !(ok = mbar_wait_warp(&bar.p_empty[sb], ((j >> 1) & 1) ^ 1, abort_flag, status))) break;
-      uint8_t* pbuf = sP + sb * kPBytes;
       float rs = 0.f;
-#pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
-        float sv[32];
-        tmem_ld32(s_addr + 32 * g, sv);
-        tmem_ld_wait();
-        uint32_t pk[16];
-        if (full) {
+      uint32_t pk[32];
+      if (full) {
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float x0 = fmaf(sv[c], scale_log2, -m), x1 = fmaf(sv[c + 1], scale_log2, -m);
-            // one in four exponentials on the FMA pipe, the rest on the SFU
-            const float p0 = ex2_approx(x0);
-            const float p1 = ((c & 2) == 2) ? exp2_fma(x1) : ex2_approx(x1);
-            rs += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float p0 = (32 * g + c < cnt) ? ex2_approx(fmaf(sv[c], scale_log2, -m)) : 0.f;
-            const float p1 = (32 * g + c + 1 < cnt) ? ex2_approx(fmaf(sv[c + 1], scale_log2, -m)) : 0.f;
-            rs += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
-          }
+        for (int c = 0; c < 64; c += 2) {
+          const float x0 = fmaf(sv[c], scale_log2, -m), x1 = fmaf(sv[c + 1], scale_log2, -m);
+          // one in four exponentials on the FMA pipe, the rest on the SFU
+          const float p0 = ex2_approx(x0);
+          const float p1 = ((c & 2) == 2) ? exp2_fma(x1) : ex2_approx(x1);
+          ps[(c >> 1) & 7] += p0 + p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
         }
+        rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      } else {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(pbuf + swz128_offset(r, 32 * g + 8 * u, 128)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = (c < cnt) ? ex2_approx(fmaf(sv[c], scale_log2, -m)) : 0.f;
+          const float p1 = (c + 1 < cnt) ? ex2_approx(fmaf(sv[c + 1], scale_log2, -m)) : 0.f;
+          rs += p0 + p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
       }
+      tmem_st32_sync(tmem + lane_addr + kColP + 32 * sb, pk);
       l += rs;
       tc_fence_before();
-      fence_async_shared();
       mbar_arrive(&bar.p_full[sb]);
     }
     if (ok && mbar_wait_warp(&bar.p_empty[(nk - 1) & 1], ((nk - 1) >> 1) & 1, abort_flag, status)) {
@@ -303,25 +324,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       __syncwarp();
       const int t = q0 + r;
       const float inv = l > 0.f ? 1.0f / l : 0.f;   // causal rows that see no key: zeros
-#pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
-        float ov[32];
-        tmem_ld32(tmem + lane_addr + kColO + 32 * g, ov);
-        tmem_ld_wait();
-        if (t < hi) {
-          bf16* op = o + ((int64_t)t * H + h) * kD + 32 * g;
+      float ov[64];
+      tmem_ld64_sync(tmem + lane_addr + kColO, ov);
+      if (t < hi) {
+        bf16* op = o + ((int64_t)t * H + h) * kD;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16x2(ov[8 * u] * inv, ov[8 * u + 1] * inv);
-            w.y = pack_bf16x2(ov[8 * u + 2] * inv, ov[8 * u + 3] * inv);
-            w.z = pack_bf16x2(ov[8 * u + 4] * inv, ov[8 * u + 5] * inv);
-            w.w = pack_bf16x2(ov[8 * u + 6] * inv, ov[8 * u + 7] * inv);
-            *reinterpret_cast<uint4*>(op + 8 * u) = w;
-          }
+        for (int u = 0; u < 8; ++u) {
+          uint4 w;
+          w.x = pack_bf16x2(ov[8 * u] * inv, ov[8 * u + 1] * inv);
+          w.y = pack_bf16x2(ov[8 * u + 2] * inv, ov[8 * u + 3] * inv);
+          w.z = pack_bf16x2(ov[8 * u + 4] * inv, ov[8 * u + 5] * inv);
+          w.w = pack_bf16x2(ov[8 * u + 6] * inv, ov[8 * u + 7] * inv);
+          *reinterpret_cast<uint4*>(op + 8 * u) = w;
         }
+        if (lse) lse[(int64_t)h * T + t] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
-      if (t < hi && lse) lse[(int64_t)h * T + t] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   }
 
@@ -350,9 +367,8 @@ bool attn_tc_supported(nt_dtype dt, int d) { return dt == NT_BF16 && d == kD; }
 cudaError_t launch_attn_tc(const AttnProblem& p, unsigned int* status, cudaStream_t s) {
   if (p.T_q == 0 || p.B == 0) return cudaSuccess;
   if (p.T_k == 0) return cudaErrorInvalidValue;   // no key tensor to map; the caller routes this case
-  CUtensorMap mq, mk, mv;
-  if (!make_map_thd(&mq, p.q, p.T_q, p.H, kBQ) || !make_map_thd(&mk, p.k, p.T_k, p.H, kBK) ||
-      !make_map_thd(&mv, p.v, p.T_k, p.H, kBK))
+  CUtensorMap mk, mv;
+  if (!make_map_thd(&mk, p.k, p.T_k, p.H, kBK) || !make_map_thd(&mv, p.v, p.T_k, p.H, kBK))
     return cudaErrorInvalidValue;
   const int QT = max(1, (p.max_len_q + kBQ - 1) / kBQ);
   const int64_t items = (int64_t)p.B * QT * p.H;
@@ -361,8 +377,8 @@ cudaError_t launch_attn_tc(const AttnProblem& p, unsigned int* status, cudaStrea
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const float scale_log2 = p.scale * 1.4426950408889634f;
-  kern<<<(unsigned)items, kThreads, kSmemBytes, s>>>(mq, mk, mv, p.cu_q, p.cu_k, p.B, p.T_q, p.T_k, p.H, QT,
-                                                     scale_log2, (bf16*)p.o, p.lse, status);
+  kern<<<(unsigned)items, kThreads, kSmemBytes, s>>>(mk, mv, (const bf16*)p.q, p.cu_q, p.cu_k, p.B, p.T_q, p.T_k,
+                                                     p.H, QT, scale_log2, (bf16*)p.o, p.lse, status);
   return cudaGetLastError();
 }
 
