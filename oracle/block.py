@@ -25,6 +25,14 @@ across valid positions").  Readings where the pages leave a step open:
 Packing follows Eq. 2/3: cell (a, b) of sample i is packed row
 o_i + a * N_i + b with o the exclusive scan of N_i^2.
 
+Rectangular pairs (section 3.2 "Consuming one logical axis", Eq. 4;
+Appendix A.1 "the rectangular variant has distinct row and column inputs and
+divides its column mean by M_i"): rows come from X_i (N_i x C), columns from
+Z_i (M_i x C), P_i[a, b] = u(X_i[a]) + v(Z_i[b]) over N_i x M_i cells packed
+at o_i + a * M_i + b, and the mean over b divides by M_i.  Reading: a sample
+with M_i = 0 has an empty column sum; its row means are taken as zero (the
+pages define the mean for non-empty rows only).
+
 Everything is float64; inputs are the exact values handed to the GPU.
 """
 from __future__ import annotations
@@ -34,7 +42,7 @@ from typing import List, Optional, Sequence
 
 import numpy as np
 
-from .partition import partition
+from .partition import packed_rect_row, partition, partition_rect
 
 
 def linear(x: np.ndarray, W: np.ndarray, b: Optional[np.ndarray] = None) -> np.ndarray:
@@ -99,6 +107,19 @@ def block_sample(X: np.ndarray, w: Weights, X_right: Optional[np.ndarray] = None
     return SampleResult(P, P_tilde, M, X_tilde)
 
 
+def block_sample_rect(X: np.ndarray, Z: np.ndarray, w: Weights) -> SampleResult:
+    """The rectangular block for one sample: rows from X (N x C), columns
+    from Z (M x C), mean over the M columns."""
+    U = linear(X, w.W_a)                       # u(X[a]), (N, C_p)
+    V = linear(Z, w.W_b)                       # v(Z[b]), (M, C_p)
+    P = U[:, None, :] + V[None, :, :]          # (N, M, C_p)
+    P_tilde = transition(P, w.gamma, w.beta, w.eps, w.W1, w.b1, w.W2, w.b2)
+    Mi = Z.shape[0]
+    Mean = P_tilde.sum(axis=1) / Mi if Mi > 0 else np.zeros((X.shape[0], U.shape[1]))
+    X_tilde = X + linear(Mean, w.W_g, w.b_g)
+    return SampleResult(P, P_tilde, Mean, X_tilde)
+
+
 @dataclass
 class PackedResult:
     z: np.ndarray        # (P, C_p) packed pair state before the transition
@@ -126,6 +147,30 @@ def block_packed(lengths: Sequence[int], s: np.ndarray, w: Weights) -> PackedRes
         z_tilde[o:o + N * N] = r.P_tilde.reshape(N * N, C_p)
         m[part.cu_seqlens[i]:part.cu_seqlens[i + 1]] = r.M
         s_out[part.cu_seqlens[i]:part.cu_seqlens[i + 1]] = r.X_tilde
+    return PackedResult(z, z_tilde, m, s_out)
+
+
+def block_packed_rect(rows: Sequence[int], cols: Sequence[int], s_row: np.ndarray, s_col: np.ndarray,
+                      w: Weights) -> PackedResult:
+    """``block_sample_rect`` on every sample, packed by Eq. 4's layout."""
+    part = partition_rect(rows, cols)
+    C_p = w.W_a.shape[0]
+    z = np.zeros((part.P, C_p))
+    z_tilde = np.zeros((part.P, C_p))
+    m = np.zeros((part.T_rows, C_p))
+    s_out = np.zeros((part.T_rows, s_row.shape[1]))
+    for i in range(len(part.rows)):
+        N, M = int(part.rows[i]), int(part.cols[i])
+        if N == 0:
+            continue
+        X = s_row[part.cu_rows[i]:part.cu_rows[i + 1]]
+        Z = s_col[part.cu_cols[i]:part.cu_cols[i + 1]]
+        r = block_sample_rect(X, Z, w)
+        o = int(part.pair_off[i])
+        z[o:o + N * M] = r.P.reshape(N * M, C_p)
+        z_tilde[o:o + N * M] = r.P_tilde.reshape(N * M, C_p)
+        m[part.cu_rows[i]:part.cu_rows[i + 1]] = r.M
+        s_out[part.cu_rows[i]:part.cu_rows[i + 1]] = r.X_tilde
     return PackedResult(z, z_tilde, m, s_out)
 
 
@@ -205,6 +250,38 @@ def pair_reduce(lengths, z, W_g=None, b_g=None, s_in=None):
     s_out = linear(m, W_g, b_g)
     if s_in is not None:
         s_out = s_in + s_out
+    return m, s_out
+
+
+def pair_broadcast_rect(rows, cols, s_row, s_col, W_a, W_b) -> np.ndarray:
+    """z[o_i + a M_i + b] = u(X_i[a]) + v(Z_i[b]) over the sum N_i M_i cells."""
+    part = partition_rect(rows, cols)
+    z = np.zeros((part.P, W_a.shape[0]))
+    for i in range(len(part.rows)):
+        N, M = int(part.rows[i]), int(part.cols[i])
+        U = linear(s_row[part.cu_rows[i]:part.cu_rows[i + 1]], W_a)
+        V = linear(s_col[part.cu_cols[i]:part.cu_cols[i + 1]], W_b)
+        for a in range(N):
+            for b in range(M):
+                z[packed_rect_row(part.pair_off, part.cols, i, a, b)] = U[a] + V[b]
+    return z
+
+
+def pair_reduce_rect(rows, cols, z, W_g=None, b_g=None, s_in=None):
+    """Eq. 4's column sum divided by M_i: m[eta_i + a] = (1/M_i) sum_b
+    z[o_i + a M_i + b] (zero when M_i = 0); optionally s_out = s_in + g(m)."""
+    part = partition_rect(rows, cols)
+    m = np.zeros((part.T_rows, z.shape[1]))
+    for i in range(len(part.rows)):
+        N, M = int(part.rows[i]), int(part.cols[i])
+        for a in range(N):
+            if M == 0:
+                continue
+            acc = np.zeros(z.shape[1])
+            for b in range(M):
+                acc += z[packed_rect_row(part.pair_off, part.cols, i, a, b)]
+            m[part.cu_rows[i] + a] = acc / M
+    s_out = None if W_g is None else s_in + linear(m, W_g, b_g)
     return m, s_out
 
 

@@ -14,6 +14,10 @@ Learning":
     (pairs); the second-level splits delimit each pair row's cells.
   * Appendix A "Structural invariants": o_0 = 0, o_{i+1} - o_i = p_i, o_B = T;
     the innermost splits of a pair tensor hold 1 + sum_i N_i entries.
+  * section 3.2 "Consuming one logical axis", Eq. 4: a rectangular pair state
+    P_i of N_i x M_i cells packs cell (a, b) at o_i + a * M_i + b, with o the
+    exclusive scan of N_i * M_i, and its rows are grouped by
+    eta_i = sum_{k<i} N_k.
 """
 from __future__ import annotations
 
@@ -67,6 +71,53 @@ def partition(lengths: Sequence[int]) -> Partition:
         row_start=np.asarray(row_start, dtype=np.int64),
         row_sample=np.asarray(row_sample, dtype=np.int64),
         T=int(cu[-1]), P=int(pair_off[-1]), max_len=max(N) if N else 0)
+
+
+@dataclass
+class RectPartition:
+    rows: np.ndarray        # N_i, int64 (B,)
+    cols: np.ndarray        # M_i, int64 (B,)
+    cu_rows: np.ndarray     # eta of Eq. 4: offsets of the row singles, (B+1,)
+    cu_cols: np.ndarray     # offsets of the column singles, (B+1,)
+    pair_off: np.ndarray    # o: exclusive scan of N_i * M_i, (B+1,)
+    row_start: np.ndarray   # first cell of each pair row, (T_rows+1,)
+    row_sample: np.ndarray  # sample owning each pair row, (T_rows,)
+    T_rows: int
+    T_cols: int
+    P: int
+    max_rows: int
+    max_cols: int
+
+
+def packed_rect_row(pair_off: np.ndarray, cols: np.ndarray, i: int, a: int, b: int) -> int:
+    """o_i + a * M_i + b (the packed row of cell (a, b) in Eq. 4)."""
+    return int(pair_off[i]) + a * int(cols[i]) + b
+
+
+def partition_rect(rows: Sequence[int], cols: Sequence[int]) -> RectPartition:
+    """Partitions of a batch of rectangular pair states: row singles of
+    lengths N_i, column singles of lengths M_i, N_i x M_i cells each."""
+    N = [int(n) for n in rows]
+    M = [int(m) for m in cols]
+    if len(N) != len(M):
+        raise ValueError("one column length per sample")
+    if any(n < 0 for n in N) or any(m < 0 for m in M):
+        raise ValueError("lengths must be non-negative")
+    M_arr = np.asarray(M, dtype=np.int64)
+    cu_r = sample_offsets(N)
+    cu_c = sample_offsets(M)
+    pair_off = sample_offsets([n * m for n, m in zip(N, M)])
+    row_start, row_sample = [], []
+    for i, n in enumerate(N):
+        for a in range(n):
+            row_start.append(packed_rect_row(pair_off, M_arr, i, a, 0))
+            row_sample.append(i)
+    row_start.append(int(pair_off[-1]))
+    return RectPartition(
+        rows=np.asarray(N, dtype=np.int64), cols=M_arr, cu_rows=cu_r, cu_cols=cu_c, pair_off=pair_off,
+        row_start=np.asarray(row_start, dtype=np.int64), row_sample=np.asarray(row_sample, dtype=np.int64),
+        T_rows=int(cu_r[-1]), T_cols=int(cu_c[-1]), P=int(pair_off[-1]),
+        max_rows=max(N) if N else 0, max_cols=max(M) if M else 0)
 
 
 def padded_cells(lengths: Sequence[int]) -> int:

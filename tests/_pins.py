@@ -331,3 +331,97 @@ def pin_attention_causal_masked(varlen_attention, masked_full_attention_causal, 
     # the first query of every segment sees only its own key: O = v
     for b in range(3):
         assert np.allclose(O1[cu[b]], v[cu[b]], rtol=1e-14, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# Rectangular pairs ("DanLing NestedTensor" section 3.2 "Consuming one logical
+# axis", Eq. 4; Appendix A.1, rectangular variant)
+# ----------------------------------------------------------------------------
+
+def pin_rect_partition_bruteforce(partition_rect, rows, cols):
+    """Walking every (sample, a, b) with b < M_i in order numbers the cells
+    0, 1, 2, ...; each row starts at its split; rows and columns scan
+    separately; M = N gives the square partition."""
+    p = partition_rect(rows, cols)
+    cell, row = 0, 0
+    for i, (n, m) in enumerate(zip(rows, cols)):
+        assert p.cu_rows[i] == sum(rows[:i]) and p.cu_cols[i] == sum(cols[:i])
+        for a in range(n):
+            assert p.row_start[row] == cell and p.row_sample[row] == i
+            cell += m
+            row += 1
+    assert row == p.T_rows == sum(rows) and cell == p.P == sum(n * m for n, m in zip(rows, cols))
+    assert p.T_cols == sum(cols) and p.row_start[-1] == p.P
+    assert np.array_equal(np.diff(p.pair_off), np.asarray(rows) * np.asarray(cols))
+
+
+def pin_rect_square_case(partition_rect, partition, lengths):
+    """A rectangular partition with M_i = N_i is the square partition."""
+    r, s = partition_rect(lengths, lengths), partition(lengths)
+    assert np.array_equal(r.pair_off, s.pair_off) and np.array_equal(r.row_start, s.row_start)
+    assert np.array_equal(r.cu_rows, s.cu_seqlens) and np.array_equal(r.cu_cols, s.cu_seqlens)
+
+
+def pin_rect_broadcast_onehot(pair_broadcast_rect, rng):
+    """One-hot projections: with W_b = 0 cell (a, b) holds the selected
+    features of row single a; with W_a = 0, those of column single b.  Rows
+    and columns come from their own inputs at their own offsets."""
+    rows, cols = [2, 0, 3, 1], [3, 2, 1, 0]
+    C, C_p = 4, 2
+    s_row = rng.standard_normal((sum(rows), C))
+    s_col = rng.standard_normal((sum(cols), C))
+    Wsel = np.zeros((C_p, C))
+    Wsel[0, 3] = 1.0
+    Wsel[1, 1] = 1.0
+    Z = np.zeros((C_p, C))
+    za = pair_broadcast_rect(rows, cols, s_row, s_col, Wsel, Z)
+    zb = pair_broadcast_rect(rows, cols, s_row, s_col, Z, Wsel)
+    assert za.shape == (sum(n * m for n, m in zip(rows, cols)), C_p)
+    cell, r0, c0 = 0, 0, 0
+    for n, m in zip(rows, cols):
+        for a in range(n):
+            for b in range(m):
+                assert np.array_equal(za[cell], s_row[r0 + a, [3, 1]])
+                assert np.array_equal(zb[cell], s_col[c0 + b, [3, 1]])
+                cell += 1
+        r0 += n
+        c0 += m
+
+
+def pin_rect_broadcast_library(pair_broadcast_rect, rng):
+    """Every cell equals torch's linear of its row single plus its column single."""
+    rows, cols = [2, 3], [4, 1]
+    C, C_p = 3, 5
+    s_row, s_col = rng.standard_normal((5, C)), rng.standard_normal((5, C))
+    Wa, Wb = rng.standard_normal((C_p, C)), rng.standard_normal((C_p, C))
+    z = pair_broadcast_rect(rows, cols, s_row, s_col, Wa, Wb)
+    tR, tC, ta, tb = (torch.from_numpy(x) for x in (s_row, s_col, Wa, Wb))
+    cell, r0, c0 = 0, 0, 0
+    for n, m in zip(rows, cols):
+        for a in range(n):
+            for b in range(m):
+                ref = F.linear(tR[r0 + a], ta) + F.linear(tC[c0 + b], tb)
+                assert np.allclose(z[cell], ref.numpy(), rtol=1e-13, atol=1e-13)
+                cell += 1
+        r0 += n
+        c0 += m
+
+
+def pin_rect_reduce_closed_form(pair_broadcast_rect, pair_reduce_rect, rng):
+    """Without a transition, (1/M_i) sum_b (U[a] + V[b]) = U[a] + mean of the
+    sample's M_i column projections; M_i = 0 gives zero rows."""
+    rows, cols = [3, 2, 4, 1], [5, 1, 2, 0]
+    C, C_p = 4, 3
+    s_row = rng.standard_normal((sum(rows), C))
+    s_col = rng.standard_normal((sum(cols), C))
+    Wa, Wb = rng.standard_normal((C_p, C)), rng.standard_normal((C_p, C))
+    z = pair_broadcast_rect(rows, cols, s_row, s_col, Wa, Wb)
+    m, _ = pair_reduce_rect(rows, cols, z)
+    U, V = s_row @ Wa.T, s_col @ Wb.T
+    r0, c0 = 0, 0
+    for n, mm in zip(rows, cols):
+        for a in range(n):
+            ref = U[r0 + a] + V[c0:c0 + mm].sum(axis=0) / mm if mm else np.zeros(C_p)
+            assert np.allclose(m[r0 + a], ref, rtol=1e-12, atol=1e-12)
+        r0 += n
+        c0 += mm

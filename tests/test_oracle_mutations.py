@@ -235,3 +235,49 @@ def test_cross_uses_query_offsets_for_keys_caught():
                                       v[:T] if v.shape[0] >= T else np.resize(v, q.shape),
                                       cu, scale, segments, causal, None)
     _fails(pins.pin_attention_cross_sdpa, same_cu, rng(18))
+
+
+# --- rectangular pairs ---------------------------------------------------------
+
+def rect_partition_row_stride_n(rows, cols):
+    p = opart.partition_rect(rows, cols)      # rows stride by N_i instead of M_i
+    rs = []
+    for i, n in enumerate(p.rows):
+        rs += [int(p.pair_off[i]) + a * int(n) for a in range(int(n))]
+    p.row_start = np.asarray(rs + [p.P])
+    return p
+
+
+def rect_reduce_divides_by_rows(rows, cols, z, W_g=None, b_g=None, s_in=None):
+    m, s_out = oblock.pair_reduce_rect(rows, cols, z, W_g, b_g, s_in)
+    p = opart.partition_rect(rows, cols)
+    for i in range(len(p.rows)):
+        n, mm = int(p.rows[i]), int(p.cols[i])
+        if n and mm:
+            m[p.cu_rows[i]:p.cu_rows[i + 1]] *= mm / n
+    return m, s_out
+
+
+def rect_broadcast_cols_from_row_offsets(rows, cols, s_row, s_col, W_a, W_b):
+    p = opart.partition_rect(rows, cols)
+    z = np.zeros((p.P, W_a.shape[0]))
+    for i in range(len(p.rows)):
+        n, m = int(p.rows[i]), int(p.cols[i])
+        U = oblock.linear(s_row[p.cu_rows[i]:p.cu_rows[i + 1]], W_a)
+        V = oblock.linear(np.resize(s_col[p.cu_rows[i]:], (max(m, 1), s_col.shape[1]))[:m], W_b)
+        for a in range(n):
+            for b in range(m):
+                z[int(p.pair_off[i]) + a * m + b] = U[a] + V[b]
+    return z
+
+
+def test_rect_row_stride_caught():
+    _fails(pins.pin_rect_partition_bruteforce, rect_partition_row_stride_n, [2, 3], [4, 1])
+
+
+def test_rect_divisor_caught():
+    _fails(pins.pin_rect_reduce_closed_form, oblock.pair_broadcast_rect, rect_reduce_divides_by_rows, rng(23))
+
+
+def test_rect_column_offsets_caught():
+    _fails(pins.pin_rect_broadcast_onehot, rect_broadcast_cols_from_row_offsets, rng(21))

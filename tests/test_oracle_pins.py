@@ -188,3 +188,45 @@ def test_attention_cross_sdpa():
 
 def test_attention_causal_masked():
     pins.pin_attention_causal_masked(oattn.varlen_attention, oattn.masked_full_attention_causal, rng(19))
+
+
+def test_rect_partition_bruteforce():
+    from oracle import partition as op
+    pins.pin_rect_partition_bruteforce(op.partition_rect, [2, 0, 3, 1, 4], [3, 2, 0, 1, 4])
+    r = rng(20)
+    for _ in range(20):
+        B = int(r.integers(0, 7))
+        pins.pin_rect_partition_bruteforce(op.partition_rect, list(r.integers(0, 9, B)), list(r.integers(0, 9, B)))
+
+
+def test_rect_square_case():
+    from oracle import partition as op
+    pins.pin_rect_square_case(op.partition_rect, op.partition, [2, 3, 0, 5])
+
+
+def test_rect_broadcast_onehot():
+    pins.pin_rect_broadcast_onehot(oblock.pair_broadcast_rect, rng(21))
+
+
+def test_rect_broadcast_library():
+    pins.pin_rect_broadcast_library(oblock.pair_broadcast_rect, rng(22))
+
+
+def test_rect_reduce_closed_form():
+    pins.pin_rect_reduce_closed_form(oblock.pair_broadcast_rect, oblock.pair_reduce_rect, rng(23))
+
+
+def test_rect_block_square_case_equals_square_block():
+    """The rectangular block with Z = X and M_i = N_i is the square block."""
+    r = rng(24)
+    lengths = [3, 1, 4]
+    C, C_p, H = 6, 4, 8
+    s = r.standard_normal((sum(lengths), C))
+    w = oblock.Weights(W_a=r.standard_normal((C_p, C)), W_b=r.standard_normal((C_p, C)),
+                       gamma=1 + 0.1 * r.standard_normal(C_p), beta=0.1 * r.standard_normal(C_p), eps=1e-5,
+                       W1=r.standard_normal((H, C_p)), b1=r.standard_normal(H), W2=r.standard_normal((C_p, H)),
+                       b2=r.standard_normal(C_p), W_g=r.standard_normal((C, C_p)), b_g=r.standard_normal(C))
+    a = oblock.block_packed_rect(lengths, lengths, s, s, w)
+    b = oblock.block_packed(lengths, s, w)
+    for x, y in ((a.z, b.z), (a.z_tilde, b.z_tilde), (a.m, b.m), (a.s_out, b.s_out)):
+        assert np.allclose(x, y, rtol=1e-13, atol=1e-13)
