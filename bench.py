@@ -687,6 +687,54 @@ def run_padsweep(args):
         print(json.dumps(line), flush=True)
 
 
+def run_rect(args):
+    """The rectangular block (N_i x M_i pair states, distinct row and column
+    singles) on the B=8 batch with N_i, M_i ~ U[64, 256]: per-call device
+    time (L2 flushed), cells/s of the block and the broadcast/reduce HBM
+    fractions.  One JSON line."""
+    from variable_length_batching_gb300 import build, nt
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks, _ = load_peaks()
+    cfg = wl.RECT_BF16
+    inp = wl.make_rect_inputs(cfg)
+    w = _dev_weights(inp.blocks[0], dev)
+    part = nt.nt_partition_build_rect(torch.as_tensor(inp.rows).to(dev), torch.as_tensor(inp.cols).to(dev))
+    sr, sc = inp.s_row.to(dev), inp.s_col.to(dev)
+    z = torch.empty(part.P, cfg.C_z, dtype=sr.dtype, device=dev)
+    ws = torch.empty(nt.nt_pair_broadcast_workspace_bytes_rect(part.T, part.T_cols, cfg.C_z), dtype=torch.uint8,
+                     device=dev)
+    m = torch.empty(part.T, cfg.C_z, dtype=sr.dtype, device=dev)
+    so = torch.empty_like(sr)
+    calls = {
+        "broadcast": lambda: nt.nt_pair_broadcast(part, sr, sc, w.W_a, w.W_b, z=z, workspace=ws, stream=stream),
+        "transition": lambda: nt.nt_pair_transition(part, z, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2,
+                                                    out=z, stream=stream),
+        "reduce": lambda: nt.nt_pair_reduce(part, z, w.W_g, w.b_g, s_in=sr, m=m, s_out=so, stream=stream),
+    }
+    for _ in range(3):
+        for f in calls.values():
+            f()
+    out = {"report": "rect", "workload": cfg.name, "T_rows": part.T, "T_cols": part.T_cols, "P": part.P}
+    tot = 0.0
+    for name, f in calls.items():
+        med, p10, p90 = _timed(f, flush, args.steps, stream)
+        out[name] = {"ms": med, "ms_p10_p90": [p10, p90]}
+        tot += med
+    es = 2
+    out["broadcast"]["hbm_frac"] = part.P * cfg.C_z * es / (out["broadcast"]["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    out["reduce"]["hbm_frac"] = part.P * cfg.C_z * es / (out["reduce"]["ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"]
+    out["transition"]["tensor_frac"] = (4 * cfg.C_z * cfg.H_t * part.P / (out["transition"]["ms"] * 1e-3) / 1e12
+                                        / peaks["bf16_tflops"])
+    out["block_ms"] = tot
+    out["cells_per_s"] = part.P / (tot * 1e-3)
+    nt.nt_device_status(stream)
+    print(json.dumps(out), flush=True)
+
+
 def run_only(args):
     """Time one call on one workload (profiling and per-kernel rooflines):
     ``--only {partition,broadcast,transition,reduce,block,attention}``."""
@@ -773,7 +821,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["partition", "broadcast", "transition", "reduce", "block", "attention",
-                             "packing", "padsweep"],
+                             "packing", "padsweep", "rect"],
                     help="time one call on one workload instead of the whole step; 'packing' and "
                          "'padsweep' print the packed-vs-padded reports")
     ap.add_argument("--workload", default="pairformer", choices=sorted(WORKLOADS))
@@ -784,6 +832,9 @@ def main():
         return
     if args.only == "padsweep":
         run_padsweep(args)
+        return
+    if args.only == "rect":
+        run_rect(args)
         return
     if args.only:
         run_only(args)

@@ -69,6 +69,14 @@ typedef enum { NT_F32 = 0, NT_BF16 = 1 } nt_dtype;
  *   row_sample[T]    sample index owning each single row / pair row.
  * T = sum N_i, P = sum N_i^2, max_len = max N_i.  All pointers are device
  * pointers owned by the caller; the struct itself is host memory.
+ *
+ * Rectangular pair states ([DL] section 3.2 "Consuming one logical axis",
+ * Eq. 4): sample i has N_i rows and M_i columns, its cells are packed at
+ * pair_off[i] + a * M_i + b with pair_off the exclusive scan of N_i * M_i,
+ * and row_start[cu_seqlens[i] + a] = pair_off[i] + a * M_i.  The column
+ * fields below describe M_i; nt_partition_build sets them to alias the row
+ * fields (M_i = N_i), and a struct whose col_lengths is NULL is read as
+ * square too.  T, max_len, lengths and cu_seqlens always describe the rows.
  */
 typedef struct nt_partition {
   int32_t B;
@@ -80,6 +88,10 @@ typedef struct nt_partition {
   const int64_t* pair_off;
   const int64_t* row_start;   /* NULL until nt_partition_rows */
   const int32_t* row_sample;  /* NULL until nt_partition_rows */
+  const int32_t* col_lengths;     /* M_i [B], or NULL for square pairs */
+  const int32_t* col_cu_seqlens;  /* [B+1] exclusive scan of M_i (column singles) */
+  int64_t T_cols;                 /* sum M_i */
+  int32_t max_col_len;            /* max M_i */
 } nt_partition;
 
 /*
@@ -100,8 +112,27 @@ nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_
                              void* stream);
 
 /*
- * nt_partition_rows -- second-level row splits of the square pair state
- * ([DL] Figure 2: 1 + sum N_i entries; Eq. 3 with b = 0).
+ * nt_partition_build_rect -- partitions of rectangular pair states ([DL]
+ * section 3.2 "Consuming one logical axis", Eq. 4; Appendix A.1, the
+ * rectangular variant with distinct row and column inputs).
+ *   d_rows, d_cols  [B] int32, N_i >= 0 rows and M_i >= 0 columns.
+ *   d_cu_rows       [B+1] int32 out, exclusive scan of N_i (eta of Eq. 4).
+ *   d_cu_cols       [B+1] int32 out, exclusive scan of M_i.
+ *   d_pair_off      [B+1] int64 out, exclusive scan of N_i * M_i.
+ *   d_totals        [8] int64 device scratch.
+ *   out             filled like nt_partition_build, with the column fields
+ *                   pointing at d_cols / d_cu_cols.
+ * Synchronises `stream` once.  NT_ERR_INVALID for a negative length,
+ * NT_ERR_OVERFLOW if sum N_i or sum M_i does not fit int32.  Integer-exact.
+ */
+nt_status nt_partition_build_rect(const int32_t* d_rows, const int32_t* d_cols, int32_t B,
+                                  int32_t* d_cu_rows, int32_t* d_cu_cols, int64_t* d_pair_off,
+                                  int64_t* d_totals, nt_partition* out, void* stream);
+
+/*
+ * nt_partition_rows -- second-level row splits of the pair state ([DL]
+ * Figure 2: 1 + sum N_i entries; Eq. 3 with b = 0; rows of a rectangular
+ * state are M_i cells long, Eq. 4).
  *   part          a partition from nt_partition_build (T, P known).
  *   d_row_start   [T+1] int64 out.   d_row_sample [T] int32 out.
  * Sets part->row_start and part->row_sample.  Asynchronous.
@@ -109,22 +140,28 @@ nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_
 nt_status nt_partition_rows(nt_partition* part, int64_t* d_row_start, int32_t* d_row_sample,
                             void* stream);
 
-/* Bytes of device workspace nt_pair_broadcast needs: the two projected
- * single representations u and v in fp32, 2 * T * C_z * 4. */
+/* Bytes of device workspace nt_pair_broadcast needs for a square partition:
+ * the two projected single representations u and v in fp32, 2 * T * C_z * 4. */
 size_t nt_pair_broadcast_workspace_bytes(int64_t T, int32_t C_z);
+
+/* The same for a rectangular partition: (T_rows + T_cols) * C_z * 4. */
+size_t nt_pair_broadcast_workspace_bytes_rect(int64_t T_rows, int64_t T_cols, int32_t C_z);
 
 /*
  * nt_pair_broadcast -- pair construction of [DL] Eq. 1, first line, with the
  * broadcast of section 3.2 "Creating axes through broadcasting":
- *     u = s_left W_a^T,  v = s_right W_b^T            (T x C_z, fp32)
- *     z[pair_off[i] + a N_i + b, :] = u[cu_i + a] + v[cu_i + b]
- * over the P = sum N_i^2 cells only; no activation at construction ([DL]
- * Appendix A.1).
+ *     u = s_left W_a^T,  v = s_right W_b^T            (fp32)
+ *     z[pair_off[i] + a M_i + b, :] = u[cu_i + a] + v[col_cu_i + b]
+ * over the P = sum N_i M_i cells only (M_i = N_i and col_cu = cu for square
+ * pairs); no activation at construction ([DL] Appendix A.1).
  *   part          partition with row splits (nt_partition_rows done).
- *   s_left, s_right  [T, C_s] singles (the same pointer for square pairs).
+ *   s_left        [T, C_s] row singles.
+ *   s_right       [T_cols, C_s] column singles (the same pointer as s_left
+ *                 for square pairs built from one single representation).
  *   W_a, W_b      [C_z, C_s].        z [P, C_z] out.
- *   workspace     >= nt_pair_broadcast_workspace_bytes(T, C_z) device bytes,
- *                 16-byte aligned; holds u and v while the call runs.
+ *   workspace     >= (T + T_cols) * C_z * 4 device bytes (see the two
+ *                 workspace-size calls), 16-byte aligned; holds u and v
+ *                 while the call runs.
  * Asynchronous.  Rounds z once to the I/O dtype (round-to-nearest-even).
  */
 nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void* s_left,
@@ -145,7 +182,8 @@ nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void
  * library declares in device memory (8 MiB, held on every GPU that loads the
  * library until the process exits).  It allocates nothing: no cudaMalloc, no
  * cudaFree, no allocating library routine.
- *   Limit: 2 * T * C_z <= 2,097,152; larger problems return
+ *   Limit: (T + T_cols) * C_z <= 2,097,152 (2 * T * C_z for square
+ *   partitions); larger problems return
  *   NT_ERR_UNSUPPORTED (see nt_last_error) and enqueue nothing.
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
@@ -181,8 +219,10 @@ nt_status nt_pair_transition(const nt_partition* part, nt_dtype dtype, const voi
 
 /*
  * nt_pair_reduce -- the column mean of [DL] Eq. 1, third line, as the
- * segmented sum of Eq. 4 divided by N_i:
- *     m[cu_i + a, :] = (1/N_i) sum_b z[pair_off[i] + a N_i + b, :]
+ * segmented sum of Eq. 4 divided by the row length M_i (= N_i for square
+ * pairs; [DL] Appendix A.1 for the rectangular variant):
+ *     m[cu_i + a, :] = (1/M_i) sum_b z[pair_off[i] + a M_i + b, :]
+ * (zero for a sample with M_i = 0, whose column sum is empty)
  * then, if W_g is not NULL:  s_out = s_in + m W_g^T + b_g.
  *   z [P, C_z].  m [T, C_z] out (fp32 accumulation, stored in the I/O dtype).
  *   W_g [C_s, C_z] or NULL.  b_g [C_s] fp32 or NULL.  s_in [T, C_s] or NULL

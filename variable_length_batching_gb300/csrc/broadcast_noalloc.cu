@@ -12,7 +12,8 @@
 //
 // Cost of the choice: every GPU that loads the library holds the array
 // (kNoAllocScratchFloats * 4 bytes = 8 MiB) until the process exits, the
-// problem size is capped at 2 * T * C_z <= kNoAllocScratchFloats, and all
+// problem size is capped at (T + T_cols) * C_z <= kNoAllocScratchFloats
+// (2 * T * C_z for square pairs), and all
 // calls share the one array, so calls that overlap on the GPU (different
 // streams, or different host threads on the same device) race on it.  The
 // kernels overwrite every element of u and v they read, so nothing needs to
@@ -63,10 +64,12 @@ nt_status nt_pair_broadcast_noalloc(const nt_partition* part, nt_dtype dtype, co
                                     int32_t C_z, void* z, void* stream) {
   if (!part) return record_error(NT_ERR_INVALID, "partition is NULL");
   if (part->T < 0 || C_z <= 0) return record_error(NT_ERR_INVALID, "T must be >= 0 and C_z > 0");
-  const size_t need = (size_t)2 * (size_t)part->T * (size_t)C_z;
+  const int64_t T_cols = t_cols_of(part);
+  if (T_cols < 0) return record_error(NT_ERR_INVALID, "T_cols must be >= 0");
+  const size_t need = (size_t)(part->T + T_cols) * (size_t)C_z;   // u and v
   if (need > kNoAllocScratchFloats)
     return record_error(NT_ERR_UNSUPPORTED,
-                        "2 * T * C_z exceeds the 2,097,152 fp32 elements of the built-in scratch; "
+                        "(T + T_cols) * C_z exceeds the 2,097,152 fp32 elements of the built-in scratch; "
                         "use nt_pair_broadcast with a caller workspace");
   float* scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess)

@@ -64,9 +64,16 @@ nt_status check_partition(const nt_partition* p, bool need_rows) {
     return fail(NT_ERR_INVALID, "partition pointers are NULL");
   if (need_rows && p->T > 0 && (!p->row_start || !p->row_sample))
     return fail(NT_ERR_INVALID, "partition has no row splits (call nt_partition_rows)");
-  if (p->P < p->T || (p->T > 0 && p->P > p->T * (int64_t)p->max_len))
+  if (p->col_lengths) {
+    if (p->T_cols < 0 || p->max_col_len < 0 || (p->T_cols > 0 && !p->col_cu_seqlens))
+      return fail(NT_ERR_INVALID, "partition column fields are inconsistent");
+    if (p->T > 0 && p->P > p->T * (int64_t)p->max_col_len)
+      return fail(NT_ERR_INVALID, "partition totals are inconsistent (T=%lld P=%lld max_col_len=%d)",
+                  (long long)p->T, (long long)p->P, p->max_col_len);
+  } else if (p->P < p->T || (p->T > 0 && p->P > p->T * (int64_t)p->max_len)) {
     return fail(NT_ERR_INVALID, "partition totals are inconsistent (T=%lld P=%lld max_len=%d)",
                 (long long)p->T, (long long)p->P, p->max_len);
+  }
   return NT_OK;
 }
 
@@ -117,7 +124,7 @@ nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_
   if (!aligned16(d_totals) || !aligned16(d_pair_off) || !aligned16(d_cu_seqlens))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_partition_scan(d_lengths, B, d_cu_seqlens, d_pair_off, d_totals, s);
+  cudaError_t e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, s);
   if (e != cudaSuccess) return cuda_fail(e, "partition scan launch");
   int64_t tot[4] = {0, 0, 0, 0};
   e = cudaMemcpyAsync(tot, d_totals, sizeof(tot), cudaMemcpyDeviceToHost, s);
@@ -132,8 +139,49 @@ nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_
   out->pair_off = d_pair_off;
   out->row_start = nullptr;
   out->row_sample = nullptr;
+  // square: the column side is the row side
+  out->col_lengths = d_lengths;
+  out->col_cu_seqlens = d_cu_seqlens;
+  out->T_cols = tot[0];
+  out->max_col_len = (int32_t)tot[2];
   if (tot[3] & 1) return fail(NT_ERR_INVALID, "a sample length is negative");
   if (tot[3] & 2) return fail(NT_ERR_OVERFLOW, "T = %lld does not fit int32 cu_seqlens", (long long)tot[0]);
+  return NT_OK;
+}
+
+nt_status nt_partition_build_rect(const int32_t* d_rows, const int32_t* d_cols, int32_t B,
+                                  int32_t* d_cu_rows, int32_t* d_cu_cols, int64_t* d_pair_off,
+                                  int64_t* d_totals, nt_partition* out, void* stream) {
+  if (!out) return fail(NT_ERR_INVALID, "out is NULL");
+  if (B < 0) return fail(NT_ERR_INVALID, "B = %d < 0", B);
+  if ((B > 0 && (!d_rows || !d_cols)) || !d_cu_rows || !d_cu_cols || !d_pair_off || !d_totals)
+    return fail(NT_ERR_INVALID, "NULL device pointer");
+  if (!aligned16(d_totals) || !aligned16(d_pair_off) || !aligned16(d_cu_rows) || !aligned16(d_cu_cols))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_partition_scan(d_rows, B > 0 ? d_cols : d_rows, B, d_cu_rows, d_cu_cols, d_pair_off,
+                                        d_totals, s);
+  if (e != cudaSuccess) return cuda_fail(e, "partition scan launch");
+  int64_t tot[6] = {0, 0, 0, 0, 0, 0};
+  e = cudaMemcpyAsync(tot, d_totals, sizeof(tot), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
+  out->B = B;
+  out->T = tot[0];
+  out->P = tot[1];
+  out->max_len = (int32_t)tot[2];
+  out->lengths = d_rows;
+  out->cu_seqlens = d_cu_rows;
+  out->pair_off = d_pair_off;
+  out->row_start = nullptr;
+  out->row_sample = nullptr;
+  out->col_lengths = B > 0 ? d_cols : d_rows;
+  out->col_cu_seqlens = d_cu_cols;
+  out->T_cols = B > 0 ? tot[4] : 0;
+  out->max_col_len = B > 0 ? (int32_t)tot[5] : 0;
+  if (tot[3] & 1) return fail(NT_ERR_INVALID, "a sample length is negative");
+  if (tot[3] & 2) return fail(NT_ERR_OVERFLOW, "sum N_i = %lld does not fit int32", (long long)tot[0]);
+  if (tot[3] & 4) return fail(NT_ERR_OVERFLOW, "sum M_i = %lld does not fit int32", (long long)tot[4]);
   return NT_OK;
 }
 
@@ -145,8 +193,8 @@ nt_status nt_partition_rows(nt_partition* part, int64_t* d_row_start, int32_t* d
     return fail(NT_ERR_INVALID, "NULL row split pointer");
   if (!aligned16(d_row_start) || !aligned16(d_row_sample))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
-  cudaError_t e = launch_partition_rows(part->lengths, part->cu_seqlens, part->pair_off, part->B,
-                                        part->T, part->P, d_row_start, d_row_sample,
+  cudaError_t e = launch_partition_rows(part->lengths, part->col_lengths, part->cu_seqlens, part->pair_off,
+                                        part->B, part->T, part->P, d_row_start, d_row_sample,
                                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "partition rows launch");
   part->row_start = d_row_start;
@@ -157,6 +205,11 @@ nt_status nt_partition_rows(nt_partition* part, int64_t* d_row_start, int32_t* d
 size_t nt_pair_broadcast_workspace_bytes(int64_t T, int32_t C_z) {
   if (T < 0 || C_z < 0) return 0;
   return (size_t)2 * (size_t)T * (size_t)C_z * sizeof(float);
+}
+
+size_t nt_pair_broadcast_workspace_bytes_rect(int64_t T_rows, int64_t T_cols, int32_t C_z) {
+  if (T_rows < 0 || T_cols < 0 || C_z < 0) return 0;
+  return (size_t)(T_rows + T_cols) * (size_t)C_z * sizeof(float);
 }
 
 nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void* s_left,
@@ -174,17 +227,31 @@ nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void
   if (!aligned16(s_left) || !aligned16(s_right) || !aligned16(W_a) || !aligned16(W_b) ||
       !aligned16(z) || !aligned16(workspace))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
-  if (workspace_bytes < nt_pair_broadcast_workspace_bytes(part->T, C_z))
-    return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes,
-                nt_pair_broadcast_workspace_bytes(part->T, C_z));
+  const int64_t T_cols = t_cols_of(part);
+  const size_t need = nt_pair_broadcast_workspace_bytes_rect(part->T, T_cols, C_z);
+  if (workspace_bytes < need)
+    return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
   if (part->T == 0) return NT_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* u = static_cast<float*>(workspace);
   float* v = u + part->T * (int64_t)C_z;
   LinearProblem probs[2] = {{s_left, W_a, nullptr, nullptr, u}, {s_right, W_b, nullptr, nullptr, v}};
-  cudaError_t e = linear_tc_supported(dtype, part->T, C_z, C_s)
-                      ? launch_linear_tc(1, probs, 2, part->T, C_z, C_s, status_word(), s)
-                      : launch_linear(dtype, 1, probs, 2, part->T, C_z, C_s, s);
+  cudaError_t e = cudaSuccess;
+  if (T_cols == part->T) {
+    // one launch for both projections
+    e = linear_tc_supported(dtype, part->T, C_z, C_s)
+            ? launch_linear_tc(1, probs, 2, part->T, C_z, C_s, status_word(), s)
+            : launch_linear(dtype, 1, probs, 2, part->T, C_z, C_s, s);
+  } else {
+    // rectangular: row and column singles have different row counts
+    const int64_t rows[2] = {part->T, T_cols};
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+      if (rows[k] == 0) continue;
+      e = linear_tc_supported(dtype, rows[k], C_z, C_s)
+              ? launch_linear_tc(1, &probs[k], 1, rows[k], C_z, C_s, status_word(), s)
+              : launch_linear(dtype, 1, &probs[k], 1, rows[k], C_z, C_s, s);
+    }
+  }
   if (e != cudaSuccess) return cuda_fail(e, "projection launch");
   e = launch_broadcast(dtype, u, v, part, C_z, z, s);
   if (e != cudaSuccess) return cuda_fail(e, "broadcast launch");

@@ -83,10 +83,21 @@ __device__ __forceinline__ void flag_device(unsigned int* status, unsigned int b
 // Internal launchers (one per kernel family), called by the ABI layer after
 // argument validation.  Each returns cudaGetLastError() of its launches.
 // ----------------------------------------------------------------------------
-cudaError_t launch_partition_scan(const int32_t* lengths, int32_t B, int32_t* cu, int64_t* pair_off,
-                                  int64_t* totals, cudaStream_t s);
-cudaError_t launch_partition_rows(const int32_t* lengths, const int32_t* cu, const int64_t* pair_off,
-                                  int32_t B, int64_t T, int64_t P, int64_t* row_start,
+// Column side of a partition (rectangular pair states); square partitions
+// may leave col_lengths NULL, which means M_i = N_i.
+inline const int32_t* col_lengths_of(const nt_partition* p) { return p->col_lengths ? p->col_lengths : p->lengths; }
+inline const int32_t* col_cu_of(const nt_partition* p) {
+  return p->col_lengths ? p->col_cu_seqlens : p->cu_seqlens;
+}
+inline int64_t t_cols_of(const nt_partition* p) { return p->col_lengths ? p->T_cols : p->T; }
+inline int32_t max_cols_of(const nt_partition* p) { return p->col_lengths ? p->max_col_len : p->max_len; }
+
+// cols / cu_cols NULL: square (M_i = N_i).  totals = {T, P, max_len, check,
+// T_cols, max_col_len} (the last two only with cols).
+cudaError_t launch_partition_scan(const int32_t* lengths, const int32_t* cols, int32_t B, int32_t* cu,
+                                  int32_t* cu_cols, int64_t* pair_off, int64_t* totals, cudaStream_t s);
+cudaError_t launch_partition_rows(const int32_t* lengths, const int32_t* cols, const int32_t* cu,
+                                  const int64_t* pair_off, int32_t B, int64_t T, int64_t P, int64_t* row_start,
                                   int32_t* row_sample, cudaStream_t s);
 
 // Y[M, N] = X[M, K] W[N, K]^T (+ bias[N]) (+ R[M, N]).  Up to two independent

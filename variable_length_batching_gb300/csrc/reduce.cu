@@ -1,7 +1,9 @@
 // Segmented column mean over the pair state ("DanLing NestedTensor" Eq. 1
 // third line and Eq. 4, "Consuming one logical axis"):
-//     m[cu_i + a] = (1/N_i) sum_b z[pair_off_i + a N_i + b]
-// Every pair row's N_i cells are contiguous, so one CTA owns one pair row:
+//     m[cu_i + a] = (1/M_i) sum_b z[pair_off_i + a M_i + b]
+// with M_i the row length (= N_i for square pairs; the rectangular variant
+// divides by M_i, Appendix A.1), zero rows when M_i = 0.
+// Every pair row's M_i cells are contiguous, so one CTA owns one pair row:
 // its threads split the row's cells, each keeping a 16-byte feature vector
 // of fp32 sums, then the cell groups are combined through shared memory.
 // HBM-bound: reads P * C_z elements once, writes T * C_z.
@@ -14,7 +16,7 @@ constexpr int kThreads = 128;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ lengths,
+reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ row_len,
               const int32_t* __restrict__ row_sample, const int64_t* __restrict__ row_start,
               int64_t rows, int C_z, T* __restrict__ m) {
   extern __shared__ float part[];              // [groups][C_z]
@@ -23,7 +25,7 @@ reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ lengths,
   const int lane = threadIdx.x % lanes, grp = threadIdx.x / lanes;
   const bool active = grp < groups;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const int64_t n = lengths[row_sample[r]];
+    const int64_t n = row_len[row_sample[r]];
     const T* zr = z + row_start[r] * C_z + lane * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (active) {
@@ -53,7 +55,7 @@ reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ lengths,
       for (int g = 1; g < groups; ++g)
 #pragma unroll
         for (int t = 0; t < 8; ++t) tot[t] += part[g * C_z + lane * 8 + t];
-      const float inv = 1.0f / (float)n;
+      const float inv = n > 0 ? 1.0f / (float)n : 0.f;
 #pragma unroll
       for (int t = 0; t < 8; ++t) tot[t] *= inv;
       store8(m + r * C_z + lane * 8, tot);
@@ -63,17 +65,17 @@ reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ lengths,
 }
 
 // fp32 widths that are multiples of 4 but not of 8: one thread per feature.
-__global__ void reduce_kernel_f32_scalar(const float* __restrict__ z, const int32_t* __restrict__ lengths,
+__global__ void reduce_kernel_f32_scalar(const float* __restrict__ z, const int32_t* __restrict__ row_len,
                                          const int32_t* __restrict__ row_sample,
                                          const int64_t* __restrict__ row_start, int64_t rows, int C_z,
                                          float* __restrict__ m) {
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const int64_t n = lengths[row_sample[r]];
+    const int64_t n = row_len[row_sample[r]];
     const float* zr = z + row_start[r] * C_z;
     for (int c = threadIdx.x; c < C_z; c += blockDim.x) {
       float acc = 0.f;
       for (int64_t b = 0; b < n; ++b) acc += zr[b * C_z + c];
-      m[r * C_z + c] = acc / (float)n;
+      m[r * C_z + c] = n > 0 ? acc / (float)n : 0.f;
     }
   }
 }
@@ -85,17 +87,18 @@ cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int
   if (p->T == 0) return cudaSuccess;
   const int sms = sm_count();
   const int grid = (int)min64(p->T, (int64_t)sms * 32);
+  const int32_t* cl = col_lengths_of(p);     // cells per pair row
   if (C_z % 8 == 0 && C_z / 8 <= kThreads) {
     const int groups = kThreads / (C_z / 8);
     const size_t smem = sizeof(float) * groups * C_z;
     if (dt == NT_BF16)
-      reduce_kernel<bf16><<<grid, kThreads, smem, s>>>((const bf16*)z, p->lengths, p->row_sample,
+      reduce_kernel<bf16><<<grid, kThreads, smem, s>>>((const bf16*)z, cl, p->row_sample,
                                                        p->row_start, p->T, C_z, (bf16*)m);
     else
-      reduce_kernel<float><<<grid, kThreads, smem, s>>>((const float*)z, p->lengths, p->row_sample,
+      reduce_kernel<float><<<grid, kThreads, smem, s>>>((const float*)z, cl, p->row_sample,
                                                         p->row_start, p->T, C_z, (float*)m);
   } else {
-    reduce_kernel_f32_scalar<<<grid, 128, 0, s>>>((const float*)z, p->lengths, p->row_sample,
+    reduce_kernel_f32_scalar<<<grid, 128, 0, s>>>((const float*)z, cl, p->row_sample,
                                                  p->row_start, p->T, C_z, (float*)m);
   }
   return cudaGetLastError();

@@ -32,7 +32,9 @@ class nt_partition(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int64), ("P", ctypes.c_int64),
                 ("max_len", ctypes.c_int32), ("lengths", ctypes.c_void_p),
                 ("cu_seqlens", ctypes.c_void_p), ("pair_off", ctypes.c_void_p),
-                ("row_start", ctypes.c_void_p), ("row_sample", ctypes.c_void_p)]
+                ("row_start", ctypes.c_void_p), ("row_sample", ctypes.c_void_p),
+                ("col_lengths", ctypes.c_void_p), ("col_cu_seqlens", ctypes.c_void_p),
+                ("T_cols", ctypes.c_int64), ("max_col_len", ctypes.c_int32)]
 
 
 _lib = None
@@ -41,8 +43,10 @@ _P, _I32, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctype
 _PP = ctypes.POINTER(nt_partition)
 SIGNATURES = {
     "nt_partition_build": (_I32, [_P, _I32, _P, _P, _P, _PP, _P]),
+    "nt_partition_build_rect": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _PP, _P]),
     "nt_partition_rows": (_I32, [_PP, _P, _P, _P]),
     "nt_pair_broadcast_workspace_bytes": (_SZ, [_I64, _I32]),
+    "nt_pair_broadcast_workspace_bytes_rect": (_SZ, [_I64, _I64, _I32]),
     "nt_pair_broadcast": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P, _SZ, _P]),
     "nt_pair_broadcast_noalloc": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P]),
     "nt_pair_transition": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P]),
@@ -107,7 +111,9 @@ def _f32(t: Optional[torch.Tensor]):
 
 @dataclass
 class Partition:
-    """Device partitions of a packed batch plus the host totals."""
+    """Device partitions of a packed batch plus the host totals.  For a
+    rectangular batch ``col_lengths`` / ``col_cu_seqlens`` hold M_i and its
+    scan; for a square one they are the row tensors."""
     lengths: torch.Tensor
     cu_seqlens: torch.Tensor
     pair_off: torch.Tensor
@@ -115,6 +121,14 @@ class Partition:
     row_start: torch.Tensor
     row_sample: torch.Tensor
     c: nt_partition
+    col_lengths: Optional[torch.Tensor] = None
+    col_cu_seqlens: Optional[torch.Tensor] = None
+
+    @property
+    def T_cols(self): return self.c.T_cols
+
+    @property
+    def max_col_len(self): return self.c.max_col_len
 
     @property
     def B(self): return self.c.B
@@ -150,8 +164,37 @@ def nt_partition_build(lengths: torch.Tensor, stream=None) -> Partition:
     return Partition(lengths, cu, pair_off, totals, row_start, row_sample, c)
 
 
+def nt_partition_build_rect(rows: torch.Tensor, cols: torch.Tensor, stream=None) -> Partition:
+    """Row lengths N_i and column lengths M_i (int32, on the device) ->
+    partitions of the N_i x M_i pair states (``nt_partition_build_rect`` +
+    ``nt_partition_rows``)."""
+    if rows.dtype != torch.int32 or cols.dtype != torch.int32:
+        raise ValueError("lengths must be int32")
+    if rows.numel() != cols.numel():
+        raise ValueError("one column length per sample")
+    dev = rows.device
+    B = rows.numel()
+    cu_r = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    cu_c = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    pair_off = torch.empty(B + 1, dtype=torch.int64, device=dev)
+    totals = torch.empty(8, dtype=torch.int64, device=dev)
+    c = nt_partition()
+    st = lib().nt_partition_build_rect(_ptr(rows) if B else None, _ptr(cols) if B else None, B, _ptr(cu_r),
+                                       _ptr(cu_c), _ptr(pair_off), _ptr(totals), ctypes.byref(c), _stream(stream))
+    _check(st, "nt_partition_build_rect")
+    row_start = torch.empty(c.T + 1, dtype=torch.int64, device=dev)
+    row_sample = torch.empty(max(c.T, 1), dtype=torch.int32, device=dev)
+    _check(lib().nt_partition_rows(ctypes.byref(c), _ptr(row_start), _ptr(row_sample), _stream(stream)),
+           "nt_partition_rows")
+    return Partition(rows, cu_r, pair_off, totals, row_start, row_sample, c, cols, cu_c)
+
+
 def nt_pair_broadcast_workspace_bytes(T: int, C_z: int) -> int:
     return int(lib().nt_pair_broadcast_workspace_bytes(T, C_z))
+
+
+def nt_pair_broadcast_workspace_bytes_rect(T_rows: int, T_cols: int, C_z: int) -> int:
+    return int(lib().nt_pair_broadcast_workspace_bytes_rect(T_rows, T_cols, C_z))
 
 
 def nt_pair_broadcast(part: Partition, s_left: torch.Tensor, s_right: torch.Tensor,
@@ -159,15 +202,16 @@ def nt_pair_broadcast(part: Partition, s_left: torch.Tensor, s_right: torch.Tens
                       workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     T, C_s = s_left.shape
     C_z = W_a.shape[0]
-    if T != part.T or tuple(s_right.shape) != (T, C_s):
-        raise ValueError(f"singles {tuple(s_left.shape)} do not match the partition (T={part.T})")
+    if T != part.T or tuple(s_right.shape) != (part.T_cols, C_s):
+        raise ValueError(f"singles {tuple(s_left.shape)}, {tuple(s_right.shape)} do not match the partition "
+                         f"(T={part.T}, T_cols={part.T_cols})")
     if tuple(W_a.shape) != (C_z, C_s) or tuple(W_b.shape) != (C_z, C_s):
         raise ValueError("W_a, W_b must be (C_z, C_s)")
     if z is None:
         z = torch.empty(part.P, C_z, dtype=s_left.dtype, device=s_left.device)
     elif tuple(z.shape) != (part.P, C_z):
         raise ValueError(f"z {tuple(z.shape)} must be (P={part.P}, C_z={C_z})")
-    need = nt_pair_broadcast_workspace_bytes(T, C_z)
+    need = nt_pair_broadcast_workspace_bytes_rect(T, part.T_cols, C_z)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=s_left.device)
     st = lib().nt_pair_broadcast(ctypes.byref(part.c), _dtype(s_left), _ptr(s_left), _ptr(s_right), C_s,
@@ -181,7 +225,7 @@ def nt_pair_broadcast_noalloc(part: Partition, s_left: torch.Tensor, s_right: to
                               W_a: torch.Tensor, W_b: torch.Tensor, z: Optional[torch.Tensor] = None,
                               stream=None) -> torch.Tensor:
     """nt_pair_broadcast without a workspace argument: u and v live in the
-    library's own fixed device array (2 * T * C_z <= 2,097,152), for callers
+    library's own fixed device array ((T + T_cols) * C_z <= 2,097,152), for callers
     that cannot allocate device memory.  ``z`` must then be supplied by the
     caller too if the call itself may not allocate."""
     T, C_s = s_left.shape
@@ -294,11 +338,13 @@ def nt_device_status(stream=None) -> int:
 
 def block_forward(part: Partition, s: torch.Tensor, w, ln_eps: float = 1e-5,
                   z: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                  s_out: Optional[torch.Tensor] = None, stream=None):
+                  s_out: Optional[torch.Tensor] = None, stream=None, s_col: Optional[torch.Tensor] = None):
     """One single->pair->single block (Eq. 1) as the three pair calls; ``w``
     holds W_a, W_b, ln_gamma, ln_beta, W1, b1, W2, b2, W_g, b_g on the device.
-    The transition runs in place on z.  Returns (z~, m, s_out)."""
-    z = nt_pair_broadcast(part, s, s, w.W_a, w.W_b, z=z, workspace=workspace, stream=stream)
+    The transition runs in place on z.  ``s_col`` gives the column singles of
+    a rectangular partition (default: ``s``).  Returns (z~, m, s_out)."""
+    z = nt_pair_broadcast(part, s, s if s_col is None else s_col, w.W_a, w.W_b, z=z, workspace=workspace,
+                          stream=stream)
     nt_pair_transition(part, z, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2, ln_eps=ln_eps,
                        out=z, stream=stream)
     m, s_out = nt_pair_reduce(part, z, w.W_g, w.b_g, s_in=s, s_out=s_out, stream=stream)

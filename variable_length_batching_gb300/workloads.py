@@ -177,6 +177,41 @@ def make_block_inputs(cfg: BlockConfig, lengths: Optional[Sequence[int]] = None,
     return BlockInputs(cfg, lens, s, blocks)
 
 
+# Rectangular pair states: the Pairformer-style block with independent row
+# and column lengths, both ~ U[64, 256], rows drawn first.
+RECT_BF16 = BlockConfig(  # T_rows=1,031, T_cols=1,543, P=187,394
+    "rect_bf16_B8_N64-256xM64-256_Cs384_Cz128", B=8, length_rule="uniform",
+    rule_args=(64, 256), C_s=384, C_z=128, H_t=512, dtype=BF16)
+RECT_TINY_FP32 = BlockConfig(
+    "rect_tiny_fp32_B4_N8-32xM8-32_Cs32_Cz16", B=4, length_rule="uniform", rule_args=(8, 32),
+    C_s=32, C_z=16, H_t=64, dtype=F32)
+
+
+@dataclass
+class RectInputs:
+    cfg: BlockConfig
+    rows: np.ndarray      # N_i int32 (B,)
+    cols: np.ndarray      # M_i int32 (B,)
+    s_row: torch.Tensor   # (sum N_i, C_s) host, I/O dtype
+    s_col: torch.Tensor   # (sum M_i, C_s)
+    blocks: List[BlockWeights] = field(default_factory=list)
+
+
+def make_rect_inputs(cfg: BlockConfig, rows: Optional[Sequence[int]] = None, cols: Optional[Sequence[int]] = None,
+                     biases: bool = False, seed: Optional[int] = None) -> RectInputs:
+    """Seeded rectangular inputs: row lengths, column lengths (both by the
+    config's rule unless given), row singles, column singles, weights."""
+    rng = np.random.default_rng(cfg.seed if seed is None else seed)
+    r_drawn = draw_lengths(cfg, rng)
+    c_drawn = draw_lengths(cfg, rng)
+    N = r_drawn if rows is None else np.asarray(rows, dtype=np.int32)
+    M = c_drawn if cols is None else np.asarray(cols, dtype=np.int32)
+    s_row = to_io(rng.standard_normal((int(N.astype(np.int64).sum()), cfg.C_s)).astype(np.float32), cfg.dtype)
+    s_col = to_io(rng.standard_normal((int(M.astype(np.int64).sum()), cfg.C_s)).astype(np.float32), cfg.dtype)
+    blocks = [make_block_weights(rng, cfg.C_s, cfg.C_z, cfg.H_t, cfg.dtype, biases) for _ in range(cfg.n_blocks)]
+    return RectInputs(cfg, N, M, s_row, s_col, blocks)
+
+
 def random_rows(rows: int, width: int, dtype: str, seed: int, scale: float = 1.0) -> torch.Tensor:
     """A (rows, width) host tensor of N(0, scale^2) values in the I/O dtype."""
     rng = np.random.default_rng(seed)
