@@ -33,6 +33,11 @@ at o_i + a * M_i + b, and the mean over b divides by M_i.  Reading: a sample
 with M_i = 0 has an empty column sum; its row means are taken as zero (the
 pages define the mean for non-empty rows only).
 
+SwiGLU transition (Eq. 1: h is "a SwiGLU feature update" after Shazeer 2020;
+Appendix A.1: transition expansion four): h(y) = W2 (SiLU(W1 y + b1) *
+(W3 y + b3)) + b2 with SiLU(x) = x sigmoid(x) (Swish with beta = 1), W1 the
+gate and W3 the value projection, both C_p -> H_t.  Biases are optional.
+
 Everything is float64; inputs are the exact values handed to the GPU.
 """
 from __future__ import annotations
@@ -63,6 +68,23 @@ def layer_norm(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float) -
 def h_theta(x, W1, b1, W2, b2):
     """Feature update: Linear(C_p -> H_t), ReLU, Linear(H_t -> C_p)."""
     return linear(np.maximum(linear(x, W1, b1), 0.0), W2, b2)
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """x * sigmoid(x) = x / (1 + exp(-x))."""
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def h_swiglu(x, W1, b1, W3, b3, W2, b2):
+    """Gated update: Linear(C_p -> H_t) through SiLU, times a second
+    Linear(C_p -> H_t), then Linear(H_t -> C_p)."""
+    return linear(silu(linear(x, W1, b1)) * linear(x, W3, b3), W2, b2)
+
+
+def transition_swiglu(P, gamma, beta, eps, W1, b1, W3, b3, W2, b2):
+    """P~ = P + h_swiglu(LN(P)) on every cell independently."""
+    return P + h_swiglu(layer_norm(P, gamma, beta, eps), W1, b1, W3, b3, W2, b2)
 
 
 def transition(P, gamma, beta, eps, W1, b1, W2, b2):

@@ -425,3 +425,44 @@ def pin_rect_reduce_closed_form(pair_broadcast_rect, pair_reduce_rect, rng):
             assert np.allclose(m[r0 + a], ref, rtol=1e-12, atol=1e-12)
         r0 += n
         c0 += mm
+
+
+# ----------------------------------------------------------------------------
+# SwiGLU transition ("DanLing NestedTensor" Eq. 1, h is a SwiGLU update)
+# ----------------------------------------------------------------------------
+
+def pin_silu(silu):
+    """SiLU(0) = 0; SiLU(x) - SiLU(-x) = x for every x; SiLU(x) -> x for
+    large x and -> 0 for large negative x."""
+    x = np.linspace(-30, 30, 121)
+    y = silu(x)
+    assert silu(np.array([0.0]))[0] == 0.0
+    assert np.allclose(y - silu(-x), x, rtol=1e-14, atol=1e-13)
+    assert abs(silu(np.array([40.0]))[0] - 40.0) < 1e-12 and abs(silu(np.array([-40.0]))[0]) < 1e-12
+
+
+def pin_swiglu_library(transition_swiglu, rng, biases=True):
+    """LN -> (SiLU(gate) * value) -> Linear plus residual equals
+    torch.nn.functional's layer_norm / linear / silu in float64."""
+    P, C_p, H = 29, 8, 32
+    z = rng.standard_normal((P, C_p)) * 2.0 - 0.3
+    gamma = 1.0 + 0.1 * rng.standard_normal(C_p)
+    beta = 0.1 * rng.standard_normal(C_p)
+    W1, W3, W2 = rng.standard_normal((H, C_p)), rng.standard_normal((H, C_p)), rng.standard_normal((C_p, H))
+    b1, b3, b2 = (rng.standard_normal(n) if biases else None for n in (H, H, C_p))
+    got = transition_swiglu(z, gamma, beta, 1e-5, W1, b1, W3, b3, W2, b2)
+    t = lambda a: None if a is None else torch.from_numpy(a)
+    ln = F.layer_norm(t(z), (C_p,), t(gamma), t(beta), 1e-5)
+    hid = F.silu(F.linear(ln, t(W1), t(b1))) * F.linear(ln, t(W3), t(b3))
+    ref = t(z) + F.linear(hid, t(W2), t(b2))
+    assert np.allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_swiglu_zero_gate(transition_swiglu, rng):
+    """A zero gate (W1 = 0, b1 = 0) closes the update: SiLU(0) = 0, so
+    z~ = z + b2 exactly, whatever W3 and W2 are."""
+    z = rng.standard_normal((9, 6))
+    b2 = rng.standard_normal(6)
+    out = transition_swiglu(z, np.ones(6), np.zeros(6), 1e-5, np.zeros((12, 6)), None,
+                            rng.standard_normal((12, 6)), rng.standard_normal(12), rng.standard_normal((6, 12)), b2)
+    assert np.array_equal(out, z + b2)

@@ -281,3 +281,30 @@ def test_rect_divisor_caught():
 
 def test_rect_column_offsets_caught():
     _fails(pins.pin_rect_broadcast_onehot, rect_broadcast_cols_from_row_offsets, rng(21))
+
+
+# --- SwiGLU transition ----------------------------------------------------------
+
+def swiglu_swapped(P, gamma, beta, eps, W1, b1, W3, b3, W2, b2):
+    return oblock.transition_swiglu(P, gamma, beta, eps, W3, b3, W1, b1, W2, b2)   # value gated
+
+
+def swiglu_sigmoid(P, gamma, beta, eps, W1, b1, W3, b3, W2, b2):
+    y = oblock.layer_norm(P, gamma, beta, eps)
+    g = oblock.linear(y, W1, b1)
+    return P + oblock.linear(g / g * (1 / (1 + np.exp(-g))) * oblock.linear(y, W3, b3), W2, b2)
+
+
+def swiglu_no_residual(P, gamma, beta, eps, W1, b1, W3, b3, W2, b2):
+    return oblock.transition_swiglu(P, gamma, beta, eps, W1, b1, W3, b3, W2, b2) - P
+
+
+def test_swiglu_mistakes_caught():
+    _fails(pins.pin_swiglu_library, swiglu_swapped, rng(25))
+    _fails(pins.pin_swiglu_library, swiglu_sigmoid, rng(25))
+    _fails(pins.pin_swiglu_library, swiglu_no_residual, rng(25))
+    _fails(pins.pin_swiglu_zero_gate, swiglu_no_residual, rng(27))
+
+
+def test_silu_mistake_caught():
+    _fails(pins.pin_silu, lambda x: 1 / (1 + np.exp(-x)))

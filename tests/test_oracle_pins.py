@@ -230,3 +230,16 @@ def test_rect_block_square_case_equals_square_block():
     b = oblock.block_packed(lengths, s, w)
     for x, y in ((a.z, b.z), (a.z_tilde, b.z_tilde), (a.m, b.m), (a.s_out, b.s_out)):
         assert np.allclose(x, y, rtol=1e-13, atol=1e-13)
+
+
+def test_silu():
+    pins.pin_silu(oblock.silu)
+
+
+def test_swiglu_library():
+    pins.pin_swiglu_library(oblock.transition_swiglu, rng(25))
+    pins.pin_swiglu_library(oblock.transition_swiglu, rng(26), biases=False)
+
+
+def test_swiglu_zero_gate():
+    pins.pin_swiglu_zero_gate(oblock.transition_swiglu, rng(27))
