@@ -783,8 +783,17 @@ def run_only(args):
             "block": (lambda: nt.block_forward(part, s, wd, z=z, workspace=ws, s_out=so, stream=stream),
                       {k: sum(v[k] for v in bw.values()) for k in ("bytes", "flops")}, "tensor"),
         }
+        if args.swiglu:
+            sw = wl.make_swiglu_weights(cfg.C_z, cfg.H_t, cfg.dtype)
+            d = lambda t: None if t is None else t.to(dev)
+            g1, be1, W1s, W3s, W2s = d(sw.ln_gamma), d(sw.ln_beta), d(sw.W1), d(sw.W3), d(sw.W2)
+            # gate and value GEMMs (2 x 2 C_z H_t) plus the output GEMM (2 H_t C_z) per cell
+            fns["transition"] = (lambda: nt.nt_pair_transition_swiglu(part, z, g1, be1, W1s, None, W3s, None, W2s,
+                                                                       None, out=zt, stream=stream),
+                                 {"bytes": bw["transition"]["bytes"] + cfg.H_t * cfg.C_z * es,
+                                  "flops": 6 * cfg.C_z * cfg.H_t * part.P}, "tensor")
         fn, w, bound = fns[args.only]
-        name = cfg.name
+        name = cfg.name + ("_swiglu" if args.swiglu and args.only == "transition" else "")
     for _ in range(args.warmup):
         flush.fill_(0.0)
         fn()
@@ -826,6 +835,7 @@ def main():
                          "'padsweep' print the packed-vs-padded reports")
     ap.add_argument("--workload", default="pairformer", choices=sorted(WORKLOADS))
     ap.add_argument("--causal", action="store_true", help="with --only attention: the causal mask")
+    ap.add_argument("--swiglu", action="store_true", help="with --only transition: the SwiGLU update")
     args = ap.parse_args()
     if args.only == "packing":
         run_packing(args)

@@ -218,6 +218,25 @@ nt_status nt_pair_transition(const nt_partition* part, nt_dtype dtype, const voi
                              const float* b1, const void* W2, const float* b2, void* stream);
 
 /*
+ * nt_pair_transition_swiglu -- the transition with the SwiGLU update that
+ * [DL] measures (Eq. 1: h is "a SwiGLU feature update"; Appendix A.1:
+ * transition expansion four):
+ *     y  = LN(z)                                      (as nt_pair_transition)
+ *     z~ = z + W2 (SiLU(W1 y + b1) * (W3 y + b3)) + b2,  SiLU(x) = x sigmoid(x)
+ *   W1 [H_t, C_z] the gate projection, W3 [H_t, C_z] the value projection,
+ *   W2 [C_z, H_t]; b1, b3 [H_t] and b2 [C_z] fp32 or NULL.
+ * bf16 with C_z = 128 and H_t a multiple of 64 runs on the tensor cores
+ * (hidden chunks of 64 units, gate and value from one MMA); other shapes
+ * and NT_F32 on CUDA cores.  W3 == NULL is NT_ERR_INVALID.  Other
+ * arguments, errors and in-place use are those of nt_pair_transition.
+ */
+nt_status nt_pair_transition_swiglu(const nt_partition* part, nt_dtype dtype, const void* z_in,
+                                    void* z_out, int32_t C_z, int32_t H_t, const float* ln_gamma,
+                                    const float* ln_beta, float ln_eps, const void* W1,
+                                    const float* b1, const void* W3, const float* b3,
+                                    const void* W2, const float* b2, void* stream);
+
+/*
  * nt_pair_reduce -- the column mean of [DL] Eq. 1, third line, as the
  * segmented sum of Eq. 4 divided by the row length M_i (= N_i for square
  * pairs; [DL] Appendix A.1 for the rectangular variant):

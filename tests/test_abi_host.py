@@ -89,6 +89,9 @@ def test_host_side_rejections(L):
     # bad dtype
     assert lib.nt_pair_transition(P, 7, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, fake,
                                   None, None) == 1
+    # SwiGLU without its value projection
+    assert lib.nt_pair_transition_swiglu(P, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None,
+                                         fake, None, None) == 1
     # W_g without s_out
     assert lib.nt_pair_reduce(P, 1, fake, 128, fake, fake, None, None, None, 384, None) == 1
     # attention: T > 0 without segments; bad head count; T beyond int32

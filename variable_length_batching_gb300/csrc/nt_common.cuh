@@ -118,15 +118,16 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
 cudaError_t launch_broadcast(nt_dtype dt, const float* u, const float* v, const nt_partition* p,
                              int C_z, void* z, cudaStream_t s);
 
+// W3 == NULL: ReLU update; W3 given: SwiGLU update SiLU(W1 x + b1) * (W3 x + b3).
 cudaError_t launch_transition_simt(nt_dtype dt, const void* z_in, void* z_out, int64_t P, int C_z,
                                    int H_t, const float* gamma, const float* beta, float eps,
-                                   const void* W1, const float* b1, const void* W2,
-                                   const float* b2, cudaStream_t s);
-bool transition_tc_supported(nt_dtype dt, int C_z, int H_t);
+                                   const void* W1, const float* b1, const void* W3, const float* b3,
+                                   const void* W2, const float* b2, cudaStream_t s);
+bool transition_tc_supported(nt_dtype dt, int C_z, int H_t, bool glu);
 cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t,
                                  const float* gamma, const float* beta, float eps, const void* W1,
-                                 const float* b1, const void* W2, const float* b2,
-                                 unsigned int* status, cudaStream_t s);
+                                 const float* b1, const void* W3, const float* b3, const void* W2,
+                                 const float* b2, unsigned int* status, cudaStream_t s);
 
 cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m,
                           cudaStream_t s);

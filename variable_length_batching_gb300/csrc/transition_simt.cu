@@ -1,6 +1,8 @@
 // Residual transition on fp32 CUDA cores: z~ = z + W2 ReLU(W1 LN(z) + b1) + b2
 // per packed cell ("DanLing NestedTensor" Eq. 1 second line; section 3.2
-// "Retaining structure through feature transformations").  Used for the fp32
+// "Retaining structure through feature transformations"), or with the
+// SwiGLU update the paper measures (W3 given): the hidden unit is
+// SiLU(W1 x + b1) * (W3 x + b3).  Used for the fp32
 // mode (no fp32 tensor-core path exists) and for widths the tensor-core
 // kernel does not cover.  The cell-wise math never looks at the partition:
 // every packed row is one independent cell.
@@ -12,11 +14,14 @@ namespace {
 constexpr int kRowsPerCta = 8;   // one warp normalises one cell
 constexpr int kThreads = 256;
 
-template <typename T>
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+template <typename T, bool kGLU>
 __global__ void __launch_bounds__(kThreads)
 transition_simt_kernel(const T* z_in, T* z_out, int64_t P, int C_z,
                        int H_t, const float* __restrict__ gamma, const float* __restrict__ beta,
                        float eps, const T* __restrict__ W1, const float* __restrict__ b1,
+                       const T* __restrict__ W3, const float* __restrict__ b3,
                        const T* __restrict__ W2, const float* __restrict__ b2) {
   extern __shared__ float smem[];
   float* xs = smem;                         // [kRowsPerCta][C_z]  LN(z)
@@ -48,20 +53,29 @@ transition_simt_kernel(const T* z_in, T* z_out, int64_t P, int C_z,
       for (int c = lane; c < C_z; c += 32) xr[c] = (xr[c] - mean) * rstd * gamma[c] + beta[c];
     }
     __syncthreads();
-    // hidden = ReLU(W1 x + b1): thread per hidden unit, all rows at once.
+    // hidden = ReLU(W1 x + b1), or SiLU(W1 x + b1) * (W3 x + b3): thread per
+    // hidden unit, all rows at once.
     for (int h = threadIdx.x; h < H_t; h += kThreads) {
-      float acc[kRowsPerCta];
+      float acc[kRowsPerCta], accv[kRowsPerCta];
 #pragma unroll
-      for (int r = 0; r < kRowsPerCta; ++r) acc[r] = 0.f;
+      for (int r = 0; r < kRowsPerCta; ++r) { acc[r] = 0.f; accv[r] = 0.f; }
       const T* w = W1 + (int64_t)h * C_z;
+      const T* w3 = kGLU ? W3 + (int64_t)h * C_z : nullptr;
       for (int c = 0; c < C_z; ++c) {
         const float wc = to_f32(w[c]);
 #pragma unroll
         for (int r = 0; r < kRowsPerCta; ++r) acc[r] = fmaf(xs[r * C_z + c], wc, acc[r]);
+        if (kGLU) {
+          const float vc = to_f32(w3[c]);
+#pragma unroll
+          for (int r = 0; r < kRowsPerCta; ++r) accv[r] = fmaf(xs[r * C_z + c], vc, accv[r]);
+        }
       }
       const float bias = b1 ? b1[h] : 0.f;
+      const float bias3 = (kGLU && b3) ? b3[h] : 0.f;
 #pragma unroll
-      for (int r = 0; r < kRowsPerCta; ++r) hs[r * H_t + h] = fmaxf(acc[r] + bias, 0.f);
+      for (int r = 0; r < kRowsPerCta; ++r)
+        hs[r * H_t + h] = kGLU ? silu(acc[r] + bias) * (accv[r] + bias3) : fmaxf(acc[r] + bias, 0.f);
     }
     __syncthreads();
     // z~ = z + W2 hidden + b2: thread per output feature.
@@ -91,30 +105,37 @@ size_t transition_simt_smem(int C_z, int H_t) {
   return sizeof(float) * kRowsPerCta * (size_t)(C_z + H_t);
 }
 
-cudaError_t launch_transition_simt(nt_dtype dt, const void* z_in, void* z_out, int64_t P, int C_z,
-                                   int H_t, const float* gamma, const float* beta, float eps,
-                                   const void* W1, const float* b1, const void* W2,
-                                   const float* b2, cudaStream_t s) {
-  if (P == 0) return cudaSuccess;
+namespace {
+
+template <typename T, bool kGLU>
+cudaError_t launch_t(const void* z_in, void* z_out, int64_t P, int C_z, int H_t, const float* gamma,
+                     const float* beta, float eps, const void* W1, const float* b1, const void* W3,
+                     const float* b3, const void* W2, const float* b2, cudaStream_t s) {
   const size_t smem = transition_simt_smem(C_z, H_t);
   const int sms = sm_count();
   const int64_t ctas = (P + kRowsPerCta - 1) / kRowsPerCta;
   const int grid = (int)min64(ctas, (int64_t)sms * 8);
-  cudaError_t e;
-  if (dt == NT_BF16) {
-    e = cudaFuncSetAttribute(transition_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    transition_simt_kernel<bf16><<<grid, kThreads, smem, s>>>(
-        (const bf16*)z_in, (bf16*)z_out, P, C_z, H_t, gamma, beta, eps, (const bf16*)W1, b1,
-        (const bf16*)W2, b2);
-  } else {
-    e = cudaFuncSetAttribute(transition_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    transition_simt_kernel<float><<<grid, kThreads, smem, s>>>(
-        (const float*)z_in, (float*)z_out, P, C_z, H_t, gamma, beta, eps, (const float*)W1, b1,
-        (const float*)W2, b2);
-  }
+  cudaError_t e = cudaFuncSetAttribute(transition_simt_kernel<T, kGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  transition_simt_kernel<T, kGLU><<<grid, kThreads, smem, s>>>((const T*)z_in, (T*)z_out, P, C_z, H_t, gamma, beta,
+                                                               eps, (const T*)W1, b1, (const T*)W3, b3,
+                                                               (const T*)W2, b2);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_transition_simt(nt_dtype dt, const void* z_in, void* z_out, int64_t P, int C_z,
+                                   int H_t, const float* gamma, const float* beta, float eps,
+                                   const void* W1, const float* b1, const void* W3, const float* b3,
+                                   const void* W2, const float* b2, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  if (dt == NT_BF16)
+    return W3 ? launch_t<bf16, true>(z_in, z_out, P, C_z, H_t, gamma, beta, eps, W1, b1, W3, b3, W2, b2, s)
+              : launch_t<bf16, false>(z_in, z_out, P, C_z, H_t, gamma, beta, eps, W1, b1, W3, b3, W2, b2, s);
+  return W3 ? launch_t<float, true>(z_in, z_out, P, C_z, H_t, gamma, beta, eps, W1, b1, W3, b3, W2, b2, s)
+            : launch_t<float, false>(z_in, z_out, P, C_z, H_t, gamma, beta, eps, W1, b1, W3, b3, W2, b2, s);
 }
 
 }  // namespace nt

@@ -1,5 +1,8 @@
 // Residual transition on the tcgen05 tensor cores, bf16 in / fp32 accumulate:
 //     z~ = z + W2 ReLU(W1 LN(z) + b1) + b2        (one packed cell per row)
+// or, with the SwiGLU update the paper measures (Eq. 1: h is a SwiGLU
+// feature update; a template flag),
+//     z~ = z + W2 (SiLU(W1 LN(z) + b1) * (W3 LN(z) + b3)) + b2.
 // "DanLing NestedTensor" Eq. 1 second line; section 3.3 "Dense work across
 // valid positions": the feature transform is a dense contraction over the
 // sum N_i^2 packed rows, so it runs as a GEMM pair with the LayerNorm fused
@@ -19,6 +22,11 @@
 //                 +b2 + residual -> bf16 into H -> TMA store.
 // TMEM (512 columns): acc1[s] = GEMM1 chunk of sub-tile s at 128*s,
 // acc2[s] = output accumulator of sub-tile s at 256 + 128*s.
+// SwiGLU: hidden chunks are 64 units wide; a GEMM1 weight tile stacks those
+// 64 rows of W1 (gate) over the same 64 rows of W3 (value), so one N = 128
+// MMA leaves gate and value side by side in acc1, the epilogue writes the
+// 64-wide product SiLU(gate + b1) * (value + b3), and GEMM2 contracts it
+// with a 128 x 64 slice of W2 (K = 64).
 // Every operand tile is K-major with the 128-byte swizzle that TMA writes.
 #include <cudaTypedefs.h>
 
@@ -75,12 +83,16 @@ __device__ __forceinline__ void weight_order(int q, int NC, bool* is_w1, int* c)
   *c = NC - 1;
 }
 
+template <bool kGLU>
 __global__ void __launch_bounds__(kThreads, 1)
 transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_constant__ CUtensorMap tm_zout,
-                     const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
-                     const bf16* z_in, int64_t P, int H_t, const float* __restrict__ gamma,
-                     const float* __restrict__ beta, float eps, const float* __restrict__ b1,
-                     const float* __restrict__ b2, unsigned int* status) {
+                     const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w3,
+                     const __grid_constant__ CUtensorMap tm_w2, const bf16* z_in, int64_t P, int H_t,
+                     const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
+                     const float* __restrict__ b1, const float* __restrict__ b3, const float* __restrict__ b2,
+                     unsigned int* status) {
+  // hidden units per chunk; GEMM2 contracts kHid per chunk
+  constexpr int kHid = kGLU ? 64 : kChunk;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sA = smem + kOffA;
@@ -92,7 +104,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
   volatile int* abort_flag = &bar.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NC = H_t / kChunk;
+  const int NC = H_t / kHid;
   const int64_t num_tiles = (P + kTileRows - 1) / kTileRows;
 
   if (threadIdx.x == 0) {
@@ -122,6 +134,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_zin); prefetch_tmap(&tm_w1); prefetch_tmap(&tm_w2); prefetch_tmap(&tm_zout);
+      if (kGLU) prefetch_tmap(&tm_w3);
       int load_idx = 0;
       int last_tile_j = -1;
       bool ok = true;
@@ -139,14 +152,29 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           weight_order(q, NC, &w1, &c);
           const int stage = load_idx % kStages, round = load_idx / kStages;
           if (!(ok = mbar_wait(&bar.w_empty[stage], (round & 1) ^ 1, abort_flag, status))) break;
-          mbar_arrive_expect_tx(&bar.w_full[stage], kWBytes);
           uint8_t* dst = sW + stage * kWBytes;
-          if (w1) {
-            tma_load_2d(dst, &tm_w1, &bar.w_full[stage], 0, c * kChunk);
-            tma_load_2d(dst + kBlockBytes, &tm_w1, &bar.w_full[stage], 64, c * kChunk);
+          if (kGLU) {
+            if (w1) {
+              // rows 0-63: W1 (gate) rows of chunk c; rows 64-127: W3 (value) rows
+              mbar_arrive_expect_tx(&bar.w_full[stage], kWBytes);
+              for (int kb = 0; kb < 2; ++kb) {
+                tma_load_2d(dst + kb * kBlockBytes, &tm_w1, &bar.w_full[stage], kb * 64, c * kHid);
+                tma_load_2d(dst + kb * kBlockBytes + kBlockBytes / 2, &tm_w3, &bar.w_full[stage], kb * 64,
+                            c * kHid);
+              }
+            } else {
+              mbar_arrive_expect_tx(&bar.w_full[stage], kBlockBytes);    // W2[:, 64c : 64c + 64]
+              tma_load_2d(dst, &tm_w2, &bar.w_full[stage], c * kHid, 0);
+            }
           } else {
-            tma_load_2d(dst, &tm_w2, &bar.w_full[stage], c * kChunk, 0);
-            tma_load_2d(dst + kBlockBytes, &tm_w2, &bar.w_full[stage], c * kChunk + 64, 0);
+            mbar_arrive_expect_tx(&bar.w_full[stage], kWBytes);
+            if (w1) {
+              tma_load_2d(dst, &tm_w1, &bar.w_full[stage], 0, c * kChunk);
+              tma_load_2d(dst + kBlockBytes, &tm_w1, &bar.w_full[stage], 64, c * kChunk);
+            } else {
+              tma_load_2d(dst, &tm_w2, &bar.w_full[stage], c * kChunk, 0);
+              tma_load_2d(dst + kBlockBytes, &tm_w2, &bar.w_full[stage], c * kChunk + 64, 0);
+            }
           }
           ++load_idx;
         }
@@ -209,7 +237,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
             if (c == 0 && !(ok = mbar_wait(&bar.acc2_empty[s], (j & 1) ^ 1, abort_flag, status))) break;
             if (!(ok = mbar_wait(&bar.h_full[s], it & 1, abort_flag, status))) break;
             tc_fence_after();
-            for (int k = 0; k < kChunk / 16; ++k) {
+            for (int k = 0; k < kHid / 16; ++k) {
               const uint32_t koff = (k >> 2) * kBlockBytes + (k & 3) * 32;
               mma_bf16(tmem + 256 + 128 * s, sdesc_k128(h_base + s * kSubBytes + koff), sdesc_k128(wsm + koff),
                        idesc, (c > 0 || k > 0) ? 1u : 0u);
@@ -294,22 +322,49 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         if (c == 0 && j > 0 && !(ok = mbar_wait_warp(&bar.store_done[s], (j - 1) & 1, abort_flag, status))) break;
         tc_fence_after();
         __syncwarp();   // tcgen05.ld is warp-collective: reconverge after the per-lane waits
+        if (kGLU) {
+          // acc1 columns 0-63 hold the gate, 64-127 the value of hidden units
+          // 64c .. 64c + 63: H[s] gets SiLU(gate + b1) * (value + b3)
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float v[32];
-          tmem_ld32(tmem + lane_addr + 128 * s + 32 * g, v);
-          tmem_ld_wait();
-          uint32_t packed[16];
+          for (int g = 0; g < 2; ++g) {
+            float gv[32], vv[32];
+            tmem_ld32(tmem + lane_addr + 128 * s + 32 * g, gv);
+            tmem_ld32(tmem + lane_addr + 128 * s + 64 + 32 * g, vv);
+            tmem_ld_wait();
+            uint32_t packed[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int col = c * kChunk + 32 * g + 2 * e;
-            const float bb0 = b1 ? __ldg(b1 + col) : 0.f, bb1 = b1 ? __ldg(b1 + col + 1) : 0.f;
-            packed[e] = pack_bf16x2(fmaxf(v[2 * e] + bb0, 0.f), fmaxf(v[2 * e + 1] + bb1, 0.f));
+            for (int e = 0; e < 16; ++e) {
+              const int col = c * kHid + 32 * g + 2 * e;
+              const float g0 = gv[2 * e] + (b1 ? __ldg(b1 + col) : 0.f);
+              const float g1 = gv[2 * e + 1] + (b1 ? __ldg(b1 + col + 1) : 0.f);
+              const float v0 = vv[2 * e] + (b3 ? __ldg(b3 + col) : 0.f);
+              const float v1 = vv[2 * e + 1] + (b3 ? __ldg(b3 + col + 1) : 0.f);
+              packed[e] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * v0,
+                                      __fdividef(g1, 1.0f + __expf(-g1)) * v1);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(hs + swz128_offset(r, 32 * g + 8 * u, kSubRows)) =
+                  make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
           }
+        } else {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(hs + swz128_offset(r, 32 * g + 8 * u, kSubRows)) =
-                make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+          for (int g = 0; g < 4; ++g) {
+            float v[32];
+            tmem_ld32(tmem + lane_addr + 128 * s + 32 * g, v);
+            tmem_ld_wait();
+            uint32_t packed[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int col = c * kChunk + 32 * g + 2 * e;
+              const float bb0 = b1 ? __ldg(b1 + col) : 0.f, bb1 = b1 ? __ldg(b1 + col + 1) : 0.f;
+              packed[e] = pack_bf16x2(fmaxf(v[2 * e] + bb0, 0.f), fmaxf(v[2 * e + 1] + bb1, 0.f));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(hs + swz128_offset(r, 32 * g + 8 * u, kSubRows)) =
+                  make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+          }
         }
         tc_fence_before();
         mbar_arrive(&bar.acc1_empty[s]);
@@ -390,14 +445,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [outer, inner] matrix, box {64, 128},
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix, box {64, rows},
 // 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer) {
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -406,27 +461,32 @@ bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer)
 
 }  // namespace
 
-bool transition_tc_supported(nt_dtype dt, int C_z, int H_t) {
-  return dt == NT_BF16 && C_z == kCz && H_t >= kChunk && H_t % kChunk == 0 && H_t <= 16384;
+bool transition_tc_supported(nt_dtype dt, int C_z, int H_t, bool glu) {
+  const int unit = glu ? 64 : kChunk;
+  return dt == NT_BF16 && C_z == kCz && H_t >= unit && H_t % unit == 0 && H_t <= 16384;
 }
 
 cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t,
                                  const float* gamma, const float* beta, float eps, const void* W1,
-                                 const float* b1, const void* W2, const float* b2,
-                                 unsigned int* status, cudaStream_t s) {
+                                 const float* b1, const void* W3, const float* b3, const void* W2,
+                                 const float* b2, unsigned int* status, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   if (P > 0x7fffffffLL - kTileRows) return cudaErrorInvalidValue;
-  CUtensorMap m_zin, m_zout, m_w1, m_w2;
+  const bool glu = W3 != nullptr;
+  CUtensorMap m_zin, m_zout, m_w1, m_w3, m_w2;
+  // SwiGLU: W1 and W3 are read as 64-row halves of a weight tile
+  const uint32_t w_rows = glu ? 64 : 128;
   if (!make_map(&m_zin, z_in, C_z, (uint64_t)P) || !make_map(&m_zout, z_out, C_z, (uint64_t)P) ||
-      !make_map(&m_w1, W1, C_z, H_t) || !make_map(&m_w2, W2, H_t, C_z))
+      !make_map(&m_w1, W1, C_z, H_t, w_rows) || !make_map(&m_w3, glu ? W3 : W1, C_z, H_t, w_rows) ||
+      !make_map(&m_w2, W2, H_t, C_z))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(transition_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  auto kern = glu ? transition_tc_kernel<true> : transition_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t tiles = (P + kTileRows - 1) / kTileRows;
   const int grid = (int)min64(tiles, (int64_t)sm_count());
-  transition_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(m_zin, m_zout, m_w1, m_w2, (const bf16*)z_in, P, H_t,
-                                                          gamma, beta, eps, b1, b2, status);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(m_zin, m_zout, m_w1, m_w3, m_w2, (const bf16*)z_in, P, H_t, gamma, beta,
+                                          eps, b1, b3, b2, status);
   return cudaGetLastError();
 }
 

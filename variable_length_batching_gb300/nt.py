@@ -50,6 +50,8 @@ SIGNATURES = {
     "nt_pair_broadcast": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P, _SZ, _P]),
     "nt_pair_broadcast_noalloc": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _P, _P]),
     "nt_pair_transition": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P]),
+    "nt_pair_transition_swiglu": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
+                                         _P]),
     "nt_pair_reduce": (_I32, [_PP, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P]),
     "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P]),
     "nt_varlen_attn_qk": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _F, _I32,
@@ -254,6 +256,27 @@ def nt_pair_transition(part: Partition, z: torch.Tensor, ln_gamma: torch.Tensor,
                                   _ptr(_f32(ln_gamma)), _ptr(_f32(ln_beta)), ln_eps, _ptr(W1),
                                   _ptr(_f32(b1)), _ptr(W2), _ptr(_f32(b2)), _stream(stream))
     _check(st, "nt_pair_transition")
+    return out
+
+
+def nt_pair_transition_swiglu(part: Partition, z: torch.Tensor, ln_gamma: torch.Tensor, ln_beta: torch.Tensor,
+                              W1: torch.Tensor, b1: Optional[torch.Tensor], W3: torch.Tensor,
+                              b3: Optional[torch.Tensor], W2: torch.Tensor, b2: Optional[torch.Tensor],
+                              ln_eps: float = 1e-5, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """z~ = z + W2 (SiLU(W1 LN(z) + b1) * (W3 LN(z) + b3)) + b2 per cell."""
+    P, C_z = z.shape
+    H_t = W1.shape[0]
+    if P != part.P:
+        raise ValueError(f"z has {P} cells, the partition {part.P}")
+    if tuple(W1.shape) != (H_t, C_z) or tuple(W3.shape) != (H_t, C_z) or tuple(W2.shape) != (C_z, H_t):
+        raise ValueError("W1 and W3 must be (H_t, C_z) and W2 (C_z, H_t)")
+    if out is None:
+        out = torch.empty_like(z)
+    st = lib().nt_pair_transition_swiglu(ctypes.byref(part.c), _dtype(z), _ptr(z), _ptr(out), C_z, H_t,
+                                         _ptr(_f32(ln_gamma)), _ptr(_f32(ln_beta)), ln_eps, _ptr(W1),
+                                         _ptr(_f32(b1)), _ptr(W3), _ptr(_f32(b3)), _ptr(W2), _ptr(_f32(b2)),
+                                         _stream(stream))
+    _check(st, "nt_pair_transition_swiglu")
     return out
 
 

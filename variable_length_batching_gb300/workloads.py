@@ -138,6 +138,40 @@ class BlockWeights:
 
 
 @dataclass
+class SwiGLUWeights:
+    """The SwiGLU transition's parameters: gate W1 and value W3 (H_t, C_z),
+    output W2 (C_z, H_t), LN gamma/beta and optional fp32 biases."""
+    ln_gamma: torch.Tensor
+    ln_beta: torch.Tensor
+    W1: torch.Tensor
+    b1: Optional[torch.Tensor]
+    W3: torch.Tensor
+    b3: Optional[torch.Tensor]
+    W2: torch.Tensor
+    b2: Optional[torch.Tensor]
+
+
+def make_swiglu_weights(C_z: int, H_t: int, dtype: str, biases: bool = False, seed: int = 0) -> SwiGLUWeights:
+    """N(0, 1/fan_in) weights drawn in the order W1, W3, W2 (then biases,
+    gamma, beta when ``biases``)."""
+    rng = np.random.default_rng(seed)
+    W1 = to_io(_normal(rng, (H_t, C_z), 1.0 / C_z), dtype)
+    W3 = to_io(_normal(rng, (H_t, C_z), 1.0 / C_z), dtype)
+    W2 = to_io(_normal(rng, (C_z, H_t), 1.0 / H_t), dtype)
+    if biases:
+        b1 = torch.from_numpy(_normal(rng, (H_t,), 0.25))
+        b3 = torch.from_numpy(_normal(rng, (H_t,), 0.25))
+        b2 = torch.from_numpy(_normal(rng, (C_z,), 0.25))
+        gamma = torch.from_numpy(1.0 + _normal(rng, (C_z,), 0.04))
+        beta = torch.from_numpy(_normal(rng, (C_z,), 0.04))
+    else:
+        b1 = b3 = b2 = None
+        gamma = torch.ones(C_z, dtype=torch.float32)
+        beta = torch.zeros(C_z, dtype=torch.float32)
+    return SwiGLUWeights(gamma, beta, W1, b1, W3, b3, W2, b2)
+
+
+@dataclass
 class BlockInputs:
     cfg: BlockConfig
     lengths: np.ndarray            # int32 (B,)
