@@ -767,6 +767,8 @@ def run_only(args):
         part = nt.nt_partition_build(lengths)
         z = nt.nt_pair_broadcast(part, s, s, wd.W_a, wd.W_b)
         ws = torch.empty(nt.nt_pair_broadcast_workspace_bytes(part.T, cfg.C_z), dtype=torch.uint8, device=dev)
+        wsf = torch.empty(nt.lib().nt_pair_block_fused_workspace_bytes(part.T, part.T, cfg.C_z), dtype=torch.uint8,
+                          device=dev)
         zt = torch.empty_like(z)
         m = torch.empty(part.T, cfg.C_z, dtype=z.dtype, device=dev)
         so = torch.empty(part.T, cfg.C_s, dtype=z.dtype, device=dev)
@@ -782,6 +784,11 @@ def run_only(args):
                        bw["reduce"], "hbm"),
             "block": (lambda: nt.block_forward(part, s, wd, z=z, workspace=ws, s_out=so, stream=stream),
                       {k: sum(v[k] for v in bw.values()) for k in ("bytes", "flops")}, "tensor"),
+            # one pass: z~ written once (256 B/cell), singles-sized traffic besides
+            "fused": (lambda: nt.nt_pair_block_fused(part, s, s, wd, z=zt, m=m, s_out=so, workspace=wsf,
+                                                     stream=stream),
+                      {"bytes": part.P * cfg.C_z * es + bw["reduce"]["bytes"] - part.P * cfg.C_z * es,
+                       "flops": bw["transition"]["flops"]}, "tensor"),
         }
         if args.swiglu:
             sw = wl.make_swiglu_weights(cfg.C_z, cfg.H_t, cfg.dtype)
@@ -829,7 +836,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
-                    choices=["partition", "broadcast", "transition", "reduce", "block", "attention",
+                    choices=["partition", "broadcast", "transition", "reduce", "block", "fused", "attention",
                              "packing", "padsweep", "rect"],
                     help="time one call on one workload instead of the whole step; 'packing' and "
                          "'padsweep' print the packed-vs-padded reports")

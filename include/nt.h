@@ -253,6 +253,40 @@ nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z
                          void* m, const void* W_g, const float* b_g, const void* s_in,
                          void* s_out, int32_t C_s, void* stream);
 
+/* Bytes of device workspace nt_pair_block_fused needs: u (T x C_z), v
+ * (T_cols x C_z) and the fp32 row sums (T x C_z), (2 T + T_cols) * C_z * 4. */
+size_t nt_pair_block_fused_workspace_bytes(int64_t T, int64_t T_cols, int32_t C_z);
+
+/*
+ * nt_pair_block_fused -- the whole single -> pair -> single block of [DL]
+ * Eq. 1 in one pass over the pair state: the broadcast is computed inside
+ * the transition's prologue and the row sums of Eq. 4 inside its epilogue,
+ * so z is never written to HBM and z~ is written once (256 bytes per cell in
+ * bf16 instead of the 1,024 of the three separate calls).
+ *     u = s_left W_a^T, v = s_right W_b^T
+ *     z~[cell (a, b) of sample i] = transition(u[cu_i + a] + v[col_cu_i + b])
+ *     m = column mean of z~ (divided by M_i);  s_out = s_left + m W_g^T + b_g
+ * The transition is the ReLU one (W3 == NULL) or the SwiGLU one (W3 given),
+ * with the arguments of nt_pair_transition / nt_pair_transition_swiglu.
+ *   part      partition with row splits; square or rectangular.
+ *   z_out     [P, C_z] out: z~ (the pair state the block returns).
+ *   m         [T, C_z] out.   s_out [T, C_s] out when W_g is given.
+ *   workspace >= nt_pair_block_fused_workspace_bytes(T, T_cols, C_z) bytes,
+ *             16-byte aligned.
+ * z~ equals what the three calls produce bit for bit (same roundings: z is
+ * rounded to bf16 before the LayerNorm and the residual); m differs only in
+ * the order of the fp32 row sums.  bf16 with C_z = 128 runs fused on the
+ * tensor cores; other shapes run the three calls' kernels in sequence.
+ * Asynchronous; errors as for the three calls.
+ */
+nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const void* s_left,
+                              const void* s_right, int32_t C_s, const void* W_a, const void* W_b,
+                              int32_t C_z, int32_t H_t, const float* ln_gamma, const float* ln_beta,
+                              float ln_eps, const void* W1, const float* b1, const void* W3,
+                              const float* b3, const void* W2, const float* b2, const void* W_g,
+                              const float* b_g, void* z_out, void* m, void* s_out, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /*
  * nt_varlen_attn -- softmax attention restricted to each cu_seqlens segment
  * ([VA] "What it is", "How it works"; [DL] section 3.3 "Attention through

@@ -133,6 +133,28 @@ nt_status pair_transition(const nt_partition* part, nt_dtype dtype, const void* 
   return NT_OK;
 }
 
+// u = s_left W_a^T (T rows), v = s_right W_b^T (T_cols rows), fp32.
+cudaError_t project_uv(const nt_partition* part, nt_dtype dtype, const void* s_left, const void* s_right,
+                       int32_t C_s, const void* W_a, const void* W_b, int32_t C_z, float* u, float* v,
+                       cudaStream_t s) {
+  const int64_t T_cols = t_cols_of(part);
+  LinearProblem probs[2] = {{s_left, W_a, nullptr, nullptr, u}, {s_right, W_b, nullptr, nullptr, v}};
+  if (T_cols == part->T)   // one launch for both projections
+    return linear_tc_supported(dtype, part->T, C_z, C_s)
+               ? launch_linear_tc(1, probs, 2, part->T, C_z, C_s, status_word(), s)
+               : launch_linear(dtype, 1, probs, 2, part->T, C_z, C_s, s);
+  // rectangular: row and column singles have different row counts
+  const int64_t rows[2] = {part->T, T_cols};
+  cudaError_t e = cudaSuccess;
+  for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+    if (rows[k] == 0) continue;
+    e = linear_tc_supported(dtype, rows[k], C_z, C_s)
+            ? launch_linear_tc(1, &probs[k], 1, rows[k], C_z, C_s, status_word(), s)
+            : launch_linear(dtype, 1, &probs[k], 1, rows[k], C_z, C_s, s);
+  }
+  return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -273,23 +295,7 @@ nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* u = static_cast<float*>(workspace);
   float* v = u + part->T * (int64_t)C_z;
-  LinearProblem probs[2] = {{s_left, W_a, nullptr, nullptr, u}, {s_right, W_b, nullptr, nullptr, v}};
-  cudaError_t e = cudaSuccess;
-  if (T_cols == part->T) {
-    // one launch for both projections
-    e = linear_tc_supported(dtype, part->T, C_z, C_s)
-            ? launch_linear_tc(1, probs, 2, part->T, C_z, C_s, status_word(), s)
-            : launch_linear(dtype, 1, probs, 2, part->T, C_z, C_s, s);
-  } else {
-    // rectangular: row and column singles have different row counts
-    const int64_t rows[2] = {part->T, T_cols};
-    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
-      if (rows[k] == 0) continue;
-      e = linear_tc_supported(dtype, rows[k], C_z, C_s)
-              ? launch_linear_tc(1, &probs[k], 1, rows[k], C_z, C_s, status_word(), s)
-              : launch_linear(dtype, 1, &probs[k], 1, rows[k], C_z, C_s, s);
-    }
-  }
+  cudaError_t e = project_uv(part, dtype, s_left, s_right, C_s, W_a, W_b, C_z, u, v, s);
   if (e != cudaSuccess) return cuda_fail(e, "projection launch");
   e = launch_broadcast(dtype, u, v, part, C_z, z, s);
   if (e != cudaSuccess) return cuda_fail(e, "broadcast launch");
@@ -333,6 +339,74 @@ nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z
   if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
   if (W_g) {
     LinearProblem prob = {m, W_g, b_g, s_in, s_out};
+    e = linear_tc_supported(dtype, part->T, C_s, C_z)
+            ? launch_linear_tc(0, &prob, 1, part->T, C_s, C_z, status_word(), s)
+            : launch_linear(dtype, dtype == NT_F32, &prob, 1, part->T, C_s, C_z, s);
+    if (e != cudaSuccess) return cuda_fail(e, "g projection launch");
+  }
+  return NT_OK;
+}
+
+size_t nt_pair_block_fused_workspace_bytes(int64_t T, int64_t T_cols, int32_t C_z) {
+  if (T < 0 || T_cols < 0 || C_z < 0) return 0;
+  return (size_t)(2 * T + T_cols) * (size_t)C_z * sizeof(float);
+}
+
+nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const void* s_left, const void* s_right,
+                              int32_t C_s, const void* W_a, const void* W_b, int32_t C_z, int32_t H_t,
+                              const float* ln_gamma, const float* ln_beta, float ln_eps, const void* W1,
+                              const float* b1, const void* W3, const float* b3, const void* W2, const float* b2,
+                              const void* W_g, const float* b_g, void* z_out, void* m, void* s_out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  nt_status st = check_partition(part, true);
+  if (st != NT_OK) return st;
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (!width_ok(dtype, C_s) || !width_ok(dtype, C_z) || !width_ok(dtype, H_t))
+    return fail(NT_ERR_UNSUPPORTED, "C_s=%d, C_z=%d, H_t=%d must be positive multiples of %d", C_s, C_z, H_t,
+                dtype == NT_BF16 ? 8 : 4);
+  if (!s_left || !s_right || !W_a || !W_b || !ln_gamma || !ln_beta || !W1 || !W2 || !z_out || !m || !workspace)
+    return fail(NT_ERR_INVALID, "NULL pointer");
+  if (W_g && !s_out) return fail(NT_ERR_INVALID, "W_g given: s_out must be set");
+  if (!aligned16(s_left) || !aligned16(s_right) || !aligned16(W_a) || !aligned16(W_b) || !aligned16(W1) ||
+      !aligned16(W2) || !aligned16(W3) || !aligned16(z_out) || !aligned16(m) || !aligned16(workspace) ||
+      !aligned16(W_g) || !aligned16(s_out) || !aligned16(ln_gamma) || !aligned16(ln_beta) || !aligned16(b1) ||
+      !aligned16(b2) || !aligned16(b3) || !aligned16(b_g))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  if (!(ln_eps >= 0.0f)) return fail(NT_ERR_INVALID, "ln_eps must be >= 0");
+  const int64_t T_cols = t_cols_of(part);
+  const size_t need = nt_pair_block_fused_workspace_bytes(part->T, T_cols, C_z);
+  if (workspace_bytes < need)
+    return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  if (part->T == 0) return NT_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!transition_tc_supported(dtype, C_z, H_t, W3 != nullptr)) {
+    // the same block through the three pair calls' kernels
+    st = nt_pair_broadcast(part, dtype, s_left, s_right, C_s, W_a, W_b, C_z, z_out, workspace, workspace_bytes,
+                           stream);
+    if (st != NT_OK) return st;
+    st = W3 ? nt_pair_transition_swiglu(part, dtype, z_out, z_out, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W3,
+                                        b3, W2, b2, stream)
+            : nt_pair_transition(part, dtype, z_out, z_out, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W2, b2,
+                                 stream);
+    if (st != NT_OK) return st;
+    return nt_pair_reduce(part, dtype, z_out, C_z, m, W_g, b_g, s_left, s_out, C_s, stream);
+  }
+  float* u = static_cast<float*>(workspace);
+  float* v = u + part->T * (int64_t)C_z;
+  float* m_acc = v + T_cols * (int64_t)C_z;
+  cudaError_t e = project_uv(part, dtype, s_left, s_right, C_s, W_a, W_b, C_z, u, v, s);
+  if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+  e = cudaMemsetAsync(m_acc, 0, (size_t)part->T * C_z * sizeof(float), s);
+  if (e != cudaSuccess) return cuda_fail(e, "row-sum clear");
+  if (part->P > 0) {
+    e = launch_block_fused_tc(u, v, part, z_out, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W3, b3, W2, b2, m_acc,
+                              status_word(), s);
+    if (e != cudaSuccess) return cuda_fail(e, "fused block launch");
+  }
+  e = launch_mean_finish(dtype, m_acc, part, C_z, m, s);
+  if (e != cudaSuccess) return cuda_fail(e, "row mean launch");
+  if (W_g) {
+    LinearProblem prob = {m, W_g, b_g, s_left, s_out};
     e = linear_tc_supported(dtype, part->T, C_s, C_z)
             ? launch_linear_tc(0, &prob, 1, part->T, C_s, C_z, status_word(), s)
             : launch_linear(dtype, dtype == NT_F32, &prob, 1, part->T, C_s, C_z, s);

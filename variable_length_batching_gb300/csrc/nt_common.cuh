@@ -131,6 +131,14 @@ cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C
 
 cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m,
                           cudaStream_t s);
+// Fused block: the transition kernel building z from u, v and summing rows
+// into m_acc (fp32, zeroed by the caller); then m = m_acc / M_i.
+cudaError_t launch_block_fused_tc(const float* u, const float* v, const nt_partition* part, void* z_out, int C_z,
+                                  int H_t, const float* gamma, const float* beta, float eps, const void* W1,
+                                  const float* b1, const void* W3, const float* b3, const void* W2, const float* b2,
+                                  float* m_acc, unsigned int* status, cudaStream_t s);
+cudaError_t launch_mean_finish(nt_dtype dt, const float* m_acc, const nt_partition* p, int C_z, void* m,
+                               cudaStream_t s);
 
 // One varlen attention problem: queries [cu_q[b], cu_q[b+1]) attend to keys
 // [cu_k[b], cu_k[b+1]) (cu_k == cu_q for self-attention); causal masks key j

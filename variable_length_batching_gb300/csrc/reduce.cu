@@ -80,7 +80,36 @@ __global__ void reduce_kernel_f32_scalar(const float* __restrict__ z, const int3
   }
 }
 
+// m = m_acc / M_i for every single row (zero when M_i = 0), in the I/O dtype:
+// the division of the fused block's column sums (Eq. 4, then the mean).
+template <typename TOut>
+__global__ void mean_finish_kernel(const float* __restrict__ m_acc, const int32_t* __restrict__ row_len,
+                                   const int32_t* __restrict__ row_sample, int64_t T, int C_z, TOut* __restrict__ m) {
+  const int64_t vecs = T * (C_z / 4);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < vecs; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / (C_z / 4);
+    const int64_t n = row_len[row_sample[r]];
+    const float inv = n > 0 ? 1.0f / (float)n : 0.f;
+    const float4 a = reinterpret_cast<const float4*>(m_acc)[e];
+    const float o[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) m[4 * e + t] = from_f32<TOut>(o[t]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_mean_finish(nt_dtype dt, const float* m_acc, const nt_partition* p, int C_z, void* m,
+                               cudaStream_t s) {
+  if (p->T == 0) return cudaSuccess;
+  const int64_t vecs = p->T * (C_z / 4);
+  const int grid = (int)min64((vecs + 255) / 256, (int64_t)sm_count() * 16);
+  if (dt == NT_BF16)
+    mean_finish_kernel<bf16><<<grid, 256, 0, s>>>(m_acc, col_lengths_of(p), p->row_sample, p->T, C_z, (bf16*)m);
+  else
+    mean_finish_kernel<float><<<grid, 256, 0, s>>>(m_acc, col_lengths_of(p), p->row_sample, p->T, C_z, (float*)m);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m,
                           cudaStream_t s) {

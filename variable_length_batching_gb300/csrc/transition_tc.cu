@@ -28,6 +28,17 @@
 // 64-wide product SiLU(gate + b1) * (value + b3), and GEMM2 contracts it
 // with a 128 x 64 slice of W2 (K = 64).
 // Every operand tile is K-major with the 128-byte swizzle that TMA writes.
+//
+// Fused block (a second template flag; "DanLing NestedTensor" Eq. 1 as one
+// pass over the pair state): z never exists in HBM.  The LayerNorm warps
+// build each tile as bf16(u[row] + v[col]) from the two projected single
+// representations (fp32, L2-resident), with (row, col) of packed cell p
+// found from the partition's row splits; the output epilogue recomputes the
+// same bf16 z for the residual; and after staging z~ for its TMA store the
+// epilogue threads sum their feature column over the tile's cells, flushing
+// one fp32 atomic add per pair row touched into m_acc (Eq. 4's column sum).
+// HBM traffic per cell drops from 1,024 bytes (z written, read; z~
+// written, read) to the 256 bytes of z~.
 #include <cudaTypedefs.h>
 
 #include "tc_ptx.cuh"
@@ -62,11 +73,44 @@ struct Bars {
   uint64_t h_full[2], h_empty[2];
   uint64_t acc2_full[2], acc2_empty[2];
   uint64_t out_ready[2], store_done[2];
+  uint64_t colsum_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// Inputs of the fused block: u, v (fp32, C_z wide), the partition's row
+// splits and owners, the column offsets, and the fp32 accumulator of row sums.
+struct FusedIn {
+  const float* u;
+  const float* v;
+  const int64_t* row_start;
+  const int32_t* row_sample;
+  const int32_t* col_cu;
+  int64_t T;
+  float* m_acc;
+};
+
+// Pair row holding packed cell p (< P): the last r with row_start[r] <= p.
+__device__ __forceinline__ int64_t row_of(const int64_t* __restrict__ row_start, int64_t T, int64_t p) {
+  int64_t lo = 0, hi = T - 1;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) >> 1;
+    if (row_start[mid] <= p) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// bf16 pairs of z = u[row] + v[col] for features [f0, f0 + 8) of cell p.
+__device__ __forceinline__ uint4 fused_z8(const FusedIn& fz, int64_t row, int64_t vrow, int f0) {
+  const float4 a0 = __ldg(reinterpret_cast<const float4*>(fz.u + row * kCz + f0));
+  const float4 a1 = __ldg(reinterpret_cast<const float4*>(fz.u + row * kCz + f0 + 4));
+  const float4 b0 = __ldg(reinterpret_cast<const float4*>(fz.v + vrow * kCz + f0));
+  const float4 b1 = __ldg(reinterpret_cast<const float4*>(fz.v + vrow * kCz + f0 + 4));
+  return make_uint4(pack_bf16x2(a0.x + b0.x, a0.y + b0.y), pack_bf16x2(a0.z + b0.z, a0.w + b0.w),
+                    pack_bf16x2(a1.x + b1.x, a1.y + b1.y), pack_bf16x2(a1.z + b1.z, a1.w + b1.w));
+}
 
 __device__ __forceinline__ void weight_order(int q, int NC, bool* is_w1, int* c) {
   // consumption order: W1(0), then for each chunk c: W1(c+1) (if any), W2(c)
@@ -83,14 +127,14 @@ __device__ __forceinline__ void weight_order(int q, int NC, bool* is_w1, int* c)
   *c = NC - 1;
 }
 
-template <bool kGLU>
+template <bool kGLU, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_constant__ CUtensorMap tm_zout,
                      const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w3,
                      const __grid_constant__ CUtensorMap tm_w2, const bf16* z_in, int64_t P, int H_t,
                      const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
                      const float* __restrict__ b1, const float* __restrict__ b3, const float* __restrict__ b2,
-                     unsigned int* status) {
+                     const FusedIn fz, unsigned int* status) {
   // hidden units per chunk; GEMM2 contracts kHid per chunk
   constexpr int kHid = kGLU ? 64 : kChunk;
   extern __shared__ uint8_t smem_raw[];
@@ -117,6 +161,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       mbar_init(&bar.h_full[s], 128); mbar_init(&bar.h_empty[s], 1);
       mbar_init(&bar.acc2_full[s], 1); mbar_init(&bar.acc2_empty[s], 128);
       mbar_init(&bar.out_ready[s], 128); mbar_init(&bar.store_done[s], 1);
+      mbar_init(&bar.colsum_done[s], 128);
     }
     mbar_init(&bar.mma_done, 1);
     bar.abort = 0;
@@ -140,13 +185,15 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       bool ok = true;
       int j = 0;
       for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
-        if (!(ok = mbar_wait(&bar.a_empty, (j & 1) ^ 1, abort_flag, status))) break;
-        mbar_arrive_expect_tx(&bar.z_full, kABytes);
-        const int row0 = (int)(tile * kTileRows);
-        for (int s = 0; s < 2; ++s)
-          for (int kb = 0; kb < 2; ++kb)
-            tma_load_2d(sA + s * kSubBytes + kb * kBlockBytes, &tm_zin, &bar.z_full, kb * 64, row0 + s * kSubRows);
-        last_tile_j = j;
+        if (!kFused) {   // the fused block builds its z tile in the LayerNorm warps
+          if (!(ok = mbar_wait(&bar.a_empty, (j & 1) ^ 1, abort_flag, status))) break;
+          mbar_arrive_expect_tx(&bar.z_full, kABytes);
+          const int row0 = (int)(tile * kTileRows);
+          for (int s = 0; s < 2; ++s)
+            for (int kb = 0; kb < 2; ++kb)
+              tma_load_2d(sA + s * kSubBytes + kb * kBlockBytes, &tm_zin, &bar.z_full, kb * 64, row0 + s * kSubRows);
+          last_tile_j = j;
+        }
         for (int q = 0; q < 2 * NC; ++q) {
           bool w1; int c;
           weight_order(q, NC, &w1, &c);
@@ -258,7 +305,29 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
     const int t = threadIdx.x - 64;   // 0..127: row t of each sub-tile
     int j = 0;
     for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++j) {
-      if (!mbar_wait(&bar.z_full, j & 1, abort_flag, status)) break;
+      if (kFused) {
+        // A is free once the previous tile's GEMM1s have read it; then this
+        // thread writes row t of both sub-tiles: z = bf16(u[row] + v[col])
+        if (!mbar_wait(&bar.a_empty, (j & 1) ^ 1, abort_flag, status)) break;
+#pragma unroll 1
+        for (int s = 0; s < 2; ++s) {
+          uint8_t* base = sA + s * kSubBytes;
+          const int64_t p = tile * kTileRows + s * kSubRows + t;
+          if (p < P) {
+            const int64_t row = row_of(fz.row_start, fz.T, p);
+            const int64_t vrow = fz.col_cu[fz.row_sample[row]] + (p - fz.row_start[row]);
+#pragma unroll 4
+            for (int ci = 0; ci < 16; ++ci)
+              *reinterpret_cast<uint4*>(base + swz128_offset(t, ci * 8, kSubRows)) = fused_z8(fz, row, vrow, ci * 8);
+          } else {
+#pragma unroll
+            for (int ci = 0; ci < 16; ++ci)
+              *reinterpret_cast<uint4*>(base + swz128_offset(t, ci * 8, kSubRows)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      } else if (!mbar_wait(&bar.z_full, j & 1, abort_flag, status)) {
+        break;
+      }
 #pragma unroll 1
       for (int s = 0; s < 2; ++s) {
         uint8_t* base = sA + s * kSubBytes;
@@ -379,6 +448,11 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       const int64_t row_g = tile * kTileRows + s * kSubRows + r;
       const bool in_range = row_g < P;
       const bf16* zr = z_in + row_g * kCz;
+      int64_t f_row = 0, f_vrow = 0;        // fused: the cell's pair row and column single
+      if (kFused && in_range) {
+        f_row = row_of(fz.row_start, fz.T, row_g);
+        f_vrow = fz.col_cu[fz.row_sample[f_row]] + (row_g - fz.row_start[f_row]);
+      }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         float v[32];
@@ -388,7 +462,8 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 q4 = make_uint4(0, 0, 0, 0);
-          if (in_range) q4 = *reinterpret_cast<const uint4*>(zr + 32 * g + 8 * u);
+          if (in_range) q4 = kFused ? fused_z8(fz, f_row, f_vrow, 32 * g + 8 * u)
+                                    : *reinterpret_cast<const uint4*>(zr + 32 * g + 8 * u);
           rw[4 * u] = q4.x; rw[4 * u + 1] = q4.y; rw[4 * u + 2] = q4.z; rw[4 * u + 3] = q4.w;
         }
 #pragma unroll
@@ -408,8 +483,42 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       mbar_arrive(&bar.acc2_empty[s]);
       fence_async_shared();
       mbar_arrive(&bar.out_ready[s]);
-      if (leader) {
-        const int64_t y = tile * kTileRows + s * kSubRows;
+      const int64_t y = tile * kTileRows + s * kSubRows;
+      if (kFused) {
+        // every thread reads the staged z~ tile: wait until it is complete
+        if (!(ok = mbar_wait_warp(&bar.out_ready[s], j & 1, abort_flag, status))) break;
+        if (leader && y < P) {
+          tma_store_2d(&tm_zout, hs, 0, (int)y);
+          tma_store_2d(&tm_zout, hs + kBlockBytes, 64, (int)y);
+          tma_store_commit();
+        }
+        // Eq. 4's column sum: feature r of the tile's cells, one atomic add
+        // into m_acc per pair row touched
+        if (y < P) {
+          const int cmax = (int)min64(kSubRows, P - y);
+          int64_t row = row_of(fz.row_start, fz.T, y);
+          int64_t end = fz.row_start[row + 1];
+          float acc = 0.f;
+          for (int c = 0; c < cmax; ++c) {
+            while (y + c >= end) {
+              atomicAdd(fz.m_acc + row * kCz + r, acc);
+              acc = 0.f;
+              ++row;
+              end = fz.row_start[row + 1];
+            }
+            const uint32_t bits = *reinterpret_cast<const uint16_t*>(hs + swz128_offset(c, r, kSubRows));
+            acc += __uint_as_float(bits << 16);
+          }
+          atomicAdd(fz.m_acc + row * kCz + r, acc);
+        }
+        mbar_arrive(&bar.colsum_done[s]);
+        if (leader) {
+          // H[s] is reused once the column sums and the store's reads are done
+          const bool sums_done = mbar_wait(&bar.colsum_done[s], j & 1, abort_flag, status);
+          if (y < P) tma_store_wait_read0();
+          if (sums_done) mbar_arrive(&bar.store_done[s]);
+        }
+      } else if (leader) {
         if (mbar_wait(&bar.out_ready[s], j & 1, abort_flag, status) && y < P) {
           tma_store_2d(&tm_zout, hs, 0, (int)y);
           tma_store_2d(&tm_zout, hs + kBlockBytes, 64, (int)y);
@@ -466,13 +575,16 @@ bool transition_tc_supported(nt_dtype dt, int C_z, int H_t, bool glu) {
   return dt == NT_BF16 && C_z == kCz && H_t >= unit && H_t % unit == 0 && H_t <= 16384;
 }
 
-cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t,
-                                 const float* gamma, const float* beta, float eps, const void* W1,
-                                 const float* b1, const void* W3, const float* b3, const void* W2,
-                                 const float* b2, unsigned int* status, cudaStream_t s) {
+namespace {
+
+cudaError_t launch_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t, const float* gamma,
+                      const float* beta, float eps, const void* W1, const float* b1, const void* W3,
+                      const float* b3, const void* W2, const float* b2, const FusedIn* fused,
+                      unsigned int* status, cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   if (P > 0x7fffffffLL - kTileRows) return cudaErrorInvalidValue;
   const bool glu = W3 != nullptr;
+  if (fused) z_in = z_out;   // no z tensor: the unused input map is built over the output
   CUtensorMap m_zin, m_zout, m_w1, m_w3, m_w2;
   // SwiGLU: W1 and W3 are read as 64-row halves of a weight tile
   const uint32_t w_rows = glu ? 64 : 128;
@@ -480,14 +592,33 @@ cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C
       !make_map(&m_w1, W1, C_z, H_t, w_rows) || !make_map(&m_w3, glu ? W3 : W1, C_z, H_t, w_rows) ||
       !make_map(&m_w2, W2, H_t, C_z))
     return cudaErrorInvalidValue;
-  auto kern = glu ? transition_tc_kernel<true> : transition_tc_kernel<false>;
+  auto kern = fused ? (glu ? transition_tc_kernel<true, true> : transition_tc_kernel<false, true>)
+                    : (glu ? transition_tc_kernel<true, false> : transition_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int64_t tiles = (P + kTileRows - 1) / kTileRows;
   const int grid = (int)min64(tiles, (int64_t)sm_count());
+  const FusedIn none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr};
   kern<<<grid, kThreads, kSmemBytes, s>>>(m_zin, m_zout, m_w1, m_w3, m_w2, (const bf16*)z_in, P, H_t, gamma, beta,
-                                          eps, b1, b3, b2, status);
+                                          eps, b1, b3, b2, fused ? *fused : none, status);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t,
+                                 const float* gamma, const float* beta, float eps, const void* W1,
+                                 const float* b1, const void* W3, const float* b3, const void* W2,
+                                 const float* b2, unsigned int* status, cudaStream_t s) {
+  return launch_tc(z_in, z_out, P, C_z, H_t, gamma, beta, eps, W1, b1, W3, b3, W2, b2, nullptr, status, s);
+}
+
+cudaError_t launch_block_fused_tc(const float* u, const float* v, const nt_partition* part, void* z_out, int C_z,
+                                  int H_t, const float* gamma, const float* beta, float eps, const void* W1,
+                                  const float* b1, const void* W3, const float* b3, const void* W2, const float* b2,
+                                  float* m_acc, unsigned int* status, cudaStream_t s) {
+  const FusedIn fz = {u, v, part->row_start, part->row_sample, col_cu_of(part), part->T, m_acc};
+  return launch_tc(nullptr, z_out, part->P, C_z, H_t, gamma, beta, eps, W1, b1, W3, b3, W2, b2, &fz, status, s);
 }
 
 }  // namespace nt

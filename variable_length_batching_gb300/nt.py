@@ -53,6 +53,9 @@ SIGNATURES = {
     "nt_pair_transition_swiglu": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                          _P]),
     "nt_pair_reduce": (_I32, [_PP, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P]),
+    "nt_pair_block_fused_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
+    "nt_pair_block_fused": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
+                                   _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P]),
     "nt_varlen_attn_qk": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _F, _I32,
                                  _P, _P, _P]),
@@ -357,6 +360,36 @@ def nt_device_status(stream=None) -> int:
     st = lib().nt_device_status(_stream(stream))
     _check(st, "nt_device_status")
     return st
+
+
+def nt_pair_block_fused(part: Partition, s_left: torch.Tensor, s_right: torch.Tensor, w, W3=None, b3=None,
+                        ln_eps: float = 1e-5, z: Optional[torch.Tensor] = None, m: Optional[torch.Tensor] = None,
+                        s_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None):
+    """The whole block in one pass (``nt_pair_block_fused``).  ``w`` holds
+    W_a, W_b, ln_gamma, ln_beta, W1, b1, W2, b2, W_g, b_g on the device;
+    ``W3`` (and ``b3``) select the SwiGLU update.  Returns (z~, m, s_out)."""
+    T, C_s = s_left.shape
+    C_z, H_t = w.W_a.shape[0], w.W1.shape[0]
+    if T != part.T or tuple(s_right.shape) != (part.T_cols, C_s):
+        raise ValueError("singles do not match the partition")
+    dev, dt = s_left.device, s_left.dtype
+    if z is None:
+        z = torch.empty(part.P, C_z, dtype=dt, device=dev)
+    if m is None:
+        m = torch.empty(T, C_z, dtype=dt, device=dev)
+    if s_out is None and w.W_g is not None:
+        s_out = torch.empty(T, C_s, dtype=dt, device=dev)
+    need = int(lib().nt_pair_block_fused_workspace_bytes(T, part.T_cols, C_z))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = lib().nt_pair_block_fused(
+        ctypes.byref(part.c), _dtype(s_left), _ptr(s_left), _ptr(s_right), C_s, _ptr(w.W_a), _ptr(w.W_b), C_z, H_t,
+        _ptr(_f32(w.ln_gamma)), _ptr(_f32(w.ln_beta)), ln_eps, _ptr(w.W1), _ptr(_f32(w.b1)), _ptr(W3), _ptr(_f32(b3)),
+        _ptr(w.W2), _ptr(_f32(w.b2)), _ptr(w.W_g), _ptr(_f32(w.b_g)), _ptr(z), _ptr(m), _ptr(s_out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nt_pair_block_fused")
+    return z, m, s_out
 
 
 def block_forward(part: Partition, s: torch.Tensor, w, ln_eps: float = 1e-5,
