@@ -21,9 +21,8 @@
 // The softmax threads read S_j into registers first and release the S
 // buffer at once, so S_{j+1} is computed while they exponentiate S_j.  The
 // running max moves only when a tile's max exceeds it by more than 8 (log2
-// units), so O in TMEM is rescaled in place on those tiles only.  A quarter
-// of each full tile's exponentials run on the FMA pipe (exp2_fma), the rest
-// on the SFU.  Two CTAs fit on an SM (48 KB shared memory, 256 TMEM columns
+// units), so O in TMEM is rescaled in place on those tiles only.  Full
+// tiles take their exponentials two at a time on the SFU (f16x2 inputs).  Two CTAs fit on an SM (48 KB shared memory, 256 TMEM columns
 // each, 224 of them used).
 //
 // Cross-attention takes the keys of query segment b from [cu_k[b], cu_k[b+1])
@@ -298,9 +297,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           const float x0 = fmaf(sv[c], scale_log2, -m), x1 = fmaf(sv[c + 1], scale_log2, -m);
-          // one in four exponentials on the FMA pipe, the rest on the SFU
-          const float p0 = ex2_approx(x0);
-          const float p1 = ((c & 2) == 2) ? exp2_fma(x1) : ex2_approx(x1);
+          float p0, p1;
+          ex2_f16x2(x0, x1, p0, p1);             // two exponentials per SFU instruction
           ps[(c >> 1) & 7] += p0 + p1;
           pk[c / 2] = pack_bf16x2(p0, p1);
         }

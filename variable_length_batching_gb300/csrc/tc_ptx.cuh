@@ -333,20 +333,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^x on the FMA pipe, for x in [-126, 127]: x = n + f with n the nearest
-// integer (adding 1.5 * 2^23 leaves it in the low mantissa bits) and f in
-// [-1/2, 1/2]; 2^f by a cubic minimax fit (coefficients derived in
-// variable_length_batching_gb300/exp2_poly.py, max relative error 1.0e-4);
-// 2^n added to the exponent field.
-__device__ __forceinline__ float exp2_fma(float x) {
-  x = fmaxf(x, -126.0f);
-  const float t = x + 12582912.0f;
-  const float f = x - (t - 12582912.0f);
-  float p = fmaf(0.055009059607982635f, f, 0.2422109693288803f);
-  p = fmaf(p, f, 0.6932829022407532f);
-  p = fmaf(p, f, 1.0f);
-  const int n = __float_as_int(t) - 0x4B400000;
-  return __int_as_float(__float_as_int(p) + (n << 23));
+// 2^x for two values at once on the SFU: x rounded to f16 (11-bit mantissa,
+// so the relative error of 2^x stays near bf16's own rounding step for the
+// x <= 8 the attention softmax produces), ex2.approx.f16x2, back to fp32.
+__device__ __forceinline__ void ex2_f16x2(float x0, float x1, float& p0, float& p1) {
+  uint32_t xh, ph;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(xh) : "f"(x1), "f"(x0));   // x0 in the low half
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(ph) : "r"(xh));
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(p0), "=f"(p1) : "r"(ph));
 }
 // bf16x2 word -> two fp32 (exact).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
