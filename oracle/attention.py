@@ -22,6 +22,12 @@ packing", "How to use it": the varlen call of its template sets the causal
 flag) is aligned to the bottom-right corner when the lengths differ: query i of a
 segment with n_q queries and n_k keys sees keys j <= i + (n_k - n_q); a query
 that sees no key returns zeros with lse = -inf.
+
+Backward (the gradients of the same per-segment attention with respect to
+q, k and v for an upstream gradient dO), written from the chain rule of
+softmax(scale Q K^T) V: with P the attention matrix of a segment,
+dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dO * O)), dQ = scale dS K,
+dK = scale dS^T Q; masked entries have P = 0 and get no gradient.
 """
 from __future__ import annotations
 
@@ -80,6 +86,54 @@ def varlen_attention(q, k, v, cu_seqlens: Sequence[int], scale: Optional[float] 
             continue
         O[lo:hi], lse[:, lo:hi] = segment_attention(q[lo:hi], k[klo:khi], v[klo:khi], scale, causal)
     return O, lse
+
+
+def segment_attention_backward(q, k, v, do, scale: float, causal: bool = False):
+    """Gradients of one segment's attention: q, do (n_q, H, d); k, v (n_k, H, d).
+    Returns dq, dk, dv with the shapes of q, k, v."""
+    nq, H, d = q.shape
+    nk = k.shape[0]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    allowed = np.ones((nq, nk), dtype=bool)
+    if causal:
+        allowed = np.arange(nk)[None, :] <= np.arange(nq)[:, None] + (nk - nq)
+    for h in range(H):
+        S = (q[:, h, :] @ k[:, h, :].T) * scale
+        S = np.where(allowed, S, -np.inf)
+        P = np.zeros_like(S)
+        for i in range(nq):
+            if allowed[i].any():
+                e = np.exp(S[i] - S[i][allowed[i]].max())
+                P[i] = e / e.sum()
+        O = P @ v[:, h, :]
+        dO = do[:, h, :]
+        dv[:, h, :] = P.T @ dO
+        dP = dO @ v[:, h, :].T
+        Drow = (dO * O).sum(axis=1, keepdims=True)
+        dS = P * (dP - Drow)
+        dq[:, h, :] = scale * dS @ k[:, h, :]
+        dk[:, h, :] = scale * dS.T @ q[:, h, :]
+    return dq, dk, dv
+
+
+def varlen_attention_backward(q, k, v, do, cu_seqlens, scale: Optional[float] = None, causal: bool = False,
+                              cu_seqlens_k=None, segments: Optional[Sequence[int]] = None):
+    """Gradients of ``varlen_attention`` segment by segment; ``segments``
+    limits the work to the listed segments (the other rows stay zero)."""
+    T, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    cu_k = cu_seqlens if cu_seqlens_k is None else cu_seqlens_k
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    B = len(cu_seqlens) - 1
+    for b in (range(B) if segments is None else segments):
+        lo, hi = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        klo, khi = int(cu_k[b]), int(cu_k[b + 1])
+        if hi == lo or khi == klo:
+            continue
+        dq[lo:hi], dk[klo:khi], dv[klo:khi] = segment_attention_backward(q[lo:hi], k[klo:khi], v[klo:khi],
+                                                                         do[lo:hi], scale, causal)
+    return dq, dk, dv
 
 
 def masked_full_attention(q, k, v, seg_ids: Sequence[int], scale: Optional[float] = None):

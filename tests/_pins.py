@@ -466,3 +466,38 @@ def pin_swiglu_zero_gate(transition_swiglu, rng):
     out = transition_swiglu(z, np.ones(6), np.zeros(6), 1e-5, np.zeros((12, 6)), None,
                             rng.standard_normal((12, 6)), rng.standard_normal(12), rng.standard_normal((6, 12)), b2)
     assert np.array_equal(out, z + b2)
+
+
+def pin_attention_backward_autograd(varlen_attention_backward, rng):
+    """Per segment, the gradients equal torch autograd of SDPA in float64
+    (non-causal and causal, equal and differing query/key lengths)."""
+    cu_q, cu_k = [0, 5, 5, 12, 14], [0, 7, 9, 16, 16]
+    H, d = 2, 4
+    q = rng.standard_normal((cu_q[-1], H, d))
+    do = rng.standard_normal((cu_q[-1], H, d))
+    k, v = (rng.standard_normal((cu_k[-1], H, d)) for _ in range(2))
+    for causal in (False, True):
+        for ck in (None, cu_k):
+            if ck is None:                        # self-attention: keys share the query offsets
+                kk, vv, cuk = k[:cu_q[-1]], v[:cu_q[-1]], cu_q
+            else:
+                kk, vv, cuk = k, v, cu_k
+            dq, dk, dv = varlen_attention_backward(q, kk, vv, do, cu_q, causal=causal, cu_seqlens_k=ck)
+            for b in range(len(cu_q) - 1):
+                ql, qh, kl, kh = cu_q[b], cu_q[b + 1], cuk[b], cuk[b + 1]
+                if qh == ql or kh == kl:
+                    assert np.all(dq[ql:qh] == 0)
+                    continue
+                tq = torch.tensor(q[ql:qh].transpose(1, 0, 2), requires_grad=True)
+                tk = torch.tensor(kk[kl:kh].transpose(1, 0, 2), requires_grad=True)
+                tv = torch.tensor(vv[kl:kh].transpose(1, 0, 2), requires_grad=True)
+                mask = None
+                if causal:
+                    mask = torch.ones(qh - ql, kh - kl, dtype=torch.bool).tril(kh - kl - (qh - ql))
+                    if not mask.any(dim=1).all():
+                        continue          # rows with no key: SDPA gives NaN there; covered elsewhere
+                out = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask)
+                out.backward(torch.from_numpy(do[ql:qh].transpose(1, 0, 2)))
+                assert np.allclose(dq[ql:qh], tq.grad.numpy().transpose(1, 0, 2), rtol=1e-10, atol=1e-10)
+                assert np.allclose(dk[kl:kh], tk.grad.numpy().transpose(1, 0, 2), rtol=1e-10, atol=1e-10)
+                assert np.allclose(dv[kl:kh], tv.grad.numpy().transpose(1, 0, 2), rtol=1e-10, atol=1e-10)

@@ -308,3 +308,33 @@ def test_swiglu_mistakes_caught():
 
 def test_silu_mistake_caught():
     _fails(pins.pin_silu, lambda x: 1 / (1 + np.exp(-x)))
+
+
+# --- attention backward -----------------------------------------------------------
+
+def backward_without_rowsum(q, k, v, do, cu, scale=None, causal=False, cu_seqlens_k=None, segments=None):
+    """dS = P * dP (the rowsum(dO * O) term dropped)."""
+    orig = oattn.segment_attention_backward
+
+    def seg(q, k, v, do, scale, causal=False):
+        nq, H, d = q.shape
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        for h in range(H):
+            S = (q[:, h, :] @ k[:, h, :].T) * scale
+            P = np.exp(S - S.max(axis=1, keepdims=True))
+            P /= P.sum(axis=1, keepdims=True)
+            dP = do[:, h, :] @ v[:, h, :].T
+            dS = P * dP
+            dv[:, h, :] = P.T @ do[:, h, :]
+            dq[:, h, :] = scale * dS @ k[:, h, :]
+            dk[:, h, :] = scale * dS.T @ q[:, h, :]
+        return dq, dk, dv
+    oattn.segment_attention_backward = seg
+    try:
+        return oattn.varlen_attention_backward(q, k, v, do, cu, scale, causal, cu_seqlens_k, segments)
+    finally:
+        oattn.segment_attention_backward = orig
+
+
+def test_backward_rowsum_caught():
+    _fails(pins.pin_attention_backward_autograd, backward_without_rowsum, rng(28))

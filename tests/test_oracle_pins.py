@@ -243,3 +243,7 @@ def test_swiglu_library():
 
 def test_swiglu_zero_gate():
     pins.pin_swiglu_zero_gate(oblock.transition_swiglu, rng(27))
+
+
+def test_attention_backward_autograd():
+    pins.pin_attention_backward_autograd(oattn.varlen_attention_backward, rng(28))
