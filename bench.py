@@ -758,6 +758,15 @@ def run_only(args):
             fn = lambda: nt.nt_varlen_attn(q, k, v, cu, ml, out=o, stream=stream)
         w = attn_work(a.seqlens, cfg.H, cfg.d, causal=args.causal)
         bound, name = "tensor", cfg.name + ("_causal" if args.causal else "")
+        if args.backward:
+            # the forward's o and lse, then dq, dk, dv for a seeded upstream gradient
+            _, lse_f = nt.nt_varlen_attn_qk(q, k, v, cu, cu, ml, causal=args.causal, out=o, want_lse=True)
+            do = wl.random_rows(q.shape[0] * cfg.H, cfg.d, cfg.dtype, seed=1).reshape(q.shape).to(dev)
+            fn = lambda: nt.nt_varlen_attn_bwd(q, k, v, o, do, lse_f, cu, causal=args.causal, stream=stream)
+            # S recomputed, dV, dP, dQ, dK: 2.5 times the forward's flops; q, k, v, o, dO read,
+            # dq, dk, dv written
+            w = {"flops": int(2.5 * w["flops"]), "bytes": 2 * w["bytes"]}
+            name += "_backward"
     else:
         cfg = WORKLOADS[args.workload]
         inp = wl.make_block_inputs(cfg)
@@ -843,6 +852,7 @@ def main():
     ap.add_argument("--workload", default="pairformer", choices=sorted(WORKLOADS))
     ap.add_argument("--causal", action="store_true", help="with --only attention: the causal mask")
     ap.add_argument("--swiglu", action="store_true", help="with --only transition: the SwiGLU update")
+    ap.add_argument("--backward", action="store_true", help="with --only attention: the backward (dq, dk, dv)")
     args = ap.parse_args()
     if args.only == "packing":
         run_packing(args)

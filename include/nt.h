@@ -341,6 +341,35 @@ nt_status nt_varlen_attn_qk(nt_dtype dtype, const void* q, const void* k, const 
                             int64_t T_q, int64_t T_k, int32_t max_len_q, int32_t H, int32_t d, float scale,
                             int32_t causal, void* o, float* lse, void* stream);
 
+/* Bytes of device workspace nt_varlen_attn_bwd needs: H * T_q * 4. */
+size_t nt_varlen_attn_bwd_workspace_bytes(int64_t T_q, int32_t H);
+
+/*
+ * nt_varlen_attn_bwd -- gradients of nt_varlen_attn_qk (and so of
+ * nt_varlen_attn) with respect to q, k and v for an upstream gradient d_o
+ * (the backward of [VA]'s varlen attention, as training needs it): per
+ * segment and head, with P rebuilt from the forward's natural-log lse,
+ *     dV = P^T dO,  dS = P * (dO V^T - rowsum(dO * O)),
+ *     dQ = scale dS K,  dK = scale dS^T Q
+ * (masked entries, causal or across segments, get no gradient; a query that
+ * saw no key, lse = -inf, contributes nothing).
+ *   q, o, d_o, dq  [T_q, H, d];  k, v, dk, dv [T_k, H, d]; token-major,
+ *                  contiguous, dtype as given; dq, dk, dv are overwritten.
+ *   lse            [H, T_q] fp32, the forward's (natural log).
+ *   d_cu_seqlens_q, d_cu_seqlens_k, scale, causal: as in nt_varlen_attn_qk.
+ *   workspace      >= nt_varlen_attn_bwd_workspace_bytes(T_q, H) device
+ *                  bytes, 16-byte aligned.
+ * d = 32, 64 or 128, bf16 or fp32, on CUDA cores (fp32 accumulation).
+ * Asynchronous.  Errors as for nt_varlen_attn_qk; offsets inconsistent with
+ * T_q / T_k are caught on the device (NT_ERR_DEVICE_CHECK).
+ */
+nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const void* v,
+                             const void* o, const void* d_o, const float* lse,
+                             const int32_t* d_cu_seqlens_q, const int32_t* d_cu_seqlens_k,
+                             int32_t B, int64_t T_q, int64_t T_k, int32_t H, int32_t d,
+                             float scale, int32_t causal, void* dq, void* dk, void* dv,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device status word set by
  * device-side checks (bounded waits that ran out: NT_ERR_TIMEOUT; failed data
  * checks: NT_ERR_DEVICE_CHECK).  NT_OK if nothing was flagged. */

@@ -449,6 +449,45 @@ nt_status nt_varlen_attn_qk(nt_dtype dtype, const void* q, const void* k, const 
   return NT_OK;
 }
 
+size_t nt_varlen_attn_bwd_workspace_bytes(int64_t T_q, int32_t H) {
+  if (T_q < 0 || H < 0) return 0;
+  return (size_t)T_q * (size_t)H * sizeof(float);
+}
+
+nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const void* v, const void* o,
+                             const void* d_o, const float* lse, const int32_t* d_cu_seqlens_q,
+                             const int32_t* d_cu_seqlens_k, int32_t B, int64_t T_q, int64_t T_k, int32_t H,
+                             int32_t d, float scale, int32_t causal, void* dq, void* dk, void* dv, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (B < 0 || T_q < 0 || T_k < 0 || H <= 0 || d <= 0)
+    return fail(NT_ERR_INVALID, "bad sizes B=%d T_q=%lld T_k=%lld H=%d d=%d", B, (long long)T_q, (long long)T_k, H, d);
+  if (!(scale > 0.f) || std::isinf(scale)) return fail(NT_ERR_INVALID, "scale must be finite and > 0");
+  if (causal != 0 && causal != 1) return fail(NT_ERR_INVALID, "causal must be 0 or 1");
+  if (T_q > 0x7fffffffLL || T_k > 0x7fffffffLL)
+    return fail(NT_ERR_OVERFLOW, "T_q = %lld, T_k = %lld: token counts must fit int32", (long long)T_q,
+                (long long)T_k);
+  if ((T_q > 0 || T_k > 0) && B == 0) return fail(NT_ERR_INVALID, "tokens with no segments");
+  if (!attn_bwd_supported(d)) return fail(NT_ERR_UNSUPPORTED, "head width d=%d", d);
+  if (T_q > 0 && (!q || !o || !d_o || !lse || !dq || !workspace || !d_cu_seqlens_q || !d_cu_seqlens_k))
+    return fail(NT_ERR_INVALID, "NULL pointer");
+  if (T_k > 0 && (!k || !v || !dk || !dv || !d_cu_seqlens_q || !d_cu_seqlens_k))
+    return fail(NT_ERR_INVALID, "NULL key-side pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  if (workspace_bytes < nt_varlen_attn_bwd_workspace_bytes(T_q, H))
+    return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes,
+                nt_varlen_attn_bwd_workspace_bytes(T_q, H));
+  if (T_q == 0 && T_k == 0) return NT_OK;
+  const AttnBwdProblem prob = {q, k, v, o, d_o, lse, d_cu_seqlens_q, d_cu_seqlens_k, B, T_q, T_k,
+                               H, d, scale, causal != 0, dq, dk, dv};
+  cudaError_t e = launch_attn_bwd(dtype, prob, static_cast<float*>(workspace), status_word(),
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "varlen attention backward launch");
+  return NT_OK;
+}
+
 nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const void* v,
                          const int32_t* d_cu_seqlens, int32_t B, int64_t T, int32_t max_len,
                          int32_t H, int32_t d, float scale, void* o, float* lse, void* stream) {

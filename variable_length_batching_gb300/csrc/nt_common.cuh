@@ -159,6 +159,30 @@ struct AttnProblem {
   float* lse;
 };
 
+// Backward of one varlen attention problem (the forward's q, k, v, o, its
+// natural-log lse, and the upstream gradient d_o; outputs dq, dk, dv).
+struct AttnBwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* d_o;
+  const float* lse;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int32_t B;
+  int64_t T_q, T_k;
+  int H, d;
+  float scale;
+  bool causal;
+  void* dq;
+  void* dk;
+  void* dv;
+};
+bool attn_bwd_supported(int d);
+// Dbuf: H * T_q fp32 of device workspace (rowsum(dO * O)).
+cudaError_t launch_attn_bwd(nt_dtype dt, const AttnBwdProblem& p, float* Dbuf, unsigned int* status, cudaStream_t s);
+
 bool attn_simt_supported(int d);
 cudaError_t launch_attn_simt(nt_dtype dt, const AttnProblem& p, unsigned int* status, cudaStream_t s);
 bool attn_tc_supported(nt_dtype dt, int d);
