@@ -762,7 +762,8 @@ def run_only(args):
             # the forward's o and lse, then dq, dk, dv for a seeded upstream gradient
             _, lse_f = nt.nt_varlen_attn_qk(q, k, v, cu, cu, ml, causal=args.causal, out=o, want_lse=True)
             do = wl.random_rows(q.shape[0] * cfg.H, cfg.d, cfg.dtype, seed=1).reshape(q.shape).to(dev)
-            fn = lambda: nt.nt_varlen_attn_bwd(q, k, v, o, do, lse_f, cu, causal=args.causal, stream=stream)
+            fn = lambda: nt.nt_varlen_attn_bwd(q, k, v, o, do, lse_f, cu, None, ml, causal=args.causal,
+                                               stream=stream)
             # S recomputed, dV, dP, dQ, dK: 2.5 times the forward's flops; q, k, v, o, dO read,
             # dq, dk, dv written
             w = {"flops": int(2.5 * w["flops"]), "bytes": 2 * w["bytes"]}

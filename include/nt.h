@@ -357,16 +357,23 @@ size_t nt_varlen_attn_bwd_workspace_bytes(int64_t T_q, int32_t H);
  *                  contiguous, dtype as given; dq, dk, dv are overwritten.
  *   lse            [H, T_q] fp32, the forward's (natural log).
  *   d_cu_seqlens_q, d_cu_seqlens_k, scale, causal: as in nt_varlen_attn_qk.
+ *   max_len_q, max_len_k  longest query / key segment (>= every
+ *                  cu[b+1] - cu[b] of the side); they size the grid of the
+ *                  tensor-core path, which flags NT_ERR_DEVICE_CHECK when a
+ *                  segment is longer than stated.
  *   workspace      >= nt_varlen_attn_bwd_workspace_bytes(T_q, H) device
  *                  bytes, 16-byte aligned.
- * d = 32, 64 or 128, bf16 or fp32, on CUDA cores (fp32 accumulation).
- * Asynchronous.  Errors as for nt_varlen_attn_qk; offsets inconsistent with
- * T_q / T_k are caught on the device (NT_ERR_DEVICE_CHECK).
+ * bf16 with d = 64 runs on the tcgen05 tensor cores (fp32 accumulation in
+ * TMEM); d = 32, 64 or 128 in fp32, and bf16 with d = 32 or 128, on CUDA
+ * cores (fp32 accumulation).  Asynchronous.  Errors as for
+ * nt_varlen_attn_qk; offsets inconsistent with T_q / T_k are caught on the
+ * device (NT_ERR_DEVICE_CHECK).
  */
 nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const void* v,
                              const void* o, const void* d_o, const float* lse,
                              const int32_t* d_cu_seqlens_q, const int32_t* d_cu_seqlens_k,
-                             int32_t B, int64_t T_q, int64_t T_k, int32_t H, int32_t d,
+                             int32_t B, int64_t T_q, int64_t T_k, int32_t max_len_q,
+                             int32_t max_len_k, int32_t H, int32_t d,
                              float scale, int32_t causal, void* dq, void* dk, void* dv,
                              void* workspace, size_t workspace_bytes, void* stream);
 

@@ -91,10 +91,13 @@ def test_host_side_rejections(L):
                                   None, None) == 1
     # attention backward: bad head width, bad causal flag
     bw = lib.nt_varlen_attn_bwd
-    assert bw(1, fake, fake, fake, fake, fake, fake, fake, fake, 1, 64, 64, 1, 48, 0.125, 0, fake, fake, fake, fake,
-              1 << 20, None) == 2
-    assert bw(1, fake, fake, fake, fake, fake, fake, fake, fake, 1, 64, 64, 1, 64, 0.125, 3, fake, fake, fake, fake,
-              1 << 20, None) == 1
+    assert bw(1, fake, fake, fake, fake, fake, fake, fake, fake, 1, 64, 64, 64, 64, 1, 48, 0.125, 0, fake, fake,
+              fake, fake, 1 << 20, None) == 2
+    assert bw(1, fake, fake, fake, fake, fake, fake, fake, fake, 1, 64, 64, 64, 64, 1, 64, 0.125, 3, fake, fake,
+              fake, fake, 1 << 20, None) == 1
+    # a negative max length
+    assert bw(1, fake, fake, fake, fake, fake, fake, fake, fake, 1, 64, 64, 64, -1, 1, 64, 0.125, 0, fake, fake,
+              fake, fake, 1 << 20, None) == 1
     # SwiGLU without its value projection
     assert lib.nt_pair_transition_swiglu(P, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None,
                                          fake, None, None) == 1

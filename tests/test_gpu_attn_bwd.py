@@ -42,7 +42,8 @@ def _case(nt, lq, lk, H, d, dtype, causal, segments=None, seed=7):
     o_in = torch.from_numpy(O).to(tdt).to(DEV)
     lse_in = torch.from_numpy(L.astype(np.float32)).to(DEV)
     dq, dk, dv = nt.nt_varlen_attn_bwd(a.q.to(DEV), a.k.to(DEV), a.v.to(DEV), o_in, do.to(DEV), lse_in,
-                                       torch.as_tensor(cu_q).to(DEV), torch.as_tensor(cu_k).to(DEV), causal=causal)
+                                       torch.as_tensor(cu_q).to(DEV), torch.as_tensor(cu_k).to(DEV),
+                                       max(list(lq) + [0]), max(list(lk) + [0]), causal=causal)
     return (dq, dk, dv), (dq_r, dk_r, dv_r), cu_q, cu_k
 
 
@@ -54,6 +55,10 @@ def _case(nt, lq, lk, H, d, dtype, causal, segments=None, seed=7):
     ([20, 33], None, 2, 128, "f32", False),
     ([5, 0, 130, 64, 1, 200], [7, 3, 0, 64, 129, 150], 2, 64, "bf16", True),   # cross, empty and all-masked rows
     ([130], [3], 2, 64, "f32", True),                                          # 127 queries see no key
+    ([130], [3], 2, 64, "bf16", True),
+    ([3, 300], [200, 17], 3, 64, "bf16", False),                              # cross: 5 key tiles / 1 query tile
+    ([511, 1, 256, 129], None, 2, 64, "bf16", True),                           # several 128-key and 64-query tiles
+    ([511, 1, 256, 129], None, 2, 64, "bf16", False),
 ])
 def test_attention_backward(nt, lq, lk, H, d, dtype, causal):
     lk = lq if lk is None else lk
@@ -63,14 +68,15 @@ def test_attention_backward(nt, lq, lk, H, d, dtype, causal):
     nt.nt_device_status()
 
 
-def test_attention_backward_full_size_sampled(nt):
-    """The 65,536-token stream (237 segments, 12 heads x 64), causal: every
-    gradient row of a sample of segments against the oracle."""
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_backward_full_size_sampled(nt, causal):
+    """The 65,536-token stream (237 segments, 12 heads x 64): every gradient
+    row of a sample of segments against the oracle."""
     a = wl.make_attn_inputs(wl.VARLEN_ATTN_BF16)
     lens = list(a.seqlens)
     B = len(lens)
     segs = sorted(set([0, B - 1, int(np.argmax(a.seqlens)), int(np.argmin(a.seqlens)), 17, 101]))
-    got, ref, cu, _ = _case(nt, lens, lens, 12, 64, "bf16", True, segments=segs, seed=0)
+    got, ref, cu, _ = _case(nt, lens, lens, 12, 64, "bf16", causal, segments=segs, seed=0)
     rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in segs])
     idx = torch.as_tensor(rows, device=DEV)
     for g, r in zip(got, ref):

@@ -1,0 +1,518 @@
+// Backward of variable-length attention on the tcgen05 tensor cores, bf16 in
+// / fp32 accumulate, head width 64 ("Variable-length attention and data
+// packing", "What it is" / "How it works"; the causal and cross forms as in
+// the forward).  Per segment and head, with P rebuilt from the forward's
+// natural-log LSE (no running max: P = exp(scale s - lse) <= 1),
+//     dP = dO V^T,  dS = P * (dP - D),  D = rowsum(dO * O)   (D precomputed)
+//     dQ = scale dS K,   dK = scale dS^T Q,   dV = P^T dO.
+// Two kernels, so that every output row has one owner and no atomics:
+//
+// dQ kernel: one CTA per (segment, 128-query tile, head), walking the key
+// tiles of 64 the tile's queries see.
+//   S  = Q K_j^T, dP = dO V_j^T          (M=128, N=64, K=64)  -> TMEM
+//   dS -> bf16, written by the compute threads over dP's columns
+//   dQ += dS K_j                          (A from TMEM, K_j MN-major)
+//
+// dK/dV kernel: one CTA per (segment, 128-key tile, head), walking the query
+// tiles of 64 that see the tile's keys.  In the transposed frame (keys on
+// the TMEM lanes) the per-query LSE and D are column constants, staged in
+// shared memory by the producer warp beside each query tile.
+//   S^T = K Q_i^T, dP^T = V dO_i^T        -> TMEM
+//   P^T over S^T's columns, dS^T over dP^T's (bf16)
+//   dV += P^T dO_i,  dK += dS^T Q_i       (A from TMEM, B MN-major)
+//
+// Warps: 0 = TMA producer, 1 = TMEM owner and MMA issuer (one elected lane
+// issues), 2-9 = compute, two warps per TMEM lane quadrant, each taking 32
+// of a tile's 64 columns.  256 TMEM columns and about 82 KB of shared memory
+// per CTA: two CTAs share an SM.  Every wait is bounded.
+#include "tc_ptx.cuh"
+
+namespace nt {
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 64;
+constexpr int kBM = 128;                       // rows held for the CTA's life
+constexpr int kBN = 64;                        // rows of a streamed tile
+constexpr int kStages = 3;
+constexpr int kThreads = 10 * 32;
+constexpr uint32_t kBigBytes = kBM * kD * 2;   // 16 KB
+constexpr uint32_t kSmallBytes = kBN * kD * 2; // 8 KB
+constexpr uint32_t kOffBig0 = 0;
+constexpr uint32_t kOffBig1 = kBigBytes;
+constexpr uint32_t kOffRing = 2 * kBigBytes;   // stage st: tile X at +16 KB st, tile Y 8 KB after
+constexpr uint32_t kOffAux = kOffRing + kStages * 2 * kSmallBytes;
+constexpr uint32_t kAuxBytes = 2 * kBN * 4;    // per stage: lse (log2 units) and D of 64 queries
+constexpr uint32_t kOffBar = kOffAux + kStages * kAuxBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256;
+constexpr uint32_t kTmemCols = 256;
+// S (or S^T) at 0, dP (or dP^T) at 64, accumulators at 128 (dQ or dV) and 192 (dK)
+constexpr uint32_t kColS = 0, kColP = 64, kColAcc0 = 128, kColAcc1 = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Bars {
+  uint64_t big_full;
+  uint64_t full[kStages], empty[kStages];
+  uint64_t s_full, p_full, p_empty;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// TMEM column of the k-th 16-wide K chunk of an A operand that two compute
+// warps wrote as bf16 pairs: tokens [32 g, 32 g + 32) packed into columns
+// [32 g, 32 g + 16) of the base.
+__device__ __forceinline__ uint32_t a_chunk(uint32_t base, int kk) {
+  return base + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
+}
+
+// The four MMAs of one M=128, N=64, K=64 product with both operands
+// K-major in shared memory.
+__device__ __forceinline__ void mma_kmajor(uint32_t d, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk)
+    mma_bf16(d, sdesc_k128(a_base + kk * 32), sdesc_k128(b_base + kk * 32), idesc, kk > 0);
+}
+
+// D (+)= A (TMEM, bf16 pairs at `a_base`, 64 tokens of K) x B (a 64-token
+// tile of shared memory read MN-major: token rows, 64 features).
+__device__ __forceinline__ void mma_ts_mn(uint32_t d, uint32_t a_base, uint32_t b_base, uint32_t idesc,
+                                          bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk)
+    mma_bf16_ts(d, a_chunk(a_base, kk), sdesc_k128(b_base + kk * 2048), idesc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+__device__ __forceinline__ void store_row32(bf16* dst, const float* v, float mul) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul);
+    w.y = pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul);
+    w.z = pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul);
+    w.w = pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul);
+    *reinterpret_cast<uint4*>(dst + 8 * u) = w;
+  }
+}
+
+__device__ __forceinline__ void zero_rows(bf16* base, int64_t first, int rows, int H, int h) {
+  for (int e = threadIdx.x; e < rows * (kD / 8); e += kThreads) {
+    const int rr = e / (kD / 8), u = e % (kD / 8);
+    *reinterpret_cast<uint4*>(base + ((first + rr) * H + h) * kD + 8 * u) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__device__ __forceinline__ void init_bars(Bars& bar, uint32_t full_count) {
+  mbar_init(&bar.big_full, 1);
+  for (int i = 0; i < kStages; ++i) {
+    mbar_init(&bar.full[i], full_count);
+    mbar_init(&bar.empty[i], 1);
+  }
+  mbar_init(&bar.s_full, 1);
+  mbar_init(&bar.p_full, 256);
+  mbar_init(&bar.p_empty, 1);
+  mbar_init(&bar.mma_done, 1);
+  bar.abort = 0;
+  fence_mbar_init();
+  fence_async_shared();
+}
+
+// ============================================================================ dQ
+template <bool kCausal>
+__global__ void __launch_bounds__(kThreads, 2)
+attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const float* __restrict__ lse, const float* __restrict__ Dbuf, const int32_t* __restrict__ cu_q,
+                   const int32_t* __restrict__ cu_k, int B, int64_t T_q, int64_t T_k, int H, int QT,
+                   float scale, bf16* __restrict__ dq, unsigned int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int64_t item = blockIdx.x;
+  const int h = (int)(item % H);
+  const int64_t rest = item / H;
+  const int qi = kCausal ? QT - 1 - (int)(rest % QT) : (int)(rest % QT);
+  const int b = (int)(rest / QT);
+  if (b >= B) return;
+  const int lo = cu_q[b], hi = cu_q[b + 1];
+  const int klo = cu_k[b], khi = cu_k[b + 1];
+  if (lo < 0 || hi < lo || hi > T_q || klo < 0 || khi < klo || khi > T_k) {
+    if (threadIdx.x == 0 && qi == 0 && h == 0) flag_device(status, kDevCheck);
+    return;
+  }
+  const int n = hi - lo, n_k = khi - klo;
+  if (qi == QT - 1 && n > QT * kBM && threadIdx.x == 0 && h == 0) flag_device(status, kDevCheck);
+  const int q0 = lo + qi * kBM;
+  if (q0 >= hi) return;
+  const int diag = n_k - n;                    // causal: query i sees keys j <= i + diag
+  int nk = (n_k + kBN - 1) / kBN;
+  if (kCausal) {
+    const int last = min(qi * kBM + kBM - 1, n - 1) + diag;
+    nk = last < 0 ? 0 : min(nk, last / kBN + 1);
+  }
+  if (nk == 0) {                               // no query here sees a key: no gradient
+    zero_rows(dq, q0, min(kBM, hi - q0), H, h);
+    return;
+  }
+  if (smem_u32(smem_raw) & 1023) {
+    if (threadIdx.x == 0) flag_device(status, kDevCheck);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = smem_raw;
+  Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort_flag = &bar.abort;
+  if (threadIdx.x == 0) init_bars(bar, 1);
+  if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q); prefetch_tmap(&tm_do); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(&bar.big_full, 2 * kBigBytes);
+      tma_load_3d(smem + kOffBig0, &tm_q, &bar.big_full, 0, h, q0);
+      tma_load_3d(smem + kOffBig1, &tm_do, &bar.big_full, 0, h, q0);
+      int issued = 0;
+      for (int j = 0; j < nk; ++j) {
+        const int st = j % kStages;
+        if (!mbar_wait(&bar.empty[st], ((j / kStages) & 1) ^ 1, abort_flag, status)) break;
+        uint8_t* ring = smem + kOffRing + st * 2 * kSmallBytes;
+        mbar_arrive_expect_tx(&bar.full[st], 2 * kSmallBytes);
+        tma_load_3d(ring, &tm_k, &bar.full[st], 0, h, klo + j * kBN);
+        tma_load_3d(ring + kSmallBytes, &tm_v, &bar.full[st], 0, h, klo + j * kBN);
+        issued = j + 1;
+      }
+      mbar_wait(&bar.big_full, 0, nullptr, status);
+      for (int j = issued - kStages; j < issued; ++j)
+        if (j >= 0) mbar_wait(&bar.full[j % kStages], (j / kStages) & 1, nullptr, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t id_kk = idesc_bf16_f32(128, kBN);
+    const uint32_t id_mn = idesc_bf16_f32(128, kD) | (1u << 16);   // B MN-major
+    const uint32_t q_base = smem_u32(smem + kOffBig0), do_base = smem_u32(smem + kOffBig1);
+    const bool leader = elect_one();
+    bool ok = mbar_wait_warp(&bar.big_full, 0, abort_flag, status);
+    for (int j = 0; j < nk && ok; ++j) {
+      const int st = j % kStages;
+      const uint32_t kb = smem_u32(smem + kOffRing + st * 2 * kSmallBytes), vb = kb + kSmallBytes;
+      if (!(ok = mbar_wait_warp(&bar.full[st], (j / kStages) & 1, abort_flag, status))) break;
+      if (j > 0 && !(ok = mbar_wait_warp(&bar.p_empty, (j - 1) & 1, abort_flag, status))) break;
+      tc_fence_after();
+      if (leader) {
+        mma_kmajor(tmem + kColS, q_base, kb, id_kk);       // S  = Q K_j^T
+        mma_kmajor(tmem + kColP, do_base, vb, id_kk);      // dP = dO V_j^T
+        mma_commit(&bar.s_full);
+      }
+      __syncwarp();
+      if (!(ok = mbar_wait_warp(&bar.p_full, j & 1, abort_flag, status))) break;
+      tc_fence_after();
+      if (leader) {
+        mma_ts_mn(tmem + kColAcc0, tmem + kColP, kb, id_mn, j > 0);   // dQ += dS K_j
+        mma_commit(&bar.p_empty);
+        mma_commit(&bar.empty[st]);
+      }
+      __syncwarp();
+    }
+    if (leader) mma_commit(&bar.mma_done);
+    __syncwarp();
+    mbar_wait_warp(&bar.mma_done, 0, nullptr, status);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int qd = warp & 3, g = (warp - 2) >> 2;
+    const int r = qd * 32 + lane;
+    const int64_t t = (int64_t)q0 + r;
+    const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    const float scale_log2 = scale * kLog2e;
+    // rows past the segment, and rows that saw no key: P = 0 (lse -> +inf)
+    float L = INFINITY, Dr = 0.f;
+    if (t < hi) {
+      const float l = lse[(int64_t)h * T_q + t];
+      if (l != -INFINITY) {
+        L = l * kLog2e;
+        Dr = Dbuf[(int64_t)h * T_q + t];
+      }
+    }
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      if (!(ok = mbar_wait_warp(&bar.s_full, j & 1, abort_flag, status))) break;
+      tc_fence_after();
+      __syncwarp();
+      int cnt = min(kBN, n_k - j * kBN);                   // visible keys: a prefix of the tile
+      if (kCausal) cnt = max(0, min(cnt, qi * kBM + r + diag - j * kBN + 1));
+      const bool full = __all_sync(0xffffffffu, cnt >= 32 * g + 32);
+      float sv[32], dp[32];
+      tmem_ld32(lane_addr + kColS + 32 * g, sv);
+      tmem_ld32(lane_addr + kColP + 32 * g, dp);
+      tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float p0, p1;
+        ex2_f16x2(fmaf(sv[c], scale_log2, -L), fmaf(sv[c + 1], scale_log2, -L), p0, p1);
+        if (!full) {
+          if (32 * g + c >= cnt) p0 = 0.f;
+          if (32 * g + c + 1 >= cnt) p1 = 0.f;
+        }
+        pk[c / 2] = pack_bf16x2(p0 * (dp[c] - Dr), p1 * (dp[c + 1] - Dr));
+      }
+      tmem_st16_sync(lane_addr + kColP + 32 * g, pk);
+      tc_fence_before();
+      mbar_arrive(&bar.p_full);
+    }
+    if (ok && mbar_wait_warp(&bar.p_empty, (nk - 1) & 1, abort_flag, status)) {
+      tc_fence_after();
+      __syncwarp();
+      float acc[32];
+      tmem_ld32(lane_addr + kColAcc0 + 32 * g, acc);
+      tmem_ld_wait();
+      if (t < hi) store_row32(dq + (t * H + h) * kD + 32 * g, acc, scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ============================================================================ dK, dV
+template <bool kCausal>
+__global__ void __launch_bounds__(kThreads, 2)
+attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                    const float* __restrict__ lse, const float* __restrict__ Dbuf, const int32_t* __restrict__ cu_q,
+                    const int32_t* __restrict__ cu_k, int B, int64_t T_q, int64_t T_k, int H, int KT,
+                    float scale, bf16* __restrict__ dk, bf16* __restrict__ dv, unsigned int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int64_t item = blockIdx.x;
+  const int h = (int)(item % H);
+  const int64_t rest = item / H;
+  const int kt = (int)(rest % KT);             // causal: the first key tiles see the most queries
+  const int b = (int)(rest / KT);
+  if (b >= B) return;
+  const int lo = cu_q[b], hi = cu_q[b + 1];
+  const int klo = cu_k[b], khi = cu_k[b + 1];
+  if (lo < 0 || hi < lo || hi > T_q || klo < 0 || khi < klo || khi > T_k) {
+    if (threadIdx.x == 0 && kt == 0 && h == 0) flag_device(status, kDevCheck);
+    return;
+  }
+  const int n = hi - lo, n_k = khi - klo;
+  if (kt == KT - 1 && n_k > KT * kBM && threadIdx.x == 0 && h == 0) flag_device(status, kDevCheck);
+  const int k0 = klo + kt * kBM;
+  if (k0 >= khi) return;
+  const int diag = n_k - n;                    // query i sees key j when i >= j - diag
+  // the first query that sees any key of this tile, and the query tiles from there
+  const int i_first = kCausal ? max(0, kt * kBM - diag) : 0;
+  const int nq = i_first >= n ? 0 : (n - i_first + kBN - 1) / kBN;
+  if (nq == 0) {                               // no query sees these keys: no gradient
+    zero_rows(dk, k0, min(kBM, khi - k0), H, h);
+    zero_rows(dv, k0, min(kBM, khi - k0), H, h);
+    return;
+  }
+  if (smem_u32(smem_raw) & 1023) {
+    if (threadIdx.x == 0) flag_device(status, kDevCheck);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = smem_raw;
+  Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort_flag = &bar.abort;
+  if (threadIdx.x == 0) init_bars(bar, 32);    // a query tile: 32 producer lanes + its copies
+  if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_q); prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(&bar.big_full, 2 * kBigBytes);
+      tma_load_3d(smem + kOffBig0, &tm_k, &bar.big_full, 0, h, k0);
+      tma_load_3d(smem + kOffBig1, &tm_v, &bar.big_full, 0, h, k0);
+    }
+    int issued = 0;
+    for (int i = 0; i < nq; ++i) {
+      const int st = i % kStages;
+      if (!mbar_wait_warp(&bar.empty[st], ((i / kStages) & 1) ^ 1, abort_flag, status)) break;
+      const int i0 = i_first + i * kBN;        // segment-local first query of the tile
+      // lse in log2 units (+inf where there is no query, or the query saw no
+      // key, so that P = 0 there) and D, one pair per query column
+      float* aux = reinterpret_cast<float*>(smem + kOffAux + st * kAuxBytes);
+      for (int c = lane; c < kBN; c += 32) {
+        float Lc = INFINITY, Dc = 0.f;
+        if (i0 + c < n) {
+          const int64_t t = (int64_t)lo + i0 + c;
+          const float l = lse[(int64_t)h * T_q + t];
+          if (l != -INFINITY) {
+            Lc = l * kLog2e;
+            Dc = Dbuf[(int64_t)h * T_q + t];
+          }
+        }
+        aux[c] = Lc;
+        aux[kBN + c] = Dc;
+      }
+      if (lane == 0) {
+        uint8_t* ring = smem + kOffRing + st * 2 * kSmallBytes;
+        mbar_arrive_expect_tx(&bar.full[st], 2 * kSmallBytes);
+        tma_load_3d(ring, &tm_q, &bar.full[st], 0, h, lo + i0);
+        tma_load_3d(ring + kSmallBytes, &tm_do, &bar.full[st], 0, h, lo + i0);
+      } else {
+        mbar_arrive(&bar.full[st]);
+      }
+      issued = i + 1;
+    }
+    if (lane == 0) {
+      mbar_wait(&bar.big_full, 0, nullptr, status);
+      for (int i = issued - kStages; i < issued; ++i)
+        if (i >= 0) mbar_wait(&bar.full[i % kStages], (i / kStages) & 1, nullptr, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t id_kk = idesc_bf16_f32(128, kBN);
+    const uint32_t id_mn = idesc_bf16_f32(128, kD) | (1u << 16);
+    const uint32_t k_base = smem_u32(smem + kOffBig0), v_base = smem_u32(smem + kOffBig1);
+    const bool leader = elect_one();
+    bool ok = mbar_wait_warp(&bar.big_full, 0, abort_flag, status);
+    for (int i = 0; i < nq && ok; ++i) {
+      const int st = i % kStages;
+      const uint32_t qb = smem_u32(smem + kOffRing + st * 2 * kSmallBytes), dob = qb + kSmallBytes;
+      if (!(ok = mbar_wait_warp(&bar.full[st], (i / kStages) & 1, abort_flag, status))) break;
+      if (i > 0 && !(ok = mbar_wait_warp(&bar.p_empty, (i - 1) & 1, abort_flag, status))) break;
+      tc_fence_after();
+      if (leader) {
+        mma_kmajor(tmem + kColS, k_base, qb, id_kk);      // S^T  = K Q_i^T
+        mma_kmajor(tmem + kColP, v_base, dob, id_kk);     // dP^T = V dO_i^T
+        mma_commit(&bar.s_full);
+      }
+      __syncwarp();
+      if (!(ok = mbar_wait_warp(&bar.p_full, i & 1, abort_flag, status))) break;
+      tc_fence_after();
+      if (leader) {
+        mma_ts_mn(tmem + kColAcc0, tmem + kColS, dob, id_mn, i > 0);   // dV += P^T dO_i
+        mma_ts_mn(tmem + kColAcc1, tmem + kColP, qb, id_mn, i > 0);    // dK += dS^T Q_i
+        mma_commit(&bar.p_empty);
+        mma_commit(&bar.empty[st]);
+      }
+      __syncwarp();
+    }
+    if (leader) mma_commit(&bar.mma_done);
+    __syncwarp();
+    mbar_wait_warp(&bar.mma_done, 0, nullptr, status);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int qd = warp & 3, g = (warp - 2) >> 2;
+    const int r = qd * 32 + lane;
+    const int jj = kt * kBM + r;               // segment-local key of this lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    const float scale_log2 = scale * kLog2e;
+    bool ok = true;
+    for (int i = 0; i < nq; ++i) {
+      const int st = i % kStages;
+      if (!(ok = mbar_wait_warp(&bar.s_full, i & 1, abort_flag, status))) break;
+      // the aux values of this tile: acquire the producer lanes' writes directly
+      if (!(ok = mbar_wait_warp(&bar.full[st], (i / kStages) & 1, abort_flag, status))) break;
+      tc_fence_after();
+      __syncwarp();
+      const int i0 = i_first + i * kBN;
+      // causal: column c (query i0 + c) sees this key when c >= jj - diag - i0
+      const int cmin = kCausal ? jj - diag - i0 - 32 * g : 0;   // relative to this half
+      const bool full = !kCausal || __all_sync(0xffffffffu, cmin <= 0);
+      const float* aux = reinterpret_cast<const float*>(smem + kOffAux + st * kAuxBytes) + 32 * g;
+      float sv[32], dp[32];
+      tmem_ld32(lane_addr + kColS + 32 * g, sv);
+      tmem_ld32(lane_addr + kColP + 32 * g, dp);
+      tmem_ld_wait();
+      uint32_t pk[16], ds[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {            // P^T, and dS^T = P^T * (dP^T - D)
+        const float4 L4 = *reinterpret_cast<const float4*>(aux + c);
+        const float4 D4 = *reinterpret_cast<const float4*>(aux + kBN + c);
+        float p0, p1, p2, p3;
+        ex2_f16x2(fmaf(sv[c], scale_log2, -L4.x), fmaf(sv[c + 1], scale_log2, -L4.y), p0, p1);
+        ex2_f16x2(fmaf(sv[c + 2], scale_log2, -L4.z), fmaf(sv[c + 3], scale_log2, -L4.w), p2, p3);
+        if (!full) {
+          if (c < cmin) p0 = 0.f;
+          if (c + 1 < cmin) p1 = 0.f;
+          if (c + 2 < cmin) p2 = 0.f;
+          if (c + 3 < cmin) p3 = 0.f;
+        }
+        pk[c / 2] = pack_bf16x2(p0, p1);
+        pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+        ds[c / 2] = pack_bf16x2(p0 * (dp[c] - D4.x), p1 * (dp[c + 1] - D4.y));
+        ds[c / 2 + 1] = pack_bf16x2(p2 * (dp[c + 2] - D4.z), p3 * (dp[c + 3] - D4.w));
+      }
+      tmem_st16_sync(lane_addr + kColS + 32 * g, pk);
+      tmem_st16_sync(lane_addr + kColP + 32 * g, ds);
+      tc_fence_before();
+      mbar_arrive(&bar.p_full);
+    }
+    if (ok && mbar_wait_warp(&bar.p_empty, (nq - 1) & 1, abort_flag, status)) {
+      tc_fence_after();
+      __syncwarp();
+      const int64_t t = (int64_t)klo + jj;
+      float acc[32];
+      tmem_ld32(lane_addr + kColAcc0 + 32 * g, acc);
+      tmem_ld_wait();
+      if (jj < n_k) store_row32(dv + (t * H + h) * kD + 32 * g, acc, 1.0f);
+      tmem_ld32(lane_addr + kColAcc1 + 32 * g, acc);
+      tmem_ld_wait();
+      if (jj < n_k) store_row32(dk + (t * H + h) * kD + 32 * g, acc, scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+bool make_map_thd(CUtensorMap* map, const void* ptr, int64_t T, int H, uint32_t rows) {
+  const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)T};
+  const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};
+  const uint32_t box[3] = {(uint32_t)kD, 1, rows};
+  return make_tmap_bf16(map, ptr, 3, dims, strides, box);
+}
+
+}  // namespace
+
+bool attn_bwd_tc_supported(nt_dtype dt, int d) { return dt == NT_BF16 && d == kD; }
+
+cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsigned int* status, cudaStream_t s) {
+  if (p.T_q == 0 || p.T_k == 0 || p.B == 0) return cudaErrorInvalidValue;   // the caller routes these
+  CUtensorMap q128, do128, k64, v64, k128, v128, q64, do64;
+  if (!make_map_thd(&q128, p.q, p.T_q, p.H, kBM) || !make_map_thd(&do128, p.d_o, p.T_q, p.H, kBM) ||
+      !make_map_thd(&k64, p.k, p.T_k, p.H, kBN) || !make_map_thd(&v64, p.v, p.T_k, p.H, kBN) ||
+      !make_map_thd(&k128, p.k, p.T_k, p.H, kBM) || !make_map_thd(&v128, p.v, p.T_k, p.H, kBM) ||
+      !make_map_thd(&q64, p.q, p.T_q, p.H, kBN) || !make_map_thd(&do64, p.d_o, p.T_q, p.H, kBN))
+    return cudaErrorInvalidValue;
+  const int QT = max(1, (p.max_len_q + kBM - 1) / kBM);
+  const int KT = max(1, (p.max_len_k + kBM - 1) / kBM);
+  const int64_t items_q = (int64_t)p.B * QT * p.H, items_k = (int64_t)p.B * KT * p.H;
+  if (items_q > 0x7fffffffLL || items_k > 0x7fffffffLL) return cudaErrorInvalidValue;
+  auto kq = p.causal ? attn_bwd_dq_kernel<true> : attn_bwd_dq_kernel<false>;
+  auto kkv = p.causal ? attn_bwd_dkv_kernel<true> : attn_bwd_dkv_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kkv<<<(unsigned)items_k, kThreads, kSmemBytes, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
+                                                       p.T_q, p.T_k, p.H, KT, p.scale, (bf16*)p.dk, (bf16*)p.dv,
+                                                       status);
+  kq<<<(unsigned)items_q, kThreads, kSmemBytes, s>>>(q128, do128, k64, v64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
+                                                     p.T_q, p.T_k, p.H, QT, p.scale, (bf16*)p.dq, status);
+  return cudaGetLastError();
+}
+
+}  // namespace nt

@@ -456,12 +456,14 @@ size_t nt_varlen_attn_bwd_workspace_bytes(int64_t T_q, int32_t H) {
 
 nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const void* v, const void* o,
                              const void* d_o, const float* lse, const int32_t* d_cu_seqlens_q,
-                             const int32_t* d_cu_seqlens_k, int32_t B, int64_t T_q, int64_t T_k, int32_t H,
-                             int32_t d, float scale, int32_t causal, void* dq, void* dk, void* dv, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+                             const int32_t* d_cu_seqlens_k, int32_t B, int64_t T_q, int64_t T_k,
+                             int32_t max_len_q, int32_t max_len_k, int32_t H, int32_t d, float scale,
+                             int32_t causal, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             void* stream) {
   if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
-  if (B < 0 || T_q < 0 || T_k < 0 || H <= 0 || d <= 0)
-    return fail(NT_ERR_INVALID, "bad sizes B=%d T_q=%lld T_k=%lld H=%d d=%d", B, (long long)T_q, (long long)T_k, H, d);
+  if (B < 0 || T_q < 0 || T_k < 0 || H <= 0 || d <= 0 || max_len_q < 0 || max_len_k < 0)
+    return fail(NT_ERR_INVALID, "bad sizes B=%d T_q=%lld T_k=%lld H=%d d=%d max_len_q=%d max_len_k=%d", B,
+                (long long)T_q, (long long)T_k, H, d, max_len_q, max_len_k);
   if (!(scale > 0.f) || std::isinf(scale)) return fail(NT_ERR_INVALID, "scale must be finite and > 0");
   if (causal != 0 && causal != 1) return fail(NT_ERR_INVALID, "causal must be 0 or 1");
   if (T_q > 0x7fffffffLL || T_k > 0x7fffffffLL)
@@ -481,7 +483,7 @@ nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const
                 nt_varlen_attn_bwd_workspace_bytes(T_q, H));
   if (T_q == 0 && T_k == 0) return NT_OK;
   const AttnBwdProblem prob = {q, k, v, o, d_o, lse, d_cu_seqlens_q, d_cu_seqlens_k, B, T_q, T_k,
-                               H, d, scale, causal != 0, dq, dk, dv};
+                               max_len_q, max_len_k, H, d, scale, causal != 0, dq, dk, dv};
   cudaError_t e = launch_attn_bwd(dtype, prob, static_cast<float*>(workspace), status_word(),
                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "varlen attention backward launch");

@@ -172,6 +172,7 @@ struct AttnBwdProblem {
   const int32_t* cu_k;
   int32_t B;
   int64_t T_q, T_k;
+  int32_t max_len_q, max_len_k;
   int H, d;
   float scale;
   bool causal;
@@ -182,6 +183,10 @@ struct AttnBwdProblem {
 bool attn_bwd_supported(int d);
 // Dbuf: H * T_q fp32 of device workspace (rowsum(dO * O)).
 cudaError_t launch_attn_bwd(nt_dtype dt, const AttnBwdProblem& p, float* Dbuf, unsigned int* status, cudaStream_t s);
+// The tensor-core kernels (dK/dV, then dQ) after Dbuf holds rowsum(dO * O);
+// T_q, T_k and B must be > 0.
+bool attn_bwd_tc_supported(nt_dtype dt, int d);
+cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsigned int* status, cudaStream_t s);
 
 bool attn_simt_supported(int d);
 cudaError_t launch_attn_simt(nt_dtype dt, const AttnProblem& p, unsigned int* status, cudaStream_t s);

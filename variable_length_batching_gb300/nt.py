@@ -60,8 +60,8 @@ SIGNATURES = {
     "nt_varlen_attn_qk": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _F, _I32,
                                  _P, _P, _P]),
     "nt_varlen_attn_bwd_workspace_bytes": (_SZ, [_I64, _I32]),
-    "nt_varlen_attn_bwd": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _F, _I32,
-                                  _P, _P, _P, _P, _SZ, _P]),
+    "nt_varlen_attn_bwd": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _I32,
+                                  _F, _I32, _P, _P, _P, _P, _SZ, _P]),
     "nt_device_status": (_I32, [_P]),
     "nt_status_str": (ctypes.c_char_p, [_I32]),
     "nt_last_error": (ctypes.c_char_p, []),
@@ -358,14 +358,20 @@ def nt_varlen_attn_qk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seql
 
 
 def nt_varlen_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, d_o: torch.Tensor,
-                       lse: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: Optional[torch.Tensor] = None,
-                       scale: Optional[float] = None, causal: bool = False, stream=None):
+                       lse: torch.Tensor, cu_seqlens_q: torch.Tensor, cu_seqlens_k: Optional[torch.Tensor],
+                       max_len_q: int, max_len_k: Optional[int] = None, scale: Optional[float] = None,
+                       causal: bool = False, stream=None):
     """Gradients (dq, dk, dv) of varlen attention for the upstream gradient
-    ``d_o``, from the forward's ``o`` and natural-log ``lse`` [H, T_q]."""
+    ``d_o``, from the forward's ``o`` and natural-log ``lse`` [H, T_q].
+    ``cu_seqlens_k`` None means the query offsets (self-attention); the max
+    lengths bound the longest segment of each side (``max_len_k`` defaults
+    to ``max_len_q``)."""
     T_q, H, d = q.shape
     T_k = k.shape[0]
     if cu_seqlens_k is None:
         cu_seqlens_k = cu_seqlens_q
+    if max_len_k is None:
+        max_len_k = max_len_q
     if lse.dtype != torch.float32 or tuple(lse.shape) != (H, T_q):
         raise ValueError("lse must be fp32 (H, T_q)")
     B = cu_seqlens_q.numel() - 1
@@ -375,7 +381,8 @@ def nt_varlen_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: tor
     ws = torch.empty(max(int(lib().nt_varlen_attn_bwd_workspace_bytes(T_q, H)), 16), dtype=torch.uint8,
                      device=q.device)
     st = lib().nt_varlen_attn_bwd(_dtype(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), _ptr(lse),
-                                  _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, T_q, T_k, H, d, float(scale),
+                                  _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, T_q, T_k, int(max_len_q),
+                                  int(max_len_k), H, d, float(scale),
                                   int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
                                   ws.numel(), _stream(stream))
     _check(st, "nt_varlen_attn_bwd")
