@@ -36,23 +36,30 @@ __device__ __forceinline__ int segment_of(const int32_t* __restrict__ cu, int B,
   return lo;
 }
 
+// One thread per (head, token) row, tokens fastest: the row's D features
+// come in 16-byte vectors (each thread reads whole rows, so every fetched
+// sector is used) and the D values of consecutive tokens are written side by
+// side in the [H, T_q] layout.
 template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(256)
 rowdot_kernel(const T* __restrict__ o, const T* __restrict__ d_o, int64_t Tq, int H, float* __restrict__ Dbuf) {
-  constexpr int kPer = D / 32;
-  const int64_t w = (int64_t)blockIdx.x * kWarps + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
+  constexpr int kVec = 16 / (int)sizeof(T);          // elements per 16-byte vector
+  const int64_t w = (int64_t)blockIdx.x * 256 + threadIdx.x;
   if (w >= Tq * H) return;
-  const int64_t t = w / H;
-  const int h = (int)(w % H);
-  float acc = 0.f;
+  const int h = (int)(w / Tq);
+  const int64_t t = w % Tq;
+  const uint4* po = reinterpret_cast<const uint4*>(o + (t * H + h) * D);
+  const uint4* pd = reinterpret_cast<const uint4*>(d_o + (t * H + h) * D);
+  float acc[2] = {0.f, 0.f};
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int64_t idx = (t * H + h) * D + lane + 32 * u;
-    acc = fmaf(to_f32(d_o[idx]), to_f32(o[idx]), acc);
+  for (int u = 0; u < D / kVec; ++u) {
+    const uint4 a = po[u], b = pd[u];
+    const T* ea = reinterpret_cast<const T*>(&a);
+    const T* eb = reinterpret_cast<const T*>(&b);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) acc[e & 1] = fmaf(to_f32(eb[e]), to_f32(ea[e]), acc[e & 1]);
   }
-  acc = warp_sum(acc);
-  if (lane == 0) Dbuf[(int64_t)h * Tq + t] = acc;
+  Dbuf[(int64_t)h * Tq + t] = acc[0] + acc[1];
 }
 
 template <typename T, int D>
@@ -175,7 +182,9 @@ template <typename T, int D>
 cudaError_t launch_d(const AttnBwdProblem& p, float* Dbuf, unsigned int* status, cudaStream_t s) {
   const int64_t wq = p.T_q * p.H, wk = p.T_k * p.H;
   const unsigned gq = (unsigned)((wq + kWarps - 1) / kWarps), gk = (unsigned)((wk + kWarps - 1) / kWarps);
-  if (wq > 0) rowdot_kernel<T, D><<<gq, kWarps * 32, 0, s>>>((const T*)p.o, (const T*)p.d_o, p.T_q, p.H, Dbuf);
+  if (wq > 0)
+    rowdot_kernel<T, D><<<(unsigned)((wq + 255) / 256), 256, 0, s>>>((const T*)p.o, (const T*)p.d_o, p.T_q, p.H,
+                                                                     Dbuf);
   if (attn_bwd_tc_supported(std::is_same<T, bf16>::value ? NT_BF16 : NT_F32, D) && p.T_q > 0 && p.T_k > 0 &&
       p.B > 0) {
     const cudaError_t e = cudaGetLastError();

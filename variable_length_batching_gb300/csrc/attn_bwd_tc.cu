@@ -53,7 +53,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct Bars {
   uint64_t big_full;
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[kStages], empty[kStages], aux_full[kStages];
   uint64_t s_full, p_full, p_empty;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -85,7 +85,12 @@ __device__ __forceinline__ void mma_ts_mn(uint32_t d, uint32_t a_base, uint32_t 
     mma_bf16_ts(d, a_chunk(a_base, kk), sdesc_k128(b_base + kk * 2048), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-__device__ __forceinline__ void store_row32(bf16* dst, const float* v, float mul) {
+// Output rows leave through shared memory: each compute thread writes its 32
+// values (half a 128-byte row) into a [128 rows x 128 B] staging tile, 16-byte
+// chunks XOR-swizzled by row, then the 256 compute threads copy whole rows
+// out, eight threads per row, so that a warp's store covers four rows
+// instead of 32 scattered half rows.
+__device__ __forceinline__ void stage_row32(uint8_t* tile, int r, int g, const float* v, float mul) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     uint4 w;
@@ -93,7 +98,16 @@ __device__ __forceinline__ void store_row32(bf16* dst, const float* v, float mul
     w.y = pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul);
     w.z = pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul);
     w.w = pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul);
-    *reinterpret_cast<uint4*>(dst + 8 * u) = w;
+    *reinterpret_cast<uint4*>(tile + r * 128 + (((4 * g + u) ^ (r & 7)) << 4)) = w;
+  }
+}
+// Rows [0, rows) of the staging tile to out rows first, first + 1, ... of head h.
+__device__ __forceinline__ void copy_out(const uint8_t* tile, bf16* out, int64_t first, int rows, int H, int h,
+                                         int ct) {
+  for (int e = ct; e < rows * 8; e += 256) {
+    const int r = e >> 3, c = e & 7;
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + r * 128 + ((c ^ (r & 7)) << 4));
+    *reinterpret_cast<uint4*>(out + ((first + r) * H + h) * kD + 8 * c) = w;
   }
 }
 
@@ -104,11 +118,12 @@ __device__ __forceinline__ void zero_rows(bf16* base, int64_t first, int rows, i
   }
 }
 
-__device__ __forceinline__ void init_bars(Bars& bar, uint32_t full_count) {
+__device__ __forceinline__ void init_bars(Bars& bar) {
   mbar_init(&bar.big_full, 1);
   for (int i = 0; i < kStages; ++i) {
-    mbar_init(&bar.full[i], full_count);
+    mbar_init(&bar.full[i], 1);
     mbar_init(&bar.empty[i], 1);
+    mbar_init(&bar.aux_full[i], 32);
   }
   mbar_init(&bar.s_full, 1);
   mbar_init(&bar.p_full, 256);
@@ -162,7 +177,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   uint8_t* smem = smem_raw;
   Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort_flag = &bar.abort;
-  if (threadIdx.x == 0) init_bars(bar, 1);
+  if (threadIdx.x == 0) init_bars(bar);
   if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -231,10 +246,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // rows past the segment, and rows that saw no key: P = 0 (lse -> +inf)
     float L = INFINITY, Dr = 0.f;
     if (t < hi) {
-      const float l = lse[(int64_t)h * T_q + t];
+      const float l = lse[(int64_t)h * T_q + t], dv = Dbuf[(int64_t)h * T_q + t];
       if (l != -INFINITY) {
         L = l * kLog2e;
-        Dr = Dbuf[(int64_t)h * T_q + t];
+        Dr = dv;
       }
     }
     bool ok = true;
@@ -264,14 +279,19 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tc_fence_before();
       mbar_arrive(&bar.p_full);
     }
+    // Every compute warp reaches the named barrier, whether or not its waits
+    // succeeded; the copy-out runs only if no wait of the CTA gave up.
     if (ok && mbar_wait_warp(&bar.p_empty, (nk - 1) & 1, abort_flag, status)) {
       tc_fence_after();
       __syncwarp();
+      // every MMA has completed: the Q tile's buffer stages the dQ rows
       float acc[32];
       tmem_ld32(lane_addr + kColAcc0 + 32 * g, acc);
       tmem_ld_wait();
-      if (t < hi) store_row32(dq + (t * H + h) * kD + 32 * g, acc, scale);
+      stage_row32(smem + kOffBig0, r, g, acc, scale);
     }
+    named_bar_sync(1, 256);
+    if (!*abort_flag) copy_out(smem + kOffBig0, dq, q0, min(kBM, hi - q0), H, h, (int)threadIdx.x - 64);
   }
 
   tc_fence_before();
@@ -325,7 +345,7 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint8_t* smem = smem_raw;
   Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort_flag = &bar.abort;
-  if (threadIdx.x == 0) init_bars(bar, 32);    // a query tile: 32 producer lanes + its copies
+  if (threadIdx.x == 0) init_bars(bar);
   if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -345,31 +365,31 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const int st = i % kStages;
       if (!mbar_wait_warp(&bar.empty[st], ((i / kStages) & 1) ^ 1, abort_flag, status)) break;
       const int i0 = i_first + i * kBN;        // segment-local first query of the tile
-      // lse in log2 units (+inf where there is no query, or the query saw no
-      // key, so that P = 0 there) and D, one pair per query column
-      float* aux = reinterpret_cast<float*>(smem + kOffAux + st * kAuxBytes);
-      for (int c = lane; c < kBN; c += 32) {
-        float Lc = INFINITY, Dc = 0.f;
-        if (i0 + c < n) {
-          const int64_t t = (int64_t)lo + i0 + c;
-          const float l = lse[(int64_t)h * T_q + t];
-          if (l != -INFINITY) {
-            Lc = l * kLog2e;
-            Dc = Dbuf[(int64_t)h * T_q + t];
-          }
-        }
-        aux[c] = Lc;
-        aux[kBN + c] = Dc;
-      }
       if (lane == 0) {
         uint8_t* ring = smem + kOffRing + st * 2 * kSmallBytes;
         mbar_arrive_expect_tx(&bar.full[st], 2 * kSmallBytes);
         tma_load_3d(ring, &tm_q, &bar.full[st], 0, h, lo + i0);
         tma_load_3d(ring + kSmallBytes, &tm_do, &bar.full[st], 0, h, lo + i0);
-      } else {
-        mbar_arrive(&bar.full[st]);
       }
       issued = i + 1;
+      // lse in log2 units (+inf where there is no query, or the query saw no
+      // key, so that P = 0 there) and D, one pair per query column; only the
+      // compute threads wait for these, not the S^T / dP^T MMAs
+      float* aux = reinterpret_cast<float*>(smem + kOffAux + st * kAuxBytes);
+      for (int c = lane; c < kBN; c += 32) {
+        float Lc = INFINITY, Dc = 0.f;
+        if (i0 + c < n) {
+          const int64_t t = (int64_t)lo + i0 + c;
+          const float l = lse[(int64_t)h * T_q + t], dv = Dbuf[(int64_t)h * T_q + t];
+          if (l != -INFINITY) {
+            Lc = l * kLog2e;
+            Dc = dv;
+          }
+        }
+        aux[c] = Lc;
+        aux[kBN + c] = Dc;
+      }
+      mbar_arrive(&bar.aux_full[st]);
     }
     if (lane == 0) {
       mbar_wait(&bar.big_full, 0, nullptr, status);
@@ -419,8 +439,8 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     for (int i = 0; i < nq; ++i) {
       const int st = i % kStages;
       if (!(ok = mbar_wait_warp(&bar.s_full, i & 1, abort_flag, status))) break;
-      // the aux values of this tile: acquire the producer lanes' writes directly
-      if (!(ok = mbar_wait_warp(&bar.full[st], (i / kStages) & 1, abort_flag, status))) break;
+      // the aux values of this tile: acquire the producer lanes' writes
+      if (!(ok = mbar_wait_warp(&bar.aux_full[st], (i / kStages) & 1, abort_flag, status))) break;
       tc_fence_after();
       __syncwarp();
       const int i0 = i_first + i * kBN;
@@ -456,17 +476,24 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       tc_fence_before();
       mbar_arrive(&bar.p_full);
     }
+    // as in the dQ kernel: all compute warps meet at the named barrier
     if (ok && mbar_wait_warp(&bar.p_empty, (nq - 1) & 1, abort_flag, status)) {
       tc_fence_after();
       __syncwarp();
-      const int64_t t = (int64_t)klo + jj;
+      // every MMA has completed: the K and V tiles' buffers stage dV and dK
       float acc[32];
       tmem_ld32(lane_addr + kColAcc0 + 32 * g, acc);
       tmem_ld_wait();
-      if (jj < n_k) store_row32(dv + (t * H + h) * kD + 32 * g, acc, 1.0f);
+      stage_row32(smem + kOffBig1, r, g, acc, 1.0f);
       tmem_ld32(lane_addr + kColAcc1 + 32 * g, acc);
       tmem_ld_wait();
-      if (jj < n_k) store_row32(dk + (t * H + h) * kD + 32 * g, acc, scale);
+      stage_row32(smem + kOffBig0, r, g, acc, scale);
+    }
+    named_bar_sync(1, 256);
+    if (!*abort_flag) {
+      const int rows = min(kBM, khi - k0), ct = (int)threadIdx.x - 64;
+      copy_out(smem + kOffBig1, dv, k0, rows, H, h, ct);
+      copy_out(smem + kOffBig0, dk, k0, rows, H, h, ct);
     }
   }
 
