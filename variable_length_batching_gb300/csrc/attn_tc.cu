@@ -299,6 +299,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc_fence_before();
       mbar_arrive(&bar.p_full);
     }
+    // The output rows leave through shared memory (the Q tile's buffer, free
+    // once every MMA has completed): each thread stages its row, 16-byte
+    // chunks XOR-swizzled by row, then the 128 softmax threads copy whole
+    // rows out, eight per row.  Every softmax warp reaches the named barrier
+    // whether or not its waits succeeded; the copy-out runs only if no wait
+    // of the CTA gave up.
     if (ok && mbar_wait_warp(&bar.p_empty, (nk - 1) & 1, abort_flag, status)) {
       tc_fence_after();
       __syncwarp();
@@ -309,20 +315,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         float ov[32];
         tmem_ld32(tmem + lane_addr + kColO + 32 * g, ov);
         tmem_ld_wait();
-        if (t < hi) {
-          bf16* op = o + ((int64_t)t * H + h) * kD + 32 * g;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16x2(ov[8 * u] * inv, ov[8 * u + 1] * inv);
-            w.y = pack_bf16x2(ov[8 * u + 2] * inv, ov[8 * u + 3] * inv);
-            w.z = pack_bf16x2(ov[8 * u + 4] * inv, ov[8 * u + 5] * inv);
-            w.w = pack_bf16x2(ov[8 * u + 6] * inv, ov[8 * u + 7] * inv);
-            *reinterpret_cast<uint4*>(op + 8 * u) = w;
-          }
+        for (int u = 0; u < 4; ++u) {
+          uint4 w;
+          w.x = pack_bf16x2(ov[8 * u] * inv, ov[8 * u + 1] * inv);
+          w.y = pack_bf16x2(ov[8 * u + 2] * inv, ov[8 * u + 3] * inv);
+          w.z = pack_bf16x2(ov[8 * u + 4] * inv, ov[8 * u + 5] * inv);
+          w.w = pack_bf16x2(ov[8 * u + 6] * inv, ov[8 * u + 7] * inv);
+          *reinterpret_cast<uint4*>(sQ + r * 128 + (((4 * g + u) ^ (r & 7)) << 4)) = w;
         }
       }
       if (t < hi && lse) lse[(int64_t)h * T + t] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+    named_bar_sync(1, 128);
+    if (!*abort_flag) {
+      const int rows = min(kBQ, hi - q0);
+      for (int e = (int)threadIdx.x - 64; e < rows * 8; e += 128) {
+        const int rr = e >> 3, c = e & 7;
+        const uint4 w = *reinterpret_cast<const uint4*>(sQ + rr * 128 + ((c ^ (rr & 7)) << 4));
+        *reinterpret_cast<uint4*>(o + ((int64_t)(q0 + rr) * H + h) * kD + 8 * c) = w;
+      }
     }
   }
 
