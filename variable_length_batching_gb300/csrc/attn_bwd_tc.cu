@@ -43,7 +43,7 @@ constexpr uint32_t kOffBig0 = 0;
 constexpr uint32_t kOffBig1 = kBigBytes;
 constexpr uint32_t kOffRing = 2 * kBigBytes;   // stage st: tile X at +16 KB st, tile Y 8 KB after
 constexpr uint32_t kOffAux = kOffRing + kStages * 2 * kSmallBytes;
-constexpr uint32_t kAuxBytes = 2 * kBN * 4;    // per stage: lse (log2 units) and D of 64 queries
+constexpr uint32_t kAuxBytes = 2 * kBN * 4;    // per stage: -lse (log2 units) and -D of 64 queries
 constexpr uint32_t kOffBar = kOffAux + kStages * kAuxBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256;
 constexpr uint32_t kTmemCols = 256;
@@ -252,6 +252,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         Dr = dv;
       }
     }
+    const float nL = -L, nD = -Dr;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
       if (!(ok = mbar_wait_warp(&bar.s_full, j & 1, abort_flag, status))) break;
@@ -266,14 +267,17 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tmem_ld_wait();
       uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float p0, p1;
-        ex2_f16x2(fmaf(sv[c], scale_log2, -L), fmaf(sv[c + 1], scale_log2, -L), p0, p1);
+      for (int c = 0; c < 32; c += 2) {                    // packed fp32 pairs
+        float x0, x1, p0, p1, e0, e1;
+        ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, nL, nL, x0, x1);
+        ex2_f16x2(x0, x1, p0, p1);
         if (!full) {
           if (32 * g + c >= cnt) p0 = 0.f;
           if (32 * g + c + 1 >= cnt) p1 = 0.f;
         }
-        pk[c / 2] = pack_bf16x2(p0 * (dp[c] - Dr), p1 * (dp[c + 1] - Dr));
+        fadd2(dp[c], dp[c + 1], nD, nD, e0, e1);           // dP - D
+        fmul2(p0, p1, e0, e1, e0, e1);
+        pk[c / 2] = pack_bf16x2(e0, e1);
       }
       tmem_st16_sync(lane_addr + kColP + 32 * g, pk);
       tc_fence_before();
@@ -372,22 +376,22 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         tma_load_3d(ring + kSmallBytes, &tm_do, &bar.full[st], 0, h, lo + i0);
       }
       issued = i + 1;
-      // lse in log2 units (+inf where there is no query, or the query saw no
-      // key, so that P = 0 there) and D, one pair per query column; only the
+      // -lse in log2 units (-inf where there is no query, or the query saw no
+      // key, so that P = 0 there) and -D, one pair per query column; only the
       // compute threads wait for these, not the S^T / dP^T MMAs
       float* aux = reinterpret_cast<float*>(smem + kOffAux + st * kAuxBytes);
       for (int c = lane; c < kBN; c += 32) {
-        float Lc = INFINITY, Dc = 0.f;
+        float nLc = -INFINITY, nDc = 0.f;
         if (i0 + c < n) {
           const int64_t t = (int64_t)lo + i0 + c;
           const float l = lse[(int64_t)h * T_q + t], dv = Dbuf[(int64_t)h * T_q + t];
           if (l != -INFINITY) {
-            Lc = l * kLog2e;
-            Dc = dv;
+            nLc = -l * kLog2e;
+            nDc = -dv;
           }
         }
-        aux[c] = Lc;
-        aux[kBN + c] = Dc;
+        aux[c] = nLc;
+        aux[kBN + c] = nDc;
       }
       mbar_arrive(&bar.aux_full[st]);
     }
@@ -454,12 +458,14 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       tmem_ld_wait();
       uint32_t pk[16], ds[16];
 #pragma unroll
-      for (int c = 0; c < 32; c += 4) {            // P^T, and dS^T = P^T * (dP^T - D)
-        const float4 L4 = *reinterpret_cast<const float4*>(aux + c);
-        const float4 D4 = *reinterpret_cast<const float4*>(aux + kBN + c);
-        float p0, p1, p2, p3;
-        ex2_f16x2(fmaf(sv[c], scale_log2, -L4.x), fmaf(sv[c + 1], scale_log2, -L4.y), p0, p1);
-        ex2_f16x2(fmaf(sv[c + 2], scale_log2, -L4.z), fmaf(sv[c + 3], scale_log2, -L4.w), p2, p3);
+      for (int c = 0; c < 32; c += 4) {            // P^T, and dS^T = P^T * (dP^T - D), packed pairs
+        const float4 L4 = *reinterpret_cast<const float4*>(aux + c);         // -lse
+        const float4 D4 = *reinterpret_cast<const float4*>(aux + kBN + c);   // -D
+        float x0, x1, x2, x3, p0, p1, p2, p3;
+        ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, L4.x, L4.y, x0, x1);
+        ffma2(sv[c + 2], sv[c + 3], scale_log2, scale_log2, L4.z, L4.w, x2, x3);
+        ex2_f16x2(x0, x1, p0, p1);
+        ex2_f16x2(x2, x3, p2, p3);
         if (!full) {
           if (c < cmin) p0 = 0.f;
           if (c + 1 < cmin) p1 = 0.f;
@@ -468,8 +474,12 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         pk[c / 2] = pack_bf16x2(p0, p1);
         pk[c / 2 + 1] = pack_bf16x2(p2, p3);
-        ds[c / 2] = pack_bf16x2(p0 * (dp[c] - D4.x), p1 * (dp[c + 1] - D4.y));
-        ds[c / 2 + 1] = pack_bf16x2(p2 * (dp[c + 2] - D4.z), p3 * (dp[c + 3] - D4.w));
+        fadd2(dp[c], dp[c + 1], D4.x, D4.y, x0, x1);
+        fadd2(dp[c + 2], dp[c + 3], D4.z, D4.w, x2, x3);
+        fmul2(p0, p1, x0, x1, x0, x1);
+        fmul2(p2, p3, x2, x3, x2, x3);
+        ds[c / 2] = pack_bf16x2(x0, x1);
+        ds[c / 2 + 1] = pack_bf16x2(x2, x3);
       }
       tmem_st16_sync(lane_addr + kColS + 32 * g, pk);
       tmem_st16_sync(lane_addr + kColP + 32 * g, ds);

@@ -274,13 +274,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_ld_wait();
         uint32_t pk[16];
         if (full) {
+          // exponents, row sums: packed fp32 pairs (two column sums per lane
+          // pair of accumulators)
           float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float x0 = fmaf(sv[c], scale_log2, -m), x1 = fmaf(sv[c + 1], scale_log2, -m);
-            float p0, p1;
+            float x0, x1, p0, p1;
+            ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, -m, -m, x0, x1);
             ex2_f16x2(x0, x1, p0, p1);           // two exponentials per SFU instruction
-            ps[(c >> 1) & 3] += p0 + p1;
+            if ((c >> 1) & 1) fadd2(ps[2], ps[3], p0, p1, ps[2], ps[3]);
+            else fadd2(ps[0], ps[1], p0, p1, ps[0], ps[1]);
             pk[c / 2] = pack_bf16x2(p0, p1);
           }
           rs += (ps[0] + ps[1]) + (ps[2] + ps[3]);
