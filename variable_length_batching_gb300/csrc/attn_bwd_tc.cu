@@ -270,7 +270,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       for (int c = 0; c < 32; c += 2) {                    // packed fp32 pairs
         float x0, x1, p0, p1, e0, e1;
         ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, nL, nL, x0, x1);
-        ex2_f16x2(x0, x1, p0, p1);
+        p0 = ex2_approx(x0);
+        p1 = ex2_approx(x1);
         if (!full) {
           if (32 * g + c >= cnt) p0 = 0.f;
           if (32 * g + c + 1 >= cnt) p1 = 0.f;
@@ -464,8 +465,10 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         float x0, x1, x2, x3, p0, p1, p2, p3;
         ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, L4.x, L4.y, x0, x1);
         ffma2(sv[c + 2], sv[c + 3], scale_log2, scale_log2, L4.z, L4.w, x2, x3);
-        ex2_f16x2(x0, x1, p0, p1);
-        ex2_f16x2(x2, x3, p2, p3);
+        p0 = ex2_approx(x0);
+        p1 = ex2_approx(x1);
+        p2 = ex2_approx(x2);
+        p3 = ex2_approx(x3);
         if (!full) {
           if (c < cmin) p0 = 0.f;
           if (c + 1 < cmin) p1 = 0.f;

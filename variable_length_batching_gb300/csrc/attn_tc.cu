@@ -22,8 +22,9 @@
 // to stay within the registers four CTAs leave.  The running max moves only
 // when a tile's max exceeds it by more than 8 (log2 units), so O in TMEM is
 // rescaled in place on those tiles only; PV_{j-1} has completed by then
-// (S_j was issued after it).  Full tiles take their exponentials two at a
-// time on the SFU (f16x2 inputs).
+// (S_j was issued after it).  The softmax is bound by instruction issue, so
+// full tiles use packed fp32 pairs for the exponent FMA and the row sums, a
+// three-input max for the row maximum, and one SFU exponential per element.
 //
 // Cross-attention takes the keys of query segment b from [cu_k[b], cu_k[b+1])
 // ("DanLing NestedTensor" section 3.3: the output adopts the query
@@ -64,6 +65,12 @@ struct Bars {
   int abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 4)
@@ -234,8 +241,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (full) {
           float pm[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-          for (int c = 4; c < 32; ++c) pm[c & 3] = fmaxf(pm[c & 3], sv[c]);
-          mx = fmaxf(mx, fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])));
+          for (int c = 4; c < 28; c += 8) {
+            pm[0] = max3f(pm[0], sv[c], sv[c + 1]);
+            pm[1] = max3f(pm[1], sv[c + 2], sv[c + 3]);
+            pm[2] = max3f(pm[2], sv[c + 4], sv[c + 5]);
+            pm[3] = max3f(pm[3], sv[c + 6], sv[c + 7]);
+          }
+          pm[0] = max3f(pm[0], sv[28], sv[29]);
+          pm[1] = max3f(pm[1], sv[30], sv[31]);
+          mx = max3f(mx, max3f(pm[0], pm[1], pm[2]), pm[3]);
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
@@ -274,14 +288,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_ld_wait();
         uint32_t pk[16];
         if (full) {
-          // exponents, row sums: packed fp32 pairs (two column sums per lane
-          // pair of accumulators)
+          // exponents and row sums in packed fp32 pairs (two pairs of
+          // accumulators); exponentials on the SFU
           float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             float x0, x1, p0, p1;
             ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, -m, -m, x0, x1);
-            ex2_f16x2(x0, x1, p0, p1);           // two exponentials per SFU instruction
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
             if ((c >> 1) & 1) fadd2(ps[2], ps[3], p0, p1, ps[2], ps[3]);
             else fadd2(ps[0], ps[1], p0, p1, ps[0], ps[1]);
             pk[c / 2] = pack_bf16x2(p0, p1);

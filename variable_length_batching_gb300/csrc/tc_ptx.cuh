@@ -344,16 +344,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^x for two values at once on the SFU: x rounded to f16 (11-bit mantissa,
-// so the relative error of 2^x stays near bf16's own rounding step for the
-// x <= 8 the attention softmax produces), ex2.approx.f16x2, back to fp32.
-__device__ __forceinline__ void ex2_f16x2(float x0, float x1, float& p0, float& p1) {
-  uint32_t xh, ph;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(xh) : "f"(x1), "f"(x0));   // x0 in the low half
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(ph) : "r"(xh));
-  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
-      : "=f"(p0), "=f"(p1) : "r"(ph));
-}
 // Packed fp32 pairs (sm_100+ f32x2 arithmetic, round to nearest): one
 // instruction for two lanes' worth of FMA, add or multiply.
 __device__ __forceinline__ void ffma2(float a0, float a1, float b0, float b1, float c0, float c1, float& d0,
