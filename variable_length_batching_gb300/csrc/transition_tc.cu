@@ -112,6 +112,19 @@ __device__ __forceinline__ uint4 fused_z8(const FusedIn& fz, int64_t row, int64_
                     pack_bf16x2(a1.x + b1.x, a1.y + b1.y), pack_bf16x2(a1.z + b1.z, a1.w + b1.w));
 }
 
+// ReLU of a bf16 pair (max with +0 per half); rounding to bf16 keeps the
+// sign, so this equals rounding ReLU(x) itself.
+__device__ __forceinline__ uint32_t relu_bf16x2(uint32_t w) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(0u));
+  return d;
+}
+// Four consecutive fp32 bias values (zeros when there is no bias); b is
+// 16-byte aligned and i a multiple of 4.
+__device__ __forceinline__ float4 bias4(const float* __restrict__ b, int i) {
+  return b ? __ldg(reinterpret_cast<const float4*>(b + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 __device__ __forceinline__ void weight_order(int q, int NC, bool* is_w1, int* c) {
   // consumption order: W1(0), then for each chunk c: W1(c+1) (if any), W2(c)
   if (q == 0) { *is_w1 = true; *c = 0; return; }
@@ -334,18 +347,21 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         // statistics in one pass over the row, shifted by its first element
         // so that E[d^2] - E[d]^2 does not cancel when |mean| >> std
         const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(base + swz128_offset(t, 0, kSubRows)));
-        float s1 = 0.f, s2 = 0.f;
+        // packed fp32 pairs: even and odd features accumulate side by side
+        float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
 #pragma unroll
         for (int ci = 0; ci < 16; ++ci) {
           const uint4 v = *reinterpret_cast<const uint4*>(base + swz128_offset(t, ci * 8, kSubRows));
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float d0 = bf16lo(w[e]) - shift, d1 = bf16hi(w[e]) - shift;
-            s1 += d0 + d1;
-            s2 += d0 * d0 + d1 * d1;
+            float d0, d1;
+            fadd2(bf16lo(w[e]), bf16hi(w[e]), -shift, -shift, d0, d1);
+            fadd2(s1a, s1b, d0, d1, s1a, s1b);
+            ffma2(d0, d1, d0, d1, s2a, s2b, s2a, s2b);
           }
         }
+        const float s1 = s1a + s1b, s2 = s2a + s2b;
         const float m1 = s1 * (1.0f / kCz);
         const float mean = shift + m1;
         const float var = fmaxf(s2 * (1.0f / kCz) - m1 * m1, 0.f);
@@ -363,9 +379,13 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           const float bt[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
           uint32_t o[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            o[e] = pack_bf16x2((bf16lo(w[e]) - mean) * rstd * gg[2 * e] + bt[2 * e],
-                               (bf16hi(w[e]) - mean) * rstd * gg[2 * e + 1] + bt[2 * e + 1]);
+          for (int e = 0; e < 4; ++e) {     // ((x - mean) * rstd) * gamma + beta, packed pairs
+            float y0, y1;
+            fadd2(bf16lo(w[e]), bf16hi(w[e]), -mean, -mean, y0, y1);
+            fmul2(y0, y1, rstd, rstd, y0, y1);
+            ffma2(y0, y1, gg[2 * e], gg[2 * e + 1], bt[2 * e], bt[2 * e + 1], y0, y1);
+            o[e] = pack_bf16x2(y0, y1);
+          }
           *reinterpret_cast<uint4*>(p) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
@@ -402,14 +422,19 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
             tmem_ld_wait();
             uint32_t packed[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int col = c * kHid + 32 * g + 2 * e;
-              const float g0 = gv[2 * e] + (b1 ? __ldg(b1 + col) : 0.f);
-              const float g1 = gv[2 * e + 1] + (b1 ? __ldg(b1 + col + 1) : 0.f);
-              const float v0 = vv[2 * e] + (b3 ? __ldg(b3 + col) : 0.f);
-              const float v1 = vv[2 * e + 1] + (b3 ? __ldg(b3 + col + 1) : 0.f);
-              packed[e] = pack_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * v0,
-                                      __fdividef(g1, 1.0f + __expf(-g1)) * v1);
+            for (int q = 0; q < 8; ++q) {
+              const int col = c * kHid + 32 * g + 4 * q;
+              const float4 bg = bias4(b1, col), bv = bias4(b3, col);
+              float g4[4], v4[4];
+              fadd2(gv[4 * q], gv[4 * q + 1], bg.x, bg.y, g4[0], g4[1]);
+              fadd2(gv[4 * q + 2], gv[4 * q + 3], bg.z, bg.w, g4[2], g4[3]);
+              fadd2(vv[4 * q], vv[4 * q + 1], bv.x, bv.y, v4[0], v4[1]);
+              fadd2(vv[4 * q + 2], vv[4 * q + 3], bv.z, bv.w, v4[2], v4[3]);
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+                packed[2 * q + e] = pack_bf16x2(__fdividef(g4[2 * e], 1.0f + __expf(-g4[2 * e])) * v4[2 * e],
+                                                __fdividef(g4[2 * e + 1], 1.0f + __expf(-g4[2 * e + 1])) *
+                                                    v4[2 * e + 1]);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -424,10 +449,13 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
             tmem_ld_wait();
             uint32_t packed[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int col = c * kChunk + 32 * g + 2 * e;
-              const float bb0 = b1 ? __ldg(b1 + col) : 0.f, bb1 = b1 ? __ldg(b1 + col + 1) : 0.f;
-              packed[e] = pack_bf16x2(fmaxf(v[2 * e] + bb0, 0.f), fmaxf(v[2 * e + 1] + bb1, 0.f));
+            for (int q = 0; q < 8; ++q) {          // + b1 in packed pairs, ReLU on the bf16 pairs
+              const float4 bb = bias4(b1, c * kChunk + 32 * g + 4 * q);
+              float a0, a1, a2, a3;
+              fadd2(v[4 * q], v[4 * q + 1], bb.x, bb.y, a0, a1);
+              fadd2(v[4 * q + 2], v[4 * q + 3], bb.z, bb.w, a2, a3);
+              packed[2 * q] = relu_bf16x2(pack_bf16x2(a0, a1));
+              packed[2 * q + 1] = relu_bf16x2(pack_bf16x2(a2, a3));
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -469,12 +497,15 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint32_t o[4];
+          const float4 bq0 = bias4(b2, 32 * g + 8 * u), bq1 = bias4(b2, 32 * g + 8 * u + 4);
+          const float bb[8] = {bq0.x, bq0.y, bq0.z, bq0.w, bq1.x, bq1.y, bq1.z, bq1.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cl = 32 * g + 8 * u + 2 * e;
+          for (int e = 0; e < 4; ++e) {      // (z + acc2) + b2, packed pairs
             const uint32_t zw = rw[4 * u + e];
-            const float bb0 = b2 ? __ldg(b2 + cl) : 0.f, bb1 = b2 ? __ldg(b2 + cl + 1) : 0.f;
-            o[e] = pack_bf16x2(bf16lo(zw) + v[8 * u + 2 * e] + bb0, bf16hi(zw) + v[8 * u + 2 * e + 1] + bb1);
+            float y0, y1;
+            fadd2(bf16lo(zw), bf16hi(zw), v[8 * u + 2 * e], v[8 * u + 2 * e + 1], y0, y1);
+            fadd2(y0, y1, bb[2 * e], bb[2 * e + 1], y0, y1);
+            o[e] = pack_bf16x2(y0, y1);
           }
           *reinterpret_cast<uint4*>(hs + swz128_offset(r, 32 * g + 8 * u, kSubRows)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
