@@ -82,3 +82,34 @@ def test_attention_backward_full_size_sampled(nt, causal):
     for g, r in zip(got, ref):
         assert normwise_err(to_np(g[idx]), r[rows]) <= TOL["bf16"]
     nt.nt_device_status()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_attention_backward_bad_cu_flagged(nt, dtype):
+    """Offsets whose last entry exceeds T are caught by the kernels' own
+    bounds checks (status word, NT_ERR_DEVICE_CHECK), with no access beyond
+    the buffers, on the tensor-core (bf16) and CUDA-core (fp32) paths."""
+    T, H, d = 64, 1, 64
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = torch.zeros(T, H, d, dtype=tdt, device=DEV)
+    lse = torch.zeros(H, T, dtype=torch.float32, device=DEV)
+    cu_bad = torch.tensor([0, 32, 96], dtype=torch.int32, device=DEV)
+    nt.nt_varlen_attn_bwd(x, x, x, x, x, lse, cu_bad, None, 64)
+    with pytest.raises(nt.NTError) as ei:
+        nt.nt_device_status()
+    assert ei.value.status == 6
+
+
+def test_attention_backward_understated_max_len_flagged(nt):
+    """A longest segment longer than the stated max_len is reported
+    (NT_ERR_DEVICE_CHECK) instead of leaving gradient rows silently unwritten."""
+    lens = [200, 10]
+    a = wl.make_cross_attn_inputs(lens, lens, 2, 64, "bf16", seed=3)
+    q, k, v = a.q.to(DEV), a.k.to(DEV), a.v.to(DEV)
+    cu = torch.as_tensor(_cu(lens)).to(DEV)
+    o, lse = nt.nt_varlen_attn_qk(q, k, v, cu, cu, max(lens), want_lse=True)
+    nt.nt_device_status()
+    nt.nt_varlen_attn_bwd(q, k, v, o, torch.ones_like(o), lse, cu, None, 64)
+    with pytest.raises(nt.NTError) as ei:
+        nt.nt_device_status()
+    assert ei.value.status == 6
