@@ -57,6 +57,7 @@ def _check(o, l, O_ref, lse_ref, dtype):
     ([3, 1, 5, 0, 7, 64, 65, 130], 2, 64, "f32"),
     ([40, 9, 77], 2, 32, "f32"),
     ([40, 9, 77, 200], 2, 128, "bf16"),
+    ([900, 1100], 2, 64, "bf16"),           # mean length > 768: one CTA per (segment, tile, head)
 ])
 def test_causal_self_attention(nt, seqlens, H, d, dtype):
     a, o, l, O_ref, lse_ref = _run(nt, seqlens, seqlens, H, d, dtype, causal=True)
@@ -73,6 +74,7 @@ CROSS = [
     ([256, 100], [40, 300]),
     ([130], [3]),                                           # causal: the first 127 queries see no key
     ([5, 70], [200, 64]),
+    ([1000, 1200], [800, 1500]),                            # mean query length > 768: one CTA per item
 ]
 
 

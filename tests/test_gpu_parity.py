@@ -233,6 +233,8 @@ def _attn_case(nt, seqlens, H, d, dtype, seed=0, lse=True):
     ([40, 9, 77], 2, 32, "f32"),
     ([40, 9, 77], 2, 128, "bf16"),
     ([512], 12, 64, "bf16"),
+    ([1000, 1537], 2, 64, "bf16"),          # mean length > 768: one CTA per (segment, tile, head)
+    ([1, 2000, 3, 0, 5, 2, 1, 7, 9, 4000], 1, 64, "bf16"),   # mean 603: persistent, mostly empty tiles
 ])
 def test_varlen_attention(nt, seqlens, H, d, dtype):
     a, cu, o, l = _attn_case(nt, seqlens, H, d, dtype)
@@ -290,6 +292,14 @@ def test_varlen_attention_bad_cu_flagged(nt):
     q = torch.zeros(T, H, d, dtype=torch.bfloat16, device=DEV)
     cu_bad = torch.tensor([0, 32, 96], dtype=torch.int32, device=DEV)
     nt.nt_varlen_attn(q, q, q, cu_bad, 64)
+    with pytest.raises(nt.NTError) as ei:
+        nt.nt_device_status()
+    assert ei.value.status == 6
+    # the same check on the one-CTA-per-item schedule (mean length > 768)
+    T = 2048
+    q = torch.zeros(T, H, d, dtype=torch.bfloat16, device=DEV)
+    cu_bad = torch.tensor([0, 1000, 2500], dtype=torch.int32, device=DEV)
+    nt.nt_varlen_attn(q, q, q, cu_bad, 1500)
     with pytest.raises(nt.NTError) as ei:
         nt.nt_device_status()
     assert ei.value.status == 6
