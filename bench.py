@@ -440,37 +440,22 @@ def run_gpu(args, rank, world, local_rank):
 
 
 def run_e2e(nt, binp, dev, stream, args):
-    """The block through the binding with the step's inputs in pinned host
-    memory: every step copies the lengths and the singles in and reads z~ and
-    s_out back.  The block's weights are resident on the device, as a model's
-    parameters are, and are copied once before the timed steps.  z~ is final
-    once the transition has run, so its read-back (41 MB, bound by the host
-    link) starts then on a second stream, beside the reduce."""
+    """The block host to host through the package's BlockGraph: every step
+    copies the lengths and the singles in from pinned host memory, rebuilds
+    the partition (a totals read-back), replays the captured broadcast ->
+    transition (three slices, each slice's z~ read back on a second stream as
+    soon as it is done) -> reduce graph, and reads s_out back.  The block's
+    weights are resident on the device, as a model's parameters are."""
+    from variable_length_batching_gb300 import graph
     host = {"lengths": torch.as_tensor(binp.lengths).pin_memory(), "s": binp.s.pin_memory()}
-    wd = _dev_weights(binp.blocks[0], dev)
+    runner = graph.BlockGraph(_dev_weights(binp.blocks[0], dev), slices=3)
     T = int(binp.lengths.sum())
     P = int((binp.lengths.astype(np.int64) ** 2).sum())
-    z_host = torch.empty(P, BLOCK_CFG.C_z, dtype=torch.bfloat16).pin_memory()
-    s_host = torch.empty(T, BLOCK_CFG.C_s, dtype=torch.bfloat16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = z_host.numel() * 2 + s_host.numel() * 2
-
-    copy_stream = torch.cuda.Stream(device=dev)
+    d2h = P * BLOCK_CFG.C_z * 2 + T * BLOCK_CFG.C_s * 2
 
     def one():
-        lengths = host["lengths"].to(dev, non_blocking=True)
-        s = host["s"].to(dev, non_blocking=True)
-        part = nt.nt_partition_build(lengths, stream=stream)
-        z = nt.nt_pair_broadcast(part, s, s, wd.W_a, wd.W_b, stream=stream)
-        nt.nt_pair_transition(part, z, wd.ln_gamma, wd.ln_beta, wd.W1, wd.b1, wd.W2, wd.b2, out=z,
-                              stream=stream)
-        copy_stream.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(copy_stream):
-            z_host.copy_(z, non_blocking=True)
-        m, s_out = nt.nt_pair_reduce(part, z, wd.W_g, wd.b_g, s_in=s, stream=stream)
-        s_host.copy_(s_out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        copy_stream.synchronize()
+        runner.run(host["lengths"], host["s"])
 
     for _ in range(max(args.warmup, 1)):
         one()
@@ -482,8 +467,9 @@ def run_e2e(nt, binp, dev, stream, args):
     dt = (time.perf_counter() - t0) / args.steps
     return {"value": P / dt, "unit": "pair cells/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3,
-            "path": "pinned host -> H2D of lengths and singles -> nt_partition_build/broadcast/transition/reduce "
-                    "-> D2H of z~ (side stream, beside the reduce) and s_out (weights resident on the device)"}
+            "path": "pinned host -> H2D of lengths and singles -> nt_partition_build (totals read-back) -> "
+                    "CUDA-graph replay of broadcast / transition in 3 slices / reduce, with each slice's z~ and "
+                    "then s_out read back (weights resident on the device)"}
 
 
 # ----------------------------------------------------------------------------

@@ -237,6 +237,26 @@ nt_status nt_pair_transition_swiglu(const nt_partition* part, nt_dtype dtype, co
                                     const void* W2, const float* b2, void* stream);
 
 /*
+ * nt_pair_transition_cells -- the transition of nt_pair_transition (W3 NULL)
+ * or nt_pair_transition_swiglu (W3 given) over n_cells consecutive packed
+ * cells, with no partition: the transition maps every cell's feature vector
+ * on its own ("DanLing NestedTensor" section 3.3, dense work across valid
+ * positions), so a caller may run it over any slice [c0, c0 + n_cells) of a
+ * pair state by passing z_in + c0 * C_z and z_out + c0 * C_z, for instance to
+ * read finished slices back while the next one is computed.  Every cell's
+ * result is bit-identical to the whole-state call's.
+ *   n_cells        >= 0 (0 is a no-op, whatever the pointers).
+ *   other arguments as in nt_pair_transition / nt_pair_transition_swiglu
+ *                  (b3 is ignored when W3 is NULL).
+ * Asynchronous; errors as for nt_pair_transition.
+ */
+nt_status nt_pair_transition_cells(int64_t n_cells, nt_dtype dtype, const void* z_in, void* z_out,
+                                   int32_t C_z, int32_t H_t, const float* ln_gamma,
+                                   const float* ln_beta, float ln_eps, const void* W1,
+                                   const float* b1, const void* W3, const float* b3,
+                                   const void* W2, const float* b2, void* stream);
+
+/*
  * nt_pair_reduce -- the column mean of [DL] Eq. 1, third line, as the
  * segmented sum of Eq. 4 divided by the row length M_i (= N_i for square
  * pairs; [DL] Appendix A.1 for the rectangular variant):

@@ -101,6 +101,12 @@ def test_host_side_rejections(L):
     # SwiGLU without its value projection
     assert lib.nt_pair_transition_swiglu(P, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None,
                                          fake, None, None) == 1
+    # transition over a cell range: negative count, bad dtype, misaligned slice; zero cells is a no-op
+    tc = lib.nt_pair_transition_cells
+    assert tc(-1, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None, fake, None, None) == 1
+    assert tc(10, 7, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None, fake, None, None) == 1
+    assert tc(10, 1, odd, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None, fake, None, None) == 1
+    assert tc(0, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None, fake, None, None) == 0
     # W_g without s_out
     assert lib.nt_pair_reduce(P, 1, fake, 128, fake, fake, None, None, None, 384, None) == 1
     # attention: T > 0 without segments; bad head count; T beyond int32

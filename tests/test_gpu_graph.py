@@ -1,0 +1,56 @@
+"""GPU parity of BlockGraph, the host-to-host block step replayed from a
+CUDA graph ("DanLing NestedTensor" Eq. 1): its z~ and s_out equal the eager
+three calls' bit for bit (the transition runs in slices of cells, which is
+cell-for-cell identical), on the first step (eager pass plus capture), on
+replays, and after new lengths force a new capture."""
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+import torch
+
+from variable_length_batching_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def mods():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from variable_length_batching_gb300 import build, graph, nt as ntmod
+    build.build()
+    return ntmod, graph
+
+
+def _eager(nt, inp, wd):
+    part = nt.nt_partition_build(torch.as_tensor(np.asarray(inp.lengths, dtype=np.int32)).to(DEV))
+    z, m, s_out = nt.block_forward(part, inp.s.to(DEV), wd)
+    return z.cpu(), s_out.cpu()
+
+
+def test_block_graph_matches_eager(mods):
+    nt, graph = mods
+    cfg = wl.PAIRFORMER_BF16
+    inp = wl.make_block_inputs(cfg, biases=True)
+    w = inp.blocks[0]
+    g = lambda t: None if t is None else t.to(DEV).contiguous()
+    wd = SimpleNamespace(W_a=g(w.W_a), W_b=g(w.W_b), ln_gamma=g(w.ln_gamma), ln_beta=g(w.ln_beta), W1=g(w.W1),
+                         b1=g(w.b1), W2=g(w.W2), b2=g(w.b2), W_g=g(w.W_g), b_g=g(w.b_g))
+    runner = graph.BlockGraph(wd, slices=3)
+    lengths = torch.as_tensor(np.asarray(inp.lengths, dtype=np.int32)).pin_memory()
+    s = inp.s.pin_memory()
+    z_ref, s_ref = _eager(nt, inp, wd)
+    for _ in range(3):                                   # capture, then two replays
+        z_h, s_h = runner.run(lengths, s)
+        assert torch.equal(z_h, z_ref) and torch.equal(s_h, s_ref)
+    # other lengths: a new capture
+    inp2 = wl.make_block_inputs(cfg, lengths=[64, 1, 200, 0, 37, 5, 128, 90], biases=True)
+    z2_ref, s2_ref = _eager(nt, inp2, wd)
+    for _ in range(2):
+        z_h, s_h = runner.run(torch.as_tensor(np.asarray(inp2.lengths, dtype=np.int32)).pin_memory(),
+                              inp2.s.pin_memory())
+        assert torch.equal(z_h, z2_ref) and torch.equal(s_h, s2_ref)
+    nt.nt_device_status()

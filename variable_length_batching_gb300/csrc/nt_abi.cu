@@ -99,14 +99,15 @@ using namespace nt;
 
 namespace {
 
-// The residual transition with the ReLU update (W3 == NULL) or the SwiGLU one.
-nt_status pair_transition(const nt_partition* part, nt_dtype dtype, const void* z_in, void* z_out, int32_t C_z,
-                          int32_t H_t, const float* ln_gamma, const float* ln_beta, float ln_eps, const void* W1,
-                          const float* b1, const void* W3, const float* b3, const void* W2, const float* b2,
-                          void* stream) {
-  nt_status st = check_partition(part, false);
-  if (st != NT_OK) return st;
+// The residual transition of P cells with the ReLU update (W3 == NULL) or
+// the SwiGLU one.
+nt_status transition_cells(int64_t P, nt_dtype dtype, const void* z_in, void* z_out, int32_t C_z, int32_t H_t,
+                           const float* ln_gamma, const float* ln_beta, float ln_eps, const void* W1,
+                           const float* b1, const void* W3, const float* b3, const void* W2, const float* b2,
+                           void* stream) {
+  if (P < 0) return fail(NT_ERR_INVALID, "cell count %lld < 0", (long long)P);
   if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (P == 0) return NT_OK;                  // nothing to map (the pointers of empty tensors may be NULL)
   if (!width_ok(dtype, C_z) || !width_ok(dtype, H_t))
     return fail(NT_ERR_UNSUPPORTED, "C_z=%d, H_t=%d must be positive multiples of %d", C_z, H_t,
                 dtype == NT_BF16 ? 8 : 4);
@@ -116,21 +117,30 @@ nt_status pair_transition(const nt_partition* part, nt_dtype dtype, const void* 
       !aligned16(ln_gamma) || !aligned16(ln_beta) || !aligned16(b1) || !aligned16(b2) || !aligned16(b3))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
   if (!(ln_eps >= 0.0f)) return fail(NT_ERR_INVALID, "ln_eps must be >= 0");
-  if (part->P == 0) return NT_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (transition_tc_supported(dtype, C_z, H_t, W3 != nullptr)) {
-    e = launch_transition_tc(z_in, z_out, part->P, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W3, b3, W2,
+    e = launch_transition_tc(z_in, z_out, P, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W3, b3, W2,
                              b2, status_word(), s);
     if (e != cudaSuccess) return cuda_fail(e, "transition (tensor core) launch");
     return NT_OK;
   }
   if (sizeof(float) * 8 * (size_t)(C_z + H_t) > 200 * 1024)
     return fail(NT_ERR_UNSUPPORTED, "C_z + H_t = %d too wide for the CUDA-core transition", C_z + H_t);
-  e = launch_transition_simt(dtype, z_in, z_out, part->P, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1,
+  e = launch_transition_simt(dtype, z_in, z_out, P, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1,
                              b1, W3, b3, W2, b2, s);
   if (e != cudaSuccess) return cuda_fail(e, "transition launch");
   return NT_OK;
+}
+
+nt_status pair_transition(const nt_partition* part, nt_dtype dtype, const void* z_in, void* z_out, int32_t C_z,
+                          int32_t H_t, const float* ln_gamma, const float* ln_beta, float ln_eps, const void* W1,
+                          const float* b1, const void* W3, const float* b3, const void* W2, const float* b2,
+                          void* stream) {
+  nt_status st = check_partition(part, false);
+  if (st != NT_OK) return st;
+  return transition_cells(part->P, dtype, z_in, z_out, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W3, b3, W2,
+                          b2, stream);
 }
 
 // u = s_left W_a^T (T rows), v = s_right W_b^T (T_cols rows), fp32.
@@ -317,6 +327,14 @@ nt_status nt_pair_transition_swiglu(const nt_partition* part, nt_dtype dtype, co
   if (!W3) return fail(NT_ERR_INVALID, "W3 (the value projection) is NULL");
   return pair_transition(part, dtype, z_in, z_out, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W3, b3, W2, b2,
                          stream);
+}
+
+nt_status nt_pair_transition_cells(int64_t n_cells, nt_dtype dtype, const void* z_in, void* z_out, int32_t C_z,
+                                   int32_t H_t, const float* ln_gamma, const float* ln_beta, float ln_eps,
+                                   const void* W1, const float* b1, const void* W3, const float* b3,
+                                   const void* W2, const float* b2, void* stream) {
+  return transition_cells(n_cells, dtype, z_in, z_out, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W3, b3, W2,
+                          b2, stream);
 }
 
 nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z, int32_t C_z,

@@ -52,6 +52,8 @@ SIGNATURES = {
     "nt_pair_transition": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P]),
     "nt_pair_transition_swiglu": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                          _P]),
+    "nt_pair_transition_cells": (_I32, [_I64, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
+                                        _P]),
     "nt_pair_reduce": (_I32, [_PP, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P]),
     "nt_pair_block_fused_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
     "nt_pair_block_fused": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
@@ -283,6 +285,29 @@ def nt_pair_transition_swiglu(part: Partition, z: torch.Tensor, ln_gamma: torch.
                                          _ptr(_f32(b1)), _ptr(W3), _ptr(_f32(b3)), _ptr(W2), _ptr(_f32(b2)),
                                          _stream(stream))
     _check(st, "nt_pair_transition_swiglu")
+    return out
+
+
+def nt_pair_transition_cells(z: torch.Tensor, ln_gamma: torch.Tensor, ln_beta: torch.Tensor, W1: torch.Tensor,
+                             b1: Optional[torch.Tensor], W2: torch.Tensor, b2: Optional[torch.Tensor],
+                             W3: Optional[torch.Tensor] = None, b3: Optional[torch.Tensor] = None,
+                             ln_eps: float = 1e-5, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The transition over the cells of ``z`` (any slice of a pair state,
+    rows contiguous), with no partition: ReLU, or SwiGLU when ``W3`` is given.
+    Each cell's result equals the whole-state call's bit for bit."""
+    P, C_z = z.shape
+    H_t = W1.shape[0]
+    if tuple(W1.shape) != (H_t, C_z) or tuple(W2.shape) != (C_z, H_t) or \
+            (W3 is not None and tuple(W3.shape) != (H_t, C_z)):
+        raise ValueError("W1 (and W3) must be (H_t, C_z) and W2 (C_z, H_t)")
+    if not z.is_contiguous():
+        raise ValueError("z must be contiguous")
+    if out is None:
+        out = torch.empty_like(z)
+    st = lib().nt_pair_transition_cells(P, _dtype(z), _ptr(z), _ptr(out), C_z, H_t, _ptr(_f32(ln_gamma)),
+                                        _ptr(_f32(ln_beta)), ln_eps, _ptr(W1), _ptr(_f32(b1)), _ptr(W3),
+                                        _ptr(_f32(b3)), _ptr(W2), _ptr(_f32(b2)), _stream(stream))
+    _check(st, "nt_pair_transition_cells")
     return out
 
 
