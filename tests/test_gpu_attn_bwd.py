@@ -59,6 +59,10 @@ def _case(nt, lq, lk, H, d, dtype, causal, segments=None, seed=7):
     ([3, 300], [200, 17], 3, 64, "bf16", False),                              # cross: 5 key tiles / 1 query tile
     ([511, 1, 256, 129], None, 2, 64, "bf16", True),                           # several 128-key and 64-query tiles
     ([511, 1, 256, 129], None, 2, 64, "bf16", False),
+    ([1000, 1300], None, 2, 64, "bf16", False),                               # mean > 768: one CTA per item
+    ([1000, 1300], None, 2, 64, "bf16", True),
+    ([900, 1000], [1200, 700], 2, 64, "bf16", True),
+    ([1, 2000, 3, 0, 5, 2, 1, 7, 9, 400], None, 1, 64, "bf16", True),          # persistent, mostly empty tiles
 ])
 def test_attention_backward(nt, lq, lk, H, d, dtype, causal):
     lk = lq if lk is None else lk

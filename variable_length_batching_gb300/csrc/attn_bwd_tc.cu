@@ -25,6 +25,8 @@
 // issues), 2-9 = compute, two warps per TMEM lane quadrant, each taking 32
 // of a tile's 64 columns.  256 TMEM columns and about 82 KB of shared memory
 // per CTA: two CTAs share an SM.  Every wait is bounded.
+#include <atomic>
+
 #include "tc_ptx.cuh"
 
 namespace nt {
@@ -132,6 +134,81 @@ __device__ __forceinline__ void init_bars(Bars& bar) {
   bar.abort = 0;
   fence_mbar_init();
   fence_async_shared();
+}
+
+// dQ kernel, one key tile: dS = P * (dP - D) for this thread's query row
+// (segment-local index row_q) over columns [32 g, 32 g + 32), written as bf16
+// pairs over dP's columns.  nL = -lse (log2 units, -inf for a row with no
+// key or past the segment), nD = -D.
+template <bool kCausal>
+__device__ __forceinline__ void dq_tile(uint32_t lane_addr, int g, int j, int n_k, int row_q, int diag,
+                                        float scale_log2, float nL, float nD) {
+  int cnt = min(kBN, n_k - j * kBN);                   // visible keys: a prefix of the tile
+  if (kCausal) cnt = max(0, min(cnt, row_q + diag - j * kBN + 1));
+  const bool full = __all_sync(0xffffffffu, cnt >= 32 * g + 32);
+  float sv[32], dp[32];
+  tmem_ld32(lane_addr + kColS + 32 * g, sv);
+  tmem_ld32(lane_addr + kColP + 32 * g, dp);
+  tmem_ld_wait();
+  uint32_t pk[16];
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {                    // packed fp32 pairs
+    float x0, x1, p0, p1, e0, e1;
+    ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, nL, nL, x0, x1);
+    p0 = ex2_approx(x0);
+    p1 = ex2_approx(x1);
+    if (!full) {
+      if (32 * g + c >= cnt) p0 = 0.f;
+      if (32 * g + c + 1 >= cnt) p1 = 0.f;
+    }
+    fadd2(dp[c], dp[c + 1], nD, nD, e0, e1);           // dP - D
+    fmul2(p0, p1, e0, e1, e0, e1);
+    pk[c / 2] = pack_bf16x2(e0, e1);
+  }
+  tmem_st16_sync(lane_addr + kColP + 32 * g, pk);
+}
+
+// dK/dV kernel, one query tile: P^T and dS^T = P^T * (dP^T - D) for this
+// thread's key row over query columns [32 g, 32 g + 32), written as bf16
+// pairs over S^T's and dP^T's columns.  aux holds this tile's staged -lse
+// (log2 units) and, kBN floats on, -D, from column 32 g; causal: columns
+// below cmin (relative to this half) are masked.
+template <bool kCausal>
+__device__ __forceinline__ void dkv_tile(uint32_t lane_addr, int g, int cmin, const float* aux, float scale_log2) {
+  const bool full = !kCausal || __all_sync(0xffffffffu, cmin <= 0);
+  float sv[32], dp[32];
+  tmem_ld32(lane_addr + kColS + 32 * g, sv);
+  tmem_ld32(lane_addr + kColP + 32 * g, dp);
+  tmem_ld_wait();
+  uint32_t pk[16], ds[16];
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {            // P^T, and dS^T = P^T * (dP^T - D), packed pairs
+    const float4 L4 = *reinterpret_cast<const float4*>(aux + c);         // -lse
+    const float4 D4 = *reinterpret_cast<const float4*>(aux + kBN + c);   // -D
+    float x0, x1, x2, x3, p0, p1, p2, p3;
+    ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, L4.x, L4.y, x0, x1);
+    ffma2(sv[c + 2], sv[c + 3], scale_log2, scale_log2, L4.z, L4.w, x2, x3);
+    p0 = ex2_approx(x0);
+    p1 = ex2_approx(x1);
+    p2 = ex2_approx(x2);
+    p3 = ex2_approx(x3);
+    if (!full) {
+      if (c < cmin) p0 = 0.f;
+      if (c + 1 < cmin) p1 = 0.f;
+      if (c + 2 < cmin) p2 = 0.f;
+      if (c + 3 < cmin) p3 = 0.f;
+    }
+    pk[c / 2] = pack_bf16x2(p0, p1);
+    pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+    fadd2(dp[c], dp[c + 1], D4.x, D4.y, x0, x1);
+    fadd2(dp[c + 2], dp[c + 3], D4.z, D4.w, x2, x3);
+    fmul2(p0, p1, x0, x1, x0, x1);
+    fmul2(p2, p3, x2, x3, x2, x3);
+    ds[c / 2] = pack_bf16x2(x0, x1);
+    ds[c / 2 + 1] = pack_bf16x2(x2, x3);
+  }
+  tmem_st16_sync(lane_addr + kColS + 32 * g, pk);
+  tmem_st16_sync(lane_addr + kColP + 32 * g, ds);
 }
 
 // ============================================================================ dQ
@@ -258,29 +335,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (!(ok = mbar_wait_warp(&bar.s_full, j & 1, abort_flag, status))) break;
       tc_fence_after();
       __syncwarp();
-      int cnt = min(kBN, n_k - j * kBN);                   // visible keys: a prefix of the tile
-      if (kCausal) cnt = max(0, min(cnt, qi * kBM + r + diag - j * kBN + 1));
-      const bool full = __all_sync(0xffffffffu, cnt >= 32 * g + 32);
-      float sv[32], dp[32];
-      tmem_ld32(lane_addr + kColS + 32 * g, sv);
-      tmem_ld32(lane_addr + kColP + 32 * g, dp);
-      tmem_ld_wait();
-      uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {                    // packed fp32 pairs
-        float x0, x1, p0, p1, e0, e1;
-        ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, nL, nL, x0, x1);
-        p0 = ex2_approx(x0);
-        p1 = ex2_approx(x1);
-        if (!full) {
-          if (32 * g + c >= cnt) p0 = 0.f;
-          if (32 * g + c + 1 >= cnt) p1 = 0.f;
-        }
-        fadd2(dp[c], dp[c + 1], nD, nD, e0, e1);           // dP - D
-        fmul2(p0, p1, e0, e1, e0, e1);
-        pk[c / 2] = pack_bf16x2(e0, e1);
-      }
-      tmem_st16_sync(lane_addr + kColP + 32 * g, pk);
+      dq_tile<kCausal>(lane_addr, g, j, n_k, qi * kBM + r, diag, scale_log2, nL, nD);
       tc_fence_before();
       mbar_arrive(&bar.p_full);
     }
@@ -451,41 +506,8 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       const int i0 = i_first + i * kBN;
       // causal: column c (query i0 + c) sees this key when c >= jj - diag - i0
       const int cmin = kCausal ? jj - diag - i0 - 32 * g : 0;   // relative to this half
-      const bool full = !kCausal || __all_sync(0xffffffffu, cmin <= 0);
-      const float* aux = reinterpret_cast<const float*>(smem + kOffAux + st * kAuxBytes) + 32 * g;
-      float sv[32], dp[32];
-      tmem_ld32(lane_addr + kColS + 32 * g, sv);
-      tmem_ld32(lane_addr + kColP + 32 * g, dp);
-      tmem_ld_wait();
-      uint32_t pk[16], ds[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 4) {            // P^T, and dS^T = P^T * (dP^T - D), packed pairs
-        const float4 L4 = *reinterpret_cast<const float4*>(aux + c);         // -lse
-        const float4 D4 = *reinterpret_cast<const float4*>(aux + kBN + c);   // -D
-        float x0, x1, x2, x3, p0, p1, p2, p3;
-        ffma2(sv[c], sv[c + 1], scale_log2, scale_log2, L4.x, L4.y, x0, x1);
-        ffma2(sv[c + 2], sv[c + 3], scale_log2, scale_log2, L4.z, L4.w, x2, x3);
-        p0 = ex2_approx(x0);
-        p1 = ex2_approx(x1);
-        p2 = ex2_approx(x2);
-        p3 = ex2_approx(x3);
-        if (!full) {
-          if (c < cmin) p0 = 0.f;
-          if (c + 1 < cmin) p1 = 0.f;
-          if (c + 2 < cmin) p2 = 0.f;
-          if (c + 3 < cmin) p3 = 0.f;
-        }
-        pk[c / 2] = pack_bf16x2(p0, p1);
-        pk[c / 2 + 1] = pack_bf16x2(p2, p3);
-        fadd2(dp[c], dp[c + 1], D4.x, D4.y, x0, x1);
-        fadd2(dp[c + 2], dp[c + 3], D4.z, D4.w, x2, x3);
-        fmul2(p0, p1, x0, x1, x0, x1);
-        fmul2(p2, p3, x2, x3, x2, x3);
-        ds[c / 2] = pack_bf16x2(x0, x1);
-        ds[c / 2 + 1] = pack_bf16x2(x2, x3);
-      }
-      tmem_st16_sync(lane_addr + kColS + 32 * g, pk);
-      tmem_st16_sync(lane_addr + kColP + 32 * g, ds);
+      dkv_tile<kCausal>(lane_addr, g, cmin, reinterpret_cast<const float*>(smem + kOffAux + st * kAuxBytes) + 32 * g,
+                        scale_log2);
       tc_fence_before();
       mbar_arrive(&bar.p_full);
     }
@@ -519,12 +541,539 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   }
 }
 
+
+// ============================================================================ persistent
+// Persistent forms of the two kernels for short segments: two CTAs per SM
+// take work items from a global counter (one per launch slot).  Lane 0 of
+// the producer warp fetches the next item while the current one's ring is
+// full and publishes it through a two-slot queue in shared memory; the next
+// item's resident tiles are loaded once the current item's last S/dP MMA has
+// completed, and its first accumulating MMA waits until the compute threads
+// have read the accumulators out of TMEM ("acc free").  Output rows are
+// stored directly (the resident buffers already hold the next item's tiles).
+// Every barrier keeps its phase across items.
+
+constexpr int kQueue = 2;
+constexpr int kCounterSlots = 64;
+__device__ unsigned int g_bwd_next[kCounterSlots];
+
+// One work item: segment b's 128-row tile t (keys for dK/dV, queries for dQ)
+// for head h; n = streamed tiles; first = the first streamed token (segment
+// local).  b < 0 ends the queue.
+struct BItem {
+  int b, t, h, n, first;
+  int lo, hi, klo, khi;
+};
+
+struct PBars {
+  uint64_t big_full, big_empty;
+  uint64_t full[kStages], empty[kStages], aux_full[kStages];
+  uint64_t s_full, p_full, p_empty, acc_free;
+  uint64_t it_full[kQueue], it_empty[kQueue];
+  uint64_t mma_done;
+  BItem item[kQueue];
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(PBars) <= 256, "barrier block");
+
+__device__ __forceinline__ void init_pbars(PBars& bar) {
+  mbar_init(&bar.big_full, 1);
+  mbar_init(&bar.big_empty, 1);
+  for (int i = 0; i < kStages; ++i) {
+    mbar_init(&bar.full[i], 1);
+    mbar_init(&bar.empty[i], 1);
+    mbar_init(&bar.aux_full[i], 32);
+  }
+  mbar_init(&bar.s_full, 1);
+  mbar_init(&bar.p_full, 256);
+  mbar_init(&bar.p_empty, 1);
+  mbar_init(&bar.acc_free, 256);
+  for (int i = 0; i < kQueue; ++i) {
+    mbar_init(&bar.it_full[i], 1);
+    mbar_init(&bar.it_empty[i], 9);            // the MMA warp and eight compute warps
+  }
+  mbar_init(&bar.mma_done, 1);
+  bar.abort = 0;
+  fence_mbar_init();
+  fence_async_shared();
+}
+
+// The next valid item from the counter.  kKV: items are (segment, 128-key
+// tile, head) with the query tiles that see the keys; otherwise (segment,
+// 128-query tile, head) with the key tiles the queries see.  Heads vary
+// fastest.  An index whose tile lies past its segment's end moves the counter
+// past the segment's other such indices (all invalid) in one atomicMax.
+template <bool kKV, bool kCausal>
+__device__ BItem fetch_bitem(unsigned int* next, unsigned int total, const int32_t* __restrict__ cu_q,
+                             const int32_t* __restrict__ cu_k, int64_t T_q, int64_t T_k, int H, int NT,
+                             volatile int* abort_flag, unsigned int* status) {
+  BItem it;
+  it.b = -1;
+  while (!*abort_flag) {
+    const unsigned int idx = atomicAdd(next, 1u);
+    if (idx >= total) break;
+    const int h = (int)(idx % (unsigned int)H);
+    const unsigned int rest = idx / (unsigned int)H;
+    // dQ, causal: the longest query tiles (largest index) of a segment first
+    const int t = (!kKV && kCausal) ? NT - 1 - (int)(rest % (unsigned int)NT) : (int)(rest % (unsigned int)NT);
+    const int b = (int)(rest / (unsigned int)NT);
+    const int lo = cu_q[b], hi = cu_q[b + 1], klo = cu_k[b], khi = cu_k[b + 1];
+    if (lo < 0 || hi < lo || hi > T_q || klo < 0 || khi < klo || khi > T_k) {
+      if (t == 0 && h == 0) flag_device(status, kDevCheck);
+      continue;
+    }
+    const int n = hi - lo, n_k = khi - klo;
+    const int own = kKV ? n_k : n;              // rows this kind of item tiles
+    const int diag = n_k - n;
+    if (t == NT - 1 && own > NT * kBM && h == 0) flag_device(status, kDevCheck);
+    const unsigned int seg0 = (unsigned int)b * (unsigned int)NT * (unsigned int)H;
+    if (t * kBM >= own) {
+      const unsigned int tiles = (unsigned int)((own + kBM - 1) / kBM);
+      atomicMax(next, (!kKV && kCausal) ? seg0 + ((unsigned int)NT - tiles) * (unsigned int)H
+                                        : seg0 + (unsigned int)NT * (unsigned int)H);
+      continue;
+    }
+    int first = 0, cnt;
+    if (kKV) {                                  // query tiles of 64 from the first query that sees a key here
+      first = kCausal ? max(0, t * kBM - diag) : 0;
+      cnt = first >= n ? 0 : (n - first + kBN - 1) / kBN;
+    } else {                                    // key tiles of 64 the tile's queries see
+      cnt = (n_k + kBN - 1) / kBN;
+      if (kCausal) {
+        const int last = min(t * kBM + kBM - 1, n - 1) + diag;
+        cnt = last < 0 ? 0 : min(cnt, last / kBN + 1);
+      }
+    }
+    it = BItem{b, t, h, cnt, first, lo, hi, klo, khi};
+    break;
+  }
+  return it;
+}
+
+__device__ __forceinline__ bool publish_bitem(PBars& bar, int n, const BItem& it, volatile int* abort_flag,
+                                              unsigned int* status) {
+  const int slot = n % kQueue;
+  if (!mbar_wait(&bar.it_empty[slot], ((n / kQueue) & 1) ^ 1, abort_flag, status)) return false;
+  bar.item[slot] = it;
+  mbar_arrive(&bar.it_full[slot]);
+  return true;
+}
+
+// Item n for a consumer warp; lane 0 releases the slot once the warp holds it.
+__device__ __forceinline__ bool take_bitem(PBars& bar, int n, volatile int* abort_flag, unsigned int* status,
+                                           BItem& it) {
+  const int slot = n % kQueue;
+  if (!mbar_wait_warp(&bar.it_full[slot], (n / kQueue) & 1, abort_flag, status)) return false;
+  it = bar.item[slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&bar.it_empty[slot]);
+  return true;
+}
+
+// Broadcast lane 0's item to the warp.
+__device__ __forceinline__ BItem shfl_bitem(BItem it) {
+  int* f = reinterpret_cast<int*>(&it);
+#pragma unroll
+  for (int i = 0; i < 9; ++i) f[i] = __shfl_sync(0xffffffffu, f[i], 0);
+  return it;
+}
+
+__device__ __forceinline__ void store_half32(bf16* dst, const float* v, float mul) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul);
+    w.y = pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul);
+    w.z = pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul);
+    w.w = pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul);
+    *reinterpret_cast<uint4*>(dst + 8 * u) = w;
+  }
+}
+__device__ __forceinline__ void zero_half32(bf16* dst) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(dst + 8 * u) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ---------------------------------------------------------------------------- dK, dV persistent
+template <bool kCausal>
+__global__ void __launch_bounds__(kThreads, 2)
+attn_bwd_dkv_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                        const float* __restrict__ lse, const float* __restrict__ Dbuf,
+                        const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B, int64_t T_q,
+                        int64_t T_k, int H, int KT, float scale, bf16* __restrict__ dk, bf16* __restrict__ dv,
+                        unsigned int* next, unsigned int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023) {
+    if (threadIdx.x == 0) flag_device(status, kDevCheck);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = smem_raw;
+  PBars& bar = *reinterpret_cast<PBars*>(smem + kOffBar);
+  volatile int* abort_flag = &bar.abort;
+  if (threadIdx.x == 0) init_pbars(bar);
+  if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  const unsigned int total = (unsigned int)B * (unsigned int)KT * (unsigned int)H;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer and scheduler
+    // Lane 0 waits and issues the copies; the whole warp stages each query
+    // tile's -lse and -D.  Lanes 1-31 learn of lane 0's progress through warp
+    // shuffles, so they never poll a barrier.
+    if (lane == 0) { prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_q); prefetch_tmap(&tm_do); }
+    int gt = 0, kvc = 0, issued = 0;
+    BItem cur;
+    bool ok = true;
+    if (lane == 0) {
+      cur = fetch_bitem<true, kCausal>(next, total, cu_q, cu_k, T_q, T_k, H, KT, abort_flag, status);
+      ok = publish_bitem(bar, 0, cur, abort_flag, status);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    cur = shfl_bitem(cur);
+    for (int n = 0; ok && cur.b >= 0; ++n) {
+      const int n_q = cur.hi - cur.lo;
+      if (cur.n > 0) {
+        if (lane == 0) {
+          // K and V of this item once the previous item's last S^T / dP^T are computed
+          ok = mbar_wait(&bar.big_empty, (kvc & 1) ^ 1, abort_flag, status);
+          if (ok) {
+            mbar_arrive_expect_tx(&bar.big_full, 2 * kBigBytes);
+            tma_load_3d(smem + kOffBig0, &tm_k, &bar.big_full, 0, cur.h, cur.klo + cur.t * kBM);
+            tma_load_3d(smem + kOffBig1, &tm_v, &bar.big_full, 0, cur.h, cur.klo + cur.t * kBM);
+          }
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        ++kvc;
+      }
+      BItem nxt;
+      nxt.b = -1;
+      for (int i = 0; i <= cur.n && ok; ++i) {
+        if (i == min(cur.n, kStages)) {         // the next item, while the ring is full
+          if (lane == 0) {
+            nxt = fetch_bitem<true, kCausal>(next, total, cu_q, cu_k, T_q, T_k, H, KT, abort_flag, status);
+            ok = publish_bitem(bar, n + 1, nxt, abort_flag, status);
+          }
+          if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+          nxt = shfl_bitem(nxt);
+        }
+        if (i == cur.n) break;
+        const int st = gt % kStages;
+        const int i0 = cur.first + i * kBN;
+        if (lane == 0) {
+          ok = mbar_wait(&bar.empty[st], ((gt / kStages) & 1) ^ 1, abort_flag, status);
+          if (ok) {
+            uint8_t* ring = smem + kOffRing + st * 2 * kSmallBytes;
+            mbar_arrive_expect_tx(&bar.full[st], 2 * kSmallBytes);
+            tma_load_3d(ring, &tm_q, &bar.full[st], 0, cur.h, cur.lo + i0);
+            tma_load_3d(ring + kSmallBytes, &tm_do, &bar.full[st], 0, cur.h, cur.lo + i0);
+            issued = gt + 1;
+          }
+        }
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        float* aux = reinterpret_cast<float*>(smem + kOffAux + st * kAuxBytes);
+        for (int c = lane; c < kBN; c += 32) {
+          float nLc = -INFINITY, nDc = 0.f;
+          if (i0 + c < n_q) {
+            const int64_t t = (int64_t)cur.lo + i0 + c;
+            const float l = lse[(int64_t)cur.h * T_q + t], dvv = Dbuf[(int64_t)cur.h * T_q + t];
+            if (l != -INFINITY) {
+              nLc = -l * kLog2e;
+              nDc = -dvv;
+            }
+          }
+          aux[c] = nLc;
+          aux[kBN + c] = nDc;
+        }
+        mbar_arrive(&bar.aux_full[st]);
+        ++gt;
+      }
+      cur = nxt;
+    }
+    if (lane == 0) {
+      if (kvc > 0) mbar_wait(&bar.big_full, (kvc - 1) & 1, nullptr, status);
+      for (int j = issued - kStages; j < issued; ++j)
+        if (j >= 0) mbar_wait(&bar.full[j % kStages], (j / kStages) & 1, nullptr, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t id_kk = idesc_bf16_f32(128, kBN);
+    const uint32_t id_mn = idesc_bf16_f32(128, kD) | (1u << 16);
+    const uint32_t k_base = smem_u32(smem + kOffBig0), v_base = smem_u32(smem + kOffBig1);
+    const bool leader = elect_one();
+    int gt = 0, kvc = 0;
+    bool ok = true;
+    BItem it;
+    for (int n = 0; ok && (ok = take_bitem(bar, n, abort_flag, status, it)); ++n) {
+      if (it.b < 0) break;
+      if (it.n == 0) continue;
+      if (!(ok = mbar_wait_warp(&bar.big_full, kvc & 1, abort_flag, status))) break;
+      for (int i = 0; i < it.n && ok; ++i, ++gt) {
+        const int st = gt % kStages;
+        const uint32_t qb = smem_u32(smem + kOffRing + st * 2 * kSmallBytes), dob = qb + kSmallBytes;
+        if (!(ok = mbar_wait_warp(&bar.full[st], (gt / kStages) & 1, abort_flag, status))) break;
+        if (gt > 0 && !(ok = mbar_wait_warp(&bar.p_empty, (gt - 1) & 1, abort_flag, status))) break;
+        tc_fence_after();
+        if (leader) {
+          mma_kmajor(tmem + kColS, k_base, qb, id_kk);      // S^T  = K Q_i^T
+          mma_kmajor(tmem + kColP, v_base, dob, id_kk);     // dP^T = V dO_i^T
+          mma_commit(&bar.s_full);
+          if (i == it.n - 1) mma_commit(&bar.big_empty);  // K and V are free once these complete
+        }
+        __syncwarp();
+        if (!(ok = mbar_wait_warp(&bar.p_full, gt & 1, abort_flag, status))) break;
+        // the item's first accumulation overwrites dV, dK: the previous item's were read
+        if (i == 0 && kvc > 0 && !(ok = mbar_wait_warp(&bar.acc_free, (kvc - 1) & 1, abort_flag, status))) break;
+        tc_fence_after();
+        if (leader) {
+          mma_ts_mn(tmem + kColAcc0, tmem + kColS, dob, id_mn, i > 0);   // dV += P^T dO_i
+          mma_ts_mn(tmem + kColAcc1, tmem + kColP, qb, id_mn, i > 0);    // dK += dS^T Q_i
+          mma_commit(&bar.p_empty);
+          mma_commit(&bar.empty[st]);
+        }
+        __syncwarp();
+      }
+      ++kvc;
+    }
+    if (leader) mma_commit(&bar.mma_done);
+    __syncwarp();
+    mbar_wait_warp(&bar.mma_done, 0, nullptr, status);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int qd = warp & 3, g = (warp - 2) >> 2;
+    const int r = qd * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    const float scale_log2 = scale * kLog2e;
+    int gt = 0;
+    bool ok = true;
+    BItem it;
+    for (int n = 0; ok && (ok = take_bitem(bar, n, abort_flag, status, it)); ++n) {
+      if (it.b < 0) break;
+      const int n_q = it.hi - it.lo, n_k = it.khi - it.klo, diag = n_k - n_q;
+      const int jj = it.t * kBM + r;             // segment-local key of this lane
+      const int64_t row = (int64_t)it.klo + jj;
+      if (it.n == 0) {                           // no query sees these keys: no gradient
+        if (jj < n_k) {
+          zero_half32(dk + (row * H + it.h) * kD + 32 * g);
+          zero_half32(dv + (row * H + it.h) * kD + 32 * g);
+        }
+        continue;
+      }
+      for (int i = 0; i < it.n; ++i, ++gt) {
+        const int st = gt % kStages;
+        if (!(ok = mbar_wait_warp(&bar.s_full, gt & 1, abort_flag, status))) break;
+        if (!(ok = mbar_wait_warp(&bar.aux_full[st], (gt / kStages) & 1, abort_flag, status))) break;
+        tc_fence_after();
+        __syncwarp();
+        const int i0 = it.first + i * kBN;
+        const int cmin = kCausal ? jj - diag - i0 - 32 * g : 0;
+        dkv_tile<kCausal>(lane_addr, g, cmin,
+                          reinterpret_cast<const float*>(smem + kOffAux + st * kAuxBytes) + 32 * g, scale_log2);
+        tc_fence_before();
+        mbar_arrive(&bar.p_full);
+      }
+      if (!ok) break;
+      if (!(ok = mbar_wait_warp(&bar.p_empty, (gt - 1) & 1, abort_flag, status))) break;
+      tc_fence_after();
+      __syncwarp();
+      float av[32], ak[32];
+      tmem_ld32(lane_addr + kColAcc0 + 32 * g, av);
+      tmem_ld32(lane_addr + kColAcc1 + 32 * g, ak);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bar.acc_free);               // the next item may overwrite dV, dK
+      if (jj < n_k) {
+        store_half32(dv + (row * H + it.h) * kD + 32 * g, av, 1.0f);
+        store_half32(dk + (row * H + it.h) * kD + 32 * g, ak, scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------- dQ persistent
+template <bool kCausal>
+__global__ void __launch_bounds__(kThreads, 2)
+attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const float* __restrict__ lse, const float* __restrict__ Dbuf,
+                       const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B, int64_t T_q,
+                       int64_t T_k, int H, int QT, float scale, bf16* __restrict__ dq, unsigned int* next,
+                       unsigned int* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023) {
+    if (threadIdx.x == 0) flag_device(status, kDevCheck);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = smem_raw;
+  PBars& bar = *reinterpret_cast<PBars*>(smem + kOffBar);
+  volatile int* abort_flag = &bar.abort;
+  if (threadIdx.x == 0) init_pbars(bar);
+  if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  const unsigned int total = (unsigned int)B * (unsigned int)QT * (unsigned int)H;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer and scheduler (lane 0)
+    if (lane == 0) {
+      prefetch_tmap(&tm_q); prefetch_tmap(&tm_do); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
+      int gt = 0, qc = 0, issued = 0;
+      BItem cur = fetch_bitem<false, kCausal>(next, total, cu_q, cu_k, T_q, T_k, H, QT, abort_flag, status);
+      bool ok = publish_bitem(bar, 0, cur, abort_flag, status);
+      for (int n = 0; ok && cur.b >= 0; ++n) {
+        if (cur.n > 0) {
+          // Q and dO of this item once the previous item's last S / dP are computed
+          if (!(ok = mbar_wait(&bar.big_empty, (qc & 1) ^ 1, abort_flag, status))) break;
+          const int q0 = cur.lo + cur.t * kBM;
+          mbar_arrive_expect_tx(&bar.big_full, 2 * kBigBytes);
+          tma_load_3d(smem + kOffBig0, &tm_q, &bar.big_full, 0, cur.h, q0);
+          tma_load_3d(smem + kOffBig1, &tm_do, &bar.big_full, 0, cur.h, q0);
+          ++qc;
+        }
+        BItem nxt;
+        nxt.b = -1;
+        for (int j = 0; j <= cur.n && ok; ++j) {
+          if (j == min(cur.n, kStages)) {
+            nxt = fetch_bitem<false, kCausal>(next, total, cu_q, cu_k, T_q, T_k, H, QT, abort_flag, status);
+            if (!(ok = publish_bitem(bar, n + 1, nxt, abort_flag, status))) break;
+          }
+          if (j == cur.n) break;
+          const int st = gt % kStages;
+          if (!(ok = mbar_wait(&bar.empty[st], ((gt / kStages) & 1) ^ 1, abort_flag, status))) break;
+          uint8_t* ring = smem + kOffRing + st * 2 * kSmallBytes;
+          mbar_arrive_expect_tx(&bar.full[st], 2 * kSmallBytes);
+          tma_load_3d(ring, &tm_k, &bar.full[st], 0, cur.h, cur.klo + j * kBN);
+          tma_load_3d(ring + kSmallBytes, &tm_v, &bar.full[st], 0, cur.h, cur.klo + j * kBN);
+          issued = gt + 1;
+          ++gt;
+        }
+        cur = nxt;
+      }
+      if (qc > 0) mbar_wait(&bar.big_full, (qc - 1) & 1, nullptr, status);
+      for (int j = issued - kStages; j < issued; ++j)
+        if (j >= 0) mbar_wait(&bar.full[j % kStages], (j / kStages) & 1, nullptr, status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t id_kk = idesc_bf16_f32(128, kBN);
+    const uint32_t id_mn = idesc_bf16_f32(128, kD) | (1u << 16);
+    const uint32_t q_base = smem_u32(smem + kOffBig0), do_base = smem_u32(smem + kOffBig1);
+    const bool leader = elect_one();
+    int gt = 0, qc = 0;
+    bool ok = true;
+    BItem it;
+    for (int n = 0; ok && (ok = take_bitem(bar, n, abort_flag, status, it)); ++n) {
+      if (it.b < 0) break;
+      if (it.n == 0) continue;
+      if (!(ok = mbar_wait_warp(&bar.big_full, qc & 1, abort_flag, status))) break;
+      for (int j = 0; j < it.n && ok; ++j, ++gt) {
+        const int st = gt % kStages;
+        const uint32_t kb = smem_u32(smem + kOffRing + st * 2 * kSmallBytes), vb = kb + kSmallBytes;
+        if (!(ok = mbar_wait_warp(&bar.full[st], (gt / kStages) & 1, abort_flag, status))) break;
+        if (gt > 0 && !(ok = mbar_wait_warp(&bar.p_empty, (gt - 1) & 1, abort_flag, status))) break;
+        tc_fence_after();
+        if (leader) {
+          mma_kmajor(tmem + kColS, q_base, kb, id_kk);       // S  = Q K_j^T
+          mma_kmajor(tmem + kColP, do_base, vb, id_kk);      // dP = dO V_j^T
+          mma_commit(&bar.s_full);
+          if (j == it.n - 1) mma_commit(&bar.big_empty);   // Q and dO are free once these complete
+        }
+        __syncwarp();
+        if (!(ok = mbar_wait_warp(&bar.p_full, gt & 1, abort_flag, status))) break;
+        if (j == 0 && qc > 0 && !(ok = mbar_wait_warp(&bar.acc_free, (qc - 1) & 1, abort_flag, status))) break;
+        tc_fence_after();
+        if (leader) {
+          mma_ts_mn(tmem + kColAcc0, tmem + kColP, kb, id_mn, j > 0);   // dQ += dS K_j
+          mma_commit(&bar.p_empty);
+          mma_commit(&bar.empty[st]);
+        }
+        __syncwarp();
+      }
+      ++qc;
+    }
+    if (leader) mma_commit(&bar.mma_done);
+    __syncwarp();
+    mbar_wait_warp(&bar.mma_done, 0, nullptr, status);
+  } else {
+    // ------------------------------------------------------------ compute
+    const int qd = warp & 3, g = (warp - 2) >> 2;
+    const int r = qd * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    const float scale_log2 = scale * kLog2e;
+    int gt = 0;
+    bool ok = true;
+    BItem it;
+    for (int n = 0; ok && (ok = take_bitem(bar, n, abort_flag, status, it)); ++n) {
+      if (it.b < 0) break;
+      const int n_q = it.hi - it.lo, n_k = it.khi - it.klo, diag = n_k - n_q;
+      const int64_t t = (int64_t)it.lo + it.t * kBM + r;
+      if (it.n == 0) {                           // no query here sees a key: no gradient
+        if (t < it.hi) zero_half32(dq + (t * H + it.h) * kD + 32 * g);
+        continue;
+      }
+      // rows past the segment, and rows that saw no key: P = 0 (-lse -> -inf)
+      float nL = -INFINITY, nD = 0.f;
+      if (t < it.hi) {
+        const float l = lse[(int64_t)it.h * T_q + t], dvv = Dbuf[(int64_t)it.h * T_q + t];
+        if (l != -INFINITY) {
+          nL = -l * kLog2e;
+          nD = -dvv;
+        }
+      }
+      for (int j = 0; j < it.n; ++j, ++gt) {
+        if (!(ok = mbar_wait_warp(&bar.s_full, gt & 1, abort_flag, status))) break;
+        tc_fence_after();
+        __syncwarp();
+        dq_tile<kCausal>(lane_addr, g, j, n_k, it.t * kBM + r, diag, scale_log2, nL, nD);
+        tc_fence_before();
+        mbar_arrive(&bar.p_full);
+      }
+      if (!ok) break;
+      if (!(ok = mbar_wait_warp(&bar.p_empty, (gt - 1) & 1, abort_flag, status))) break;
+      tc_fence_after();
+      __syncwarp();
+      float acc[32];
+      tmem_ld32(lane_addr + kColAcc0 + 32 * g, acc);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bar.acc_free);               // the next item may overwrite dQ
+      if (t < it.hi) store_half32(dq + (t * H + it.h) * kD + 32 * g, acc, scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 bool make_map_thd(CUtensorMap* map, const void* ptr, int64_t T, int H, uint32_t rows) {
   const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)T};
   const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};
   const uint32_t box[3] = {(uint32_t)kD, 1, rows};
   return make_tmap_bf16(map, ptr, 3, dims, strides, box);
 }
+
+std::atomic<unsigned int> g_bwd_slot{0};
 
 }  // namespace
 
@@ -542,16 +1091,55 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsig
   const int KT = max(1, (p.max_len_k + kBM - 1) / kBM);
   const int64_t items_q = (int64_t)p.B * QT * p.H, items_k = (int64_t)p.B * KT * p.H;
   if (items_q > 0x7fffffffLL || items_k > 0x7fffffffLL) return cudaErrorInvalidValue;
-  auto kq = p.causal ? attn_bwd_dq_kernel<true> : attn_bwd_dq_kernel<false>;
-  auto kkv = p.causal ? attn_bwd_dkv_kernel<true> : attn_bwd_dkv_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
-  kkv<<<(unsigned)items_k, kThreads, kSmemBytes, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
-                                                       p.T_q, p.T_k, p.H, KT, p.scale, (bf16*)p.dk, (bf16*)p.dv,
-                                                       status);
-  kq<<<(unsigned)items_q, kThreads, kSmemBytes, s>>>(q128, do128, k64, v64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
-                                                     p.T_q, p.T_k, p.H, QT, p.scale, (bf16*)p.dq, status);
+  const int slots = 2 * sm_count();
+  cudaError_t e = cudaSuccess;
+  // Persistent CTAs over a work counter where items are short (mean length
+  // up to 768 tokens on the side a kernel tiles) and uneven (the longest
+  // segment over 1.25 times the mean); one CTA per item otherwise, where the
+  // hardware scheduler balances the work and the staged, row-contiguous
+  // epilogue of the per-item kernels pays.
+  const bool pkv = p.T_k <= (int64_t)768 * p.B && (int64_t)4 * p.max_len_k * p.B > (int64_t)5 * p.T_k;
+  const bool pq = p.T_q <= (int64_t)768 * p.B && (int64_t)4 * p.max_len_q * p.B > (int64_t)5 * p.T_q;
+  unsigned int* counters = nullptr;
+  if (pkv || pq) {
+    void* base = nullptr;
+    e = cudaGetSymbolAddress(&base, g_bwd_next);
+    if (e != cudaSuccess) return e;
+    const unsigned int slot = (g_bwd_slot.fetch_add(2) % kCounterSlots) & ~1u;
+    counters = static_cast<unsigned int*>(base) + slot;
+    e = cudaMemsetAsync(counters, 0, 2 * sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+  }
+  if (pkv) {
+    auto kkv = p.causal ? attn_bwd_dkv_persistent<true> : attn_bwd_dkv_persistent<false>;
+    e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kkv<<<(unsigned)min64(items_k, slots), kThreads, kSmemBytes, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q,
+                                                                       p.cu_k, p.B, p.T_q, p.T_k, p.H, KT, p.scale,
+                                                                       (bf16*)p.dk, (bf16*)p.dv, counters, status);
+  } else {
+    auto kkv = p.causal ? attn_bwd_dkv_kernel<true> : attn_bwd_dkv_kernel<false>;
+    e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kkv<<<(unsigned)items_k, kThreads, kSmemBytes, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
+                                                         p.T_q, p.T_k, p.H, KT, p.scale, (bf16*)p.dk, (bf16*)p.dv,
+                                                         status);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (pq) {
+    auto kq = p.causal ? attn_bwd_dq_persistent<true> : attn_bwd_dq_persistent<false>;
+    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kq<<<(unsigned)min64(items_q, slots), kThreads, kSmemBytes, s>>>(q128, do128, k64, v64, p.lse, Dbuf, p.cu_q,
+                                                                      p.cu_k, p.B, p.T_q, p.T_k, p.H, QT, p.scale,
+                                                                      (bf16*)p.dq, counters + 1, status);
+  } else {
+    auto kq = p.causal ? attn_bwd_dq_kernel<true> : attn_bwd_dq_kernel<false>;
+    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kq<<<(unsigned)items_q, kThreads, kSmemBytes, s>>>(q128, do128, k64, v64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
+                                                       p.T_q, p.T_k, p.H, QT, p.scale, (bf16*)p.dq, status);
+  }
   return cudaGetLastError();
 }
 
