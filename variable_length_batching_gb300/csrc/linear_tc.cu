@@ -4,9 +4,13 @@
 // 3.3 "Dense work across valid positions") over the T packed single rows.
 //
 // One CTA per 128 x 128 output tile (and per problem: u and v run in one
-// launch).  Warp 0 streams 64-wide K blocks of X and W through a 2-stage
-// TMA ring, warp 1 issues the MMAs into a 128-column TMEM accumulator, and
-// all four warps run the epilogue: TMEM -> +bias (+residual) -> global.
+// launch).  Warp 0 streams 64-wide K blocks of X and W through a TMA ring
+// of up to six stages, warp 1 issues the MMAs into a 128-column TMEM
+// accumulator, and all four warps run the epilogue: TMEM -> +bias
+// (+residual) -> global.  The grids are small (tens of CTAs for the
+// block's projections), so each CTA's chain of copies sets the time: the
+// ring holds every K block of a C_s = 384 contraction at once, and one
+// round of copies replaces three.
 #include "tc_ptx.cuh"
 
 namespace nt {
@@ -18,10 +22,11 @@ constexpr int kBM = 128, kBN = 128, kBK = 64;
 constexpr int kThreads = 128;
 constexpr uint32_t kOpBytes = 128 * kBK * 2;          // 16 KB per operand block
 constexpr uint32_t kStageBytes = 2 * kOpBytes;        // X block + W block
-constexpr uint32_t kSmemBytes = 2 * kStageBytes + 128;
+constexpr int kMaxStages = 6;
+constexpr uint32_t kBarBytes = 256;
 
 struct Bars {
-  uint64_t full[2], empty[2], acc_full;
+  uint64_t full[kMaxStages], empty[kMaxStages], acc_full;
   uint32_t tmem_base;
   int abort;
 };
@@ -36,7 +41,7 @@ template <bool kOutF32>
 __global__ void __launch_bounds__(kThreads)
 linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant__ CUtensorMap tw0,
                  const __grid_constant__ CUtensorMap tx1, const __grid_constant__ CUtensorMap tw1, Prob p0, Prob p1,
-                 int64_t M, int N, int K, unsigned int* status) {
+                 int64_t M, int N, int K, int stages, unsigned int* status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023) {
     if (threadIdx.x == 0) flag_device(status, kDevCheck);
@@ -45,7 +50,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
   const CUtensorMap* tx = blockIdx.z == 0 ? &tx0 : &tx1;
   const CUtensorMap* tw = blockIdx.z == 0 ? &tw0 : &tw1;
   const Prob& pr = blockIdx.z == 0 ? p0 : p1;
-  Bars& bar = *reinterpret_cast<Bars*>(smem + 2 * kStageBytes);
+  Bars& bar = *reinterpret_cast<Bars*>(smem + stages * kStageBytes);
   volatile int* abort_flag = &bar.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m0 = (int64_t)blockIdx.x * kBM;
@@ -53,7 +58,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
   const int nkb = K / kBK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
+    for (int i = 0; i < stages; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
     mbar_init(&bar.acc_full, 1);
     bar.abort = 0;
     fence_mbar_init();
@@ -68,21 +73,21 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
   if (warp == 0 && lane == 0) {
     int issued = 0;
     for (int kb = 0; kb < nkb; ++kb) {
-      const int st = kb & 1;
-      if (!mbar_wait(&bar.empty[st], ((kb >> 1) & 1) ^ 1, abort_flag, status)) break;
+      const int st = kb % stages;
+      if (!mbar_wait(&bar.empty[st], ((kb / stages) & 1) ^ 1, abort_flag, status)) break;
       mbar_arrive_expect_tx(&bar.full[st], kStageBytes);
       tma_load_2d(smem + st * kStageBytes, tx, &bar.full[st], kb * kBK, (int)m0);
       tma_load_2d(smem + st * kStageBytes + kOpBytes, tw, &bar.full[st], kb * kBK, n0);
       issued = kb + 1;
     }
-    for (int kb = issued - 2; kb < issued; ++kb)
-      if (kb >= 0) mbar_wait(&bar.full[kb & 1], (kb >> 1) & 1, nullptr, status);
+    for (int kb = issued - stages; kb < issued; ++kb)
+      if (kb >= 0) mbar_wait(&bar.full[kb % stages], (kb / stages) & 1, nullptr, status);
   } else if (warp == 1 && lane == 0) {
     const uint32_t idesc = idesc_bf16_f32(kBM, kBN);
     const uint32_t base = smem_u32(smem);
     for (int kb = 0; kb < nkb; ++kb) {
-      const int st = kb & 1;
-      if (!mbar_wait(&bar.full[st], (kb >> 1) & 1, abort_flag, status)) break;
+      const int st = kb % stages;
+      if (!mbar_wait(&bar.full[st], (kb / stages) & 1, abort_flag, status)) break;
       tc_fence_after();
       const uint32_t a = base + st * kStageBytes, b = a + kOpBytes;
       for (int k = 0; k < kBK / 16; ++k)
@@ -167,15 +172,21 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
     pp[i] = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y};
   }
   dim3 grid((unsigned)((M + kBM - 1) / kBM), N / kBN, nprob);
+  const int stages = min(K / kBK, kMaxStages);
+  const uint32_t smem = stages * kStageBytes + kBarBytes;
   cudaError_t e;
   if (out_f32) {
-    e = cudaFuncSetAttribute(linear_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(linear_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kMaxStages * kStageBytes + kBarBytes));
     if (e != cudaSuccess) return e;
-    linear_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tx[0], tw[0], tx[1], tw[1], pp[0], pp[1], M, N, K, status);
+    linear_tc_kernel<true><<<grid, kThreads, smem, s>>>(tx[0], tw[0], tx[1], tw[1], pp[0], pp[1], M, N, K, stages,
+                                                        status);
   } else {
-    e = cudaFuncSetAttribute(linear_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(linear_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kMaxStages * kStageBytes + kBarBytes));
     if (e != cudaSuccess) return e;
-    linear_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tx[0], tw[0], tx[1], tw[1], pp[0], pp[1], M, N, K, status);
+    linear_tc_kernel<false><<<grid, kThreads, smem, s>>>(tx[0], tw[0], tx[1], tw[1], pp[0], pp[1], M, N, K, stages,
+                                                         status);
   }
   return cudaGetLastError();
 }
