@@ -90,6 +90,10 @@ struct FusedIn {
   const int32_t* col_cu;
   int64_t T;
   float* m_acc;
+  const int64_t* pair_off;   // B + 1 cell offsets of the samples
+  const int32_t* cu;         // B + 1 row offsets
+  const int32_t* col_len;    // M_i
+  int B;
 };
 
 // Pair row holding packed cell p (< P): the last r with row_start[r] <= p.
@@ -100,6 +104,23 @@ __device__ __forceinline__ int64_t row_of(const int64_t* __restrict__ row_start,
     if (row_start[mid] <= p) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// Pair row and column single of packed cell p (< P): the sample by a binary
+// search over the B cell offsets (the last one <= p, which steps past
+// samples with no cells; a few steps, cached), then the row and column
+// within the sample's N_i x M_i block by one division.
+__device__ __forceinline__ void cell_of(const FusedIn& fz, int64_t p, int64_t& row, int64_t& vrow) {
+  int lo = 0, hi = fz.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(fz.pair_off + mid) <= p) lo = mid; else hi = mid - 1;
+  }
+  const int64_t off = p - __ldg(fz.pair_off + lo);
+  const int64_t m = __ldg(fz.col_len + lo);
+  const int64_t a = off / m;
+  row = __ldg(fz.cu + lo) + a;
+  vrow = __ldg(fz.col_cu + lo) + (off - a * m);
 }
 
 // bf16 pairs of z = u[row] + v[col] for features [f0, f0 + 8) of cell p.
@@ -335,8 +356,8 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           uint8_t* base = sA + s * kSubBytes;
           const int64_t p = tile * kTileRows + s * kSubRows + t;
           if (p < P) {
-            const int64_t row = row_of(fz.row_start, fz.T, p);
-            const int64_t vrow = fz.col_cu[fz.row_sample[row]] + (p - fz.row_start[row]);
+            int64_t row, vrow;
+            cell_of(fz, p, row, vrow);
 #pragma unroll 4
             for (int ci = 0; ci < 16; ++ci)
               *reinterpret_cast<uint4*>(base + swz128_offset(t, ci * 8, kSubRows)) = fused_z8(fz, row, vrow, ci * 8);
@@ -484,8 +505,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       const bf16* zr = z_in + row_g * kCz;
       int64_t f_row = 0, f_vrow = 0;        // fused: the cell's pair row and column single
       if (kFused && in_range) {
-        f_row = row_of(fz.row_start, fz.T, row_g);
-        f_vrow = fz.col_cu[fz.row_sample[f_row]] + (row_g - fz.row_start[f_row]);
+        cell_of(fz, row_g, f_row, f_vrow);
       }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -635,7 +655,7 @@ cudaError_t launch_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t
   if (e != cudaSuccess) return e;
   const int64_t tiles = (P + kTileRows - 1) / kTileRows;
   const int grid = (int)min64(tiles, (int64_t)sm_count());
-  const FusedIn none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr};
+  const FusedIn none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, 0};
   kern<<<grid, kThreads, kSmemBytes, s>>>(m_zin, m_zout, m_w1, m_w3, m_w2, (const bf16*)z_in, P, H_t, gamma, beta,
                                           eps, b1, b3, b2, fused ? *fused : none, status);
   return cudaGetLastError();
@@ -654,7 +674,8 @@ cudaError_t launch_block_fused_tc(const float* u, const float* v, const nt_parti
                                   int H_t, const float* gamma, const float* beta, float eps, const void* W1,
                                   const float* b1, const void* W3, const float* b3, const void* W2, const float* b2,
                                   float* m_acc, unsigned int* status, cudaStream_t s) {
-  const FusedIn fz = {u, v, part->row_start, part->row_sample, col_cu_of(part), part->T, m_acc};
+  const FusedIn fz = {u,      v,        part->row_start, part->row_sample,     col_cu_of(part), part->T,
+                      m_acc,  part->pair_off, part->cu_seqlens, col_lengths_of(part), part->B};
   return launch_tc(nullptr, z_out, part->P, C_z, H_t, gamma, beta, eps, W1, b1, W3, b3, W2, b2, &fz, status, s);
 }
 
