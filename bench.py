@@ -301,10 +301,11 @@ def run_gpu(args, rank, world, local_rank):
     names = ("partition", "broadcast", "transition", "reduce", "attention")
 
     def step(ev):
-        # ev[0..1] bracket the partition build (it ends with the host reading
-        # the totals back); ev[2..6] bracket the four device-only calls.
+        # ev[0..1] bracket the partition build (scan and row splits in one
+        # call, bounded by the singles' row count; it ends with the host
+        # reading the totals back); ev[2..6] bracket the four device-only calls.
         ev[0].record(stream)
-        p = nt.nt_partition_build(lengths_d, stream=stream)
+        p = nt.nt_partition_build(lengths_d, stream=stream, T=s_d.shape[0])
         ev[1].record(stream)
         # The partition's readback left the stream idle.  A short device
         # sleep, outside every timed interval, lets the host enqueue the next
@@ -777,7 +778,8 @@ def run_only(args):
         es = 2 if cfg.dtype == wl.BF16 else 4
         bw = block_work(part.T, part.P, cfg.C_s, cfg.C_z, cfg.H_t, es)
         fns = {
-            "partition": (lambda: nt.nt_partition_build(lengths, stream=stream), bw["partition"], "latency"),
+            "partition": (lambda: nt.nt_partition_build(lengths, stream=stream, T=s.shape[0]), bw["partition"],
+                          "latency"),
             "broadcast": (lambda: nt.nt_pair_broadcast(part, s, s, wd.W_a, wd.W_b, z=z, workspace=ws,
                                                        stream=stream), bw["broadcast"], "hbm"),
             "transition": (lambda: nt.nt_pair_transition(part, z, wd.ln_gamma, wd.ln_beta, wd.W1, wd.b1, wd.W2,

@@ -140,6 +140,25 @@ nt_status nt_partition_build_rect(const int32_t* d_rows, const int32_t* d_cols, 
 nt_status nt_partition_rows(nt_partition* part, int64_t* d_row_start, int32_t* d_row_sample,
                             void* stream);
 
+/*
+ * nt_partition_build_with_rows -- nt_partition_build and nt_partition_rows
+ * in one call and one host round trip: the row-split kernel follows the scan
+ * in the stream and reads T and P from d_totals, so only the totals come
+ * back to the host.  For callers that know an upper bound on T, such as the
+ * row count of the packed singles they hold.
+ *   T_cap          >= 0; d_row_start holds T_cap + 1 entries and d_row_sample
+ *                  max(T_cap, 1).  Device writes never go past them.
+ *   other arguments as in nt_partition_build / nt_partition_rows; on NT_OK
+ *                  *out is filled including row_start and row_sample.
+ * Returns NT_ERR_INVALID if the lengths sum to more than T_cap (the row
+ * splits are then incomplete; *out still holds the totals), and the errors
+ * of nt_partition_build.  Synchronises `stream` once.
+ */
+nt_status nt_partition_build_with_rows(const int32_t* d_lengths, int32_t B, int64_t T_cap,
+                                       int32_t* d_cu_seqlens, int64_t* d_pair_off, int64_t* d_totals,
+                                       int64_t* d_row_start, int32_t* d_row_sample,
+                                       nt_partition* out, void* stream);
+
 /* Bytes of device workspace nt_pair_broadcast needs for a square partition:
  * the two projected single representations u and v in fp32, 2 * T * C_z * 4. */
 size_t nt_pair_broadcast_workspace_bytes(int64_t T, int32_t C_z);

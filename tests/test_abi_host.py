@@ -101,6 +101,12 @@ def test_host_side_rejections(L):
     # SwiGLU without its value projection
     assert lib.nt_pair_transition_swiglu(P, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None,
                                          fake, None, None) == 1
+    # partition with row splits in one call: NULL out, negative B or capacity, NULL row buffers
+    pw = lib.nt_partition_build_with_rows
+    assert pw(fake, 4, 16, fake, fake, fake, fake, fake, None, None) == 1
+    assert pw(fake, -1, 16, fake, fake, fake, fake, fake, P, None) == 1
+    assert pw(fake, 4, -1, fake, fake, fake, fake, fake, P, None) == 1
+    assert pw(fake, 4, 16, fake, fake, fake, None, fake, P, None) == 1
     # transition over a cell range: negative count, bad dtype, misaligned slice; zero cells is a no-op
     tc = lib.nt_pair_transition_cells
     assert tc(-1, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None, fake, None, None) == 1

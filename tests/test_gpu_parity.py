@@ -2,6 +2,7 @@
 inputs.  Partitions are compared bit for bit; floats normwise,
 max|gpu - oracle| / max|oracle| <= 2e-2 (bf16 I/O, fp32 accumulation) or
 1e-5 (fp32 mode), per output tensor."""
+import ctypes
 from types import SimpleNamespace
 
 import numpy as np
@@ -60,6 +61,47 @@ def test_partition_bit_exact(nt, lengths):
     assert np.array_equal(part.row_start.cpu().numpy(), ref.row_start)
     if ref.T:
         assert np.array_equal(part.row_sample[: ref.T].cpu().numpy(), ref.row_sample)
+    nt.nt_device_status()
+
+
+@pytest.mark.parametrize("lengths", [[3, 0, 5, 1, 130, 7], [0, 0], [4], list(range(1, 200))])
+def test_partition_with_rows_matches_two_calls(nt, lengths):
+    """nt_partition_build_with_rows (row splits after the scan in the stream,
+    T and P from the device totals) equals the two-call partition bit for
+    bit, with an exact capacity and with a larger one."""
+    ref = nt.nt_partition_build(dev_lengths(lengths))
+    T = int(sum(lengths))
+    for cap in (T, T + 37):
+        got = nt.nt_partition_build(dev_lengths(lengths), T=cap)
+        assert (got.T, got.P, got.max_len) == (ref.T, ref.P, ref.max_len)
+        for a, b in ((got.cu_seqlens, ref.cu_seqlens), (got.pair_off, ref.pair_off)):
+            assert torch.equal(a, b)
+        assert torch.equal(got.row_start[:T + 1], ref.row_start)
+        if T:
+            assert torch.equal(got.row_sample[:T], ref.row_sample[:T])
+    nt.nt_device_status()
+
+
+def test_partition_with_rows_small_capacity_rejected(nt):
+    """A capacity below the lengths' sum is reported (NT_ERR_INVALID) after
+    the totals come back; the row-split kernel writes nothing past the
+    buffers it was given."""
+    lengths = [64, 100, 3]
+    guard = torch.full((64,), -7, dtype=torch.int64, device=DEV)
+    buf = torch.empty(50 + 1 + 64, dtype=torch.int64, device=DEV)
+    buf[51:] = guard
+    with pytest.raises(nt.NTError) as ei:
+        c = nt.nt_partition()
+        L = dev_lengths(lengths)
+        cu = torch.empty(4, dtype=torch.int32, device=DEV)
+        po = torch.empty(4, dtype=torch.int64, device=DEV)
+        tot = torch.empty(4, dtype=torch.int64, device=DEV)
+        rs = torch.empty(64, dtype=torch.int32, device=DEV)
+        st = nt.lib().nt_partition_build_with_rows(nt._ptr(L), 3, 50, nt._ptr(cu), nt._ptr(po), nt._ptr(tot),
+                                                   nt._ptr(buf), nt._ptr(rs), ctypes.byref(c), nt._stream(None))
+        nt._check(st, "nt_partition_build_with_rows")
+    assert ei.value.status == 1
+    assert torch.equal(buf[51:], guard)          # nothing written past row_start's 51 entries
     nt.nt_device_status()
 
 

@@ -255,6 +255,49 @@ nt_status nt_partition_build_rect(const int32_t* d_rows, const int32_t* d_cols, 
   return NT_OK;
 }
 
+nt_status nt_partition_build_with_rows(const int32_t* d_lengths, int32_t B, int64_t T_cap, int32_t* d_cu_seqlens,
+                                       int64_t* d_pair_off, int64_t* d_totals, int64_t* d_row_start,
+                                       int32_t* d_row_sample, nt_partition* out, void* stream) {
+  if (!out) return fail(NT_ERR_INVALID, "out is NULL");
+  if (B < 0) return fail(NT_ERR_INVALID, "B = %d < 0", B);
+  if (T_cap < 0) return fail(NT_ERR_INVALID, "T_cap = %lld < 0", (long long)T_cap);
+  if ((B > 0 && !d_lengths) || !d_cu_seqlens || !d_pair_off || !d_totals || !d_row_start ||
+      (T_cap > 0 && !d_row_sample))
+    return fail(NT_ERR_INVALID, "NULL device pointer");
+  if (!aligned16(d_totals) || !aligned16(d_pair_off) || !aligned16(d_cu_seqlens) || !aligned16(d_row_start) ||
+      !aligned16(d_row_sample))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, s);
+  if (e == cudaSuccess)
+    e = launch_partition_rows_dev(d_lengths, nullptr, d_cu_seqlens, d_pair_off, B, d_totals, T_cap, d_row_start,
+                                  d_row_sample, s);
+  if (e != cudaSuccess) return cuda_fail(e, "partition launch");
+  int64_t tot[4] = {0, 0, 0, 0};
+  e = cudaMemcpyAsync(tot, d_totals, sizeof(tot), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
+  out->B = B;
+  out->T = tot[0];
+  out->P = tot[1];
+  out->max_len = (int32_t)tot[2];
+  out->lengths = d_lengths;
+  out->cu_seqlens = d_cu_seqlens;
+  out->pair_off = d_pair_off;
+  out->row_start = d_row_start;
+  out->row_sample = d_row_sample;
+  out->col_lengths = d_lengths;
+  out->col_cu_seqlens = d_cu_seqlens;
+  out->T_cols = tot[0];
+  out->max_col_len = (int32_t)tot[2];
+  if (tot[3] & 1) return fail(NT_ERR_INVALID, "a sample length is negative");
+  if (tot[3] & 2) return fail(NT_ERR_OVERFLOW, "T = %lld does not fit int32 cu_seqlens", (long long)tot[0]);
+  if (tot[0] > T_cap)
+    return fail(NT_ERR_INVALID, "the lengths sum to T = %lld > T_cap = %lld: row splits incomplete",
+                (long long)tot[0], (long long)T_cap);
+  return NT_OK;
+}
+
 nt_status nt_partition_rows(nt_partition* part, int64_t* d_row_start, int32_t* d_row_sample,
                             void* stream) {
   nt_status st = check_partition(part, false);

@@ -99,6 +99,11 @@ cudaError_t launch_partition_scan(const int32_t* lengths, const int32_t* cols, i
 cudaError_t launch_partition_rows(const int32_t* lengths, const int32_t* cols, const int32_t* cu,
                                   const int64_t* pair_off, int32_t B, int64_t T, int64_t P, int64_t* row_start,
                                   int32_t* row_sample, cudaStream_t s);
+// Row splits after the scan in the same stream, T and P from the device
+// totals, writes bounded by the capacity cap (rows of row_start: cap + 1).
+cudaError_t launch_partition_rows_dev(const int32_t* lengths, const int32_t* cols, const int32_t* cu,
+                                      const int64_t* pair_off, int32_t B, const int64_t* totals, int64_t cap,
+                                      int64_t* row_start, int32_t* row_sample, cudaStream_t s);
 
 // Y[M, N] = X[M, K] W[N, K]^T (+ bias[N]) (+ R[M, N]).  Up to two independent
 // problems in one launch (gridDim.z); all row-major, contiguous.

@@ -130,7 +130,44 @@ __global__ void partition_rows_kernel(const int32_t* __restrict__ lengths, const
   if (blockIdx.x == 0 && threadIdx.x == 0) row_start[T] = P;
 }
 
+// The same row splits with T and P read from the scan's device totals, so
+// the kernel can follow the scan in the stream without a host round trip.
+// Writes are bounded by the caller's capacity `cap` (rows of row_start
+// beyond it, and negative offsets from invalid lengths, are skipped; the
+// host reports the shortfall after reading the totals back).
+__global__ void partition_rows_dev_kernel(const int32_t* __restrict__ lengths, const int32_t* __restrict__ cols,
+                                          const int32_t* __restrict__ cu, const int64_t* __restrict__ pair_off,
+                                          int32_t B, const int64_t* __restrict__ totals, int64_t cap,
+                                          int64_t* __restrict__ row_start, int32_t* __restrict__ row_sample) {
+  for (int i = blockIdx.x; i < B; i += gridDim.x) {
+    const int64_t n = lengths[i];
+    const int64_t mcols = cols ? cols[i] : n;
+    const int64_t c0 = cu[i];
+    const int64_t o = pair_off[i];
+    for (int64_t a = threadIdx.x; a < n; a += blockDim.x) {
+      const int64_t r = c0 + a;
+      if (r >= 0 && r < cap) {
+        row_start[r] = o + a * mcols;
+        row_sample[r] = i;
+      }
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const int64_t T = totals[0];
+    if (T >= 0 && T <= cap) row_start[T] = totals[1];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_partition_rows_dev(const int32_t* lengths, const int32_t* cols, const int32_t* cu,
+                                      const int64_t* pair_off, int32_t B, const int64_t* totals, int64_t cap,
+                                      int64_t* row_start, int32_t* row_sample, cudaStream_t s) {
+  const int grid = B < 4096 ? (B > 0 ? B : 1) : 4096;
+  partition_rows_dev_kernel<<<grid, 256, 0, s>>>(lengths, cols, cu, pair_off, B, totals, cap, row_start,
+                                                 row_sample);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_partition_scan(const int32_t* lengths, const int32_t* cols, int32_t B, int32_t* cu,
                                   int32_t* cu_cols, int64_t* pair_off, int64_t* totals, cudaStream_t s) {

@@ -2,8 +2,8 @@
 host inputs and outputs, replayed from a CUDA graph.
 
 Each step copies the sample lengths and the singles in from pinned host
-memory and rebuilds the partition (its totals come back to the host: they
-decide the pair state's size).  Everything after that has fixed sizes for a
+memory and rebuilds the partition in one call (its totals come back to the
+host: they decide the pair state's size).  Everything after that has fixed sizes for a
 given (B, T, P) and runs as one captured graph: the broadcast, the
 transition in slices of cells (each slice's z~ copied back to the host on a
 second stream as soon as it is done, so the read-back overlaps the next
@@ -60,16 +60,15 @@ class BlockGraph:
         self.key = None
 
     def _partition(self, stream) -> "_nt.Partition":
+        # scan and row splits in one call (the singles' row count bounds T)
         c = _nt.nt_partition()
-        lib = _nt.lib()
-        st = lib.nt_partition_build(_nt._ptr(self.lengths) if self.B else None, self.B, _nt._ptr(self.cu),
-                                    _nt._ptr(self.pair_off), _nt._ptr(self.totals), ctypes.byref(c),
-                                    _nt._stream(stream))
-        _nt._check(st, "nt_partition_build")
+        st = _nt.lib().nt_partition_build_with_rows(
+            _nt._ptr(self.lengths) if self.B else None, self.B, self.T, _nt._ptr(self.cu), _nt._ptr(self.pair_off),
+            _nt._ptr(self.totals), _nt._ptr(self.row_start), _nt._ptr(self.row_sample), ctypes.byref(c),
+            _nt._stream(stream))
+        _nt._check(st, "nt_partition_build_with_rows")
         if c.T != self.T:
             raise ValueError(f"the lengths sum to {c.T}, the singles have {self.T} rows")
-        _nt._check(lib.nt_partition_rows(ctypes.byref(c), _nt._ptr(self.row_start), _nt._ptr(self.row_sample),
-                                         _nt._stream(stream)), "nt_partition_rows")
         return _nt.Partition(self.lengths, self.cu, self.pair_off, self.totals, self.row_start, self.row_sample, c)
 
     # -- the captured part ---------------------------------------------------------

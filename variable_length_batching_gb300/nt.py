@@ -52,6 +52,7 @@ SIGNATURES = {
     "nt_pair_transition": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P]),
     "nt_pair_transition_swiglu": (_I32, [_PP, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                          _P]),
+    "nt_partition_build_with_rows": (_I32, [_P, _I32, _I64, _P, _P, _P, _P, _P, _PP, _P]),
     "nt_pair_transition_cells": (_I32, [_I64, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                         _P]),
     "nt_pair_reduce": (_I32, [_PP, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P]),
@@ -153,9 +154,11 @@ class Partition:
     def max_len(self): return self.c.max_len
 
 
-def nt_partition_build(lengths: torch.Tensor, stream=None) -> Partition:
+def nt_partition_build(lengths: torch.Tensor, stream=None, T: Optional[int] = None) -> Partition:
     """Sizes N_i (int32, on the device) -> cu_seqlens, pair offsets and the
-    second-level row splits (``nt_partition_build`` + ``nt_partition_rows``)."""
+    second-level row splits (``nt_partition_build`` + ``nt_partition_rows``).
+    ``T``, when the caller knows the lengths' sum (the packed singles' row
+    count), selects ``nt_partition_build_with_rows``: one host round trip."""
     if lengths.dtype != torch.int32:
         raise ValueError("lengths must be int32")
     dev = lengths.device
@@ -164,6 +167,14 @@ def nt_partition_build(lengths: torch.Tensor, stream=None) -> Partition:
     pair_off = torch.empty(B + 1, dtype=torch.int64, device=dev)
     totals = torch.empty(4, dtype=torch.int64, device=dev)
     c = nt_partition()
+    if T is not None:
+        row_start = torch.empty(int(T) + 1, dtype=torch.int64, device=dev)
+        row_sample = torch.empty(max(int(T), 1), dtype=torch.int32, device=dev)
+        st = lib().nt_partition_build_with_rows(_ptr(lengths) if B else None, B, int(T), _ptr(cu), _ptr(pair_off),
+                                                _ptr(totals), _ptr(row_start), _ptr(row_sample), ctypes.byref(c),
+                                                _stream(stream))
+        _check(st, "nt_partition_build_with_rows")
+        return Partition(lengths, cu, pair_off, totals, row_start, row_sample, c)
     st = lib().nt_partition_build(_ptr(lengths) if B else None, B, _ptr(cu), _ptr(pair_off),
                                   _ptr(totals), ctypes.byref(c), _stream(stream))
     _check(st, "nt_partition_build")
