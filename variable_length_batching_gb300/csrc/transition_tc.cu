@@ -13,27 +13,38 @@
 // chunk (half the weight traffic of 128-row tiles).
 //
 // Warp roles (14 warps):
-//   warp 0        TMA producer: z tile (4 boxes of 64 x 128) into A; weight
-//                 chunks of 128 x 128 through a 3-stage ring.
+//   warp 0        TMA producer: z tile (4 boxes of 64 x 128) into one of two
+//                 input slots; weight chunks of 128 x 128 through a 3-stage
+//                 ring, in the order W1(0), W2(0), W1(1), ...
 //   warp 1        TMEM owner and MMA issuer (one thread).
-//   warps 2-5     LayerNorm, in place on the TMA-loaded tile in A.
+//   warps 2-5     LayerNorm, in place on the tile in its input slot.
 //   warps 6-9     epilogue of sub-tile 0; warps 10-13 of sub-tile 1: TMEM
-//                 -> +b1, ReLU -> bf16 hidden chunk in H; at the end TMEM ->
-//                 +b2 + residual -> bf16 into H -> TMA store.
-// TMEM (512 columns): acc1[s] = GEMM1 chunk of sub-tile s at 128*s,
-// acc2[s] = output accumulator of sub-tile s at 256 + 128*s.
+//                 -> +b1, ReLU -> the bf16 hidden chunk written back over
+//                 the columns it came from; at the end TMEM -> +b2 +
+//                 residual -> bf16, staged in the tile's input slot -> TMA
+//                 store.
+// TMEM (512 columns): acc1[s] = GEMM1 chunk of sub-tile s at 128*s (and,
+// once the epilogue has read it, the hidden chunk as bf16 pairs over its
+// first columns), acc2[s] = output accumulator of sub-tile s at 256 + 128*s.
+// GEMM2 takes the hidden chunk as its A operand straight from TMEM (B = the
+// W2 chunk from shared memory), half by half as the epilogue writes it, so
+// the hidden chunk never passes through shared memory; GEMM1 of the next
+// chunk of a sub-tile waits until that sub-tile's GEMM2 has read it.  The
+// shared memory this frees holds a second input slot: the next tile's z load
+// and LayerNorm run while the current tile computes.  A slot is released by
+// the tile's last GEMM1s and both sub-tiles' output stores.
 // SwiGLU: hidden chunks are 64 units wide; a GEMM1 weight tile stacks those
 // 64 rows of W1 (gate) over the same 64 rows of W3 (value), so one N = 128
 // MMA leaves gate and value side by side in acc1, the epilogue writes the
-// 64-wide product SiLU(gate + b1) * (value + b3), and GEMM2 contracts it
-// with a 128 x 64 slice of W2 (K = 64).
+// 64-wide product SiLU(gate + b1) * (value + b3) back over the gate, and
+// GEMM2 contracts it with a 128 x 64 slice of W2 (K = 64).
 // Every operand tile is K-major with the 128-byte swizzle that TMA writes.
 //
 // Fused block (a second template flag; "DanLing NestedTensor" Eq. 1 as one
 // pass over the pair state): z never exists in HBM.  The LayerNorm warps
 // build each tile as bf16(u[row] + v[col]) from the two projected single
 // representations (fp32, L2-resident), with (row, col) of packed cell p
-// found from the partition's row splits; the output epilogue recomputes the
+// found from the sample offsets; the output epilogue recomputes the
 // same bf16 z for the residual; and after staging z~ for its TMA store the
 // epilogue threads sum their feature column over the tile's cells, flushing
 // one fp32 atomic add per pair row touched into m_acc (Eq. 4's column sum).
@@ -56,23 +67,21 @@ constexpr int kStages = 3;
 constexpr int kThreads = 14 * 32;
 constexpr uint32_t kBlockBytes = kSubRows * 128;          // one 64-column block: 16 KB
 constexpr uint32_t kSubBytes = 2 * kBlockBytes;           // 128 x 128 bf16: 32 KB
-constexpr uint32_t kABytes = 2 * kSubBytes;               // z / LN(z) tile: 64 KB
-constexpr uint32_t kHBytes = 2 * kSubBytes;               // hidden chunk per sub-tile: 64 KB
+constexpr uint32_t kABytes = 2 * kSubBytes;               // z / LN(z) tile: 64 KB (two slots)
 constexpr uint32_t kWBytes = kChunk * kCz * 2;            // one weight chunk: 32 KB
 constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffH = kOffA + kABytes;
-constexpr uint32_t kOffW = kOffH + kHBytes;
+constexpr uint32_t kOffW = kOffA + 2 * kABytes;
 constexpr uint32_t kOffLN = kOffW + kStages * kWBytes;    // gamma, beta: 1 KB
 constexpr uint32_t kOffBar = kOffLN + 2 * kCz * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;     // + barriers + alignment slack
 
 struct Bars {
-  uint64_t z_full, a_full, a_empty;
+  uint64_t z_full[2], a_full[2], a_empty[2];       // per input slot
   uint64_t w_full[kStages], w_empty[kStages];
-  uint64_t acc1_full[2], acc1_empty[2];
-  uint64_t h_full[2], h_empty[2];
+  uint64_t acc1_full[2], g2_done[2];               // per sub-tile
+  uint64_t h_full[2][2];                           // per sub-tile, per half of the hidden chunk
   uint64_t acc2_full[2], acc2_empty[2];
-  uint64_t out_ready[2], store_done[2];
+  uint64_t out_ready[2];
   uint64_t colsum_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -154,21 +163,6 @@ __device__ __forceinline__ float4 bias4(const float* __restrict__ b, int i) {
   return b ? __ldg(reinterpret_cast<const float4*>(b + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-__device__ __forceinline__ void weight_order(int q, int NC, bool* is_w1, int* c) {
-  // consumption order: W1(0), then for each chunk c: W1(c+1) (if any), W2(c)
-  if (q == 0) { *is_w1 = true; *c = 0; return; }
-  const int qq = q - 1;
-  if (NC == 1) { *is_w1 = false; *c = 0; return; }
-  const int pairs = NC - 1;                 // chunks c = 0..NC-2 bring a W1(c+1)
-  if (qq < 2 * pairs) {
-    *c = qq / 2;
-    if ((qq & 1) == 0) { *is_w1 = true; *c += 1; } else { *is_w1 = false; }
-    return;
-  }
-  *is_w1 = false;
-  *c = NC - 1;
-}
-
 template <bool kGLU, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_constant__ CUtensorMap tm_zout,
@@ -182,7 +176,6 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sA = smem + kOffA;
-  uint8_t* sH = smem + kOffH;
   uint8_t* sW = smem + kOffW;
   float* sGamma = reinterpret_cast<float*>(smem + kOffLN);
   float* sBeta = sGamma + kCz;
@@ -194,15 +187,17 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
   const int64_t num_tiles = (P + kTileRows - 1) / kTileRows;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar.z_full, 1);
-    mbar_init(&bar.a_full, 128);
-    mbar_init(&bar.a_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.z_full[i], 1);
+      mbar_init(&bar.a_full[i], 128);
+      mbar_init(&bar.a_empty[i], 3);           // the tile's last GEMM1s + both sub-tiles' output stores
+    }
     for (int i = 0; i < kStages; ++i) { mbar_init(&bar.w_full[i], 1); mbar_init(&bar.w_empty[i], 1); }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar.acc1_full[s], 1); mbar_init(&bar.acc1_empty[s], 128);
-      mbar_init(&bar.h_full[s], 128); mbar_init(&bar.h_empty[s], 1);
+      mbar_init(&bar.acc1_full[s], 1); mbar_init(&bar.g2_done[s], 1);
+      mbar_init(&bar.h_full[s][0], 128); mbar_init(&bar.h_full[s][1], 128);
       mbar_init(&bar.acc2_full[s], 1); mbar_init(&bar.acc2_empty[s], 128);
-      mbar_init(&bar.out_ready[s], 128); mbar_init(&bar.store_done[s], 1);
+      mbar_init(&bar.out_ready[s], 128);
       mbar_init(&bar.colsum_done[s], 128);
     }
     mbar_init(&bar.mma_done, 1);
@@ -223,22 +218,26 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       prefetch_tmap(&tm_zin); prefetch_tmap(&tm_w1); prefetch_tmap(&tm_w2); prefetch_tmap(&tm_zout);
       if (kGLU) prefetch_tmap(&tm_w3);
       int load_idx = 0;
-      int last_tile_j = -1;
+      int last_j[2] = {-1, -1};                  // the last tile whose z each slot received
       bool ok = true;
       int j = 0;
       for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
+        const int slot = j & 1;
         if (!kFused) {   // the fused block builds its z tile in the LayerNorm warps
-          if (!(ok = mbar_wait(&bar.a_empty, (j & 1) ^ 1, abort_flag, status))) break;
-          mbar_arrive_expect_tx(&bar.z_full, kABytes);
+          if (!(ok = mbar_wait(&bar.a_empty[slot], ((j >> 1) & 1) ^ 1, abort_flag, status))) break;
+          uint8_t* a = sA + slot * kABytes;
+          mbar_arrive_expect_tx(&bar.z_full[slot], kABytes);
           const int row0 = (int)(tile * kTileRows);
           for (int s = 0; s < 2; ++s)
             for (int kb = 0; kb < 2; ++kb)
-              tma_load_2d(sA + s * kSubBytes + kb * kBlockBytes, &tm_zin, &bar.z_full, kb * 64, row0 + s * kSubRows);
-          last_tile_j = j;
+              tma_load_2d(a + s * kSubBytes + kb * kBlockBytes, &tm_zin, &bar.z_full[slot], kb * 64,
+                          row0 + s * kSubRows);
+          last_j[slot] = j;
         }
+        // weights in consumption order: W1(c), W2(c), W1(c + 1), ...
         for (int q = 0; q < 2 * NC; ++q) {
-          bool w1; int c;
-          weight_order(q, NC, &w1, &c);
+          const bool w1 = (q & 1) == 0;
+          const int c = q >> 1;
           const int stage = load_idx % kStages, round = load_idx / kStages;
           if (!(ok = mbar_wait(&bar.w_empty[stage], (round & 1) ^ 1, abort_flag, status))) break;
           uint8_t* dst = sW + stage * kWBytes;
@@ -269,16 +268,21 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         }
       }
       // drain: every copy this thread issued has landed before the CTA exits
-      if (last_tile_j >= 0) mbar_wait(&bar.z_full, last_tile_j & 1, nullptr, status);
+      for (int sl = 0; sl < 2; ++sl)
+        if (last_j[sl] >= 0) mbar_wait(&bar.z_full[sl], (last_j[sl] >> 1) & 1, nullptr, status);
       for (int l = load_idx - kStages; l < load_idx; ++l)
         if (l >= 0) mbar_wait(&bar.w_full[l % kStages], (l / kStages) & 1, nullptr, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per chunk c: GEMM1 of both sub-tiles (each once GEMM2 of chunk c - 1 on
+    // that sub-tile has read the hidden chunk out of acc1), then GEMM2 of
+    // both (each once the epilogue has written the hidden chunk over acc1).
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, 128);
-      const uint32_t a_base = smem_u32(sA), h_base = smem_u32(sH), w_base = smem_u32(sW);
+      const uint32_t w_base = smem_u32(sW);
       int load_idx = 0;
+      int g2n[2] = {0, 0};                        // GEMM2s issued per sub-tile
       bool ok = true;
       int j = 0;
       auto take_w = [&](uint32_t* wsm) -> bool {
@@ -292,46 +296,46 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         mma_commit(&bar.w_empty[load_idx % kStages]);
         ++load_idx;
       };
-      auto gemm1 = [&](int s, int it, uint32_t wsm) -> bool {
-        if (!mbar_wait(&bar.acc1_empty[s], (it & 1) ^ 1, abort_flag, status)) return false;
-        tc_fence_after();
-        for (int k = 0; k < kCz / 16; ++k) {
-          const uint32_t koff = (k >> 2) * kBlockBytes + (k & 3) * 32;
-          mma_bf16(tmem + 128 * s, sdesc_k128(a_base + s * kSubBytes + koff), sdesc_k128(wsm + koff), idesc,
-                   k > 0);
-        }
-        mma_commit(&bar.acc1_full[s]);
-        return true;
-      };
       for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
-        if (!(ok = mbar_wait(&bar.a_full, j & 1, abort_flag, status))) break;
+        const int slot = j & 1;
+        const uint32_t a_base = smem_u32(sA + slot * kABytes);
+        if (!(ok = mbar_wait(&bar.a_full[slot], (j >> 1) & 1, abort_flag, status))) break;
         tc_fence_after();
-        uint32_t wsm;
-        if (!(ok = take_w(&wsm))) break;
-        for (int s = 0; s < 2 && ok; ++s) ok = gemm1(s, j * NC, wsm);
-        if (!ok) break;
-        release_w();
-        if (NC == 1) mma_commit(&bar.a_empty);
         for (int c = 0; c < NC && ok; ++c) {
-          if (c + 1 < NC) {
-            if (!(ok = take_w(&wsm))) break;
-            for (int s = 0; s < 2 && ok; ++s) ok = gemm1(s, j * NC + c + 1, wsm);
-            if (!ok) break;
-            release_w();
-            if (c + 1 == NC - 1) mma_commit(&bar.a_empty);
+          uint32_t wsm;
+          if (!(ok = take_w(&wsm))) break;
+          for (int s = 0; s < 2; ++s) {
+            // acc1[s] is free once the previous GEMM2 of sub-tile s has completed
+            if (g2n[s] > 0 && !(ok = mbar_wait(&bar.g2_done[s], (g2n[s] - 1) & 1, abort_flag, status))) break;
+            tc_fence_after();
+            for (int k = 0; k < kCz / 16; ++k) {
+              const uint32_t koff = (k >> 2) * kBlockBytes + (k & 3) * 32;
+              mma_bf16(tmem + 128 * s, sdesc_k128(a_base + s * kSubBytes + koff), sdesc_k128(wsm + koff), idesc,
+                       k > 0);
+            }
+            mma_commit(&bar.acc1_full[s]);
           }
+          if (!ok) break;
+          release_w();
+          if (c == NC - 1) mma_commit(&bar.a_empty[slot]);   // the slot's last reads by the tensor core
           if (!(ok = take_w(&wsm))) break;
           const int it = j * NC + c;
           for (int s = 0; s < 2; ++s) {
             if (c == 0 && !(ok = mbar_wait(&bar.acc2_empty[s], (j & 1) ^ 1, abort_flag, status))) break;
-            if (!(ok = mbar_wait(&bar.h_full[s], it & 1, abort_flag, status))) break;
-            tc_fence_after();
-            for (int k = 0; k < kHid / 16; ++k) {
-              const uint32_t koff = (k >> 2) * kBlockBytes + (k & 3) * 32;
-              mma_bf16(tmem + 256 + 128 * s, sdesc_k128(h_base + s * kSubBytes + koff), sdesc_k128(wsm + koff),
-                       idesc, (c > 0 || k > 0) ? 1u : 0u);
+            // the hidden chunk as bf16 pairs in acc1[s] (16 hidden units = 8
+            // columns), contracted half by half as the epilogue writes it
+            for (int half = 0; half < 2 && ok; ++half) {
+              if (!(ok = mbar_wait(&bar.h_full[s][half], it & 1, abort_flag, status))) break;
+              tc_fence_after();
+              for (int k = half * kHid / 32; k < (half + 1) * kHid / 32; ++k) {
+                const uint32_t koff = (k >> 2) * kBlockBytes + (k & 3) * 32;
+                mma_bf16_ts(tmem + 256 + 128 * s, tmem + 128 * s + 8 * k, sdesc_k128(wsm + koff), idesc,
+                            (c > 0 || k > 0) ? 1u : 0u);
+              }
             }
-            mma_commit(&bar.h_empty[s]);
+            if (!ok) break;
+            mma_commit(&bar.g2_done[s]);
+            ++g2n[s];
             if (c == NC - 1) mma_commit(&bar.acc2_full[s]);
           }
           if (!ok) break;
@@ -347,13 +351,16 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
     const int t = threadIdx.x - 64;   // 0..127: row t of each sub-tile
     int j = 0;
     for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++j) {
+      const int slot = j & 1;
+      uint8_t* a = sA + slot * kABytes;
       if (kFused) {
-        // A is free once the previous tile's GEMM1s have read it; then this
-        // thread writes row t of both sub-tiles: z = bf16(u[row] + v[col])
-        if (!mbar_wait(&bar.a_empty, (j & 1) ^ 1, abort_flag, status)) break;
+        // the slot is free once its previous tile's GEMM1s and output stores
+        // are done; then this thread writes row t of both sub-tiles:
+        // z = bf16(u[row] + v[col])
+        if (!mbar_wait(&bar.a_empty[slot], ((j >> 1) & 1) ^ 1, abort_flag, status)) break;
 #pragma unroll 1
         for (int s = 0; s < 2; ++s) {
-          uint8_t* base = sA + s * kSubBytes;
+          uint8_t* base = a + s * kSubBytes;
           const int64_t p = tile * kTileRows + s * kSubRows + t;
           if (p < P) {
             int64_t row, vrow;
@@ -367,12 +374,12 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
               *reinterpret_cast<uint4*>(base + swz128_offset(t, ci * 8, kSubRows)) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
-      } else if (!mbar_wait(&bar.z_full, j & 1, abort_flag, status)) {
+      } else if (!mbar_wait(&bar.z_full[slot], (j >> 1) & 1, abort_flag, status)) {
         break;
       }
 #pragma unroll 1
       for (int s = 0; s < 2; ++s) {
-        uint8_t* base = sA + s * kSubBytes;
+        uint8_t* base = a + s * kSubBytes;
         // statistics in one pass over the row, shifted by its first element
         // so that E[d^2] - E[d]^2 does not cancel when |mean| >> std
         const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(base + swz128_offset(t, 0, kSubRows)));
@@ -419,7 +426,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         }
       }
       fence_async_shared();
-      mbar_arrive(&bar.a_full);
+      mbar_arrive(&bar.a_full[slot]);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -427,27 +434,27 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
     const int qd = warp & 3;                       // TMEM lane quarter of this warp
     const int r = qd * 32 + lane;                  // row within the sub-tile
     const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
-    uint8_t* hs = sH + s * kSubBytes;
+    const uint32_t acc1 = tmem + lane_addr + 128 * s;
     const bool leader = (warp == 6 + 4 * s) && lane == 0;
     int it = 0;
     int j = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
+      const int slot = j & 1;
       for (int c = 0; c < NC; ++c, ++it) {
         if (!(ok = mbar_wait_warp(&bar.acc1_full[s], it & 1, abort_flag, status))) break;
-        // H[s] is free once the previous GEMM2 read it and any output store drained
-        if (!(ok = mbar_wait_warp(&bar.h_empty[s], (it & 1) ^ 1, abort_flag, status))) break;
-        if (c == 0 && j > 0 && !(ok = mbar_wait_warp(&bar.store_done[s], (j - 1) & 1, abort_flag, status))) break;
         tc_fence_after();
         __syncwarp();   // tcgen05.ld is warp-collective: reconverge after the per-lane waits
+        // the hidden chunk goes back over acc1 as bf16 pairs, each group into
+        // columns this thread has already read
         if (kGLU) {
           // acc1 columns 0-63 hold the gate, 64-127 the value of hidden units
-          // 64c .. 64c + 63: H[s] gets SiLU(gate + b1) * (value + b3)
+          // 64c .. 64c + 63: SiLU(gate + b1) * (value + b3) into columns 0-31
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
             float gv[32], vv[32];
-            tmem_ld32(tmem + lane_addr + 128 * s + 32 * g, gv);
-            tmem_ld32(tmem + lane_addr + 128 * s + 64 + 32 * g, vv);
+            tmem_ld32(acc1 + 32 * g, gv);
+            tmem_ld32(acc1 + 64 + 32 * g, vv);
             tmem_ld_wait();
             uint32_t packed[16];
 #pragma unroll
@@ -463,16 +470,15 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
               for (int e = 0; e < 2; ++e)
                 packed[2 * q + e] = pack_bf16x2(silu_f(g4[2 * e]) * v4[2 * e], silu_f(g4[2 * e + 1]) * v4[2 * e + 1]);
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(hs + swz128_offset(r, 32 * g + 8 * u, kSubRows)) =
-                  make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+            tmem_st16_sync(acc1 + 16 * g, packed);
+            tc_fence_before();
+            mbar_arrive(&bar.h_full[s][g]);        // half g of the hidden chunk is in TMEM
           }
         } else {
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             float v[32];
-            tmem_ld32(tmem + lane_addr + 128 * s + 32 * g, v);
+            tmem_ld32(acc1 + 32 * g, v);
             tmem_ld_wait();
             uint32_t packed[16];
 #pragma unroll
@@ -484,29 +490,26 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
               packed[2 * q] = relu_bf16x2(pack_bf16x2(a0, a1));
               packed[2 * q + 1] = relu_bf16x2(pack_bf16x2(a2, a3));
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(hs + swz128_offset(r, 32 * g + 8 * u, kSubRows)) =
-                  make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+            tmem_st16_sync(acc1 + 16 * g, packed);
+            if (g & 1) {                            // groups 0-1, then 2-3: the two halves
+              tc_fence_before();
+              mbar_arrive(&bar.h_full[s][g >> 1]);
+            }
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bar.acc1_empty[s]);
-        fence_async_shared();
-        mbar_arrive(&bar.h_full[s]);
       }
       if (!ok) break;
-      // output: z~ = z + acc2 + b2, staged through H[s] for a TMA store
+      // output: z~ = z + acc2 + b2, staged in this tile's input slot (its
+      // GEMM1s completed before acc2 did) for a TMA store
       if (!(ok = mbar_wait_warp(&bar.acc2_full[s], j & 1, abort_flag, status))) break;
       tc_fence_after();
       __syncwarp();
+      uint8_t* hs = sA + slot * kABytes + s * kSubBytes;
       const int64_t row_g = tile * kTileRows + s * kSubRows + r;
       const bool in_range = row_g < P;
       const bf16* zr = z_in + row_g * kCz;
       int64_t f_row = 0, f_vrow = 0;        // fused: the cell's pair row and column single
-      if (kFused && in_range) {
-        cell_of(fz, row_g, f_row, f_vrow);
-      }
+      if (kFused && in_range) cell_of(fz, row_g, f_row, f_vrow);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         float v[32];
@@ -570,10 +573,10 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         }
         mbar_arrive(&bar.colsum_done[s]);
         if (leader) {
-          // H[s] is reused once the column sums and the store's reads are done
+          // the slot is reused once the column sums and the store's reads are done
           const bool sums_done = mbar_wait(&bar.colsum_done[s], j & 1, abort_flag, status);
           if (y < P) tma_store_wait_read0();
-          if (sums_done) mbar_arrive(&bar.store_done[s]);
+          if (sums_done) mbar_arrive(&bar.a_empty[slot]);
         }
       } else if (leader) {
         if (mbar_wait(&bar.out_ready[s], j & 1, abort_flag, status) && y < P) {
@@ -582,7 +585,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           tma_store_commit();
           tma_store_wait_read0();
         }
-        mbar_arrive(&bar.store_done[s]);
+        mbar_arrive(&bar.a_empty[slot]);
       }
       __syncwarp();
     }
