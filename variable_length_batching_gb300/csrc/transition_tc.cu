@@ -474,7 +474,29 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
             tc_fence_before();
             mbar_arrive(&bar.h_full[s][g]);        // half g of the hidden chunk is in TMEM
           }
+        } else if (!kFused) {
+          // ReLU: the two halves, 64 columns read with one wait each
+#pragma unroll 1
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float v[64];
+            tmem_ld64_sync(acc1 + 64 * h2, v);
+            uint32_t packed[32];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {          // + b1 in packed pairs, ReLU on the bf16 pairs
+              const float4 bb = bias4(b1, c * kChunk + 64 * h2 + 4 * q);
+              float a0, a1, a2, a3;
+              fadd2(v[4 * q], v[4 * q + 1], bb.x, bb.y, a0, a1);
+              fadd2(v[4 * q + 2], v[4 * q + 3], bb.z, bb.w, a2, a3);
+              packed[2 * q] = relu_bf16x2(pack_bf16x2(a0, a1));
+              packed[2 * q + 1] = relu_bf16x2(pack_bf16x2(a2, a3));
+            }
+            tmem_st32_sync(acc1 + 32 * h2, packed);  // into columns this half has just read
+            tc_fence_before();
+            mbar_arrive(&bar.h_full[s][h2]);
+          }
         } else {
+          // ReLU in the fused block: per 32-column group (fewer live registers
+          // beside the fused epilogue's)
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             float v[32];
@@ -482,7 +504,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
             tmem_ld_wait();
             uint32_t packed[16];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {          // + b1 in packed pairs, ReLU on the bf16 pairs
+            for (int q = 0; q < 8; ++q) {
               const float4 bb = bias4(b1, c * kChunk + 32 * g + 4 * q);
               float a0, a1, a2, a3;
               fadd2(v[4 * q], v[4 * q + 1], bb.x, bb.y, a0, a1);
