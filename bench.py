@@ -449,7 +449,7 @@ def run_e2e(nt, binp, dev, stream, args):
     weights are resident on the device, as a model's parameters are."""
     from variable_length_batching_gb300 import graph
     host = {"lengths": torch.as_tensor(binp.lengths).pin_memory(), "s": binp.s.pin_memory()}
-    runner = graph.BlockGraph(_dev_weights(binp.blocks[0], dev), slices=3)
+    runner = graph.BlockGraph(_dev_weights(binp.blocks[0], dev))
     T = int(binp.lengths.sum())
     P = int((binp.lengths.astype(np.int64) ** 2).sum())
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -469,8 +469,8 @@ def run_e2e(nt, binp, dev, stream, args):
     return {"value": P / dt, "unit": "pair cells/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3,
             "path": "pinned host -> H2D of lengths and singles -> nt_partition_build (totals read-back) -> "
-                    "CUDA-graph replay of broadcast / transition in 3 slices / reduce, with each slice's z~ and "
-                    "then s_out read back (weights resident on the device)"}
+                    f"CUDA-graph replay of broadcast / transition in {runner.slices} slices growing x{runner.growth:g} / "
+                    "reduce, with each slice's z~ and then s_out read back (weights resident on the device)"}
 
 
 # ----------------------------------------------------------------------------

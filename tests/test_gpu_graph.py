@@ -31,7 +31,8 @@ def _eager(nt, inp, wd):
     return z.cpu(), s_out.cpu()
 
 
-def test_block_graph_matches_eager(mods):
+@pytest.mark.parametrize("slices,growth", [(3, 2.0), (4, 1.0), (1, 1.0)])
+def test_block_graph_matches_eager(mods, slices, growth):
     nt, graph = mods
     cfg = wl.PAIRFORMER_BF16
     inp = wl.make_block_inputs(cfg, biases=True)
@@ -39,7 +40,7 @@ def test_block_graph_matches_eager(mods):
     g = lambda t: None if t is None else t.to(DEV).contiguous()
     wd = SimpleNamespace(W_a=g(w.W_a), W_b=g(w.W_b), ln_gamma=g(w.ln_gamma), ln_beta=g(w.ln_beta), W1=g(w.W1),
                          b1=g(w.b1), W2=g(w.W2), b2=g(w.b2), W_g=g(w.W_g), b_g=g(w.b_g))
-    runner = graph.BlockGraph(wd, slices=3)
+    runner = graph.BlockGraph(wd, slices=slices, growth=growth)
     lengths = torch.as_tensor(np.asarray(inp.lengths, dtype=np.int32)).pin_memory()
     s = inp.s.pin_memory()
     z_ref, s_ref = _eager(nt, inp, wd)

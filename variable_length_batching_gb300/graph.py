@@ -5,31 +5,50 @@ Each step copies the sample lengths and the singles in from pinned host
 memory and rebuilds the partition in one call (its totals come back to the
 host: they decide the pair state's size).  Everything after that has fixed sizes for a
 given (B, T, P) and runs as one captured graph: the broadcast, the
-transition in slices of cells (each slice's z~ copied back to the host on a
-second stream as soon as it is done, so the read-back overlaps the next
-slice), the reduce, and the copy-back of s_out.  A new (B, T, P) captures a
+transition in slices of cells of growing length (each slice's z~ copied
+back to the host on a second stream as soon as it is done, so the read-back
+overlaps the next slice), the reduce, and the copy-back of s_out.  A new (B, T, P) captures a
 new graph.  Every device step runs in the library's kernels; this module
 only owns the buffers, the streams and the graph.
 """
 import ctypes
-from typing import Optional
+from typing import List, Optional
 
 import torch
 
 from . import nt as _nt
 
 
+def slice_cuts(P: int, slices: int, growth: float = 1.0) -> List[int]:
+    """Cell boundaries of ``slices`` consecutive ranges covering [0, P), each
+    ``growth`` times as long as the one before (up to rounding).  A small
+    first range lets the first read-back start early; the later, longer
+    ones are transformed while the host link drains the earlier ones."""
+    if slices < 1 or growth <= 0:
+        raise ValueError("slices must be >= 1 and growth > 0")
+    w = [growth ** i for i in range(slices)]
+    tot = sum(w)
+    cuts, acc = [0], 0.0
+    for x in w[:-1]:
+        acc += x
+        cuts.append(min(P, max(cuts[-1], int(round(P * acc / tot)))))
+    cuts.append(P)
+    return cuts
+
+
 class BlockGraph:
     """Host-to-host block steps for fixed weights ``w`` (a namespace of device
     tensors W_a, W_b, ln_gamma, ln_beta, W1, b1, W2, b2, W_g, b_g; bf16 or
-    fp32 like the singles).  ``slices`` is the number of cell ranges the
-    transition runs in."""
+    fp32 like the singles).  The transition runs in ``slices`` cell ranges,
+    each ``growth`` times as long as the one before."""
 
-    def __init__(self, w, slices: int = 3, ln_eps: float = 1e-5, device: Optional[torch.device] = None):
-        if slices < 1:
-            raise ValueError("slices must be >= 1")
+    def __init__(self, w, slices: int = 3, growth: float = 2.0, ln_eps: float = 1e-5,
+                 device: Optional[torch.device] = None):
+        if slices < 1 or growth <= 0:
+            raise ValueError("slices must be >= 1 and growth > 0")
         self.w = w
         self.slices = slices
+        self.growth = growth
         self.ln_eps = ln_eps
         self.dev = device if device is not None else w.W_a.device
         self.C_z, self.C_s = w.W_a.shape
@@ -77,7 +96,7 @@ class BlockGraph:
         main = torch.cuda.current_stream(self.dev)
         _nt.nt_pair_broadcast(part, self.s, self.s, w.W_a, w.W_b, z=self.z, workspace=self.ws)
         P = part.P
-        cuts = [P * i // self.slices for i in range(self.slices + 1)]
+        cuts = slice_cuts(P, self.slices, self.growth)
         for c0, c1 in zip(cuts[:-1], cuts[1:]):
             if c1 == c0:
                 continue
