@@ -26,8 +26,11 @@
  *   - Alignment: every pointer 16-byte aligned; feature widths multiples of
  *     8 (bf16) or 4 (fp32).  Otherwise NT_ERR_INVALID / NT_ERR_UNSUPPORTED.
  *   - Asynchrony: calls enqueue work on `stream` (a cudaStream_t; NULL is the
- *     legacy default stream) and return.  nt_partition_build is the one call
- *     that synchronises the stream, once, to return the totals.
+ *     legacy default stream) and return.  nt_partition_build (and its
+ *     _rect and _with_rows forms) is the one call that synchronises the
+ *     stream, once, to return the totals; they come back through a 64-byte
+ *     pinned host buffer per calling thread, allocated on first use and kept
+ *     for the life of the process.  The library allocates no device memory.
  *   - Errors: argument errors are detected on the host before anything is
  *     enqueued; the call then writes nothing.  NT_ERR_CUDA reports a launch
  *     failure (outputs undefined).  Device-side checks (bounded waits, data
@@ -144,8 +147,10 @@ nt_status nt_partition_rows(nt_partition* part, int64_t* d_row_start, int32_t* d
  * nt_partition_build_with_rows -- nt_partition_build and nt_partition_rows
  * in one call and one host round trip: the row-split kernel follows the scan
  * in the stream and reads T and P from d_totals, so only the totals come
- * back to the host.  For callers that know an upper bound on T, such as the
- * row count of the packed singles they hold.
+ * back to the host.  For 1 <= B <= 1024 and T_cap <= 65,536 the scan and the
+ * row splits run as one single-CTA launch (same outputs).  For callers that
+ * know an upper bound on T, such as the row count of the packed singles they
+ * hold.
  *   T_cap          >= 0; d_row_start holds T_cap + 1 entries and d_row_sample
  *                  max(T_cap, 1).  Device writes never go past them.
  *   other arguments as in nt_partition_build / nt_partition_rows; on NT_OK

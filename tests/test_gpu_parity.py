@@ -82,26 +82,55 @@ def test_partition_with_rows_matches_two_calls(nt, lengths):
     nt.nt_device_status()
 
 
-def test_partition_with_rows_small_capacity_rejected(nt):
+# one-launch partitions (1 <= B <= 1024, capacity <= 65,536) and the scan +
+# row-split pair beyond either bound, each at its edge
+WITH_ROWS_CASES = [
+    ([2, 3], None), ([0, 0, 5, 0], None), ([7, 0], None), ([1] * 1024, None), ([1] * 1025, None),
+    ([256] * 256, None), ([256] * 256, 65537), ([300] * 10, 70000), (list(range(0, 300, 3)), None),
+]
+
+
+@pytest.mark.parametrize("lengths,cap", WITH_ROWS_CASES)
+def test_partition_with_rows_bit_exact(nt, lengths, cap):
+    """nt_partition_build_with_rows against the oracle's partition, bit for
+    bit, on both kernel paths."""
+    ref = opart.partition(lengths)
+    part = nt.nt_partition_build(dev_lengths(lengths), T=ref.T if cap is None else cap)
+    assert (part.T, part.P, part.max_len) == (ref.T, ref.P, ref.max_len)
+    assert np.array_equal(part.cu_seqlens.cpu().numpy(), ref.cu_seqlens)
+    assert np.array_equal(part.pair_off.cpu().numpy(), ref.pair_off)
+    assert np.array_equal(part.row_start[: ref.T + 1].cpu().numpy(), ref.row_start)
+    if ref.T:
+        assert np.array_equal(part.row_sample[: ref.T].cpu().numpy(), ref.row_sample)
+    nt.nt_device_status()
+
+
+@pytest.mark.parametrize("lengths,cap", [([64, 100, 3], 50), ([2] * 1100, 2000)])
+def test_partition_with_rows_small_capacity_rejected(nt, lengths, cap):
     """A capacity below the lengths' sum is reported (NT_ERR_INVALID) after
-    the totals come back; the row-split kernel writes nothing past the
-    buffers it was given."""
-    lengths = [64, 100, 3]
+    the totals come back; the row splits write nothing past the buffers they
+    were given (one-launch path, then the scan + row-split pair)."""
+    B = len(lengths)
     guard = torch.full((64,), -7, dtype=torch.int64, device=DEV)
-    buf = torch.empty(50 + 1 + 64, dtype=torch.int64, device=DEV)
-    buf[51:] = guard
+    buf = torch.empty(cap + 1 + 64, dtype=torch.int64, device=DEV)
+    buf[cap + 1:] = guard
+    rs_guard = torch.full((64,), -9, dtype=torch.int32, device=DEV)
+    rs = torch.empty(cap + 64, dtype=torch.int32, device=DEV)
+    rs[cap:] = rs_guard
     with pytest.raises(nt.NTError) as ei:
         c = nt.nt_partition()
         L = dev_lengths(lengths)
-        cu = torch.empty(4, dtype=torch.int32, device=DEV)
-        po = torch.empty(4, dtype=torch.int64, device=DEV)
+        cu = torch.empty(B + 1, dtype=torch.int32, device=DEV)
+        po = torch.empty(B + 1, dtype=torch.int64, device=DEV)
         tot = torch.empty(4, dtype=torch.int64, device=DEV)
-        rs = torch.empty(64, dtype=torch.int32, device=DEV)
-        st = nt.lib().nt_partition_build_with_rows(nt._ptr(L), 3, 50, nt._ptr(cu), nt._ptr(po), nt._ptr(tot),
+        st = nt.lib().nt_partition_build_with_rows(nt._ptr(L), B, cap, nt._ptr(cu), nt._ptr(po), nt._ptr(tot),
                                                    nt._ptr(buf), nt._ptr(rs), ctypes.byref(c), nt._stream(None))
         nt._check(st, "nt_partition_build_with_rows")
     assert ei.value.status == 1
-    assert torch.equal(buf[51:], guard)          # nothing written past row_start's 51 entries
+    assert torch.equal(buf[cap + 1:], guard)     # nothing written past row_start's cap + 1 entries
+    assert torch.equal(rs[cap:], rs_guard)       # nor past row_sample's cap entries
+    ref = opart.partition(lengths)
+    assert np.array_equal(buf[:cap].cpu().numpy(), ref.row_start[:cap])   # the rows that fit are right
     nt.nt_device_status()
 
 

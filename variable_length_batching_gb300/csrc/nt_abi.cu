@@ -184,6 +184,28 @@ const char* nt_status_str(nt_status s) {
 
 const char* nt_last_error(void) { return g_last_error; }
 
+// The partition's totals come back through a small pinned buffer per host
+// thread (allocated on first use, kept for the process), so the copy is a
+// direct DMA rather than one staged through pageable memory; if pinning
+// fails, the copy goes to pageable memory instead.
+static cudaError_t read_totals(int64_t* host, const int64_t* d_totals, int n, cudaStream_t s) {
+  static thread_local int64_t* pinned = nullptr;
+  static thread_local bool tried = false;
+  if (!tried) {
+    tried = true;
+    if (cudaMallocHost(reinterpret_cast<void**>(&pinned), 8 * sizeof(int64_t)) != cudaSuccess) {
+      pinned = nullptr;
+      cudaGetLastError();
+    }
+  }
+  int64_t* dst = pinned ? pinned : host;
+  cudaError_t e = cudaMemcpyAsync(dst, d_totals, n * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && pinned)
+    for (int i = 0; i < n; ++i) host[i] = pinned[i];
+  return e;
+}
+
 nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_seqlens,
                              int64_t* d_pair_off, int64_t* d_totals, nt_partition* out,
                              void* stream) {
@@ -197,8 +219,7 @@ nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_
   cudaError_t e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, s);
   if (e != cudaSuccess) return cuda_fail(e, "partition scan launch");
   int64_t tot[4] = {0, 0, 0, 0};
-  e = cudaMemcpyAsync(tot, d_totals, sizeof(tot), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  e = read_totals(tot, d_totals, 4, s);
   if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
   out->B = B;
   out->T = tot[0];
@@ -233,8 +254,7 @@ nt_status nt_partition_build_rect(const int32_t* d_rows, const int32_t* d_cols, 
                                         d_totals, s);
   if (e != cudaSuccess) return cuda_fail(e, "partition scan launch");
   int64_t tot[6] = {0, 0, 0, 0, 0, 0};
-  e = cudaMemcpyAsync(tot, d_totals, sizeof(tot), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  e = read_totals(tot, d_totals, 6, s);
   if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
   out->B = B;
   out->T = tot[0];
@@ -268,14 +288,18 @@ nt_status nt_partition_build_with_rows(const int32_t* d_lengths, int32_t B, int6
       !aligned16(d_row_sample))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, s);
-  if (e == cudaSuccess)
-    e = launch_partition_rows_dev(d_lengths, nullptr, d_cu_seqlens, d_pair_off, B, d_totals, T_cap, d_row_start,
-                                  d_row_sample, s);
+  cudaError_t e;
+  if (partition_fused_fits(B, T_cap)) {
+    e = launch_partition_fused(d_lengths, B, T_cap, d_cu_seqlens, d_pair_off, d_totals, d_row_start, d_row_sample, s);
+  } else {
+    e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, s);
+    if (e == cudaSuccess)
+      e = launch_partition_rows_dev(d_lengths, nullptr, d_cu_seqlens, d_pair_off, B, d_totals, T_cap, d_row_start,
+                                    d_row_sample, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "partition launch");
   int64_t tot[4] = {0, 0, 0, 0};
-  e = cudaMemcpyAsync(tot, d_totals, sizeof(tot), cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  e = read_totals(tot, d_totals, 4, s);
   if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
   out->B = B;
   out->T = tot[0];

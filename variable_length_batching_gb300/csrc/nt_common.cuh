@@ -104,6 +104,11 @@ cudaError_t launch_partition_rows(const int32_t* lengths, const int32_t* cols, c
 cudaError_t launch_partition_rows_dev(const int32_t* lengths, const int32_t* cols, const int32_t* cu,
                                       const int64_t* pair_off, int32_t B, const int64_t* totals, int64_t cap,
                                       int64_t* row_start, int32_t* row_sample, cudaStream_t s);
+// Square partitions of small batches (partition_fused_fits): the scan and the
+// row splits of the two calls above in one single-CTA launch, same outputs.
+bool partition_fused_fits(int32_t B, int64_t cap);
+cudaError_t launch_partition_fused(const int32_t* lengths, int32_t B, int64_t cap, int32_t* cu, int64_t* pair_off,
+                                   int64_t* totals, int64_t* row_start, int32_t* row_sample, cudaStream_t s);
 
 // Y[M, N] = X[M, K] W[N, K]^T (+ bias[N]) (+ R[M, N]).  Up to two independent
 // problems in one launch (gridDim.z); all row-major, contiguous.

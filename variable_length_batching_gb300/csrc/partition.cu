@@ -158,7 +158,105 @@ __global__ void partition_rows_dev_kernel(const int32_t* __restrict__ lengths, c
   }
 }
 
+// Square partitions of small batches in one launch: one CTA scans N_i and
+// N_i^2 (B <= 1024, one chunk) into shared memory, writes cu, pair_off and
+// the totals, then its threads take rows t = tid, tid + 1024, ... below
+// min(T, cap) and find the row's sample by binary search over the scanned
+// offsets (the last i with cu_i <= t, so empty samples are passed over).
+// Outputs and capacity rules are those of the scan followed by the row
+// splits above.
+constexpr int kFusedMaxB = kScanThreads;
+constexpr int64_t kFusedMaxRows = 65536;
+
+__global__ void __launch_bounds__(kScanThreads)
+partition_fused_kernel(const int32_t* __restrict__ lengths, int32_t B, int64_t cap, int32_t* __restrict__ cu,
+                       int64_t* __restrict__ pair_off, int64_t* __restrict__ totals,
+                       int64_t* __restrict__ row_start, int32_t* __restrict__ row_sample) {
+  __shared__ long long warp_n[32], warp_nm[32];
+  __shared__ int warp_max[32];
+  __shared__ long long s_cu[kFusedMaxB + 1], s_off[kFusedMaxB + 1];
+  __shared__ int s_len[kFusedMaxB];
+  __shared__ int bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  long long n = 0;
+  if (tid < B) {
+    const int nb = lengths[tid];
+    if (nb < 0) atomicOr(&bad, 1);
+    n = nb < 0 ? 0 : nb;
+  }
+  const long long nm = n * n;
+  long long in_n = n, in_nm = nm;
+  int mx = (int)n;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long t1 = __shfl_up_sync(0xffffffffu, in_n, off);
+    const long long t3 = __shfl_up_sync(0xffffffffu, in_nm, off);
+    if (lane >= off) { in_n += t1; in_nm += t3; }
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  if (lane == 31) { warp_n[warp] = in_n; warp_nm[warp] = in_nm; }
+  if (lane == 0) warp_max[warp] = mx;
+  __syncthreads();
+  if (warp == 0) {
+    long long wn = warp_n[lane], wnm = warp_nm[lane];
+    int wx = warp_max[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long t1 = __shfl_up_sync(0xffffffffu, wn, off);
+      const long long t3 = __shfl_up_sync(0xffffffffu, wnm, off);
+      if (lane >= off) { wn += t1; wnm += t3; }
+      wx = max(wx, __shfl_xor_sync(0xffffffffu, wx, off));
+    }
+    warp_n[lane] = wn;
+    warp_nm[lane] = wnm;
+    if (lane == 0) warp_max[0] = wx;
+  }
+  __syncthreads();
+  const long long before_n = (warp > 0 ? warp_n[warp - 1] : 0) + in_n - n;
+  const long long before_nm = (warp > 0 ? warp_nm[warp - 1] : 0) + in_nm - nm;
+  if (tid < B) {
+    if (before_n > 0x7fffffffLL) atomicOr(&bad, 2);
+    cu[tid] = (int32_t)before_n;
+    pair_off[tid] = before_nm;
+    s_cu[tid] = before_n;
+    s_off[tid] = before_nm;
+    s_len[tid] = (int)n;
+  }
+  const long long T = warp_n[31], P = warp_nm[31];
+  __syncthreads();
+  if (tid == 0) {
+    if (T > 0x7fffffffLL) bad |= 2;
+    cu[B] = (int32_t)T;
+    pair_off[B] = P;
+    totals[0] = T;
+    totals[1] = P;
+    totals[2] = warp_max[0];
+    totals[3] = bad;
+    if (T <= cap) row_start[T] = P;
+  }
+  const long long rows = T < cap ? T : cap;
+  for (long long t = tid; t < rows; t += kScanThreads) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_cu[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    row_start[t] = s_off[lo] + (t - s_cu[lo]) * s_len[lo];
+    row_sample[t] = lo;
+  }
+}
+
 }  // namespace
+
+bool partition_fused_fits(int32_t B, int64_t cap) { return B >= 1 && B <= kFusedMaxB && cap <= kFusedMaxRows; }
+
+cudaError_t launch_partition_fused(const int32_t* lengths, int32_t B, int64_t cap, int32_t* cu, int64_t* pair_off,
+                                   int64_t* totals, int64_t* row_start, int32_t* row_sample, cudaStream_t s) {
+  partition_fused_kernel<<<1, kScanThreads, 0, s>>>(lengths, B, cap, cu, pair_off, totals, row_start, row_sample);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_partition_rows_dev(const int32_t* lengths, const int32_t* cols, const int32_t* cu,
                                       const int64_t* pair_off, int32_t B, const int64_t* totals, int64_t cap,
