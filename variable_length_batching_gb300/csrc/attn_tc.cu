@@ -358,13 +358,17 @@ attn_item_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int r = qd * 32 + lane;                 // query row within the tile
     const uint32_t lane_addr = (uint32_t)(qd * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + kColS;
+    // a warp whose 32 rows all lie past the segment's end keeps the
+    // hand-offs but skips the arithmetic: its rows are never copied out
+    const bool live = __any_sync(0xffffffffu, q0 + r < hi);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
       if (!(ok = mbar_wait_warp(&bar.s_full, j & 1, abort_flag, status))) break;
       tc_fence_after();
       __syncwarp();
-      softmax_tile<kCausal>(s_addr, tmem + lane_addr + kColO, j, n_k, qi * kBQ + r, diag, scale_log2, m, l);
+      if (live)
+        softmax_tile<kCausal>(s_addr, tmem + lane_addr + kColO, j, n_k, qi * kBQ + r, diag, scale_log2, m, l);
       tc_fence_before();
       mbar_arrive(&bar.p_full);
     }
@@ -380,7 +384,7 @@ attn_item_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int t = q0 + r;
       const float inv = l > 0.f ? 1.0f / l : 0.f;   // causal rows that see no key: zeros
 #pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
+      for (int g = 0; g < 2 && live; ++g) {
         float ov[32];
         tmem_ld32(tmem + lane_addr + kColO + 32 * g, ov);
         tmem_ld_wait();
@@ -659,12 +663,17 @@ attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         }
         continue;
       }
+      // a warp whose 32 rows all lie past the segment's end (the last query
+      // tile of a segment) keeps the hand-offs but skips the arithmetic:
+      // its P and O rows are never stored
+      const bool live = __any_sync(0xffffffffu, t < it.hi);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.nk; ++j, ++gt) {
         if (!(ok = mbar_wait_warp(&bar.s_full, (uint32_t)gt & 1, abort_flag, status))) break;
         tc_fence_after();
         __syncwarp();
-        softmax_tile<kCausal>(s_addr, tmem + lane_addr + kColO, j, n_k, qi * kBQ + r, diag, scale_log2, m, l);
+        if (live)
+          softmax_tile<kCausal>(s_addr, tmem + lane_addr + kColO, j, n_k, qi * kBQ + r, diag, scale_log2, m, l);
         tc_fence_before();
         mbar_arrive(&bar.p_full);
       }
@@ -675,7 +684,7 @@ attn_persistent_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       __syncwarp();
       const float inv = l > 0.f ? 1.0f / l : 0.f;   // causal rows that see no key: zeros
 #pragma unroll 1
-      for (int g = 0; g < 2; ++g) {
+      for (int g = 0; g < 2 && live; ++g) {
         float ov[32];
         tmem_ld32(tmem + lane_addr + kColO + 32 * g, ov);
         tmem_ld_wait();
