@@ -28,6 +28,8 @@ broadcast_fixed_slice_kernel(const float* __restrict__ u, const float* __restric
                              const int32_t* __restrict__ col_lengths, const int32_t* __restrict__ col_cu,
                              const int32_t* __restrict__ row_sample, const int64_t* __restrict__ row_start,
                              int64_t T, int C_z, TOut* __restrict__ z) {
+  pdl_wait();                                 // u and v come from the kernel before
+  pdl_trigger();
   const int vecs = C_z / 8;
   const int f = (threadIdx.x % vecs) * 8;
   const int b_step = kThreads / vecs;
@@ -151,12 +153,11 @@ cudaError_t launch_broadcast(nt_dtype dt, const float* u, const float* v, const 
     const int64_t groups = (p->T + kRows - 1) / kRows;
     const int grid = (int)min64(groups, (int64_t)sms * 16);
     if (dt == NT_BF16)
-      broadcast_fixed_slice_kernel<bf16><<<grid, kThreads, 0, s>>>(u, v, p->lengths, p->cu_seqlens, cl, cc, p->row_sample,
-                                                                   p->row_start, p->T, C_z, (bf16*)z);
+      return launch_pdl(broadcast_fixed_slice_kernel<bf16>, dim3(grid), dim3(kThreads), 0, s, u, v, p->lengths,
+                        p->cu_seqlens, cl, cc, p->row_sample, p->row_start, p->T, C_z, (bf16*)z);
     else
-      broadcast_fixed_slice_kernel<float><<<grid, kThreads, 0, s>>>(u, v, p->lengths, p->cu_seqlens, cl, cc,
-                                                                    p->row_sample, p->row_start, p->T, C_z,
-                                                                    (float*)z);
+      return launch_pdl(broadcast_fixed_slice_kernel<float>, dim3(grid), dim3(kThreads), 0, s, u, v, p->lengths,
+                        p->cu_seqlens, cl, cc, p->row_sample, p->row_start, p->T, C_z, (float*)z);
   } else if (C_z % 8 == 0) {
     const int64_t groups = (p->T + kRows - 1) / kRows;
     const int grid = (int)min64(groups, (int64_t)sms * 16);

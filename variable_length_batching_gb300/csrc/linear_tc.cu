@@ -44,6 +44,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
                  int64_t M, int N, int K, int stages, unsigned int* status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023) {
+    pdl_wait();   // a kernel that waits on this one must also see the previous one done
     if (threadIdx.x == 0) flag_device(status, kDevCheck);
     return;
   }
@@ -69,6 +70,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
+  // the set-up above overlaps the previous kernel's tail; its outputs (X, R)
+  // are read only after it has completed
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0 && lane == 0) {
     int issued = 0;
@@ -179,14 +184,16 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
     e = cudaFuncSetAttribute(linear_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(kMaxStages * kStageBytes + kBarBytes));
     if (e != cudaSuccess) return e;
-    linear_tc_kernel<true><<<grid, kThreads, smem, s>>>(tx[0], tw[0], tx[1], tw[1], pp[0], pp[1], M, N, K, stages,
-                                                        status);
+    e = launch_pdl(linear_tc_kernel<true>, grid, dim3(kThreads), smem, s, tx[0], tw[0], tx[1], tw[1], pp[0], pp[1],
+                   M, N, K, stages, status);
+    if (e != cudaSuccess) return e;
   } else {
     e = cudaFuncSetAttribute(linear_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(kMaxStages * kStageBytes + kBarBytes));
     if (e != cudaSuccess) return e;
-    linear_tc_kernel<false><<<grid, kThreads, smem, s>>>(tx[0], tw[0], tx[1], tw[1], pp[0], pp[1], M, N, K, stages,
-                                                         status);
+    e = launch_pdl(linear_tc_kernel<false>, grid, dim3(kThreads), smem, s, tx[0], tw[0], tx[1], tw[1], pp[0], pp[1],
+                   M, N, K, stages, status);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

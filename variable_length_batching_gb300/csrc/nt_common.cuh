@@ -79,6 +79,31 @@ __device__ __forceinline__ void flag_device(unsigned int* status, unsigned int b
   if (status) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch.  A kernel started by launch_pdl may begin
+// while the kernel before it in the stream is still running: every thread
+// calls pdl_wait() before it reads or writes global memory that kernel
+// touches (the wait returns once that kernel has completed and its writes
+// are visible).  pdl_trigger() lets the next kernel in the stream start its
+// CTAs early.  Both are no-ops in a kernel launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ----------------------------------------------------------------------------
 // Internal launchers (one per kernel family), called by the ABI layer after
 // argument validation.  Each returns cudaGetLastError() of its launches.

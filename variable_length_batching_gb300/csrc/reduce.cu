@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(kThreads)
 reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ row_len,
               const int32_t* __restrict__ row_sample, const int64_t* __restrict__ row_start,
               int64_t rows, int C_z, T* __restrict__ m) {
+  pdl_wait();                                  // z comes from the kernel before
+  pdl_trigger();
   extern __shared__ float part[];              // [groups][C_z]
   const int lanes = C_z / 8;                   // vectors per cell (<= kThreads)
   const int groups = kThreads / lanes;         // cells summed concurrently
@@ -121,11 +123,11 @@ cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int
     const int groups = kThreads / (C_z / 8);
     const size_t smem = sizeof(float) * groups * C_z;
     if (dt == NT_BF16)
-      reduce_kernel<bf16><<<grid, kThreads, smem, s>>>((const bf16*)z, cl, p->row_sample,
-                                                       p->row_start, p->T, C_z, (bf16*)m);
+      return launch_pdl(reduce_kernel<bf16>, dim3(grid), dim3(kThreads), smem, s, (const bf16*)z, cl, p->row_sample,
+                        p->row_start, p->T, C_z, (bf16*)m);
     else
-      reduce_kernel<float><<<grid, kThreads, smem, s>>>((const float*)z, cl, p->row_sample,
-                                                        p->row_start, p->T, C_z, (float*)m);
+      return launch_pdl(reduce_kernel<float>, dim3(grid), dim3(kThreads), smem, s, (const float*)z, cl,
+                        p->row_sample, p->row_start, p->T, C_z, (float*)m);
   } else {
     reduce_kernel_f32_scalar<<<grid, 128, 0, s>>>((const float*)z, cl, p->row_sample,
                                                  p->row_start, p->T, C_z, (float*)m);

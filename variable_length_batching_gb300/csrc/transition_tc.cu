@@ -211,6 +211,10 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bar.tmem_base;
+  // the set-up above overlaps the previous kernel's tail; z (or u and v) is
+  // read, and z~ written, only after it has completed
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -681,9 +685,8 @@ cudaError_t launch_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t
   const int64_t tiles = (P + kTileRows - 1) / kTileRows;
   const int grid = (int)min64(tiles, (int64_t)sm_count());
   const FusedIn none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, 0};
-  kern<<<grid, kThreads, kSmemBytes, s>>>(m_zin, m_zout, m_w1, m_w3, m_w2, (const bf16*)z_in, P, H_t, gamma, beta,
-                                          eps, b1, b3, b2, fused ? *fused : none, status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, m_zin, m_zout, m_w1, m_w3, m_w2,
+                    (const bf16*)z_in, P, H_t, gamma, beta, eps, b1, b3, b2, fused ? *fused : none, status);
 }
 
 }  // namespace
