@@ -28,9 +28,12 @@
  *   - Asynchrony: calls enqueue work on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and return.  nt_partition_build (and its
  *     _rect and _with_rows forms) is the one call that synchronises the
- *     stream, once, to return the totals; they come back through a 64-byte
- *     pinned host buffer per calling thread, allocated on first use and kept
- *     for the life of the process.  The library allocates no device memory.
+ *     stream, once, to return the totals.  The partition kernel writes them
+ *     straight into a 64-byte mapped pinned host buffer per calling thread
+ *     (allocated on first use, kept for the life of the process), so no copy
+ *     engine is involved and the read-back does not queue behind large
+ *     device-to-host copies on other streams.  The library allocates no
+ *     device memory.
  *   - Errors: argument errors are detected on the host before anything is
  *     enqueued; the call then writes nothing.  NT_ERR_CUDA reports a launch
  *     failure (outputs undefined).  Device-side checks (bounded waits, data

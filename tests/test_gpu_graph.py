@@ -55,3 +55,39 @@ def test_block_graph_matches_eager(mods, slices, growth):
                               inp2.s.pin_memory())
         assert torch.equal(z_h, z2_ref) and torch.equal(s_h, s2_ref)
     nt.nt_device_status()
+
+
+def test_block_graph_pipelined_steps(mods):
+    """Steps in flight two at a time (submit the next before waiting for the
+    previous): each step's z~ and s_out equal its own eager block's, bit for
+    bit, though its compute overlaps the previous step's read-back."""
+    nt, graph = mods
+    cfg = wl.PAIRFORMER_BF16
+    base = wl.make_block_inputs(cfg, biases=True)
+    # the same lengths (one key: the graphs are reused), other singles
+    inps = [base] + [wl.make_block_inputs(cfg, lengths=base.lengths, biases=True, seed=sd) for sd in (1, 2, 3)]
+    w = inps[0].blocks[0]
+    g = lambda t: None if t is None else t.to(DEV).contiguous()
+    wd = SimpleNamespace(W_a=g(w.W_a), W_b=g(w.W_b), ln_gamma=g(w.ln_gamma), ln_beta=g(w.ln_beta), W1=g(w.W1),
+                         b1=g(w.b1), W2=g(w.W2), b2=g(w.b2), W_g=g(w.W_g), b_g=g(w.b_g))
+    refs = []
+    for x in inps:
+        x.blocks = inps[0].blocks           # the same weights, other singles
+        refs.append(_eager(nt, x, wd))
+    runner = graph.BlockGraph(wd, depth=2)
+    lengths = torch.as_tensor(np.asarray(inps[0].lengths, dtype=np.int32)).pin_memory()
+    hs = [x.s.pin_memory() for x in inps]
+    tickets, got = [], []
+    for i, s in enumerate(hs + hs):          # eight steps, two passes over the four inputs
+        tickets.append(runner.submit(lengths, s))
+        if i >= 1:
+            z_h, s_h = runner.wait(tickets[i - 1])
+            got.append((z_h.clone(), s_h.clone()))
+    z_h, s_h = runner.wait(tickets[-1])
+    got.append((z_h.clone(), s_h.clone()))
+    for i, (z_h, s_h) in enumerate(got):
+        z_ref, s_ref = refs[i % 4]
+        assert torch.equal(z_h, z_ref) and torch.equal(s_h, s_ref), f"step {i}"
+    with pytest.raises(ValueError):
+        runner.wait(tickets[0])              # reused two submissions later
+    nt.nt_device_status()

@@ -184,25 +184,50 @@ const char* nt_status_str(nt_status s) {
 
 const char* nt_last_error(void) { return g_last_error; }
 
-// The partition's totals come back through a small pinned buffer per host
-// thread (allocated on first use, kept for the process), so the copy is a
-// direct DMA rather than one staged through pageable memory; if pinning
-// fails, the copy goes to pageable memory instead.
-static cudaError_t read_totals(int64_t* host, const int64_t* d_totals, int n, cudaStream_t s) {
-  static thread_local int64_t* pinned = nullptr;
-  static thread_local bool tried = false;
-  if (!tried) {
-    tried = true;
-    if (cudaMallocHost(reinterpret_cast<void**>(&pinned), 8 * sizeof(int64_t)) != cudaSuccess) {
-      pinned = nullptr;
-      cudaGetLastError();
+// The partition's totals come back through a small mapped pinned buffer per
+// host thread (allocated on first use, kept for the process).  The scan
+// kernel writes them there itself, through the buffer's device alias, so the
+// host needs only a stream sync and no copy engine: a copy would queue
+// behind any large device-to-host transfer in flight on another stream.  If
+// mapping fails, the totals are copied back (to pageable memory if pinning
+// fails too).
+struct PinnedTotals {
+  int64_t* host = nullptr;
+  int64_t* dev = nullptr;     // device alias of host; null when not mapped
+  bool tried = false;
+};
+
+static PinnedTotals& pinned_totals() {
+  static thread_local PinnedTotals p;
+  if (!p.tried) {
+    p.tried = true;
+    void* h = nullptr;
+    if (cudaHostAlloc(&h, 8 * sizeof(int64_t), cudaHostAllocMapped | cudaHostAllocPortable) == cudaSuccess) {
+      p.host = static_cast<int64_t*>(h);
+      void* d = nullptr;
+      if (cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess) p.dev = static_cast<int64_t*>(d);
     }
+    cudaGetLastError();
   }
-  int64_t* dst = pinned ? pinned : host;
-  cudaError_t e = cudaMemcpyAsync(dst, d_totals, n * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+  return p;
+}
+
+// `mapped`: the launch was given pinned_totals().dev, so the totals are
+// already on their way to the host buffer.
+static cudaError_t read_totals(int64_t* host, const int64_t* d_totals, int n, cudaStream_t s, bool mapped) {
+  PinnedTotals& p = pinned_totals();
+  cudaError_t e;
+  if (mapped) {
+    e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess)
+      for (int i = 0; i < n; ++i) host[i] = reinterpret_cast<volatile int64_t*>(p.host)[i];
+    return e;
+  }
+  int64_t* dst = p.host ? p.host : host;
+  e = cudaMemcpyAsync(dst, d_totals, n * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess && pinned)
-    for (int i = 0; i < n; ++i) host[i] = pinned[i];
+  if (e == cudaSuccess && p.host)
+    for (int i = 0; i < n; ++i) host[i] = p.host[i];
   return e;
 }
 
@@ -216,10 +241,11 @@ nt_status nt_partition_build(const int32_t* d_lengths, int32_t B, int32_t* d_cu_
   if (!aligned16(d_totals) || !aligned16(d_pair_off) || !aligned16(d_cu_seqlens))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, s);
+  int64_t* ht = pinned_totals().dev;
+  cudaError_t e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, ht, s);
   if (e != cudaSuccess) return cuda_fail(e, "partition scan launch");
   int64_t tot[4] = {0, 0, 0, 0};
-  e = read_totals(tot, d_totals, 4, s);
+  e = read_totals(tot, d_totals, 4, s, ht != nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
   out->B = B;
   out->T = tot[0];
@@ -250,11 +276,12 @@ nt_status nt_partition_build_rect(const int32_t* d_rows, const int32_t* d_cols, 
   if (!aligned16(d_totals) || !aligned16(d_pair_off) || !aligned16(d_cu_rows) || !aligned16(d_cu_cols))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t* ht = pinned_totals().dev;
   cudaError_t e = launch_partition_scan(d_rows, B > 0 ? d_cols : d_rows, B, d_cu_rows, d_cu_cols, d_pair_off,
-                                        d_totals, s);
+                                        d_totals, ht, s);
   if (e != cudaSuccess) return cuda_fail(e, "partition scan launch");
   int64_t tot[6] = {0, 0, 0, 0, 0, 0};
-  e = read_totals(tot, d_totals, 6, s);
+  e = read_totals(tot, d_totals, 6, s, ht != nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
   out->B = B;
   out->T = tot[0];
@@ -288,18 +315,20 @@ nt_status nt_partition_build_with_rows(const int32_t* d_lengths, int32_t B, int6
       !aligned16(d_row_sample))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t* ht = pinned_totals().dev;
   cudaError_t e;
   if (partition_fused_fits(B, T_cap)) {
-    e = launch_partition_fused(d_lengths, B, T_cap, d_cu_seqlens, d_pair_off, d_totals, d_row_start, d_row_sample, s);
+    e = launch_partition_fused(d_lengths, B, T_cap, d_cu_seqlens, d_pair_off, d_totals, d_row_start, d_row_sample,
+                               ht, s);
   } else {
-    e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, s);
+    e = launch_partition_scan(d_lengths, nullptr, B, d_cu_seqlens, nullptr, d_pair_off, d_totals, ht, s);
     if (e == cudaSuccess)
       e = launch_partition_rows_dev(d_lengths, nullptr, d_cu_seqlens, d_pair_off, B, d_totals, T_cap, d_row_start,
                                     d_row_sample, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "partition launch");
   int64_t tot[4] = {0, 0, 0, 0};
-  e = read_totals(tot, d_totals, 4, s);
+  e = read_totals(tot, d_totals, 4, s, ht != nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "partition totals readback");
   out->B = B;
   out->T = tot[0];

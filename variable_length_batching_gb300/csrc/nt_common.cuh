@@ -118,9 +118,12 @@ inline int64_t t_cols_of(const nt_partition* p) { return p->col_lengths ? p->T_c
 inline int32_t max_cols_of(const nt_partition* p) { return p->col_lengths ? p->max_col_len : p->max_len; }
 
 // cols / cu_cols NULL: square (M_i = N_i).  totals = {T, P, max_len, check,
-// T_cols, max_col_len} (the last two only with cols).
+// T_cols, max_col_len} (the last two only with cols).  host_totals (nullable):
+// a device-accessible alias of mapped pinned host memory that receives the
+// same totals, so the host reads them after a stream sync with no copy.
 cudaError_t launch_partition_scan(const int32_t* lengths, const int32_t* cols, int32_t B, int32_t* cu,
-                                  int32_t* cu_cols, int64_t* pair_off, int64_t* totals, cudaStream_t s);
+                                  int32_t* cu_cols, int64_t* pair_off, int64_t* totals, int64_t* host_totals,
+                                  cudaStream_t s);
 cudaError_t launch_partition_rows(const int32_t* lengths, const int32_t* cols, const int32_t* cu,
                                   const int64_t* pair_off, int32_t B, int64_t T, int64_t P, int64_t* row_start,
                                   int32_t* row_sample, cudaStream_t s);
@@ -133,7 +136,8 @@ cudaError_t launch_partition_rows_dev(const int32_t* lengths, const int32_t* col
 // row splits of the two calls above in one single-CTA launch, same outputs.
 bool partition_fused_fits(int32_t B, int64_t cap);
 cudaError_t launch_partition_fused(const int32_t* lengths, int32_t B, int64_t cap, int32_t* cu, int64_t* pair_off,
-                                   int64_t* totals, int64_t* row_start, int32_t* row_sample, cudaStream_t s);
+                                   int64_t* totals, int64_t* row_start, int32_t* row_sample, int64_t* host_totals,
+                                   cudaStream_t s);
 
 // Y[M, N] = X[M, K] W[N, K]^T (+ bias[N]) (+ R[M, N]).  Up to two independent
 // problems in one launch (gridDim.z); all row-major, contiguous.

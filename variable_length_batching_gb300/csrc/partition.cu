@@ -19,7 +19,7 @@ constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads)
 partition_scan_kernel(const int32_t* __restrict__ lengths, const int32_t* __restrict__ cols, int32_t B,
                       int32_t* __restrict__ cu, int32_t* __restrict__ cu_cols, int64_t* __restrict__ pair_off,
-                      int64_t* __restrict__ totals) {
+                      int64_t* __restrict__ totals, int64_t* host_totals) {
   __shared__ long long warp_n[32], warp_m[32], warp_nm[32];
   __shared__ int warp_max[32], warp_maxm[32];
   __shared__ long long carry_n, carry_m, carry_nm;
@@ -106,6 +106,10 @@ partition_scan_kernel(const int32_t* __restrict__ lengths, const int32_t* __rest
       totals[4] = carry_m;
       totals[5] = carry_maxm;
     }
+    if (host_totals) {
+      for (int i = 0; i < (cols ? 6 : 4); ++i) host_totals[i] = totals[i];
+      __threadfence_system();
+    }
   }
 }
 
@@ -171,7 +175,7 @@ constexpr int64_t kFusedMaxRows = 65536;
 __global__ void __launch_bounds__(kScanThreads)
 partition_fused_kernel(const int32_t* __restrict__ lengths, int32_t B, int64_t cap, int32_t* __restrict__ cu,
                        int64_t* __restrict__ pair_off, int64_t* __restrict__ totals,
-                       int64_t* __restrict__ row_start, int32_t* __restrict__ row_sample) {
+                       int64_t* __restrict__ row_start, int32_t* __restrict__ row_sample, int64_t* host_totals) {
   __shared__ long long warp_n[32], warp_nm[32];
   __shared__ int warp_max[32];
   __shared__ long long s_cu[kFusedMaxB + 1], s_off[kFusedMaxB + 1];
@@ -235,6 +239,13 @@ partition_fused_kernel(const int32_t* __restrict__ lengths, int32_t B, int64_t c
     totals[2] = warp_max[0];
     totals[3] = bad;
     if (T <= cap) row_start[T] = P;
+    if (host_totals) {
+      host_totals[0] = T;
+      host_totals[1] = P;
+      host_totals[2] = warp_max[0];
+      host_totals[3] = bad;
+      __threadfence_system();
+    }
   }
   const long long rows = T < cap ? T : cap;
   for (long long t = tid; t < rows; t += kScanThreads) {
@@ -253,8 +264,10 @@ partition_fused_kernel(const int32_t* __restrict__ lengths, int32_t B, int64_t c
 bool partition_fused_fits(int32_t B, int64_t cap) { return B >= 1 && B <= kFusedMaxB && cap <= kFusedMaxRows; }
 
 cudaError_t launch_partition_fused(const int32_t* lengths, int32_t B, int64_t cap, int32_t* cu, int64_t* pair_off,
-                                   int64_t* totals, int64_t* row_start, int32_t* row_sample, cudaStream_t s) {
-  partition_fused_kernel<<<1, kScanThreads, 0, s>>>(lengths, B, cap, cu, pair_off, totals, row_start, row_sample);
+                                   int64_t* totals, int64_t* row_start, int32_t* row_sample, int64_t* host_totals,
+                                   cudaStream_t s) {
+  partition_fused_kernel<<<1, kScanThreads, 0, s>>>(lengths, B, cap, cu, pair_off, totals, row_start, row_sample,
+                                                    host_totals);
   return cudaGetLastError();
 }
 
@@ -268,8 +281,9 @@ cudaError_t launch_partition_rows_dev(const int32_t* lengths, const int32_t* col
 }
 
 cudaError_t launch_partition_scan(const int32_t* lengths, const int32_t* cols, int32_t B, int32_t* cu,
-                                  int32_t* cu_cols, int64_t* pair_off, int64_t* totals, cudaStream_t s) {
-  partition_scan_kernel<<<1, kScanThreads, 0, s>>>(lengths, cols, B, cu, cu_cols, pair_off, totals);
+                                  int32_t* cu_cols, int64_t* pair_off, int64_t* totals, int64_t* host_totals,
+                                  cudaStream_t s) {
+  partition_scan_kernel<<<1, kScanThreads, 0, s>>>(lengths, cols, B, cu, cu_cols, pair_off, totals, host_totals);
   return cudaGetLastError();
 }
 

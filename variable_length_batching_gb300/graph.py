@@ -1,15 +1,23 @@
 """One single -> pair -> single block step ("DanLing NestedTensor" Eq. 1) with
-host inputs and outputs, replayed from a CUDA graph.
+host inputs and outputs, replayed from CUDA graphs, and consecutive steps
+pipelined.
 
 Each step copies the sample lengths and the singles in from pinned host
 memory and rebuilds the partition in one call (its totals come back to the
-host: they decide the pair state's size).  Everything after that has fixed sizes for a
-given (B, T, P) and runs as one captured graph: the broadcast, the
-transition in slices of cells of growing length (each slice's z~ copied
-back to the host on a second stream as soon as it is done, so the read-back
-overlaps the next slice), the reduce, and the copy-back of s_out.  A new (B, T, P) captures a
-new graph.  Every device step runs in the library's kernels; this module
-only owns the buffers, the streams and the graph.
+host: they decide the pair state's size).  Everything after that has fixed
+sizes for a given (B, T, P) and runs as captured graphs, one per slice of
+cells: the first holds the broadcast and the first transition slice, the
+last the last slice and the reduce.  Slices grow in length; each slice's z~
+is copied back to the host on a second stream as soon as its graph is done,
+then s_out.
+
+Steps are pipelined: the device buffers a step writes (z~, m, s_out) and the
+host buffers it fills come from one of ``depth`` sets, used in turn, so the
+next step's copies in, partition and compute run while the host link still
+drains the previous step's z~.  A set is reused only after its last
+read-back has completed.  A new (B, T, P) drains the pipeline and captures
+new graphs.  Every device step runs in the library's kernels; this module
+owns the buffers, the streams, the events and the graphs.
 """
 import ctypes
 from typing import List, Optional
@@ -36,29 +44,44 @@ def slice_cuts(P: int, slices: int, growth: float = 1.0) -> List[int]:
     return cuts
 
 
+class _Set:
+    """Output buffers, graphs and events of one pipeline slot."""
+
+    def __init__(self):
+        self.graphs = []
+        self.sliced = []        # event per slice, recorded on the main stream after its graph
+        self.done = None        # recorded on the copy stream after the step's last read-back
+        self.busy = False
+        self.ticket = -1
+
+
 class BlockGraph:
     """Host-to-host block steps for fixed weights ``w`` (a namespace of device
     tensors W_a, W_b, ln_gamma, ln_beta, W1, b1, W2, b2, W_g, b_g; bf16 or
     fp32 like the singles).  The transition runs in ``slices`` cell ranges,
-    each ``growth`` times as long as the one before."""
+    each ``growth`` times as long as the one before; ``depth`` steps may be
+    in flight at once (``submit`` / ``wait``)."""
 
-    def __init__(self, w, slices: int = 3, growth: float = 2.0, ln_eps: float = 1e-5,
+    def __init__(self, w, slices: int = 3, growth: float = 2.0, depth: int = 2, ln_eps: float = 1e-5,
                  device: Optional[torch.device] = None):
-        if slices < 1 or growth <= 0:
-            raise ValueError("slices must be >= 1 and growth > 0")
+        if slices < 1 or growth <= 0 or depth < 1:
+            raise ValueError("slices and depth must be >= 1, growth > 0")
         self.w = w
         self.slices = slices
         self.growth = growth
+        self.depth = depth
         self.ln_eps = ln_eps
         self.dev = device if device is not None else w.W_a.device
         self.C_z, self.C_s = w.W_a.shape
         self.copy_stream = torch.cuda.Stream(device=self.dev)
-        self.graph = None
         self.key = None
+        self.sets: List[_Set] = []
+        self.submitted = 0
         self.B = -1
         self.T = -1
+        self.s = None
 
-    # -- static buffers --------------------------------------------------------------
+    # -- static input buffers ------------------------------------------------------
     def _ensure_b(self, B: int):
         if B == self.B:
             return
@@ -70,7 +93,7 @@ class BlockGraph:
         self.key = None
 
     def _ensure_t(self, T: int, dtype: torch.dtype):
-        if T == self.T and getattr(self, "s", None) is not None and self.s.dtype == dtype:
+        if T == self.T and self.s is not None and self.s.dtype == dtype:
             return
         self.T = T
         self.s = torch.empty(T, self.C_s, dtype=dtype, device=self.dev)
@@ -90,58 +113,115 @@ class BlockGraph:
             raise ValueError(f"the lengths sum to {c.T}, the singles have {self.T} rows")
         return _nt.Partition(self.lengths, self.cu, self.pair_off, self.totals, self.row_start, self.row_sample, c)
 
-    # -- the captured part ---------------------------------------------------------
-    def _body(self, part):
+    # -- the captured parts ------------------------------------------------------------
+    def _piece(self, part, k: int, idx: int):
+        """Slice ``idx`` of set ``k``'s step: the broadcast before the first
+        slice, the reduce after the last."""
         w = self.w
-        main = torch.cuda.current_stream(self.dev)
-        _nt.nt_pair_broadcast(part, self.s, self.s, w.W_a, w.W_b, z=self.z, workspace=self.ws)
-        P = part.P
-        cuts = slice_cuts(P, self.slices, self.growth)
-        for c0, c1 in zip(cuts[:-1], cuts[1:]):
-            if c1 == c0:
-                continue
-            _nt.nt_pair_transition_cells(self.z[c0:c1], w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2,
-                                         ln_eps=self.ln_eps, out=self.z[c0:c1])
-            self.copy_stream.wait_stream(main)
-            with torch.cuda.stream(self.copy_stream):
-                self.z_host[c0:c1].copy_(self.z[c0:c1], non_blocking=True)
-        _nt.nt_pair_reduce(part, self.z, w.W_g, w.b_g, s_in=self.s, m=self.m, s_out=self.s_out)
-        self.s_out_host.copy_(self.s_out, non_blocking=True)
-        main.wait_stream(self.copy_stream)
+        st = self.sets[k]
+        c0, c1 = self.cuts[idx], self.cuts[idx + 1]
+        if idx == 0:
+            _nt.nt_pair_broadcast(part, self.s, self.s, w.W_a, w.W_b, z=st.z, workspace=self.ws)
+        if c1 > c0:
+            _nt.nt_pair_transition_cells(st.z[c0:c1], w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2,
+                                         ln_eps=self.ln_eps, out=st.z[c0:c1])
+        if idx == self.slices - 1:
+            _nt.nt_pair_reduce(part, st.z, w.W_g, w.b_g, s_in=self.s, m=st.m, s_out=st.s_out)
 
-    def _capture(self, part, dtype):
+    def _drain(self):
+        for st in self.sets:
+            if st.busy:
+                st.done.synchronize()
+                st.busy = False
+        torch.cuda.synchronize(self.dev)
+
+    def _setup(self, part, dtype):
+        """Buffers for a new (B, T, P); graphs are captured on each set's first use."""
+        self._drain()
         P, T = part.P, part.T
-        self.z = torch.empty(P, self.C_z, dtype=dtype, device=self.dev)
-        self.m = torch.empty(T, self.C_z, dtype=dtype, device=self.dev)
-        self.s_out = torch.empty(T, self.C_s, dtype=dtype, device=self.dev)
+        self.cuts = slice_cuts(P, self.slices, self.growth)
         need = _nt.nt_pair_broadcast_workspace_bytes_rect(T, T, self.C_z)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.dev)
-        self.z_host = torch.empty(P, self.C_z, dtype=dtype).pin_memory()
-        self.s_out_host = torch.empty(T, self.C_s, dtype=dtype).pin_memory()
-        # one eager pass first (launch attributes, tensor maps, the library's
-        # own lazy set-up happen outside the capture)
-        self._body(part)
-        torch.cuda.synchronize(self.dev)
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph):
-            self._body(part)
+        self.sets = []
+        for _ in range(self.depth):
+            st = _Set()
+            st.z = torch.empty(P, self.C_z, dtype=dtype, device=self.dev)
+            st.m = torch.empty(T, self.C_z, dtype=dtype, device=self.dev)
+            st.s_out = torch.empty(T, self.C_s, dtype=dtype, device=self.dev)
+            st.z_host = torch.empty(P, self.C_z, dtype=dtype).pin_memory()
+            st.s_out_host = torch.empty(T, self.C_s, dtype=dtype).pin_memory()
+            st.sliced = [torch.cuda.Event() for _ in range(self.slices)]
+            st.done = torch.cuda.Event()
+            self.sets.append(st)
         self.key = (self.B, T, P)
 
-    def run(self, lengths_host: torch.Tensor, s_host: torch.Tensor):
-        """One step: ``lengths_host`` (int32, B) and ``s_host`` (T x C_s), both
-        in pinned host memory.  Returns pinned host tensors (z~ of P x C_z,
-        s_out of T x C_s), overwritten by the next call."""
+    def _capture(self, part, k: int):
+        # one eager pass first (launch attributes, tensor maps, the library's
+        # own lazy set-up happen outside the capture)
+        for idx in range(self.slices):
+            self._piece(part, k, idx)
+        torch.cuda.synchronize(self.dev)
+        graphs = []
+        for idx in range(self.slices):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._piece(part, k, idx)
+            graphs.append(g)
+        self.sets[k].graphs = graphs
+
+    # -- steps ----------------------------------------------------------------------------
+    def submit(self, lengths_host: torch.Tensor, s_host: torch.Tensor) -> int:
+        """Enqueue one step: ``lengths_host`` (int32, B) and ``s_host`` (T x C_s),
+        both in pinned host memory.  Returns a ticket for ``wait`` once the
+        step's device work and read-backs are enqueued (after the
+        partition's totals have come back)."""
         if lengths_host.dtype != torch.int32 or s_host.dim() != 2 or s_host.shape[1] != self.C_s:
             raise ValueError("lengths must be int32 (B,) and s (T, C_s)")
         main = torch.cuda.current_stream(self.dev)
-        self._ensure_b(lengths_host.numel())
-        self._ensure_t(s_host.shape[0], s_host.dtype)
+        B, T = lengths_host.numel(), s_host.shape[0]
+        if self.s is None or B != self.B or T != self.T or self.s.dtype != s_host.dtype:
+            self._drain()            # in-flight steps still read the old input buffers
+        self._ensure_b(B)
+        self._ensure_t(T, s_host.dtype)
         self.lengths.copy_(lengths_host, non_blocking=True)
         self.s.copy_(s_host, non_blocking=True)
         part = self._partition(main)
         if self.key != (self.B, part.T, part.P):
-            self._capture(part, s_host.dtype)
-        else:
-            self.graph.replay()
-        main.synchronize()
-        return self.z_host, self.s_out_host
+            self._setup(part, s_host.dtype)
+        ticket = self.submitted
+        k = ticket % self.depth
+        st = self.sets[k]
+        if st.busy:
+            main.wait_event(st.done)     # the set's previous read-back has finished with z~ and s_out
+        if not st.graphs:
+            self._capture(part, k)
+        for idx in range(self.slices):
+            st.graphs[idx].replay()
+            st.sliced[idx].record(main)
+        with torch.cuda.stream(self.copy_stream):
+            for idx in range(self.slices):
+                c0, c1 = self.cuts[idx], self.cuts[idx + 1]
+                self.copy_stream.wait_event(st.sliced[idx])
+                if c1 > c0:
+                    st.z_host[c0:c1].copy_(st.z[c0:c1], non_blocking=True)
+            st.s_out_host.copy_(st.s_out, non_blocking=True)
+            st.done.record(self.copy_stream)
+        st.busy = True
+        st.ticket = ticket
+        self.submitted += 1
+        return ticket
+
+    def wait(self, ticket: int):
+        """The pinned host results of step ``ticket`` (z~ of P x C_z, s_out of
+        T x C_s), valid until the step ``depth`` submissions later reuses
+        them."""
+        if not self.sets or self.sets[ticket % self.depth].ticket != ticket:
+            raise ValueError(f"step {ticket} is no longer held (depth {self.depth})")
+        st = self.sets[ticket % self.depth]
+        st.done.synchronize()
+        return st.z_host, st.s_out_host
+
+    def run(self, lengths_host: torch.Tensor, s_host: torch.Tensor):
+        """One step, waited for: returns pinned host tensors (z~ of P x C_z,
+        s_out of T x C_s), overwritten ``depth`` steps later."""
+        return self.wait(self.submit(lengths_host, s_host))
