@@ -104,11 +104,20 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
   // epilogue: every warp, one accumulator row per thread
   const int r = warp * 32 + lane;
   const int64_t row = m0 + r;
+  // the residual row does not depend on the MMAs: its loads are issued
+  // before the accumulator wait and land while the tensor core works
+  uint4 res[kBN / 8];
+  const bool has_r = pr.R != nullptr && row < M;
+  if (has_r) {
+    const uint4* rp = reinterpret_cast<const uint4*>(pr.R + row * N + n0);
+#pragma unroll
+    for (int u = 0; u < kBN / 8; ++u) res[u] = rp[u];
+  }
   if (mbar_wait_warp(&bar.acc_full, 0, abort_flag, status)) {
     tc_fence_after();
     __syncwarp();
     const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-#pragma unroll 1
+#pragma unroll
     for (int g = 0; g < kBN / 32; ++g) {
       float v[32];
       tmem_ld32(tmem + lane_addr + 32 * g, v);
@@ -119,11 +128,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] += pr.bias[c0 + c];
         }
-        if (pr.R) {
-          const bf16* rp = pr.R + row * N + c0;
+        if (has_r) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint4 q4 = *reinterpret_cast<const uint4*>(rp + 8 * u);
+            const uint4 q4 = res[4 * g + u];
             const uint32_t w[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
