@@ -3,9 +3,9 @@
 // block ("DanLing NestedTensor" Eq. 1; projections are V W^T + b, section
 // 3.3 "Dense work across valid positions") over the T packed single rows.
 //
-// One CTA per 128 x 128 output tile (and per problem: u and v run in one
+// One CTA per 128 x 64 output tile (and per problem: u and v run in one
 // launch).  Warp 0 streams 64-wide K blocks of X and W through a TMA ring
-// of up to six stages, warp 1 issues the MMAs into a 128-column TMEM
+// of up to six stages, warp 1 issues the MMAs into a 64-column TMEM
 // accumulator, and all four warps run the epilogue: TMEM -> +bias
 // (+residual) -> global.  The grids are small (tens of CTAs for the
 // block's projections), so each CTA's chain of copies sets the time: the
@@ -18,10 +18,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;
+constexpr int kBM = 128, kBN = 64, kBK = 64;
 constexpr int kThreads = 128;
-constexpr uint32_t kOpBytes = 128 * kBK * 2;          // 16 KB per operand block
-constexpr uint32_t kStageBytes = 2 * kOpBytes;        // X block + W block
+constexpr uint32_t kXBytes = kBM * kBK * 2;           // 16 KB X block per stage
+constexpr uint32_t kWBytes = kBN * kBK * 2;           // 8 KB W block per stage
+constexpr uint32_t kStageBytes = kXBytes + kWBytes;   // a multiple of the 1 KB swizzle atom
+constexpr uint32_t kTmemCols = kBN;                   // one fp32 accumulator column per output column
 constexpr int kMaxStages = 6;
 constexpr uint32_t kBarBytes = 256;
 
@@ -65,7 +67,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
     fence_mbar_init();
     fence_async_shared();
   }
-  if (warp == 1) tmem_alloc(&bar.tmem_base, 128);
+  if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -82,7 +84,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
       if (!mbar_wait(&bar.empty[st], ((kb / stages) & 1) ^ 1, abort_flag, status)) break;
       mbar_arrive_expect_tx(&bar.full[st], kStageBytes);
       tma_load_2d(smem + st * kStageBytes, tx, &bar.full[st], kb * kBK, (int)m0);
-      tma_load_2d(smem + st * kStageBytes + kOpBytes, tw, &bar.full[st], kb * kBK, n0);
+      tma_load_2d(smem + st * kStageBytes + kXBytes, tw, &bar.full[st], kb * kBK, n0);
       issued = kb + 1;
     }
     for (int kb = issued - stages; kb < issued; ++kb)
@@ -94,7 +96,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
       const int st = kb % stages;
       if (!mbar_wait(&bar.full[st], (kb / stages) & 1, abort_flag, status)) break;
       tc_fence_after();
-      const uint32_t a = base + st * kStageBytes, b = a + kOpBytes;
+      const uint32_t a = base + st * kStageBytes, b = a + kXBytes;
       for (int k = 0; k < kBK / 16; ++k)
         mma_bf16(tmem, sdesc_k128(a + k * 32), sdesc_k128(b + k * 32), idesc, (kb > 0 || k > 0) ? 1u : 0u);
       mma_commit(&bar.empty[st]);
@@ -163,7 +165,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -180,7 +182,8 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
   Prob pp[2];
   for (int i = 0; i < 2; ++i) {
     const LinearProblem& lp = probs[i < nprob ? i : 0];
-    if (!make_tmap_rows(&tx[i], lp.X, (uint64_t)K, (uint64_t)M) || !make_tmap_rows(&tw[i], lp.W, (uint64_t)K, (uint64_t)N))
+    if (!make_tmap_rows(&tx[i], lp.X, (uint64_t)K, (uint64_t)M, kBM) ||
+        !make_tmap_rows(&tw[i], lp.W, (uint64_t)K, (uint64_t)N, kBN))
       return cudaErrorInvalidValue;
     pp[i] = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y};
   }

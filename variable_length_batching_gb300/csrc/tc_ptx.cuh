@@ -371,7 +371,7 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 // Host: TMA tensor maps over bf16 tensors with the 128-byte swizzle.
 bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int rank, const uint64_t* dims,
                     const uint64_t* strides_bytes, const uint32_t* box);
-// Row-major [outer, inner] matrix, box {64, 128}.
-bool make_tmap_rows(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer);
+// Row-major [outer, inner] matrix, box {64 (inner), rows}.
+bool make_tmap_rows(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t rows = 128);
 
 }  // namespace nt

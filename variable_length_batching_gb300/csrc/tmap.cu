@@ -40,10 +40,10 @@ bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int rank, const uint64_t*
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_tmap_rows(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer) {
+bool make_tmap_rows(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t rows) {
   const uint64_t dims[2] = {inner, outer};
   const uint64_t strides[1] = {inner * 2};
-  const uint32_t box[2] = {64, 128};
+  const uint32_t box[2] = {64, rows};
   return make_tmap_bf16(map, ptr, 2, dims, strides, box);
 }
 
