@@ -150,11 +150,18 @@ def test_partition_negative_length_rejected(nt):
 # a2-a4 one call at a time, inputs straight from the seeded generators
 # ----------------------------------------------------------------------------
 
+# bf16 widths other than the bench's: the u, v projections at N = C_z = 64
+# (one 64-column tile) and g at N = C_s = 192 (three) with K = 64 and 192
+NARROW_BF16 = wl.BlockConfig("narrow_bf16_B5_N8-150_Cs192_Cz64", B=5, length_rule="uniform", rule_args=(8, 150),
+                             C_s=192, C_z=64, H_t=256, dtype=wl.BF16)
+
 STEP_CASES = [
     (wl.TINY_FP32, None),
     (wl.PAIRFORMER_BF16, None),
     (wl.PAIRFORMER_BF16, [0, 1, 7, 0, 130, 2, 1, 33]),   # zero and unit lengths, ragged tails
     (wl.TINY_FP32, [0, 9, 1, 0, 31, 3]),
+    (NARROW_BF16, None),
+    (NARROW_BF16, [0, 9, 150, 1, 77, 130]),
 ]
 
 
