@@ -457,7 +457,7 @@ def run_e2e(nt, binp, dev, stream, args):
     T = int(binp.lengths.sum())
     P = int((binp.lengths.astype(np.int64) ** 2).sum())
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = P * BLOCK_CFG.C_z * 2 + T * BLOCK_CFG.C_s * 2
+    d2h = P * BLOCK_CFG.C_z * 2 + T * BLOCK_CFG.C_s * 2 + 4 * 8   # z~, s_out and the partition's four totals
 
     def steps(n, pipelined):
         tickets = []
