@@ -353,6 +353,78 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
   } else if (warp < 6) {
     // ------------------------------------------------------------ LayerNorm
     const int t = threadIdx.x - 64;   // 0..127: row t of each sub-tile
+    // Without the fused prologue these warps also write each tile's output,
+    // z~ = z + acc2 + b2, after the next tile's LayerNorm: the epilogue
+    // warps then go straight from a tile's last hidden chunk to the next
+    // tile's first.  The output is staged in the tile's own input slot (its
+    // GEMM1s completed before acc2 did) for a TMA store; a slot's next
+    // LayerNorm comes after its output in this order, so nothing waits on
+    // itself.  Row r of acc2 is TMEM lane r: warp w reads quarter w & 3.
+    const int r_out = (warp & 3) * 32 + lane;
+    const uint32_t lane_out = (uint32_t)((warp & 3) * 32) << 16;
+    const bool st_leader = threadIdx.x == 64;
+    auto out_tile = [&](int64_t otile, int oj) -> bool {
+      const int oslot = oj & 1;
+#pragma unroll 1
+      for (int so = 0; so < 2; ++so) {
+        if (!mbar_wait_warp(&bar.acc2_full[so], oj & 1, abort_flag, status)) return false;
+        tc_fence_after();
+        __syncwarp();
+        uint8_t* hs = sA + oslot * kABytes + so * kSubBytes;
+        const int64_t row_g = otile * kTileRows + so * kSubRows + r_out;
+        const bool in_range = row_g < P;
+        const bf16* zr = z_in + row_g * kCz;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float v[32];
+          tmem_ld32(tmem + lane_out + 256 + 128 * so + 32 * g, v);
+          tmem_ld_wait();
+          uint32_t rw[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 q4 = make_uint4(0, 0, 0, 0);
+            if (in_range) q4 = *reinterpret_cast<const uint4*>(zr + 32 * g + 8 * u);
+            rw[4 * u] = q4.x; rw[4 * u + 1] = q4.y; rw[4 * u + 2] = q4.z; rw[4 * u + 3] = q4.w;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t o[4];
+            const float4 bq0 = bias4(b2, 32 * g + 8 * u), bq1 = bias4(b2, 32 * g + 8 * u + 4);
+            const float bb[8] = {bq0.x, bq0.y, bq0.z, bq0.w, bq1.x, bq1.y, bq1.z, bq1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {      // (z + acc2) + b2, packed pairs
+              const uint32_t zw = rw[4 * u + e];
+              float y0, y1;
+              fadd2(bf16lo(zw), bf16hi(zw), v[8 * u + 2 * e], v[8 * u + 2 * e + 1], y0, y1);
+              fadd2(y0, y1, bb[2 * e], bb[2 * e + 1], y0, y1);
+              o[e] = pack_bf16x2(y0, y1);
+            }
+            *reinterpret_cast<uint4*>(hs + swz128_offset(r_out, 32 * g + 8 * u, kSubRows)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&bar.acc2_empty[so]);
+        fence_async_shared();
+        mbar_arrive(&bar.out_ready[so]);
+        const int64_t y = otile * kTileRows + so * kSubRows;
+        if (st_leader && mbar_wait(&bar.out_ready[so], oj & 1, abort_flag, status) && y < P) {
+          tma_store_2d(&tm_zout, hs, 0, (int)y);
+          tma_store_2d(&tm_zout, hs + kBlockBytes, 64, (int)y);
+          tma_store_commit();
+        }
+      }
+      if (st_leader) {
+        // the slot is reused once both stores have read it: one arrival per sub-tile
+        tma_store_wait_read0();
+        mbar_arrive(&bar.a_empty[oslot]);
+        mbar_arrive(&bar.a_empty[oslot]);
+      }
+      __syncwarp();
+      return true;
+    };
+    int64_t prev_tile = -1;
+    bool ok_out = true;
     int j = 0;
     for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++j) {
       const int slot = j & 1;
@@ -431,6 +503,14 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       }
       fence_async_shared();
       mbar_arrive(&bar.a_full[slot]);
+      if (!kFused) {
+        if (prev_tile >= 0 && !(ok_out = out_tile(prev_tile, j - 1))) break;
+        prev_tile = tile;
+      }
+    }
+    if (!kFused) {
+      if (ok_out && prev_tile >= 0) out_tile(prev_tile, j - 1);
+      if (st_leader) tma_store_wait0();
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -525,6 +605,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         }
       }
       if (!ok) break;
+      if (!kFused) continue;                       // the LayerNorm warps write the output
       // output: z~ = z + acc2 + b2, staged in this tile's input slot (its
       // GEMM1s completed before acc2 did) for a TMA store
       if (!(ok = mbar_wait_warp(&bar.acc2_full[s], j & 1, abort_flag, status))) break;
@@ -615,7 +696,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       }
       __syncwarp();
     }
-    if (leader) tma_store_wait0();
+    if (kFused && leader) tma_store_wait0();
   }
 
   tc_fence_before();
