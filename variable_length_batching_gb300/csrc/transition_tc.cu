@@ -105,16 +105,6 @@ struct FusedIn {
   int B;
 };
 
-// Pair row holding packed cell p (< P): the last r with row_start[r] <= p.
-__device__ __forceinline__ int64_t row_of(const int64_t* __restrict__ row_start, int64_t T, int64_t p) {
-  int64_t lo = 0, hi = T - 1;
-  while (lo < hi) {
-    const int64_t mid = (lo + hi + 1) >> 1;
-    if (row_start[mid] <= p) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 // Pair row and column single of packed cell p (< P): the sample by a binary
 // search over the B cell offsets (the last one <= p, which steps past
 // samples with no cells; a few steps, cached), then the row and column
@@ -659,24 +649,33 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           tma_store_2d(&tm_zout, hs + kBlockBytes, 64, (int)y);
           tma_store_commit();
         }
-        // Eq. 4's column sum: feature r of the tile's cells, one atomic add
-        // into m_acc per pair row touched
-        if (y < P) {
-          const int cmax = (int)min64(kSubRows, P - y);
-          int64_t row = row_of(fz.row_start, fz.T, y);
+        // Eq. 4's column sum: features fp and fp + 1 over half ch of the
+        // sub-tile's cells (one 32-bit shared load per cell), one atomic add
+        // per feature into m_acc per pair row touched.  The first cell's pair
+        // row comes from the sample offsets (a few cached steps).
+        const int fp = 2 * (r & 63), ch = r >> 6;
+        const int cmax = y < P ? (int)min64(kSubRows, P - y) : 0;
+        if (64 * ch < cmax) {
+          const int c_end = min(cmax, 64 * ch + 64);
+          int64_t row, vrow_unused;
+          cell_of(fz, y + 64 * ch, row, vrow_unused);
           int64_t end = fz.row_start[row + 1];
-          float acc = 0.f;
-          for (int c = 0; c < cmax; ++c) {
+          float acc0 = 0.f, acc1 = 0.f;
+          for (int c = 64 * ch; c < c_end; ++c) {
             while (y + c >= end) {
-              atomicAdd(fz.m_acc + row * kCz + r, acc);
-              acc = 0.f;
+              atomicAdd(fz.m_acc + row * kCz + fp, acc0);
+              atomicAdd(fz.m_acc + row * kCz + fp + 1, acc1);
+              acc0 = 0.f;
+              acc1 = 0.f;
               ++row;
               end = fz.row_start[row + 1];
             }
-            const uint32_t bits = *reinterpret_cast<const uint16_t*>(hs + swz128_offset(c, r, kSubRows));
-            acc += __uint_as_float(bits << 16);
+            const uint32_t bits = *reinterpret_cast<const uint32_t*>(hs + swz128_offset(c, fp, kSubRows));
+            acc0 += bf16lo(bits);
+            acc1 += bf16hi(bits);
           }
-          atomicAdd(fz.m_acc + row * kCz + r, acc);
+          atomicAdd(fz.m_acc + row * kCz + fp, acc0);
+          atomicAdd(fz.m_acc + row * kCz + fp + 1, acc1);
         }
         mbar_arrive(&bar.colsum_done[s]);
         if (leader) {
