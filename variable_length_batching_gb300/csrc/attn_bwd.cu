@@ -36,30 +36,39 @@ __device__ __forceinline__ int segment_of(const int32_t* __restrict__ cu, int B,
   return lo;
 }
 
-// One thread per (head, token) row, tokens fastest: the row's D features
-// come in 16-byte vectors (each thread reads whole rows, so every fetched
-// sector is used) and the D values of consecutive tokens are written side by
-// side in the [H, T_q] layout.
+// One warp per token: the token's rows of O and dO for all H heads are
+// H * D contiguous elements, read as 16-byte chunks with consecutive lanes
+// on consecutive chunks (lane l takes chunks l, l + 32, ...).  A head's
+// D / kVec chunks sit in consecutive lanes of one pass (kVec divides D and
+// D / kVec divides 32), so a butterfly over those lanes finishes the head's
+// sum and its first lane writes D[h, t] in the [H, T_q] layout.
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 rowdot_kernel(const T* __restrict__ o, const T* __restrict__ d_o, int64_t Tq, int H, float* __restrict__ Dbuf) {
-  constexpr int kVec = 16 / (int)sizeof(T);          // elements per 16-byte vector
-  const int64_t w = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  if (w >= Tq * H) return;
-  const int h = (int)(w / Tq);
-  const int64_t t = w % Tq;
-  const uint4* po = reinterpret_cast<const uint4*>(o + (t * H + h) * D);
-  const uint4* pd = reinterpret_cast<const uint4*>(d_o + (t * H + h) * D);
-  float acc[2] = {0.f, 0.f};
+  constexpr int kVec = 16 / (int)sizeof(T);          // elements per 16-byte chunk
+  constexpr int kCph = D / kVec;                      // chunks per head: 2 .. 32
+  static_assert(32 % kCph == 0, "a head's chunks must not straddle two passes");
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= Tq) return;                                // warp-uniform
+  const uint4* po = reinterpret_cast<const uint4*>(o + t * H * D);
+  const uint4* pd = reinterpret_cast<const uint4*>(d_o + t * H * D);
+  const int chunks = H * kCph;
+  for (int base = 0; base < chunks; base += 32) {     // warp-uniform trip count
+    const int c = base + lane;
+    float acc[2] = {0.f, 0.f};
+    if (c < chunks) {
+      const uint4 a = po[c], b = pd[c];
+      const T* ea = reinterpret_cast<const T*>(&a);
+      const T* eb = reinterpret_cast<const T*>(&b);
 #pragma unroll
-  for (int u = 0; u < D / kVec; ++u) {
-    const uint4 a = po[u], b = pd[u];
-    const T* ea = reinterpret_cast<const T*>(&a);
-    const T* eb = reinterpret_cast<const T*>(&b);
+      for (int e = 0; e < kVec; ++e) acc[e & 1] = fmaf(to_f32(eb[e]), to_f32(ea[e]), acc[e & 1]);
+    }
+    float sum = acc[0] + acc[1];
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) acc[e & 1] = fmaf(to_f32(eb[e]), to_f32(ea[e]), acc[e & 1]);
+    for (int off = 1; off < kCph; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (c < chunks && (lane % kCph) == 0) Dbuf[(int64_t)(c / kCph) * Tq + t] = sum;
   }
-  Dbuf[(int64_t)h * Tq + t] = acc[0] + acc[1];
 }
 
 template <typename T, int D>
@@ -183,8 +192,8 @@ cudaError_t launch_d(const AttnBwdProblem& p, float* Dbuf, unsigned int* status,
   const int64_t wq = p.T_q * p.H, wk = p.T_k * p.H;
   const unsigned gq = (unsigned)((wq + kWarps - 1) / kWarps), gk = (unsigned)((wk + kWarps - 1) / kWarps);
   if (wq > 0)
-    rowdot_kernel<T, D><<<(unsigned)((wq + 255) / 256), 256, 0, s>>>((const T*)p.o, (const T*)p.d_o, p.T_q, p.H,
-                                                                     Dbuf);
+    rowdot_kernel<T, D><<<(unsigned)((p.T_q + 7) / 8), 256, 0, s>>>((const T*)p.o, (const T*)p.d_o, p.T_q, p.H,
+                                                                    Dbuf);
   if (attn_bwd_tc_supported(std::is_same<T, bf16>::value ? NT_BF16 : NT_F32, D) && p.T_q > 0 && p.T_k > 0 &&
       p.B > 0) {
     const cudaError_t e = cudaGetLastError();
