@@ -212,9 +212,16 @@ nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void
  *   Limit: (T + T_cols) * C_z <= 2,097,152 (2 * T * C_z for square
  *   partitions); larger problems return
  *   NT_ERR_UNSUPPORTED (see nt_last_error) and enqueue nothing.
- *   Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture on the device.
+ *   Set-up: every call looks up the array's device address
+ *   (cudaGetSymbolAddress) with the calling thread's device current, so the
+ *   call stays valid across cudaDeviceReset.  With CUDA's default lazy
+ *   module loading, the first call on a device is what loads the array onto
+ *   that device: that call commits its 8 MiB of device memory and is where
+ *   an out-of-memory failure would appear (as NT_ERR_CUDA; with
+ *   CUDA_MODULE_LOADING=EAGER the array is committed when the library loads
+ *   instead).  A caller that must not allocate on its hot path makes one
+ *   warm-up call on each device outside it; make that first call before any
+ *   stream capture on the device.
  *   Sharing: every call uses the same array.  Calls that overlap on the GPU
  *   (other streams, other host threads on the same device) race on it; order
  *   them on one stream.  The kernels overwrite every element of u and v they
@@ -335,6 +342,18 @@ nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const vo
                               size_t workspace_bytes, void* stream);
 
 /*
+ * nt_varlen_attn_workspace_bytes -- bytes of device workspace that
+ * nt_varlen_attn and nt_varlen_attn_qk take for their work counter (a small
+ * constant, 256).  The counter belongs to the call that is given it: calls
+ * that may overlap on the GPU (other streams, other host threads, replays of
+ * a captured graph on several streams) each need a workspace of their own;
+ * calls ordered on one stream may share one.  Each call clears its counter
+ * on its own stream before the kernel runs, so nothing needs clearing by the
+ * caller, and the library keeps no mutable device state between calls.
+ */
+size_t nt_varlen_attn_workspace_bytes(void);
+
+/*
  * nt_varlen_attn -- softmax attention restricted to each cu_seqlens segment
  * ([VA] "What it is", "How it works"; [DL] section 3.3 "Attention through
  * packed blocks"): for token t of segment i and head h,
@@ -347,13 +366,22 @@ nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const vo
  *   scale         score scale, finite and > 0 (d^-1/2 for the usual
  *                 attention); anything else is NT_ERR_INVALID.
  *   lse           [H, T] fp32 natural-log log-sum-exp, or NULL.
+ *   workspace     >= nt_varlen_attn_workspace_bytes() device bytes, 16-byte
+ *                 aligned, or NULL (with workspace_bytes 0).  With a
+ *                 workspace, batches of short segments (mean length up to
+ *                 768) run on persistent CTAs that take work items from a
+ *                 counter kept there; without one, every batch runs one CTA
+ *                 per (segment, query tile, head), which needs no shared
+ *                 state but pays a per-item start-up cost.  Same results
+ *                 either way.
  * bf16 with d = 64 runs on the tcgen05 tensor cores; NT_F32 and other head
  * widths (32, 64, 128) run on fp32 CUDA cores.  Asynchronous.  Identical to
  * nt_varlen_attn_qk with d_cu_seqlens_k = d_cu_seqlens, T_k = T, causal = 0.
  */
 nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const void* v,
                          const int32_t* d_cu_seqlens, int32_t B, int64_t T, int32_t max_len,
-                         int32_t H, int32_t d, float scale, void* o, float* lse, void* stream);
+                         int32_t H, int32_t d, float scale, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /*
  * nt_varlen_attn_qk -- varlen attention with separate query and key
@@ -377,18 +405,24 @@ nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const voi
  *   scale         finite and > 0.
  *   causal        0 or 1.
  *   lse           [H, T_q] fp32 natural-log log-sum-exp, or NULL.
+ *   workspace, workspace_bytes  as in nt_varlen_attn.
  * Host errors: NT_ERR_INVALID (bad sizes, flags, scale, NULL or misaligned
- * pointers), NT_ERR_OVERFLOW (T_q or T_k beyond int32), NT_ERR_UNSUPPORTED
- * (head width).  bf16 with d = 64 and T_k > 0 runs on the tensor cores;
- * the rest on CUDA cores.  Asynchronous on `stream`; buffers stay owned by
- * the caller.
+ * pointers, a workspace smaller than nt_varlen_attn_workspace_bytes()),
+ * NT_ERR_OVERFLOW (T_q or T_k beyond int32), NT_ERR_UNSUPPORTED (head
+ * width).  bf16 with d = 64 and T_k > 0 runs on the tensor cores; the rest
+ * on CUDA cores.  Asynchronous on `stream`; buffers stay owned by the
+ * caller.
  */
 nt_status nt_varlen_attn_qk(nt_dtype dtype, const void* q, const void* k, const void* v,
                             const int32_t* d_cu_seqlens_q, const int32_t* d_cu_seqlens_k, int32_t B,
                             int64_t T_q, int64_t T_k, int32_t max_len_q, int32_t H, int32_t d, float scale,
-                            int32_t causal, void* o, float* lse, void* stream);
+                            int32_t causal, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
-/* Bytes of device workspace nt_varlen_attn_bwd needs: H * T_q * 4. */
+/* Bytes of device workspace nt_varlen_attn_bwd needs: the H * T_q fp32 row
+ * sums rowsum(dO * O), rounded up to 256 bytes, then 256 bytes for the work
+ * counters of its persistent kernels (cleared by the call on its stream).
+ * Overlapping backward calls need workspaces of their own. */
 size_t nt_varlen_attn_bwd_workspace_bytes(int64_t T_q, int32_t H);
 
 /*

@@ -116,19 +116,23 @@ def test_host_side_rejections(L):
     # W_g without s_out
     assert lib.nt_pair_reduce(P, 1, fake, 128, fake, fake, None, None, None, 384, None) == 1
     # attention: T > 0 without segments; bad head count; T beyond int32
-    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 0, 64, 64, 12, 64, 0.125, fake, None, None) == 1
-    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 64, 64, 0, 64, 0.125, fake, None, None) == 1
-    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 1 << 31, 64, 1, 64, 0.125, fake, None, None) == 3
+    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 0, 64, 64, 12, 64, 0.125, fake, None, None, 0, None) == 1
+    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 64, 64, 0, 64, 0.125, fake, None, None, 0, None) == 1
+    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 1 << 31, 64, 1, 64, 0.125, fake, None, None, 0, None) == 3
     # an empty stream is a no-op success
-    assert lib.nt_varlen_attn(1, None, None, None, None, 0, 0, 0, 12, 64, 0.125, None, None, None) == 0
+    assert lib.nt_varlen_attn(1, None, None, None, None, 0, 0, 0, 12, 64, 0.125, None, None, None, 0, None) == 0
     # scale must be finite and > 0
     for bad in (0.0, -0.125, float("inf"), float("nan")):
-        assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 64, 64, 1, 64, bad, fake, None, None) == 1
+        assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 64, 64, 1, 64, bad, fake, None, None, 0, None) == 1
     # qk form: causal flag 0/1 only; T_k beyond int32; key pointers needed when T_k > 0
     qk = lib.nt_varlen_attn_qk
-    assert qk(1, fake, fake, fake, fake, fake, 1, 64, 64, 64, 1, 64, 0.125, 2, fake, None, None) == 1
-    assert qk(1, fake, fake, fake, fake, fake, 1, 64, 1 << 31, 64, 1, 64, 0.125, 0, fake, None, None) == 3
-    assert qk(1, fake, None, None, fake, fake, 1, 64, 32, 64, 1, 64, 0.125, 0, fake, None, None) == 1
-    assert qk(1, fake, fake, fake, fake, fake, 1, -1, 32, 64, 1, 64, 0.125, 0, fake, None, None) == 1
-    assert qk(1, None, None, None, None, None, 0, 0, 0, 0, 4, 64, 0.125, 1, None, None, None) == 0
+    assert qk(1, fake, fake, fake, fake, fake, 1, 64, 64, 64, 1, 64, 0.125, 2, fake, None, None, 0, None) == 1
+    assert qk(1, fake, fake, fake, fake, fake, 1, 64, 1 << 31, 64, 1, 64, 0.125, 0, fake, None, None, 0, None) == 3
+    assert qk(1, fake, None, None, fake, fake, 1, 64, 32, 64, 1, 64, 0.125, 0, fake, None, None, 0, None) == 1
+    assert qk(1, fake, fake, fake, fake, fake, 1, -1, 32, 64, 1, 64, 0.125, 0, fake, None, None, 0, None) == 1
+    assert qk(1, None, None, None, None, None, 0, 0, 0, 0, 4, 64, 0.125, 1, None, None, None, 0, None) == 0
+    # a workspace smaller than the stated size, or misaligned
+    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 64, 64, 1, 64, 0.125, fake, None, fake, 4, None) == 1
+    assert lib.nt_varlen_attn(1, fake, fake, fake, fake, 1, 64, 64, 1, 64, 0.125, fake, None, odd, 256, None) == 1
+    assert lib.nt_varlen_attn_workspace_bytes() >= 4
     assert lib.nt_last_error()  # a detail string was recorded

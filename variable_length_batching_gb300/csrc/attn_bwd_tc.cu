@@ -25,7 +25,6 @@
 // issues), 2-9 = compute, two warps per TMEM lane quadrant, each taking 32
 // of a tile's 64 columns.  256 TMEM columns and about 82 KB of shared memory
 // per CTA: two CTAs share an SM.  Every wait is bounded.
-#include <atomic>
 
 #include "tc_ptx.cuh"
 
@@ -544,7 +543,7 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 // ============================================================================ persistent
 // Persistent forms of the two kernels for short segments: two CTAs per SM
-// take work items from a global counter (one per launch slot).  Lane 0 of
+// take work items from a counter in the caller's workspace.  Lane 0 of
 // the producer warp fetches the next item while the current one's ring is
 // full and publishes it through a two-slot queue in shared memory; the next
 // item's resident tiles are loaded once the current item's last S/dP MMA has
@@ -554,8 +553,6 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 // Every barrier keeps its phase across items.
 
 constexpr int kQueue = 2;
-constexpr int kCounterSlots = 64;
-__device__ unsigned int g_bwd_next[kCounterSlots];
 
 // One work item: segment b's 128-row tile t (keys for dK/dV, queries for dQ)
 // for head h; n = streamed tiles; first = the first streamed token (segment
@@ -1073,8 +1070,6 @@ bool make_map_thd(CUtensorMap* map, const void* ptr, int64_t T, int H, uint32_t 
   return make_tmap_bf16(map, ptr, 3, dims, strides, box);
 }
 
-std::atomic<unsigned int> g_bwd_slot{0};
-
 }  // namespace
 
 bool attn_bwd_tc_supported(nt_dtype dt, int d) { return dt == NT_BF16 && d == kD; }
@@ -1098,15 +1093,12 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsig
   // segment over 1.25 times the mean); one CTA per item otherwise, where the
   // hardware scheduler balances the work and the staged, row-contiguous
   // epilogue of the per-item kernels pays.
-  const bool pkv = p.T_k <= (int64_t)768 * p.B && (int64_t)4 * p.max_len_k * p.B > (int64_t)5 * p.T_k;
-  const bool pq = p.T_q <= (int64_t)768 * p.B && (int64_t)4 * p.max_len_q * p.B > (int64_t)5 * p.T_q;
-  unsigned int* counters = nullptr;
+  // The counters are the caller's (two words of its workspace); without
+  // them every kernel runs one CTA per item.
+  const bool pkv = p.work && p.T_k <= (int64_t)768 * p.B && (int64_t)4 * p.max_len_k * p.B > (int64_t)5 * p.T_k;
+  const bool pq = p.work && p.T_q <= (int64_t)768 * p.B && (int64_t)4 * p.max_len_q * p.B > (int64_t)5 * p.T_q;
+  unsigned int* counters = p.work;
   if (pkv || pq) {
-    void* base = nullptr;
-    e = cudaGetSymbolAddress(&base, g_bwd_next);
-    if (e != cudaSuccess) return e;
-    const unsigned int slot = (g_bwd_slot.fetch_add(2) % kCounterSlots) & ~1u;
-    counters = static_cast<unsigned int*>(base) + slot;
     e = cudaMemsetAsync(counters, 0, 2 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;
   }

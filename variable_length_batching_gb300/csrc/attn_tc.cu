@@ -10,12 +10,14 @@
 //     long segments each CTA walks many key tiles and its set-up, Q load and
 //     epilogue cost little.
 //   - persistent CTAs (attn_persistent_kernel), four per SM, taking items
-//     from a global counter: the producer warp fetches the next item while
-//     the current one's K/V ring is full, loads its Q as soon as the current
-//     item's last S has been computed, and the next item's first S is issued
-//     while the softmax warps write out the current item's O.  With short
-//     segments this hides the per-item cost that dominates one CTA per item.
-//   The launcher picks by the mean segment length.
+//     from a counter in the caller's workspace: the producer warp fetches
+//     the next item while the current one's K/V ring is full, loads its Q as
+//     soon as the current item's last S has been computed, and the next
+//     item's first S is issued while the softmax warps write out the current
+//     item's O.  With short segments this hides the per-item cost that
+//     dominates one CTA per item.
+//   The launcher picks by the mean segment length (and takes one CTA per
+//   item when the caller gives no workspace).
 //
 // Warps: 0 = TMA producer (Q per item; K and V tiles of 64 tokens through a
 // 2-stage ring, 3-D tensor maps over the token-major [T, H, d] tensors),
@@ -44,8 +46,6 @@
 // bottom-right corner: each item loads only the key tiles its last query row
 // can see, tiles wholly under every row's diagonal run the unmasked path,
 // and a query that sees no key gets zeros with lse = -inf.
-#include <atomic>
-
 #include "tc_ptx.cuh"
 
 namespace nt {
@@ -70,11 +70,6 @@ constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kColS = 0, kColO = 64;
 
 constexpr int kQueue = 2;
-constexpr int kCounterSlots = 64;
-
-// Work counters: each launch takes one slot (round robin), cleared on its
-// stream before the launch.
-__device__ unsigned int g_attn_next[kCounterSlots];
 
 // One work item: segment b's query tile qi for head h, with its offsets and
 // key-tile count.  b < 0 ends the queue.
@@ -432,7 +427,7 @@ __device__ __forceinline__ bool take_item(PBars& bar, int n, volatile int* abort
   return true;
 }
 
-// The next valid work item of the launch from the global counter (b = -1
+// The next valid work item of the launch from the work counter (b = -1
 // once the counter has passed every (segment, query tile, head)).  Indices
 // run over (segment, query tile, head), heads fastest; an index whose query
 // tile lies past its segment's end is skipped, and the counter is moved past
@@ -725,8 +720,6 @@ bool make_map_thd(CUtensorMap* map, const void* ptr, int64_t T, int H, uint32_t 
   return make_tmap_bf16(map, ptr, 3, dims, strides, box);
 }
 
-std::atomic<unsigned int> g_next_slot{0};
-
 }  // namespace
 
 bool attn_tc_supported(nt_dtype dt, int d) { return dt == NT_BF16 && d == kD; }
@@ -743,14 +736,12 @@ cudaError_t launch_attn_tc(const AttnProblem& p, unsigned int* status, cudaStrea
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const float scale_log2 = p.scale * 1.4426950408889634f;
   cudaError_t e;
-  // Short segments (few key tiles per item): persistent CTAs; long ones: one
-  // CTA per item.  The crossover measured on the 65,536-token sweeps lies
-  // between mean lengths of 512 and 1,024 tokens.
-  if (p.T_q <= (int64_t)768 * p.B) {
-    void* base = nullptr;
-    e = cudaGetSymbolAddress(&base, g_attn_next);
-    if (e != cudaSuccess) return e;
-    unsigned int* next = static_cast<unsigned int*>(base) + (g_next_slot.fetch_add(1) % kCounterSlots);
+  // Short segments (few key tiles per item): persistent CTAs over the
+  // caller's work counter; long ones, or no counter given: one CTA per item.
+  // The crossover measured on the 65,536-token sweeps lies between mean
+  // lengths of 512 and 1,024 tokens.
+  if (p.work && p.T_q <= (int64_t)768 * p.B) {
+    unsigned int* next = p.work;
     e = cudaMemsetAsync(next, 0, sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;
     auto kern = p.causal ? attn_persistent_kernel<true> : attn_persistent_kernel<false>;

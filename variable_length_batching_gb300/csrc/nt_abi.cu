@@ -99,6 +99,16 @@ using namespace nt;
 
 namespace {
 
+// Device workspace of the attention calls' persistent schedules: their work
+// counters (a few 32-bit words), padded to 256 bytes.
+constexpr size_t kAttnWorkBytes = 256;
+
+// Byte offset of the backward's two work counters in its workspace, after
+// the H * T_q fp32 row sums rowsum(dO * O) (256-byte aligned).
+size_t bwd_counter_offset(int64_t T_q, int32_t H) {
+  return ((size_t)T_q * (size_t)H * sizeof(float) + 255) & ~(size_t)255;
+}
+
 // The residual transition of P cells with the ReLU update (W3 == NULL) or
 // the SwiGLU one.
 nt_status transition_cells(int64_t P, nt_dtype dtype, const void* z_in, void* z_out, int32_t C_z, int32_t H_t,
@@ -529,10 +539,13 @@ nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const vo
   return NT_OK;
 }
 
+size_t nt_varlen_attn_workspace_bytes(void) { return kAttnWorkBytes; }
+
 nt_status nt_varlen_attn_qk(nt_dtype dtype, const void* q, const void* k, const void* v,
                             const int32_t* d_cu_seqlens_q, const int32_t* d_cu_seqlens_k, int32_t B,
                             int64_t T_q, int64_t T_k, int32_t max_len_q, int32_t H, int32_t d, float scale,
-                            int32_t causal, void* o, float* lse, void* stream) {
+                            int32_t causal, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream) {
   if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
   if (B < 0 || T_q < 0 || T_k < 0 || H <= 0 || d <= 0 || max_len_q < 0)
     return fail(NT_ERR_INVALID, "bad sizes B=%d T_q=%lld T_k=%lld H=%d d=%d max_len_q=%d", B, (long long)T_q,
@@ -545,12 +558,15 @@ nt_status nt_varlen_attn_qk(nt_dtype dtype, const void* q, const void* k, const 
   if (T_q > 0 && B == 0) return fail(NT_ERR_INVALID, "T_q > 0 with no segments");
   if (T_q > 0 && (!q || !o || !d_cu_seqlens_q || !d_cu_seqlens_k)) return fail(NT_ERR_INVALID, "NULL pointer");
   if (T_q > 0 && T_k > 0 && (!k || !v)) return fail(NT_ERR_INVALID, "NULL key or value pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(workspace))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  if (workspace && workspace_bytes < kAttnWorkBytes)
+    return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, kAttnWorkBytes);
   if (T_q == 0) return NT_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const AttnProblem prob = {q, k, v, d_cu_seqlens_q, d_cu_seqlens_k, B, T_q, T_k, max_len_q,
-                            H, d, scale, causal != 0, o, lse};
+                            H, d, scale, causal != 0, o, lse, static_cast<unsigned int*>(workspace)};
   cudaError_t e;
   if (attn_tc_supported(dtype, d) && T_k > 0) {
     e = launch_attn_tc(prob, status_word(), s);
@@ -565,7 +581,7 @@ nt_status nt_varlen_attn_qk(nt_dtype dtype, const void* q, const void* k, const 
 
 size_t nt_varlen_attn_bwd_workspace_bytes(int64_t T_q, int32_t H) {
   if (T_q < 0 || H < 0) return 0;
-  return (size_t)T_q * (size_t)H * sizeof(float);
+  return bwd_counter_offset(T_q, H) + kAttnWorkBytes;
 }
 
 nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const void* v, const void* o,
@@ -597,7 +613,9 @@ nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const
                 nt_varlen_attn_bwd_workspace_bytes(T_q, H));
   if (T_q == 0 && T_k == 0) return NT_OK;
   const AttnBwdProblem prob = {q, k, v, o, d_o, lse, d_cu_seqlens_q, d_cu_seqlens_k, B, T_q, T_k,
-                               max_len_q, max_len_k, H, d, scale, causal != 0, dq, dk, dv};
+                               max_len_q, max_len_k, H, d, scale, causal != 0, dq, dk, dv,
+                               reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) +
+                                                               bwd_counter_offset(T_q, H))};
   cudaError_t e = launch_attn_bwd(dtype, prob, static_cast<float*>(workspace), status_word(),
                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "varlen attention backward launch");
@@ -606,9 +624,10 @@ nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const
 
 nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const void* v,
                          const int32_t* d_cu_seqlens, int32_t B, int64_t T, int32_t max_len,
-                         int32_t H, int32_t d, float scale, void* o, float* lse, void* stream) {
+                         int32_t H, int32_t d, float scale, void* o, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   return nt_varlen_attn_qk(dtype, q, k, v, d_cu_seqlens, d_cu_seqlens, B, T, T, max_len, H, d, scale, 0, o,
-                           lse, stream);
+                           lse, workspace, workspace_bytes, stream);
 }
 
 nt_status nt_device_status(void* stream) {

@@ -196,6 +196,9 @@ struct AttnProblem {
   bool causal;
   void* o;
   float* lse;
+  // Caller-owned work counter of the persistent schedule (one 32-bit word,
+  // cleared on the launch's stream), or NULL: one CTA per work item then.
+  unsigned int* work;
 };
 
 // Backward of one varlen attention problem (the forward's q, k, v, o, its
@@ -218,6 +221,10 @@ struct AttnBwdProblem {
   void* dq;
   void* dk;
   void* dv;
+  // Caller-owned work counters of the persistent dK/dV and dQ kernels (two
+  // 32-bit words, cleared on the launch's stream), or NULL: one CTA per
+  // work item then.
+  unsigned int* work;
 };
 bool attn_bwd_supported(int d);
 // Dbuf: H * T_q fp32 of device workspace (rowsum(dO * O)).

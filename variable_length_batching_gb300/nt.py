@@ -59,9 +59,10 @@ SIGNATURES = {
     "nt_pair_block_fused_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
     "nt_pair_block_fused": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P]),
+    "nt_varlen_attn_workspace_bytes": (_SZ, []),
+    "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _P]),
     "nt_varlen_attn_qk": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _F, _I32,
-                                 _P, _P, _P]),
+                                 _P, _P, _P, _SZ, _P]),
     "nt_varlen_attn_bwd_workspace_bytes": (_SZ, [_I64, _I32]),
     "nt_varlen_attn_bwd": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _I32,
                                   _F, _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -344,9 +345,26 @@ def nt_pair_reduce(part: Partition, z: torch.Tensor, W_g: Optional[torch.Tensor]
     return m, s_out
 
 
+def nt_varlen_attn_workspace_bytes() -> int:
+    return int(lib().nt_varlen_attn_workspace_bytes())
+
+
+def _attn_workspace(workspace, device):
+    """The attention calls' work-counter workspace: a given uint8 tensor, a
+    fresh one (None), or no workspace at all (False: one CTA per item)."""
+    if workspace is False:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nt_varlen_attn_workspace_bytes(), dtype=torch.uint8, device=device)
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
 def nt_varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
                    max_len: int, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                   lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+                   lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None, workspace=None):
+    """``workspace``: a device tensor of at least nt_varlen_attn_workspace_bytes()
+    bytes for the persistent schedule's work counter (None allocates one per
+    call; False passes none, which runs one CTA per work item)."""
     T, H, d = q.shape
     if k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must share the shape (T, H, d)")
@@ -359,8 +377,9 @@ def nt_varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
         out = torch.empty_like(q)
     if want_lse and lse is None:
         lse = torch.empty(H, T, dtype=torch.float32, device=q.device)
+    ws, ws_bytes = _attn_workspace(workspace, q.device)
     st = lib().nt_varlen_attn(_dtype(q), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, T, int(max_len),
-                              H, d, float(scale), _ptr(out), _ptr(lse), _stream(stream))
+                              H, d, float(scale), _ptr(out), _ptr(lse), ws, ws_bytes, _stream(stream))
     _check(st, "nt_varlen_attn")
     return out, lse
 
@@ -368,9 +387,11 @@ def nt_varlen_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
 def nt_varlen_attn_qk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
                       cu_seqlens_k: torch.Tensor, max_len_q: int, scale: Optional[float] = None,
                       causal: bool = False, out: Optional[torch.Tensor] = None,
-                      lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None):
+                      lse: Optional[torch.Tensor] = None, want_lse: bool = False, stream=None,
+                      workspace=None):
     """Queries of segment b attend to keys [cu_k[b], cu_k[b+1]); with
-    ``causal`` the diagonal is aligned to each segment's bottom-right corner."""
+    ``causal`` the diagonal is aligned to each segment's bottom-right corner.
+    ``workspace`` as in :func:`nt_varlen_attn`."""
     T_q, H, d = q.shape
     T_k = k.shape[0]
     if tuple(k.shape[1:]) != (H, d) or v.shape != k.shape:
@@ -386,9 +407,10 @@ def nt_varlen_attn_qk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seql
         out = torch.empty_like(q)
     if want_lse and lse is None:
         lse = torch.empty(H, T_q, dtype=torch.float32, device=q.device)
+    ws, ws_bytes = _attn_workspace(workspace, q.device)
     st = lib().nt_varlen_attn_qk(_dtype(q), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                                  B, T_q, T_k, int(max_len_q), H, d, float(scale), int(bool(causal)),
-                                 _ptr(out), _ptr(lse), _stream(stream))
+                                 _ptr(out), _ptr(lse), ws, ws_bytes, _stream(stream))
     _check(st, "nt_varlen_attn_qk")
     return out, lse
 
