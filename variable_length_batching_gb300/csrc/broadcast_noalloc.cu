@@ -18,8 +18,6 @@
 // streams, or different host threads on the same device) race on it.  The
 // kernels overwrite every element of u and v they read, so nothing needs to
 // start at zero and the previous call's contents never leak into a result.
-#include <mutex>
-
 #include "nt_common.cuh"
 
 namespace nt {
@@ -29,26 +27,18 @@ constexpr size_t kNoAllocScratchFloats = size_t(1) << 21;   // 8 MiB of fp32
 
 static __device__ __align__(256) float g_noalloc_uv[kNoAllocScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevices] = {};
-
 // Device address of g_noalloc_uv on the current device.  In host code the
-// array's name is only a stand-in; the real address is looked up once per
-// device, with that device current, by this function.
+// array's name is only a stand-in; the real address is looked up with the
+// device current, on every call (a cheap query): after a cudaDeviceReset the
+// module is loaded again and the array may sit elsewhere, so no address is
+// kept from one call to the next.  With CUDA's default lazy module loading
+// the first lookup on a device is what loads the module holding the array,
+// which commits its 8 MiB of device memory there and can fail then.
 cudaError_t noalloc_scratch(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_uv);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_uv);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+  *out = static_cast<float*>(p);
   return cudaSuccess;
 }
 
@@ -73,7 +63,8 @@ nt_status nt_pair_broadcast_noalloc(const nt_partition* part, nt_dtype dtype, co
                         "use nt_pair_broadcast with a caller workspace");
   float* scratch = nullptr;
   if (noalloc_scratch(&scratch) != cudaSuccess)
-    return record_error(NT_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch failed");
+    return record_error(NT_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch failed (the first call on a "
+                                     "device loads the 8 MiB array there)");
   // The regular entry point validates every argument and launches the same
   // kernels; the library's own array stands in for the caller's workspace.
   return nt_pair_broadcast(part, dtype, s_left, s_right, C_s, W_a, W_b, C_z, z, scratch,
