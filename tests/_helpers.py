@@ -15,6 +15,13 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 # Normwise tolerances: max|gpu - oracle| / max|oracle| per output tensor.
 TOL = {"bf16": 2e-2, "f32": 1e-5}
+# Bounds on the elementwise diagnostic |g - r| / max(|r|, 1e-3 max|r|).  At
+# the floor the normwise bound alone would allow TOL / 1e-3 (20 for bf16,
+# 1e-2 for fp32); these are 2.5 times tighter, about three times the worst
+# value measured over the GPU parity suite (2.7 bf16, 3.4e-4 fp32), whose
+# largest entries sit at the floor: the rounding of a large neighbour seen
+# against an entry a thousand times smaller.
+ELEM_BOUND = {"bf16": 8.0, "f32": 4e-3}
 
 
 def golden(name):
@@ -36,15 +43,44 @@ def oracle_weights(w: BlockWeights, eps: float = 1e-5) -> Weights:
                    W_g=f64(w.W_g), b_g=f64(w.b_g))
 
 
-def normwise_err(got, ref) -> float:
+# Per-test record of both error measures, filled by normwise_err and printed
+# (and optionally written as JSON) by conftest at the end of the session.
+PARITY_RECORD = []
+
+
+def elementwise_err(got, ref) -> float:
+    """Elementwise relative error with a floor: max |g - r| / max(|r|,
+    1e-3 max|r|).  A diagnostic beside the normwise bound: it exposes large
+    relative errors in the small-magnitude entries that the normwise measure
+    scales away."""
+    got = f64(got) if not isinstance(got, np.ndarray) else got.astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    top = np.abs(ref).max()
+    if top == 0:
+        return float(np.abs(got - ref).max())
+    return float((np.abs(got - ref) / np.maximum(np.abs(ref), 1e-3 * top)).max())
+
+
+def normwise_err(got, ref, dtype: str = "bf16") -> float:
+    """Normwise relative error max |g - r| / max |r| (the pass bar).  The
+    elementwise diagnostic of the same pair is recorded beside it and must
+    stay within ELEM_BOUND[dtype] (an AssertionError otherwise)."""
     got = f64(got) if not isinstance(got, np.ndarray) else got.astype(np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     if ref.size == 0:
         return 0.0
     denom = np.abs(ref).max()
     if denom == 0:
-        return float(np.abs(got - ref).max())
-    return float(np.abs(got - ref).max() / denom)
+        err = float(np.abs(got - ref).max())
+    else:
+        err = float(np.abs(got - ref).max() / denom)
+    elem = elementwise_err(got, ref)
+    PARITY_RECORD.append({"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0],
+                          "shape": list(ref.shape), "dtype": dtype, "normwise": err, "elementwise": elem})
+    assert elem <= ELEM_BOUND[dtype], f"elementwise error {elem:.3e} > {ELEM_BOUND[dtype]} ({dtype})"
+    return err
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:

@@ -68,7 +68,7 @@ def test_attention_backward(nt, lq, lk, H, d, dtype, causal):
     lk = lq if lk is None else lk
     got, ref, _, _ = _case(nt, lq, lk, H, d, dtype, causal)
     for g, r in zip(got, ref):
-        assert normwise_err(to_np(g), r) <= TOL[dtype]
+        assert normwise_err(to_np(g), r, dtype=dtype) <= TOL[dtype]
     nt.nt_device_status()
 
 
@@ -84,7 +84,7 @@ def test_attention_backward_full_size_sampled(nt, causal):
     rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in segs])
     idx = torch.as_tensor(rows, device=DEV)
     for g, r in zip(got, ref):
-        assert normwise_err(to_np(g[idx]), r[rows]) <= TOL["bf16"]
+        assert normwise_err(to_np(g[idx]), r[rows], dtype="bf16") <= TOL["bf16"]
     nt.nt_device_status()
 
 

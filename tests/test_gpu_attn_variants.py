@@ -45,7 +45,7 @@ def _check(o, l, O_ref, lse_ref, dtype):
     assert np.array_equal(np.isneginf(l), dead)
     for h in range(dead.shape[0]):
         assert np.all(o[dead[h], h, :] == 0.0)
-    assert normwise_err(o, O_ref) <= TOL[dtype]
+    assert normwise_err(o, O_ref, dtype=dtype) <= TOL[dtype]
     live = ~dead
     if live.any():
         assert np.abs(l[live] - lse_ref[live]).max() <= (1e-4 if dtype == "f32" else 2e-2)
@@ -141,7 +141,7 @@ def test_causal_full_size_sampled(nt):
     O_ref, lse_ref = oattn.varlen_attention(f64(a.q), f64(a.k), f64(a.v), cu, segments=segs, causal=True)
     rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in segs])
     idx = torch.as_tensor(rows, device=DEV)
-    assert normwise_err(to_np(o[idx]), O_ref[rows]) <= TOL["bf16"]
+    assert normwise_err(to_np(o[idx]), O_ref[rows], dtype="bf16") <= TOL["bf16"]
     assert np.abs(to_np(l[:, idx]) - lse_ref[:, rows]).max() <= 2e-2
     nt.nt_device_status()
 

@@ -52,12 +52,12 @@ def test_fused_block_square(nt, cfg, lengths, biases):
     zu, mu, su = nt.block_forward(part, s, w)
     assert torch.equal(zf, zu)                      # same roundings, same kernels for z~
     tol = TOL[cfg.dtype]
-    assert normwise_err(to_np(mf), to_np(mu)) <= tol and normwise_err(to_np(sf), to_np(su)) <= tol
+    assert normwise_err(to_np(mf), to_np(mu), dtype=cfg.dtype) <= tol and normwise_err(to_np(sf), to_np(su), dtype=cfg.dtype) <= tol
     if cfg.name != wl.LOGNORMAL_BF16.name:          # the dense oracle on the small batches
         ref = oblock.block_packed(inp.lengths, f64(inp.s), oracle_weights(inp.blocks[0]))
-        assert normwise_err(to_np(zf), ref.z_tilde) <= tol
-        assert normwise_err(to_np(mf), ref.m) <= tol
-        assert normwise_err(to_np(sf), ref.s_out) <= tol
+        assert normwise_err(to_np(zf), ref.z_tilde, dtype=cfg.dtype) <= tol
+        assert normwise_err(to_np(mf), ref.m, dtype=cfg.dtype) <= tol
+        assert normwise_err(to_np(sf), ref.s_out, dtype=cfg.dtype) <= tol
     nt.nt_device_status()
 
 
@@ -72,9 +72,9 @@ def test_fused_block_rect(nt, rows, cols):
     ref = oblock.block_packed_rect(inp.rows, inp.cols, f64(inp.s_row), f64(inp.s_col), oracle_weights(inp.blocks[0]))
     zu, mu, su = nt.block_forward(part, sr, w, s_col=sc)
     assert torch.equal(zf, zu)
-    assert normwise_err(to_np(zf), ref.z_tilde) <= TOL["bf16"]
-    assert normwise_err(to_np(mf), ref.m) <= TOL["bf16"]
-    assert normwise_err(to_np(sf), ref.s_out) <= TOL["bf16"]
+    assert normwise_err(to_np(zf), ref.z_tilde, dtype="bf16") <= TOL["bf16"]
+    assert normwise_err(to_np(mf), ref.m, dtype="bf16") <= TOL["bf16"]
+    assert normwise_err(to_np(sf), ref.s_out, dtype="bf16") <= TOL["bf16"]
     nt.nt_device_status()
 
 
@@ -92,8 +92,8 @@ def test_fused_block_swiglu(nt):
     zu = nt.nt_pair_transition_swiglu(part, z, w.ln_gamma, w.ln_beta, w.W1, w.b1, W3, b3, w.W2, w.b2)
     mu, su = nt.nt_pair_reduce(part, zu, w.W_g, w.b_g, s_in=s)
     assert torch.equal(zf, zu)
-    assert normwise_err(to_np(mf), to_np(mu)) <= TOL["bf16"]
-    assert normwise_err(to_np(sf), to_np(su)) <= TOL["bf16"]
+    assert normwise_err(to_np(mf), to_np(mu), dtype="bf16") <= TOL["bf16"]
+    assert normwise_err(to_np(sf), to_np(su), dtype="bf16") <= TOL["bf16"]
     nt.nt_device_status()
 
 

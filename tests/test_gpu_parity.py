@@ -174,7 +174,7 @@ def test_broadcast(nt, cfg, lengths):
     z = nt.nt_pair_broadcast(part, s, s, w.W_a.to(DEV), w.W_b.to(DEV))
     ref = oblock.pair_broadcast(inp.lengths, f64(inp.s), f64(inp.s), f64(w.W_a), f64(w.W_b))
     assert z.shape == ref.shape
-    assert normwise_err(to_np(z), ref) <= TOL[cfg.dtype]
+    assert normwise_err(to_np(z), ref, dtype=cfg.dtype) <= TOL[cfg.dtype]
     nt.nt_device_status()
 
 
@@ -186,7 +186,7 @@ def test_broadcast_left_right_distinct(nt):
     part = nt.nt_partition_build(dev_lengths(inp.lengths))
     z = nt.nt_pair_broadcast(part, inp.s.to(DEV), sR.to(DEV), w.W_a.to(DEV), w.W_b.to(DEV))
     ref = oblock.pair_broadcast(inp.lengths, f64(inp.s), f64(sR), f64(w.W_a), f64(w.W_b))
-    assert normwise_err(to_np(z), ref) <= TOL[cfg.dtype]
+    assert normwise_err(to_np(z), ref, dtype=cfg.dtype) <= TOL[cfg.dtype]
 
 
 @pytest.mark.parametrize("cfg,rows,biases", [(wl.TINY_FP32, 1966, False), (wl.TINY_FP32, 517, True),
@@ -203,7 +203,7 @@ def test_transition(nt, cfg, rows, biases):
     out = nt.nt_pair_transition(part, zd, wd.ln_gamma, wd.ln_beta, wd.W1, wd.b1, wd.W2, wd.b2)
     ref = oblock.pair_transition(f64(z), f64(w.ln_gamma), f64(w.ln_beta), 1e-5, f64(w.W1), f64(w.b1),
                                  f64(w.W2), f64(w.b2))
-    assert normwise_err(to_np(out), ref) <= TOL[cfg.dtype]
+    assert normwise_err(to_np(out), ref, dtype=cfg.dtype) <= TOL[cfg.dtype]
     # in place gives the same bits
     nt.nt_pair_transition(part, zd, wd.ln_gamma, wd.ln_beta, wd.W1, wd.b1, wd.W2, wd.b2, out=zd)
     assert torch.equal(zd, out)
@@ -220,8 +220,8 @@ def test_reduce(nt, cfg, lengths):
     s = inp.s.to(DEV)
     m, s_out = nt.nt_pair_reduce(part, z.to(DEV), w.W_g.to(DEV), w.b_g.to(DEV), s_in=s)
     m_ref, s_ref = oblock.pair_reduce(inp.lengths, f64(z), f64(w.W_g), f64(w.b_g), f64(inp.s))
-    assert normwise_err(to_np(m), m_ref) <= TOL[cfg.dtype]
-    assert normwise_err(to_np(s_out), s_ref) <= TOL[cfg.dtype]
+    assert normwise_err(to_np(m), m_ref, dtype=cfg.dtype) <= TOL[cfg.dtype]
+    assert normwise_err(to_np(s_out), s_ref, dtype=cfg.dtype) <= TOL[cfg.dtype]
     m2, none = nt.nt_pair_reduce(part, z.to(DEV))
     assert none is None and torch.equal(m2, m)
 
@@ -240,9 +240,9 @@ def test_block_full(nt, cfg, lengths, biases):
     z, m, s_out = nt.block_forward(part, inp.s.to(DEV), dev_weights(w))
     ref = oblock.block_packed(inp.lengths, f64(inp.s), oracle_weights(w))
     tol = TOL[cfg.dtype]
-    assert normwise_err(to_np(z), ref.z_tilde) <= tol
-    assert normwise_err(to_np(m), ref.m) <= tol
-    assert normwise_err(to_np(s_out), ref.s_out) <= tol
+    assert normwise_err(to_np(z), ref.z_tilde, dtype=cfg.dtype) <= tol
+    assert normwise_err(to_np(m), ref.m, dtype=cfg.dtype) <= tol
+    assert normwise_err(to_np(s_out), ref.s_out, dtype=cfg.dtype) <= tol
     nt.nt_device_status()
 
 
@@ -264,12 +264,12 @@ def test_block_full_size_sampled(nt, cfg):
                             ref_part.pair_off[:-1], [ref_part.P - 1]])
     _, Pt = oblock.block_cells(inp.lengths, f64(inp.s), ow, cells)
     got = to_np(z[torch.as_tensor(cells, device=DEV)])
-    assert normwise_err(got, Pt) <= TOL[cfg.dtype]
+    assert normwise_err(got, Pt, dtype=cfg.dtype) <= TOL[cfg.dtype]
     rows = np.concatenate([rng.integers(0, ref_part.T, size=12), ref_part.cu_seqlens[:-1]])
     m_ref, s_ref = oblock.block_rows(inp.lengths, f64(inp.s), ow, rows)
     idx = torch.as_tensor(rows, device=DEV)
-    assert normwise_err(to_np(m[idx]), m_ref) <= TOL[cfg.dtype]
-    assert normwise_err(to_np(s_out[idx]), s_ref) <= TOL[cfg.dtype]
+    assert normwise_err(to_np(m[idx]), m_ref, dtype=cfg.dtype) <= TOL[cfg.dtype]
+    assert normwise_err(to_np(s_out[idx]), s_ref, dtype=cfg.dtype) <= TOL[cfg.dtype]
     nt.nt_device_status()
 
 
@@ -285,8 +285,8 @@ def test_stacked_blocks_chain(nt):
     for w in inp.blocks:
         z, m, s = nt.block_forward(part, s, dev_weights(w))
     x_ref, last = oblock.stacked_blocks(inp.lengths, f64(inp.s), [oracle_weights(w) for w in inp.blocks])
-    assert normwise_err(to_np(s), x_ref) <= TOL["bf16"]
-    assert normwise_err(to_np(z), last.z_tilde) <= TOL["bf16"]
+    assert normwise_err(to_np(s), x_ref, dtype="bf16") <= TOL["bf16"]
+    assert normwise_err(to_np(z), last.z_tilde, dtype="bf16") <= TOL["bf16"]
     nt.nt_device_status()
 
 
@@ -317,7 +317,7 @@ def _attn_case(nt, seqlens, H, d, dtype, seed=0, lse=True):
 def test_varlen_attention(nt, seqlens, H, d, dtype):
     a, cu, o, l = _attn_case(nt, seqlens, H, d, dtype)
     O_ref, lse_ref = oattn.varlen_attention(f64(a.q), f64(a.k), f64(a.v), cu)
-    assert normwise_err(to_np(o), O_ref) <= TOL[dtype]
+    assert normwise_err(to_np(o), O_ref, dtype=dtype) <= TOL[dtype]
     assert np.abs(to_np(l) - lse_ref).max() <= (1e-4 if dtype == "f32" else 2e-2)
     nt.nt_device_status()
 
@@ -339,7 +339,7 @@ def test_varlen_attention_zero_leakage(nt):
     # a constant V comes back as that constant, within the bf16 tolerance: the
     # kernel normalises by a running max that may trail the true one, so the
     # largest probability is not exactly 1 and P's bf16 rounding stays visible
-    assert normwise_err(to_np(o2[lo:hi]), np.full((hi - lo, 2, 64), 7.0)) <= TOL["bf16"]
+    assert normwise_err(to_np(o2[lo:hi]), np.full((hi - lo, 2, 64), 7.0), dtype="bf16") <= TOL["bf16"]
 
 
 def test_varlen_attention_full_size_sampled(nt):
@@ -358,7 +358,7 @@ def test_varlen_attention_full_size_sampled(nt):
     O_ref, lse_ref = oattn.varlen_attention(f64(a.q), f64(a.k), f64(a.v), cu, segments=segs)
     rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in segs])
     idx = torch.as_tensor(rows, device=DEV)
-    assert normwise_err(to_np(o[idx]), O_ref[rows]) <= TOL["bf16"]
+    assert normwise_err(to_np(o[idx]), O_ref[rows], dtype="bf16") <= TOL["bf16"]
     assert np.abs(to_np(l[:, idx]) - lse_ref[:, rows]).max() <= 2e-2
     nt.nt_device_status()
 

@@ -76,9 +76,9 @@ def test_rect_block(nt, cfg, rows, cols, biases):
     ref = oblock.block_packed_rect(inp.rows, inp.cols, f64(inp.s_row), f64(inp.s_col), oracle_weights(w))
     tol = TOL[cfg.dtype]
     assert z.shape == (ref.z_tilde.shape[0], cfg.C_z)
-    assert normwise_err(to_np(z), ref.z_tilde) <= tol
-    assert normwise_err(to_np(m), ref.m) <= tol
-    assert normwise_err(to_np(s_out), ref.s_out) <= tol
+    assert normwise_err(to_np(z), ref.z_tilde, dtype=cfg.dtype) <= tol
+    assert normwise_err(to_np(m), ref.m, dtype=cfg.dtype) <= tol
+    assert normwise_err(to_np(s_out), ref.s_out, dtype=cfg.dtype) <= tol
     # rows of a sample with M_i = 0 have exact zero means
     cu = np.concatenate([[0], np.cumsum(inp.rows)])
     for i in np.nonzero(np.asarray(inp.cols) == 0)[0]:
@@ -94,7 +94,7 @@ def test_rect_broadcast_alone(nt):
     part = nt.nt_partition_build_rect(_dev(inp.rows), _dev(inp.cols))
     z = nt.nt_pair_broadcast(part, inp.s_row.to(DEV), inp.s_col.to(DEV), w.W_a.to(DEV), w.W_b.to(DEV))
     ref = oblock.pair_broadcast_rect(inp.rows, inp.cols, f64(inp.s_row), f64(inp.s_col), f64(w.W_a), f64(w.W_b))
-    assert normwise_err(to_np(z), ref) <= TOL["bf16"]
+    assert normwise_err(to_np(z), ref, dtype="bf16") <= TOL["bf16"]
 
 
 def test_rect_with_equal_lengths_is_the_square_path(nt):

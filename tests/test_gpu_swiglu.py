@@ -55,7 +55,7 @@ def _ref(z, w, rows=None):
 ])
 def test_swiglu_transition(nt, lengths, C_z, H_t, dtype, biases, in_place):
     z, w, out = _run(nt, lengths, C_z, H_t, dtype, biases, in_place=in_place)
-    assert normwise_err(to_np(out), _ref(z, w)) <= TOL[dtype]
+    assert normwise_err(to_np(out), _ref(z, w), dtype=dtype) <= TOL[dtype]
     nt.nt_device_status()
 
 
@@ -69,7 +69,7 @@ def test_swiglu_full_size_sampled(nt):
     rng = np.random.default_rng(3)
     rows = np.concatenate([rng.integers(0, part.P, 3000), part.pair_off[:-1], part.pair_off[1:] - 1])
     got = to_np(out[torch.as_tensor(rows, device=DEV)])
-    assert normwise_err(got, _ref(z, w, rows)) <= TOL["bf16"]
+    assert normwise_err(got, _ref(z, w, rows), dtype="bf16") <= TOL["bf16"]
     nt.nt_device_status()
 
 
