@@ -1,8 +1,9 @@
 """Benchmark of the packed single->pair->single block and varlen attention.
 
 One step is one pass of the whole hot path:
-  * the block on the B=8 Pairformer-style batch (N_i ~ U[64, 256], C_s=384,
-    C_z=128, transition 128->512->128, bf16 I/O, fp32 accumulation):
+  * the block on the near-uniform B=16 batch (N_i ~ U[700, 768], P =
+    8,633,186 packed cells, C_s=384, C_z=128, transition 128->512->128, bf16
+    I/O, fp32 accumulation), the largest single-GPU block workload:
     partition build + row splits, pair broadcast, transition, reduce + g;
   * varlen attention on the packed stream of 65,536 tokens (segments
     ~ U[16, 512], 12 heads x 64, bf16, non-causal).
@@ -11,7 +12,14 @@ its device time per step); the attention's TFLOPS ride beside it in
 ``attn``.  L2 is flushed (a 512 MB write) before every timed step, outside
 the timed events.  The partition build ends with a host readback; a short
 device sleep after it (also outside the events) lets the host queue the
-remaining calls ahead of the device, so each call's interval is device time.  ``--impl reference`` times the CPU oracle instead.
+remaining calls ahead of the device, so each call's interval is device time.
+
+The same line carries, measured in the same run: per-call figures of every
+other block workload (``workloads``: the B=8 Pairformer batch, the
+lognormal B=16 batch, the four stacked blocks of the skewed batch), the
+packed-against-padded report (``packing``: cells, pair bytes, measured peak
+allocation, block time) and the varlen-attention padding sweep
+(``padsweep``).  ``--impl reference`` times the CPU oracle instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun every rank runs its own replica (weak scaling).
@@ -40,13 +48,16 @@ from variable_length_batching_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "packed pair cells/sec per block and varlen attn TFLOPS; % of HBM/tensor roofline"
 HOST_LEAD_CYCLES = 400_000     # ~0.2 ms of device sleep at 2 GHz, outside the timed intervals
-BLOCK_CFG = wl.PAIRFORMER_BF16
+BLOCK_CFG = wl.NEAR_UNIFORM_BF16          # the headline block workload
+SIDE_BLOCK_CFGS = (wl.PAIRFORMER_BF16, wl.LOGNORMAL_BF16, wl.STACKED4_BF16)
 ATTN_CFG = wl.VARLEN_ATTN_BF16
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
-# kernels of ours launched per step: partition scan, partition rows,
-# projection, broadcast, transition, reduce, g projection, attention
-LAUNCHES_PER_STEP = 8
+# kernels of ours launched per step: partition (scan and row splits in one
+# launch), u/v projection, broadcast, transition, reduce, g projection,
+# attention
+LAUNCHES_PER_STEP = 7
+SIDE_STEPS = 20                  # timed repetitions of each side report's calls
 
 
 def load_peaks():
@@ -58,15 +69,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_record(kernel: str):
-    """Per-launch DRAM bytes from a committed ncu capture, or None when the
-    kernel's source changed since the capture."""
+def traffic_record(kernel: str, workload: str):
+    """Per-launch DRAM bytes of ``kernel`` on ``workload`` from a committed ncu
+    capture, or None when there is none or the kernel's source changed
+    since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel)
-    if not rec:
+    if not rec or rec.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "variable_length_batching_gb300", "csrc", rec["source"])
     with open(src, "rb") as f:
@@ -82,12 +94,14 @@ def traffic_record(kernel: str):
 def block_work(T, P, C_s, C_z, H_t, es=2):
     return {
         "partition": {"bytes": 0, "flops": 0},
-        # writes P*C_z outputs; reads singles and weights; u, v (fp32) written once, read once
-        "broadcast": {"bytes": P * C_z * es + T * C_s * es + 2 * C_z * C_s * es + 2 * 2 * T * C_z * 4,
+        # the whole call (projection GEMM + broadcast): writes P*C_z outputs,
+        # reads the singles and the two projection weights
+        "broadcast": {"bytes": P * C_z * es + T * C_s * es + 2 * C_z * C_s * es,
                       "flops": 2 * 2 * T * C_s * C_z},
         # reads and writes every cell once; 2 GEMMs of C_z x H_t per cell
         "transition": {"bytes": 2 * P * C_z * es + 2 * H_t * C_z * es, "flops": 4 * C_z * H_t * P},
-        # reads every cell once; writes m, reads s_in, writes s_out
+        # the whole call (reduce + g projection): reads every cell once;
+        # writes m, reads s_in and W_g, writes s_out
         "reduce": {"bytes": P * C_z * es + T * C_z * es + 2 * T * C_s * es + C_s * C_z * es,
                    "flops": 2 * T * C_z * C_s},
     }
@@ -270,42 +284,39 @@ def _dev_weights(w, dev):
                            W1=g(w.W1), b1=g(w.b1), W2=g(w.W2), b2=g(w.b2), W_g=g(w.W_g), b_g=g(w.b_g))
 
 
-def run_gpu(args, rank, world, local_rank):
-    from variable_length_batching_gb300 import build, nt
-    build.build()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
+class BlockRun:
+    """Device inputs and buffers of one block workload: the partition is
+    built in every step; the pair state, the broadcast workspace and the
+    singles outputs are allocated once.  A stacked workload chains its
+    blocks through the singles, reusing one pair buffer."""
 
-    # ---- inputs, resident in HBM before the timed region ----
-    binp = wl.make_block_inputs(BLOCK_CFG)
-    w = _dev_weights(binp.blocks[0], dev)
-    lengths_d = torch.as_tensor(binp.lengths).to(dev)
-    s_d = binp.s.to(dev)
-    ainp = wl.make_attn_inputs(ATTN_CFG)
-    apart = nt.nt_partition_build(torch.as_tensor(ainp.seqlens).to(dev))   # cu_seqlens on the device
-    cu_d = apart.cu_seqlens
-    q_d, k_d, v_d = ainp.q.to(dev), ainp.k.to(dev), ainp.v.to(dev)
-    max_len = apart.max_len
-    o_d = torch.empty_like(q_d)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    def __init__(self, nt, cfg, dev, lengths=None):
+        self.nt, self.cfg = nt, cfg
+        self.inp = wl.make_block_inputs(cfg, lengths=lengths)
+        self.ws = [_dev_weights(b, dev) for b in self.inp.blocks]
+        self.lengths_d = torch.as_tensor(self.inp.lengths).to(dev)
+        self.s_d = self.inp.s.to(dev)
+        part = nt.nt_partition_build(self.lengths_d)
+        self.T, self.P = part.T, part.P
+        self.z = torch.empty(self.P, cfg.C_z, dtype=self.s_d.dtype, device=dev)
+        self.wsp = torch.empty(max(nt.nt_pair_broadcast_workspace_bytes(self.T, cfg.C_z), 16), dtype=torch.uint8,
+                               device=dev)
+        self.m = torch.empty(self.T, cfg.C_z, dtype=self.s_d.dtype, device=dev)
+        self.souts = [torch.empty_like(self.s_d) for _ in self.ws]
 
-    part = nt.nt_partition_build(lengths_d)
-    T, P = part.T, part.P
-    C_s, C_z, H_t = BLOCK_CFG.C_s, BLOCK_CFG.C_z, BLOCK_CFG.H_t
-    z_d = torch.empty(P, C_z, dtype=torch.bfloat16, device=dev)
-    ws_d = torch.empty(nt.nt_pair_broadcast_workspace_bytes(T, C_z), dtype=torch.uint8, device=dev)
-    m_d = torch.empty(T, C_z, dtype=torch.bfloat16, device=dev)
-    sout_d = torch.empty(T, C_s, dtype=torch.bfloat16, device=dev)
+    @property
+    def n_events(self):
+        return 3 + 3 * len(self.ws)
 
-    names = ("partition", "broadcast", "transition", "reduce", "attention")
-
-    def step(ev):
-        # ev[0..1] bracket the partition build (scan and row splits in one
-        # call, bounded by the singles' row count; it ends with the host
-        # reading the totals back); ev[2..6] bracket the four device-only calls.
+    def step(self, ev, stream, attn=None):
+        """One block step (and, with ``attn``, the attention call after it).
+        ev[0..1] bracket the partition build (scan and row splits in one call,
+        bounded by the singles' row count; it ends with the host reading the
+        totals back); then per block k, ev[2+3k..5+3k] bracket its
+        broadcast, transition and reduce; ev[-1] closes the attention call."""
+        nt = self.nt
         ev[0].record(stream)
-        p = nt.nt_partition_build(lengths_d, stream=stream, T=s_d.shape[0])
+        p = nt.nt_partition_build(self.lengths_d, stream=stream, T=self.s_d.shape[0])
         ev[1].record(stream)
         # The partition's readback left the stream idle.  A short device
         # sleep, outside every timed interval, lets the host enqueue the next
@@ -313,22 +324,99 @@ def run_gpu(args, rank, world, local_rank):
         # not host launch latency.
         torch.cuda._sleep(HOST_LEAD_CYCLES)
         ev[2].record(stream)
-        nt.nt_pair_broadcast(p, s_d, s_d, w.W_a, w.W_b, z=z_d, workspace=ws_d, stream=stream)
-        ev[3].record(stream)
-        nt.nt_pair_transition(p, z_d, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2, out=z_d,
-                              stream=stream)
-        ev[4].record(stream)
-        nt.nt_pair_reduce(p, z_d, w.W_g, w.b_g, s_in=s_d, m=m_d, s_out=sout_d, stream=stream)
-        ev[5].record(stream)
-        nt.nt_varlen_attn(q_d, k_d, v_d, cu_d, max_len, out=o_d, stream=stream)
-        ev[6].record(stream)
+        s_cur = self.s_d
+        for k, (w, so) in enumerate(zip(self.ws, self.souts)):
+            nt.nt_pair_broadcast(p, s_cur, s_cur, w.W_a, w.W_b, z=self.z, workspace=self.wsp, stream=stream)
+            ev[3 + 3 * k].record(stream)
+            nt.nt_pair_transition(p, self.z, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2, out=self.z,
+                                  stream=stream)
+            ev[4 + 3 * k].record(stream)
+            nt.nt_pair_reduce(p, self.z, w.W_g, w.b_g, s_in=s_cur, m=self.m, s_out=so, stream=stream)
+            ev[5 + 3 * k].record(stream)
+            s_cur = so
+        if attn is not None:
+            attn()
+            ev[-1].record(stream)
 
-    def new_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    def call_times(self, evs):
+        """Per-step ms of each call (summed over the stacked blocks)."""
+        nb = len(self.ws)
+        per = {"partition": [], "broadcast": [], "transition": [], "reduce": []}
+        for ev in evs:
+            per["partition"].append(ev[0].elapsed_time(ev[1]))
+            for name, off in (("broadcast", 0), ("transition", 1), ("reduce", 2)):
+                per[name].append(sum(ev[2 + 3 * k + off].elapsed_time(ev[3 + 3 * k + off]) for k in range(nb)))
+        return per
+
+
+def kstat(times_ms, w_bytes, w_flops, bound, peaks):
+    """Achieved figure of one call against its bound, from its per-step
+    times (mean; p10/p50/p90 beside it)."""
+    ms = float(np.mean(times_ms))
+    t = ms * 1e-3
+    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    spread = {"ms": ms, "ms_p10_p50_p90": [float(x) for x in np.percentile(times_ms, [10, 50, 90])]}
+    if bound == "tensor":
+        a = w_flops / t / 1e12
+        out = {"bound": "tensor", "achieved": a, "peak": tc, "unit": "TFLOP/s", "frac": a / tc}
+        # attainable roofline: min(tensor peak, arithmetic intensity x HBM bandwidth)
+        att = min(tc, w_flops / w_bytes * hbm / 1e3)
+        out.update({"attainable": att, "frac_attainable": a / att})
+    else:
+        a = w_bytes / t / 1e9
+        out = {"bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s", "frac": a / hbm}
+    out.update(spread)
+    return out
+
+
+def block_kernels(run, per, peaks):
+    """Per-call roofline figures of one block workload: broadcast and reduce
+    are whole calls (projection GEMM included), against HBM; the transition
+    against the bf16 tensor peak.  Work and times are summed over stacked
+    blocks."""
+    cfg, nb = run.cfg, len(run.ws)
+    es = 2 if cfg.dtype == wl.BF16 else 4
+    work = block_work(run.T, run.P, cfg.C_s, cfg.C_z, cfg.H_t, es)
+    return {
+        "broadcast": dict(kstat(per["broadcast"], nb * work["broadcast"]["bytes"], 0, "hbm", peaks),
+                          call="whole call: u/v projection GEMM + broadcast kernel"),
+        "transition": kstat(per["transition"], nb * work["transition"]["bytes"], nb * work["transition"]["flops"],
+                            "tensor", peaks),
+        "reduce": dict(kstat(per["reduce"], nb * work["reduce"]["bytes"], 0, "hbm", peaks),
+                       call="whole call: reduce kernel + g projection GEMM"),
+        "partition": {"ms": float(np.mean(per["partition"])), "note": "scan + row splits + one totals readback"},
+    }
+
+
+def run_gpu(args, rank, world, local_rank):
+    from variable_length_batching_gb300 import build, nt
+    build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+
+    # ---- inputs, resident in HBM before the timed region ----
+    run = BlockRun(nt, BLOCK_CFG, dev)
+    ainp = wl.make_attn_inputs(ATTN_CFG)
+    apart = nt.nt_partition_build(torch.as_tensor(ainp.seqlens).to(dev))   # cu_seqlens on the device
+    cu_d = apart.cu_seqlens
+    q_d, k_d, v_d = ainp.q.to(dev), ainp.k.to(dev), ainp.v.to(dev)
+    max_len = apart.max_len
+    o_d = torch.empty_like(q_d)
+    attn_ws = torch.empty(nt.nt_varlen_attn_workspace_bytes(), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    T, P = run.T, run.P
+    C_s, C_z, H_t = BLOCK_CFG.C_s, BLOCK_CFG.C_z, BLOCK_CFG.H_t
+
+    attn = lambda: nt.nt_varlen_attn(q_d, k_d, v_d, cu_d, max_len, out=o_d, stream=stream, workspace=attn_ws)
+
+    def new_events(n):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        step(new_events())
+        run.step(new_events(run.n_events + 1), stream, attn)
     nt.nt_device_status(stream)
 
     dist = None
@@ -341,8 +429,8 @@ def run_gpu(args, rank, world, local_rank):
         t0 = time.perf_counter()
         for _ in range(args.steps):
             flush.fill_(float(len(evs)))     # L2 flush, outside the step's events
-            ev = new_events()
-            step(ev)
+            ev = new_events(run.n_events + 1)
+            run.step(ev, stream, attn)
             evs.append(ev)
         torch.cuda.synchronize()
         t1 = time.perf_counter()
@@ -352,60 +440,45 @@ def run_gpu(args, rank, world, local_rank):
         dist.barrier()
     nt.nt_device_status(stream)
 
-    per = {n: [] for n in names}
-    spans = {"partition": (0, 1), "broadcast": (2, 3), "transition": (3, 4), "reduce": (4, 5),
-             "attention": (5, 6)}
-    for ev in evs:
-        for n in names:
-            a, b = spans[n]
-            per[n].append(ev[a].elapsed_time(ev[b]))
+    per = run.call_times(evs)
+    per["attention"] = [ev[-2].elapsed_time(ev[-1]) for ev in evs]
     ms = {n: float(np.mean(v)) for n, v in per.items()}
     block_ms = ms["partition"] + ms["broadcast"] + ms["transition"] + ms["reduce"]
     step_ms = block_ms + ms["attention"]
     block_ms_max, attn_ms_max, step_ms_max = max_over_ranks([block_ms, ms["attention"], step_ms], world, dev)
 
     # ---- end to end through the C ABI with host buffers ----
-    e2e = run_e2e(nt, binp, dev, stream, args)
+    e2e = run_e2e(nt, run.inp, dev, stream, args)
+
+    # ---- the other block workloads, packing and padding reports (same run) ----
+    side_steps = max(3, min(args.steps, SIDE_STEPS))
+    workloads = {BLOCK_CFG.name: None}
+    for cfg in SIDE_BLOCK_CFGS:
+        workloads[cfg.name] = measure_block(nt, cfg, dev, stream, flush, side_steps, args.warmup, peaks)
+    del run.z
+    torch.cuda.empty_cache()
+    packing = run_packing(nt, dev, stream, flush, side_steps)
+    padsweep = run_padsweep(nt, dev, stream, flush, side_steps, peaks)
 
     if rank != 0:
         return None
-    peaks, peak_src = load_peaks()
-    work = block_work(T, P, C_s, C_z, H_t)
     aw = attn_work(ainp.seqlens, ATTN_CFG.H, ATTN_CFG.d)
-    hbm, tc = peaks["hbm_gbs"], peaks["bf16_tflops"]
-
-    def kstat(name, w_bytes, w_flops, bound):
-        t = ms[name] * 1e-3
-        spread = {"ms": ms[name], "ms_p10_p50_p90": [float(x) for x in np.percentile(per[name], [10, 50, 90])]}
-        if bound == "tensor":
-            a = w_flops / t / 1e12
-            out = {"bound": "tensor", "achieved": a, "peak": tc, "unit": "TFLOP/s", "frac": a / tc}
-            # attainable roofline: min(tensor peak, arithmetic intensity x HBM bandwidth)
-            att = min(tc, w_flops / w_bytes * hbm / 1e3)
-            out.update({"attainable": att, "frac_attainable": a / att})
-            out.update(spread)
-            return out
-        a = w_bytes / t / 1e9
-        out = {"bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s", "frac": a / hbm}
-        out.update(spread)
-        return out
-
-    kernels = {
-        "broadcast": kstat("broadcast", work["broadcast"]["bytes"], 0, "hbm"),
-        "transition": kstat("transition", work["transition"]["bytes"], work["transition"]["flops"], "tensor"),
-        "reduce": kstat("reduce", work["reduce"]["bytes"], 0, "hbm"),
-        "attention": kstat("attention", aw["bytes"], aw["flops"], "tensor"),
-        "partition": {"ms": ms["partition"], "note": "scan + row splits + one totals readback"},
-    }
+    kernels = block_kernels(run, per, peaks)
+    kernels["attention"] = kstat(per["attention"], aw["bytes"], aw["flops"], "tensor", peaks)
+    workloads[BLOCK_CFG.name] = {"B": BLOCK_CFG.B, "T": T, "P": P, "blocks": 1, "block_ms": block_ms,
+                                 "cells_per_s": P / (block_ms * 1e-3), "steps": args.steps,
+                                 "kernels": {k: v for k, v in kernels.items() if k != "attention"},
+                                 "note": "the headline workload (the main timed steps)"}
     # the kernel with the largest share of the step's device time
     dom = max(("broadcast", "transition", "reduce", "attention"), key=lambda n: ms[n])
-    roof = {k: v for k, v in kernels[dom].items() if not k.startswith("ms")}
+    roof = {k: v for k, v in kernels[dom].items() if not k.startswith("ms") and k != "call"}
     roof["kernel"] = dom
+    roof["share_of_step"] = ms[dom] / step_ms
     roof["peak_source"] = f"{peak_src} ({'burst copy' if roof['bound'] == 'hbm' else 'cuBLAS bf16 burst'})"
-    tr = traffic_record(dom)
-    roof["traffic"] = tr
+    roof["traffic"] = traffic_record(dom, BLOCK_CFG.name if dom != "attention" else ATTN_CFG.name)
     cells_per_s = job_throughput(P, world, block_ms_max)
     attn_tflops = job_throughput(aw["flops"], world, attn_ms_max) / 1e12
+    nmax = int(run.inp.lengths.max())
     line = {
         "metric": METRIC,
         "value": cells_per_s,
@@ -420,7 +493,7 @@ def run_gpu(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded numpy draws of the pages' workload shapes; random-init weights)",
         "config": {"workload": f"block: {BLOCK_CFG.name} (T={T}, P={P} packed cells vs "
-                               f"{BLOCK_CFG.B * int(binp.lengths.max()) ** 2} padded); "
+                               f"{BLOCK_CFG.B * nmax ** 2} padded); "
                                f"attention: {ATTN_CFG.name} ({len(ainp.seqlens)} segments)",
                    "B": BLOCK_CFG.B, "T": T, "P": P, "C_s": C_s, "C_z": C_z, "H_t": H_t,
                    "attn_T": int(ainp.seqlens.sum()), "attn_segments": int(len(ainp.seqlens)),
@@ -432,12 +505,42 @@ def run_gpu(args, rank, world, local_rank):
                  "roofline": {k: v for k, v in kernels["attention"].items() if not k.startswith("ms")}},
         "kernels": kernels,
         "roofline": roof,
+        "workloads": workloads,
+        "packing": packing,
+        "padsweep": padsweep,
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
     return line
+
+
+def measure_block(nt, cfg, dev, stream, flush, steps, warmup, peaks):
+    """Per-call figures of one block workload: ``steps`` block steps with L2
+    flushed before each, per-call CUDA events."""
+    run = BlockRun(nt, cfg, dev)
+    for _ in range(max(3, warmup)):
+        flush.fill_(0.0)
+        run.step([torch.cuda.Event(enable_timing=True) for _ in range(run.n_events)], stream)
+    evs = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(run.n_events)]
+        run.step(ev, stream)
+        evs.append(ev)
+    torch.cuda.synchronize()
+    nt.nt_device_status(stream)
+    per = run.call_times(evs)
+    ms = {n: float(np.mean(v)) for n, v in per.items()}
+    block_ms = sum(ms.values())
+    nb = len(run.ws)
+    out = {"B": cfg.B, "T": run.T, "P": run.P, "blocks": nb, "block_ms": block_ms,
+           "cells_per_s": nb * run.P / (block_ms * 1e-3), "steps": steps,
+           "kernels": block_kernels(run, per, peaks)}
+    del run
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(nt, binp, dev, stream, args):
@@ -493,25 +596,43 @@ def run_e2e(nt, binp, dev, stream, args):
 # CPU oracle: the baseline beside the GPU number, and the reference arm
 # ----------------------------------------------------------------------------
 
+class OracleBlock:
+    """The oracle on the headline block workload, one sample at a time (its
+    own loop is per sample, so a sample is the natural bounded unit)."""
+
+    def __init__(self):
+        from oracle import block as oblock
+        self.ob = oblock
+        binp = wl.make_block_inputs(BLOCK_CFG)
+        w = binp.blocks[0]
+        f = wl.io_bits_to_f64
+        self.w = oblock.Weights(f(w.W_a), f(w.W_b), f(w.ln_gamma), f(w.ln_beta), 1e-5, f(w.W1), None, f(w.W2),
+                                None, f(w.W_g), None)
+        self.lengths = binp.lengths
+        self.cu = np.concatenate([[0], np.cumsum(binp.lengths.astype(np.int64))])
+        self.s = f(binp.s)
+
+    def sample(self, b):
+        """Runs sample b of the batch; returns its pair cells."""
+        n = int(self.lengths[b])
+        self.ob.block_packed(self.lengths[b:b + 1], self.s[self.cu[b]:self.cu[b] + n], self.w)
+        return n * n
+
+
 def oracle_block_sample(budget_s=12.0):
-    """The oracle on the same block workload, whole batches repeated until
-    ``budget_s`` of CPU time; returns cells/s."""
-    from oracle import block as oblock
-    binp = wl.make_block_inputs(BLOCK_CFG)
-    w = binp.blocks[0]
-    f = wl.io_bits_to_f64
-    ow = oblock.Weights(f(w.W_a), f(w.W_b), f(w.ln_gamma), f(w.ln_beta), 1e-5, f(w.W1), None, f(w.W2),
-                        None, f(w.W_g), None)
-    s = f(binp.s)
-    P = int((binp.lengths.astype(np.int64) ** 2).sum())
-    n, t0 = 0, time.perf_counter()
+    """The oracle on the headline block workload, whole samples in batch
+    order until ``budget_s`` of CPU time has passed; returns (cells/s, what
+    the sample was)."""
+    ob = OracleBlock()
+    cells, b, t0 = 0, 0, time.perf_counter()
     while True:
-        oblock.block_packed(binp.lengths, s, ow)
-        n += 1
+        cells += ob.sample(b % BLOCK_CFG.B)
+        b += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return n * P / dt, f"{n} full pass(es) of the block on the B=8 batch ({P} cells), {dt:.1f} s"
+    return cells / dt, (f"the first {b} of the {BLOCK_CFG.B} samples of the near-uniform batch "
+                        f"({cells} pair cells, every step of the block per sample), {dt:.1f} s")
 
 
 def oracle_attn_sample(budget_s=8.0):
@@ -531,24 +652,33 @@ def oracle_attn_sample(budget_s=8.0):
 
 
 def cpu_cores():
-    return int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    return os.cpu_count() or 1
+
+
+def cpu_threads():
+    """Thread counts in effect for the oracle's numpy/BLAS calls: bench.py
+    sets both variables to the core count before numpy loads, unless the
+    caller set them."""
+    return {"OPENBLAS_NUM_THREADS": int(os.environ.get("OPENBLAS_NUM_THREADS", "1")),
+            "OMP_NUM_THREADS": int(os.environ.get("OMP_NUM_THREADS", "1"))}
 
 
 def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on the headline workload: each
+    step runs one whole sample of the near-uniform batch (samples in batch
+    order, about 1.5 s each on 16 cores); value = pair cells per second."""
     if rank != 0:
         return None
-    vals = []
-    samples = []
-    for _ in range(args.warmup):
-        oracle_block_sample(budget_s=0.0)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        v, smp = oracle_block_sample(budget_s=4.0)
-        vals.append(v)
-        samples.append(smp)
+    ob = OracleBlock()
+    for i in range(min(args.warmup, 1)):
+        ob.sample(i)
+    cells, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        cells += ob.sample(i % BLOCK_CFG.B)
     wall = time.perf_counter() - t0
-    value = float(np.mean(vals))
-    P = int((wl.make_block_inputs(BLOCK_CFG).lengths.astype(np.int64) ** 2).sum())
+    value = cells / wall
+    sample = (f"{args.steps} steps, one whole sample of the near-uniform batch per step ({cells} pair cells), "
+              f"{wall:.1f} s")
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -557,15 +687,16 @@ def run_reference(args, rank, world):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": 1e3 * P / value,
+        "ms_per_step": 1e3 * wall / max(args.steps, 1),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded numpy draws of the pages' workload shapes; random-init weights)",
-        "config": {"workload": f"block: {BLOCK_CFG.name} (CPU oracle, float64)", "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": "pair cells/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": samples[-1] if samples else ""},
+        "config": {"workload": f"block: {BLOCK_CFG.name} (CPU oracle, float64, one sample per step)",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "pair cells/s", "cores": cpu_cores(), "threads": cpu_threads(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "pair cells/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": wall,
     }
@@ -590,25 +721,20 @@ def _timed(fn, flush, reps, stream):
     return [float(x) for x in np.percentile(v, [50, 10, 90])]
 
 
-def run_packing(args):
+def run_packing(nt, dev, stream, flush, steps):
     """Packed against padded pair state for every block workload: cells and
     bytes of the pair tensor, measured peak device allocation of one block
     (all four chained blocks for the stacked workload, with the pair buffer
     reused and with every block's pair output retained), and block time.  The
     padded rows run the same kernels on every sample padded to N_max, the
-    cost a padded layout pays.  One JSON line per workload."""
-    from variable_length_batching_gb300 import build, nt
-    build.build()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    cost a padded layout pays.  Returns one record per workload."""
+    out = []
     for name in ("tiny", "pairformer", "lognormal", "near_uniform", "stacked4"):
         cfg = WORKLOADS[name]
         base = wl.make_block_inputs(cfg)
         nmax = int(base.lengths.max())
         es = 2 if cfg.dtype == wl.BF16 else 4
-        line = {"report": "packing", "workload": cfg.name, "B": cfg.B, "C_z": cfg.C_z, "blocks": cfg.n_blocks,
+        line = {"workload": cfg.name, "B": cfg.B, "C_z": cfg.C_z, "blocks": cfg.n_blocks,
                 "lengths": [int(x) for x in base.lengths]}
         for layout, lens in (("packed", base.lengths), ("padded", np.full(cfg.B, nmax, dtype=np.int32))):
             inp = wl.make_block_inputs(cfg, lengths=lens)
@@ -648,52 +774,72 @@ def run_packing(args):
                     s_cur = so
             for _ in range(3):
                 chain()
-            med, p10, p90 = _timed(chain, flush, args.steps, stream)
+            med, p10, p90 = _timed(chain, flush, steps, stream)
             line[layout] = {"cells": int(part.P), "pair_bytes": int(part.P) * cfg.C_z * es,
                             "peak_alloc_bytes": res, "ms": med, "ms_p10_p90": [p10, p90],
                             "cells_per_s": part.P * cfg.n_blocks / (med * 1e-3)}
-            del z, wsp, sos, m, part
+            del z, wsp, sos, m, part, ws, s0
             torch.cuda.empty_cache()
         line["pair_bytes_ratio"] = line["padded"]["pair_bytes"] / line["packed"]["pair_bytes"]
+        line["peak_alloc_ratio"] = line["padded"]["peak_alloc_bytes"]["reuse"] / line["packed"]["peak_alloc_bytes"]["reuse"]
         line["speedup_packed_over_padded"] = line["padded"]["ms"] / line["packed"]["ms"]
-        print(json.dumps(line), flush=True)
+        out.append(line)
+    nt.nt_device_status(stream)
+    return out
 
 
-def run_padsweep(args):
+def _device_qkv(T, H, d, seed, dev):
+    """N(0, 1) q, k, v of T tokens drawn on the device from a seeded
+    generator (timing inputs of the padding sweep, where the host draw of
+    the padded layouts would take longer than the measurement)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    return [torch.randn(T, H, d, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            for _ in range(3)]
+
+
+def run_padsweep(nt, dev, stream, flush, steps, peaks):
     """Varlen attention over the packed stream against the same kernel on the
     same number of segments padded to 512 tokens, at equivalent padding rates
-    from 3% to 90% (65,536 real tokens, 12 heads x 64).  One JSON line per rate."""
+    from 3% to 90% (65,536 real tokens, 12 heads x 64).  Returns one record
+    per rate."""
+    out = []
+    ws = torch.empty(nt.nt_varlen_attn_workspace_bytes(), dtype=torch.uint8, device=dev)
+    for rate in wl.PADDING_SWEEP:
+        lo, hi = wl.sweep_length_range(rate)
+        rng = np.random.default_rng(0)
+        lens = wl.draw_segments(ATTN_CFG.total_tokens, lo, hi, rng)
+        line = {"target_rate": rate, "len_range": [lo, hi], "segments": int(len(lens)), "pad_to": wl.PAD_TO,
+                "equivalent_pad_rate": 1.0 - float(lens.sum()) / (len(lens) * wl.PAD_TO)}
+        w = attn_work(lens, ATTN_CFG.H, ATTN_CFG.d)
+        for layout, L in (("varlen", lens), ("padded", np.full(len(lens), wl.PAD_TO, dtype=np.int32))):
+            part = nt.nt_partition_build(torch.as_tensor(L).to(dev))
+            q, k, v = _device_qkv(int(L.sum()), ATTN_CFG.H, ATTN_CFG.d, 0, dev)
+            o = torch.empty_like(q)
+            fn = lambda: nt.nt_varlen_attn(q, k, v, part.cu_seqlens, part.max_len, out=o, stream=stream,
+                                           workspace=ws)
+            for _ in range(3):
+                fn()
+            med, p10, p90 = _timed(fn, flush, steps, stream)
+            line[layout] = {"tokens": int(L.sum()), "ms": med, "ms_p10_p90": [p10, p90],
+                            "useful_tflops": w["flops"] / (med * 1e-3) / 1e12}
+            del q, k, v, o, part
+            torch.cuda.empty_cache()
+        line["measured_savings"] = 1.0 - line["varlen"]["ms"] / line["padded"]["ms"]
+        line["varlen_frac_of_peak"] = line["varlen"]["useful_tflops"] / peaks["bf16_tflops"]
+        out.append(line)
+    nt.nt_device_status(stream)
+    return out
+
+
+def _report_setup():
     from variable_length_batching_gb300 import build, nt
     build.build()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    peaks, _ = load_peaks()
-    for rate in (0.03, 0.10, 0.25, 0.48, 0.75, 0.90):
-        lo, hi = wl.sweep_length_range(rate)
-        rng = np.random.default_rng(0)
-        lens = wl.draw_segments(ATTN_CFG.total_tokens, lo, hi, rng)
-        line = {"report": "padsweep", "target_rate": rate, "len_range": [lo, hi], "segments": int(len(lens)),
-                "pad_to": wl.PAD_TO,
-                "equivalent_pad_rate": 1.0 - float(lens.sum()) / (len(lens) * wl.PAD_TO)}
-        w = attn_work(lens, ATTN_CFG.H, ATTN_CFG.d)
-        for layout, L in (("varlen", lens), ("padded", np.full(len(lens), wl.PAD_TO, dtype=np.int32))):
-            a = wl.make_attn_inputs(ATTN_CFG, seqlens=L)
-            part = nt.nt_partition_build(torch.as_tensor(a.seqlens).to(dev))
-            q, k, v = a.q.to(dev), a.k.to(dev), a.v.to(dev)
-            o = torch.empty_like(q)
-            fn = lambda: nt.nt_varlen_attn(q, k, v, part.cu_seqlens, part.max_len, out=o, stream=stream)
-            for _ in range(3):
-                fn()
-            med, p10, p90 = _timed(fn, flush, args.steps, stream)
-            line[layout] = {"tokens": int(L.sum()), "ms": med, "ms_p10_p90": [p10, p90],
-                            "useful_tflops": w["flops"] / (med * 1e-3) / 1e12}
-            del q, k, v, o, a, part
-            torch.cuda.empty_cache()
-        line["measured_savings"] = 1.0 - line["varlen"]["ms"] / line["padded"]["ms"]
-        line["varlen_frac_of_peak"] = line["varlen"]["useful_tflops"] / peaks["bf16_tflops"]
-        print(json.dumps(line), flush=True)
+    return nt, dev, stream, flush
 
 
 def run_rect(args):
@@ -761,10 +907,11 @@ def run_only(args):
         cu, ml = apart.cu_seqlens, apart.max_len
         q, k, v = a.q.to(dev), a.k.to(dev), a.v.to(dev)
         o = torch.empty_like(q)
+        aws = torch.empty(nt.nt_varlen_attn_workspace_bytes(), dtype=torch.uint8, device=dev)
         if args.causal:
-            fn = lambda: nt.nt_varlen_attn_qk(q, k, v, cu, cu, ml, causal=True, out=o, stream=stream)
+            fn = lambda: nt.nt_varlen_attn_qk(q, k, v, cu, cu, ml, causal=True, out=o, stream=stream, workspace=aws)
         else:
-            fn = lambda: nt.nt_varlen_attn(q, k, v, cu, ml, out=o, stream=stream)
+            fn = lambda: nt.nt_varlen_attn(q, k, v, cu, ml, out=o, stream=stream, workspace=aws)
         w = attn_work(a.seqlens, cfg.H, cfg.d, causal=args.causal)
         bound, name = "tensor", cfg.name + ("_causal" if args.causal else "")
         if args.backward:
@@ -866,10 +1013,14 @@ def main():
     ap.add_argument("--backward", action="store_true", help="with --only attention: the backward (dq, dk, dv)")
     args = ap.parse_args()
     if args.only == "packing":
-        run_packing(args)
+        nt, dev, stream, flush = _report_setup()
+        for line in run_packing(nt, dev, stream, flush, args.steps):
+            print(json.dumps(dict(report="packing", **line)), flush=True)
         return
     if args.only == "padsweep":
-        run_padsweep(args)
+        nt, dev, stream, flush = _report_setup()
+        for line in run_padsweep(nt, dev, stream, flush, args.steps, load_peaks()[0]):
+            print(json.dumps(dict(report="padsweep", **line)), flush=True)
         return
     if args.only == "rect":
         run_rect(args)
@@ -898,8 +1049,9 @@ def main():
         if not args.no_cpu_baseline:
             v, smp = oracle_block_sample()
             av, asmp = oracle_attn_sample()
-            line["cpu_baseline"] = {"value": v, "unit": "pair cells/s", "cores": cpu_cores(), "kind": "oracle",
-                                    "sample": smp, "attn_tflops": av, "attn_sample": asmp}
+            line["cpu_baseline"] = {"value": v, "unit": "pair cells/s", "cores": cpu_cores(),
+                                    "threads": cpu_threads(), "kind": "oracle", "sample": smp,
+                                    "attn_tflops": av, "attn_sample": asmp}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
