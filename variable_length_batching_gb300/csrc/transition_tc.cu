@@ -73,10 +73,11 @@ constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffW = kOffA + 2 * kABytes;
 constexpr uint32_t kOffLN = kOffW + kStages * kWBytes;    // gamma, beta: 1 KB
 constexpr uint32_t kOffBar = kOffLN + 2 * kCz * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;     // + barriers + alignment slack
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;     // + barriers + alignment slack
 
 struct Bars {
   uint64_t z_full[2], a_full[2], a_empty[2];       // per input slot
+  uint64_t g1_done[2], z2_full[2];                 // per input slot: last GEMM1s done, residual z reloaded
   uint64_t w_full[kStages], w_empty[kStages];
   uint64_t acc1_full[2], g2_done[2];               // per sub-tile
   uint64_t h_full[2][2];                           // per sub-tile, per half of the hidden chunk
@@ -87,7 +88,7 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // Inputs of the fused block: u, v (fp32, C_z wide), the partition's row
 // splits and owners, the column offsets, and the fp32 accumulator of row sums.
@@ -180,7 +181,12 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.z_full[i], 1);
       mbar_init(&bar.a_full[i], 128);
-      mbar_init(&bar.a_empty[i], 3);           // the tile's last GEMM1s + both sub-tiles' output stores
+      // fused: the tile's last GEMM1s + both sub-tiles' output stores; otherwise
+      // both output stores (the last GEMM1s release the slot for the residual
+      // reload through g1_done, before the output)
+      mbar_init(&bar.a_empty[i], kFused ? 3 : 2);
+      mbar_init(&bar.g1_done[i], 1);
+      mbar_init(&bar.z2_full[i], 1);
     }
     for (int i = 0; i < kStages; ++i) { mbar_init(&bar.w_full[i], 1); mbar_init(&bar.w_empty[i], 1); }
     for (int s = 0; s < 2; ++s) {
@@ -213,20 +219,37 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       if (kGLU) prefetch_tmap(&tm_w3);
       int load_idx = 0;
       int last_j[2] = {-1, -1};                  // the last tile whose z each slot received
+      int last_r[2] = {-1, -1};                  // the last tile whose residual each slot received
+      // z of `tile` into slot (j & 1), completing on `bar_`
+      auto load_z = [&](int64_t ztile, int zj, uint64_t* bar_) {
+        uint8_t* a = sA + (zj & 1) * kABytes;
+        mbar_arrive_expect_tx(bar_, kABytes);
+        const int row0 = (int)(ztile * kTileRows);
+        for (int s = 0; s < 2; ++s)
+          for (int kb = 0; kb < 2; ++kb)
+            tma_load_2d(a + s * kSubBytes + kb * kBlockBytes, &tm_zin, bar_, kb * 64, row0 + s * kSubRows);
+      };
+      // The residual z of tile zj comes back into its slot once the tile's
+      // last GEMM1s have completed (they were the slot's last readers; GEMM2
+      // takes its A operand from TMEM), so the output epilogue reads it from
+      // shared memory.
+      auto reload = [&](int64_t ztile, int zj) -> bool {
+        if (!mbar_wait(&bar.g1_done[zj & 1], (zj >> 1) & 1, abort_flag, status)) return false;
+        load_z(ztile, zj, &bar.z2_full[zj & 1]);
+        last_r[zj & 1] = zj;
+        return true;
+      };
       bool ok = true;
       int j = 0;
+      int64_t prev_tile = -1;
       for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
         const int slot = j & 1;
         if (!kFused) {   // the fused block builds its z tile in the LayerNorm warps
           if (!(ok = mbar_wait(&bar.a_empty[slot], ((j >> 1) & 1) ^ 1, abort_flag, status))) break;
-          uint8_t* a = sA + slot * kABytes;
-          mbar_arrive_expect_tx(&bar.z_full[slot], kABytes);
-          const int row0 = (int)(tile * kTileRows);
-          for (int s = 0; s < 2; ++s)
-            for (int kb = 0; kb < 2; ++kb)
-              tma_load_2d(a + s * kSubBytes + kb * kBlockBytes, &tm_zin, &bar.z_full[slot], kb * 64,
-                          row0 + s * kSubRows);
+          load_z(tile, j, &bar.z_full[slot]);
           last_j[slot] = j;
+          if (prev_tile >= 0 && !(ok = reload(prev_tile, j - 1))) break;
+          prev_tile = tile;
         }
         // weights in consumption order: W1(c), W2(c), W1(c + 1), ...
         for (int q = 0; q < 2 * NC; ++q) {
@@ -261,9 +284,12 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           ++load_idx;
         }
       }
+      if (ok && prev_tile >= 0) reload(prev_tile, j - 1);
       // drain: every copy this thread issued has landed before the CTA exits
-      for (int sl = 0; sl < 2; ++sl)
+      for (int sl = 0; sl < 2; ++sl) {
         if (last_j[sl] >= 0) mbar_wait(&bar.z_full[sl], (last_j[sl] >> 1) & 1, nullptr, status);
+        if (last_r[sl] >= 0) mbar_wait(&bar.z2_full[sl], (last_r[sl] >> 1) & 1, nullptr, status);
+      }
       for (int l = load_idx - kStages; l < load_idx; ++l)
         if (l >= 0) mbar_wait(&bar.w_full[l % kStages], (l / kStages) & 1, nullptr, status);
     }
@@ -311,7 +337,8 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           }
           if (!ok) break;
           release_w();
-          if (c == NC - 1) mma_commit(&bar.a_empty[slot]);   // the slot's last reads by the tensor core
+          if (c == NC - 1)   // the slot's last reads by the tensor core
+            mma_commit(kFused ? &bar.a_empty[slot] : &bar.g1_done[slot]);
           if (!(ok = take_w(&wsm))) break;
           const int it = j * NC + c;
           for (int s = 0; s < 2; ++s) {
@@ -360,22 +387,21 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         if (!mbar_wait_warp(&bar.acc2_full[so], oj & 1, abort_flag, status)) return false;
         tc_fence_after();
         __syncwarp();
+        // the residual z is back in the slot (rows past P read as zeros); each
+        // thread overwrites its own row's 16-byte chunks with the output
         uint8_t* hs = sA + oslot * kABytes + so * kSubBytes;
-        const int64_t row_g = otile * kTileRows + so * kSubRows + r_out;
-        const bool in_range = row_g < P;
-        const bf16* zr = z_in + row_g * kCz;
+        if (so == 0 && !mbar_wait_warp(&bar.z2_full[oslot], (oj >> 1) & 1, abort_flag, status)) return false;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          float v[32];
-          tmem_ld32(tmem + lane_out + 256 + 128 * so + 32 * g, v);
-          tmem_ld_wait();
+          // the group's residual first, so its shared-memory loads overlap the TMEM load
           uint32_t rw[16];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            uint4 q4 = make_uint4(0, 0, 0, 0);
-            if (in_range) q4 = *reinterpret_cast<const uint4*>(zr + 32 * g + 8 * u);
+            const uint4 q4 = *reinterpret_cast<const uint4*>(hs + swz128_offset(r_out, 32 * g + 8 * u, kSubRows));
             rw[4 * u] = q4.x; rw[4 * u + 1] = q4.y; rw[4 * u + 2] = q4.z; rw[4 * u + 3] = q4.w;
           }
+          float v[32];
+          tmem_ld32_sync(tmem + lane_out + 256 + 128 * so + 32 * g, v);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint32_t o[4];
@@ -443,52 +469,62 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       } else if (!mbar_wait(&bar.z_full[slot], (j >> 1) & 1, abort_flag, status)) {
         break;
       }
-#pragma unroll 1
-      for (int s = 0; s < 2; ++s) {
-        uint8_t* base = a + s * kSubBytes;
-        // statistics in one pass over the row, shifted by its first element
-        // so that E[d^2] - E[d]^2 does not cancel when |mean| >> std
-        const float shift = bf16lo(*reinterpret_cast<const uint32_t*>(base + swz128_offset(t, 0, kSubRows)));
-        // packed fp32 pairs: even and odd features accumulate side by side
-        float s1a = 0.f, s1b = 0.f, s2a = 0.f, s2b = 0.f;
+      {
+        // this thread's two rows (row t of each sub-tile) side by side: two
+        // independent chains, and one gamma / beta load serves both
+        uint8_t* base[2] = {a, a + kSubBytes};
+        float shift[2], mean[2], rstd[2];
+        float s1a[2] = {0.f, 0.f}, s1b[2] = {0.f, 0.f}, s2a[2] = {0.f, 0.f}, s2b[2] = {0.f, 0.f};
 #pragma unroll
-        for (int ci = 0; ci < 16; ++ci) {
-          const uint4 v = *reinterpret_cast<const uint4*>(base + swz128_offset(t, ci * 8, kSubRows));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float d0, d1;
-            fadd2(bf16lo(w[e]), bf16hi(w[e]), -shift, -shift, d0, d1);
-            fadd2(s1a, s1b, d0, d1, s1a, s1b);
-            ffma2(d0, d1, d0, d1, s2a, s2b, s2a, s2b);
-          }
-        }
-        const float s1 = s1a + s1b, s2 = s2a + s2b;
-        const float m1 = s1 * (1.0f / kCz);
-        const float mean = shift + m1;
-        const float var = fmaxf(s2 * (1.0f / kCz) - m1 * m1, 0.f);
-        const float rstd = rsqrtf(var + eps);
+        for (int s = 0; s < 2; ++s)
+          shift[s] = bf16lo(*reinterpret_cast<const uint32_t*>(base[s] + swz128_offset(t, 0, kSubRows)));
 #pragma unroll 4
         for (int ci = 0; ci < 16; ++ci) {
-          uint8_t* p = base + swz128_offset(t, ci * 8, kSubRows);
-          const uint4 v = *reinterpret_cast<const uint4*>(p);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const uint4 v = *reinterpret_cast<const uint4*>(base[s] + swz128_offset(t, ci * 8, kSubRows));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float d0, d1;
+              fadd2(bf16lo(w[e]), bf16hi(w[e]), -shift[s], -shift[s], d0, d1);
+              fadd2(s1a[s], s1b[s], d0, d1, s1a[s], s1b[s]);
+              ffma2(d0, d1, d0, d1, s2a[s], s2b[s], s2a[s], s2b[s]);
+            }
+          }
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const float s1 = s1a[s] + s1b[s], s2 = s2a[s] + s2b[s];
+          const float m1 = s1 * (1.0f / kCz);
+          mean[s] = shift[s] + m1;
+          const float var = fmaxf(s2 * (1.0f / kCz) - m1 * m1, 0.f);
+          rstd[s] = rsqrtf(var + eps);
+        }
+#pragma unroll 2
+        for (int ci = 0; ci < 16; ++ci) {
           const float4 g0 = *reinterpret_cast<const float4*>(sGamma + ci * 8);
           const float4 g1 = *reinterpret_cast<const float4*>(sGamma + ci * 8 + 4);
           const float4 be0 = *reinterpret_cast<const float4*>(sBeta + ci * 8);
           const float4 be1 = *reinterpret_cast<const float4*>(sBeta + ci * 8 + 4);
           const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
           const float bt[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
-          uint32_t o[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {     // ((x - mean) * rstd) * gamma + beta, packed pairs
-            float y0, y1;
-            fadd2(bf16lo(w[e]), bf16hi(w[e]), -mean, -mean, y0, y1);
-            fmul2(y0, y1, rstd, rstd, y0, y1);
-            ffma2(y0, y1, gg[2 * e], gg[2 * e + 1], bt[2 * e], bt[2 * e + 1], y0, y1);
-            o[e] = pack_bf16x2(y0, y1);
+          for (int s = 0; s < 2; ++s) {
+            uint8_t* p = base[s] + swz128_offset(t, ci * 8, kSubRows);
+            const uint4 v = *reinterpret_cast<const uint4*>(p);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {   // ((x - mean) * rstd) * gamma + beta, packed pairs
+              float y0, y1;
+              fadd2(bf16lo(w[e]), bf16hi(w[e]), -mean[s], -mean[s], y0, y1);
+              fmul2(y0, y1, rstd[s], rstd[s], y0, y1);
+              ffma2(y0, y1, gg[2 * e], gg[2 * e + 1], bt[2 * e], bt[2 * e + 1], y0, y1);
+              o[e] = pack_bf16x2(y0, y1);
+            }
+            *reinterpret_cast<uint4*>(p) = make_uint4(o[0], o[1], o[2], o[3]);
           }
-          *reinterpret_cast<uint4*>(p) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
       fence_async_shared();
