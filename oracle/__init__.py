@@ -15,6 +15,9 @@ time, written to be checked against the pages by eye:
 * ``block``      -- Eq. 1 of the same paper (section 3), per sample, densely;
   plus a padded-then-gathered route that reaches the same cells through a
   B x N_max x N_max envelope.
+* ``block_backward`` -- the sample-weighted squared loss of the same
+  paper's Appendix A.1, Eq. 5, on the block's two outputs, and the block's
+  gradients (the chain rule of Eq. 1), per sample, densely.
 * ``attention``  -- softmax attention restricted to each cu_seqlens segment
   ("Variable-length attention and data packing", sections "What it is" and
   "How it works"), and the full T x T block-diagonal masked form of that

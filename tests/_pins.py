@@ -501,3 +501,131 @@ def pin_attention_backward_autograd(varlen_attention_backward, rng):
                 assert np.allclose(dq[ql:qh], tq.grad.numpy().transpose(1, 0, 2), rtol=1e-10, atol=1e-10)
                 assert np.allclose(dk[kl:kh], tk.grad.numpy().transpose(1, 0, 2), rtol=1e-10, atol=1e-10)
                 assert np.allclose(dv[kl:kh], tv.grad.numpy().transpose(1, 0, 2), rtol=1e-10, atol=1e-10)
+
+
+# ----------------------------------------------------------------------------
+# Eq. 5 loss and the block's gradients ("DanLing NestedTensor" Appendix A.1,
+# Eq. 5; the chain rule of Eq. 1)
+# ----------------------------------------------------------------------------
+
+def pin_eq5_weights(eq5_sample_weights):
+    """alpha_i = 1 + i/B and beta_i = 1.5 - i/(2B), evaluated by hand for B = 4."""
+    a, b = eq5_sample_weights(4)
+    assert np.allclose(a, [1.0, 1.25, 1.5, 1.75], rtol=0, atol=1e-15)
+    assert np.allclose(b, [1.5, 1.375, 1.25, 1.125], rtol=0, atol=1e-15)
+
+
+def pin_eq5_closed_form(eq5_loss):
+    """All-ones outputs: L = sum_i alpha_i N_i / T + sum_i beta_i N_i^2 / P
+    (C and C_p cancel); doubling both outputs multiplies L by four; an
+    output of zeros contributes nothing."""
+    lengths = [3, 0, 2, 5]
+    T, P = 10, 9 + 4 + 25
+    a = [1.0, 1.25, 1.5, 1.75]
+    b = [1.5, 1.375, 1.25, 1.125]
+    s_out = np.ones((T, 6))
+    z = np.ones((P, 4))
+    want = (a[0] * 3 + a[2] * 2 + a[3] * 5) / T + (b[0] * 9 + b[2] * 4 + b[3] * 25) / P
+    assert abs(eq5_loss(lengths, s_out, z) - want) < 1e-12
+    assert abs(eq5_loss(lengths, 2 * s_out, 2 * z) - 4 * want) < 1e-12
+    assert abs(eq5_loss(lengths, 0 * s_out, z) - (b[0] * 9 + b[2] * 4 + b[3] * 25) / P) < 1e-12
+
+
+def _torch_block_eq5(lengths, s, W, with_bias):
+    """Eq. 1 per sample and Eq. 5 in torch float64 (F.linear, F.layer_norm,
+    relu, mean over the column axis), for autograd."""
+    B = len(lengths)
+    C, C_p = s.shape[1], W["W_a"].shape[0]
+    T = sum(lengths)
+    P = sum(n * n for n in lengths)
+    lx = s.new_zeros(())
+    lp = s.new_zeros(())
+    off = 0
+    for i, n in enumerate(lengths):
+        if n == 0:
+            continue
+        X = s[off:off + n]
+        off += n
+        pair = F.linear(X, W["W_a"])[:, None, :] + F.linear(X, W["W_b"])[None, :, :]
+        y = F.layer_norm(pair, (C_p,), W["gamma"], W["beta"], eps=1e-5)
+        upd = F.linear(torch.relu(F.linear(y, W["W1"], W["b1"] if with_bias else None)), W["W2"],
+                       W["b2"] if with_bias else None)
+        pt = pair + upd
+        xt = X + F.linear(pt.mean(dim=1), W["W_g"], W["b_g"] if with_bias else None)
+        lx = lx + (1 + i / B) * (xt ** 2).sum()
+        lp = lp + (1.5 - i / (2 * B)) * (pt ** 2).sum()
+    return lx / (C * T) + lp / (C_p * P)
+
+
+def _block_problem(rng, lengths, C=6, C_p=4, H=8, with_bias=True):
+    from oracle.block import Weights
+    T = sum(lengths)
+    s = rng.standard_normal((T, C))
+    W = {"W_a": rng.standard_normal((C_p, C)) / np.sqrt(C), "W_b": rng.standard_normal((C_p, C)) / np.sqrt(C),
+         "gamma": 1 + 0.3 * rng.standard_normal(C_p), "beta": 0.2 * rng.standard_normal(C_p),
+         "W1": rng.standard_normal((H, C_p)) / 2, "b1": 0.3 * rng.standard_normal(H),
+         "W2": rng.standard_normal((C_p, H)) / 3, "b2": 0.2 * rng.standard_normal(C_p),
+         "W_g": rng.standard_normal((C, C_p)) / 2, "b_g": 0.1 * rng.standard_normal(C)}
+    if not with_bias:
+        W["b1"] = W["b2"] = W["b_g"] = None
+    w = Weights(W["W_a"], W["W_b"], W["gamma"], W["beta"], 1e-5, W["W1"], W["b1"], W["W2"], W["b2"], W["W_g"],
+                W["b_g"])
+    return s, W, w
+
+
+def pin_block_backward_autograd(block_loss_and_grads, block_packed, rng):
+    """The loss and every gradient equal torch autograd of an independent
+    torch formulation of Eq. 1 + Eq. 5 in float64 (zero-length samples
+    included, with and without biases)."""
+    for lengths, with_bias in (([3, 0, 4, 1], True), ([5, 2], False)):
+        s, W, w = _block_problem(rng, lengths, with_bias=with_bias)
+        fwd = block_packed(lengths, s, w)
+        loss, g = block_loss_and_grads(lengths, s, w, fwd.z_tilde, fwd.s_out)
+        ts = torch.tensor(s, requires_grad=True)
+        tW = {k: (None if v is None else torch.tensor(v, requires_grad=True)) for k, v in W.items()}
+        tl = _torch_block_eq5(lengths, ts, tW, with_bias)
+        tl.backward()
+        tlf = float(tl.detach())
+        assert abs(loss - tlf) < 1e-12 * max(1.0, abs(tlf))
+        pairs = [("ds", ts), ("dW_a", tW["W_a"]), ("dW_b", tW["W_b"]), ("dgamma", tW["gamma"]),
+                 ("dbeta", tW["beta"]), ("dW1", tW["W1"]), ("dW2", tW["W2"]), ("dW_g", tW["W_g"])]
+        if with_bias:
+            pairs += [("db1", tW["b1"]), ("db2", tW["b2"]), ("db_g", tW["b_g"])]
+        for name, t in pairs:
+            got = getattr(g, name)
+            assert got.shape == tuple(t.grad.shape), name
+            assert np.allclose(got, t.grad.numpy(), rtol=1e-9, atol=1e-12), name
+
+
+def pin_block_backward_finite_differences(block_loss_and_grads, block_packed, rng):
+    """Central differences of the loss (through the oracle's own forward)
+    match the gradient on a few coordinates of the singles and weights."""
+    from oracle.block_backward import eq5_loss
+    lengths = [2, 3]
+    s, W, w = _block_problem(rng, lengths)
+    fwd = block_packed(lengths, s, w)
+    _, g = block_loss_and_grads(lengths, s, w, fwd.z_tilde, fwd.s_out)
+
+    def loss_at(s_, w_):
+        f = block_packed(lengths, s_, w_)
+        return eq5_loss(lengths, f.s_out, f.z_tilde)
+
+    h = 1e-6
+    for name, idx in (("ds", (1, 2)), ("dW1", (3, 1)), ("dW_a", (2, 4)), ("dgamma", (1,)), ("dW_g", (0, 3)),
+                      ("db2", (2,))):
+        if name == "ds":
+            sp, sm = s.copy(), s.copy()
+            sp[idx] += h
+            sm[idx] -= h
+            fd = (loss_at(sp, w) - loss_at(sm, w)) / (2 * h)
+        else:
+            attr = {"dW1": "W1", "dW_a": "W_a", "dgamma": "gamma", "dW_g": "W_g", "db2": "b2"}[name]
+            arr = getattr(w, attr)
+            old = arr[idx]
+            arr[idx] = old + h
+            lp_ = loss_at(s, w)
+            arr[idx] = old - h
+            lm_ = loss_at(s, w)
+            arr[idx] = old
+            fd = (lp_ - lm_) / (2 * h)
+        assert abs(fd - getattr(g, name)[idx]) < 1e-6 * max(1.0, abs(fd)), name

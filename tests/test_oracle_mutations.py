@@ -338,3 +338,51 @@ def backward_without_rowsum(q, k, v, do, cu, scale=None, causal=False, cu_seqlen
 
 def test_backward_rowsum_caught():
     _fails(pins.pin_attention_backward_autograd, backward_without_rowsum, rng(28))
+
+
+# --- Eq. 5 loss and the block's gradients ------------------------------------
+
+def _mutated_backward(old, new):
+    """A copy of oracle.block_backward with one planted mistake (source
+    replacement), loaded as a separate module; the real one is untouched."""
+    import importlib.util
+    import os
+    import oracle
+    path = os.path.join(os.path.dirname(oracle.__file__), "block_backward.py")
+    src = open(path).read()
+    assert src.count(old) == 1, old
+    spec = importlib.util.spec_from_loader("oracle._mutated_block_backward", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"
+    exec(compile(src.replace(old, new), path, "exec"), mod.__dict__)
+    return mod
+
+
+BACKWARD_MISTAKES = [
+    # the column mean's 1/N dropped in the reduce backward
+    ("dPt = dP_tilde + dM[:, None, :] / N", "dPt = dP_tilde + dM[:, None, :]"),
+    # ReLU's mask forgotten
+    ("dA = dH * (A > 0)", "dA = dH"),
+    # the LayerNorm backward without its xhat term
+    ("- xhat * (dxhat * xhat).mean(axis=-1, keepdims=True)) / sigma", ") / sigma"),
+    # column and row sums of the broadcast swapped
+    ("dU = dP.sum(axis=1)", "dU = dP.sum(axis=0)"),
+    # the singles' residual path dropped
+    ("dX = dX_tilde.copy()", "dX = 0 * dX_tilde"),
+    # Eq. 5's weights swapped between the two terms
+    ("return 1.0 + i / B, 1.5 - i / (2.0 * B)", "return 1.5 - i / (2.0 * B), 1.0 + i / B"),
+    # pair term normalised by sum N_i instead of sum N_i^2
+    ("dz[c0:c1] = 2.0 * beta[i] * z_tilde[c0:c1] / (C_p * part.P)",
+     "dz[c0:c1] = 2.0 * beta[i] * z_tilde[c0:c1] / (C_p * part.T)"),
+]
+
+
+@pytest.mark.parametrize("old,new", BACKWARD_MISTAKES)
+def test_backward_mistakes_caught(old, new):
+    mod = _mutated_backward(old, new)
+    _fails(pins.pin_block_backward_autograd, mod.block_loss_and_grads, oblock.block_packed, rng(5))
+
+
+def test_eq5_weight_mistake_caught_by_hand_values():
+    mod = _mutated_backward(*BACKWARD_MISTAKES[5])
+    _fails(pins.pin_eq5_weights, mod.eq5_sample_weights)
