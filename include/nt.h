@@ -341,6 +341,76 @@ nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const vo
                               const float* b_g, void* z_out, void* m, void* s_out, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace nt_pair_block_loss needs (its partial sums). */
+size_t nt_pair_block_loss_workspace_bytes(void);
+
+/*
+ * nt_pair_block_loss -- the sample-weighted squared loss of [DL] Appendix
+ * A.1, Eq. 5, on both outputs of one block (square pairs, the packed layout
+ * being a leading one, S = 1):
+ *     L = sum_i alpha_i ||X~_i||_F^2 / (C_s sum_i N_i)
+ *       + sum_i beta_i  ||P~_i||_F^2 / (C_z sum_i N_i^2),
+ *     alpha_i = 1 + i / B,  beta_i = 1.5 - i / (2 B),
+ * with X~_i the sample's rows of s_out and P~_i its cells of z_tilde.
+ *   s_out     [T, C_s], z_tilde [P, C_z] in the I/O dtype.
+ *   d_loss    one fp32 on the device, written.  The squared sums accumulate
+ *             in fp32 per thread and in double across the batch, in a fixed
+ *             order (the result does not depend on scheduling).
+ *   ds_out    [T, C_s] fp32 or NULL: if given, dL/ds_out = 2 alpha_i X~ / (C_s T).
+ *   dz_tilde  [P, C_z] fp32 or NULL: if given, dL/dz~ = 2 beta_i P~ / (C_z P).
+ *   workspace >= nt_pair_block_loss_workspace_bytes(), 16-byte aligned.
+ * Asynchronous.  Errors as for nt_pair_reduce.
+ */
+nt_status nt_pair_block_loss(const nt_partition* part, nt_dtype dtype, const void* s_out, int32_t C_s,
+                             const void* z_tilde, int32_t C_z, float* d_loss, float* ds_out, float* dz_tilde,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace nt_pair_block_backward needs: u, v, dM, du, dv
+ * ([T, C_z] fp32 each) and dz ([P, C_z] fp32), (5 T + P) * C_z * 4. */
+size_t nt_pair_block_backward_workspace_bytes(int64_t T, int64_t P, int32_t C_z);
+
+/*
+ * nt_pair_block_backward -- gradients of one single -> pair -> single block
+ * ([DL] Eq. 1 with the ReLU transition of nt_pair_transition) with respect to
+ * its singles and every parameter, for upstream gradients of its two
+ * outputs (for Eq. 5, the ds_out and dz_tilde that nt_pair_block_loss
+ * writes).  The chain rule of Eq. 1 ([DL] section 3.4: gradients flow from
+ * the eager loss back through the pair update, the reduction and the
+ * projections):
+ *     dM = ds_out W_g,  dW_g = ds_out^T m,  db_g = sum ds_out
+ *     dP~ = dz_tilde + dM[row] / N_i            (the column mean's backward)
+ *     A = LN(z) W1^T + b1:  dH = dP~ W2,  dA = dH [A > 0],  dY = dA W1,
+ *       dW1 = dA^T LN(z),  dW2 = dP~^T ReLU(A),  db1 = sum dA,  db2 = sum dP~
+ *     dz = dP~ + the LayerNorm backward of dY   (dgamma, dbeta)
+ *     du = row sums of dz,  dv = column sums of dz (within each sample)
+ *     dW_a = du^T s,  dW_b = dv^T s,  ds = ds_out + du W_a + dv W_b
+ * z is rebuilt from s (u = s W_a^T, v = s W_b^T, rounded to the I/O dtype as
+ * the forward rounds it), so the forward's pair state need not be kept.
+ *   part       square partition with row splits (rectangular ones are
+ *              NT_ERR_UNSUPPORTED).
+ *   s          [T, C_s] the block's input singles;  m [T, C_z] the row means
+ *              the forward's nt_pair_reduce wrote.
+ *   W_a, W_b, ln_gamma, ln_beta, ln_eps, W1, b1 (nullable), W2, W_g: the
+ *              forward's parameters (b2 and b_g do not enter the gradients).
+ *   ds_out     [T, C_s] fp32, required;  dz_tilde [P, C_z] fp32 or NULL (no
+ *              gradient reaches z~ from downstream).
+ *   ds         [T, C_s] fp32 out.  dW_a, dW_b [C_z, C_s], dgamma, dbeta [C_z],
+ *              dW1 [H_t, C_z], db1 [H_t], dW2 [C_z, H_t], db2 [C_z],
+ *              dW_g [C_s, C_z], db_g [C_s]: fp32 out, overwritten (the call
+ *              clears them on its stream before accumulating).
+ *   workspace  >= nt_pair_block_backward_workspace_bytes(T, P, C_z) bytes.
+ * Supported: 8 <= C_z <= 128, H_t a multiple of 64, either dtype.  CUDA
+ * cores, fp32 arithmetic; weight gradients accumulate with fp32 atomics, so
+ * they are not bit-reproducible from run to run.  Asynchronous.
+ */
+nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const void* s, int32_t C_s,
+                                 const void* W_a, const void* W_b, int32_t C_z, int32_t H_t, const float* ln_gamma,
+                                 const float* ln_beta, float ln_eps, const void* W1, const float* b1, const void* W2,
+                                 const void* W_g, const void* m, const float* ds_out, const float* dz_tilde,
+                                 float* ds, float* dW_a, float* dW_b, float* dgamma, float* dbeta, float* dW1,
+                                 float* db1, float* dW2, float* db2, float* dW_g, float* db_g, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /*
  * nt_varlen_attn_workspace_bytes -- bytes of device workspace that
  * nt_varlen_attn and nt_varlen_attn_qk take for their work counter (a small

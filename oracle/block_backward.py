@@ -133,10 +133,10 @@ def block_backward_sample(X: np.ndarray, w: Weights, dX_tilde: np.ndarray, dP_ti
     dPt = dP_tilde + dM[:, None, :] / N
     # P~ = P + H W2^T + b2
     dH = dPt @ w.W2                                            # (N, N, H_t)
-    g["dW2"] = np.einsum("abc,abh->ch", dPt, H)
+    g["dW2"] = np.einsum("abc,abh->ch", dPt, H, optimize=True)
     g["db2"] = dPt.sum(axis=(0, 1))
     dA = dH * (A > 0)
-    g["dW1"] = np.einsum("abh,abc->hc", dA, Y)
+    g["dW1"] = np.einsum("abh,abc->hc", dA, Y, optimize=True)
     g["db1"] = dA.sum(axis=(0, 1))
     dY = dA @ w.W1                                             # (N, N, C_p)
     g["dgamma"] = (dY * xhat).sum(axis=(0, 1))

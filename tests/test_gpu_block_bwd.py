@@ -1,0 +1,100 @@
+"""GPU parity of the Eq. 5 loss and of the block's backward
+("DanLing NestedTensor" Appendix A.1, Eq. 5; the chain rule of Eq. 1)
+against the CPU oracle on the same seeded inputs: the loss within 1e-5
+relative (fp32 accumulation of the squared sums), every gradient normwise
+within 2e-2 (bf16 I/O) or 1e-5 (fp32), the oracle running its own forward
+on the exact inputs."""
+import numpy as np
+import pytest
+import torch
+
+from _helpers import TOL, f64, normwise_err, oracle_weights, to_np
+from oracle import block as oblock
+from oracle import block_backward as obwd
+from variable_length_batching_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+NAMES = ("ds", "dW_a", "dW_b", "dgamma", "dbeta", "dW1", "db1", "dW2", "db2", "dW_g", "db_g")
+
+
+@pytest.fixture(scope="module")
+def nt():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from variable_length_batching_gb300 import build, nt as ntmod
+    build.build()
+    return ntmod
+
+
+def _dw(w):
+    from types import SimpleNamespace
+    d = lambda t: None if t is None else t.to(DEV)
+    return SimpleNamespace(W_a=d(w.W_a), W_b=d(w.W_b), ln_gamma=d(w.ln_gamma), ln_beta=d(w.ln_beta), W1=d(w.W1),
+                           b1=d(w.b1), W2=d(w.W2), b2=d(w.b2), W_g=d(w.W_g), b_g=d(w.b_g))
+
+
+def _run(nt, cfg, lengths, biases, seed=0):
+    inp = wl.make_block_inputs(cfg, lengths=lengths, biases=biases, seed=seed)
+    w = _dw(inp.blocks[0])
+    part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(DEV))
+    s = inp.s.to(DEV)
+    z, m, s_out = nt.block_forward(part, s, w)
+    loss, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z)
+    g = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
+    torch.cuda.synchronize()
+    nt.nt_device_status()
+    ow = oracle_weights(inp.blocks[0])
+    fwd = oblock.block_packed(inp.lengths, f64(inp.s), ow)
+    ref_loss, ref = obwd.block_loss_and_grads(inp.lengths, f64(inp.s), ow, fwd.z_tilde, fwd.s_out)
+    return float(loss.item()), g, ref_loss, ref, cfg.dtype
+
+
+def _check(loss, g, ref_loss, ref, dtype, names=NAMES):
+    assert abs(loss - ref_loss) <= (1e-5 if dtype == "f32" else 2e-2) * abs(ref_loss)
+    for n in names:
+        got, want = to_np(g[n]), getattr(ref, n)
+        assert got.shape == want.shape, n
+        e = normwise_err(got, want, dtype=dtype)
+        assert e <= TOL[dtype], f"{n}: normwise error {e:.3e}"
+
+
+@pytest.mark.parametrize("lengths,biases", [(None, True), ([3, 0, 1, 17], False), ([1], True)])
+def test_block_backward_tiny_fp32(nt, lengths, biases):
+    _check(*_run(nt, wl.TINY_FP32, lengths, biases))
+
+
+@pytest.mark.parametrize("lengths,biases", [([37, 1, 0, 70], True), ([64, 31, 5], False)])
+def test_block_backward_bf16(nt, lengths, biases):
+    _check(*_run(nt, wl.PAIRFORMER_BF16, lengths, biases))
+
+
+def test_block_backward_pairformer_batch(nt):
+    """The B=8 Pairformer-style batch itself (N_i ~ U[64, 256], P = 157,023)."""
+    _check(*_run(nt, wl.PAIRFORMER_BF16, None, False))
+
+
+def test_loss_is_reproducible(nt):
+    """The loss sums its partials in a fixed order: two calls give the same bits."""
+    inp = wl.make_block_inputs(wl.PAIRFORMER_BF16)
+    w = _dw(inp.blocks[0])
+    part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(DEV))
+    z, m, s_out = nt.block_forward(part, inp.s.to(DEV), w)
+    l1, _, _ = nt.nt_pair_block_loss(part, s_out, z, want_grads=False)
+    l2, _, _ = nt.nt_pair_block_loss(part, s_out, z, want_grads=False)
+    torch.cuda.synchronize()
+    assert torch.equal(l1, l2)
+
+
+def test_rectangular_partition_refused(nt):
+    part = nt.nt_partition_build_rect(torch.tensor([3, 2], dtype=torch.int32, device=DEV),
+                                      torch.tensor([4, 1], dtype=torch.int32, device=DEV))
+    inp = wl.make_block_inputs(wl.TINY_FP32, lengths=[3, 2])
+    w = _dw(inp.blocks[0])
+    s = inp.s.to(DEV)
+    ds_out = torch.zeros(5, s.shape[1], device=DEV)
+    m = torch.zeros(5, 16, device=DEV)
+    with pytest.raises(nt.NTError) as e:
+        nt.nt_pair_block_backward(part, s, w, m, ds_out)
+    assert e.value.status == 2

@@ -1,0 +1,597 @@
+// The sample-weighted squared loss of the single->pair->single block and
+// the block's gradients, on CUDA cores (fp32 arithmetic; bf16 or fp32
+// inputs; every gradient fp32).
+//
+// "DanLing NestedTensor" Appendix A.1, Eq. 5:
+//     L = sum_i alpha_i ||X~_i||^2 / (C sum N_i) + sum_i beta_i ||P~_i||^2 / (C_p sum N_i^2),
+//     alpha_i = 1 + i/B, beta_i = 1.5 - i/(2B)
+// (S = 1: the packed layout is a leading one), and the chain rule of Eq. 1
+// (section 3.4: the gradient flows from the eager loss back through the
+// pair update, the reduction and the projections):
+//     dM = dX~ W_g, dW_g = dX~^T M, db_g = sum dX~
+//     dP~ = dP~_up + dM[row] / N          (the column mean's backward)
+//     A = LN(z) W1^T + b1:  dH = dP~ W2, dA = dH [A > 0], dY = dA W1,
+//       dW1 = dA^T LN(z), dW2 = dP~^T ReLU(A), db1 = sum dA, db2 = sum dP~
+//     dz = dP~ + LayerNorm backward of dY (dgamma, dbeta on the way)
+//     du[row] = sum over the row's cells of dz, dv[col] = sum over the column's
+//     dW_a = du^T s, dW_b = dv^T s, ds = dX~ + du W_a + dv W_b
+// z is rebuilt from u = s W_a^T and v = s W_b^T, rounded to the I/O dtype as
+// the forward rounds it.  Square partitions only.
+//
+// Kernels:
+//   eq5_partial / eq5_finish     the loss (per pair row, fixed-order final sum)
+//                                and, optionally, its gradients dX~, dP~
+//   rowmm                         Y = A W (+ A2 W2) (+ R) over the T single rows
+//   gram                          G += A^T B over the T single rows (weight gradients)
+//   colsum                        column sums over the T single rows (bias gradients)
+//   trans_bwd_cells               per 32-cell tile: z, LayerNorm, A, dH, dA, dY over
+//                                 64-unit hidden chunks, the LayerNorm backward -> dz;
+//                                 dgamma, dbeta, db2
+//   trans_bwd_weights             per (hidden chunk, cell range): dW1, dW2, db1
+//   pair_rowcol_sum               du (row sums) and dv (column sums) of dz
+#include "nt_common.cuh"
+
+namespace nt {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTC = 32;      // cells per tile
+constexpr int kHC = 64;      // hidden units per chunk
+constexpr int kCmax = 128;   // largest pair width the cell kernels hold
+constexpr int kLossBlocks = 1024;   // CTAs (and double partial pairs) of the loss
+
+// Sample of packed cell p: the last b with pair_off[b] <= p (steps past
+// samples with no cells), then the row and column within its N x N block.
+__device__ __forceinline__ void cell_coords(const int64_t* __restrict__ pair_off, const int32_t* __restrict__ cu,
+                                            const int32_t* __restrict__ len, int B, int64_t p, int64_t& row,
+                                            int64_t& col, int& n) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pair_off[mid] <= p) lo = mid; else hi = mid - 1;
+  }
+  n = len[lo];
+  const int64_t off = p - pair_off[lo];
+  const int64_t a = off / n;
+  row = cu[lo] + a;
+  col = cu[lo] + (off - a * n);
+}
+
+__device__ __forceinline__ float round_io(float x, float*) { return x; }
+__device__ __forceinline__ float round_io(float x, bf16*) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// ---------------------------------------------------------------- the loss
+
+// One CTA per group of pair rows: sum over its rows of alpha_b ||X~ row||^2
+// and of beta_b ||P~ row's cells||^2, in double, into partial[blockIdx];
+// optionally writes dX~ = 2 alpha_b X~ / (C T) and dP~ = 2 beta_b P~ / (C_p P).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+eq5_partial_kernel(const T* __restrict__ s_out, const T* __restrict__ zt, const int64_t* __restrict__ row_start,
+                   const int32_t* __restrict__ row_sample, int B, int64_t Trows, int64_t P, int C, int Cp,
+                   double* __restrict__ partial, float* __restrict__ ds_out, float* __restrict__ dz) {
+  __shared__ double red[2][kThreads / 32];
+  double ax = 0.0, ap = 0.0;
+  for (int64_t r = blockIdx.x; r < Trows; r += gridDim.x) {
+    const int b = row_sample[r];
+    const double alpha = 1.0 + (double)b / B, beta = 1.5 - (double)b / (2.0 * B);
+    const float gx = (float)(2.0 * alpha / ((double)C * Trows)), gp = (float)(2.0 * beta / ((double)Cp * P));
+    float sx = 0.f;
+    for (int k = threadIdx.x; k < C; k += kThreads) {
+      const float x = to_f32(s_out[r * C + k]);
+      sx += x * x;
+      if (ds_out) ds_out[r * C + k] = gx * x;
+    }
+    ax += alpha * sx;
+    const int64_t c0 = row_start[r] * Cp, c1 = row_start[r + 1] * Cp;
+    float sp = 0.f;
+    for (int64_t e = c0 + threadIdx.x; e < c1; e += kThreads) {
+      const float x = to_f32(zt[e]);
+      sp += x * x;
+      if (dz) dz[e] = gp * x;
+    }
+    ap += beta * sp;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    ax += __shfl_xor_sync(0xffffffffu, ax, o);
+    ap += __shfl_xor_sync(0xffffffffu, ap, o);
+  }
+  if ((threadIdx.x & 31) == 0) { red[0][threadIdx.x >> 5] = ax; red[1][threadIdx.x >> 5] = ap; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tx = 0.0, tp = 0.0;
+    for (int w = 0; w < kThreads / 32; ++w) { tx += red[0][w]; tp += red[1][w]; }
+    partial[2 * blockIdx.x] = tx;
+    partial[2 * blockIdx.x + 1] = tp;
+  }
+}
+
+// The partial sums in a fixed order, then Eq. 5's normalisations.
+__global__ void eq5_finish_kernel(const double* __restrict__ partial, int nblocks, int64_t Trows, int64_t P, int C,
+                                  int Cp, float* __restrict__ loss) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double tx = 0.0, tp = 0.0;
+  for (int i = 0; i < nblocks; ++i) { tx += partial[2 * i]; tp += partial[2 * i + 1]; }
+  double l = 0.0;
+  if (Trows > 0) l += tx / ((double)C * Trows);
+  if (P > 0) l += tp / ((double)Cp * P);
+  *loss = (float)l;
+}
+
+// ------------------------------------------------------- the single rows side
+
+// Y[r, n] = R[r, n] + sum_k A[r, k] W[k, n] + sum_k A2[r, k] W2[k, n]
+// (A, A2 fp32 [rows, K]; W, W2 [K, N] row-major in the I/O dtype; R fp32 or
+// null; A2 and W2 may be null).  One CTA per 16 rows; its threads walk the
+// N columns.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+rowmm_kernel(const float* __restrict__ A, const T* __restrict__ W, const float* __restrict__ A2,
+             const T* __restrict__ W2, const float* __restrict__ R, int64_t rows, int K, int N,
+             float* __restrict__ Y) {
+  extern __shared__ float sa[];               // [16][K] of A, then [16][K] of A2
+  const int64_t r0 = (int64_t)blockIdx.x * 16;
+  const int nr = (int)min64(16, rows - r0);
+  for (int e = threadIdx.x; e < 16 * K; e += kThreads) {
+    const int rr = e / K, k = e % K;
+    sa[e] = rr < nr ? A[(r0 + rr) * K + k] : 0.f;
+    if (A2) sa[16 * K + e] = rr < nr ? A2[(r0 + rr) * K + k] : 0.f;
+  }
+  __syncthreads();
+  for (int n = threadIdx.x; n < N; n += kThreads) {
+    float acc[16];
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
+    for (int k = 0; k < K; ++k) {
+      const float w = to_f32(W[(int64_t)k * N + n]);
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) acc[rr] = fmaf(sa[rr * K + k], w, acc[rr]);
+    }
+    if (A2) {
+      for (int k = 0; k < K; ++k) {
+        const float w = to_f32(W2[(int64_t)k * N + n]);
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) acc[rr] = fmaf(sa[16 * K + rr * K + k], w, acc[rr]);
+      }
+    }
+    for (int rr = 0; rr < nr; ++rr) Y[(r0 + rr) * N + n] = (R ? R[(r0 + rr) * N + n] : 0.f) + acc[rr];
+  }
+}
+
+// G[i, j] += sum_r A[r, i] B[r, j] over a range of the single rows (A fp32
+// [rows, M], B [rows, N] fp32 or I/O dtype): one CTA per 32 x 32 tile of G
+// and per range of rows, fp32 atomics into G.
+template <typename TB>
+__global__ void __launch_bounds__(kThreads)
+gram_kernel(const float* __restrict__ A, const TB* __restrict__ Bm, int64_t rows, int M, int N, int splits,
+            float* __restrict__ G) {
+  __shared__ float ta[32][33], tb[32][33];
+  const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  const int64_t rlo = rows * blockIdx.z / splits, rhi = rows * (blockIdx.z + 1) / splits;
+  const int ti = threadIdx.x >> 3, tj = (threadIdx.x & 7) * 4;   // 32 x (8 x 4): four outputs per thread
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int64_t rb = rlo; rb < rhi; rb += 32) {
+    for (int e = threadIdx.x; e < 32 * 32; e += kThreads) {
+      const int rr = e >> 5, c = e & 31;
+      const int64_t r = rb + rr;
+      ta[rr][c] = (r < rhi && i0 + c < M) ? A[r * M + i0 + c] : 0.f;
+      tb[rr][c] = (r < rhi && j0 + c < N) ? to_f32(Bm[r * N + j0 + c]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int rr = 0; rr < 32; ++rr) {
+      const float a = ta[rr][ti];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] = fmaf(a, tb[rr][tj + q], acc[q]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (i0 + ti < M && j0 + tj + q < N) atomicAdd(G + (int64_t)(i0 + ti) * N + j0 + tj + q, acc[q]);
+}
+
+// out[j] += sum_r A[r, j] over a range of rows (fp32 atomics).
+__global__ void __launch_bounds__(kThreads)
+colsum_kernel(const float* __restrict__ A, int64_t rows, int N, int splits, float* __restrict__ out) {
+  const int64_t rlo = rows * blockIdx.y / splits, rhi = rows * (blockIdx.y + 1) / splits;
+  for (int j = blockIdx.x * kThreads + threadIdx.x; j < N; j += gridDim.x * kThreads) {
+    float acc = 0.f;
+    for (int64_t r = rlo; r < rhi; ++r) acc += A[r * N + j];
+    atomicAdd(out + j, acc);
+  }
+}
+
+// du[t] = sum of dz over the cells of pair row t; dv[t] = sum of dz over
+// the cells of column t (the same sample's rows).  One CTA per single row.
+__global__ void __launch_bounds__(kThreads)
+pair_rowcol_sum_kernel(const float* __restrict__ dz, const int32_t* __restrict__ cu,
+                       const int64_t* __restrict__ pair_off, const int32_t* __restrict__ len,
+                       const int32_t* __restrict__ row_sample, int64_t Trows, int C, float* __restrict__ du,
+                       float* __restrict__ dv) {
+  extern __shared__ float part[];            // [2][groups][C]
+  const int groups = kThreads / C;
+  const int f = threadIdx.x % C, g = threadIdx.x / C;
+  for (int64_t t = blockIdx.x; t < Trows; t += gridDim.x) {
+    const int b = row_sample[t];
+    const int64_t n = len[b], a = t - cu[b], base = pair_off[b];
+    float sr = 0.f, sc = 0.f;
+    if (g < groups) {
+      for (int64_t j = g; j < n; j += groups) {
+        sr += dz[(base + a * n + j) * C + f];      // row a, column j
+        sc += dz[(base + j * n + a) * C + f];      // row j, column a
+      }
+      part[g * C + f] = sr;
+      part[(groups + g) * C + f] = sc;
+    }
+    __syncthreads();
+    if (g == 0) {
+      for (int q = 1; q < groups; ++q) { sr += part[q * C + f]; sc += part[(groups + q) * C + f]; }
+      du[t * C + f] = sr;
+      dv[t * C + f] = sc;
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------- the pair cells side
+
+template <typename T>
+struct CellArgs {
+  const float* u;            // [T, C] fp32, s W_a^T
+  const float* v;            // [T, C] fp32, s W_b^T
+  const int64_t* pair_off;
+  const int32_t* cu;
+  const int32_t* len;
+  int B;
+  int64_t P;
+  int C, H;
+  const float* gamma;
+  const float* beta;
+  float eps;
+  const T* W1;               // [H, C]
+  const float* b1;           // [H] or null
+  const T* W2;               // [C, H]
+  const float* dM;           // [T, C] fp32: dX~ W_g
+  const float* dz_up;        // [P, C] fp32 or null: gradient reaching P~ from downstream
+};
+
+// Loads one 32-cell tile: x-hat of the rebuilt z (rounded to the I/O dtype
+// as the forward rounds it) and dP~ = dz_up + dM[row] / N.  Thread t owns
+// cell t / 8 and features f = t % 8 + 8 j.  Cells past P get zeros.
+template <typename T>
+__device__ __forceinline__ void load_tile(const CellArgs<T>& a, int64_t p0, float* xh, float* dpt, float* rstd) {
+  const int cell = threadIdx.x >> 3, sub = threadIdx.x & 7;
+  const int64_t p = p0 + cell;
+  const bool valid = p < a.P;
+  float zv[kCmax / 8];
+  float s1 = 0.f;
+  int64_t row = 0, col = 0;
+  int n = 1;
+  if (valid) cell_coords(a.pair_off, a.cu, a.len, a.B, p, row, col, n);
+  const int nf = (a.C - sub + 7) >> 3;
+#pragma unroll
+  for (int j = 0; j < kCmax / 8; ++j) {
+    zv[j] = 0.f;
+    if (j < nf && valid) {
+      const int f = sub + 8 * j;
+      zv[j] = round_io(a.u[row * a.C + f] + a.v[col * a.C + f], (T*)nullptr);
+      s1 += zv[j];
+    }
+  }
+  s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+  s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+  s1 += __shfl_xor_sync(0xffffffffu, s1, 4);
+  const float mean = s1 / a.C;
+  float s2 = 0.f;
+#pragma unroll
+  for (int j = 0; j < kCmax / 8; ++j)
+    if (j < nf && valid) { const float d = zv[j] - mean; s2 += d * d; }
+  s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+  s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+  s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
+  const float rs = rsqrtf(s2 / a.C + a.eps);
+  const float inv_n = 1.0f / (float)n;
+#pragma unroll
+  for (int j = 0; j < kCmax / 8; ++j) {
+    if (j < nf) {
+      const int f = sub + 8 * j;
+      xh[cell * a.C + f] = valid ? (zv[j] - mean) * rs : 0.f;
+      float d = 0.f;
+      if (valid) {
+        d = a.dM[row * a.C + f] * inv_n;
+        if (a.dz_up) d += a.dz_up[p * a.C + f];
+      }
+      dpt[cell * a.C + f] = d;
+    }
+  }
+  if (sub == 0) rstd[cell] = valid ? rs : 0.f;
+}
+
+// A and dH of hidden chunk c for this thread's cell and its 8 hidden units
+// (hg .. hg + 7): A = y W1^T + b1 with y = gamma x-hat + beta, dH = dP~ W2.
+template <typename T>
+__device__ __forceinline__ void chunk_a_dh(const CellArgs<T>& a, int c, const float* xh, const float* dpt,
+                                           const float* w1c, const float* w2c, int cell, int hg, float* av,
+                                           float* dh) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    av[i] = a.b1 ? a.b1[c * kHC + hg + i] : 0.f;
+    dh[i] = 0.f;
+  }
+  for (int k = 0; k < a.C; ++k) {
+    const float y = fmaf(a.gamma[k], xh[cell * a.C + k], a.beta[k]);
+    const float g = dpt[cell * a.C + k];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      av[i] = fmaf(y, w1c[(hg + i) * (a.C + 1) + k], av[i]);
+      dh[i] = fmaf(g, w2c[k * (kHC + 1) + hg + i], dh[i]);
+    }
+  }
+}
+
+// W1 rows [64 c, 64 c + 64) as w1c[h][k] (row stride C + 1) and W2 columns
+// [64 c, 64 c + 64) as w2c[k][h] (row stride 65), in fp32.
+template <typename T>
+__device__ __forceinline__ void load_chunk(const CellArgs<T>& a, int c, float* w1c, float* w2c) {
+  for (int e = threadIdx.x; e < kHC * a.C; e += kThreads) {
+    const int h = e / a.C, k = e % a.C;
+    w1c[h * (a.C + 1) + k] = to_f32(a.W1[(int64_t)(c * kHC + h) * a.C + k]);
+  }
+  for (int e = threadIdx.x; e < kHC * a.C; e += kThreads) {
+    const int k = e / kHC, h = e % kHC;
+    w2c[k * (kHC + 1) + h] = to_f32(a.W2[(int64_t)k * a.H + c * kHC + h]);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+trans_bwd_cells_kernel(CellArgs<T> a, float* __restrict__ dz_out, float* __restrict__ dgamma,
+                       float* __restrict__ dbeta, float* __restrict__ db2) {
+  extern __shared__ float sm[];
+  float* xh = sm;                               // [32][C]
+  float* dpt = xh + kTC * a.C;                  // [32][C]
+  float* dab = dpt + kTC * a.C;                 // [32][64] dA of the chunk
+  float* w1c = dab + kTC * kHC;                 // [64][C + 1]
+  float* w2c = w1c + kHC * (a.C + 1);           // [C][65]
+  float* rstd = w2c + a.C * (kHC + 1);          // [32]
+  const int cell = threadIdx.x >> 3, sub = threadIdx.x & 7, hg = sub * 8;
+  const int nf = (a.C - sub + 7) >> 3;
+  float pg[kCmax / 8], pb[kCmax / 8], pd[kCmax / 8];   // partial dgamma, dbeta, db2 of features sub + 8 j
+#pragma unroll
+  for (int j = 0; j < kCmax / 8; ++j) pg[j] = pb[j] = pd[j] = 0.f;
+  const int nchunk = a.H / kHC;
+  const int64_t ntiles = (a.P + kTC - 1) / kTC;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t p0 = tile * kTC;
+    __syncthreads();                            // the previous tile's readers are done
+    load_tile(a, p0, xh, dpt, rstd);
+    float dy[kCmax / 8];
+#pragma unroll
+    for (int j = 0; j < kCmax / 8; ++j) dy[j] = 0.f;
+    for (int c = 0; c < nchunk; ++c) {
+      __syncthreads();                          // tile loaded / previous chunk's dA read
+      load_chunk(a, c, w1c, w2c);
+      __syncthreads();
+      float av[8], dh[8];
+      chunk_a_dh(a, c, xh, dpt, w1c, w2c, cell, hg, av, dh);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dab[cell * kHC + hg + i] = av[i] > 0.f ? dh[i] : 0.f;
+      __syncthreads();
+      // dY[cell][f] += sum_h dA[cell][h] W1[64 c + h][f], features f = sub + 8 j
+      for (int h = 0; h < kHC; ++h) {
+        const float d = dab[cell * kHC + h];
+#pragma unroll
+        for (int j = 0; j < kCmax / 8; ++j)
+          if (j < nf) dy[j] = fmaf(d, w1c[h * (a.C + 1) + sub + 8 * j], dy[j]);
+      }
+    }
+    // LayerNorm backward: dz = dP~ + rstd (dx - mean(dx) - xh mean(dx xh)), dx = dY gamma
+    const float rs = rstd[cell];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < kCmax / 8; ++j)
+      if (j < nf) {
+        const int f = sub + 8 * j;
+        const float dx = dy[j] * a.gamma[f];
+        s1 += dx;
+        s2 += dx * xh[cell * a.C + f];
+      }
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 4);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
+    const float m1 = s1 / a.C, m2 = s2 / a.C;
+    const int64_t p = p0 + cell;
+#pragma unroll
+    for (int j = 0; j < kCmax / 8; ++j)
+      if (j < nf) {
+        const int f = sub + 8 * j;
+        const float x = xh[cell * a.C + f];
+        const float g = dpt[cell * a.C + f];
+        if (p < a.P) dz_out[p * a.C + f] = g + rs * (dy[j] * a.gamma[f] - m1 - x * m2);
+        pg[j] += dy[j] * x;
+        pb[j] += dy[j];
+        pd[j] += g;
+      }
+  }
+  // this CTA's feature sums: over the four cells of each warp that share a
+  // feature set (lanes sub, sub + 8, sub + 16, sub + 24), then one atomic per warp
+#pragma unroll
+  for (int j = 0; j < kCmax / 8; ++j) {
+    float g = pg[j], b = pb[j], d = pd[j];
+    g += __shfl_xor_sync(0xffffffffu, g, 8);  g += __shfl_xor_sync(0xffffffffu, g, 16);
+    b += __shfl_xor_sync(0xffffffffu, b, 8);  b += __shfl_xor_sync(0xffffffffu, b, 16);
+    d += __shfl_xor_sync(0xffffffffu, d, 8);  d += __shfl_xor_sync(0xffffffffu, d, 16);
+    if (j < nf && (threadIdx.x & 31) < 8) {
+      const int f = sub + 8 * j;
+      atomicAdd(dgamma + f, g);
+      atomicAdd(dbeta + f, b);
+      atomicAdd(db2 + f, d);
+    }
+  }
+}
+
+// Weight gradients of hidden chunk c = blockIdx.x over the cell range of
+// blockIdx.y: dW1[64 c + h][k] += sum_cells dA[h] y[k], dW2[k][64 c + h] +=
+// sum_cells dP~[k] ReLU(A)[h], db1 += sum_cells dA.  Each thread keeps its
+// outputs (o = t + 256 j of the 64 x C block of each) in registers over
+// the range, then adds them with one atomic each.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+trans_bwd_weights_kernel(CellArgs<T> a, int splits, float* __restrict__ dW1, float* __restrict__ dW2,
+                         float* __restrict__ db1) {
+  extern __shared__ float sm[];
+  float* xh = sm;                               // [32][C]
+  float* dpt = xh + kTC * a.C;                  // [32][C]
+  float* yb = dpt + kTC * a.C;                  // [32][C] y = gamma xh + beta
+  float* dab = yb + kTC * a.C;                  // [32][64] dA
+  float* hb = dab + kTC * kHC;                  // [32][64] ReLU(A)
+  float* w1c = hb + kTC * kHC;                  // [64][C + 1]
+  float* w2c = w1c + kHC * (a.C + 1);           // [C][65]
+  float* rstd = w2c + a.C * (kHC + 1);          // [32]
+  const int c = blockIdx.x;
+  const int cell = threadIdx.x >> 3, hg = (threadIdx.x & 7) * 8;
+  const int64_t ntiles = (a.P + kTC - 1) / kTC;
+  const int64_t tlo = ntiles * blockIdx.y / splits, thi = ntiles * (blockIdx.y + 1) / splits;
+  const int nout = kHC * a.C;                   // outputs of each of dW1, dW2 for the chunk
+  float g1[kHC * kCmax / kThreads], g2[kHC * kCmax / kThreads];
+#pragma unroll
+  for (int j = 0; j < kHC * kCmax / kThreads; ++j) g1[j] = g2[j] = 0.f;
+  float gb = 0.f;                               // db1 of hidden unit threadIdx.x (< 64)
+  load_chunk(a, c, w1c, w2c);
+  for (int64_t tile = tlo; tile < thi; ++tile) {
+    __syncthreads();                            // chunk loaded / previous tile read
+    load_tile(a, tile * kTC, xh, dpt, rstd);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kTC * a.C; e += kThreads) {
+      const int f = e % a.C;
+      yb[e] = fmaf(a.gamma[f], xh[e], a.beta[f]);
+    }
+    float av[8], dh[8];
+    chunk_a_dh(a, c, xh, dpt, w1c, w2c, cell, hg, av, dh);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      dab[cell * kHC + hg + i] = av[i] > 0.f ? dh[i] : 0.f;
+      hb[cell * kHC + hg + i] = fmaxf(av[i], 0.f);
+    }
+    __syncthreads();
+    // dW1 block element o = (h, k) = (o / C, o % C); dW2 block element o = (k, h) = (o / 64, o % 64)
+#pragma unroll
+    for (int j = 0; j < kHC * kCmax / kThreads; ++j) {
+      const int o = threadIdx.x + kThreads * j;
+      if (o < nout) {
+        const int h1 = o / a.C, k1 = o % a.C;
+        const int k2 = o / kHC, h2 = o % kHC;
+        float s1 = 0.f, s2 = 0.f;
+        for (int q = 0; q < kTC; ++q) {
+          s1 = fmaf(dab[q * kHC + h1], yb[q * a.C + k1], s1);
+          s2 = fmaf(dpt[q * a.C + k2], hb[q * kHC + h2], s2);
+        }
+        g1[j] += s1;
+        g2[j] += s2;
+      }
+    }
+    if (threadIdx.x < kHC)
+      for (int q = 0; q < kTC; ++q) gb += dab[q * kHC + threadIdx.x];
+  }
+#pragma unroll
+  for (int j = 0; j < kHC * kCmax / kThreads; ++j) {
+    const int o = threadIdx.x + kThreads * j;
+    if (o < nout) {
+      const int h1 = o / a.C, k1 = o % a.C;
+      const int k2 = o / kHC, h2 = o % kHC;
+      atomicAdd(dW1 + (int64_t)(c * kHC + h1) * a.C + k1, g1[j]);
+      atomicAdd(dW2 + (int64_t)k2 * a.H + c * kHC + h2, g2[j]);
+    }
+  }
+  if (threadIdx.x < kHC) atomicAdd(db1 + c * kHC + threadIdx.x, gb);
+}
+
+template <typename T>
+cudaError_t eq5_loss_t(const nt_partition* p, const void* s_out, int C_s, const void* zt, int C_z, float* loss,
+                       float* ds_out, float* dz, double* partial, int nblocks, cudaStream_t s) {
+  eq5_partial_kernel<T><<<nblocks, kThreads, 0, s>>>((const T*)s_out, (const T*)zt, p->row_start, p->row_sample,
+                                                     p->B, p->T, p->P, C_s, C_z, partial, ds_out, dz);
+  eq5_finish_kernel<<<1, 32, 0, s>>>(partial, nblocks, p->T, p->P, C_s, C_z, loss);
+  return cudaGetLastError();
+}
+
+size_t cell_smem(int C, bool weights) {
+  const size_t base = (size_t)kTC * C * 2 + (size_t)kTC * kHC + (size_t)kHC * (C + 1) + (size_t)C * (kHC + 1) + kTC;
+  return sizeof(float) * (weights ? base + (size_t)kTC * C + (size_t)kTC * kHC : base);
+}
+
+template <typename T>
+cudaError_t block_backward_t(const BlockBwd& q, cudaStream_t s) {
+  const nt_partition* p = q.part;
+  const int C = q.C_z, Cs = q.C_s;
+  const int64_t Trows = p->T;
+  cudaError_t e;
+  // dM = dX~ W_g ([T, C_s] x [C_s, C_z]); dW_g += dX~^T m; db_g += column sums of dX~
+  if (Trows > 0) {
+    const unsigned g = (unsigned)((Trows + 15) / 16);
+    rowmm_kernel<T><<<g, kThreads, 16 * Cs * sizeof(float), s>>>(q.ds_out, (const T*)q.W_g, nullptr, nullptr,
+                                                                  nullptr, Trows, Cs, C, q.dM);
+    const int splits = (int)min64(64, (Trows + 255) / 256);
+    gram_kernel<T><<<dim3((Cs + 31) / 32, (C + 31) / 32, splits), kThreads, 0, s>>>(q.ds_out, (const T*)q.m,
+                                                                                      Trows, Cs, C, splits, q.dW_g);
+    colsum_kernel<<<dim3((Cs + kThreads - 1) / kThreads, splits), kThreads, 0, s>>>(q.ds_out, Trows, Cs, splits,
+                                                                                     q.db_g);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // the pair cells: dz, dgamma, dbeta, db2, then dW1, dW2, db1
+  if (p->P > 0) {
+    CellArgs<T> a = {q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, p->P, C, q.H_t, q.gamma, q.beta,
+                     q.eps, (const T*)q.W1, q.b1, (const T*)q.W2, q.dM, q.dz_up};
+    const size_t sm1 = cell_smem(C, false), sm2 = cell_smem(C, true);
+    e = cudaFuncSetAttribute(trans_bwd_cells_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(trans_bwd_weights_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2);
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = (p->P + kTC - 1) / kTC;
+    const int grid1 = (int)min64(ntiles, (int64_t)sm_count() * 2);
+    trans_bwd_cells_kernel<T><<<grid1, kThreads, sm1, s>>>(a, q.dz, q.dgamma, q.dbeta, q.db2);
+    const int nchunk = q.H_t / kHC;
+    const int splits = (int)max64(1, min64(ntiles, (int64_t)sm_count() * 2 / nchunk));
+    trans_bwd_weights_kernel<T><<<dim3(nchunk, splits), kThreads, sm2, s>>>(a, splits, q.dW1, q.dW2, q.db1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // the broadcast: du, dv; dW_a += du^T s, dW_b += dv^T s; ds = dX~ + du W_a + dv W_b
+  if (Trows > 0) {
+    pair_rowcol_sum_kernel<<<(unsigned)min64(Trows, 4096), kThreads, 2 * kThreads * sizeof(float), s>>>(
+        q.dz, p->cu_seqlens, p->pair_off, p->lengths, p->row_sample, Trows, C, q.du, q.dv);
+    const int splits = (int)min64(64, (Trows + 255) / 256);
+    gram_kernel<T><<<dim3((C + 31) / 32, (Cs + 31) / 32, splits), kThreads, 0, s>>>(q.du, (const T*)q.s, Trows, C,
+                                                                                     Cs, splits, q.dW_a);
+    gram_kernel<T><<<dim3((C + 31) / 32, (Cs + 31) / 32, splits), kThreads, 0, s>>>(q.dv, (const T*)q.s, Trows, C,
+                                                                                     Cs, splits, q.dW_b);
+    const unsigned g = (unsigned)((Trows + 15) / 16);
+    rowmm_kernel<T><<<g, kThreads, 2 * 16 * C * sizeof(float), s>>>(q.du, (const T*)q.W_a, q.dv, (const T*)q.W_b,
+                                                                     q.ds_out, Trows, C, Cs, q.ds);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+bool block_bwd_supported(int C_z, int H_t) { return C_z >= 8 && C_z <= kCmax && H_t >= kHC && H_t % kHC == 0; }
+
+cudaError_t launch_eq5_loss(nt_dtype dt, const nt_partition* p, const void* s_out, int C_s, const void* zt, int C_z,
+                            float* loss, float* ds_out, float* dz, void* workspace, cudaStream_t s) {
+  const int nblocks = (int)max64(1, min64(p->T, kLossBlocks));
+  double* partial = static_cast<double*>(workspace);
+  return dt == NT_BF16 ? eq5_loss_t<bf16>(p, s_out, C_s, zt, C_z, loss, ds_out, dz, partial, nblocks, s)
+                       : eq5_loss_t<float>(p, s_out, C_s, zt, C_z, loss, ds_out, dz, partial, nblocks, s);
+}
+
+size_t eq5_loss_workspace_bytes() { return sizeof(double) * 2 * kLossBlocks; }
+
+cudaError_t launch_block_backward(nt_dtype dt, const BlockBwd& q, cudaStream_t s) {
+  return dt == NT_BF16 ? block_backward_t<bf16>(q, s) : block_backward_t<float>(q, s);
+}
+
+}  // namespace nt

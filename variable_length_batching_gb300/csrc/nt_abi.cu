@@ -630,6 +630,87 @@ nt_status nt_varlen_attn(nt_dtype dtype, const void* q, const void* k, const voi
                            lse, workspace, workspace_bytes, stream);
 }
 
+size_t nt_pair_block_loss_workspace_bytes(void) { return eq5_loss_workspace_bytes(); }
+
+nt_status nt_pair_block_loss(const nt_partition* part, nt_dtype dtype, const void* s_out, int32_t C_s,
+                             const void* z_tilde, int32_t C_z, float* d_loss, float* ds_out, float* dz_tilde,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  nt_status st = check_partition(part, true);
+  if (st != NT_OK) return st;
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (!width_ok(dtype, C_s) || !width_ok(dtype, C_z))
+    return fail(NT_ERR_UNSUPPORTED, "C_s=%d, C_z=%d must be positive multiples of %d", C_s, C_z,
+                dtype == NT_BF16 ? 8 : 4);
+  if (!d_loss || !workspace || (part->T > 0 && !s_out) || (part->P > 0 && !z_tilde))
+    return fail(NT_ERR_INVALID, "NULL pointer");
+  if (!aligned16(s_out) || !aligned16(z_tilde) || !aligned16(ds_out) || !aligned16(dz_tilde) ||
+      !aligned16(workspace))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  if (workspace_bytes < eq5_loss_workspace_bytes())
+    return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, eq5_loss_workspace_bytes());
+  cudaError_t e = launch_eq5_loss(dtype, part, s_out, C_s, z_tilde, C_z, d_loss, ds_out, dz_tilde, workspace,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "loss launch");
+  return NT_OK;
+}
+
+size_t nt_pair_block_backward_workspace_bytes(int64_t T, int64_t P, int32_t C_z) {
+  if (T < 0 || P < 0 || C_z < 0) return 0;
+  return (size_t)(5 * T + P) * (size_t)C_z * sizeof(float);
+}
+
+nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const void* s, int32_t C_s,
+                                 const void* W_a, const void* W_b, int32_t C_z, int32_t H_t, const float* ln_gamma,
+                                 const float* ln_beta, float ln_eps, const void* W1, const float* b1, const void* W2,
+                                 const void* W_g, const void* m, const float* ds_out, const float* dz_tilde,
+                                 float* ds, float* dW_a, float* dW_b, float* dgamma, float* dbeta, float* dW1,
+                                 float* db1, float* dW2, float* db2, float* dW_g, float* db_g, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  nt_status st = check_partition(part, true);
+  if (st != NT_OK) return st;
+  if (part->col_lengths && (part->col_lengths != part->lengths || part->col_cu_seqlens != part->cu_seqlens))
+    return fail(NT_ERR_UNSUPPORTED, "the block backward takes square partitions");
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (!width_ok(dtype, C_s) || !width_ok(dtype, C_z) || !block_bwd_supported(C_z, H_t))
+    return fail(NT_ERR_UNSUPPORTED, "C_s=%d, C_z=%d (8..128), H_t=%d (a multiple of 64)", C_s, C_z, H_t);
+  if (!(ln_eps >= 0.0f)) return fail(NT_ERR_INVALID, "ln_eps must be >= 0");
+  if (!W_a || !W_b || !ln_gamma || !ln_beta || !W1 || !W2 || !W_g || !dW_a || !dW_b || !dgamma || !dbeta ||
+      !dW1 || !db1 || !dW2 || !db2 || !dW_g || !db_g || !workspace)
+    return fail(NT_ERR_INVALID, "NULL pointer");
+  if (part->T > 0 && (!s || !m || !ds_out || !ds)) return fail(NT_ERR_INVALID, "NULL single-row pointer");
+  const void* ptrs[] = {s, W_a, W_b, ln_gamma, ln_beta, W1, b1, W2, W_g, m, ds_out, dz_tilde, ds, dW_a, dW_b,
+                        dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  const size_t need = nt_pair_block_backward_workspace_bytes(part->T, part->P, C_z);
+  if (workspace_bytes < need) return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  // the gradients that are sums start at zero
+  const size_t f4 = sizeof(float);
+  struct { float* p; size_t n; } zero[] = {
+      {dW_a, (size_t)C_z * C_s}, {dW_b, (size_t)C_z * C_s}, {dgamma, (size_t)C_z}, {dbeta, (size_t)C_z},
+      {dW1, (size_t)H_t * C_z}, {db1, (size_t)H_t}, {dW2, (size_t)C_z * H_t}, {db2, (size_t)C_z},
+      {dW_g, (size_t)C_s * C_z}, {db_g, (size_t)C_s}};
+  for (auto& zr : zero) {
+    cudaError_t e = cudaMemsetAsync(zr.p, 0, zr.n * f4, st_);
+    if (e != cudaSuccess) return cuda_fail(e, "gradient clear");
+  }
+  if (part->T == 0) return NT_OK;
+  float* u = static_cast<float*>(workspace);
+  float* v = u + part->T * (int64_t)C_z;
+  float* dM = v + part->T * (int64_t)C_z;
+  float* du = dM + part->T * (int64_t)C_z;
+  float* dv = du + part->T * (int64_t)C_z;
+  float* dz = dv + part->T * (int64_t)C_z;
+  cudaError_t e = project_uv(part, dtype, s, s, C_s, W_a, W_b, C_z, u, v, st_);
+  if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+  BlockBwd q = {part, C_s, C_z, H_t, s, W_a, W_b, ln_gamma, ln_beta, ln_eps, W1, b1, W2, W_g, m, ds_out, dz_tilde,
+                ds, dW_a, dW_b, dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g, u, v, dM, dz, du, dv};
+  e = launch_block_backward(dtype, q, st_);
+  if (e != cudaSuccess) return cuda_fail(e, "block backward launch");
+  return NT_OK;
+}
+
 nt_status nt_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

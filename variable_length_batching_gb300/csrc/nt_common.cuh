@@ -234,6 +234,55 @@ cudaError_t launch_attn_bwd(nt_dtype dt, const AttnBwdProblem& p, float* Dbuf, u
 bool attn_bwd_tc_supported(nt_dtype dt, int d);
 cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsigned int* status, cudaStream_t s);
 
+// The Eq. 5 loss ("DanLing NestedTensor" Appendix A.1) on the block's outputs
+// and, optionally, its gradients dX~ [T, C_s] and dP~ [P, C_z] (fp32).
+// workspace: eq5_loss_workspace_bytes() for the partial sums.
+size_t eq5_loss_workspace_bytes();
+cudaError_t launch_eq5_loss(nt_dtype dt, const nt_partition* p, const void* s_out, int C_s, const void* z_tilde,
+                            int C_z, float* loss, float* ds_out, float* dz, void* workspace, cudaStream_t s);
+
+// The block's backward (the chain rule of Eq. 1) for upstream gradients
+// ds_out [T, C_s] and dz_up [P, C_z] (nullable), fp32; square partitions.
+// u, v, dM, dz, du, dv are fp32 scratch the caller provides ([T, C_z] each,
+// dz [P, C_z]); u and v must hold s W_a^T, s W_b^T.  The gradient outputs
+// that are sums (every weight and bias gradient) must be zero on entry.
+struct BlockBwd {
+  const nt_partition* part;
+  int C_s, C_z, H_t;
+  const void* s;
+  const void* W_a;
+  const void* W_b;
+  const float* gamma;
+  const float* beta;
+  float eps;
+  const void* W1;
+  const float* b1;
+  const void* W2;
+  const void* W_g;
+  const void* m;
+  const float* ds_out;
+  const float* dz_up;
+  float* ds;
+  float* dW_a;
+  float* dW_b;
+  float* dgamma;
+  float* dbeta;
+  float* dW1;
+  float* db1;
+  float* dW2;
+  float* db2;
+  float* dW_g;
+  float* db_g;
+  float* u;
+  float* v;
+  float* dM;
+  float* dz;
+  float* du;
+  float* dv;
+};
+bool block_bwd_supported(int C_z, int H_t);
+cudaError_t launch_block_backward(nt_dtype dt, const BlockBwd& q, cudaStream_t s);
+
 bool attn_simt_supported(int d);
 cudaError_t launch_attn_simt(nt_dtype dt, const AttnProblem& p, unsigned int* status, cudaStream_t s);
 bool attn_tc_supported(nt_dtype dt, int d);

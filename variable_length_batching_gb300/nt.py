@@ -59,6 +59,11 @@ SIGNATURES = {
     "nt_pair_block_fused_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
     "nt_pair_block_fused": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nt_pair_block_loss_workspace_bytes": (_SZ, []),
+    "nt_pair_block_loss": (_I32, [_PP, _I32, _P, _I32, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "nt_pair_block_backward_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
+    "nt_pair_block_backward": (_I32, [_PP, _I32, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
+                                      _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "nt_varlen_attn_workspace_bytes": (_SZ, []),
     "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _P]),
     "nt_varlen_attn_qk": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _F, _I32,
@@ -343,6 +348,52 @@ def nt_pair_reduce(part: Partition, z: torch.Tensor, W_g: Optional[torch.Tensor]
                               _ptr(_f32(b_g)), _ptr(s_in), _ptr(s_out), C_s, _stream(stream))
     _check(st, "nt_pair_reduce")
     return m, s_out
+
+
+def nt_pair_block_loss(part: Partition, s_out: torch.Tensor, z_tilde: torch.Tensor, want_grads: bool = True,
+                       stream=None):
+    """Eq. 5 on one block's outputs: returns (loss as a 1-element fp32
+    device tensor, dL/ds_out, dL/dz~) -- the gradients fp32, or None when
+    ``want_grads`` is False."""
+    T, C_s = s_out.shape
+    C_z = z_tilde.shape[1]
+    if T != part.T or z_tilde.shape[0] != part.P:
+        raise ValueError("outputs do not match the partition")
+    dev = s_out.device
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    ds = torch.empty(T, C_s, dtype=torch.float32, device=dev) if want_grads else None
+    dz = torch.empty(part.P, C_z, dtype=torch.float32, device=dev) if want_grads else None
+    ws = torch.empty(int(lib().nt_pair_block_loss_workspace_bytes()), dtype=torch.uint8, device=dev)
+    st = lib().nt_pair_block_loss(ctypes.byref(part.c), _dtype(s_out), _ptr(s_out), C_s, _ptr(z_tilde), C_z,
+                                  _ptr(loss), _ptr(ds), _ptr(dz), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "nt_pair_block_loss")
+    return loss, ds, dz
+
+
+def nt_pair_block_backward(part: Partition, s: torch.Tensor, w, m: torch.Tensor, ds_out: torch.Tensor,
+                           dz_tilde: Optional[torch.Tensor] = None, ln_eps: float = 1e-5, workspace=None,
+                           stream=None):
+    """Gradients of one block (ReLU transition) for upstream gradients of its
+    outputs; ``w`` holds the forward's parameters.  Returns a dict of fp32
+    tensors: ds, dW_a, dW_b, dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g."""
+    T, C_s = s.shape
+    C_z = w.W_a.shape[0]
+    H_t = w.W1.shape[0]
+    dev = s.device
+    f = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=dev)
+    g = {"ds": f(T, C_s), "dW_a": f(C_z, C_s), "dW_b": f(C_z, C_s), "dgamma": f(C_z), "dbeta": f(C_z),
+         "dW1": f(H_t, C_z), "db1": f(H_t), "dW2": f(C_z, H_t), "db2": f(C_z), "dW_g": f(C_s, C_z), "db_g": f(C_s)}
+    need = int(lib().nt_pair_block_backward_workspace_bytes(part.T, part.P, C_z))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = lib().nt_pair_block_backward(
+        ctypes.byref(part.c), _dtype(s), _ptr(s), C_s, _ptr(w.W_a), _ptr(w.W_b), C_z, H_t, _ptr(_f32(w.ln_gamma)),
+        _ptr(_f32(w.ln_beta)), float(ln_eps), _ptr(w.W1), _ptr(_f32(w.b1)), _ptr(w.W2), _ptr(w.W_g), _ptr(m),
+        _ptr(ds_out), _ptr(dz_tilde), _ptr(g["ds"]), _ptr(g["dW_a"]), _ptr(g["dW_b"]), _ptr(g["dgamma"]),
+        _ptr(g["dbeta"]), _ptr(g["dW1"]), _ptr(g["db1"]), _ptr(g["dW2"]), _ptr(g["db2"]), _ptr(g["dW_g"]),
+        _ptr(g["db_g"]), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nt_pair_block_backward")
+    return g
 
 
 def nt_varlen_attn_workspace_bytes() -> int:
