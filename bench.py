@@ -58,6 +58,8 @@ L2_FLUSH_BYTES = 512 << 20
 # attention
 LAUNCHES_PER_STEP = 7
 SIDE_STEPS = 20                  # timed repetitions of each side report's calls
+BACKWARD_CFG = wl.PAIRFORMER_BF16  # the block backward (CUDA cores) on the B=8 batch
+BACKWARD_STEPS = 3
 
 
 def load_peaks():
@@ -459,6 +461,9 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.empty_cache()
     packing = run_packing(nt, dev, stream, flush, side_steps)
     padsweep = run_padsweep(nt, dev, stream, flush, side_steps, peaks)
+    backward = {"attention": measure_attn_backward(nt, dev, stream, flush, side_steps, peaks, ainp, q_d, k_d, v_d,
+                                                   cu_d, max_len),
+                "block": measure_block_backward(nt, BACKWARD_CFG, dev, stream, flush, BACKWARD_STEPS, peaks)}
 
     if rank != 0:
         return None
@@ -508,12 +513,81 @@ def run_gpu(args, rank, world, local_rank):
         "workloads": workloads,
         "packing": packing,
         "padsweep": padsweep,
+        "backward": backward,
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
     return line
+
+
+def _event_ms(fn, stream, flush, steps, warmup=3):
+    """Mean CUDA-event time (ms) of ``fn`` on ``stream``, L2 flushed before each run."""
+    for _ in range(warmup):
+        flush.fill_(0.0)
+        fn()
+    times = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in times]))
+
+
+def fp32_fma_tflops(dev, peaks):
+    """fp32 FMA peak: 128 lanes per SM per clock x 2 flop x SMs x max SM clock."""
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    return 2 * 128 * torch.cuda.get_device_properties(dev).multi_processor_count * mhz * 1e6 / 1e12
+
+
+def measure_attn_backward(nt, dev, stream, flush, steps, peaks, ainp, q, k, v, cu, max_len):
+    """dq, dk, dv of the attention stream for a seeded upstream gradient
+    (the forward's o and lse made once, outside the timed calls)."""
+    o = torch.empty_like(q)
+    _, lse = nt.nt_varlen_attn_qk(q, k, v, cu, cu, max_len, out=o, want_lse=True, stream=stream)
+    d_o = wl.random_rows(q.shape[0] * ATTN_CFG.H, ATTN_CFG.d, ATTN_CFG.dtype, seed=1).reshape(q.shape).to(dev)
+    ms = _event_ms(lambda: nt.nt_varlen_attn_bwd(q, k, v, o, d_o, lse, cu, None, max_len, stream=stream),
+                   stream, flush, steps)
+    nt.nt_device_status(stream)
+    aw = attn_work(ainp.seqlens, ATTN_CFG.H, ATTN_CFG.d)
+    flops = 2.5 * aw["flops"]        # S recomputed, dV, dP, dQ, dK: 2.5 times the forward's flops
+    return {"workload": ATTN_CFG.name, "ms": ms, "bound": "tensor", "achieved": flops / ms / 1e9,
+            "unit": "TFLOP/s", "peak": peaks["bf16_tflops"], "frac": flops / ms / 1e9 / peaks["bf16_tflops"],
+            "flops": flops, "steps": steps, "call": "D pass + dK/dV kernel + dQ kernel"}
+
+
+def measure_block_backward(nt, cfg, dev, stream, flush, steps, peaks):
+    """The Eq. 5 loss and the block's gradients (CUDA cores, fp32) on one
+    block workload; the forward's outputs are made once, outside the timed
+    calls."""
+    inp = wl.make_block_inputs(cfg)
+    wd = _dev_weights(inp.blocks[0], dev)
+    s = inp.s.to(dev)
+    part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(dev))
+    z, m, s_out = nt.block_forward(part, s, wd, stream=stream)
+    ws = torch.empty(nt.lib().nt_pair_block_backward_workspace_bytes(part.T, part.P, cfg.C_z), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        _, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z, stream=stream)
+        nt.nt_pair_block_backward(part, s, wd, m, ds_out, dz, workspace=ws, stream=stream)
+    ms = _event_ms(step, stream, flush, steps, warmup=2)
+    nt.nt_device_status(stream)
+    # per cell: A recomputed, dH, dY, dW1, dW2 (five C_z x H_t products)
+    flops = 5 * 2 * cfg.C_z * cfg.H_t * part.P
+    peak = fp32_fma_tflops(dev, peaks)
+    out = {"workload": cfg.name, "P": part.P, "ms": ms, "bound": "alu", "achieved": flops / ms / 1e9,
+           "unit": "TFLOP/s", "peak": peak, "frac": flops / ms / 1e9 / peak, "flops": flops, "steps": steps,
+           "peak_source": "fp32 FMA: 128 lanes per SM per clock x 2 flop x SMs x max SM clock",
+           "call": "nt_pair_block_loss + nt_pair_block_backward (fp32 CUDA cores)"}
+    del z, m, s_out, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_block(nt, cfg, dev, stream, flush, steps, warmup, peaks):
@@ -957,6 +1031,17 @@ def run_only(args):
                       {"bytes": part.P * cfg.C_z * es + bw["reduce"]["bytes"] - part.P * cfg.C_z * es,
                        "flops": bw["transition"]["flops"]}, "tensor"),
         }
+        # the Eq. 5 loss and the block's backward (CUDA cores): the forward's
+        # outputs are made once, outside the timed calls
+        zb, mb, sob = nt.block_forward(part, s, wd)
+        bws = torch.empty(nt.lib().nt_pair_block_backward_workspace_bytes(part.T, part.P, cfg.C_z),
+                          dtype=torch.uint8, device=dev)
+
+        def backward_step():
+            _, ds_out, dz = nt.nt_pair_block_loss(part, sob, zb, stream=stream)
+            nt.nt_pair_block_backward(part, s, wd, mb, ds_out, dz, workspace=bws, stream=stream)
+        # per cell: A recomputed, dH, dY, dW1, dW2 (five C_z x H_t products); on fp32 FMA units
+        fns["backward"] = (backward_step, {"bytes": 0, "flops": 5 * 2 * cfg.C_z * cfg.H_t * part.P}, "fma")
         if args.swiglu:
             sw = wl.make_swiglu_weights(cfg.C_z, cfg.H_t, cfg.dtype)
             d = lambda t: None if t is None else t.to(dev)
@@ -989,9 +1074,13 @@ def run_only(args):
                     "peak": peaks["bf16_tflops"]})
     elif bound == "hbm":
         out.update({"bound": "hbm", "achieved": w["bytes"] / ms / 1e6, "unit": "GB/s", "peak": peaks["hbm_gbs"]})
+    elif bound == "fma":
+        fp32_peak = fp32_fma_tflops(dev, peaks)
+        out.update({"bound": "alu", "achieved": w["flops"] / ms / 1e9, "unit": "TFLOP/s", "peak": fp32_peak,
+                    "peak_source": "fp32 FMA: 128 per SM per clock x 2 flop x SMs x max SM clock"})
     if "peak" in out:
         out["frac"] = out["achieved"] / out["peak"]
-        out["peak_source"] = peak_src
+        out.setdefault("peak_source", peak_src)
     print(json.dumps(out), flush=True)
 
 
@@ -1004,7 +1093,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["partition", "broadcast", "transition", "reduce", "block", "fused", "attention",
-                             "packing", "padsweep", "rect"],
+                             "backward", "packing", "padsweep", "rect"],
                     help="time one call on one workload instead of the whole step; 'packing' and "
                          "'padsweep' print the packed-vs-padded reports")
     ap.add_argument("--workload", default="pairformer", choices=sorted(WORKLOADS))
