@@ -10,7 +10,10 @@
 //
 // Shape: C_z = 128, H_t = 128 * NC.  Persistent CTAs, one per SM; a tile is
 // 256 packed rows handled as two 128-row sub-tiles that share every weight
-// chunk (half the weight traffic of 128-row tiles).
+// chunk (half the weight traffic of 128-row tiles).  Work goes out in units,
+// round robin over the CTAs: F full tiles first, then the rows after them
+// in half tiles of one 128-row sub-tile, when those fit in one wave (the
+// launcher picks F); a unit's sub-tile 1 is idle in a half tile.
 //
 // Warp roles (14 warps):
 //   warp 0        TMA producer: z tile (4 boxes of 64 x 128) into one of two
@@ -154,6 +157,18 @@ __device__ __forceinline__ float4 bias4(const float* __restrict__ b, int i) {
   return b ? __ldg(reinterpret_cast<const float4*>(b + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// First row and sub-tile count of work unit u: full tiles of 256 rows
+// before F, half tiles of 128 rows after.
+__device__ __forceinline__ void unit_rows(int64_t u, int64_t F, int64_t& row0, int& nsub) {
+  if (u < F) {
+    row0 = u * kTileRows;
+    nsub = 2;
+  } else {
+    row0 = F * kTileRows + (u - F) * kSubRows;
+    nsub = 1;
+  }
+}
+
 template <bool kGLU, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_constant__ CUtensorMap tm_zout,
@@ -161,7 +176,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
                      const __grid_constant__ CUtensorMap tm_w2, const bf16* z_in, int64_t P, int H_t,
                      const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
                      const float* __restrict__ b1, const float* __restrict__ b3, const float* __restrict__ b2,
-                     const FusedIn fz, unsigned int* status) {
+                     const FusedIn fz, int64_t F, int64_t U, unsigned int* status) {
   // hidden units per chunk; GEMM2 contracts kHid per chunk
   constexpr int kHid = kGLU ? 64 : kChunk;
   extern __shared__ uint8_t smem_raw[];
@@ -175,7 +190,6 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NC = H_t / kHid;
-  const int64_t num_tiles = (P + kTileRows - 1) / kTileRows;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -220,12 +234,12 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       int load_idx = 0;
       int last_j[2] = {-1, -1};                  // the last tile whose z each slot received
       int last_r[2] = {-1, -1};                  // the last tile whose residual each slot received
-      // z of `tile` into slot (j & 1), completing on `bar_`
-      auto load_z = [&](int64_t ztile, int zj, uint64_t* bar_) {
+      // z of the unit at row zrow (zsub sub-tiles) into slot (zj & 1), completing on `bar_`
+      auto load_z = [&](int64_t zrow, int zsub, int zj, uint64_t* bar_) {
         uint8_t* a = sA + (zj & 1) * kABytes;
-        mbar_arrive_expect_tx(bar_, kABytes);
-        const int row0 = (int)(ztile * kTileRows);
-        for (int s = 0; s < 2; ++s)
+        mbar_arrive_expect_tx(bar_, (uint32_t)zsub * kSubBytes);
+        const int row0 = (int)zrow;
+        for (int s = 0; s < zsub; ++s)
           for (int kb = 0; kb < 2; ++kb)
             tma_load_2d(a + s * kSubBytes + kb * kBlockBytes, &tm_zin, bar_, kb * 64, row0 + s * kSubRows);
       };
@@ -233,23 +247,28 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       // last GEMM1s have completed (they were the slot's last readers; GEMM2
       // takes its A operand from TMEM), so the output epilogue reads it from
       // shared memory.
-      auto reload = [&](int64_t ztile, int zj) -> bool {
+      auto reload = [&](int64_t zrow, int zsub, int zj) -> bool {
         if (!mbar_wait(&bar.g1_done[zj & 1], (zj >> 1) & 1, abort_flag, status)) return false;
-        load_z(ztile, zj, &bar.z2_full[zj & 1]);
+        load_z(zrow, zsub, zj, &bar.z2_full[zj & 1]);
         last_r[zj & 1] = zj;
         return true;
       };
       bool ok = true;
       int j = 0;
-      int64_t prev_tile = -1;
-      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
+      int64_t prev_row = -1;
+      int prev_sub = 0;
+      for (int64_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++j) {
         const int slot = j & 1;
+        int64_t row0;
+        int nsub;
+        unit_rows(u, F, row0, nsub);
         if (!kFused) {   // the fused block builds its z tile in the LayerNorm warps
           if (!(ok = mbar_wait(&bar.a_empty[slot], ((j >> 1) & 1) ^ 1, abort_flag, status))) break;
-          load_z(tile, j, &bar.z_full[slot]);
+          load_z(row0, nsub, j, &bar.z_full[slot]);
           last_j[slot] = j;
-          if (prev_tile >= 0 && !(ok = reload(prev_tile, j - 1))) break;
-          prev_tile = tile;
+          if (prev_row >= 0 && !(ok = reload(prev_row, prev_sub, j - 1))) break;
+          prev_row = row0;
+          prev_sub = nsub;
         }
         // weights in consumption order: W1(c), W2(c), W1(c + 1), ...
         for (int q = 0; q < 2 * NC; ++q) {
@@ -284,7 +303,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           ++load_idx;
         }
       }
-      if (ok && prev_tile >= 0) reload(prev_tile, j - 1);
+      if (ok && prev_row >= 0) reload(prev_row, prev_sub, j - 1);
       // drain: every copy this thread issued has landed before the CTA exits
       for (int sl = 0; sl < 2; ++sl) {
         if (last_j[sl] >= 0) mbar_wait(&bar.z_full[sl], (last_j[sl] >> 1) & 1, nullptr, status);
@@ -316,15 +335,16 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         mma_commit(&bar.w_empty[load_idx % kStages]);
         ++load_idx;
       };
-      for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
+      for (int64_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++j) {
         const int slot = j & 1;
+        const int nsub = u < F ? 2 : 1;
         const uint32_t a_base = smem_u32(sA + slot * kABytes);
         if (!(ok = mbar_wait(&bar.a_full[slot], (j >> 1) & 1, abort_flag, status))) break;
         tc_fence_after();
         for (int c = 0; c < NC && ok; ++c) {
           uint32_t wsm;
           if (!(ok = take_w(&wsm))) break;
-          for (int s = 0; s < 2; ++s) {
+          for (int s = 0; s < nsub; ++s) {
             // acc1[s] is free once the previous GEMM2 of sub-tile s has completed
             if (g2n[s] > 0 && !(ok = mbar_wait(&bar.g2_done[s], (g2n[s] - 1) & 1, abort_flag, status))) break;
             tc_fence_after();
@@ -340,8 +360,8 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           if (c == NC - 1)   // the slot's last reads by the tensor core
             mma_commit(kFused ? &bar.a_empty[slot] : &bar.g1_done[slot]);
           if (!(ok = take_w(&wsm))) break;
-          const int it = j * NC + c;
-          for (int s = 0; s < 2; ++s) {
+          const int it = j * NC + c;   // sub-tile 1 idles only in half tiles, which come last
+          for (int s = 0; s < nsub; ++s) {
             if (c == 0 && !(ok = mbar_wait(&bar.acc2_empty[s], (j & 1) ^ 1, abort_flag, status))) break;
             // the hidden chunk as bf16 pairs in acc1[s] (16 hidden units = 8
             // columns), contracted half by half as the epilogue writes it
@@ -380,10 +400,10 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
     const int r_out = (warp & 3) * 32 + lane;
     const uint32_t lane_out = (uint32_t)((warp & 3) * 32) << 16;
     const bool st_leader = threadIdx.x == 64;
-    auto out_tile = [&](int64_t otile, int oj) -> bool {
+    auto out_tile = [&](int64_t orow, int osub, int oj) -> bool {
       const int oslot = oj & 1;
 #pragma unroll 1
-      for (int so = 0; so < 2; ++so) {
+      for (int so = 0; so < osub; ++so) {
         if (!mbar_wait_warp(&bar.acc2_full[so], oj & 1, abort_flag, status)) return false;
         tc_fence_after();
         __syncwarp();
@@ -423,7 +443,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         mbar_arrive(&bar.acc2_empty[so]);
         fence_async_shared();
         mbar_arrive(&bar.out_ready[so]);
-        const int64_t y = otile * kTileRows + so * kSubRows;
+        const int64_t y = orow + so * kSubRows;
         if (st_leader && mbar_wait(&bar.out_ready[so], oj & 1, abort_flag, status) && y < P) {
           tma_store_2d(&tm_zout, hs, 0, (int)y);
           tma_store_2d(&tm_zout, hs + kBlockBytes, 64, (int)y);
@@ -431,7 +451,8 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         }
       }
       if (st_leader) {
-        // the slot is reused once both stores have read it: one arrival per sub-tile
+        // the slot is reused once the stores have read it: two arrivals
+        // (one per sub-tile of a full tile)
         tma_store_wait_read0();
         mbar_arrive(&bar.a_empty[oslot]);
         mbar_arrive(&bar.a_empty[oslot]);
@@ -439,11 +460,15 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       __syncwarp();
       return true;
     };
-    int64_t prev_tile = -1;
+    int64_t prev_row = -1;
+    int prev_sub = 0;
     bool ok_out = true;
     int j = 0;
-    for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++j) {
+    for (int64_t u = blockIdx.x; u < U; u += gridDim.x, ++j) {
       const int slot = j & 1;
+      int64_t row0;
+      int nsub;
+      unit_rows(u, F, row0, nsub);
       uint8_t* a = sA + slot * kABytes;
       if (kFused) {
         // the slot is free once its previous tile's GEMM1s and output stores
@@ -451,9 +476,9 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
         // z = bf16(u[row] + v[col])
         if (!mbar_wait(&bar.a_empty[slot], ((j >> 1) & 1) ^ 1, abort_flag, status)) break;
 #pragma unroll 1
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < nsub; ++s) {
           uint8_t* base = a + s * kSubBytes;
-          const int64_t p = tile * kTileRows + s * kSubRows + t;
+          const int64_t p = row0 + s * kSubRows + t;
           if (p < P) {
             int64_t row, vrow;
             cell_of(fz, p, row, vrow);
@@ -530,12 +555,13 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       fence_async_shared();
       mbar_arrive(&bar.a_full[slot]);
       if (!kFused) {
-        if (prev_tile >= 0 && !(ok_out = out_tile(prev_tile, j - 1))) break;
-        prev_tile = tile;
+        if (prev_row >= 0 && !(ok_out = out_tile(prev_row, prev_sub, j - 1))) break;
+        prev_row = row0;
+        prev_sub = nsub;
       }
     }
     if (!kFused) {
-      if (ok_out && prev_tile >= 0) out_tile(prev_tile, j - 1);
+      if (ok_out && prev_row >= 0) out_tile(prev_row, prev_sub, j - 1);
       if (st_leader) tma_store_wait0();
     }
   } else {
@@ -549,8 +575,12 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
     int it = 0;
     int j = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++j) {
+    for (int64_t u = blockIdx.x; u < U && ok; u += gridDim.x, ++j) {
       const int slot = j & 1;
+      int64_t row0;
+      int nsub;
+      unit_rows(u, F, row0, nsub);
+      if (s >= nsub) continue;                     // sub-tile 1 of a half tile: idle
       for (int c = 0; c < NC; ++c, ++it) {
         if (!(ok = mbar_wait_warp(&bar.acc1_full[s], it & 1, abort_flag, status))) break;
         tc_fence_after();
@@ -638,7 +668,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       tc_fence_after();
       __syncwarp();
       uint8_t* hs = sA + slot * kABytes + s * kSubBytes;
-      const int64_t row_g = tile * kTileRows + s * kSubRows + r;
+      const int64_t row_g = row0 + s * kSubRows + r;
       const bool in_range = row_g < P;
       const bf16* zr = z_in + row_g * kCz;
       int64_t f_row = 0, f_vrow = 0;        // fused: the cell's pair row and column single
@@ -676,7 +706,7 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
       mbar_arrive(&bar.acc2_empty[s]);
       fence_async_shared();
       mbar_arrive(&bar.out_ready[s]);
-      const int64_t y = tile * kTileRows + s * kSubRows;
+      const int64_t y = row0 + s * kSubRows;
       if (kFused) {
         // every thread reads the staged z~ tile: wait until it is complete
         if (!(ok = mbar_wait_warp(&bar.out_ready[s], j & 1, abort_flag, status))) break;
@@ -718,7 +748,10 @@ transition_tc_kernel(const __grid_constant__ CUtensorMap tm_zin, const __grid_co
           // the slot is reused once the column sums and the store's reads are done
           const bool sums_done = mbar_wait(&bar.colsum_done[s], j & 1, abort_flag, status);
           if (y < P) tma_store_wait_read0();
-          if (sums_done) mbar_arrive(&bar.a_empty[slot]);
+          if (sums_done) {
+            mbar_arrive(&bar.a_empty[slot]);
+            if (nsub == 1) mbar_arrive(&bar.a_empty[slot]);   // for the idle sub-tile 1
+          }
         }
       } else if (leader) {
         if (mbar_wait(&bar.out_ready[s], j & 1, abort_flag, status) && y < P) {
@@ -798,11 +831,33 @@ cudaError_t launch_tc(const void* z_in, void* z_out, int64_t P, int C_z, int H_t
                     : (glu ? transition_tc_kernel<true, false> : transition_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
+  // Work units: S sub-tiles of 128 rows.  At most one sub-tile per SM: one
+  // half tile per CTA.  Otherwise full tiles in whole waves of the grid and
+  // the sub-tiles left in half tiles, when those fit in one more wave (the
+  // slowest CTA then does one half tile more than the rest rather than one
+  // full tile); else full tiles only.
+  const int64_t S = (P + kSubRows - 1) / kSubRows;
   const int64_t tiles = (P + kTileRows - 1) / kTileRows;
-  const int grid = (int)min64(tiles, (int64_t)sm_count());
+  const int64_t sms = sm_count();
+  int64_t grid, F, U;
+  if (S <= sms) {
+    grid = S;
+    F = 0;
+    U = S;
+  } else {
+    grid = min64(tiles, sms);
+    const int64_t k = S / (2 * grid), H = S - 2 * k * grid;
+    if (H <= grid) {
+      F = k * grid;
+      U = F + H;
+    } else {
+      F = tiles;
+      U = tiles;
+    }
+  }
   const FusedIn none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, 0};
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, m_zin, m_zout, m_w1, m_w3, m_w2,
-                    (const bf16*)z_in, P, H_t, gamma, beta, eps, b1, b3, b2, fused ? *fused : none, status);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, m_zin, m_zout, m_w1, m_w3, m_w2,
+                    (const bf16*)z_in, P, H_t, gamma, beta, eps, b1, b3, b2, fused ? *fused : none, F, U, status);
 }
 
 }  // namespace
