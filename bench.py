@@ -59,7 +59,7 @@ L2_CLEAN_BYTES = 256 << 20
 # attention
 LAUNCHES_PER_STEP = 7
 SIDE_STEPS = 20                  # timed repetitions of each side report's calls
-BACKWARD_CFG = wl.PAIRFORMER_BF16  # the block backward (CUDA cores) on the B=8 batch
+BACKWARD_CFG = wl.NEAR_UNIFORM_BF16  # the block backward on the headline batch
 BACKWARD_STEPS = 3
 
 
@@ -578,16 +578,33 @@ def measure_attn_backward(nt, dev, stream, flush, steps, peaks, ainp, q, k, v, c
             "flops": flops, "steps": steps, "call": "D pass + dK/dV kernel + dQ kernel"}
 
 
+def backward_route(cfg):
+    """The pair-cell part of the block backward runs on the tensor cores for
+    bf16 with C_z = 128 and H_t a multiple of 128, else on CUDA cores."""
+    return "tensor" if cfg.dtype == wl.BF16 and cfg.C_z == 128 and cfg.H_t % 128 == 0 else "fma"
+
+
+def backward_roof(route, flops, ms, dev, peaks):
+    """Achieved algorithmic TFLOP/s against the bf16 tensor peak (tensor-core
+    route) or the derived fp32 FMA peak (CUDA-core route)."""
+    achieved = flops / ms / 1e9
+    if route == "tensor":
+        return {"bound": "tensor", "achieved": achieved, "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
+                "frac": achieved / peaks["bf16_tflops"], "peak_source": "measured bf16"}
+    peak = fp32_fma_tflops(dev, peaks)
+    return {"bound": "alu", "achieved": achieved, "unit": "TFLOP/s", "peak": peak, "frac": achieved / peak,
+            "peak_source": "fp32 FMA: 128 lanes per SM per clock x 2 flop x SMs x max SM clock"}
+
+
 def measure_block_backward(nt, cfg, dev, stream, flush, steps, peaks):
-    """The Eq. 5 loss and the block's gradients (CUDA cores, fp32) on one
-    block workload; the forward's outputs are made once, outside the timed
-    calls."""
+    """The Eq. 5 loss and the block's gradients on one block workload; the
+    forward's outputs are made once, outside the timed calls."""
     inp = wl.make_block_inputs(cfg)
     wd = _dev_weights(inp.blocks[0], dev)
     s = inp.s.to(dev)
     part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(dev))
     z, m, s_out = nt.block_forward(part, s, wd, stream=stream)
-    ws = torch.empty(nt.lib().nt_pair_block_backward_workspace_bytes(part.T, part.P, cfg.C_z), dtype=torch.uint8,
+    ws = torch.empty(nt.nt_pair_block_backward_workspace_bytes(nt._dtype(s), part.T, part.P, cfg.C_z, cfg.H_t), dtype=torch.uint8,
                      device=dev)
 
     def step():
@@ -597,11 +614,11 @@ def measure_block_backward(nt, cfg, dev, stream, flush, steps, peaks):
     nt.nt_device_status(stream)
     # per cell: A recomputed, dH, dY, dW1, dW2 (five C_z x H_t products)
     flops = 5 * 2 * cfg.C_z * cfg.H_t * part.P
-    peak = fp32_fma_tflops(dev, peaks)
-    out = {"workload": cfg.name, "P": part.P, "ms": ms, "bound": "alu", "achieved": flops / ms / 1e9,
-           "unit": "TFLOP/s", "peak": peak, "frac": flops / ms / 1e9 / peak, "flops": flops, "steps": steps,
-           "peak_source": "fp32 FMA: 128 lanes per SM per clock x 2 flop x SMs x max SM clock",
-           "call": "nt_pair_block_loss + nt_pair_block_backward (fp32 CUDA cores)"}
+    route = backward_route(cfg)
+    out = {"workload": cfg.name, "P": part.P, "ms": ms, "flops": flops, "steps": steps,
+           **backward_roof(route, flops, ms, dev, peaks),
+           "call": "nt_pair_block_loss + nt_pair_block_backward ("
+                   + ("pair cells on tcgen05 GEMMs" if route == "tensor" else "fp32 CUDA cores") + ")"}
     del z, m, s_out, ws
     torch.cuda.empty_cache()
     return out
@@ -1051,14 +1068,15 @@ def run_only(args):
         # the Eq. 5 loss and the block's backward (CUDA cores): the forward's
         # outputs are made once, outside the timed calls
         zb, mb, sob = nt.block_forward(part, s, wd)
-        bws = torch.empty(nt.lib().nt_pair_block_backward_workspace_bytes(part.T, part.P, cfg.C_z),
+        bws = torch.empty(nt.nt_pair_block_backward_workspace_bytes(nt._dtype(s), part.T, part.P, cfg.C_z, cfg.H_t),
                           dtype=torch.uint8, device=dev)
 
         def backward_step():
             _, ds_out, dz = nt.nt_pair_block_loss(part, sob, zb, stream=stream)
             nt.nt_pair_block_backward(part, s, wd, mb, ds_out, dz, workspace=bws, stream=stream)
-        # per cell: A recomputed, dH, dY, dW1, dW2 (five C_z x H_t products); on fp32 FMA units
-        fns["backward"] = (backward_step, {"bytes": 0, "flops": 5 * 2 * cfg.C_z * cfg.H_t * part.P}, "fma")
+        # per cell: A recomputed, dH, dY, dW1, dW2 (five C_z x H_t products)
+        fns["backward"] = (backward_step, {"bytes": 0, "flops": 5 * 2 * cfg.C_z * cfg.H_t * part.P},
+                           "tensor" if backward_route(cfg) == "tensor" else "fma")
         if args.swiglu:
             sw = wl.make_swiglu_weights(cfg.C_z, cfg.H_t, cfg.dtype)
             d = lambda t: None if t is None else t.to(dev)

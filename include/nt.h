@@ -365,9 +365,14 @@ nt_status nt_pair_block_loss(const nt_partition* part, nt_dtype dtype, const voi
                              const void* z_tilde, int32_t C_z, float* d_loss, float* ds_out, float* dz_tilde,
                              void* workspace, size_t workspace_bytes, void* stream);
 
-/* Bytes of device workspace nt_pair_block_backward needs: u, v, dM, du, dv
- * ([T, C_z] fp32 each) and dz ([P, C_z] fp32), (5 T + P) * C_z * 4. */
-size_t nt_pair_block_backward_workspace_bytes(int64_t T, int64_t P, int32_t C_z);
+/* Bytes of device workspace nt_pair_block_backward needs for this dtype and
+ * these sizes: u, v, dM, du, dv ([T, C_z] fp32 each) and dz ([P, C_z] fp32),
+ * (5 T + P) * C_z * 4 rounded up to 256; for bf16 with C_z = 128 and H_t a
+ * multiple of 128 (the tensor-core route), also the cells' rows LN(z) and
+ * dP~ ([P, C_z] bf16 each), H and dA ([P, H_t] bf16 each), the LayerNorm
+ * statistics ([P, 2] fp32), the transposed W1 and W2 and the split
+ * weight-gradient partials.  0 for negative sizes. */
+size_t nt_pair_block_backward_workspace_bytes(nt_dtype dtype, int64_t T, int64_t P, int32_t C_z, int32_t H_t);
 
 /*
  * nt_pair_block_backward -- gradients of one single -> pair -> single block
@@ -398,10 +403,17 @@ size_t nt_pair_block_backward_workspace_bytes(int64_t T, int64_t P, int32_t C_z)
  *              dW1 [H_t, C_z], db1 [H_t], dW2 [C_z, H_t], db2 [C_z],
  *              dW_g [C_s, C_z], db_g [C_s]: fp32 out, overwritten (the call
  *              clears them on its stream before accumulating).
- *   workspace  >= nt_pair_block_backward_workspace_bytes(T, P, C_z) bytes.
- * Supported: 8 <= C_z <= 128, H_t a multiple of 64, either dtype.  CUDA
- * cores, fp32 arithmetic; weight gradients accumulate with fp32 atomics, so
- * they are not bit-reproducible from run to run.  Asynchronous.
+ *   workspace  >= nt_pair_block_backward_workspace_bytes(dtype, T, P, C_z,
+ *              H_t) bytes.
+ * Supported: 8 <= C_z <= 128, H_t a multiple of 64, either dtype.  bf16 with
+ * C_z = 128 and H_t a multiple of 128 runs the pair cells on the tcgen05
+ * tensor cores: LN(z) and dP~ as bf16 rows, H = ReLU(LN(z) W1^T + b1),
+ * dA = (dP~ W2) where H > 0 and dY = dA W1 as GEMMs, dW1 = dA^T LN(z) and
+ * dW2 = dP~^T H (with db1, db2) split over the cells and summed in a fixed
+ * order; the GEMM operands are bf16, every accumulation fp32.  Otherwise
+ * CUDA cores in fp32.  dgamma, dbeta and the single-row gradients
+ * accumulate with fp32 atomics, so they are not bit-reproducible from run
+ * to run.  Asynchronous.
  */
 nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const void* s, int32_t C_s,
                                  const void* W_a, const void* W_b, int32_t C_z, int32_t H_t, const float* ln_gamma,

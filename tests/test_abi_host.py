@@ -57,6 +57,21 @@ def test_workspace_bytes(L):
     assert L.nt_pair_broadcast_workspace_bytes(-1, 128) == 0
 
 
+def test_block_backward_workspace_bytes():
+    """The CUDA-core route needs (5 T + P) C_z fp32 words (rounded up to 256
+    bytes); the bf16 tensor-core route (C_z = 128, H_t % 128 == 0) adds its
+    cell rows: [hi | lo] LN(z) and dP~ ([P, C_z] bf16-sized), H and dA
+    ([P, H_t] bf16 each) and the per-cell statistics, so at least that."""
+    from variable_length_batching_gb300 import nt
+    T, P, C, H = 1031, 157023, 128, 512
+    base = -(-(5 * T + P) * C * 4 // 256) * 256
+    assert nt.nt_pair_block_backward_workspace_bytes(nt.NT_F32, T, P, C, H) == base
+    assert nt.nt_pair_block_backward_workspace_bytes(nt.NT_BF16, T, P, 64, 256) == -(-(5 * T + P) * 64 * 4 // 256) * 256
+    tc = nt.nt_pair_block_backward_workspace_bytes(nt.NT_BF16, T, P, C, H)
+    assert tc >= base + P * (2 * C * 2 + C * 2 + 2 * H * 2 + 8)
+    assert nt.nt_pair_block_backward_workspace_bytes(nt.NT_BF16, -1, P, C, H) == 0
+
+
 def test_host_side_rejections(L):
     """Calls that must fail on argument checks alone (nothing reaches CUDA)."""
     from variable_length_batching_gb300 import nt

@@ -70,6 +70,30 @@ def test_block_backward_bf16(nt, lengths, biases):
     _check(*_run(nt, wl.PAIRFORMER_BF16, lengths, biases))
 
 
+def test_block_backward_bf16_cuda_core_route(nt):
+    """bf16 at C_z = 64 (not the tensor-core route's 128): the CUDA-core
+    kernels, against the oracle."""
+    import dataclasses
+    cfg = dataclasses.replace(wl.PAIRFORMER_BF16, name="bf16_Cz64", C_s=128, C_z=64, H_t=256)
+    _check(*_run(nt, cfg, [40, 3, 0, 25], True))
+
+
+def test_tensor_core_weight_gradients_reproducible(nt):
+    """dW1, db1, dW2 and db2 of the tensor-core route are summed over fixed
+    cell splits in a fixed order: two calls give the same bits."""
+    inp = wl.make_block_inputs(wl.PAIRFORMER_BF16)
+    w = _dw(inp.blocks[0])
+    part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(DEV))
+    s = inp.s.to(DEV)
+    z, m, s_out = nt.block_forward(part, s, w)
+    _, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z)
+    g1 = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
+    g2 = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
+    torch.cuda.synchronize()
+    for n in ("dW1", "db1", "dW2", "db2"):
+        assert torch.equal(g1[n], g2[n]), n
+
+
 def test_block_backward_pairformer_batch(nt):
     """The B=8 Pairformer-style batch itself (N_i ~ U[64, 256], P = 157,023)."""
     _check(*_run(nt, wl.PAIRFORMER_BF16, None, False))

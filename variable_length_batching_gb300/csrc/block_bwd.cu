@@ -18,6 +18,17 @@
 // z is rebuilt from u = s W_a^T and v = s W_b^T, rounded to the I/O dtype as
 // the forward rounds it.  Square partitions only.
 //
+// bf16 with C_z = 128 and H_t a multiple of 128 takes the pair-cell part on
+// the tensor cores, through the cells' row-major intermediates:
+//   bwd_prep      per cell: LN(z) and dP~ as bf16 rows, the LayerNorm's mean
+//                 and rstd
+//   tcgen05 GEMMs H = ReLU(LN(z) W1^T + b1), dA = (dP~ W2) where H > 0,
+//                 dY = dA W1 (linear_tc), dW1 = dA^T LN(z), dW2 = dP~^T H,
+//                 db1, db2 (wgrad_tc: split over the cells)
+//   bwd_ln        per cell: the LayerNorm backward -> dz; dgamma, dbeta
+// The GEMM operands are bf16 (dP~ and dA rounded once); every accumulation
+// is fp32.  fp32 I/O and other widths run the CUDA-core kernels below.
+//
 // Kernels:
 //   eq5_partial / eq5_finish     the loss (per pair row, fixed-order final sum)
 //                                and, optionally, its gradients dX~, dP~
@@ -29,7 +40,7 @@
 //                                 dgamma, dbeta, db2
 //   trans_bwd_weights             per (hidden chunk, cell range): dW1, dW2, db1
 //   pair_rowcol_sum               du (row sums) and dv (column sums) of dz
-#include "nt_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace nt {
 namespace {
@@ -524,8 +535,10 @@ size_t cell_smem(int C, bool weights) {
   return sizeof(float) * (weights ? base + (size_t)kTC * C + (size_t)kTC * kHC : base);
 }
 
+cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* status, cudaStream_t s);
+
 template <typename T>
-cudaError_t block_backward_t(const BlockBwd& q, cudaStream_t s) {
+cudaError_t block_backward_t(const BlockBwd& q, unsigned int* status, cudaStream_t s) {
   const nt_partition* p = q.part;
   const int C = q.C_z, Cs = q.C_s;
   const int64_t Trows = p->T;
@@ -543,7 +556,9 @@ cudaError_t block_backward_t(const BlockBwd& q, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // the pair cells: dz, dgamma, dbeta, db2, then dW1, dW2, db1
-  if (p->P > 0) {
+  if (p->P > 0 && q.tc_ws) {
+    if ((e = cells_backward_tc(q, static_cast<uint8_t*>(q.tc_ws), status, s)) != cudaSuccess) return e;
+  } else if (p->P > 0) {
     CellArgs<T> a = {q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, p->P, C, q.H_t, q.gamma, q.beta,
                      q.eps, (const T*)q.W1, q.b1, (const T*)q.W2, q.dM, q.dz_up};
     const size_t sm1 = cell_smem(C, false), sm2 = cell_smem(C, true);
@@ -576,9 +591,278 @@ cudaError_t block_backward_t(const BlockBwd& q, cudaStream_t s) {
   return cudaSuccess;
 }
 
+
+// ------------------------------------------------ the tensor-core route (bf16)
+
+using tc::pack_bf16x2;
+
+constexpr int kTcC = 128;          // pair width of the tensor-core route
+constexpr int kPrepCells = kThreads / 8;   // cells per CTA pass: 8 threads x 16 features each
+
+// Rows of the route: per cell p, 8 threads own features 16 q .. 16 q + 15.
+// LN(z) as two bf16 parts, hi = bf16(y) and lo = bf16(y - hi), side by side
+// in a row of 2 C_z (A = [hi | lo] [W1 | W1]^T carries y to about 16 bits,
+// so A's sign, the ReLU's decision, is that of the fp32 y); dP~ = dz_up +
+// dM[row] / N as bf16; the LayerNorm's mean and rstd of the rebuilt z
+// (bf16-rounded as in the forward).
+__global__ void __launch_bounds__(kThreads)
+bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
+                const int32_t* __restrict__ cu, const int32_t* __restrict__ len, int B, int64_t P,
+                const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
+                const float* __restrict__ dM, const float* __restrict__ dz_up, bf16* __restrict__ Y,
+                bf16* __restrict__ dPt, float2* __restrict__ stats) {
+  const int q = threadIdx.x & 7;
+  for (int64_t p = (int64_t)blockIdx.x * kPrepCells + (threadIdx.x >> 3); p - (threadIdx.x >> 3) < P;
+       p += (int64_t)gridDim.x * kPrepCells) {
+    const bool valid = p < P;
+    int64_t row = 0, col = 0;
+    int n = 1;
+    if (valid) cell_coords(pair_off, cu, len, B, p, row, col, n);
+    float z[16];
+    float s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (valid) {
+        a = *reinterpret_cast<const float4*>(u + row * kTcC + 16 * q + j);
+        b = *reinterpret_cast<const float4*>(v + col * kTcC + 16 * q + j);
+      }
+      z[j] = round_io(a.x + b.x, (bf16*)nullptr);
+      z[j + 1] = round_io(a.y + b.y, (bf16*)nullptr);
+      z[j + 2] = round_io(a.z + b.z, (bf16*)nullptr);
+      z[j + 3] = round_io(a.w + b.w, (bf16*)nullptr);
+      s1 += (z[j] + z[j + 1]) + (z[j + 2] + z[j + 3]);
+    }
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 4);
+    const float mean = s1 * (1.0f / kTcC);
+    float s2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float d = z[j] - mean;
+      s2 = fmaf(d, d, s2);
+    }
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
+    const float rs = rsqrtf(s2 * (1.0f / kTcC) + eps);
+    if (!valid) continue;
+    const float inv_n = 1.0f / (float)n;
+    uint32_t yw[8], lw[8], gw[8];
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const int f = 16 * q + j;
+      const float y0 = fmaf((z[j] - mean) * rs, gamma[f], beta[f]);
+      const float y1 = fmaf((z[j + 1] - mean) * rs, gamma[f + 1], beta[f + 1]);
+      const float h0 = round_io(y0, (bf16*)nullptr), h1 = round_io(y1, (bf16*)nullptr);
+      lw[j / 2] = pack_bf16x2(y0 - h0, y1 - h1);
+      float g0 = dM[row * kTcC + f] * inv_n, g1 = dM[row * kTcC + f + 1] * inv_n;
+      if (dz_up) {
+        g0 += dz_up[p * kTcC + f];
+        g1 += dz_up[p * kTcC + f + 1];
+      }
+      yw[j / 2] = pack_bf16x2(y0, y1);
+      gw[j / 2] = pack_bf16x2(g0, g1);
+    }
+    uint4* yo = reinterpret_cast<uint4*>(Y + p * 2 * kTcC + 16 * q);
+    uint4* lo = reinterpret_cast<uint4*>(Y + p * 2 * kTcC + kTcC + 16 * q);
+    uint4* go = reinterpret_cast<uint4*>(dPt + p * kTcC + 16 * q);
+    yo[0] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+    yo[1] = make_uint4(yw[4], yw[5], yw[6], yw[7]);
+    lo[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    lo[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+    go[0] = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+    go[1] = make_uint4(gw[4], gw[5], gw[6], gw[7]);
+    if (q == 0) stats[p] = make_float2(mean, rs);
+  }
+}
+
+// The LayerNorm backward per cell, in place: dY (fp32, from the GEMM) in
+// the dz buffer becomes dz = dP~ + (dxhat - mean(dxhat) - xhat mean(dxhat
+// xhat)) rstd, dxhat = dY gamma, with x-hat of the rebuilt z and dP~ exact
+// in fp32.  dgamma += dY xhat and dbeta += dY, reduced over the CTA's cells
+// then added atomically.
+__global__ void __launch_bounds__(kThreads)
+bwd_ln_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
+              const int32_t* __restrict__ cu, const int32_t* __restrict__ len, int B, int64_t P,
+              const float* __restrict__ gamma, const float2* __restrict__ stats, const float* __restrict__ dM,
+              const float* __restrict__ dz_up, float* __restrict__ dz, float* __restrict__ dgamma,
+              float* __restrict__ dbeta) {
+  __shared__ float red[2][kTcC];
+  const int q = threadIdx.x & 7, slot = threadIdx.x >> 3;
+  float pg[16], pb[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) { pg[j] = 0.f; pb[j] = 0.f; }
+  for (int64_t p = (int64_t)blockIdx.x * kPrepCells + slot; p - slot < P; p += (int64_t)gridDim.x * kPrepCells) {
+    const bool valid = p < P;
+    int64_t row = 0, col = 0;
+    int n = 1;
+    float2 st = make_float2(0.f, 0.f);
+    if (valid) {
+      cell_coords(pair_off, cu, len, B, p, row, col, n);
+      st = stats[p];
+    }
+    float xh[16], dy[16];
+    float m1 = 0.f, m2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, g = a;
+      if (valid) {
+        a = *reinterpret_cast<const float4*>(u + row * kTcC + 16 * q + j);
+        b = *reinterpret_cast<const float4*>(v + col * kTcC + 16 * q + j);
+        g = *reinterpret_cast<const float4*>(dz + p * kTcC + 16 * q + j);
+      }
+      const float za[4] = {a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w};
+      const float ga[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        xh[j + e] = valid ? (round_io(za[e], (bf16*)nullptr) - st.x) * st.y : 0.f;
+        dy[j + e] = ga[e];
+        const float dx = ga[e] * gamma[16 * q + j + e];
+        m1 += dx;
+        m2 = fmaf(dx, xh[j + e], m2);
+      }
+    }
+    m1 += __shfl_xor_sync(0xffffffffu, m1, 1);
+    m1 += __shfl_xor_sync(0xffffffffu, m1, 2);
+    m1 += __shfl_xor_sync(0xffffffffu, m1, 4);
+    m2 += __shfl_xor_sync(0xffffffffu, m2, 1);
+    m2 += __shfl_xor_sync(0xffffffffu, m2, 2);
+    m2 += __shfl_xor_sync(0xffffffffu, m2, 4);
+    if (!valid) continue;
+    m1 *= 1.0f / kTcC;
+    m2 *= 1.0f / kTcC;
+    const float inv_n = 1.0f / (float)n;
+    float out[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int f = 16 * q + j;
+      const float dx = dy[j] * gamma[f];
+      float g = dM[row * kTcC + f] * inv_n;
+      if (dz_up) g += dz_up[p * kTcC + f];
+      out[j] = g + (dx - m1 - xh[j] * m2) * st.y;
+      pg[j] = fmaf(dy[j], xh[j], pg[j]);
+      pb[j] += dy[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 16; j += 4)
+      *reinterpret_cast<float4*>(dz + p * kTcC + 16 * q + j) = make_float4(out[j], out[j + 1], out[j + 2], out[j + 3]);
+  }
+  // features 16 q + j: summed over the CTA's cell slots in shared memory,
+  // then one global atomic per feature
+  if (threadIdx.x < 2 * kTcC) red[threadIdx.x / kTcC][threadIdx.x % kTcC] = 0.f;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    atomicAdd(&red[0][16 * q + j], pg[j]);
+    atomicAdd(&red[1][16 * q + j], pb[j]);
+  }
+  __syncthreads();
+  if (threadIdx.x < kTcC) {
+    atomicAdd(dgamma + threadIdx.x, red[0][threadIdx.x]);
+    atomicAdd(dbeta + threadIdx.x, red[1][threadIdx.x]);
+  }
+}
+
+// out[c][r] = in[r][c] for a bf16 [R, Cc] matrix (the weights, once per call).
+__global__ void transpose_bf16_kernel(const bf16* __restrict__ in, int R, int Cc, bf16* __restrict__ out) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < (int64_t)R * Cc;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(e / Cc), c = (int)(e % Cc);
+    out[(int64_t)c * R + r] = in[e];
+  }
+}
+
+// out[r] = [in[r] | in[r]] for a bf16 [R, Cc] matrix: W1 beside itself.
+__global__ void twice_bf16_kernel(const bf16* __restrict__ in, int R, int Cc, bf16* __restrict__ out) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < (int64_t)R * Cc;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / Cc, c = e % Cc;
+    out[r * 2 * Cc + c] = in[e];
+    out[r * 2 * Cc + Cc + c] = in[e];
+  }
+}
+
+// Byte offsets of the route's buffers in the workspace past the CUDA-core
+// route's (each 256-byte aligned).
+struct TcLayout {
+  size_t Y, dPt, H, dA, stats, W1t, W2t, W1x2, wg, end;
+};
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+TcLayout tc_layout(int64_t P, int C, int H) {
+  TcLayout L;
+  size_t o = 0;
+  L.Y = o; o = align256(o + (size_t)P * 2 * C * 2);   // [hi | lo] rows
+  L.dPt = o; o = align256(o + (size_t)P * C * 2);
+  L.H = o; o = align256(o + (size_t)P * H * 2);
+  L.dA = o; o = align256(o + (size_t)P * H * 2);
+  L.stats = o; o = align256(o + (size_t)P * 8);
+  L.W1t = o; o = align256(o + (size_t)C * H * 2);
+  L.W2t = o; o = align256(o + (size_t)C * H * 2);
+  L.W1x2 = o; o = align256(o + (size_t)2 * C * H * 2);
+  L.wg = o;
+  const size_t w1 = wgrad_tc_workspace_bytes(P, H, C), w2 = wgrad_tc_workspace_bytes(P, C, H);
+  o = align256(o + (w1 > w2 ? w1 : w2));
+  L.end = o;
+  return L;
+}
+
+cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* status, cudaStream_t s) {
+  const nt_partition* p = q.part;
+  const int C = q.C_z, H = q.H_t;
+  const int64_t P = p->P;
+  const TcLayout L = tc_layout(P, C, H);
+  bf16* Y = reinterpret_cast<bf16*>(tcw + L.Y);
+  bf16* dPt = reinterpret_cast<bf16*>(tcw + L.dPt);
+  bf16* Hm = reinterpret_cast<bf16*>(tcw + L.H);
+  bf16* dA = reinterpret_cast<bf16*>(tcw + L.dA);
+  float2* stats = reinterpret_cast<float2*>(tcw + L.stats);
+  bf16* W1t = reinterpret_cast<bf16*>(tcw + L.W1t);
+  bf16* W2t = reinterpret_cast<bf16*>(tcw + L.W2t);
+  bf16* W1x2 = reinterpret_cast<bf16*>(tcw + L.W1x2);
+  void* wg = tcw + L.wg;
+  const int gcells = (int)min64((P + kPrepCells - 1) / kPrepCells, (int64_t)sm_count() * 8);
+  const unsigned gt = (unsigned)min64(((int64_t)C * H + 255) / 256, 1024);
+  transpose_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W1, H, C, W1t);   // W1 [H, C] -> [C, H]
+  transpose_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W2, C, H, W2t);   // W2 [C, H] -> [H, C]
+  twice_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W1, H, C, W1x2);       // [W1 | W1], [H, 2C]
+  bwd_prep_kernel<<<gcells, kThreads, 0, s>>>(q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, P, q.gamma,
+                                              q.beta, q.eps, q.dM, q.dz_up, Y, dPt, stats);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // H = ReLU([hi | lo] [W1 | W1]^T + b1); dA = (dP~ W2) where H > 0; dY = dA W1 (into the dz buffer)
+  LinearProblem g1 = {Y, W1x2, q.b1, nullptr, Hm};
+  g1.epi = kEpiRelu;
+  if ((e = launch_linear_tc(0, &g1, 1, P, H, 2 * C, status, s)) != cudaSuccess) return e;
+  LinearProblem g2 = {dPt, W2t, nullptr, Hm, dA};
+  g2.epi = kEpiMask;
+  if ((e = launch_linear_tc(0, &g2, 1, P, H, C, status, s)) != cudaSuccess) return e;
+  LinearProblem g3 = {dA, W1t, nullptr, nullptr, q.dz};
+  if ((e = launch_linear_tc(1, &g3, 1, P, C, H, status, s)) != cudaSuccess) return e;
+  // dz, dgamma, dbeta
+  bwd_ln_kernel<<<gcells, kThreads, 0, s>>>(q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, P, q.gamma,
+                                            stats, q.dM, q.dz_up, q.dz, q.dgamma, q.dbeta);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // dW1 = dA^T LN(z) (the hi part, every other C_z block of the rows), db1 =
+  // sum dA; dW2 = dP~^T H, db2 = sum dP~
+  if ((e = launch_wgrad_tc(dA, H, Y, 2 * C, P, H, C, q.dW1, q.db1, wg, status, s)) != cudaSuccess) return e;
+  return launch_wgrad_tc(dPt, C, Hm, H, P, C, H, q.dW2, q.db2, wg, status, s);
+}
+
 }  // namespace
 
 bool block_bwd_supported(int C_z, int H_t) { return C_z >= 8 && C_z <= kCmax && H_t >= kHC && H_t % kHC == 0; }
+
+bool block_bwd_tc(nt_dtype dt, int64_t P, int C_z, int H_t) {
+  return dt == NT_BF16 && C_z == kTcC && H_t % 128 == 0 && P > 0 && linear_tc_supported(NT_BF16, P, H_t, C_z) &&
+         linear_tc_supported(NT_BF16, P, C_z, H_t) && wgrad_tc_supported(P, H_t, C_z);
+}
+
+size_t block_bwd_workspace_bytes(nt_dtype dt, int64_t T, int64_t P, int C_z, int H_t) {
+  const size_t base = align256((size_t)(5 * T + P) * (size_t)C_z * sizeof(float));
+  return block_bwd_tc(dt, P, C_z, H_t) ? base + tc_layout(P, C_z, H_t).end : base;
+}
 
 cudaError_t launch_eq5_loss(nt_dtype dt, const nt_partition* p, const void* s_out, int C_s, const void* zt, int C_z,
                             float* loss, float* ds_out, float* dz, void* workspace, cudaStream_t s) {
@@ -590,8 +874,8 @@ cudaError_t launch_eq5_loss(nt_dtype dt, const nt_partition* p, const void* s_ou
 
 size_t eq5_loss_workspace_bytes() { return sizeof(double) * 2 * kLossBlocks; }
 
-cudaError_t launch_block_backward(nt_dtype dt, const BlockBwd& q, cudaStream_t s) {
-  return dt == NT_BF16 ? block_backward_t<bf16>(q, s) : block_backward_t<float>(q, s);
+cudaError_t launch_block_backward(nt_dtype dt, const BlockBwd& q, unsigned int* status, cudaStream_t s) {
+  return dt == NT_BF16 ? block_backward_t<bf16>(q, status, s) : block_backward_t<float>(q, status, s);
 }
 
 }  // namespace nt

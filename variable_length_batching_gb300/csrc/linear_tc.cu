@@ -35,8 +35,9 @@ struct Bars {
 
 struct Prob {
   const float* bias;
-  const bf16* R;     // residual [M, N] or null
+  const bf16* R;     // residual (or, with kEpiMask, the mask) [M, N], or null
   void* Y;           // [M, N], fp32 or bf16
+  int epi;           // kEpiPlain, kEpiRelu or kEpiMask
 };
 
 template <bool kOutF32>
@@ -126,11 +127,26 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
       tmem_ld_wait();
       if (row < M) {
         const int c0 = n0 + 32 * g;
-        if (pr.bias) {
+        if (pr.bias && pr.epi != kEpiMask) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] += pr.bias[c0 + c];
         }
-        if (has_r) {
+        if (pr.epi == kEpiRelu) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = fmaxf(v[c], 0.f);
+        } else if (pr.epi == kEpiMask && has_r) {
+          // keep the entries whose mask element is positive
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 q4 = res[4 * g + u];
+            const uint32_t w[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (!(bf16lo(w[e]) > 0.f)) v[8 * u + 2 * e] = 0.f;
+              if (!(bf16hi(w[e]) > 0.f)) v[8 * u + 2 * e + 1] = 0.f;
+            }
+          }
+        } else if (has_r) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint4 q4 = res[4 * g + u];
@@ -185,7 +201,7 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
     if (!make_tmap_rows(&tx[i], lp.X, (uint64_t)K, (uint64_t)M, kBM) ||
         !make_tmap_rows(&tw[i], lp.W, (uint64_t)K, (uint64_t)N, kBN))
       return cudaErrorInvalidValue;
-    pp[i] = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y};
+    pp[i] = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y, lp.epi};
   }
   dim3 grid((unsigned)((M + kBM - 1) / kBM), N / kBN, nprob);
   const int stages = min(K / kBK, kMaxStages);

@@ -654,9 +654,9 @@ nt_status nt_pair_block_loss(const nt_partition* part, nt_dtype dtype, const voi
   return NT_OK;
 }
 
-size_t nt_pair_block_backward_workspace_bytes(int64_t T, int64_t P, int32_t C_z) {
-  if (T < 0 || P < 0 || C_z < 0) return 0;
-  return (size_t)(5 * T + P) * (size_t)C_z * sizeof(float);
+size_t nt_pair_block_backward_workspace_bytes(nt_dtype dtype, int64_t T, int64_t P, int32_t C_z, int32_t H_t) {
+  if (T < 0 || P < 0 || C_z < 0 || H_t < 0) return 0;
+  return block_bwd_workspace_bytes(dtype, T, P, C_z, H_t);
 }
 
 nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const void* s, int32_t C_s,
@@ -682,7 +682,7 @@ nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const
                         dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g, workspace};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
-  const size_t need = nt_pair_block_backward_workspace_bytes(part->T, part->P, C_z);
+  const size_t need = nt_pair_block_backward_workspace_bytes(dtype, part->T, part->P, C_z, H_t);
   if (workspace_bytes < need) return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
   cudaStream_t st_ = static_cast<cudaStream_t>(stream);
   // the gradients that are sums start at zero
@@ -704,9 +704,14 @@ nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const
   float* dz = dv + part->T * (int64_t)C_z;
   cudaError_t e = project_uv(part, dtype, s, s, C_s, W_a, W_b, C_z, u, v, st_);
   if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+  // the tensor-core route's buffers follow the CUDA-core route's
+  const size_t base = ((size_t)(5 * part->T + part->P) * (size_t)C_z * sizeof(float) + 255) & ~(size_t)255;
+  void* tc_ws = block_bwd_tc(dtype, part->P, C_z, H_t) ? static_cast<uint8_t*>(workspace) + base : nullptr;
   BlockBwd q = {part, C_s, C_z, H_t, s, W_a, W_b, ln_gamma, ln_beta, ln_eps, W1, b1, W2, W_g, m, ds_out, dz_tilde,
-                ds, dW_a, dW_b, dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g, u, v, dM, dz, du, dv};
-  e = launch_block_backward(dtype, q, st_);
+                ds, dW_a, dW_b, dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g, u, v, dM, dz, du, dv, tc_ws};
+  unsigned int* status = status_word();
+  if (!status) return fail(NT_ERR_CUDA, "device status word unavailable");
+  e = launch_block_backward(dtype, q, status, st_);
   if (e != cudaSuccess) return cuda_fail(e, "block backward launch");
   return NT_OK;
 }

@@ -143,7 +143,12 @@ cudaError_t launch_partition_fused(const int32_t* lengths, int32_t B, int64_t ca
 // problems in one launch (gridDim.z); all row-major, contiguous.
 struct LinearProblem {
   const void* X; const void* W; const float* bias; const void* R; void* Y;
+  // epilogue of the tcgen05 path: kEpiPlain  Y = acc (+ bias) (+ R);
+  // kEpiRelu  Y = max(acc + bias, 0); kEpiMask  Y = acc where R > 0, else 0
+  // (R a bf16 [M, N] tensor; no bias)
+  int epi = 0;
 };
+constexpr int kEpiPlain = 0, kEpiRelu = 1, kEpiMask = 2;
 cudaError_t launch_linear(int in_dtype /*nt_dtype of X, W, R*/, int out_f32 /*Y fp32?*/,
                           const LinearProblem* probs, int nprob, int64_t M, int N, int K,
                           cudaStream_t s);
@@ -279,9 +284,24 @@ struct BlockBwd {
   float* dz;
   float* du;
   float* dv;
+  // the tensor-core route's buffers (bf16, C_z = 128, H_t % 128 == 0), else null
+  void* tc_ws;
 };
 bool block_bwd_supported(int C_z, int H_t);
-cudaError_t launch_block_backward(nt_dtype dt, const BlockBwd& q, cudaStream_t s);
+// Whether the pair-cell part runs on the tensor cores, and the workspace the
+// backward needs: (5 T + P) C_z fp32 words, plus the route's cell rows.
+bool block_bwd_tc(nt_dtype dt, int64_t P, int C_z, int H_t);
+size_t block_bwd_workspace_bytes(nt_dtype dt, int64_t T, int64_t P, int C_z, int H_t);
+cudaError_t launch_block_backward(nt_dtype dt, const BlockBwd& q, unsigned int* status, cudaStream_t s);
+
+// Weight gradients over the cells on the tensor cores: G[M, N] = A^T B and
+// optionally colsum[M] = sum of A's rows, A [P, M] and B [P, N] bf16
+// row-major with rows lda and ldb elements apart (multiples of 8), G and
+// colsum fp32 (written, not added to); M, N multiples of 128.
+bool wgrad_tc_supported(int64_t P, int M, int N);
+size_t wgrad_tc_workspace_bytes(int64_t P, int M, int N);
+cudaError_t launch_wgrad_tc(const void* A, int lda, const void* B, int ldb, int64_t P, int M, int N, float* G,
+                            float* colsum, void* workspace, unsigned int* status, cudaStream_t s);
 
 bool attn_simt_supported(int d);
 cudaError_t launch_attn_simt(nt_dtype dt, const AttnProblem& p, unsigned int* status, cudaStream_t s);

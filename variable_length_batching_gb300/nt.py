@@ -61,7 +61,7 @@ SIGNATURES = {
                                    _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "nt_pair_block_loss_workspace_bytes": (_SZ, []),
     "nt_pair_block_loss": (_I32, [_PP, _I32, _P, _I32, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
-    "nt_pair_block_backward_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
+    "nt_pair_block_backward_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I32, _I32]),
     "nt_pair_block_backward": (_I32, [_PP, _I32, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "nt_varlen_attn_workspace_bytes": (_SZ, []),
@@ -383,7 +383,7 @@ def nt_pair_block_backward(part: Partition, s: torch.Tensor, w, m: torch.Tensor,
     f = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=dev)
     g = {"ds": f(T, C_s), "dW_a": f(C_z, C_s), "dW_b": f(C_z, C_s), "dgamma": f(C_z), "dbeta": f(C_z),
          "dW1": f(H_t, C_z), "db1": f(H_t), "dW2": f(C_z, H_t), "db2": f(C_z), "dW_g": f(C_s, C_z), "db_g": f(C_s)}
-    need = int(lib().nt_pair_block_backward_workspace_bytes(part.T, part.P, C_z))
+    need = nt_pair_block_backward_workspace_bytes(_dtype(s), part.T, part.P, C_z, H_t)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     st = lib().nt_pair_block_backward(
@@ -394,6 +394,11 @@ def nt_pair_block_backward(part: Partition, s: torch.Tensor, w, m: torch.Tensor,
         _ptr(g["db_g"]), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nt_pair_block_backward")
     return g
+
+
+def nt_pair_block_backward_workspace_bytes(dtype: int, T: int, P: int, C_z: int, H_t: int) -> int:
+    """Device workspace bytes of nt_pair_block_backward (dtype: NT_F32 / NT_BF16 code)."""
+    return int(lib().nt_pair_block_backward_workspace_bytes(int(dtype), int(T), int(P), int(C_z), int(H_t)))
 
 
 def nt_varlen_attn_workspace_bytes() -> int:
