@@ -68,6 +68,21 @@ __device__ __forceinline__ void cell_coords(const int64_t* __restrict__ pair_off
   col = cu[lo] + (off - a * n);
 }
 
+// 16 bytes of the I/O dtype as fp32: 8 bf16 or 4 fp32 values.
+__device__ __forceinline__ void load_vec(const bf16* p, float* x) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load_vec(const float* p, float* x) {
+  const float4 q = *reinterpret_cast<const float4*>(p);
+  x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+}
+
 __device__ __forceinline__ float round_io(float x, float*) { return x; }
 __device__ __forceinline__ float round_io(float x, bf16*) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
@@ -94,12 +109,21 @@ eq5_partial_kernel(const T* __restrict__ s_out, const T* __restrict__ zt, const 
       if (ds_out) ds_out[r * C + k] = gx * x;
     }
     ax += alpha * sx;
+    // the row's cells: 16-byte loads (Cp is a multiple of 16 bytes' worth of
+    // elements, so every row starts on a 16-byte boundary)
+    constexpr int V = 16 / sizeof(T);
     const int64_t c0 = row_start[r] * Cp, c1 = row_start[r + 1] * Cp;
     float sp = 0.f;
-    for (int64_t e = c0 + threadIdx.x; e < c1; e += kThreads) {
-      const float x = to_f32(zt[e]);
-      sp += x * x;
-      if (dz) dz[e] = gp * x;
+    for (int64_t e = c0 + (int64_t)threadIdx.x * V; e < c1; e += (int64_t)kThreads * V) {
+      float x[V];
+      load_vec(zt + e, x);
+#pragma unroll
+      for (int i = 0; i < V; ++i) sp = fmaf(x[i], x[i], sp);
+      if (dz) {
+#pragma unroll
+        for (int i = 0; i < V; i += 4)
+          *reinterpret_cast<float4*>(dz + e + i) = make_float4(gp * x[i], gp * x[i + 1], gp * x[i + 2], gp * x[i + 3]);
+      }
     }
     ap += beta * sp;
   }
@@ -649,6 +673,17 @@ bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const 
     const float rs = rsqrtf(s2 * (1.0f / kTcC) + eps);
     if (!valid) continue;
     const float inv_n = 1.0f / (float)n;
+    float gv[16];
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      const float4 m4 = *reinterpret_cast<const float4*>(dM + row * kTcC + 16 * q + j);
+      float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (dz_up) u4 = *reinterpret_cast<const float4*>(dz_up + p * kTcC + 16 * q + j);
+      gv[j] = fmaf(m4.x, inv_n, u4.x);
+      gv[j + 1] = fmaf(m4.y, inv_n, u4.y);
+      gv[j + 2] = fmaf(m4.z, inv_n, u4.z);
+      gv[j + 3] = fmaf(m4.w, inv_n, u4.w);
+    }
     uint32_t yw[8], lw[8], gw[8];
 #pragma unroll
     for (int j = 0; j < 16; j += 2) {
@@ -657,11 +692,7 @@ bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const 
       const float y1 = fmaf((z[j + 1] - mean) * rs, gamma[f + 1], beta[f + 1]);
       const float h0 = round_io(y0, (bf16*)nullptr), h1 = round_io(y1, (bf16*)nullptr);
       lw[j / 2] = pack_bf16x2(y0 - h0, y1 - h1);
-      float g0 = dM[row * kTcC + f] * inv_n, g1 = dM[row * kTcC + f + 1] * inv_n;
-      if (dz_up) {
-        g0 += dz_up[p * kTcC + f];
-        g1 += dz_up[p * kTcC + f + 1];
-      }
+      const float g0 = gv[j], g1 = gv[j + 1];
       yw[j / 2] = pack_bf16x2(y0, y1);
       gw[j / 2] = pack_bf16x2(g0, g1);
     }
@@ -734,13 +765,23 @@ bwd_ln_kernel(const float* __restrict__ u, const float* __restrict__ v, const in
     m1 *= 1.0f / kTcC;
     m2 *= 1.0f / kTcC;
     const float inv_n = 1.0f / (float)n;
+    float gv[16];
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      const float4 m4 = *reinterpret_cast<const float4*>(dM + row * kTcC + 16 * q + j);
+      float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (dz_up) u4 = *reinterpret_cast<const float4*>(dz_up + p * kTcC + 16 * q + j);
+      gv[j] = fmaf(m4.x, inv_n, u4.x);
+      gv[j + 1] = fmaf(m4.y, inv_n, u4.y);
+      gv[j + 2] = fmaf(m4.z, inv_n, u4.z);
+      gv[j + 3] = fmaf(m4.w, inv_n, u4.w);
+    }
     float out[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int f = 16 * q + j;
       const float dx = dy[j] * gamma[f];
-      float g = dM[row * kTcC + f] * inv_n;
-      if (dz_up) g += dz_up[p * kTcC + f];
+      const float g = gv[j];
       out[j] = g + (dx - m1 - xh[j] * m2) * st.y;
       pg[j] = fmaf(dy[j], xh[j], pg[j]);
       pb[j] += dy[j];

@@ -57,8 +57,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
   Bars& bar = *reinterpret_cast<Bars*>(smem + stages * kStageBytes);
   volatile int* abort_flag = &bar.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t m0 = (int64_t)blockIdx.x * kBM;
-  const int n0 = blockIdx.y * kBN;
+  // the N tiles of one M tile are consecutive blocks, so they run together
+  // and read their X rows from L2 rather than each from HBM
+  const int ntiles = N / kBN;
+  const int64_t m0 = (int64_t)(blockIdx.x / ntiles) * kBM;
+  const int n0 = (int)(blockIdx.x % ntiles) * kBN;
   const int nkb = K / kBK;
 
   if (threadIdx.x == 0) {
@@ -203,7 +206,9 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
       return cudaErrorInvalidValue;
     pp[i] = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y, lp.epi};
   }
-  dim3 grid((unsigned)((M + kBM - 1) / kBM), N / kBN, nprob);
+  const int64_t blocks = (M + kBM - 1) / kBM * (N / kBN);
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)blocks, 1, nprob);
   const int stages = min(K / kBK, kMaxStages);
   const uint32_t smem = stages * kStageBytes + kBarBytes;
   cudaError_t e;
