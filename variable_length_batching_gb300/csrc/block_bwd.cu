@@ -141,12 +141,25 @@ eq5_partial_kernel(const T* __restrict__ s_out, const T* __restrict__ zt, const 
   }
 }
 
-// The partial sums in a fixed order, then Eq. 5's normalisations.
-__global__ void eq5_finish_kernel(const double* __restrict__ partial, int nblocks, int64_t Trows, int64_t P, int C,
-                                  int Cp, float* __restrict__ loss) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  double tx = 0.0, tp = 0.0;
-  for (int i = 0; i < nblocks; ++i) { tx += partial[2 * i]; tp += partial[2 * i + 1]; }
+// The partial sums in a fixed order (a pairwise tree over the partial
+// index, one block of kLossBlocks threads), then Eq. 5's normalisations.
+__global__ void __launch_bounds__(kLossBlocks)
+eq5_finish_kernel(const double* __restrict__ partial, int nblocks, int64_t Trows, int64_t P, int C, int Cp,
+                  float* __restrict__ loss) {
+  __shared__ double sx[kLossBlocks], sp[kLossBlocks];
+  const int i = threadIdx.x;
+  sx[i] = i < nblocks ? partial[2 * i] : 0.0;
+  sp[i] = i < nblocks ? partial[2 * i + 1] : 0.0;
+  __syncthreads();
+  for (int w = kLossBlocks / 2; w > 0; w >>= 1) {
+    if (i < w) {
+      sx[i] += sx[i + w];
+      sp[i] += sp[i + w];
+    }
+    __syncthreads();
+  }
+  if (i != 0) return;
+  const double tx = sx[0], tp = sp[0];
   double l = 0.0;
   if (Trows > 0) l += tx / ((double)C * Trows);
   if (P > 0) l += tp / ((double)Cp * P);
@@ -550,7 +563,7 @@ cudaError_t eq5_loss_t(const nt_partition* p, const void* s_out, int C_s, const 
                        float* ds_out, float* dz, double* partial, int nblocks, cudaStream_t s) {
   eq5_partial_kernel<T><<<nblocks, kThreads, 0, s>>>((const T*)s_out, (const T*)zt, p->row_start, p->row_sample,
                                                      p->B, p->T, p->P, C_s, C_z, partial, ds_out, dz);
-  eq5_finish_kernel<<<1, 32, 0, s>>>(partial, nblocks, p->T, p->P, C_s, C_z, loss);
+  eq5_finish_kernel<<<1, kLossBlocks, 0, s>>>(partial, nblocks, p->T, p->P, C_s, C_z, loss);
   return cudaGetLastError();
 }
 

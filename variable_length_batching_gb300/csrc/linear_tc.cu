@@ -3,14 +3,21 @@
 // block ("DanLing NestedTensor" Eq. 1; projections are V W^T + b, section
 // 3.3 "Dense work across valid positions") over the T packed single rows.
 //
-// One CTA per 128 x 64 output tile (and per problem: u and v run in one
-// launch).  Warp 0 streams 64-wide K blocks of X and W through a TMA ring
+// Small problems: one CTA per 128 x 64 output tile (and per problem: u and
+// v run in one launch).  Warp 0 streams 64-wide K blocks of X and W through a TMA ring
 // of up to six stages, warp 1 issues the MMAs into a 64-column TMEM
 // accumulator, and all four warps run the epilogue: TMEM -> +bias
 // (+residual) -> global.  The grids are small (tens of CTAs for the
 // block's projections), so each CTA's chain of copies sets the time: the
 // ring holds every K block of a C_s = 384 contraction at once, and one
 // round of copies replaces three.
+//
+// Large problems (the pair cells' GEMMs of the block backward, millions of
+// rows): persistent CTAs, two per SM, each walking 128 x 128 output tiles
+// (the N tiles of one row block consecutively, so they share its X rows in
+// L2) through one TMA ring that runs on across tiles, into two TMEM
+// accumulators used in turn: warps 2-5 write out one tile while warp 1
+// accumulates the next.
 #include "tc_ptx.cuh"
 
 namespace nt {
@@ -188,6 +195,181 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
   }
 }
 
+
+// ---------------------------------------------------------------- persistent
+
+constexpr int kPN = 128;                                  // output columns per tile
+constexpr int kPStages = 3;
+constexpr int kPThreads = 6 * 32;
+constexpr uint32_t kPXBytes = kBM * kBK * 2;              // 16 KB
+constexpr uint32_t kPWBytes = kPN * kBK * 2;              // 16 KB
+constexpr uint32_t kPStageBytes = kPXBytes + kPWBytes;
+constexpr uint32_t kPOffBar = kPStages * kPStageBytes;
+constexpr uint32_t kPSmemBytes = kPOffBar + 256 + 1024;
+constexpr uint32_t kPTmemCols = 2 * kPN;                  // two accumulators
+
+struct PBars {
+  uint64_t full[kPStages], empty[kPStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(PBars) <= 256, "barrier block");
+
+template <bool kOutF32>
+__global__ void __launch_bounds__(kPThreads)
+linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw, Prob pr,
+                            int64_t M, int N, int K, unsigned int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  PBars& bar = *reinterpret_cast<PBars*>(smem + kPOffBar);
+  volatile int* abort_flag = &bar.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = N / kPN, nkb = K / kBK;
+  const int64_t tiles = (M + kBM - 1) / kBM * ntiles;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPStages; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.acc_full[i], 1); mbar_init(&bar.acc_empty[i], 4); }
+    mbar_init(&bar.mma_done, 1);
+    bar.abort = 0;
+    fence_mbar_init();
+    fence_async_shared();
+  }
+  if (warp == 1) tmem_alloc(&bar.tmem_base, kPTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar.tmem_base;
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tx); prefetch_tmap(&tw);
+      int64_t g = 0;                              // k blocks issued, over all tiles
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m0 = (int)(t / ntiles) * kBM, n0 = (int)(t % ntiles) * kPN;
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int st = (int)(g % kPStages);
+          if (!(ok = mbar_wait(&bar.empty[st], (uint32_t)((g / kPStages) & 1) ^ 1, abort_flag, status))) break;
+          mbar_arrive_expect_tx(&bar.full[st], kPStageBytes);
+          tma_load_2d(smem + st * kPStageBytes, &tx, &bar.full[st], kb * kBK, m0);
+          tma_load_2d(smem + st * kPStageBytes + kPXBytes, &tw, &bar.full[st], kb * kBK, n0);
+        }
+      }
+      // drain the copies this thread issued
+      for (int64_t k = g - kPStages; k < g; ++k)
+        if (k >= 0) mbar_wait(&bar.full[k % kPStages], (uint32_t)((k / kPStages) & 1), nullptr, status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, kPN);
+      const uint32_t base = smem_u32(smem);
+      int64_t g = 0;
+      int i = 0;                                  // tiles of this CTA
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++i) {
+        const int b = i & 1;
+        // the accumulator is free once the epilogue has read tile i - 2 out of it
+        if (i >= 2 && !(ok = mbar_wait(&bar.acc_empty[b], (uint32_t)((i >> 1) - 1) & 1, abort_flag, status))) break;
+        tc_fence_after();
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int st = (int)(g % kPStages);
+          if (!(ok = mbar_wait(&bar.full[st], (uint32_t)((g / kPStages) & 1), abort_flag, status))) break;
+          tc_fence_after();
+          const uint32_t a = base + st * kPStageBytes, w = a + kPXBytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16(tmem + b * kPN, sdesc_k128(a + k * 32), sdesc_k128(w + k * 32), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar.empty[st]);
+        }
+        if (ok) mma_commit(&bar.acc_full[b]);
+      }
+      mma_commit(&bar.mma_done);
+      mbar_wait(&bar.mma_done, 0, nullptr, status);
+    }
+  } else {
+    // epilogue: row (warp & 3) * 32 + lane of each tile
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    int i = 0;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      const int64_t row = (t / ntiles) * kBM + r;
+      const int n0 = (int)(t % ntiles) * kPN;
+      const bool live = row < M;
+      // the row's residual or mask does not depend on the MMAs: its loads
+      // are issued before the accumulator wait
+      uint4 rall[kPN / 8];
+      if (pr.R && live) {
+        const uint4* rp = reinterpret_cast<const uint4*>(pr.R + row * N + n0);
+#pragma unroll
+        for (int u = 0; u < kPN / 8; ++u) rall[u] = rp[u];
+      }
+      if (!mbar_wait_warp(&bar.acc_full[b], (uint32_t)(i >> 1) & 1, abort_flag, status)) break;
+      tc_fence_after();
+      __syncwarp();
+#pragma unroll
+      for (int gq = 0; gq < kPN / 32; ++gq) {
+        const int c0 = n0 + 32 * gq;
+        const uint4* rq = rall + 4 * gq;
+        float v[32];
+        tmem_ld32_sync(tmem + lane_addr + b * kPN + 32 * gq, v);
+        if (!live) continue;
+        if (pr.bias && pr.epi != kEpiMask) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] += pr.bias[c0 + c];
+        }
+        if (pr.epi == kEpiRelu) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = fmaxf(v[c], 0.f);
+        } else if (pr.R) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t w[4] = {rq[u].x, rq[u].y, rq[u].z, rq[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (pr.epi == kEpiMask) {
+                if (!(bf16lo(w[e]) > 0.f)) v[8 * u + 2 * e] = 0.f;
+                if (!(bf16hi(w[e]) > 0.f)) v[8 * u + 2 * e + 1] = 0.f;
+              } else {
+                v[8 * u + 2 * e] += bf16lo(w[e]);
+                v[8 * u + 2 * e + 1] += bf16hi(w[e]);
+              }
+            }
+          }
+        }
+        if (kOutF32) {
+          float* y = static_cast<float*>(pr.Y) + row * N + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(y + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+        } else {
+          bf16* y = static_cast<bf16*>(pr.Y) + row * N + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 8)
+            *reinterpret_cast<uint4*>(y + c) = make_uint4(pack_bf16x2(v[c], v[c + 1]), pack_bf16x2(v[c + 2], v[c + 3]),
+                                                          pack_bf16x2(v[c + 4], v[c + 5]), pack_bf16x2(v[c + 6], v[c + 7]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar.acc_empty[b]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kPTmemCols);
+  }
+}
+
 }  // namespace
 
 bool linear_tc_supported(int in_dtype, int64_t M, int N, int K) {
@@ -197,6 +379,23 @@ bool linear_tc_supported(int in_dtype, int64_t M, int N, int K) {
 cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob, int64_t M, int N, int K,
                              unsigned int* status, cudaStream_t s) {
   if (M == 0 || nprob == 0) return cudaSuccess;
+  const int64_t ptiles = (M + kBM - 1) / kBM * (N / kPN);
+  if (nprob == 1 && N % kPN == 0 && ptiles >= (int64_t)8 * sm_count()) {
+    // large: persistent CTAs, two per SM
+    const LinearProblem& lp = probs[0];
+    CUtensorMap px, pw;
+    if (!make_tmap_rows(&px, lp.X, (uint64_t)K, (uint64_t)M, kBM) ||
+        !make_tmap_rows(&pw, lp.W, (uint64_t)K, (uint64_t)N, kPN))
+      return cudaErrorInvalidValue;
+    const Prob pp0 = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y, lp.epi};
+    const int grid = (int)min64(ptiles, (int64_t)2 * sm_count());
+    auto kern = out_f32 ? linear_tc_persistent_kernel<true> : linear_tc_persistent_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, dim3(grid), dim3(kPThreads), kPSmemBytes, s, px, pw, pp0, M, N, K, status);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   CUtensorMap tx[2], tw[2];
   Prob pp[2];
   for (int i = 0; i < 2; ++i) {
