@@ -652,52 +652,67 @@ def measure_block(nt, cfg, dev, stream, flush, steps, warmup, peaks):
 
 
 def run_e2e(nt, binp, dev, stream, args):
-    """The block host to host through the package's BlockGraph: every step
+    """The block host to host through the package's BlockGraph.  Every step
     copies the lengths and the singles in from pinned host memory, rebuilds
     the partition (a totals read-back), replays the captured broadcast ->
-    transition (three slices, each slice's z~ read back on a second stream as
-    soon as it is done) -> reduce graphs, and reads s_out back.  Two steps are
+    transition -> reduce graph, computes the Eq. 5 loss of the step's two
+    outputs on the device and reads the loss and s_out back.  Two steps are
     in flight: step i is submitted before step i - 1's results are waited
     for, so its copies in, partition and compute overlap the previous
     step's read-back.  The timed region ends once the last step's results
     are on the host.  The block's weights are resident on the device, as a
-    model's parameters are."""
+    model's parameters are.  ``pair_readback`` measures the same steps
+    reading the whole pair output z~ back instead of the loss (three
+    transition slices, each read back on a second stream as soon as it is
+    done), which the host link bounds."""
     from variable_length_batching_gb300 import graph
     host = {"lengths": torch.as_tensor(binp.lengths).pin_memory(), "s": binp.s.pin_memory()}
-    runner = graph.BlockGraph(_dev_weights(binp.blocks[0], dev), depth=2)
     T = int(binp.lengths.sum())
     P = int((binp.lengths.astype(np.int64) ** 2).sum())
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = P * BLOCK_CFG.C_z * 2 + T * BLOCK_CFG.C_s * 2 + 4 * 8   # z~, s_out and the partition's four totals
 
-    def steps(n, pipelined):
-        tickets = []
-        for i in range(n):
-            tickets.append(runner.submit(host["lengths"], host["s"]))
-            if not pipelined:
-                runner.wait(tickets[i])
-            elif i >= 1:
-                runner.wait(tickets[i - 1])
-        if pipelined and tickets:
-            runner.wait(tickets[-1])
+    def measure(readback):
+        runner = graph.BlockGraph(_dev_weights(binp.blocks[0], dev), depth=2, readback=readback)
 
-    def timed(pipelined):
-        steps(max(args.warmup, 3), pipelined)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        steps(args.steps, pipelined)
-        torch.cuda.synchronize()
-        return (time.perf_counter() - t0) / args.steps
+        def steps(n, pipelined):
+            tickets = []
+            for i in range(n):
+                tickets.append(runner.submit(host["lengths"], host["s"]))
+                if not pipelined:
+                    runner.wait(tickets[i])
+                elif i >= 1:
+                    runner.wait(tickets[i - 1])
+            if pipelined and tickets:
+                runner.wait(tickets[-1])
 
-    dt_seq = timed(False)
-    dt = timed(True)
-    return {"value": P / dt, "unit": "pair cells/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": dt * 1e3,
-            "ms_per_step_one_at_a_time": dt_seq * 1e3,
-            "path": "pinned host -> H2D of lengths and singles -> nt_partition_build (totals read-back) -> "
-                    f"CUDA-graph replays of broadcast / transition in {runner.slices} slices growing "
-                    f"x{runner.growth:g} / reduce, with each slice's z~ and then s_out read back on a second "
-                    f"stream; {runner.depth} steps in flight (weights resident on the device)"}
+        def timed(pipelined):
+            steps(max(args.warmup, 3), pipelined)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            steps(args.steps, pipelined)
+            torch.cuda.synchronize()
+            return (time.perf_counter() - t0) / args.steps
+
+        dt_seq = timed(False)
+        dt = timed(True)
+        out_bytes = (P * BLOCK_CFG.C_z * 2 if readback == "pair" else 4) + T * BLOCK_CFG.C_s * 2
+        path = ("pinned host -> H2D of lengths and singles -> nt_partition_build (totals read-back) -> "
+                + (f"CUDA-graph replays of broadcast / transition in {runner.slices} slices growing "
+                   f"x{runner.growth:g} / reduce, with each slice's z~ and then s_out read back on a second stream"
+                   if readback == "pair" else
+                   "one CUDA-graph replay of broadcast / transition / reduce / Eq. 5 loss, then the loss and "
+                   "s_out read back on a second stream")
+                + f"; {runner.depth} steps in flight (weights resident on the device)")
+        res = {"value": P / dt, "unit": "pair cells/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(out_bytes + 4 * 8),   # + the partition's four totals
+               "ms_per_step": dt * 1e3, "ms_per_step_one_at_a_time": dt_seq * 1e3, "path": path}
+        del runner
+        torch.cuda.empty_cache()
+        return res
+
+    e2e = measure("loss")
+    e2e["pair_readback"] = measure("pair")
+    return e2e
 
 
 # ----------------------------------------------------------------------------

@@ -91,3 +91,50 @@ def test_block_graph_pipelined_steps(mods):
     with pytest.raises(ValueError):
         runner.wait(tickets[0])              # reused two submissions later
     nt.nt_device_status()
+
+
+def test_block_graph_loss_readback(mods):
+    """readback="loss": each step reads back the Eq. 5 loss of its two
+    outputs ("DanLing NestedTensor" Appendix A.1), computed on the device in
+    the captured graph, and s_out; both equal the eager block followed by
+    nt_pair_block_loss bit for bit, over pipelined steps with other singles
+    and after new lengths."""
+    nt, graph = mods
+    cfg = wl.PAIRFORMER_BF16
+    base = wl.make_block_inputs(cfg, biases=True)
+    inps = [base] + [wl.make_block_inputs(cfg, lengths=base.lengths, biases=True, seed=sd) for sd in (1, 2)]
+    w = base.blocks[0]
+    g = lambda t: None if t is None else t.to(DEV).contiguous()
+    wd = SimpleNamespace(W_a=g(w.W_a), W_b=g(w.W_b), ln_gamma=g(w.ln_gamma), ln_beta=g(w.ln_beta), W1=g(w.W1),
+                         b1=g(w.b1), W2=g(w.W2), b2=g(w.b2), W_g=g(w.W_g), b_g=g(w.b_g))
+
+    def eager_loss(x):
+        part = nt.nt_partition_build(torch.as_tensor(np.asarray(x.lengths, dtype=np.int32)).to(DEV))
+        z, m, s_out = nt.block_forward(part, x.s.to(DEV), wd)
+        loss, _, _ = nt.nt_pair_block_loss(part, s_out, z, want_grads=False)
+        return loss.cpu(), s_out.cpu()
+
+    refs = [eager_loss(x) for x in inps]
+    runner = graph.BlockGraph(wd, depth=2, readback="loss")
+    assert runner.slices == 1
+    lengths = torch.as_tensor(np.asarray(base.lengths, dtype=np.int32)).pin_memory()
+    hs = [x.s.pin_memory() for x in inps]
+    tickets, got = [], []
+    for i, s in enumerate(hs + hs):
+        tickets.append(runner.submit(lengths, s))
+        if i >= 1:
+            l_h, s_h = runner.wait(tickets[i - 1])
+            got.append((l_h.clone(), s_h.clone()))
+    l_h, s_h = runner.wait(tickets[-1])
+    got.append((l_h.clone(), s_h.clone()))
+    for i, (l_h, s_h) in enumerate(got):
+        l_ref, s_ref = refs[i % 3]
+        assert torch.equal(l_h, l_ref) and torch.equal(s_h, s_ref), f"step {i}"
+    inp2 = wl.make_block_inputs(cfg, lengths=[64, 1, 200, 0, 37, 5, 128, 90], biases=True)
+    inp2.blocks = base.blocks
+    l2_ref, s2_ref = eager_loss(inp2)
+    l_h, s_h = runner.run(torch.as_tensor(np.asarray(inp2.lengths, dtype=np.int32)).pin_memory(), inp2.s.pin_memory())
+    assert torch.equal(l_h, l2_ref) and torch.equal(s_h, s2_ref)
+    with pytest.raises(ValueError):
+        graph.BlockGraph(wd, readback="z")
+    nt.nt_device_status()

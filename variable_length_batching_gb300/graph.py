@@ -58,14 +58,24 @@ class _Set:
 class BlockGraph:
     """Host-to-host block steps for fixed weights ``w`` (a namespace of device
     tensors W_a, W_b, ln_gamma, ln_beta, W1, b1, W2, b2, W_g, b_g; bf16 or
-    fp32 like the singles).  The transition runs in ``slices`` cell ranges,
-    each ``growth`` times as long as the one before; ``depth`` steps may be
-    in flight at once (``submit`` / ``wait``)."""
+    fp32 like the singles).  ``readback`` chooses what a step returns to the
+    host: "pair", the pair output z~ and s_out (the transition then runs in
+    ``slices`` cell ranges, each ``growth`` times as long as the one before,
+    so that each range's z~ is read back while the next one computes), or
+    "loss", the Eq. 5 loss of the step's two outputs, computed on the device
+    ("DanLing NestedTensor" Appendix A.1), and s_out (z~ stays on the
+    device; one range).  ``depth`` steps may be in flight at once
+    (``submit`` / ``wait``)."""
 
     def __init__(self, w, slices: int = 3, growth: float = 2.0, depth: int = 2, ln_eps: float = 1e-5,
-                 device: Optional[torch.device] = None):
+                 device: Optional[torch.device] = None, readback: str = "pair"):
         if slices < 1 or growth <= 0 or depth < 1:
             raise ValueError("slices and depth must be >= 1, growth > 0")
+        if readback not in ("pair", "loss"):
+            raise ValueError("readback must be 'pair' or 'loss'")
+        self.readback = readback
+        if readback == "loss":
+            slices = 1
         self.w = w
         self.slices = slices
         self.growth = growth
@@ -127,6 +137,9 @@ class BlockGraph:
                                          ln_eps=self.ln_eps, out=st.z[c0:c1])
         if idx == self.slices - 1:
             _nt.nt_pair_reduce(part, st.z, w.W_g, w.b_g, s_in=self.s, m=st.m, s_out=st.s_out)
+            if self.readback == "loss":
+                _nt.nt_pair_block_loss(part, st.s_out, st.z, want_grads=False, loss=st.loss,
+                                       workspace=self.loss_ws)
 
     def _drain(self):
         for st in self.sets:
@@ -142,13 +155,19 @@ class BlockGraph:
         self.cuts = slice_cuts(P, self.slices, self.growth)
         need = _nt.nt_pair_broadcast_workspace_bytes_rect(T, T, self.C_z)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.dev)
+        self.loss_ws = torch.empty(max(int(_nt.lib().nt_pair_block_loss_workspace_bytes()), 16), dtype=torch.uint8,
+                                   device=self.dev)
         self.sets = []
         for _ in range(self.depth):
             st = _Set()
             st.z = torch.empty(P, self.C_z, dtype=dtype, device=self.dev)
             st.m = torch.empty(T, self.C_z, dtype=dtype, device=self.dev)
             st.s_out = torch.empty(T, self.C_s, dtype=dtype, device=self.dev)
-            st.z_host = torch.empty(P, self.C_z, dtype=dtype).pin_memory()
+            if self.readback == "pair":
+                st.z_host = torch.empty(P, self.C_z, dtype=dtype).pin_memory()
+            else:
+                st.loss = torch.empty(1, dtype=torch.float32, device=self.dev)
+                st.loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
             st.s_out_host = torch.empty(T, self.C_s, dtype=dtype).pin_memory()
             st.sliced = [torch.cuda.Event() for _ in range(self.slices)]
             st.done = torch.cuda.Event()
@@ -202,8 +221,10 @@ class BlockGraph:
             for idx in range(self.slices):
                 c0, c1 = self.cuts[idx], self.cuts[idx + 1]
                 self.copy_stream.wait_event(st.sliced[idx])
-                if c1 > c0:
+                if c1 > c0 and self.readback == "pair":
                     st.z_host[c0:c1].copy_(st.z[c0:c1], non_blocking=True)
+            if self.readback == "loss":
+                st.loss_host.copy_(st.loss, non_blocking=True)
             st.s_out_host.copy_(st.s_out, non_blocking=True)
             st.done.record(self.copy_stream)
         st.busy = True
@@ -212,16 +233,17 @@ class BlockGraph:
         return ticket
 
     def wait(self, ticket: int):
-        """The pinned host results of step ``ticket`` (z~ of P x C_z, s_out of
-        T x C_s), valid until the step ``depth`` submissions later reuses
-        them."""
+        """The pinned host results of step ``ticket``, valid until the step
+        ``depth`` submissions later reuses them: (z~ of P x C_z, s_out of
+        T x C_s) with readback "pair", (the Eq. 5 loss as a 1-element fp32
+        tensor, s_out) with readback "loss"."""
         if not self.sets or self.sets[ticket % self.depth].ticket != ticket:
             raise ValueError(f"step {ticket} is no longer held (depth {self.depth})")
         st = self.sets[ticket % self.depth]
         st.done.synchronize()
-        return st.z_host, st.s_out_host
+        return (st.z_host if self.readback == "pair" else st.loss_host), st.s_out_host
 
     def run(self, lengths_host: torch.Tensor, s_host: torch.Tensor):
-        """One step, waited for: returns pinned host tensors (z~ of P x C_z,
-        s_out of T x C_s), overwritten ``depth`` steps later."""
+        """One step, waited for: returns the pinned host tensors of ``wait``,
+        overwritten ``depth`` steps later."""
         return self.wait(self.submit(lengths_host, s_host))

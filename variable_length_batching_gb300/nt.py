@@ -351,19 +351,24 @@ def nt_pair_reduce(part: Partition, z: torch.Tensor, W_g: Optional[torch.Tensor]
 
 
 def nt_pair_block_loss(part: Partition, s_out: torch.Tensor, z_tilde: torch.Tensor, want_grads: bool = True,
-                       stream=None):
+                       stream=None, loss: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
     """Eq. 5 on one block's outputs: returns (loss as a 1-element fp32
     device tensor, dL/ds_out, dL/dz~) -- the gradients fp32, or None when
-    ``want_grads`` is False."""
+    ``want_grads`` is False.  ``loss`` and ``workspace`` may be given (a
+    1-element fp32 tensor and nt_pair_block_loss_workspace_bytes() bytes),
+    so that a captured graph writes into fixed buffers."""
     T, C_s = s_out.shape
     C_z = z_tilde.shape[1]
     if T != part.T or z_tilde.shape[0] != part.P:
         raise ValueError("outputs do not match the partition")
     dev = s_out.device
-    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
     ds = torch.empty(T, C_s, dtype=torch.float32, device=dev) if want_grads else None
     dz = torch.empty(part.P, C_z, dtype=torch.float32, device=dev) if want_grads else None
-    ws = torch.empty(int(lib().nt_pair_block_loss_workspace_bytes()), dtype=torch.uint8, device=dev)
+    ws = workspace
+    if ws is None:
+        ws = torch.empty(int(lib().nt_pair_block_loss_workspace_bytes()), dtype=torch.uint8, device=dev)
     st = lib().nt_pair_block_loss(ctypes.byref(part.c), _dtype(s_out), _ptr(s_out), C_s, _ptr(z_tilde), C_z,
                                   _ptr(loss), _ptr(ds), _ptr(dz), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "nt_pair_block_loss")
