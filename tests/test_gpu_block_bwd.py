@@ -122,3 +122,38 @@ def test_rectangular_partition_refused(nt):
     with pytest.raises(nt.NTError) as e:
         nt.nt_pair_block_backward(part, s, w, m, ds_out)
     assert e.value.status == 2
+
+
+def test_block_backward_near_uniform_sampled(nt):
+    """The near-uniform B=16 batch itself (P = 8.6 M cells, the size the bench
+    times): the loss and backward of the whole batch on the GPU, and the
+    single-row gradient ds of its shortest sample against the oracle, which
+    needs that sample alone (ds of a sample's rows depends on its own cells;
+    Eq. 5's weights and totals are the batch's)."""
+    cfg = wl.NEAR_UNIFORM_BF16
+    inp = wl.make_block_inputs(cfg)
+    w = _dw(inp.blocks[0])
+    part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(DEV))
+    s = inp.s.to(DEV)
+    z, m, s_out = nt.block_forward(part, s, w)
+    _, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z)
+    del z
+    g = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
+    torch.cuda.synchronize()
+    nt.nt_device_status()
+    lengths = np.asarray(inp.lengths, dtype=np.int64)
+    k = int(np.argmin(lengths))
+    n = int(lengths[k])
+    r0 = int(lengths[:k].sum())
+    B, T, P = len(lengths), int(lengths.sum()), int((lengths ** 2).sum())
+    ow = oracle_weights(inp.blocks[0])
+    X = f64(inp.s)[r0:r0 + n]
+    res = oblock.block_sample(X, ow)
+    alpha, beta = obwd.eq5_sample_weights(B)
+    C, Cp = X.shape[1], res.P_tilde.shape[2]
+    dX_up = 2.0 * alpha[k] * res.X_tilde / (C * T)
+    dP_up = 2.0 * beta[k] * res.P_tilde / (Cp * P)
+    ref_ds, _ = obwd.block_backward_sample(X, ow, dX_up, dP_up)
+    got = to_np(g["ds"][r0:r0 + n])
+    e = normwise_err(got, ref_ds, dtype="bf16")
+    assert e <= TOL["bf16"], f"ds of sample {k} (N = {n}): {e:.3e}"
