@@ -604,22 +604,32 @@ def measure_block_backward(nt, cfg, dev, stream, flush, steps, peaks):
     s = inp.s.to(dev)
     part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(dev))
     z, m, s_out = nt.block_forward(part, s, wd, stream=stream)
-    ws = torch.empty(nt.nt_pair_block_backward_workspace_bytes(nt._dtype(s), part.T, part.P, cfg.C_z, cfg.H_t), dtype=torch.uint8,
-                     device=dev)
+    dt = nt._dtype(s)
+    ws = torch.empty(nt.nt_pair_block_loss_backward_workspace_bytes(dt, part.T, part.P, cfg.C_s, cfg.C_z, cfg.H_t),
+                     dtype=torch.uint8, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
 
-    def step():
+    def fused():
+        nt.nt_pair_block_loss_backward(part, s, wd, m, s_out, z, loss=loss, workspace=ws, stream=stream)
+    ms = _event_ms(fused, stream, flush, steps, warmup=2)
+    del ws
+    ws2 = torch.empty(nt.nt_pair_block_backward_workspace_bytes(dt, part.T, part.P, cfg.C_z, cfg.H_t),
+                      dtype=torch.uint8, device=dev)
+
+    def two_calls():
         _, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z, stream=stream)
-        nt.nt_pair_block_backward(part, s, wd, m, ds_out, dz, workspace=ws, stream=stream)
-    ms = _event_ms(step, stream, flush, steps, warmup=2)
+        nt.nt_pair_block_backward(part, s, wd, m, ds_out, dz, workspace=ws2, stream=stream)
+    ms2 = _event_ms(two_calls, stream, flush, steps, warmup=2)
     nt.nt_device_status(stream)
     # per cell: A recomputed, dH, dY, dW1, dW2 (five C_z x H_t products)
     flops = 5 * 2 * cfg.C_z * cfg.H_t * part.P
     route = backward_route(cfg)
     out = {"workload": cfg.name, "P": part.P, "ms": ms, "flops": flops, "steps": steps,
            **backward_roof(route, flops, ms, dev, peaks),
-           "call": "nt_pair_block_loss + nt_pair_block_backward ("
-                   + ("pair cells on tcgen05 GEMMs" if route == "tensor" else "fp32 CUDA cores") + ")"}
-    del z, m, s_out, ws
+           "call": "nt_pair_block_loss_backward ("
+                   + ("pair cells on tcgen05 GEMMs" if route == "tensor" else "fp32 CUDA cores") + ")",
+           "two_calls_ms": ms2}
+    del z, m, s_out, ws2
     torch.cuda.empty_cache()
     return out
 
@@ -1083,15 +1093,26 @@ def run_only(args):
         # the Eq. 5 loss and the block's backward (CUDA cores): the forward's
         # outputs are made once, outside the timed calls
         zb, mb, sob = nt.block_forward(part, s, wd)
-        bws = torch.empty(nt.nt_pair_block_backward_workspace_bytes(nt._dtype(s), part.T, part.P, cfg.C_z, cfg.H_t),
-                          dtype=torch.uint8, device=dev)
-
-        def backward_step():
-            _, ds_out, dz = nt.nt_pair_block_loss(part, sob, zb, stream=stream)
-            nt.nt_pair_block_backward(part, s, wd, mb, ds_out, dz, workspace=bws, stream=stream)
+        bound_b = "tensor" if backward_route(cfg) == "tensor" else "fma"
         # per cell: A recomputed, dH, dY, dW1, dW2 (five C_z x H_t products)
-        fns["backward"] = (backward_step, {"bytes": 0, "flops": 5 * 2 * cfg.C_z * cfg.H_t * part.P},
-                           "tensor" if backward_route(cfg) == "tensor" else "fma")
+        work_b = {"bytes": 0, "flops": 5 * 2 * cfg.C_z * cfg.H_t * part.P}
+        if args.only == "backward":
+            lws = torch.empty(nt.nt_pair_block_loss_backward_workspace_bytes(nt._dtype(s), part.T, part.P, cfg.C_s,
+                                                                             cfg.C_z, cfg.H_t),
+                              dtype=torch.uint8, device=dev)
+            lossb = torch.empty(1, dtype=torch.float32, device=dev)
+            fns["backward"] = (lambda: nt.nt_pair_block_loss_backward(part, s, wd, mb, sob, zb, loss=lossb,
+                                                                      workspace=lws, stream=stream),
+                               work_b, bound_b)
+        if args.only == "backward_two_calls":
+            bws = torch.empty(nt.nt_pair_block_backward_workspace_bytes(nt._dtype(s), part.T, part.P, cfg.C_z,
+                                                                        cfg.H_t),
+                              dtype=torch.uint8, device=dev)
+
+            def backward_step():
+                _, ds_out, dz = nt.nt_pair_block_loss(part, sob, zb, stream=stream)
+                nt.nt_pair_block_backward(part, s, wd, mb, ds_out, dz, workspace=bws, stream=stream)
+            fns["backward_two_calls"] = (backward_step, work_b, bound_b)
         if args.swiglu:
             sw = wl.make_swiglu_weights(cfg.C_z, cfg.H_t, cfg.dtype)
             d = lambda t: None if t is None else t.to(dev)
@@ -1143,7 +1164,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["partition", "broadcast", "transition", "reduce", "block", "fused", "attention",
-                             "backward", "packing", "padsweep", "rect"],
+                             "backward", "backward_two_calls", "packing", "padsweep", "rect"],
                     help="time one call on one workload instead of the whole step; 'packing' and "
                          "'padsweep' print the packed-vs-padded reports")
     ap.add_argument("--workload", default="pairformer", choices=sorted(WORKLOADS))

@@ -423,6 +423,42 @@ nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const
                                  float* db1, float* dW2, float* db2, float* dW_g, float* db_g, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace nt_pair_block_loss_backward needs: the loss's
+ * partial sums, dL/dX~ ([T, C_s] fp32), dL/dz~ ([P, C_z] fp32) except on the
+ * tensor-core route, and nt_pair_block_backward_workspace_bytes(dtype, T, P,
+ * C_z, H_t), each part rounded up to 256 bytes.  0 for negative sizes. */
+size_t nt_pair_block_loss_backward_workspace_bytes(nt_dtype dtype, int64_t T, int64_t P, int32_t C_s,
+                                                   int32_t C_z, int32_t H_t);
+
+/*
+ * nt_pair_block_loss_backward -- the Eq. 5 loss of [DL] Appendix A.1 on the
+ * block's outputs and the block's gradients for it, in one call: the same
+ * loss as nt_pair_block_loss and the same gradients as nt_pair_block_backward
+ * given that call's ds_out and dz_tilde, value for value (the upstream
+ * gradients are formed by the same fp32 operations).  dL/dz~ = gp_i P~ with
+ * gp_i = 2 beta_i / (C_z sum_i N_i^2) is linear in z~, so on the tensor-core
+ * route (bf16, C_z = 128, H_t a multiple of 128) it is never stored: the
+ * two kernels that read it form it from z~ ([P, C_z] bf16, half the bytes of
+ * the fp32 gradient, and no pass that writes it).  Other routes store it in
+ * the workspace first.
+ *   s_out, z_tilde   the block's outputs (as nt_pair_block_loss takes them).
+ *   d_loss           one fp32 on the device, written.
+ *   every other argument as for nt_pair_block_backward (no ds_out or
+ *   dz_tilde: they are this loss's).
+ *   workspace  >= nt_pair_block_loss_backward_workspace_bytes(dtype, T, P,
+ *              C_s, C_z, H_t) bytes, 16-byte aligned.
+ * Errors as for nt_pair_block_backward, plus NT_ERR_INVALID for a NULL
+ * d_loss, s_out (T > 0) or z_tilde (P > 0).  Asynchronous.
+ */
+nt_status nt_pair_block_loss_backward(const nt_partition* part, nt_dtype dtype, const void* s, int32_t C_s,
+                                      const void* W_a, const void* W_b, int32_t C_z, int32_t H_t,
+                                      const float* ln_gamma, const float* ln_beta, float ln_eps, const void* W1,
+                                      const float* b1, const void* W2, const void* W_g, const void* m,
+                                      const void* s_out, const void* z_tilde, float* d_loss, float* ds, float* dW_a,
+                                      float* dW_b, float* dgamma, float* dbeta, float* dW1, float* db1, float* dW2,
+                                      float* db2, float* dW_g, float* db_g, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
 /*
  * nt_varlen_attn_workspace_bytes -- bytes of device workspace that
  * nt_varlen_attn and nt_varlen_attn_qk take for their work counter (a small

@@ -72,6 +72,20 @@ def test_block_backward_workspace_bytes():
     assert nt.nt_pair_block_backward_workspace_bytes(nt.NT_BF16, -1, P, C, H) == 0
 
 
+def test_block_loss_backward_workspace_bytes():
+    """The fused loss + backward needs the loss's partial sums, dL/dX~ ([T,
+    C_s] fp32) and the backward's workspace; dL/dz~ ([P, C_z] fp32) as well,
+    except on the tensor-core route, which forms it from z~."""
+    from variable_length_batching_gb300 import nt
+    T, P, Cs, C, H = 1031, 157023, 384, 128, 512
+    loss_ws = int(nt.lib().nt_pair_block_loss_workspace_bytes())
+    for dt, Cz, Ht, dz in ((nt.NT_BF16, C, H, 0), (nt.NT_F32, C, H, P * C * 4), (nt.NT_BF16, 64, 256, P * 64 * 4)):
+        got = nt.nt_pair_block_loss_backward_workspace_bytes(dt, T, P, Cs, Cz, Ht)
+        bwd = nt.nt_pair_block_backward_workspace_bytes(dt, T, P, Cz, Ht)
+        assert bwd + loss_ws + T * Cs * 4 + dz <= got <= bwd + loss_ws + T * Cs * 4 + dz + 3 * 256
+    assert nt.nt_pair_block_loss_backward_workspace_bytes(nt.NT_BF16, T, P, -1, C, H) == 0
+
+
 def test_host_side_rejections(L):
     """Calls that must fail on argument checks alone (nothing reaches CUDA)."""
     from variable_length_batching_gb300 import nt

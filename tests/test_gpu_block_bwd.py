@@ -73,14 +73,13 @@ def test_block_backward_bf16(nt, lengths, biases):
 def test_block_backward_bf16_cuda_core_route(nt):
     """bf16 at C_z = 64 (not the tensor-core route's 128): the CUDA-core
     kernels, against the oracle."""
-    import dataclasses
-    cfg = dataclasses.replace(wl.PAIRFORMER_BF16, name="bf16_Cz64", C_s=128, C_z=64, H_t=256)
-    _check(*_run(nt, cfg, [40, 3, 0, 25], True))
+    _check(*_run(nt, _cz64(), [40, 3, 0, 25], True))
 
 
 def test_tensor_core_weight_gradients_reproducible(nt):
     """dW1, db1, dW2 and db2 of the tensor-core route are summed over fixed
-    cell splits in a fixed order: two calls give the same bits."""
+    cell splits in a fixed order, and du, dv (hence ds) over fixed 32 x 32
+    cell items: two calls give the same bits."""
     inp = wl.make_block_inputs(wl.PAIRFORMER_BF16)
     w = _dw(inp.blocks[0])
     part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(DEV))
@@ -90,8 +89,60 @@ def test_tensor_core_weight_gradients_reproducible(nt):
     g1 = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
     g2 = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
     torch.cuda.synchronize()
-    for n in ("dW1", "db1", "dW2", "db2"):
+    for n in ("ds", "dW1", "db1", "dW2", "db2"):
         assert torch.equal(g1[n], g2[n]), n
+
+
+def _cz64():
+    import dataclasses
+    return dataclasses.replace(wl.PAIRFORMER_BF16, name="bf16_Cz64", C_s=128, C_z=64, H_t=256)
+
+
+@pytest.mark.parametrize("route", ["tensor_core", "tensor_core_batch", "cuda_core_f32", "cuda_core_bf16"])
+def test_loss_backward_equals_two_calls(nt, route):
+    """nt_pair_block_loss_backward against nt_pair_block_loss followed by
+    nt_pair_block_backward on the same inputs: the same loss bits on every
+    route; on the tensor-core route (where dL/dz~ = gp_i z~ is formed from
+    z~ where it is read) also the same ds and split-summed weight gradients,
+    bit for bit; the gradients accumulated with atomics within 1e-6."""
+    cfg, lengths = {"tensor_core": (wl.PAIRFORMER_BF16, [33, 0, 1, 32, 31, 65, 37]),
+                    "tensor_core_batch": (wl.PAIRFORMER_BF16, None),
+                    "cuda_core_f32": (wl.TINY_FP32, [5, 0, 9, 1]),
+                    "cuda_core_bf16": (_cz64(), [40, 3, 0, 25])}[route]
+    inp = wl.make_block_inputs(cfg, lengths=lengths, biases=True, seed=4)
+    w = _dw(inp.blocks[0])
+    part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(DEV))
+    s = inp.s.to(DEV)
+    z, m, s_out = nt.block_forward(part, s, w)
+    l1, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z)
+    g1 = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
+    l2, g2 = nt.nt_pair_block_loss_backward(part, s, w, m, s_out, z)
+    torch.cuda.synchronize()
+    nt.nt_device_status()
+    assert torch.equal(l1, l2)
+    exact = ("ds", "dW1", "db1", "dW2", "db2") if route.startswith("tensor_core") else ()
+    for n in NAMES:
+        if n in exact:
+            assert torch.equal(g1[n], g2[n]), n
+        else:
+            assert normwise_err(to_np(g2[n]), to_np(g1[n]), dtype="f32") <= 1e-6, n
+
+
+def test_loss_backward_against_oracle(nt):
+    """The fused call on a bf16 batch with 31-, 32- and 33-token samples (the
+    edges of the 32 x 32 cell items), against the oracle."""
+    inp = wl.make_block_inputs(wl.PAIRFORMER_BF16, lengths=[33, 0, 1, 32, 31, 65], biases=True, seed=6)
+    w = _dw(inp.blocks[0])
+    part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(DEV))
+    s = inp.s.to(DEV)
+    z, m, s_out = nt.block_forward(part, s, w)
+    loss, g = nt.nt_pair_block_loss_backward(part, s, w, m, s_out, z)
+    torch.cuda.synchronize()
+    nt.nt_device_status()
+    ow = oracle_weights(inp.blocks[0])
+    fwd = oblock.block_packed(inp.lengths, f64(inp.s), ow)
+    ref_loss, ref = obwd.block_loss_and_grads(inp.lengths, f64(inp.s), ow, fwd.z_tilde, fwd.s_out)
+    _check(float(loss.item()), g, ref_loss, ref, "bf16")
 
 
 def test_block_backward_pairformer_batch(nt):

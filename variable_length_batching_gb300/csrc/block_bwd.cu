@@ -25,7 +25,10 @@
 //   tcgen05 GEMMs H = ReLU(LN(z) W1^T + b1), dA = (dP~ W2) where H > 0,
 //                 dY = dA W1 (linear_tc), dW1 = dA^T LN(z), dW2 = dP~^T H,
 //                 db1, db2 (wgrad_tc: split over the cells)
-//   bwd_ln        per cell: the LayerNorm backward -> dz; dgamma, dbeta
+//   bwd_ln_sums   per 32 x 32 cell item: the LayerNorm backward -> dz in
+//                 registers, summed at once into row and column partials of
+//                 du and dv (dz is not stored); dgamma, dbeta
+//   sums_finish   du, dv from the partials in a fixed order
 // The GEMM operands are bf16 (dP~ and dA rounded once); every accumulation
 // is fp32.  fp32 I/O and other widths run the CUDA-core kernels below.
 //
@@ -55,13 +58,14 @@ constexpr int kLossBlocks = 1024;   // CTAs (and double partial pairs) of the lo
 // samples with no cells), then the row and column within its N x N block.
 __device__ __forceinline__ void cell_coords(const int64_t* __restrict__ pair_off, const int32_t* __restrict__ cu,
                                             const int32_t* __restrict__ len, int B, int64_t p, int64_t& row,
-                                            int64_t& col, int& n) {
+                                            int64_t& col, int& n, int* sample = nullptr) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (pair_off[mid] <= p) lo = mid; else hi = mid - 1;
   }
   n = len[lo];
+  if (sample) *sample = lo;
   const int64_t off = p - pair_off[lo];
   const int64_t a = off / n;
   row = cu[lo] + a;
@@ -88,6 +92,14 @@ __device__ __forceinline__ float round_io(float x, bf16*) { return __bfloat162fl
 
 // ---------------------------------------------------------------- the loss
 
+// dL/dP~ = gp_b P~ for the cells of sample b: gp_b = 2 beta_b / (C_p P),
+// beta_b = 1.5 - b / (2B), formed in double and rounded once to fp32 (the
+// loss kernel and the fused loss + backward read the same value).
+__device__ __forceinline__ float eq5_pair_scale(int b, int B, int Cp, int64_t P) {
+  const double beta = 1.5 - (double)b / (2.0 * B);
+  return (float)(2.0 * beta / ((double)Cp * P));
+}
+
 // One CTA per group of pair rows: sum over its rows of alpha_b ||X~ row||^2
 // and of beta_b ||P~ row's cells||^2, in double, into partial[blockIdx];
 // optionally writes dX~ = 2 alpha_b X~ / (C T) and dP~ = 2 beta_b P~ / (C_p P).
@@ -101,7 +113,7 @@ eq5_partial_kernel(const T* __restrict__ s_out, const T* __restrict__ zt, const 
   for (int64_t r = blockIdx.x; r < Trows; r += gridDim.x) {
     const int b = row_sample[r];
     const double alpha = 1.0 + (double)b / B, beta = 1.5 - (double)b / (2.0 * B);
-    const float gx = (float)(2.0 * alpha / ((double)C * Trows)), gp = (float)(2.0 * beta / ((double)Cp * P));
+    const float gx = (float)(2.0 * alpha / ((double)C * Trows)), gp = eq5_pair_scale(b, B, Cp, P);
     float sx = 0.f;
     for (int k = threadIdx.x; k < C; k += kThreads) {
       const float x = to_f32(s_out[r * C + k]);
@@ -611,10 +623,12 @@ cudaError_t block_backward_t(const BlockBwd& q, unsigned int* status, cudaStream
     trans_bwd_weights_kernel<T><<<dim3(nchunk, splits), kThreads, sm2, s>>>(a, splits, q.dW1, q.dW2, q.db1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  // the broadcast: du, dv; dW_a += du^T s, dW_b += dv^T s; ds = dX~ + du W_a + dv W_b
+  // the broadcast: du, dv (already summed on the tensor-core route); dW_a += du^T s, dW_b += dv^T s;
+  // ds = dX~ + du W_a + dv W_b
   if (Trows > 0) {
-    pair_rowcol_sum_kernel<<<(unsigned)min64(Trows, 4096), kThreads, 2 * kThreads * sizeof(float), s>>>(
-        q.dz, p->cu_seqlens, p->pair_off, p->lengths, p->row_sample, Trows, C, q.du, q.dv);
+    if (!(p->P > 0 && q.tc_ws))
+      pair_rowcol_sum_kernel<<<(unsigned)min64(Trows, 4096), kThreads, 2 * kThreads * sizeof(float), s>>>(
+          q.dz, p->cu_seqlens, p->pair_off, p->lengths, p->row_sample, Trows, C, q.du, q.dv);
     const int splits = (int)min64(64, (Trows + 255) / 256);
     gram_kernel<T><<<dim3((C + 31) / 32, (Cs + 31) / 32, splits), kThreads, 0, s>>>(q.du, (const T*)q.s, Trows, C,
                                                                                      Cs, splits, q.dW_a);
@@ -631,6 +645,14 @@ cudaError_t block_backward_t(const BlockBwd& q, unsigned int* status, cudaStream
 
 // ------------------------------------------------ the tensor-core route (bf16)
 
+using tc::bf16hi;
+using tc::bf16lo;
+using tc::bulk_load;
+using tc::fence_mbar_init;
+using tc::mbar_arrive_expect_tx;
+using tc::mbar_init;
+using tc::mbar_wait;
+using tc::mbar_wait_warp;
 using tc::pack_bf16x2;
 
 constexpr int kTcC = 128;          // pair width of the tensor-core route
@@ -639,22 +661,58 @@ constexpr int kPrepCells = kThreads / 8;   // cells per CTA pass: 8 threads x 16
 // Rows of the route: per cell p, 8 threads own features 16 q .. 16 q + 15.
 // LN(z) as two bf16 parts, hi = bf16(y) and lo = bf16(y - hi), side by side
 // in a row of 2 C_z (A = [hi | lo] [W1 | W1]^T carries y to about 16 bits,
-// so A's sign, the ReLU's decision, is that of the fp32 y); dP~ = dz_up +
-// dM[row] / N as bf16; the LayerNorm's mean and rstd of the rebuilt z
-// (bf16-rounded as in the forward).
+// so A's sign, the ReLU's decision, is that of the fp32 y) and dP~ = dz_up +
+// dM[row] / N as bf16, with z rebuilt bf16-rounded as the forward rounds
+// it.  With zt_up, dz_up is Eq. 5's gp_b z~, formed here as the loss forms
+// it.
 __global__ void __launch_bounds__(kThreads)
 bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ len, int B, int64_t P,
                 const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
-                const float* __restrict__ dM, const float* __restrict__ dz_up, bf16* __restrict__ Y,
-                bf16* __restrict__ dPt, float2* __restrict__ stats) {
+                const float* __restrict__ dM, const float* __restrict__ dz_up, const bf16* __restrict__ zt_up,
+                bf16* __restrict__ Y, bf16* __restrict__ dPt) {
   const int q = threadIdx.x & 7;
+  int gp_b = -1;       // the sample whose Eq. 5 scale gp holds (formed in double, so once per sample)
+  float gp = 0.f;
   for (int64_t p = (int64_t)blockIdx.x * kPrepCells + (threadIdx.x >> 3); p - (threadIdx.x >> 3) < P;
        p += (int64_t)gridDim.x * kPrepCells) {
     const bool valid = p < P;
     int64_t row = 0, col = 0;
-    int n = 1;
-    if (valid) cell_coords(pair_off, cu, len, B, p, row, col, n);
+    int n = 1, b = 0;
+    if (valid) cell_coords(pair_off, cu, len, B, p, row, col, n, &b);
+    // dP~ = dz_up + dM[row] / N first: its loads are the ones from HBM (with
+    // zt_up, dz_up = gp_b z~, Eq. 5's, formed here as the loss forms it)
+    const float inv_n = 1.0f / (float)n;
+    float up[16];
+    if (zt_up) {
+      if (b != gp_b) {
+        gp = eq5_pair_scale(b, B, kTcC, P);
+        gp_b = b;
+      }
+      if (valid) {
+        load_vec(zt_up + p * kTcC + 16 * q, up);
+        load_vec(zt_up + p * kTcC + 16 * q + 8, up + 8);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) up[j] = valid ? gp * up[j] : 0.f;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) {
+        float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid && dz_up) u4 = *reinterpret_cast<const float4*>(dz_up + p * kTcC + 16 * q + j);
+        up[j] = u4.x; up[j + 1] = u4.y; up[j + 2] = u4.z; up[j + 3] = u4.w;
+      }
+    }
+    float gv[16];
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+      float4 m4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (valid) m4 = *reinterpret_cast<const float4*>(dM + row * kTcC + 16 * q + j);
+      gv[j] = fmaf(m4.x, inv_n, up[j]);
+      gv[j + 1] = fmaf(m4.y, inv_n, up[j + 1]);
+      gv[j + 2] = fmaf(m4.z, inv_n, up[j + 2]);
+      gv[j + 3] = fmaf(m4.w, inv_n, up[j + 3]);
+    }
     float z[16];
     float s1 = 0.f;
 #pragma unroll
@@ -685,18 +743,6 @@ bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const 
     s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
     const float rs = rsqrtf(s2 * (1.0f / kTcC) + eps);
     if (!valid) continue;
-    const float inv_n = 1.0f / (float)n;
-    float gv[16];
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      const float4 m4 = *reinterpret_cast<const float4*>(dM + row * kTcC + 16 * q + j);
-      float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (dz_up) u4 = *reinterpret_cast<const float4*>(dz_up + p * kTcC + 16 * q + j);
-      gv[j] = fmaf(m4.x, inv_n, u4.x);
-      gv[j + 1] = fmaf(m4.y, inv_n, u4.y);
-      gv[j + 2] = fmaf(m4.z, inv_n, u4.z);
-      gv[j + 3] = fmaf(m4.w, inv_n, u4.w);
-    }
     uint32_t yw[8], lw[8], gw[8];
 #pragma unroll
     for (int j = 0; j < 16; j += 2) {
@@ -718,104 +764,290 @@ bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const 
     lo[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
     go[0] = make_uint4(gw[0], gw[1], gw[2], gw[3]);
     go[1] = make_uint4(gw[4], gw[5], gw[6], gw[7]);
-    if (q == 0) stats[p] = make_float2(mean, rs);
   }
 }
 
-// The LayerNorm backward per cell, in place: dY (fp32, from the GEMM) in
-// the dz buffer becomes dz = dP~ + (dxhat - mean(dxhat) - xhat mean(dxhat
-// xhat)) rstd, dxhat = dY gamma, with x-hat of the rebuilt z and dP~ exact
-// in fp32.  dgamma += dY xhat and dbeta += dY, reduced over the CTA's cells
-// then added atomically.
-__global__ void __launch_bounds__(kThreads)
-bwd_ln_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
-              const int32_t* __restrict__ cu, const int32_t* __restrict__ len, int B, int64_t P,
-              const float* __restrict__ gamma, const float2* __restrict__ stats, const float* __restrict__ dM,
-              const float* __restrict__ dz_up, float* __restrict__ dz, float* __restrict__ dgamma,
-              float* __restrict__ dbeta) {
+// ---------------------------------------- the LayerNorm and broadcast backward, fused
+
+// The cells of sample b (N = N_b, c = ceil(N / 32)) are cut into c x c items
+// of up to 32 rows (a row block) by 32 columns (a column chunk).  Slot bases
+// follow from the partition's own scans, so no per-call table is built:
+//   item slots of b:   [pair_off[b] / 1024 + cu[b] / 16 + b, the same for b + 1),
+//                      at least c^2 of them (a CTA past the first c^2 exits);
+//   partial rows of b: from pair_off[b] / 32 + cu[b], at least c N of them:
+//                      du partial of (column chunk k, row a) and dv partial of
+//                      (row block k, column a) at k N + a.
+// Over the batch: at most P / 1024 + T / 16 + B items and P / 32 + T partial
+// rows of each kind.
+constexpr int kSumTile = 32;
+
+__device__ __forceinline__ int64_t sum_item_base(const int64_t* pair_off, const int32_t* cu, int b) {
+  return pair_off[b] / 1024 + cu[b] / 16 + b;
+}
+__device__ __forceinline__ int64_t sum_part_base(const int64_t* pair_off, const int32_t* cu, int b) {
+  return pair_off[b] / kSumTile + cu[b];
+}
+
+// One CTA of 512 threads per item slot: 16 threads per column, thread q of
+// a column owning features 4q..4q+3 and 64+4q..64+4q+3.  Per row of the
+// item, its dY and upstream-gradient cells (32 contiguous cells each) and
+// the row's u and dM are staged in shared memory by 1-D bulk copies, two
+// rows per copy group and three groups in flight, issued by thread 0 once
+// every thread has read the buffer (the group's barrier); the column's v
+// stays in registers, so no per-row load waits on memory.  Per row the
+// threads rebuild z = bf16(u + v), its LayerNorm mean and rstd, and form
+// the LayerNorm backward in fp32 registers,
+//     dz = dP~ + (dxhat - mean(dxhat) - xhat mean(dxhat xhat)) rstd,
+//     dxhat = dY gamma, dP~ = dz_up + dM[row] / N
+// (dz is never stored), and add dz into their column's sum over the item's rows; the
+// item's 32 columns are summed per row, first over the warp's two columns
+// (an exchange that leaves each lane 4 of the row's 128 features), then
+// over the 16 warps in warp order through shared memory.  Fixed orders
+// throughout, so du and dv are reproducible.  dgamma += dY xhat and dbeta
+// += dY are reduced over the CTA in shared memory, then added with one
+// atomic per feature.  A copy wait that runs out flags the status word and
+// ends the CTA once the copies it issued have landed (bounded as well).
+constexpr int kSumThreads = 512;
+constexpr int kSumWarps = kSumThreads / 32;
+constexpr int kSumRows = 2;                                   // rows per copy group
+constexpr int kSumBufs = 3;                                   // copy groups in flight
+constexpr int kSumHalf = kSumTile * kTcC * 4;                 // 32 cells of fp32 features: 16 KB
+constexpr int kSumRowBytes = 2 * kSumHalf + 2 * kTcC * 4;     // dY, the upstream gradient, u[row], dM[row]
+constexpr size_t kSumSmem = (size_t)kSumBufs * kSumRows * kSumRowBytes + (size_t)kSumRows * kSumWarps * kTcC * 4 +
+                            kSumBufs * sizeof(uint64_t);
+
+__global__ void __launch_bounds__(kSumThreads, 1)
+bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
+                   const int32_t* __restrict__ cu, const int32_t* __restrict__ len, int B,
+                   const float* __restrict__ gamma, float eps, const float* __restrict__ dM,
+                   const float* __restrict__ dz_up, const bf16* __restrict__ zt_up, const float* __restrict__ dY,
+                   float* __restrict__ du_part, float* __restrict__ dv_part, float* __restrict__ dgamma,
+                   float* __restrict__ dbeta, unsigned int* status) {
+  extern __shared__ __align__(128) uint8_t sum_smem[];
+  uint8_t* bufs = sum_smem;                                                        // [buf][row][dY | up]
+  float4* rp = reinterpret_cast<float4*>(sum_smem + (size_t)kSumBufs * kSumRows * kSumRowBytes);  // [row][warp][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(rp + kSumRows * kSumWarps * (kTcC / 4));
   __shared__ float red[2][kTcC];
-  const int q = threadIdx.x & 7, slot = threadIdx.x >> 3;
-  float pg[16], pb[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) { pg[j] = 0.f; pb[j] = 0.f; }
-  for (int64_t p = (int64_t)blockIdx.x * kPrepCells + slot; p - slot < P; p += (int64_t)gridDim.x * kPrepCells) {
-    const bool valid = p < P;
-    int64_t row = 0, col = 0;
-    int n = 1;
-    float2 st = make_float2(0.f, 0.f);
-    if (valid) {
-      cell_coords(pair_off, cu, len, B, p, row, col, n);
-      st = stats[p];
-    }
-    float xh[16], dy[16];
-    float m1 = 0.f, m2 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, g = a;
-      if (valid) {
-        a = *reinterpret_cast<const float4*>(u + row * kTcC + 16 * q + j);
-        b = *reinterpret_cast<const float4*>(v + col * kTcC + 16 * q + j);
-        g = *reinterpret_cast<const float4*>(dz + p * kTcC + 16 * q + j);
-      }
-      const float za[4] = {a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w};
-      const float ga[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        xh[j + e] = valid ? (round_io(za[e], (bf16*)nullptr) - st.x) * st.y : 0.f;
-        dy[j + e] = ga[e];
-        const float dx = ga[e] * gamma[16 * q + j + e];
-        m1 += dx;
-        m2 = fmaf(dx, xh[j + e], m2);
-      }
-    }
-    m1 += __shfl_xor_sync(0xffffffffu, m1, 1);
-    m1 += __shfl_xor_sync(0xffffffffu, m1, 2);
-    m1 += __shfl_xor_sync(0xffffffffu, m1, 4);
-    m2 += __shfl_xor_sync(0xffffffffu, m2, 1);
-    m2 += __shfl_xor_sync(0xffffffffu, m2, 2);
-    m2 += __shfl_xor_sync(0xffffffffu, m2, 4);
-    if (!valid) continue;
-    m1 *= 1.0f / kTcC;
-    m2 *= 1.0f / kTcC;
-    const float inv_n = 1.0f / (float)n;
-    float gv[16];
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      const float4 m4 = *reinterpret_cast<const float4*>(dM + row * kTcC + 16 * q + j);
-      float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (dz_up) u4 = *reinterpret_cast<const float4*>(dz_up + p * kTcC + 16 * q + j);
-      gv[j] = fmaf(m4.x, inv_n, u4.x);
-      gv[j + 1] = fmaf(m4.y, inv_n, u4.y);
-      gv[j + 2] = fmaf(m4.z, inv_n, u4.z);
-      gv[j + 3] = fmaf(m4.w, inv_n, u4.w);
-    }
-    float out[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int f = 16 * q + j;
-      const float dx = dy[j] * gamma[f];
-      const float g = gv[j];
-      out[j] = g + (dx - m1 - xh[j] * m2) * st.y;
-      pg[j] = fmaf(dy[j], xh[j], pg[j]);
-      pb[j] += dy[j];
-    }
-#pragma unroll
-    for (int j = 0; j < 16; j += 4)
-      *reinterpret_cast<float4*>(dz + p * kTcC + 16 * q + j) = make_float4(out[j], out[j + 1], out[j + 2], out[j + 3]);
+  __shared__ float gs[kTcC];
+  __shared__ int abort_flag;
+  const int64_t g = blockIdx.x;
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sum_item_base(pair_off, cu, mid) <= g) lo = mid; else hi = mid - 1;
   }
-  // features 16 q + j: summed over the CTA's cell slots in shared memory,
-  // then one global atomic per feature
+  const int b = lo;
+  const int n = len[b];
+  const int c = (n + kSumTile - 1) / kSumTile;
+  const int64_t local = g - sum_item_base(pair_off, cu, b);
+  if (local >= (int64_t)c * c) return;   // CTA-uniform, before any barrier
+  const int rb = (int)(local / c), cc = (int)(local % c);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int q = threadIdx.x & 15, slot = threadIdx.x >> 4;
+  const int j0 = cc * kSumTile, j = j0 + slot;
+  const int ncols = min(n - j0, kSumTile);
+  const bool cv = slot < ncols;
+  const int a_lo = rb * kSumTile, a_hi = min(n, a_lo + kSumTile);
+  const int ngroups = (a_hi - a_lo + kSumRows - 1) / kSumRows;
+  const int64_t P0 = pair_off[b], t0 = cu[b], pb0 = sum_part_base(pair_off, cu, b);
+  const float inv_n = 1.0f / (float)n;
+  const float gp = zt_up ? eq5_pair_scale(b, B, kTcC, pair_off[B]) : 0.f;
+  const uint32_t up_cell = zt_up ? kTcC * 2 : (dz_up ? kTcC * 4 : 0);   // upstream bytes per cell
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSumBufs; ++i) mbar_init(&full[i], 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  if (threadIdx.x < kTcC) gs[threadIdx.x] = gamma[threadIdx.x];
+  __syncthreads();
+  // copy group k: rows a_lo + 2k, a_lo + 2k + 1 into buffer k % 3
+  auto issue = [&](int k) {
+    const int buf = k % kSumBufs, a0 = a_lo + k * kSumRows, nr = min(kSumRows, a_hi - a0);
+    mbar_arrive_expect_tx(&full[buf], (uint32_t)nr * ((uint32_t)ncols * (kTcC * 4 + up_cell) + 2 * kTcC * 4));
+    for (int r = 0; r < nr; ++r) {
+      const int64_t p = P0 + (int64_t)(a0 + r) * n + j0;
+      uint8_t* dst = bufs + (size_t)(buf * kSumRows + r) * kSumRowBytes;
+      bulk_load(dst + 2 * kSumHalf, u + (t0 + a0 + r) * kTcC, kTcC * 4, &full[buf]);
+      bulk_load(dst + 2 * kSumHalf + kTcC * 4, dM + (t0 + a0 + r) * kTcC, kTcC * 4, &full[buf]);
+      bulk_load(dst, dY + p * kTcC, (uint32_t)ncols * kTcC * 4, &full[buf]);
+      if (zt_up) bulk_load(dst + kSumHalf, zt_up + p * kTcC, (uint32_t)ncols * up_cell, &full[buf]);
+      else if (dz_up) bulk_load(dst + kSumHalf, dz_up + p * kTcC, (uint32_t)ncols * up_cell, &full[buf]);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int k = 0; k < min(kSumBufs, ngroups); ++k) issue(k);
+  float vv[8];          // the column's v, features 4q.. and 64+4q..
+  {
+    const float* vcol = v + (t0 + (cv ? j : j0)) * kTcC;
+    const float4 v0 = *reinterpret_cast<const float4*>(vcol + 4 * q);
+    const float4 v1 = *reinterpret_cast<const float4*>(vcol + 64 + 4 * q);
+    vv[0] = v0.x; vv[1] = v0.y; vv[2] = v0.z; vv[3] = v0.w;
+    vv[4] = v1.x; vv[5] = v1.y; vv[6] = v1.z; vv[7] = v1.w;
+  }
+  float cs[8], pg[8], pbt[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) { cs[k] = 0.f; pg[k] = 0.f; pbt[k] = 0.f; }
+  const bool hi4 = (lane & 16) != 0;
+  int k = 0;
+  for (; k < ngroups; ++k) {
+    const int buf = k % kSumBufs, a0 = a_lo + k * kSumRows, nr = min(kSumRows, a_hi - a0);
+    // warp-uniform: the row arithmetic below has full-warp shuffles
+    if (mbar_wait_warp(&full[buf], (uint32_t)(k / kSumBufs) & 1, &abort_flag, status)) {
+      for (int r = 0; r < nr; ++r) {
+        const uint8_t* sr = bufs + (size_t)(buf * kSumRows + r) * kSumRowBytes;
+        const float* su = reinterpret_cast<const float*>(sr + 2 * kSumHalf);
+        const float* sdm = su + kTcC;
+        float dy[8], up[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { dy[e] = 0.f; up[e] = 0.f; }
+        if (cv) {
+          const float4 y0 = *reinterpret_cast<const float4*>(sr + slot * kTcC * 4 + 16 * q);
+          const float4 y1 = *reinterpret_cast<const float4*>(sr + slot * kTcC * 4 + 256 + 16 * q);
+          dy[0] = y0.x; dy[1] = y0.y; dy[2] = y0.z; dy[3] = y0.w;
+          dy[4] = y1.x; dy[5] = y1.y; dy[6] = y1.z; dy[7] = y1.w;
+          if (zt_up) {
+            const uint2 w0 = *reinterpret_cast<const uint2*>(sr + kSumHalf + slot * kTcC * 2 + 8 * q);
+            const uint2 w1 = *reinterpret_cast<const uint2*>(sr + kSumHalf + slot * kTcC * 2 + 128 + 8 * q);
+            up[0] = gp * bf16lo(w0.x); up[1] = gp * bf16hi(w0.x); up[2] = gp * bf16lo(w0.y); up[3] = gp * bf16hi(w0.y);
+            up[4] = gp * bf16lo(w1.x); up[5] = gp * bf16hi(w1.x); up[6] = gp * bf16lo(w1.y); up[7] = gp * bf16hi(w1.y);
+          } else if (dz_up) {
+            const float4 u0 = *reinterpret_cast<const float4*>(sr + kSumHalf + slot * kTcC * 4 + 16 * q);
+            const float4 u1 = *reinterpret_cast<const float4*>(sr + kSumHalf + slot * kTcC * 4 + 256 + 16 * q);
+            up[0] = u0.x; up[1] = u0.y; up[2] = u0.z; up[3] = u0.w;
+            up[4] = u1.x; up[5] = u1.y; up[6] = u1.z; up[7] = u1.w;
+          }
+        }
+        // z rebuilt as the forward rounds it; its LayerNorm statistics over
+        // the 16 threads of the column
+        float xh[8], gv[8], gm[8];
+        float s1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int f = 64 * h + 4 * q;
+          const float4 a4 = *reinterpret_cast<const float4*>(su + f);
+          const float4 m4 = *reinterpret_cast<const float4*>(sdm + f);
+          const float za[4] = {a4.x + vv[4 * h], a4.y + vv[4 * h + 1], a4.z + vv[4 * h + 2], a4.w + vv[4 * h + 3]};
+          const float ma[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * h + e;
+            gm[i] = gs[f + e];
+            gv[i] = fmaf(ma[e], inv_n, up[i]);
+            xh[i] = round_io(za[e], (bf16*)nullptr);
+            s1 += xh[i];
+          }
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        const float mean = s1 * (1.0f / kTcC);
+        float s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          xh[i] -= mean;
+          s2 = fmaf(xh[i], xh[i], s2);
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        const float rs = rsqrtf(s2 * (1.0f / kTcC) + eps);
+        float m1 = 0.f, m2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          xh[i] = cv ? xh[i] * rs : 0.f;
+          const float dx = dy[i] * gm[i];
+          m1 += dx;
+          m2 = fmaf(dx, xh[i], m2);
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+          m1 += __shfl_xor_sync(0xffffffffu, m1, o);
+          m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+        }
+        m1 *= 1.0f / kTcC;
+        m2 *= 1.0f / kTcC;
+        float out[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float dx = dy[i] * gm[i];
+          out[i] = cv ? gv[i] + (dx - m1 - xh[i] * m2) * rs : 0.f;
+          cs[i] += out[i];
+          pg[i] = fmaf(dy[i], xh[i], pg[i]);
+          pbt[i] += dy[i];
+        }
+        // the row over the warp's two columns (lane bit 4): the even column
+        // keeps features 4q.. and adds the odd column's copy, the odd column
+        // keeps 64+4q.. and adds the even column's
+        float r4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float send = hi4 ? out[i] : out[i + 4];
+          r4[i] = (hi4 ? out[i + 4] : out[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+        rp[(r * kSumWarps + warp) * (kTcC / 4) + (hi4 ? 16 : 0) + q] = make_float4(r4[0], r4[1], r4[2], r4[3]);
+      }
+    }
+    __syncthreads();
+    if (abort_flag) break;   // read after the barrier: the same in every thread
+    if (threadIdx.x == 0 && k + kSumBufs < ngroups) issue(k + kSumBufs);   // buffer k % 3 has been read
+    {
+      const int f = threadIdx.x & (kTcC - 1), r = threadIdx.x / kTcC;
+      if (r < nr) {
+        const float* rr = reinterpret_cast<const float*>(rp + r * kSumWarps * (kTcC / 4));
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSumWarps; ++w) acc += rr[w * kTcC + f];
+        du_part[(pb0 + (int64_t)cc * n + a0 + r) * kTcC + f] = acc;
+      }
+    }
+    __syncthreads();
+  }
+  if (abort_flag) {
+    // let the copies still in flight land before the CTA's shared memory goes
+    if (threadIdx.x == 0)
+      for (int k2 = k; k2 < min(k + kSumBufs, ngroups); ++k2)
+        mbar_wait(&full[k2 % kSumBufs], (uint32_t)(k2 / kSumBufs) & 1, nullptr, status);
+    return;
+  }
+  if (cv) {
+    float* o = dv_part + (pb0 + (int64_t)rb * n + j) * kTcC;
+    *reinterpret_cast<float4*>(o + 4 * q) = make_float4(cs[0], cs[1], cs[2], cs[3]);
+    *reinterpret_cast<float4*>(o + 64 + 4 * q) = make_float4(cs[4], cs[5], cs[6], cs[7]);
+  }
   if (threadIdx.x < 2 * kTcC) red[threadIdx.x / kTcC][threadIdx.x % kTcC] = 0.f;
   __syncthreads();
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    atomicAdd(&red[0][16 * q + j], pg[j]);
-    atomicAdd(&red[1][16 * q + j], pb[j]);
+  for (int i = 0; i < 8; ++i) {
+    const int f = 64 * (i >> 2) + 4 * q + (i & 3);
+    atomicAdd(&red[0][f], pg[i]);
+    atomicAdd(&red[1][f], pbt[i]);
   }
   __syncthreads();
   if (threadIdx.x < kTcC) {
     atomicAdd(dgamma + threadIdx.x, red[0][threadIdx.x]);
     atomicAdd(dbeta + threadIdx.x, red[1][threadIdx.x]);
+  }
+}
+
+// du[t] = sum over column chunks k of the du partials of row t, dv[t] = sum
+// over row blocks k of the dv partials of column t, in k order.
+__global__ void __launch_bounds__(kThreads)
+sums_finish_kernel(const float* __restrict__ du_part, const float* __restrict__ dv_part,
+                   const int64_t* __restrict__ pair_off, const int32_t* __restrict__ cu,
+                   const int32_t* __restrict__ len, const int32_t* __restrict__ row_sample, int64_t T,
+                   float* __restrict__ du, float* __restrict__ dv) {
+  for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < T * kTcC; e += (int64_t)gridDim.x * kThreads) {
+    const int64_t t = e / kTcC;
+    const int f = (int)(e % kTcC);
+    const int b = row_sample[t];
+    const int n = len[b];
+    const int c = (n + kSumTile - 1) / kSumTile;
+    const int64_t base = sum_part_base(pair_off, cu, b) + (t - cu[b]);
+    float su = 0.f, sv = 0.f;
+    for (int k = 0; k < c; ++k) {
+      su += du_part[(base + (int64_t)k * n) * kTcC + f];
+      sv += dv_part[(base + (int64_t)k * n) * kTcC + f];
+    }
+    du[e] = su;
+    dv[e] = sv;
   }
 }
 
@@ -841,20 +1073,22 @@ __global__ void twice_bf16_kernel(const bf16* __restrict__ in, int R, int Cc, bf
 // Byte offsets of the route's buffers in the workspace past the CUDA-core
 // route's (each 256-byte aligned).
 struct TcLayout {
-  size_t Y, dPt, H, dA, stats, W1t, W2t, W1x2, wg, end;
+  size_t Y, dPt, H, dA, W1t, W2t, W1x2, du_part, dv_part, wg, end;
 };
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-TcLayout tc_layout(int64_t P, int C, int H) {
+TcLayout tc_layout(int64_t P, int64_t T, int C, int H) {
   TcLayout L;
   size_t o = 0;
   L.Y = o; o = align256(o + (size_t)P * 2 * C * 2);   // [hi | lo] rows
   L.dPt = o; o = align256(o + (size_t)P * C * 2);
   L.H = o; o = align256(o + (size_t)P * H * 2);
   L.dA = o; o = align256(o + (size_t)P * H * 2);
-  L.stats = o; o = align256(o + (size_t)P * 8);
   L.W1t = o; o = align256(o + (size_t)C * H * 2);
   L.W2t = o; o = align256(o + (size_t)C * H * 2);
   L.W1x2 = o; o = align256(o + (size_t)2 * C * H * 2);
+  const size_t part_rows = (size_t)(P / kSumTile + T + 1);
+  L.du_part = o; o = align256(o + part_rows * C * 4);
+  L.dv_part = o; o = align256(o + part_rows * C * 4);
   L.wg = o;
   const size_t w1 = wgrad_tc_workspace_bytes(P, H, C), w2 = wgrad_tc_workspace_bytes(P, C, H);
   o = align256(o + (w1 > w2 ? w1 : w2));
@@ -866,15 +1100,16 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
   const nt_partition* p = q.part;
   const int C = q.C_z, H = q.H_t;
   const int64_t P = p->P;
-  const TcLayout L = tc_layout(P, C, H);
+  const TcLayout L = tc_layout(P, p->T, C, H);
   bf16* Y = reinterpret_cast<bf16*>(tcw + L.Y);
   bf16* dPt = reinterpret_cast<bf16*>(tcw + L.dPt);
   bf16* Hm = reinterpret_cast<bf16*>(tcw + L.H);
   bf16* dA = reinterpret_cast<bf16*>(tcw + L.dA);
-  float2* stats = reinterpret_cast<float2*>(tcw + L.stats);
   bf16* W1t = reinterpret_cast<bf16*>(tcw + L.W1t);
   bf16* W2t = reinterpret_cast<bf16*>(tcw + L.W2t);
   bf16* W1x2 = reinterpret_cast<bf16*>(tcw + L.W1x2);
+  float* du_part = reinterpret_cast<float*>(tcw + L.du_part);
+  float* dv_part = reinterpret_cast<float*>(tcw + L.dv_part);
   void* wg = tcw + L.wg;
   const int gcells = (int)min64((P + kPrepCells - 1) / kPrepCells, (int64_t)sm_count() * 8);
   const unsigned gt = (unsigned)min64(((int64_t)C * H + 255) / 256, 1024);
@@ -882,7 +1117,7 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
   transpose_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W2, C, H, W2t);   // W2 [C, H] -> [H, C]
   twice_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W1, H, C, W1x2);       // [W1 | W1], [H, 2C]
   bwd_prep_kernel<<<gcells, kThreads, 0, s>>>(q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, P, q.gamma,
-                                              q.beta, q.eps, q.dM, q.dz_up, Y, dPt, stats);
+                                              q.beta, q.eps, q.dM, q.dz_up, (const bf16*)q.zt_up, Y, dPt);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // H = ReLU([hi | lo] [W1 | W1]^T + b1); dA = (dP~ W2) where H > 0; dY = dA W1 (into the dz buffer)
@@ -894,9 +1129,18 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
   if ((e = launch_linear_tc(0, &g2, 1, P, H, C, status, s)) != cudaSuccess) return e;
   LinearProblem g3 = {dA, W1t, nullptr, nullptr, q.dz};
   if ((e = launch_linear_tc(1, &g3, 1, P, C, H, status, s)) != cudaSuccess) return e;
-  // dz, dgamma, dbeta
-  bwd_ln_kernel<<<gcells, kThreads, 0, s>>>(q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, P, q.gamma,
-                                            stats, q.dM, q.dz_up, q.dz, q.dgamma, q.dbeta);
+  // the LayerNorm backward and the broadcast's: du, dv (dz is not stored), dgamma, dbeta
+  const int64_t items = P / 1024 + p->T / 16 + p->B;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if ((e = cudaFuncSetAttribute(bwd_ln_sums_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem)) !=
+      cudaSuccess)
+    return e;
+  bwd_ln_sums_kernel<<<(unsigned)items, kSumThreads, kSumSmem, s>>>(
+      q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, q.gamma, q.eps, q.dM, q.dz_up, (const bf16*)q.zt_up,
+      q.dz, du_part, dv_part, q.dgamma, q.dbeta, status);
+  sums_finish_kernel<<<(unsigned)min64((p->T * C + kThreads - 1) / kThreads, (int64_t)sm_count() * 8), kThreads, 0,
+                       s>>>(du_part, dv_part, p->pair_off, p->cu_seqlens, p->lengths, p->row_sample, p->T, q.du,
+                            q.dv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // dW1 = dA^T LN(z) (the hi part, every other C_z block of the rows), db1 =
   // sum dA; dW2 = dP~^T H, db2 = sum dP~
@@ -915,7 +1159,7 @@ bool block_bwd_tc(nt_dtype dt, int64_t P, int C_z, int H_t) {
 
 size_t block_bwd_workspace_bytes(nt_dtype dt, int64_t T, int64_t P, int C_z, int H_t) {
   const size_t base = align256((size_t)(5 * T + P) * (size_t)C_z * sizeof(float));
-  return block_bwd_tc(dt, P, C_z, H_t) ? base + tc_layout(P, C_z, H_t).end : base;
+  return block_bwd_tc(dt, P, C_z, H_t) ? base + tc_layout(P, T, C_z, H_t).end : base;
 }
 
 cudaError_t launch_eq5_loss(nt_dtype dt, const nt_partition* p, const void* s_out, int C_s, const void* zt, int C_z,

@@ -175,6 +175,77 @@ cudaError_t project_uv(const nt_partition* part, nt_dtype dtype, const void* s_l
   return e;
 }
 
+// The checks of the backward's arguments that do not depend on how its
+// upstream gradients arrive.
+nt_status check_block_backward(const nt_partition* part, nt_dtype dtype, int32_t C_s, int32_t C_z, int32_t H_t,
+                               float ln_eps) {
+  nt_status st = check_partition(part, true);
+  if (st != NT_OK) return st;
+  if (part->col_lengths && (part->col_lengths != part->lengths || part->col_cu_seqlens != part->cu_seqlens))
+    return fail(NT_ERR_UNSUPPORTED, "the block backward takes square partitions");
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (!width_ok(dtype, C_s) || !width_ok(dtype, C_z) || !block_bwd_supported(C_z, H_t))
+    return fail(NT_ERR_UNSUPPORTED, "C_s=%d, C_z=%d (8..128), H_t=%d (a multiple of 64)", C_s, C_z, H_t);
+  if (!(ln_eps >= 0.0f)) return fail(NT_ERR_INVALID, "ln_eps must be >= 0");
+  return NT_OK;
+}
+
+// The backward proper (arguments checked): zt_up non-NULL only on the
+// tensor-core route, for Eq. 5's upstream pair gradient formed from z~.
+nt_status block_backward_run(const nt_partition* part, nt_dtype dtype, const void* s, int32_t C_s, const void* W_a,
+                             const void* W_b, int32_t C_z, int32_t H_t, const float* ln_gamma, const float* ln_beta,
+                             float ln_eps, const void* W1, const float* b1, const void* W2, const void* W_g,
+                             const void* m, const float* ds_out, const float* dz_tilde, const void* zt_up, float* ds,
+                             float* dW_a, float* dW_b, float* dgamma, float* dbeta, float* dW1, float* db1,
+                             float* dW2, float* db2, float* dW_g, float* db_g, void* workspace, cudaStream_t st_) {
+  // the gradients that are sums start at zero
+  const size_t f4 = sizeof(float);
+  struct { float* p; size_t n; } zero[] = {
+      {dW_a, (size_t)C_z * C_s}, {dW_b, (size_t)C_z * C_s}, {dgamma, (size_t)C_z}, {dbeta, (size_t)C_z},
+      {dW1, (size_t)H_t * C_z}, {db1, (size_t)H_t}, {dW2, (size_t)C_z * H_t}, {db2, (size_t)C_z},
+      {dW_g, (size_t)C_s * C_z}, {db_g, (size_t)C_s}};
+  for (auto& zr : zero) {
+    cudaError_t e = cudaMemsetAsync(zr.p, 0, zr.n * f4, st_);
+    if (e != cudaSuccess) return cuda_fail(e, "gradient clear");
+  }
+  if (part->T == 0) return NT_OK;
+  float* u = static_cast<float*>(workspace);
+  float* v = u + part->T * (int64_t)C_z;
+  float* dM = v + part->T * (int64_t)C_z;
+  float* du = dM + part->T * (int64_t)C_z;
+  float* dv = du + part->T * (int64_t)C_z;
+  float* dz = dv + part->T * (int64_t)C_z;
+  cudaError_t e = project_uv(part, dtype, s, s, C_s, W_a, W_b, C_z, u, v, st_);
+  if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+  // the tensor-core route's buffers follow the CUDA-core route's
+  const size_t base = ((size_t)(5 * part->T + part->P) * (size_t)C_z * sizeof(float) + 255) & ~(size_t)255;
+  void* tc_ws = block_bwd_tc(dtype, part->P, C_z, H_t) ? static_cast<uint8_t*>(workspace) + base : nullptr;
+  BlockBwd q = {part, C_s, C_z, H_t, s, W_a, W_b, ln_gamma, ln_beta, ln_eps, W1, b1, W2, W_g, m, ds_out, dz_tilde,
+                zt_up, ds, dW_a, dW_b, dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g, u, v, dM, dz, du, dv, tc_ws};
+  unsigned int* status = status_word();
+  if (!status) return fail(NT_ERR_CUDA, "device status word unavailable");
+  e = launch_block_backward(dtype, q, status, st_);
+  if (e != cudaSuccess) return cuda_fail(e, "block backward launch");
+  return NT_OK;
+}
+
+// Workspace of the fused loss + backward: the loss's partial sums, dX~
+// ([T, C_s] fp32), on routes other than the tensor-core one dL/dz~ ([P, C_z]
+// fp32), then the backward's own (each part 256-byte aligned).
+struct LossBwdLayout {
+  size_t dx, dz, bwd, end;
+};
+LossBwdLayout loss_bwd_layout(nt_dtype dtype, int64_t T, int64_t P, int32_t C_s, int32_t C_z, int32_t H_t) {
+  auto a256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  LossBwdLayout L;
+  L.dx = a256(eq5_loss_workspace_bytes());
+  L.dz = a256(L.dx + (size_t)T * C_s * sizeof(float));
+  const size_t dz_bytes = block_bwd_tc(dtype, P, C_z, H_t) ? 0 : (size_t)P * C_z * sizeof(float);
+  L.bwd = a256(L.dz + dz_bytes);
+  L.end = L.bwd + block_bwd_workspace_bytes(dtype, T, P, C_z, H_t);
+  return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -666,14 +737,8 @@ nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const
                                  float* ds, float* dW_a, float* dW_b, float* dgamma, float* dbeta, float* dW1,
                                  float* db1, float* dW2, float* db2, float* dW_g, float* db_g, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-  nt_status st = check_partition(part, true);
+  nt_status st = check_block_backward(part, dtype, C_s, C_z, H_t, ln_eps);
   if (st != NT_OK) return st;
-  if (part->col_lengths && (part->col_lengths != part->lengths || part->col_cu_seqlens != part->cu_seqlens))
-    return fail(NT_ERR_UNSUPPORTED, "the block backward takes square partitions");
-  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
-  if (!width_ok(dtype, C_s) || !width_ok(dtype, C_z) || !block_bwd_supported(C_z, H_t))
-    return fail(NT_ERR_UNSUPPORTED, "C_s=%d, C_z=%d (8..128), H_t=%d (a multiple of 64)", C_s, C_z, H_t);
-  if (!(ln_eps >= 0.0f)) return fail(NT_ERR_INVALID, "ln_eps must be >= 0");
   if (!W_a || !W_b || !ln_gamma || !ln_beta || !W1 || !W2 || !W_g || !dW_a || !dW_b || !dgamma || !dbeta ||
       !dW1 || !db1 || !dW2 || !db2 || !dW_g || !db_g || !workspace)
     return fail(NT_ERR_INVALID, "NULL pointer");
@@ -684,36 +749,50 @@ nt_status nt_pair_block_backward(const nt_partition* part, nt_dtype dtype, const
     if (!aligned16(q)) return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
   const size_t need = nt_pair_block_backward_workspace_bytes(dtype, part->T, part->P, C_z, H_t);
   if (workspace_bytes < need) return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  return block_backward_run(part, dtype, s, C_s, W_a, W_b, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W2, W_g, m,
+                            ds_out, dz_tilde, nullptr, ds, dW_a, dW_b, dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g,
+                            workspace, static_cast<cudaStream_t>(stream));
+}
+
+size_t nt_pair_block_loss_backward_workspace_bytes(nt_dtype dtype, int64_t T, int64_t P, int32_t C_s, int32_t C_z,
+                                                   int32_t H_t) {
+  if (T < 0 || P < 0 || C_s < 0 || C_z < 0 || H_t < 0) return 0;
+  return loss_bwd_layout(dtype, T, P, C_s, C_z, H_t).end;
+}
+
+nt_status nt_pair_block_loss_backward(const nt_partition* part, nt_dtype dtype, const void* s, int32_t C_s,
+                                      const void* W_a, const void* W_b, int32_t C_z, int32_t H_t,
+                                      const float* ln_gamma, const float* ln_beta, float ln_eps, const void* W1,
+                                      const float* b1, const void* W2, const void* W_g, const void* m,
+                                      const void* s_out, const void* z_tilde, float* d_loss, float* ds, float* dW_a,
+                                      float* dW_b, float* dgamma, float* dbeta, float* dW1, float* db1, float* dW2,
+                                      float* db2, float* dW_g, float* db_g, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  nt_status st = check_block_backward(part, dtype, C_s, C_z, H_t, ln_eps);
+  if (st != NT_OK) return st;
+  if (!W_a || !W_b || !ln_gamma || !ln_beta || !W1 || !W2 || !W_g || !dW_a || !dW_b || !dgamma || !dbeta ||
+      !dW1 || !db1 || !dW2 || !db2 || !dW_g || !db_g || !d_loss || !workspace)
+    return fail(NT_ERR_INVALID, "NULL pointer");
+  if (part->T > 0 && (!s || !m || !s_out || !ds)) return fail(NT_ERR_INVALID, "NULL single-row pointer");
+  if (part->P > 0 && !z_tilde) return fail(NT_ERR_INVALID, "NULL z_tilde");
+  const void* ptrs[] = {s, W_a, W_b, ln_gamma, ln_beta, W1, b1, W2, W_g, m, s_out, z_tilde, ds, dW_a, dW_b,
+                        dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g, workspace};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  const LossBwdLayout L = loss_bwd_layout(dtype, part->T, part->P, C_s, C_z, H_t);
+  if (workspace_bytes < L.end) return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, L.end);
   cudaStream_t st_ = static_cast<cudaStream_t>(stream);
-  // the gradients that are sums start at zero
-  const size_t f4 = sizeof(float);
-  struct { float* p; size_t n; } zero[] = {
-      {dW_a, (size_t)C_z * C_s}, {dW_b, (size_t)C_z * C_s}, {dgamma, (size_t)C_z}, {dbeta, (size_t)C_z},
-      {dW1, (size_t)H_t * C_z}, {db1, (size_t)H_t}, {dW2, (size_t)C_z * H_t}, {db2, (size_t)C_z},
-      {dW_g, (size_t)C_s * C_z}, {db_g, (size_t)C_s}};
-  for (auto& zr : zero) {
-    cudaError_t e = cudaMemsetAsync(zr.p, 0, zr.n * f4, st_);
-    if (e != cudaSuccess) return cuda_fail(e, "gradient clear");
-  }
-  if (part->T == 0) return NT_OK;
-  float* u = static_cast<float*>(workspace);
-  float* v = u + part->T * (int64_t)C_z;
-  float* dM = v + part->T * (int64_t)C_z;
-  float* du = dM + part->T * (int64_t)C_z;
-  float* dv = du + part->T * (int64_t)C_z;
-  float* dz = dv + part->T * (int64_t)C_z;
-  cudaError_t e = project_uv(part, dtype, s, s, C_s, W_a, W_b, C_z, u, v, st_);
-  if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-  // the tensor-core route's buffers follow the CUDA-core route's
-  const size_t base = ((size_t)(5 * part->T + part->P) * (size_t)C_z * sizeof(float) + 255) & ~(size_t)255;
-  void* tc_ws = block_bwd_tc(dtype, part->P, C_z, H_t) ? static_cast<uint8_t*>(workspace) + base : nullptr;
-  BlockBwd q = {part, C_s, C_z, H_t, s, W_a, W_b, ln_gamma, ln_beta, ln_eps, W1, b1, W2, W_g, m, ds_out, dz_tilde,
-                ds, dW_a, dW_b, dgamma, dbeta, dW1, db1, dW2, db2, dW_g, db_g, u, v, dM, dz, du, dv, tc_ws};
-  unsigned int* status = status_word();
-  if (!status) return fail(NT_ERR_CUDA, "device status word unavailable");
-  e = launch_block_backward(dtype, q, status, st_);
-  if (e != cudaSuccess) return cuda_fail(e, "block backward launch");
-  return NT_OK;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  float* dx = reinterpret_cast<float*>(w + L.dx);
+  const bool tc = block_bwd_tc(dtype, part->P, C_z, H_t);
+  // the loss and dX~; dL/dz~ only where the backward does not form it from z~
+  float* dz = tc ? nullptr : reinterpret_cast<float*>(w + L.dz);
+  cudaError_t e = launch_eq5_loss(dtype, part, s_out, C_s, z_tilde, C_z, d_loss, part->T > 0 ? dx : nullptr,
+                                  part->P > 0 ? dz : nullptr, w, st_);
+  if (e != cudaSuccess) return cuda_fail(e, "loss launch");
+  return block_backward_run(part, dtype, s, C_s, W_a, W_b, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W2, W_g, m,
+                            dx, tc ? nullptr : dz, tc ? z_tilde : nullptr, ds, dW_a, dW_b, dgamma, dbeta, dW1, db1,
+                            dW2, db2, dW_g, db_g, w + L.bwd, st_);
 }
 
 nt_status nt_device_status(void* stream) {

@@ -267,6 +267,10 @@ struct BlockBwd {
   const void* m;
   const float* ds_out;
   const float* dz_up;
+  // the tensor-core route only: when set, the upstream pair gradient is
+  // Eq. 5's, gp_b z~ (z~ [P, C_z] bf16), formed where it is read; dz_up is
+  // then unused
+  const void* zt_up;
   float* ds;
   float* dW_a;
   float* dW_b;

@@ -64,6 +64,10 @@ SIGNATURES = {
     "nt_pair_block_backward_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I32, _I32]),
     "nt_pair_block_backward": (_I32, [_PP, _I32, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nt_pair_block_loss_backward_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I32, _I32, _I32]),
+    "nt_pair_block_loss_backward": (_I32, [_PP, _I32, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P,
+                                           _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                           _P]),
     "nt_varlen_attn_workspace_bytes": (_SZ, []),
     "nt_varlen_attn": (_I32, [_I32, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _F, _P, _P, _P, _SZ, _P]),
     "nt_varlen_attn_qk": (_I32, [_I32, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _F, _I32,
@@ -399,6 +403,44 @@ def nt_pair_block_backward(part: Partition, s: torch.Tensor, w, m: torch.Tensor,
         _ptr(g["db_g"]), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nt_pair_block_backward")
     return g
+
+
+def nt_pair_block_loss_backward(part: Partition, s: torch.Tensor, w, m: torch.Tensor, s_out: torch.Tensor,
+                                z_tilde: torch.Tensor, ln_eps: float = 1e-5, loss: Optional[torch.Tensor] = None,
+                                workspace=None, stream=None):
+    """Eq. 5 on the block's outputs and the block's gradients for it, in one
+    call: returns (loss as a 1-element fp32 device tensor, the gradient dict
+    of :func:`nt_pair_block_backward`).  Equal, value for value, to
+    nt_pair_block_loss followed by nt_pair_block_backward with its gradients;
+    on the tensor-core route dL/dz~ is formed from z~ where it is read."""
+    T, C_s = s.shape
+    C_z = w.W_a.shape[0]
+    H_t = w.W1.shape[0]
+    if s_out.shape[0] != part.T or z_tilde.shape[0] != part.P:
+        raise ValueError("outputs do not match the partition")
+    dev = s.device
+    f = lambda *shape: torch.empty(*shape, dtype=torch.float32, device=dev)
+    g = {"ds": f(T, C_s), "dW_a": f(C_z, C_s), "dW_b": f(C_z, C_s), "dgamma": f(C_z), "dbeta": f(C_z),
+         "dW1": f(H_t, C_z), "db1": f(H_t), "dW2": f(C_z, H_t), "db2": f(C_z), "dW_g": f(C_s, C_z), "db_g": f(C_s)}
+    if loss is None:
+        loss = f(1)
+    need = nt_pair_block_loss_backward_workspace_bytes(_dtype(s), part.T, part.P, C_s, C_z, H_t)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = lib().nt_pair_block_loss_backward(
+        ctypes.byref(part.c), _dtype(s), _ptr(s), C_s, _ptr(w.W_a), _ptr(w.W_b), C_z, H_t, _ptr(_f32(w.ln_gamma)),
+        _ptr(_f32(w.ln_beta)), float(ln_eps), _ptr(w.W1), _ptr(_f32(w.b1)), _ptr(w.W2), _ptr(w.W_g), _ptr(m),
+        _ptr(s_out), _ptr(z_tilde), _ptr(loss), _ptr(g["ds"]), _ptr(g["dW_a"]), _ptr(g["dW_b"]), _ptr(g["dgamma"]),
+        _ptr(g["dbeta"]), _ptr(g["dW1"]), _ptr(g["db1"]), _ptr(g["dW2"]), _ptr(g["db2"]), _ptr(g["dW_g"]),
+        _ptr(g["db_g"]), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nt_pair_block_loss_backward")
+    return loss, g
+
+
+def nt_pair_block_loss_backward_workspace_bytes(dtype: int, T: int, P: int, C_s: int, C_z: int, H_t: int) -> int:
+    """Device workspace bytes of nt_pair_block_loss_backward."""
+    return int(lib().nt_pair_block_loss_backward_workspace_bytes(int(dtype), int(T), int(P), int(C_s), int(C_z),
+                                                                 int(H_t)))
 
 
 def nt_pair_block_backward_workspace_bytes(dtype: int, T: int, P: int, C_z: int, H_t: int) -> int:
