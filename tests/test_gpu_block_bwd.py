@@ -104,7 +104,10 @@ def test_loss_backward_equals_two_calls(nt, route):
     nt_pair_block_backward on the same inputs: the same loss bits on every
     route; on the tensor-core route (where dL/dz~ = gp_i z~ is formed from
     z~ where it is read) also the same ds and split-summed weight gradients,
-    bit for bit; the gradients accumulated with atomics within 1e-6."""
+    bit for bit.  The gradients accumulated with fp32 atomics differ between
+    any two calls by the order of their sums: within 1e-5 normwise (one
+    reordering of an fp32 sum of a few thousand terms, with some
+    cancellation; two plain calls were seen 1.0e-6 apart on dbeta)."""
     cfg, lengths = {"tensor_core": (wl.PAIRFORMER_BF16, [33, 0, 1, 32, 31, 65, 37]),
                     "tensor_core_batch": (wl.PAIRFORMER_BF16, None),
                     "cuda_core_f32": (wl.TINY_FP32, [5, 0, 9, 1]),
@@ -125,7 +128,7 @@ def test_loss_backward_equals_two_calls(nt, route):
         if n in exact:
             assert torch.equal(g1[n], g2[n]), n
         else:
-            assert normwise_err(to_np(g2[n]), to_np(g1[n]), dtype="f32") <= 1e-6, n
+            assert normwise_err(to_np(g2[n]), to_np(g1[n]), dtype="f32") <= 1e-5, n
 
 
 def test_loss_backward_against_oracle(nt):

@@ -205,7 +205,9 @@ constexpr uint32_t kPXBytes = kBM * kBK * 2;              // 16 KB
 constexpr uint32_t kPWBytes = kPN * kBK * 2;              // 16 KB
 constexpr uint32_t kPStageBytes = kPXBytes + kPWBytes;
 constexpr uint32_t kPOffBar = kPStages * kPStageBytes;
-constexpr uint32_t kPSmemBytes = kPOffBar + 256 + 1024;
+constexpr uint32_t kPStgBytes = 32 * 64;                  // an epilogue warp's 32 rows x 64 bytes
+constexpr uint32_t kPOffStg = kPOffBar + 256;
+constexpr uint32_t kPSmemBytes = kPOffStg + 4 * kPStgBytes + 1024;
 constexpr uint32_t kPTmemCols = 2 * kPN;                  // two accumulators
 
 struct PBars {
@@ -292,23 +294,47 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
       mbar_wait(&bar.mma_done, 0, nullptr, status);
     }
   } else {
-    // epilogue: row (warp & 3) * 32 + lane of each tile
+    // epilogue: row (warp & 3) * 32 + lane of each tile.  Rows leave (and
+    // mask or residual rows arrive) through the warp's 32 x 64-byte buffer in
+    // shared memory, so that global accesses are 4 lanes x 16 bytes per row
+    // instead of one lane per row; the 16-byte chunk c of row r sits at
+    // chunk c ^ ((r >> 1) & 3), which keeps both access patterns free of
+    // bank conflicts.
     const int q = warp & 3;
-    const int r = q * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+    uint8_t* stg = smem + kPOffStg + q * kPStgBytes;
+    const int cr = lane >> 2, cc = lane & 3;     // coalesced role: rows cr + 8 i, chunk cc
+    auto stg_at = [&](int r, int c) { return reinterpret_cast<uint4*>(stg + r * 64 + 16 * (c ^ ((r >> 1) & 3))); };
+    // 32 rows x 64 bytes of the warp from the buffer to global rows row0 + r
+    // (row-major, `pitch` bytes apart), rows >= M skipped
+    auto flush = [&](uint8_t* g0, int64_t row0, size_t pitch) {
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = cr + 8 * i;
+        const uint4 val = *stg_at(r, cc);
+        if (row0 + r < M) *reinterpret_cast<uint4*>(g0 + (row0 + r) * pitch + 16 * cc) = val;
+      }
+      __syncwarp();
+    };
     int i = 0;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
       const int b = i & 1;
-      const int64_t row = (t / ntiles) * kBM + r;
+      const int64_t row0 = (t / ntiles) * kBM + q * 32;   // the warp's first row
       const int n0 = (int)(t % ntiles) * kPN;
-      const bool live = row < M;
-      // the row's residual or mask does not depend on the MMAs: its loads
-      // are issued before the accumulator wait
+      // the residual or mask rows do not depend on the MMAs: their loads are
+      // issued before the accumulator wait, 4 lanes per row (group gq, rows
+      // cr + 8 j)
       uint4 rall[kPN / 8];
-      if (pr.R && live) {
-        const uint4* rp = reinterpret_cast<const uint4*>(pr.R + row * N + n0);
+      if (pr.R) {
 #pragma unroll
-        for (int u = 0; u < kPN / 8; ++u) rall[u] = rp[u];
+        for (int gq = 0; gq < kPN / 32; ++gq)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int64_t rw = row0 + cr + 8 * j;
+            rall[4 * gq + j] = rw < M ? *reinterpret_cast<const uint4*>(pr.R + rw * N + n0 + 32 * gq + 8 * cc)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+          }
       }
       if (!mbar_wait_warp(&bar.acc_full[b], (uint32_t)(i >> 1) & 1, abort_flag, status)) break;
       tc_fence_after();
@@ -316,10 +342,18 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
 #pragma unroll
       for (int gq = 0; gq < kPN / 32; ++gq) {
         const int c0 = n0 + 32 * gq;
-        const uint4* rq = rall + 4 * gq;
         float v[32];
         tmem_ld32_sync(tmem + lane_addr + b * kPN + 32 * gq, v);
-        if (!live) continue;
+        uint4 rq[4];
+        if (pr.R) {
+          // the group's rows to one row per lane
+#pragma unroll
+          for (int j = 0; j < 4; ++j) *stg_at(cr + 8 * j, cc) = rall[4 * gq + j];
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) rq[c] = *stg_at(lane, c);
+          __syncwarp();
+        }
         if (pr.bias && pr.epi != kEpiMask) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] += pr.bias[c0 + c];
@@ -344,15 +378,23 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
           }
         }
         if (kOutF32) {
-          float* y = static_cast<float*>(pr.Y) + row * N + c0;
+          // two rounds of 16 columns (64 bytes of fp32)
 #pragma unroll
-          for (int c = 0; c < 32; c += 4) *reinterpret_cast<float4*>(y + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *stg_at(lane, c) = make_uint4(__float_as_uint(v[16 * h + 4 * c]), __float_as_uint(v[16 * h + 4 * c + 1]),
+                                            __float_as_uint(v[16 * h + 4 * c + 2]),
+                                            __float_as_uint(v[16 * h + 4 * c + 3]));
+            flush(reinterpret_cast<uint8_t*>(static_cast<float*>(pr.Y) + c0 + 16 * h), row0, (size_t)N * 4);
+          }
         } else {
-          bf16* y = static_cast<bf16*>(pr.Y) + row * N + c0;
 #pragma unroll
-          for (int c = 0; c < 32; c += 8)
-            *reinterpret_cast<uint4*>(y + c) = make_uint4(pack_bf16x2(v[c], v[c + 1]), pack_bf16x2(v[c + 2], v[c + 3]),
-                                                          pack_bf16x2(v[c + 4], v[c + 5]), pack_bf16x2(v[c + 6], v[c + 7]));
+          for (int c = 0; c < 4; ++c)
+            *stg_at(lane, c) = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                          pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                          pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+          flush(reinterpret_cast<uint8_t*>(static_cast<bf16*>(pr.Y) + c0), row0, (size_t)N * 2);
         }
       }
       tc_fence_before();
