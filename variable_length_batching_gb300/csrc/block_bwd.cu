@@ -656,114 +656,124 @@ using tc::mbar_wait_warp;
 using tc::pack_bf16x2;
 
 constexpr int kTcC = 128;          // pair width of the tensor-core route
-constexpr int kPrepCells = kThreads / 8;   // cells per CTA pass: 8 threads x 16 features each
+// Per pair row t (sample b, row a: cells p0 + j, j < N contiguous), one CTA
+// at a time: 16 threads per cell, thread q owning features 4q..4q+3 and
+// 64+4q..64+4q+3, 16 cells per pass and two passes in flight per thread.
+// The row's sample, u[t], dM[t] and Eq. 5's scale are read once per row;
+// each cell's v, upstream gradient and outputs move 128 to 256 contiguous
+// bytes per instruction.  Per cell: LN(z) as two bf16 parts, hi = bf16(y)
+// and lo = bf16(y - hi), side by side in a row of 2 C_z (A = [hi | lo] [W1 |
+// W1]^T carries y to about 16 bits, so A's sign, the ReLU's decision, is
+// that of the fp32 y), and dP~ = dz_up + dM[row] / N as bf16, with z
+// rebuilt bf16-rounded as the forward rounds it.  With zt_up, dz_up is
+// Eq. 5's gp_b z~, formed here as the loss forms it.
+constexpr int kPrepThreads = 256;
+constexpr int kPrepCells = kPrepThreads / 16;   // cells per pass
 
-// Rows of the route: per cell p, 8 threads own features 16 q .. 16 q + 15.
-// LN(z) as two bf16 parts, hi = bf16(y) and lo = bf16(y - hi), side by side
-// in a row of 2 C_z (A = [hi | lo] [W1 | W1]^T carries y to about 16 bits,
-// so A's sign, the ReLU's decision, is that of the fp32 y) and dP~ = dz_up +
-// dM[row] / N as bf16, with z rebuilt bf16-rounded as the forward rounds
-// it.  With zt_up, dz_up is Eq. 5's gp_b z~, formed here as the loss forms
-// it.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kPrepThreads)
 bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
-                const int32_t* __restrict__ cu, const int32_t* __restrict__ len, int B, int64_t P,
+                const int32_t* __restrict__ cu, const int32_t* __restrict__ len,
+                const int32_t* __restrict__ row_sample, int B, int64_t T, int64_t P,
                 const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
                 const float* __restrict__ dM, const float* __restrict__ dz_up, const bf16* __restrict__ zt_up,
                 bf16* __restrict__ Y, bf16* __restrict__ dPt) {
-  const int q = threadIdx.x & 7;
-  int gp_b = -1;       // the sample whose Eq. 5 scale gp holds (formed in double, so once per sample)
-  float gp = 0.f;
-  for (int64_t p = (int64_t)blockIdx.x * kPrepCells + (threadIdx.x >> 3); p - (threadIdx.x >> 3) < P;
-       p += (int64_t)gridDim.x * kPrepCells) {
-    const bool valid = p < P;
-    int64_t row = 0, col = 0;
-    int n = 1, b = 0;
-    if (valid) cell_coords(pair_off, cu, len, B, p, row, col, n, &b);
-    // dP~ = dz_up + dM[row] / N first: its loads are the ones from HBM (with
-    // zt_up, dz_up = gp_b z~, Eq. 5's, formed here as the loss forms it)
+  const int lane = threadIdx.x & 31, q = threadIdx.x & 15, slot = threadIdx.x >> 4;
+  float gm[8], bt[8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float4 g4 = *reinterpret_cast<const float4*>(gamma + 64 * h + 4 * q);
+    const float4 b4 = *reinterpret_cast<const float4*>(beta + 64 * h + 4 * q);
+    gm[4 * h] = g4.x; gm[4 * h + 1] = g4.y; gm[4 * h + 2] = g4.z; gm[4 * h + 3] = g4.w;
+    bt[4 * h] = b4.x; bt[4 * h + 1] = b4.y; bt[4 * h + 2] = b4.z; bt[4 * h + 3] = b4.w;
+  }
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    const int b = row_sample[t];
+    const int n = len[b];
+    const int64_t p0 = pair_off[b] + (t - cu[b]) * n;
     const float inv_n = 1.0f / (float)n;
-    float up[16];
+    // Eq. 5's scale of the sample, formed in double by one lane per warp
+    float gp = 0.f;
     if (zt_up) {
-      if (b != gp_b) {
-        gp = eq5_pair_scale(b, B, kTcC, P);
-        gp_b = b;
+      if (lane == 0) gp = eq5_pair_scale(b, B, kTcC, P);
+      gp = __shfl_sync(0xffffffffu, gp, 0);
+    }
+    float ur[8], mr[8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float4 a4 = *reinterpret_cast<const float4*>(u + t * kTcC + 64 * h + 4 * q);
+      const float4 m4 = *reinterpret_cast<const float4*>(dM + t * kTcC + 64 * h + 4 * q);
+      ur[4 * h] = a4.x; ur[4 * h + 1] = a4.y; ur[4 * h + 2] = a4.z; ur[4 * h + 3] = a4.w;
+      mr[4 * h] = m4.x; mr[4 * h + 1] = m4.y; mr[4 * h + 2] = m4.z; mr[4 * h + 3] = m4.w;
+    }
+    const int64_t col0 = cu[b];
+    for (int j0 = 0; j0 < n; j0 += 2 * kPrepCells) {
+      float z[2][8], up[2][8];
+      bool ok[2];
+      // loads of both cells first
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int j = j0 + c * kPrepCells + slot;
+        ok[c] = j < n;
+        const int64_t p = p0 + j;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int f = 64 * h + 4 * q;
+          float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f), d4 = v4;
+          if (ok[c]) {
+            v4 = *reinterpret_cast<const float4*>(v + (col0 + j) * kTcC + f);
+            if (zt_up) {
+              const uint2 w = *reinterpret_cast<const uint2*>(zt_up + p * kTcC + f);
+              d4 = make_float4(gp * bf16lo(w.x), gp * bf16hi(w.x), gp * bf16lo(w.y), gp * bf16hi(w.y));
+            } else if (dz_up) {
+              d4 = *reinterpret_cast<const float4*>(dz_up + p * kTcC + f);
+            }
+          }
+          z[c][4 * h] = v4.x; z[c][4 * h + 1] = v4.y; z[c][4 * h + 2] = v4.z; z[c][4 * h + 3] = v4.w;
+          up[c][4 * h] = d4.x; up[c][4 * h + 1] = d4.y; up[c][4 * h + 2] = d4.z; up[c][4 * h + 3] = d4.w;
+        }
       }
-      if (valid) {
-        load_vec(zt_up + p * kTcC + 16 * q, up);
-        load_vec(zt_up + p * kTcC + 16 * q + 8, up + 8);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float s1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          z[c][i] = round_io(ur[i] + z[c][i], (bf16*)nullptr);
+          s1 += z[c][i];
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        const float mean = s1 * (1.0f / kTcC);
+        float s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float d = z[c][i] - mean;
+          s2 = fmaf(d, d, s2);
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        const float rs = rsqrtf(s2 * (1.0f / kTcC) + eps);
+        if (!ok[c]) continue;
+        const int64_t p = p0 + j0 + c * kPrepCells + slot;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t yw[2], lw[2], gw[2];
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int i = 4 * h + e;
+            const float y0 = fmaf((z[c][i] - mean) * rs, gm[i], bt[i]);
+            const float y1 = fmaf((z[c][i + 1] - mean) * rs, gm[i + 1], bt[i + 1]);
+            const float h0 = round_io(y0, (bf16*)nullptr), h1 = round_io(y1, (bf16*)nullptr);
+            yw[e / 2] = pack_bf16x2(y0, y1);
+            lw[e / 2] = pack_bf16x2(y0 - h0, y1 - h1);
+            gw[e / 2] = pack_bf16x2(fmaf(mr[i], inv_n, up[c][i]), fmaf(mr[i + 1], inv_n, up[c][i + 1]));
+          }
+          const int f = 64 * h + 4 * q;
+          *reinterpret_cast<uint2*>(Y + p * 2 * kTcC + f) = make_uint2(yw[0], yw[1]);
+          *reinterpret_cast<uint2*>(Y + p * 2 * kTcC + kTcC + f) = make_uint2(lw[0], lw[1]);
+          *reinterpret_cast<uint2*>(dPt + p * kTcC + f) = make_uint2(gw[0], gw[1]);
+        }
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) up[j] = valid ? gp * up[j] : 0.f;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; j += 4) {
-        float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid && dz_up) u4 = *reinterpret_cast<const float4*>(dz_up + p * kTcC + 16 * q + j);
-        up[j] = u4.x; up[j + 1] = u4.y; up[j + 2] = u4.z; up[j + 3] = u4.w;
-      }
     }
-    float gv[16];
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      float4 m4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (valid) m4 = *reinterpret_cast<const float4*>(dM + row * kTcC + 16 * q + j);
-      gv[j] = fmaf(m4.x, inv_n, up[j]);
-      gv[j + 1] = fmaf(m4.y, inv_n, up[j + 1]);
-      gv[j + 2] = fmaf(m4.z, inv_n, up[j + 2]);
-      gv[j + 3] = fmaf(m4.w, inv_n, up[j + 3]);
-    }
-    float z[16];
-    float s1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-      if (valid) {
-        a = *reinterpret_cast<const float4*>(u + row * kTcC + 16 * q + j);
-        b = *reinterpret_cast<const float4*>(v + col * kTcC + 16 * q + j);
-      }
-      z[j] = round_io(a.x + b.x, (bf16*)nullptr);
-      z[j + 1] = round_io(a.y + b.y, (bf16*)nullptr);
-      z[j + 2] = round_io(a.z + b.z, (bf16*)nullptr);
-      z[j + 3] = round_io(a.w + b.w, (bf16*)nullptr);
-      s1 += (z[j] + z[j + 1]) + (z[j + 2] + z[j + 3]);
-    }
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 4);
-    const float mean = s1 * (1.0f / kTcC);
-    float s2 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float d = z[j] - mean;
-      s2 = fmaf(d, d, s2);
-    }
-    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
-    s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
-    s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
-    const float rs = rsqrtf(s2 * (1.0f / kTcC) + eps);
-    if (!valid) continue;
-    uint32_t yw[8], lw[8], gw[8];
-#pragma unroll
-    for (int j = 0; j < 16; j += 2) {
-      const int f = 16 * q + j;
-      const float y0 = fmaf((z[j] - mean) * rs, gamma[f], beta[f]);
-      const float y1 = fmaf((z[j + 1] - mean) * rs, gamma[f + 1], beta[f + 1]);
-      const float h0 = round_io(y0, (bf16*)nullptr), h1 = round_io(y1, (bf16*)nullptr);
-      lw[j / 2] = pack_bf16x2(y0 - h0, y1 - h1);
-      const float g0 = gv[j], g1 = gv[j + 1];
-      yw[j / 2] = pack_bf16x2(y0, y1);
-      gw[j / 2] = pack_bf16x2(g0, g1);
-    }
-    uint4* yo = reinterpret_cast<uint4*>(Y + p * 2 * kTcC + 16 * q);
-    uint4* lo = reinterpret_cast<uint4*>(Y + p * 2 * kTcC + kTcC + 16 * q);
-    uint4* go = reinterpret_cast<uint4*>(dPt + p * kTcC + 16 * q);
-    yo[0] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
-    yo[1] = make_uint4(yw[4], yw[5], yw[6], yw[7]);
-    lo[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    lo[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-    go[0] = make_uint4(gw[0], gw[1], gw[2], gw[3]);
-    go[1] = make_uint4(gw[4], gw[5], gw[6], gw[7]);
   }
 }
 
@@ -1111,13 +1121,13 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
   float* du_part = reinterpret_cast<float*>(tcw + L.du_part);
   float* dv_part = reinterpret_cast<float*>(tcw + L.dv_part);
   void* wg = tcw + L.wg;
-  const int gcells = (int)min64((P + kPrepCells - 1) / kPrepCells, (int64_t)sm_count() * 8);
   const unsigned gt = (unsigned)min64(((int64_t)C * H + 255) / 256, 1024);
   transpose_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W1, H, C, W1t);   // W1 [H, C] -> [C, H]
   transpose_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W2, C, H, W2t);   // W2 [C, H] -> [H, C]
   twice_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W1, H, C, W1x2);       // [W1 | W1], [H, 2C]
-  bwd_prep_kernel<<<gcells, kThreads, 0, s>>>(q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, P, q.gamma,
-                                              q.beta, q.eps, q.dM, q.dz_up, (const bf16*)q.zt_up, Y, dPt);
+  bwd_prep_kernel<<<(unsigned)min64(p->T, (int64_t)sm_count() * 16), kPrepThreads, 0, s>>>(
+      q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->row_sample, p->B, p->T, P, q.gamma, q.beta, q.eps, q.dM,
+      q.dz_up, (const bf16*)q.zt_up, Y, dPt);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // H = ReLU([hi | lo] [W1 | W1]^T + b1); dA = (dP~ W2) where H > 0; dY = dA W1 (into the dz buffer)
