@@ -22,8 +22,9 @@
 // the tensor cores, through the cells' row-major intermediates:
 //   bwd_prep      per cell: LN(z) and dP~ as bf16 rows, the LayerNorm's mean
 //                 and rstd
-//   tcgen05 GEMMs H = ReLU(LN(z) W1^T + b1), dA = (dP~ W2) where H > 0,
-//                 dY = dA W1 (linear_tc), dW1 = dA^T LN(z), dW2 = dP~^T H,
+//   tcgen05 GEMMs H = ReLU(LN(z) W1^T + b1) and dA = (dP~ W2) where H > 0
+//                 in one kernel (both accumulators per tile), dY = dA W1
+//                 (linear_tc), dW1 = dA^T LN(z), dW2 = dP~^T H,
 //                 db1, db2 (wgrad_tc: split over the cells)
 //   bwd_ln_sums   per 32 x 32 cell item: the LayerNorm backward -> dz in
 //                 registers, summed at once into row and column partials of
@@ -1130,13 +1131,10 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
       q.dz_up, (const bf16*)q.zt_up, Y, dPt);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // H = ReLU([hi | lo] [W1 | W1]^T + b1); dA = (dP~ W2) where H > 0; dY = dA W1 (into the dz buffer)
-  LinearProblem g1 = {Y, W1x2, q.b1, nullptr, Hm};
-  g1.epi = kEpiRelu;
-  if ((e = launch_linear_tc(0, &g1, 1, P, H, 2 * C, status, s)) != cudaSuccess) return e;
-  LinearProblem g2 = {dPt, W2t, nullptr, Hm, dA};
-  g2.epi = kEpiMask;
-  if ((e = launch_linear_tc(0, &g2, 1, P, H, C, status, s)) != cudaSuccess) return e;
+  // H = ReLU([hi | lo] [W1 | W1]^T + b1) and dA = (dP~ W2) where H > 0, per tile in one
+  // kernel; dY = dA W1 (into the dz buffer)
+  if ((e = launch_linear_tc_dual(Y, W1x2, q.b1, dPt, W2t, Hm, dA, P, H, 2 * C, C, status, s)) != cudaSuccess)
+    return e;
   LinearProblem g3 = {dA, W1t, nullptr, nullptr, q.dz};
   if ((e = launch_linear_tc(1, &g3, 1, P, C, H, status, s)) != cudaSuccess) return e;
   // the LayerNorm backward and the broadcast's: du, dv (dz is not stored), dgamma, dbeta

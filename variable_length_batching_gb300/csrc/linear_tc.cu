@@ -219,16 +219,22 @@ struct PBars {
 };
 static_assert(sizeof(PBars) <= 256, "barrier block");
 
-template <bool kOutF32>
+// kDual: two problems per output tile, A = X W^T (K) and B = X2 W2^T (K2),
+// into two accumulators (one pair per CTA; the SM's other CTA overlaps the
+// epilogue); Y = ReLU(A + bias) and Y2 = B where bf16(Y) > 0, both bf16.
+template <bool kOutF32, bool kDual>
 __global__ void __launch_bounds__(kPThreads)
-linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw, Prob pr,
-                            int64_t M, int N, int K, unsigned int* status) {
+linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw,
+                            const __grid_constant__ CUtensorMap tx2, const __grid_constant__ CUtensorMap tw2, Prob pr,
+                            bf16* Y2, int64_t M, int N, int K, int K2, unsigned int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   PBars& bar = *reinterpret_cast<PBars*>(smem + kPOffBar);
   volatile int* abort_flag = &bar.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = N / kPN, nkb = K / kBK;
+  const int nkt = nkb + (kDual ? K2 / kBK : 0);        // k blocks per tile
+  constexpr int kBufs = kDual ? 1 : 2;                  // accumulators (pairs) in turn
   const int64_t tiles = (M + kBM - 1) / kBM * ntiles;
 
   if (threadIdx.x == 0) {
@@ -250,16 +256,19 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tmap(&tx); prefetch_tmap(&tw);
+      if (kDual) { prefetch_tmap(&tx2); prefetch_tmap(&tw2); }
       int64_t g = 0;                              // k blocks issued, over all tiles
       bool ok = true;
       for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const int m0 = (int)(t / ntiles) * kBM, n0 = (int)(t % ntiles) * kPN;
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
+        for (int kb = 0; kb < nkt; ++kb, ++g) {
           const int st = (int)(g % kPStages);
           if (!(ok = mbar_wait(&bar.empty[st], (uint32_t)((g / kPStages) & 1) ^ 1, abort_flag, status))) break;
           mbar_arrive_expect_tx(&bar.full[st], kPStageBytes);
-          tma_load_2d(smem + st * kPStageBytes, &tx, &bar.full[st], kb * kBK, m0);
-          tma_load_2d(smem + st * kPStageBytes + kPXBytes, &tw, &bar.full[st], kb * kBK, n0);
+          const bool second = kDual && kb >= nkb;
+          const int kx = (second ? kb - nkb : kb) * kBK;
+          tma_load_2d(smem + st * kPStageBytes, second ? &tx2 : &tx, &bar.full[st], kx, m0);
+          tma_load_2d(smem + st * kPStageBytes + kPXBytes, second ? &tw2 : &tw, &bar.full[st], kx, n0);
         }
       }
       // drain the copies this thread issued
@@ -274,18 +283,24 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
       int i = 0;                                  // tiles of this CTA
       bool ok = true;
       for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++i) {
-        const int b = i & 1;
-        // the accumulator is free once the epilogue has read tile i - 2 out of it
-        if (i >= 2 && !(ok = mbar_wait(&bar.acc_empty[b], (uint32_t)((i >> 1) - 1) & 1, abort_flag, status))) break;
+        const int b = i % kBufs;
+        // the accumulator is free once the epilogue has read tile i - kBufs out of it
+        if (i >= kBufs &&
+            !(ok = mbar_wait(&bar.acc_empty[b], (uint32_t)((i / kBufs) - 1) & 1, abort_flag, status)))
+          break;
         tc_fence_after();
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
+        for (int kb = 0; kb < nkt; ++kb, ++g) {
           const int st = (int)(g % kPStages);
           if (!(ok = mbar_wait(&bar.full[st], (uint32_t)((g / kPStages) & 1), abort_flag, status))) break;
           tc_fence_after();
           const uint32_t a = base + st * kPStageBytes, w = a + kPXBytes;
+          // dual: the first problem into columns 0.., the second into kPN..
+          const bool second = kDual && kb >= nkb;
+          const uint32_t acc = tmem + (kDual ? (second ? kPN : 0) : b * kPN);
+          const bool first_kb = second ? kb == nkb : kb == 0;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16(tmem + b * kPN, sdesc_k128(a + k * 32), sdesc_k128(w + k * 32), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            mma_bf16(acc, sdesc_k128(a + k * 32), sdesc_k128(w + k * 32), idesc, (!first_kb || k > 0) ? 1u : 0u);
           mma_commit(&bar.empty[st]);
         }
         if (ok) mma_commit(&bar.acc_full[b]);
@@ -319,14 +334,14 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
     };
     int i = 0;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
-      const int b = i & 1;
+      const int b = i % kBufs;
       const int64_t row0 = (t / ntiles) * kBM + q * 32;   // the warp's first row
       const int n0 = (int)(t % ntiles) * kPN;
       // the residual or mask rows do not depend on the MMAs: their loads are
       // issued before the accumulator wait, 4 lanes per row (group gq, rows
       // cr + 8 j)
       uint4 rall[kPN / 8];
-      if (pr.R) {
+      if (!kDual && pr.R) {
 #pragma unroll
         for (int gq = 0; gq < kPN / 32; ++gq)
 #pragma unroll
@@ -336,9 +351,38 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
                                       : make_uint4(0u, 0u, 0u, 0u);
           }
       }
-      if (!mbar_wait_warp(&bar.acc_full[b], (uint32_t)(i >> 1) & 1, abort_flag, status)) break;
+      if (!mbar_wait_warp(&bar.acc_full[b], (uint32_t)(i / kBufs) & 1, abort_flag, status)) break;
       tc_fence_after();
       __syncwarp();
+      if (kDual) {
+#pragma unroll 1
+        for (int gq = 0; gq < kPN / 32; ++gq) {
+          const int c0 = n0 + 32 * gq;
+          float v[32];
+          uint32_t hw[16];
+          tmem_ld32_sync(tmem + lane_addr + 32 * gq, v);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float b0 = pr.bias ? pr.bias[c0 + 2 * c] : 0.f, b1 = pr.bias ? pr.bias[c0 + 2 * c + 1] : 0.f;
+            hw[c] = pack_bf16x2(fmaxf(v[2 * c] + b0, 0.f), fmaxf(v[2 * c + 1] + b1, 0.f));
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) *stg_at(lane, c) = make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+          flush(reinterpret_cast<uint8_t*>(static_cast<bf16*>(pr.Y) + c0), row0, (size_t)N * 2);
+          tmem_ld32_sync(tmem + lane_addr + kPN + 32 * gq, v);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (!(bf16lo(hw[c]) > 0.f)) v[2 * c] = 0.f;
+            if (!(bf16hi(hw[c]) > 0.f)) v[2 * c + 1] = 0.f;
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *stg_at(lane, c) = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                          pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                          pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+          flush(reinterpret_cast<uint8_t*>(Y2 + c0), row0, (size_t)N * 2);
+        }
+      } else
 #pragma unroll
       for (int gq = 0; gq < kPN / 32; ++gq) {
         const int c0 = n0 + 32 * gq;
@@ -418,6 +462,29 @@ bool linear_tc_supported(int in_dtype, int64_t M, int N, int K) {
   return in_dtype == NT_BF16 && M > 0 && N % kBN == 0 && K % kBK == 0 && K > 0 && M < 0x7fffffffLL - kBM;
 }
 
+cudaError_t launch_linear_tc_dual(const void* X, const void* W, const float* bias, const void* X2, const void* W2,
+                                  void* Y, void* Y2, int64_t M, int N, int K, int K2, unsigned int* status,
+                                  cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  if (N % kPN != 0 || K % kBK != 0 || K2 % kBK != 0 || K <= 0 || K2 <= 0 || M >= 0x7fffffffLL - kBM)
+    return cudaErrorInvalidValue;
+  const int64_t ptiles = (M + kBM - 1) / kBM * (N / kPN);
+  CUtensorMap px, pw, px2, pw2;
+  if (!make_tmap_rows(&px, X, (uint64_t)K, (uint64_t)M, kBM) || !make_tmap_rows(&pw, W, (uint64_t)K, (uint64_t)N, kPN) ||
+      !make_tmap_rows(&px2, X2, (uint64_t)K2, (uint64_t)M, kBM) ||
+      !make_tmap_rows(&pw2, W2, (uint64_t)K2, (uint64_t)N, kPN))
+    return cudaErrorInvalidValue;
+  const Prob pp0 = Prob{bias, nullptr, Y, kEpiRelu};
+  const int grid = (int)min64(ptiles, (int64_t)2 * sm_count());
+  auto kern = linear_tc_persistent_kernel<false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(kern, dim3(grid), dim3(kPThreads), kPSmemBytes, s, px, pw, px2, pw2, pp0, static_cast<bf16*>(Y2), M,
+                 N, K, K2, status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob, int64_t M, int N, int K,
                              unsigned int* status, cudaStream_t s) {
   if (M == 0 || nprob == 0) return cudaSuccess;
@@ -431,10 +498,11 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
       return cudaErrorInvalidValue;
     const Prob pp0 = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y, lp.epi};
     const int grid = (int)min64(ptiles, (int64_t)2 * sm_count());
-    auto kern = out_f32 ? linear_tc_persistent_kernel<true> : linear_tc_persistent_kernel<false>;
+    auto kern = out_f32 ? linear_tc_persistent_kernel<true, false> : linear_tc_persistent_kernel<false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3(grid), dim3(kPThreads), kPSmemBytes, s, px, pw, pp0, M, N, K, status);
+    e = launch_pdl(kern, dim3(grid), dim3(kPThreads), kPSmemBytes, s, px, pw, px, pw, pp0, (bf16*)nullptr, M, N, K,
+                   0, status);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }

@@ -158,6 +158,13 @@ cudaError_t launch_linear(int in_dtype /*nt_dtype of X, W, R*/, int out_f32 /*Y 
 bool linear_tc_supported(int in_dtype, int64_t M, int N, int K);
 cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob, int64_t M, int N, int K,
                              unsigned int* status, cudaStream_t s);
+// Two problems on one output tile grid, as the block backward needs them:
+// Y = ReLU(X W^T + bias) and Y2 = (X2 W2^T) where bf16(Y) > 0 (X [M, K],
+// W [N, K], X2 [M, K2], W2 [N, K2], Y and Y2 [M, N], all bf16 row-major;
+// N % 128 == 0, K and K2 multiples of 64).  Persistent CTAs.
+cudaError_t launch_linear_tc_dual(const void* X, const void* W, const float* bias, const void* X2, const void* W2,
+                                  void* Y, void* Y2, int64_t M, int N, int K, int K2, unsigned int* status,
+                                  cudaStream_t s);
 
 cudaError_t launch_broadcast(nt_dtype dt, const float* u, const float* v, const nt_partition* p,
                              int C_z, void* z, cudaStream_t s);
