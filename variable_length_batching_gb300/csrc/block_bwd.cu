@@ -650,6 +650,9 @@ using tc::bf16hi;
 using tc::bf16lo;
 using tc::bulk_load;
 using tc::fence_mbar_init;
+using tc::fmul2;
+using tc::fadd2;
+using tc::ffma2;
 using tc::mbar_arrive_expect_tx;
 using tc::mbar_init;
 using tc::mbar_wait;
@@ -929,45 +932,59 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
           }
         }
         // z rebuilt as the forward rounds it; its LayerNorm statistics over
-        // the 16 threads of the column
-        float xh[8], gv[8], gm[8];
-        float s1 = 0.f;
+        // the 16 threads of the column.  Elementwise work in fp32 pairs; a
+        // column past the sample's end takes rstd = 1/N = 0, so its x-hat,
+        // dP~ and dz are exactly 0 (dy and up are 0 there already).
+        float xh[8], gv[8], dx[8];
+        {
+          const float4 a0 = *reinterpret_cast<const float4*>(su + 4 * q);
+          const float4 a1 = *reinterpret_cast<const float4*>(su + 64 + 4 * q);
+          const float4 m0 = *reinterpret_cast<const float4*>(sdm + 4 * q);
+          const float4 m1v = *reinterpret_cast<const float4*>(sdm + 64 + 4 * q);
+          const float4 g0 = *reinterpret_cast<const float4*>(gs + 4 * q);
+          const float4 g1 = *reinterpret_cast<const float4*>(gs + 64 + 4 * q);
+          const float ua[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const float ma[8] = {m0.x, m0.y, m0.z, m0.w, m1v.x, m1v.y, m1v.z, m1v.w};
+          const float ga[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          const float in_c = cv ? inv_n : 0.f;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int f = 64 * h + 4 * q;
-          const float4 a4 = *reinterpret_cast<const float4*>(su + f);
-          const float4 m4 = *reinterpret_cast<const float4*>(sdm + f);
-          const float za[4] = {a4.x + vv[4 * h], a4.y + vv[4 * h + 1], a4.z + vv[4 * h + 2], a4.w + vv[4 * h + 3]};
-          const float ma[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 4 * h + e;
-            gm[i] = gs[f + e];
-            gv[i] = fmaf(ma[e], inv_n, up[i]);
-            xh[i] = round_io(za[e], (bf16*)nullptr);
-            s1 += xh[i];
+          for (int i = 0; i < 8; i += 2) {
+            float z0, z1;
+            fadd2(ua[i], ua[i + 1], vv[i], vv[i + 1], z0, z1);
+            const uint32_t zw = pack_bf16x2(z0, z1);
+            xh[i] = bf16lo(zw);
+            xh[i + 1] = bf16hi(zw);
+            ffma2(ma[i], ma[i + 1], in_c, in_c, up[i], up[i + 1], gv[i], gv[i + 1]);
+            fmul2(dy[i], dy[i + 1], ga[i], ga[i + 1], dx[i], dx[i + 1]);
           }
         }
+        float sa, sb;
+        fadd2(xh[0], xh[1], xh[2], xh[3], sa, sb);
+        fadd2(sa, sb, xh[4], xh[5], sa, sb);
+        fadd2(sa, sb, xh[6], xh[7], sa, sb);
+        float s1 = sa + sb;
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
         const float mean = s1 * (1.0f / kTcC);
-        float s2 = 0.f;
+        sa = 0.f;
+        sb = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          xh[i] -= mean;
-          s2 = fmaf(xh[i], xh[i], s2);
+        for (int i = 0; i < 8; i += 2) {
+          fadd2(xh[i], xh[i + 1], -mean, -mean, xh[i], xh[i + 1]);
+          ffma2(xh[i], xh[i + 1], xh[i], xh[i + 1], sa, sb, sa, sb);
         }
+        float s2 = sa + sb;
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-        const float rs = rsqrtf(s2 * (1.0f / kTcC) + eps);
-        float m1 = 0.f, m2 = 0.f;
+        const float rs = cv ? rsqrtf(s2 * (1.0f / kTcC) + eps) : 0.f;
+        float m1a = 0.f, m1b = 0.f, m2a = 0.f, m2b = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          xh[i] = cv ? xh[i] * rs : 0.f;
-          const float dx = dy[i] * gm[i];
-          m1 += dx;
-          m2 = fmaf(dx, xh[i], m2);
+        for (int i = 0; i < 8; i += 2) {
+          fmul2(xh[i], xh[i + 1], rs, rs, xh[i], xh[i + 1]);
+          fadd2(m1a, m1b, dx[i], dx[i + 1], m1a, m1b);
+          ffma2(dx[i], dx[i + 1], xh[i], xh[i + 1], m2a, m2b, m2a, m2b);
         }
+        float m1 = m1a + m1b, m2 = m2a + m2b;
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) {
           m1 += __shfl_xor_sync(0xffffffffu, m1, o);
@@ -977,12 +994,14 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
         m2 *= 1.0f / kTcC;
         float out[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float dx = dy[i] * gm[i];
-          out[i] = cv ? gv[i] + (dx - m1 - xh[i] * m2) * rs : 0.f;
-          cs[i] += out[i];
-          pg[i] = fmaf(dy[i], xh[i], pg[i]);
-          pbt[i] += dy[i];
+        for (int i = 0; i < 8; i += 2) {
+          float t0, t1;
+          fadd2(dx[i], dx[i + 1], -m1, -m1, t0, t1);                  // dxhat - mean(dxhat)
+          ffma2(xh[i], xh[i + 1], -m2, -m2, t0, t1, t0, t1);          // - xhat mean(dxhat xhat)
+          ffma2(t0, t1, rs, rs, gv[i], gv[i + 1], out[i], out[i + 1]);  // dP~ + (...) rstd
+          fadd2(cs[i], cs[i + 1], out[i], out[i + 1], cs[i], cs[i + 1]);
+          ffma2(dy[i], dy[i + 1], xh[i], xh[i + 1], pg[i], pg[i + 1], pg[i], pg[i + 1]);
+          fadd2(pbt[i], pbt[i + 1], dy[i], dy[i + 1], pbt[i], pbt[i + 1]);
         }
         // the row over the warp's two columns (lane bit 4): the even column
         // keeps features 4q.. and adds the odd column's copy, the odd column
