@@ -199,19 +199,31 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
 // ---------------------------------------------------------------- persistent
 
 constexpr int kPN = 128;                                  // output columns per tile
-constexpr int kPStages = 3;
-constexpr int kPThreads = 6 * 32;
 constexpr uint32_t kPXBytes = kBM * kBK * 2;              // 16 KB
 constexpr uint32_t kPWBytes = kPN * kBK * 2;              // 16 KB
 constexpr uint32_t kPStageBytes = kPXBytes + kPWBytes;
-constexpr uint32_t kPOffBar = kPStages * kPStageBytes;
 constexpr uint32_t kPStgBytes = 32 * 64;                  // an epilogue warp's 32 rows x 64 bytes
-constexpr uint32_t kPOffStg = kPOffBar + 256;
-constexpr uint32_t kPSmemBytes = kPOffStg + 4 * kPStgBytes + 1024;
-constexpr uint32_t kPTmemCols = 2 * kPN;                  // two accumulators
+constexpr int kPMaxStages = 6;
+
+// One problem per tile: two CTAs per SM, each with a 3-stage ring, two
+// 128-column accumulators used in turn and 4 epilogue warps.  Two problems
+// (dual): one CTA per SM with a 5-stage ring, two accumulator pairs (all
+// 512 columns) used in turn and 8 epilogue warps (each lane quadrant split
+// into two column halves).
+template <bool kDual>
+struct PCfg {
+  static constexpr int kStages = kDual ? 5 : 3;
+  static constexpr int kEpiWarps = kDual ? 8 : 4;
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;
+  static constexpr uint32_t kTmemCols = kDual ? 4 * kPN : 2 * kPN;
+  static constexpr uint32_t kOffBar = kStages * kPStageBytes;
+  static constexpr uint32_t kOffStg = kOffBar + 256;
+  static constexpr uint32_t kSmemBytes = kOffStg + kEpiWarps * kPStgBytes + 1024;
+  static constexpr int kCtasPerSm = kDual ? 1 : 2;
+};
 
 struct PBars {
-  uint64_t full[kPStages], empty[kPStages];
+  uint64_t full[kPMaxStages], empty[kPMaxStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -220,32 +232,34 @@ struct PBars {
 static_assert(sizeof(PBars) <= 256, "barrier block");
 
 // kDual: two problems per output tile, A = X W^T (K) and B = X2 W2^T (K2),
-// into two accumulators (one pair per CTA; the SM's other CTA overlaps the
-// epilogue); Y = ReLU(A + bias) and Y2 = B where bf16(Y) > 0, both bf16.
+// into one accumulator pair; Y = ReLU(A + bias) and Y2 = B where bf16(Y) >
+// 0, both bf16.
 template <bool kOutF32, bool kDual>
-__global__ void __launch_bounds__(kPThreads)
+__global__ void __launch_bounds__(PCfg<kDual>::kThreads)
 linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw,
                             const __grid_constant__ CUtensorMap tx2, const __grid_constant__ CUtensorMap tw2, Prob pr,
                             bf16* Y2, int64_t M, int N, int K, int K2, unsigned int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  PBars& bar = *reinterpret_cast<PBars*>(smem + kPOffBar);
+  using C = PCfg<kDual>;
+  constexpr int kPStages = C::kStages;
+  PBars& bar = *reinterpret_cast<PBars*>(smem + C::kOffBar);
   volatile int* abort_flag = &bar.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = N / kPN, nkb = K / kBK;
   const int nkt = nkb + (kDual ? K2 / kBK : 0);        // k blocks per tile
-  constexpr int kBufs = kDual ? 1 : 2;                  // accumulators (pairs) in turn
+  constexpr int kBufs = 2;                              // accumulators (pairs) in turn
   const int64_t tiles = (M + kBM - 1) / kBM * ntiles;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) { mbar_init(&bar.full[i], 1); mbar_init(&bar.empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&bar.acc_full[i], 1); mbar_init(&bar.acc_empty[i], 4); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar.acc_full[i], 1); mbar_init(&bar.acc_empty[i], C::kEpiWarps); }
     mbar_init(&bar.mma_done, 1);
     bar.abort = 0;
     fence_mbar_init();
     fence_async_shared();
   }
-  if (warp == 1) tmem_alloc(&bar.tmem_base, kPTmemCols);
+  if (warp == 1) tmem_alloc(&bar.tmem_base, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -296,7 +310,7 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
           const uint32_t a = base + st * kPStageBytes, w = a + kPXBytes;
           // dual: the first problem into columns 0.., the second into kPN..
           const bool second = kDual && kb >= nkb;
-          const uint32_t acc = tmem + (kDual ? (second ? kPN : 0) : b * kPN);
+          const uint32_t acc = tmem + (kDual ? b * 2 * kPN + (second ? kPN : 0) : b * kPN);
           const bool first_kb = second ? kb == nkb : kb == 0;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
@@ -315,9 +329,11 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
     // instead of one lane per row; the 16-byte chunk c of row r sits at
     // chunk c ^ ((r >> 1) & 3), which keeps both access patterns free of
     // bank conflicts.
-    const int q = warp & 3;
+    const int q = warp & 3;                       // the TMEM lane quadrant this warp may read
+    const int ew = warp - 2;                      // epilogue warp index
+    const int hh = kDual ? ew >> 2 : 0;           // dual: its half of the tile's columns
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-    uint8_t* stg = smem + kPOffStg + q * kPStgBytes;
+    uint8_t* stg = smem + C::kOffStg + ew * kPStgBytes;
     const int cr = lane >> 2, cc = lane & 3;     // coalesced role: rows cr + 8 i, chunk cc
     auto stg_at = [&](int r, int c) { return reinterpret_cast<uint4*>(stg + r * 64 + 16 * (c ^ ((r >> 1) & 3))); };
     // 32 rows x 64 bytes of the warp from the buffer to global rows row0 + r
@@ -356,11 +372,11 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
       __syncwarp();
       if (kDual) {
 #pragma unroll 1
-        for (int gq = 0; gq < kPN / 32; ++gq) {
+        for (int gq = 2 * hh; gq < 2 * hh + 2; ++gq) {
           const int c0 = n0 + 32 * gq;
           float v[32];
           uint32_t hw[16];
-          tmem_ld32_sync(tmem + lane_addr + 32 * gq, v);
+          tmem_ld32_sync(tmem + lane_addr + b * 2 * kPN + 32 * gq, v);
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const float b0 = pr.bias ? pr.bias[c0 + 2 * c] : 0.f, b1 = pr.bias ? pr.bias[c0 + 2 * c + 1] : 0.f;
@@ -369,7 +385,7 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
 #pragma unroll
           for (int c = 0; c < 4; ++c) *stg_at(lane, c) = make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
           flush(reinterpret_cast<uint8_t*>(static_cast<bf16*>(pr.Y) + c0), row0, (size_t)N * 2);
-          tmem_ld32_sync(tmem + lane_addr + kPN + 32 * gq, v);
+          tmem_ld32_sync(tmem + lane_addr + b * 2 * kPN + kPN + 32 * gq, v);
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             if (!(bf16lo(hw[c]) > 0.f)) v[2 * c] = 0.f;
@@ -452,7 +468,7 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kPTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -475,12 +491,13 @@ cudaError_t launch_linear_tc_dual(const void* X, const void* W, const float* bia
       !make_tmap_rows(&pw2, W2, (uint64_t)K2, (uint64_t)N, kPN))
     return cudaErrorInvalidValue;
   const Prob pp0 = Prob{bias, nullptr, Y, kEpiRelu};
-  const int grid = (int)min64(ptiles, (int64_t)2 * sm_count());
+  using C = PCfg<true>;
+  const int grid = (int)min64(ptiles, (int64_t)C::kCtasPerSm * sm_count());
   auto kern = linear_tc_persistent_kernel<false, true>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(grid), dim3(kPThreads), kPSmemBytes, s, px, pw, px2, pw2, pp0, static_cast<bf16*>(Y2), M,
-                 N, K, K2, status);
+  e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, px, pw, px2, pw2, pp0, static_cast<bf16*>(Y2),
+                 M, N, K, K2, status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -497,12 +514,13 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
         !make_tmap_rows(&pw, lp.W, (uint64_t)K, (uint64_t)N, kPN))
       return cudaErrorInvalidValue;
     const Prob pp0 = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y, lp.epi};
-    const int grid = (int)min64(ptiles, (int64_t)2 * sm_count());
+    using C = PCfg<false>;
+    const int grid = (int)min64(ptiles, (int64_t)C::kCtasPerSm * sm_count());
     auto kern = out_f32 ? linear_tc_persistent_kernel<true, false> : linear_tc_persistent_kernel<false, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3(grid), dim3(kPThreads), kPSmemBytes, s, px, pw, px, pw, pp0, (bf16*)nullptr, M, N, K,
-                   0, status);
+    e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, px, pw, px, pw, pp0, (bf16*)nullptr, M, N,
+                   K, 0, status);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
