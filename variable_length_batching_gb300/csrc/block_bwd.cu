@@ -674,7 +674,7 @@ constexpr int kTcC = 128;          // pair width of the tensor-core route
 constexpr int kPrepThreads = 256;
 constexpr int kPrepCells = kPrepThreads / 16;   // cells per pass
 
-__global__ void __launch_bounds__(kPrepThreads)
+__global__ void __launch_bounds__(kPrepThreads, 4)
 bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ len,
                 const int32_t* __restrict__ row_sample, int B, int64_t T, int64_t P,
@@ -682,14 +682,12 @@ bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const 
                 const float* __restrict__ dM, const float* __restrict__ dz_up, const bf16* __restrict__ zt_up,
                 bf16* __restrict__ Y, bf16* __restrict__ dPt) {
   const int lane = threadIdx.x & 31, q = threadIdx.x & 15, slot = threadIdx.x >> 4;
-  float gm[8], bt[8];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const float4 g4 = *reinterpret_cast<const float4*>(gamma + 64 * h + 4 * q);
-    const float4 b4 = *reinterpret_cast<const float4*>(beta + 64 * h + 4 * q);
-    gm[4 * h] = g4.x; gm[4 * h + 1] = g4.y; gm[4 * h + 2] = g4.z; gm[4 * h + 3] = g4.w;
-    bt[4 * h] = b4.x; bt[4 * h + 1] = b4.y; bt[4 * h + 2] = b4.z; bt[4 * h + 3] = b4.w;
+  __shared__ float gsh[kTcC], bsh[kTcC];
+  if (threadIdx.x < kTcC) {
+    gsh[threadIdx.x] = gamma[threadIdx.x];
+    bsh[threadIdx.x] = beta[threadIdx.x];
   }
+  __syncthreads();
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     const int b = row_sample[t];
     const int n = len[b];
@@ -761,11 +759,14 @@ bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const 
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t yw[2], lw[2], gw[2];
+          const float4 g4 = *reinterpret_cast<const float4*>(gsh + 64 * h + 4 * q);
+          const float4 b4 = *reinterpret_cast<const float4*>(bsh + 64 * h + 4 * q);
+          const float gm[4] = {g4.x, g4.y, g4.z, g4.w}, bt[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const int i = 4 * h + e;
-            const float y0 = fmaf((z[c][i] - mean) * rs, gm[i], bt[i]);
-            const float y1 = fmaf((z[c][i + 1] - mean) * rs, gm[i + 1], bt[i + 1]);
+            const float y0 = fmaf((z[c][i] - mean) * rs, gm[e], bt[e]);
+            const float y1 = fmaf((z[c][i + 1] - mean) * rs, gm[e + 1], bt[e + 1]);
             const float h0 = round_io(y0, (bf16*)nullptr), h1 = round_io(y1, (bf16*)nullptr);
             yw[e / 2] = pack_bf16x2(y0, y1);
             lw[e / 2] = pack_bf16x2(y0 - h0, y1 - h1);
