@@ -676,20 +676,45 @@ __device__ __forceinline__ BItem shfl_bitem(BItem it) {
   return it;
 }
 
-__device__ __forceinline__ void store_half32(bf16* dst, const float* v, float mul) {
+// The persistent kernels' output rows: a compute warp holds 32 rows (one per
+// lane) x 32 columns of bf16, 64 bytes a row, with rows H * 128 bytes apart
+// in the token-major tensor.  They leave through the warp's 2 KB buffer in
+// shared memory, four lanes per row, so that each store instruction writes
+// 8 rows x 64 contiguous bytes instead of 32 scattered pieces.  The 16-byte
+// chunk c of row r sits at chunk c ^ ((r >> 1) & 3), which keeps the row-
+// per-lane writes and the four-lanes-per-row reads free of bank conflicts.
+// Rows r >= nrows (past the segment) are not written.
+constexpr uint32_t kStgWarpBytes = 32 * 64;
+constexpr uint32_t kSmemBytesP = kSmemBytes + 8 * kStgWarpBytes;   // the persistent kernels
+__device__ __forceinline__ void staged_store_half32(uint8_t* stg, int lane, const float* v, float mul, bf16* dst0,
+                                                    int64_t pitch, int nrows) {
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
+  for (int c = 0; c < 4; ++c) {
     uint4 w;
-    w.x = pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul);
-    w.y = pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul);
-    w.z = pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul);
-    w.w = pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul);
-    *reinterpret_cast<uint4*>(dst + 8 * u) = w;
+    w.x = pack_bf16x2(v[8 * c] * mul, v[8 * c + 1] * mul);
+    w.y = pack_bf16x2(v[8 * c + 2] * mul, v[8 * c + 3] * mul);
+    w.z = pack_bf16x2(v[8 * c + 4] * mul, v[8 * c + 5] * mul);
+    w.w = pack_bf16x2(v[8 * c + 6] * mul, v[8 * c + 7] * mul);
+    *reinterpret_cast<uint4*>(stg + lane * 64 + 16 * (c ^ ((lane >> 1) & 3))) = w;
   }
-}
-__device__ __forceinline__ void zero_half32(bf16* dst) {
+  __syncwarp();
+  const int cr = lane >> 2, cc = lane & 3;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(dst + 8 * u) = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = 0; i < 4; ++i) {
+    const int r = cr + 8 * i;
+    const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + 16 * (cc ^ ((r >> 1) & 3)));
+    if (r < nrows) *reinterpret_cast<uint4*>(dst0 + r * pitch + 8 * cc) = w;
+  }
+  __syncwarp();
+}
+// The same rows as zeros (no buffer needed).
+__device__ __forceinline__ void zero_rows32(int lane, bf16* dst0, int64_t pitch, int nrows) {
+  const int cr = lane >> 2, cc = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = cr + 8 * i;
+    if (r < nrows) *reinterpret_cast<uint4*>(dst0 + r * pitch + 8 * cc) = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // ---------------------------------------------------------------------------- dK, dV persistent
@@ -846,6 +871,7 @@ attn_bwd_dkv_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_c
     const int r = qd * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
     const float scale_log2 = scale * kLog2e;
+    uint8_t* stg = smem + kSmemBytes + (warp - 2) * kStgWarpBytes;   // this warp's output buffer
     int gt = 0;
     bool ok = true;
     BItem it;
@@ -853,12 +879,13 @@ attn_bwd_dkv_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_c
       if (it.b < 0) break;
       const int n_q = it.hi - it.lo, n_k = it.khi - it.klo, diag = n_k - n_q;
       const int jj = it.t * kBM + r;             // segment-local key of this lane
-      const int64_t row = (int64_t)it.klo + jj;
+      // the warp's rows: keys it.t * 128 + 32 qd + (0..31) of the segment
+      const int nrows = min(32, max(0, n_k - (it.t * kBM + qd * 32)));
+      const int64_t pitch = (int64_t)H * kD;
+      const int64_t off0 = ((int64_t)(it.klo + it.t * kBM + qd * 32) * H + it.h) * kD + 32 * g;
       if (it.n == 0) {                           // no query sees these keys: no gradient
-        if (jj < n_k) {
-          zero_half32(dk + (row * H + it.h) * kD + 32 * g);
-          zero_half32(dv + (row * H + it.h) * kD + 32 * g);
-        }
+        zero_rows32(lane, dk + off0, pitch, nrows);
+        zero_rows32(lane, dv + off0, pitch, nrows);
         continue;
       }
       for (int i = 0; i < it.n; ++i, ++gt) {
@@ -884,10 +911,8 @@ attn_bwd_dkv_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_c
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bar.acc_free);               // the next item may overwrite dV, dK
-      if (jj < n_k) {
-        store_half32(dv + (row * H + it.h) * kD + 32 * g, av, 1.0f);
-        store_half32(dk + (row * H + it.h) * kD + 32 * g, ak, scale);
-      }
+      staged_store_half32(stg, lane, av, 1.0f, dv + off0, pitch, nrows);
+      staged_store_half32(stg, lane, ak, scale, dk + off0, pitch, nrows);
     }
   }
 
@@ -1013,6 +1038,7 @@ attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const int r = qd * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
     const float scale_log2 = scale * kLog2e;
+    uint8_t* stg = smem + kSmemBytes + (warp - 2) * kStgWarpBytes;   // this warp's output buffer
     int gt = 0;
     bool ok = true;
     BItem it;
@@ -1020,8 +1046,12 @@ attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       if (it.b < 0) break;
       const int n_q = it.hi - it.lo, n_k = it.khi - it.klo, diag = n_k - n_q;
       const int64_t t = (int64_t)it.lo + it.t * kBM + r;
+      // the warp's rows: queries it.t * 128 + 32 qd + (0..31) of the segment
+      const int nrows = (int)min64(32, max64(0, (int64_t)it.hi - (it.lo + it.t * kBM + qd * 32)));
+      const int64_t pitch = (int64_t)H * kD;
+      const int64_t off0 = ((int64_t)(it.lo + it.t * kBM + qd * 32) * H + it.h) * kD + 32 * g;
       if (it.n == 0) {                           // no query here sees a key: no gradient
-        if (t < it.hi) zero_half32(dq + (t * H + it.h) * kD + 32 * g);
+        zero_rows32(lane, dq + off0, pitch, nrows);
         continue;
       }
       // rows past the segment, and rows that saw no key: P = 0 (-lse -> -inf)
@@ -1050,7 +1080,7 @@ attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bar.acc_free);               // the next item may overwrite dQ
-      if (t < it.hi) store_half32(dq + (t * H + it.h) * kD + 32 * g, acc, scale);
+      staged_store_half32(stg, lane, acc, scale, dq + off0, pitch, nrows);
     }
   }
 
@@ -1104,9 +1134,9 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsig
   }
   if (pkv) {
     auto kkv = p.causal ? attn_bwd_dkv_persistent<true> : attn_bwd_dkv_persistent<false>;
-    e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesP);
     if (e != cudaSuccess) return e;
-    kkv<<<(unsigned)min64(items_k, slots), kThreads, kSmemBytes, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q,
+    kkv<<<(unsigned)min64(items_k, slots), kThreads, kSmemBytesP, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q,
                                                                        p.cu_k, p.B, p.T_q, p.T_k, p.H, KT, p.scale,
                                                                        (bf16*)p.dk, (bf16*)p.dv, counters, status);
   } else {
@@ -1120,9 +1150,9 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsig
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (pq) {
     auto kq = p.causal ? attn_bwd_dq_persistent<true> : attn_bwd_dq_persistent<false>;
-    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesP);
     if (e != cudaSuccess) return e;
-    kq<<<(unsigned)min64(items_q, slots), kThreads, kSmemBytes, s>>>(q128, do128, k64, v64, p.lse, Dbuf, p.cu_q,
+    kq<<<(unsigned)min64(items_q, slots), kThreads, kSmemBytesP, s>>>(q128, do128, k64, v64, p.lse, Dbuf, p.cu_q,
                                                                       p.cu_k, p.B, p.T_q, p.T_k, p.H, QT, p.scale,
                                                                       (bf16*)p.dq, counters + 1, status);
   } else {
