@@ -341,6 +341,31 @@ nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const vo
                               const float* b_g, void* z_out, void* m, void* s_out, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace nt_pair_reduce_loss needs (a constant: the
+ * loss's partial sums and up to 8,192 per-CTA partials of the pair term). */
+size_t nt_pair_reduce_loss_workspace_bytes(void);
+
+/*
+ * nt_pair_reduce_loss -- nt_pair_reduce with the g projection, and the Eq. 5
+ * loss of [DL] Appendix A.1 on the block's two outputs (s_out and z), in one
+ * call that reads z once: the reduce's pass over the cells also sums each
+ * pair row's squares, weighted by beta_i of its sample, into per-CTA
+ * partials; the single-row term follows over s_out, and one block adds both
+ * in a fixed order (the result does not depend on scheduling, only on the
+ * device's SM count, which sets the reduce's grid).  The same loss as
+ * nt_pair_block_loss up to the order of its sums.
+ *   z, C_z, m, W_g (required), b_g, s_in, s_out, C_s  as for nt_pair_reduce.
+ *   d_loss     one fp32 on the device, written.
+ *   workspace  >= nt_pair_reduce_loss_workspace_bytes(), 16-byte aligned.
+ * C_z not a multiple of 8 (fp32): the loss reads z again (nt_pair_block_loss's
+ * path).  Errors as for nt_pair_reduce, plus NT_ERR_INVALID for a NULL W_g,
+ * d_loss or workspace, a NULL z when P > 0 or a NULL m or s_out when T > 0
+ * (an empty batch writes a zero loss).  Asynchronous.
+ */
+nt_status nt_pair_reduce_loss(const nt_partition* part, nt_dtype dtype, const void* z, int32_t C_z, void* m,
+                              const void* W_g, const float* b_g, const void* s_in, void* s_out, int32_t C_s,
+                              float* d_loss, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of device workspace nt_pair_block_loss needs (its partial sums). */
 size_t nt_pair_block_loss_workspace_bytes(void);
 

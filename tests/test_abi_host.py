@@ -109,6 +109,13 @@ def test_host_side_rejections(L):
     part.P = 100
     assert lib.nt_pair_reduce(P, 1, fake, 128, fake, None, None, None, None, 0, None) == 1
     part.P = 13
+    # the reduce fused with the loss: W_g and the loss are required, and its workspace
+    rl = lib.nt_pair_reduce_loss
+    ws = int(lib.nt_pair_reduce_loss_workspace_bytes())
+    assert ws >= 8 * (2 * 1024 + 8192)
+    assert rl(P, 1, fake, 128, fake, None, None, fake, fake, 384, fake, fake, ws, None) == 1
+    assert rl(P, 1, fake, 128, fake, fake, None, fake, fake, 384, None, fake, ws, None) == 1
+    assert rl(P, 1, fake, 128, fake, fake, None, fake, fake, 384, fake, fake, 16, None) == 1
     # width not a multiple of 8 in bf16 -> unsupported
     assert lib.nt_pair_broadcast(P, 1, fake, fake, 384, fake, fake, 12, fake, fake, 1 << 20, None) == 2
     # misaligned pointer

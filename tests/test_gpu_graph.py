@@ -96,9 +96,10 @@ def test_block_graph_pipelined_steps(mods):
 def test_block_graph_loss_readback(mods):
     """readback="loss": each step reads back the Eq. 5 loss of its two
     outputs ("DanLing NestedTensor" Appendix A.1), computed on the device in
-    the captured graph, and s_out; both equal the eager block followed by
-    nt_pair_block_loss bit for bit, over pipelined steps with other singles
-    and after new lengths."""
+    the captured graph (the reduce fused with the loss), and s_out; both
+    equal the same calls made eagerly bit for bit, over pipelined steps with
+    other singles and after new lengths, and the loss equals the two-pass
+    nt_pair_block_loss up to the order of its sums."""
     nt, graph = mods
     cfg = wl.PAIRFORMER_BF16
     base = wl.make_block_inputs(cfg, biases=True)
@@ -109,9 +110,15 @@ def test_block_graph_loss_readback(mods):
                          b1=g(w.b1), W2=g(w.W2), b2=g(w.b2), W_g=g(w.W_g), b_g=g(w.b_g))
 
     def eager_loss(x):
+        # the graph's calls, eagerly: broadcast, transition, then the reduce
+        # fused with the loss; and the two-pass loss up to summation order
         part = nt.nt_partition_build(torch.as_tensor(np.asarray(x.lengths, dtype=np.int32)).to(DEV))
-        z, m, s_out = nt.block_forward(part, x.s.to(DEV), wd)
-        loss, _, _ = nt.nt_pair_block_loss(part, s_out, z, want_grads=False)
+        s = x.s.to(DEV)
+        z = nt.nt_pair_broadcast(part, s, s, wd.W_a, wd.W_b)
+        nt.nt_pair_transition(part, z, wd.ln_gamma, wd.ln_beta, wd.W1, wd.b1, wd.W2, wd.b2, out=z)
+        _, s_out, loss = nt.nt_pair_reduce_loss(part, z, wd.W_g, wd.b_g, s_in=s)
+        two_pass, _, _ = nt.nt_pair_block_loss(part, s_out, z, want_grads=False)
+        assert abs(float(loss.item()) - float(two_pass.item())) <= 1e-6 * abs(float(two_pass.item()))
         return loss.cpu(), s_out.cpu()
 
     refs = [eager_loss(x) for x in inps]

@@ -123,9 +123,10 @@ eq5_partial_kernel(const T* __restrict__ s_out, const T* __restrict__ zt, const 
     }
     ax += alpha * sx;
     // the row's cells: 16-byte loads (Cp is a multiple of 16 bytes' worth of
-    // elements, so every row starts on a 16-byte boundary)
+    // elements, so every row starts on a 16-byte boundary); none without zt
+    // (the pair term then comes from the reduce, eq5_finish's extra partials)
     constexpr int V = 16 / sizeof(T);
-    const int64_t c0 = row_start[r] * Cp, c1 = row_start[r + 1] * Cp;
+    const int64_t c0 = row_start[r] * Cp, c1 = zt ? row_start[r + 1] * Cp : c0;
     float sp = 0.f;
     for (int64_t e = c0 + (int64_t)threadIdx.x * V; e < c1; e += (int64_t)kThreads * V) {
       float x[V];
@@ -156,13 +157,17 @@ eq5_partial_kernel(const T* __restrict__ s_out, const T* __restrict__ zt, const 
 
 // The partial sums in a fixed order (a pairwise tree over the partial
 // index, one block of kLossBlocks threads), then Eq. 5's normalisations.
+// extra: nextra further partials of the weighted pair term (the reduce's),
+// thread i adding extra[i], extra[i + kLossBlocks], ... in that order.
 __global__ void __launch_bounds__(kLossBlocks)
 eq5_finish_kernel(const double* __restrict__ partial, int nblocks, int64_t Trows, int64_t P, int C, int Cp,
-                  float* __restrict__ loss) {
+                  float* __restrict__ loss, const double* __restrict__ extra = nullptr, int nextra = 0) {
   __shared__ double sx[kLossBlocks], sp[kLossBlocks];
   const int i = threadIdx.x;
   sx[i] = i < nblocks ? partial[2 * i] : 0.0;
-  sp[i] = i < nblocks ? partial[2 * i + 1] : 0.0;
+  double ep = i < nblocks ? partial[2 * i + 1] : 0.0;
+  for (int k = i; k < nextra; k += kLossBlocks) ep += extra[k];
+  sp[i] = ep;
   __syncthreads();
   for (int w = kLossBlocks / 2; w > 0; w >>= 1) {
     if (i < w) {
@@ -1199,6 +1204,21 @@ cudaError_t launch_eq5_loss(nt_dtype dt, const nt_partition* p, const void* s_ou
 }
 
 size_t eq5_loss_workspace_bytes() { return sizeof(double) * 2 * kLossBlocks; }
+
+cudaError_t launch_eq5_loss_rows(nt_dtype dt, const nt_partition* p, const void* s_out, int C_s, int C_z,
+                                 float* loss, const double* pair_sq, int npair, void* workspace, cudaStream_t s) {
+  const int nblocks = (int)max64(1, min64(p->T, kLossBlocks));
+  double* partial = static_cast<double*>(workspace);
+  if (dt == NT_BF16)
+    eq5_partial_kernel<bf16><<<nblocks, kThreads, 0, s>>>((const bf16*)s_out, nullptr, p->row_start, p->row_sample,
+                                                         p->B, p->T, p->P, C_s, C_z, partial, nullptr, nullptr);
+  else
+    eq5_partial_kernel<float><<<nblocks, kThreads, 0, s>>>((const float*)s_out, nullptr, p->row_start,
+                                                          p->row_sample, p->B, p->T, p->P, C_s, C_z, partial,
+                                                          nullptr, nullptr);
+  eq5_finish_kernel<<<1, kLossBlocks, 0, s>>>(partial, nblocks, p->T, p->P, C_s, C_z, loss, pair_sq, npair);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_block_backward(nt_dtype dt, const BlockBwd& q, unsigned int* status, cudaStream_t s) {
   return dt == NT_BF16 ? block_backward_t<bf16>(q, status, s) : block_backward_t<float>(q, status, s);

@@ -542,6 +542,46 @@ nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z
   return NT_OK;
 }
 
+size_t nt_pair_reduce_loss_workspace_bytes(void) {
+  return ((eq5_loss_workspace_bytes() + 255) & ~(size_t)255) + (size_t)kReduceMaxGrid * sizeof(double);
+}
+
+nt_status nt_pair_reduce_loss(const nt_partition* part, nt_dtype dtype, const void* z, int32_t C_z, void* m,
+                              const void* W_g, const float* b_g, const void* s_in, void* s_out, int32_t C_s,
+                              float* d_loss, void* workspace, size_t workspace_bytes, void* stream) {
+  nt_status st = check_partition(part, true);
+  if (st != NT_OK) return st;
+  if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
+  if (!width_ok(dtype, C_z) || !width_ok(dtype, C_s)) return fail(NT_ERR_UNSUPPORTED, "C_z=%d, C_s=%d", C_z, C_s);
+  if (dtype == NT_BF16 && C_z > 1024) return fail(NT_ERR_UNSUPPORTED, "bf16 C_z=%d > 1024", C_z);
+  if (!W_g || !d_loss || !workspace || (part->P > 0 && !z) || (part->T > 0 && (!m || !s_out)))
+    return fail(NT_ERR_INVALID, "NULL pointer");
+  if (!aligned16(z) || !aligned16(m) || !aligned16(W_g) || !aligned16(b_g) || !aligned16(s_in) ||
+      !aligned16(s_out) || !aligned16(workspace))
+    return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
+  const size_t need = nt_pair_reduce_loss_workspace_bytes();
+  if (workspace_bytes < need) return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  double* partial = static_cast<double*>(workspace);
+  double* pair_sq = reinterpret_cast<double*>(static_cast<uint8_t*>(workspace) +
+                                              ((eq5_loss_workspace_bytes() + 255) & ~(size_t)255));
+  const bool fused = reduce_sq_supported(C_z);
+  int npair = 0;
+  cudaError_t e = launch_reduce(dtype, z, part, C_z, m, s, fused ? pair_sq : nullptr, &npair);
+  if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
+  if (part->T > 0) {
+    LinearProblem prob = {m, W_g, b_g, s_in, s_out};
+    e = linear_tc_supported(dtype, part->T, C_s, C_z)
+            ? launch_linear_tc(0, &prob, 1, part->T, C_s, C_z, status_word(), s)
+            : launch_linear(dtype, dtype == NT_F32, &prob, 1, part->T, C_s, C_z, s);
+    if (e != cudaSuccess) return cuda_fail(e, "g projection launch");
+  }
+  e = fused ? launch_eq5_loss_rows(dtype, part, s_out, C_s, C_z, d_loss, pair_sq, npair, partial, s)
+            : launch_eq5_loss(dtype, part, s_out, C_s, z, C_z, d_loss, nullptr, nullptr, partial, s);
+  if (e != cudaSuccess) return cuda_fail(e, "loss launch");
+  return NT_OK;
+}
+
 size_t nt_pair_block_fused_workspace_bytes(int64_t T, int64_t T_cols, int32_t C_z) {
   if (T < 0 || T_cols < 0 || C_z < 0) return 0;
   return (size_t)(2 * T + T_cols) * (size_t)C_z * sizeof(float);

@@ -180,8 +180,13 @@ cudaError_t launch_transition_tc(const void* z_in, void* z_out, int64_t P, int C
                                  const float* b1, const void* W3, const float* b3, const void* W2,
                                  const float* b2, unsigned int* status, cudaStream_t s);
 
-cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m,
-                          cudaStream_t s);
+// The column mean; with sq_part (C_z a multiple of 8, reduce_sq_supported),
+// also Eq. 5's weighted pair squares, one double per CTA into sq_part, their
+// count into *sq_parts (at most kReduceMaxGrid).
+constexpr int64_t kReduceMaxGrid = 8192;
+bool reduce_sq_supported(int C_z);
+cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m, cudaStream_t s,
+                          double* sq_part = nullptr, int* sq_parts = nullptr);
 // Fused block: the transition kernel building z from u, v and summing rows
 // into m_acc (fp32, zeroed by the caller); then m = m_acc / M_i.
 cudaError_t launch_block_fused_tc(const float* u, const float* v, const nt_partition* part, void* z_out, int C_z,
@@ -250,6 +255,10 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsig
 // and, optionally, its gradients dX~ [T, C_s] and dP~ [P, C_z] (fp32).
 // workspace: eq5_loss_workspace_bytes() for the partial sums.
 size_t eq5_loss_workspace_bytes();
+// The loss with its pair term already summed by the reduce (pair_sq: npair
+// weighted partials): the single-row term here, then one fixed-order finish.
+cudaError_t launch_eq5_loss_rows(nt_dtype dt, const nt_partition* p, const void* s_out, int C_s, int C_z,
+                                 float* loss, const double* pair_sq, int npair, void* workspace, cudaStream_t s);
 cudaError_t launch_eq5_loss(nt_dtype dt, const nt_partition* p, const void* s_out, int C_s, const void* z_tilde,
                             int C_z, float* loss, float* ds_out, float* dz, void* workspace, cudaStream_t s);
 

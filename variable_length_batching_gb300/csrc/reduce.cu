@@ -14,22 +14,31 @@ namespace {
 
 constexpr int kThreads = 128;
 
-template <typename T>
+// kSq: also the weighted squared sum of Eq. 5's pair term ("DanLing
+// NestedTensor" Appendix A.1), sum over the CTA's rows of beta_b * ||row's
+// cells||^2 with beta_b = 1.5 - b / (2B): squares in fp32 per thread and row,
+// the row's total over the CTA in fp32, the rows in double, into
+// sq_part[blockIdx.x].
+template <typename T, bool kSq>
 __global__ void __launch_bounds__(kThreads)
 reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ row_len,
               const int32_t* __restrict__ row_sample, const int64_t* __restrict__ row_start,
-              int64_t rows, int C_z, T* __restrict__ m) {
+              int64_t rows, int C_z, T* __restrict__ m, double* __restrict__ sq_part, int B) {
   pdl_wait();                                  // z comes from the kernel before
   pdl_trigger();
-  extern __shared__ float part[];              // [groups][C_z]
+  extern __shared__ float part[];              // [groups][C_z], then kThreads squares (kSq)
   const int lanes = C_z / 8;                   // vectors per cell (<= kThreads)
   const int groups = kThreads / lanes;         // cells summed concurrently
   const int lane = threadIdx.x % lanes, grp = threadIdx.x / lanes;
   const bool active = grp < groups;
+  float* sqs = part + groups * C_z;
+  double cta_sq = 0.0;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const int64_t n = row_len[row_sample[r]];
+    const int bs = row_sample[r];
+    const int64_t n = row_len[bs];
     const T* zr = z + row_start[r] * C_z + lane * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float sq = 0.f;
     if (active) {
       int64_t b = grp;
       // two independent loads in flight per iteration
@@ -38,18 +47,32 @@ reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ row_len,
         load8(zr + b * C_z, x0);
         load8(zr + (b + groups) * C_z, x1);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) acc[t] += x0[t] + x1[t];
+        for (int t = 0; t < 8; ++t) {
+          acc[t] += x0[t] + x1[t];
+          if (kSq) sq = fmaf(x1[t], x1[t], fmaf(x0[t], x0[t], sq));
+        }
       }
       for (; b < n; b += groups) {
         float x0[8];
         load8(zr + b * C_z, x0);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) acc[t] += x0[t];
+        for (int t = 0; t < 8; ++t) {
+          acc[t] += x0[t];
+          if (kSq) sq = fmaf(x0[t], x0[t], sq);
+        }
       }
 #pragma unroll
       for (int t = 0; t < 8; ++t) part[grp * C_z + lane * 8 + t] = acc[t];
     }
+    if (kSq) sqs[threadIdx.x] = sq;
     __syncthreads();
+    if (kSq && threadIdx.x < 32) {
+      float v = 0.f;
+      for (int i = threadIdx.x; i < kThreads; i += 32) v += sqs[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (threadIdx.x == 0) cta_sq += (1.5 - (double)bs / (2.0 * B)) * (double)v;
+    }
     if (grp == 0) {
       float tot[8];
 #pragma unroll
@@ -64,6 +87,7 @@ reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ row_len,
     }
     __syncthreads();
   }
+  if (kSq && threadIdx.x == 0) sq_part[blockIdx.x] = cta_sq;
 }
 
 // fp32 widths that are multiples of 4 but not of 8: one thread per feature.
@@ -113,21 +137,29 @@ cudaError_t launch_mean_finish(nt_dtype dt, const float* m_acc, const nt_partiti
   return cudaGetLastError();
 }
 
+bool reduce_sq_supported(int C_z) { return C_z % 8 == 0 && C_z / 8 <= kThreads; }
+
 cudaError_t launch_reduce(nt_dtype dt, const void* z, const nt_partition* p, int C_z, void* m,
-                          cudaStream_t s) {
+                          cudaStream_t s, double* sq_part, int* sq_parts) {
+  if (sq_parts) *sq_parts = 0;
   if (p->T == 0) return cudaSuccess;
   const int sms = sm_count();
-  const int grid = (int)min64(p->T, (int64_t)sms * 32);
+  const int grid = (int)min64(min64(p->T, (int64_t)sms * 32), kReduceMaxGrid);
   const int32_t* cl = col_lengths_of(p);     // cells per pair row
-  if (C_z % 8 == 0 && C_z / 8 <= kThreads) {
+  if (reduce_sq_supported(C_z)) {
     const int groups = kThreads / (C_z / 8);
-    const size_t smem = sizeof(float) * groups * C_z;
+    const size_t smem = sizeof(float) * (groups * C_z + (sq_part ? kThreads : 0));
+    if (sq_parts && sq_part) *sq_parts = grid;
     if (dt == NT_BF16)
-      return launch_pdl(reduce_kernel<bf16>, dim3(grid), dim3(kThreads), smem, s, (const bf16*)z, cl, p->row_sample,
-                        p->row_start, p->T, C_z, (bf16*)m);
+      return sq_part ? launch_pdl(reduce_kernel<bf16, true>, dim3(grid), dim3(kThreads), smem, s, (const bf16*)z, cl,
+                                  p->row_sample, p->row_start, p->T, C_z, (bf16*)m, sq_part, p->B)
+                     : launch_pdl(reduce_kernel<bf16, false>, dim3(grid), dim3(kThreads), smem, s, (const bf16*)z, cl,
+                                  p->row_sample, p->row_start, p->T, C_z, (bf16*)m, (double*)nullptr, p->B);
     else
-      return launch_pdl(reduce_kernel<float>, dim3(grid), dim3(kThreads), smem, s, (const float*)z, cl,
-                        p->row_sample, p->row_start, p->T, C_z, (float*)m);
+      return sq_part ? launch_pdl(reduce_kernel<float, true>, dim3(grid), dim3(kThreads), smem, s, (const float*)z,
+                                  cl, p->row_sample, p->row_start, p->T, C_z, (float*)m, sq_part, p->B)
+                     : launch_pdl(reduce_kernel<float, false>, dim3(grid), dim3(kThreads), smem, s, (const float*)z,
+                                  cl, p->row_sample, p->row_start, p->T, C_z, (float*)m, (double*)nullptr, p->B);
   } else {
     reduce_kernel_f32_scalar<<<grid, 128, 0, s>>>((const float*)z, cl, p->row_sample,
                                                  p->row_start, p->T, C_z, (float*)m);

@@ -11,13 +11,17 @@ last the last slice and the reduce.  Slices grow in length; each slice's z~
 is copied back to the host on a second stream as soon as its graph is done,
 then s_out.
 
-Steps are pipelined: the device buffers a step writes (z~, m, s_out) and the
-host buffers it fills come from one of ``depth`` sets, used in turn, so the
-next step's copies in, partition and compute run while the host link still
-drains the previous step's z~.  A set is reused only after its last
-read-back has completed.  A new (B, T, P) drains the pipeline and captures
-new graphs.  Every device step runs in the library's kernels; this module
-owns the buffers, the streams, the events and the graphs.
+Steps are pipelined over ``depth`` slots used in turn.  A slot holds the
+step's device inputs (lengths, singles, the partition built from them), the
+device buffers it writes (z~, m, s_out), the host buffers it fills and its
+graphs.  The next step's copies in and partition run on an input stream of
+their own while the current step's graphs run, and its graphs run while the
+host link still drains the previous step's read-backs.  A slot's inputs are
+overwritten only after its previous graphs have read them, and its outputs
+only after their last read-back has completed.  A new (B, T, P) drains the
+pipeline and captures new graphs.  Every device step runs in the library's
+kernels; this module owns the buffers, the streams, the events and the
+graphs.
 """
 import ctypes
 from typing import List, Optional
@@ -42,6 +46,24 @@ def slice_cuts(P: int, slices: int, growth: float = 1.0) -> List[int]:
         cuts.append(min(P, max(cuts[-1], int(round(P * acc / tot)))))
     cuts.append(P)
     return cuts
+
+
+class _Inputs:
+    """Device inputs of one pipeline slot: the lengths, the singles and the
+    partition built from them."""
+
+    def __init__(self, B: int, T: int, C_s: int, dtype: torch.dtype, dev):
+        self.lengths = torch.empty(B, dtype=torch.int32, device=dev)
+        self.cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+        self.pair_off = torch.empty(B + 1, dtype=torch.int64, device=dev)
+        self.totals = torch.empty(4, dtype=torch.int64, device=dev)
+        self.s = torch.empty(T, C_s, dtype=dtype, device=dev)
+        self.row_start = torch.empty(T + 1, dtype=torch.int64, device=dev)
+        self.row_sample = torch.empty(max(T, 1), dtype=torch.int32, device=dev)
+        self.part = None
+        self.ready = torch.cuda.Event()    # input stream: copies and partition done
+        self.free = torch.cuda.Event()     # main stream: the slot's last graph has read them
+        self.used = False
 
 
 class _Set:
@@ -84,62 +106,55 @@ class BlockGraph:
         self.dev = device if device is not None else w.W_a.device
         self.C_z, self.C_s = w.W_a.shape
         self.copy_stream = torch.cuda.Stream(device=self.dev)
+        self.in_stream = torch.cuda.Stream(device=self.dev)
         self.key = None
         self.sets: List[_Set] = []
+        self.inputs: List[_Inputs] = []
+        self.in_key = None
         self.submitted = 0
-        self.B = -1
-        self.T = -1
-        self.s = None
 
-    # -- static input buffers ------------------------------------------------------
-    def _ensure_b(self, B: int):
-        if B == self.B:
+    # -- input slots --------------------------------------------------------------
+    def _ensure_inputs(self, B: int, T: int, dtype: torch.dtype):
+        if self.in_key == (B, T, dtype):
             return
-        self.B = B
-        self.lengths = torch.empty(B, dtype=torch.int32, device=self.dev)
-        self.cu = torch.empty(B + 1, dtype=torch.int32, device=self.dev)
-        self.pair_off = torch.empty(B + 1, dtype=torch.int64, device=self.dev)
-        self.totals = torch.empty(4, dtype=torch.int64, device=self.dev)
-        self.key = None
+        self._drain()            # in-flight steps still read the old input buffers
+        self.inputs = [_Inputs(B, T, self.C_s, dtype, self.dev) for _ in range(self.depth)]
+        self.in_key = (B, T, dtype)
+        self.key = None          # the graphs capture the input buffers' addresses
 
-    def _ensure_t(self, T: int, dtype: torch.dtype):
-        if T == self.T and self.s is not None and self.s.dtype == dtype:
-            return
-        self.T = T
-        self.s = torch.empty(T, self.C_s, dtype=dtype, device=self.dev)
-        self.row_start = torch.empty(T + 1, dtype=torch.int64, device=self.dev)
-        self.row_sample = torch.empty(max(T, 1), dtype=torch.int32, device=self.dev)
-        self.key = None
-
-    def _partition(self, stream) -> "_nt.Partition":
-        # scan and row splits in one call (the singles' row count bounds T)
+    def _partition(self, inp: _Inputs, B: int, T: int, stream) -> "_nt.Partition":
+        # scan and row splits in one call (the singles' row count bounds T);
+        # the totals' read-back synchronises `stream` only
         c = _nt.nt_partition()
         st = _nt.lib().nt_partition_build_with_rows(
-            _nt._ptr(self.lengths) if self.B else None, self.B, self.T, _nt._ptr(self.cu), _nt._ptr(self.pair_off),
-            _nt._ptr(self.totals), _nt._ptr(self.row_start), _nt._ptr(self.row_sample), ctypes.byref(c),
+            _nt._ptr(inp.lengths) if B else None, B, T, _nt._ptr(inp.cu), _nt._ptr(inp.pair_off),
+            _nt._ptr(inp.totals), _nt._ptr(inp.row_start), _nt._ptr(inp.row_sample), ctypes.byref(c),
             _nt._stream(stream))
         _nt._check(st, "nt_partition_build_with_rows")
-        if c.T != self.T:
-            raise ValueError(f"the lengths sum to {c.T}, the singles have {self.T} rows")
-        return _nt.Partition(self.lengths, self.cu, self.pair_off, self.totals, self.row_start, self.row_sample, c)
+        if c.T != T:
+            raise ValueError(f"the lengths sum to {c.T}, the singles have {T} rows")
+        return _nt.Partition(inp.lengths, inp.cu, inp.pair_off, inp.totals, inp.row_start, inp.row_sample, c)
 
     # -- the captured parts ------------------------------------------------------------
-    def _piece(self, part, k: int, idx: int):
-        """Slice ``idx`` of set ``k``'s step: the broadcast before the first
+    def _piece(self, k: int, idx: int):
+        """Slice ``idx`` of slot ``k``'s step: the broadcast before the first
         slice, the reduce after the last."""
         w = self.w
         st = self.sets[k]
+        inp = self.inputs[k]
+        part = inp.part
         c0, c1 = self.cuts[idx], self.cuts[idx + 1]
         if idx == 0:
-            _nt.nt_pair_broadcast(part, self.s, self.s, w.W_a, w.W_b, z=st.z, workspace=self.ws)
+            _nt.nt_pair_broadcast(part, inp.s, inp.s, w.W_a, w.W_b, z=st.z, workspace=self.ws)
         if c1 > c0:
             _nt.nt_pair_transition_cells(st.z[c0:c1], w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2,
                                          ln_eps=self.ln_eps, out=st.z[c0:c1])
         if idx == self.slices - 1:
-            _nt.nt_pair_reduce(part, st.z, w.W_g, w.b_g, s_in=self.s, m=st.m, s_out=st.s_out)
-            if self.readback == "loss":
-                _nt.nt_pair_block_loss(part, st.s_out, st.z, want_grads=False, loss=st.loss,
-                                       workspace=self.loss_ws)
+            if self.readback == "loss":      # the reduce reads z~ once for the mean and the loss
+                _nt.nt_pair_reduce_loss(part, st.z, w.W_g, w.b_g, s_in=inp.s, m=st.m, s_out=st.s_out, loss=st.loss,
+                                        workspace=self.loss_ws)
+            else:
+                _nt.nt_pair_reduce(part, st.z, w.W_g, w.b_g, s_in=inp.s, m=st.m, s_out=st.s_out)
 
     def _drain(self):
         for st in self.sets:
@@ -147,16 +162,18 @@ class BlockGraph:
                 st.done.synchronize()
                 st.busy = False
         torch.cuda.synchronize(self.dev)
+        for inp in self.inputs:
+            inp.used = False
 
     def _setup(self, part, dtype):
-        """Buffers for a new (B, T, P); graphs are captured on each set's first use."""
+        """Output buffers for a new (B, T, P); graphs are captured on each slot's first use."""
         self._drain()
         P, T = part.P, part.T
         self.cuts = slice_cuts(P, self.slices, self.growth)
         need = _nt.nt_pair_broadcast_workspace_bytes_rect(T, T, self.C_z)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.dev)
-        self.loss_ws = torch.empty(max(int(_nt.lib().nt_pair_block_loss_workspace_bytes()), 16), dtype=torch.uint8,
-                                   device=self.dev)
+        self.loss_ws = torch.empty(max(int(_nt.lib().nt_pair_reduce_loss_workspace_bytes()), 16),
+                                   dtype=torch.uint8, device=self.dev)
         self.sets = []
         for _ in range(self.depth):
             st = _Set()
@@ -172,19 +189,19 @@ class BlockGraph:
             st.sliced = [torch.cuda.Event() for _ in range(self.slices)]
             st.done = torch.cuda.Event()
             self.sets.append(st)
-        self.key = (self.B, T, P)
+        self.key = (part.c.B, T, P)
 
-    def _capture(self, part, k: int):
+    def _capture(self, k: int):
         # one eager pass first (launch attributes, tensor maps, the library's
         # own lazy set-up happen outside the capture)
         for idx in range(self.slices):
-            self._piece(part, k, idx)
+            self._piece(k, idx)
         torch.cuda.synchronize(self.dev)
         graphs = []
         for idx in range(self.slices):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                self._piece(part, k, idx)
+                self._piece(k, idx)
             graphs.append(g)
         self.sets[k].graphs = graphs
 
@@ -192,31 +209,39 @@ class BlockGraph:
     def submit(self, lengths_host: torch.Tensor, s_host: torch.Tensor) -> int:
         """Enqueue one step: ``lengths_host`` (int32, B) and ``s_host`` (T x C_s),
         both in pinned host memory.  Returns a ticket for ``wait`` once the
-        step's device work and read-backs are enqueued (after the
-        partition's totals have come back)."""
+        step's device work and read-backs are enqueued (after the partition's
+        totals have come back, which also means the host inputs have been
+        copied and may be reused)."""
         if lengths_host.dtype != torch.int32 or s_host.dim() != 2 or s_host.shape[1] != self.C_s:
             raise ValueError("lengths must be int32 (B,) and s (T, C_s)")
         main = torch.cuda.current_stream(self.dev)
         B, T = lengths_host.numel(), s_host.shape[0]
-        if self.s is None or B != self.B or T != self.T or self.s.dtype != s_host.dtype:
-            self._drain()            # in-flight steps still read the old input buffers
-        self._ensure_b(B)
-        self._ensure_t(T, s_host.dtype)
-        self.lengths.copy_(lengths_host, non_blocking=True)
-        self.s.copy_(s_host, non_blocking=True)
-        part = self._partition(main)
-        if self.key != (self.B, part.T, part.P):
-            self._setup(part, s_host.dtype)
+        self._ensure_inputs(B, T, s_host.dtype)
         ticket = self.submitted
         k = ticket % self.depth
+        inp = self.inputs[k]
+        # copies in and partition on the input stream, beside the running step
+        with torch.cuda.stream(self.in_stream):
+            if inp.used:
+                self.in_stream.wait_event(inp.free)    # the slot's previous graphs have read them
+            inp.lengths.copy_(lengths_host, non_blocking=True)
+            inp.s.copy_(s_host, non_blocking=True)
+            part = self._partition(inp, B, T, self.in_stream)
+            inp.ready.record(self.in_stream)
+        if self.key != (B, part.T, part.P):
+            self._setup(part, s_host.dtype)           # drains: every slot's graphs are captured anew
+        inp.part = part
         st = self.sets[k]
         if st.busy:
-            main.wait_event(st.done)     # the set's previous read-back has finished with z~ and s_out
+            main.wait_event(st.done)     # the slot's previous read-back has finished with z~ and s_out
+        main.wait_event(inp.ready)
         if not st.graphs:
-            self._capture(part, k)
+            self._capture(k)
         for idx in range(self.slices):
             st.graphs[idx].replay()
             st.sliced[idx].record(main)
+        inp.free.record(main)
+        inp.used = True
         with torch.cuda.stream(self.copy_stream):
             for idx in range(self.slices):
                 c0, c1 = self.cuts[idx], self.cuts[idx + 1]

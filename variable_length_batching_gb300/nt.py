@@ -59,6 +59,8 @@ SIGNATURES = {
     "nt_pair_block_fused_workspace_bytes": (_SZ, [_I64, _I64, _I32]),
     "nt_pair_block_fused": (_I32, [_PP, _I32, _P, _P, _I32, _P, _P, _I32, _I32, _P, _P, _F, _P, _P, _P, _P, _P, _P,
                                    _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "nt_pair_reduce_loss_workspace_bytes": (_SZ, []),
+    "nt_pair_reduce_loss": (_I32, [_PP, _I32, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _P, _SZ, _P]),
     "nt_pair_block_loss_workspace_bytes": (_SZ, []),
     "nt_pair_block_loss": (_I32, [_PP, _I32, _P, _I32, _P, _I32, _P, _P, _P, _P, _SZ, _P]),
     "nt_pair_block_backward_workspace_bytes": (_SZ, [_I32, _I64, _I64, _I32, _I32]),
@@ -352,6 +354,37 @@ def nt_pair_reduce(part: Partition, z: torch.Tensor, W_g: Optional[torch.Tensor]
                               _ptr(_f32(b_g)), _ptr(s_in), _ptr(s_out), C_s, _stream(stream))
     _check(st, "nt_pair_reduce")
     return m, s_out
+
+
+def nt_pair_reduce_loss(part: Partition, z: torch.Tensor, W_g: torch.Tensor, b_g: Optional[torch.Tensor] = None,
+                        s_in: Optional[torch.Tensor] = None, m: Optional[torch.Tensor] = None,
+                        s_out: Optional[torch.Tensor] = None, loss: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None):
+    """The reduce with the g projection and the Eq. 5 loss of (s_out, z) in
+    one call that reads z once: returns (m, s_out, loss as a 1-element fp32
+    device tensor).  ``m``, ``s_out``, ``loss`` and ``workspace`` (of
+    nt_pair_reduce_loss_workspace_bytes() bytes) may be given, so that a
+    captured graph writes into fixed buffers."""
+    P, C_z = z.shape
+    if P != part.P:
+        raise ValueError(f"z has {P} cells, the partition {part.P}")
+    C_s = W_g.shape[0]
+    if tuple(W_g.shape) != (C_s, C_z):
+        raise ValueError("W_g must be (C_s, C_z)")
+    dev = z.device
+    if m is None:
+        m = torch.empty(part.T, C_z, dtype=z.dtype, device=dev)
+    if s_out is None:
+        s_out = torch.empty(part.T, C_s, dtype=z.dtype, device=dev)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(int(lib().nt_pair_reduce_loss_workspace_bytes()), dtype=torch.uint8, device=dev)
+    st = lib().nt_pair_reduce_loss(ctypes.byref(part.c), _dtype(z), _ptr(z), C_z, _ptr(m), _ptr(W_g),
+                                   _ptr(_f32(b_g)), _ptr(s_in), _ptr(s_out), C_s, _ptr(loss), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nt_pair_reduce_loss")
+    return m, s_out, loss
 
 
 def nt_pair_block_loss(part: Partition, s_out: torch.Tensor, z_tilde: torch.Tensor, want_grads: bool = True,
