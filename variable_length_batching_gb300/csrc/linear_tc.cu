@@ -42,9 +42,8 @@ struct Bars {
 
 struct Prob {
   const float* bias;
-  const bf16* R;     // residual (or, with kEpiMask, the mask) [M, N], or null
+  const bf16* R;     // residual [M, N], or null
   void* Y;           // [M, N], fp32 or bf16
-  int epi;           // kEpiPlain, kEpiRelu or kEpiMask
 };
 
 template <bool kOutF32>
@@ -137,26 +136,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant_
       tmem_ld_wait();
       if (row < M) {
         const int c0 = n0 + 32 * g;
-        if (pr.bias && pr.epi != kEpiMask) {
+        if (pr.bias) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] += pr.bias[c0 + c];
         }
-        if (pr.epi == kEpiRelu) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = fmaxf(v[c], 0.f);
-        } else if (pr.epi == kEpiMask && has_r) {
-          // keep the entries whose mask element is positive
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint4 q4 = res[4 * g + u];
-            const uint32_t w[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (!(bf16lo(w[e]) > 0.f)) v[8 * u + 2 * e] = 0.f;
-              if (!(bf16hi(w[e]) > 0.f)) v[8 * u + 2 * e + 1] = 0.f;
-            }
-          }
-        } else if (has_r) {
+        if (has_r) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint4 q4 = res[4 * g + u];
@@ -414,26 +398,18 @@ linear_tc_persistent_kernel(const __grid_constant__ CUtensorMap tx, const __grid
           for (int c = 0; c < 4; ++c) rq[c] = *stg_at(lane, c);
           __syncwarp();
         }
-        if (pr.bias && pr.epi != kEpiMask) {
+        if (pr.bias) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] += pr.bias[c0 + c];
         }
-        if (pr.epi == kEpiRelu) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = fmaxf(v[c], 0.f);
-        } else if (pr.R) {
+        if (pr.R) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t w[4] = {rq[u].x, rq[u].y, rq[u].z, rq[u].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              if (pr.epi == kEpiMask) {
-                if (!(bf16lo(w[e]) > 0.f)) v[8 * u + 2 * e] = 0.f;
-                if (!(bf16hi(w[e]) > 0.f)) v[8 * u + 2 * e + 1] = 0.f;
-              } else {
-                v[8 * u + 2 * e] += bf16lo(w[e]);
-                v[8 * u + 2 * e + 1] += bf16hi(w[e]);
-              }
+              v[8 * u + 2 * e] += bf16lo(w[e]);
+              v[8 * u + 2 * e + 1] += bf16hi(w[e]);
             }
           }
         }
@@ -490,7 +466,7 @@ cudaError_t launch_linear_tc_dual(const void* X, const void* W, const float* bia
       !make_tmap_rows(&px2, X2, (uint64_t)K2, (uint64_t)M, kBM) ||
       !make_tmap_rows(&pw2, W2, (uint64_t)K2, (uint64_t)N, kPN))
     return cudaErrorInvalidValue;
-  const Prob pp0 = Prob{bias, nullptr, Y, kEpiRelu};
+  const Prob pp0 = Prob{bias, nullptr, Y};
   using C = PCfg<true>;
   const int grid = (int)min64(ptiles, (int64_t)C::kCtasPerSm * sm_count());
   auto kern = linear_tc_persistent_kernel<false, true>;
@@ -513,7 +489,7 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
     if (!make_tmap_rows(&px, lp.X, (uint64_t)K, (uint64_t)M, kBM) ||
         !make_tmap_rows(&pw, lp.W, (uint64_t)K, (uint64_t)N, kPN))
       return cudaErrorInvalidValue;
-    const Prob pp0 = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y, lp.epi};
+    const Prob pp0 = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y};
     using C = PCfg<false>;
     const int grid = (int)min64(ptiles, (int64_t)C::kCtasPerSm * sm_count());
     auto kern = out_f32 ? linear_tc_persistent_kernel<true, false> : linear_tc_persistent_kernel<false, false>;
@@ -531,7 +507,7 @@ cudaError_t launch_linear_tc(int out_f32, const LinearProblem* probs, int nprob,
     if (!make_tmap_rows(&tx[i], lp.X, (uint64_t)K, (uint64_t)M, kBM) ||
         !make_tmap_rows(&tw[i], lp.W, (uint64_t)K, (uint64_t)N, kBN))
       return cudaErrorInvalidValue;
-    pp[i] = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y, lp.epi};
+    pp[i] = Prob{lp.bias, static_cast<const bf16*>(lp.R), lp.Y};
   }
   const int64_t blocks = (M + kBM - 1) / kBM * (N / kBN);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;

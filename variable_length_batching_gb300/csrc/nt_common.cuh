@@ -142,13 +142,8 @@ cudaError_t launch_partition_fused(const int32_t* lengths, int32_t B, int64_t ca
 // Y[M, N] = X[M, K] W[N, K]^T (+ bias[N]) (+ R[M, N]).  Up to two independent
 // problems in one launch (gridDim.z); all row-major, contiguous.
 struct LinearProblem {
-  const void* X; const void* W; const float* bias; const void* R; void* Y;
-  // epilogue of the tcgen05 path: kEpiPlain  Y = acc (+ bias) (+ R);
-  // kEpiRelu  Y = max(acc + bias, 0); kEpiMask  Y = acc where R > 0, else 0
-  // (R a bf16 [M, N] tensor; no bias)
-  int epi = 0;
+  const void* X; const void* W; const float* bias; const void* R; void* Y;   // Y = X W^T (+ bias) (+ R)
 };
-constexpr int kEpiPlain = 0, kEpiRelu = 1, kEpiMask = 2;
 cudaError_t launch_linear(int in_dtype /*nt_dtype of X, W, R*/, int out_f32 /*Y fp32?*/,
                           const LinearProblem* probs, int nprob, int64_t M, int N, int K,
                           cudaStream_t s);
