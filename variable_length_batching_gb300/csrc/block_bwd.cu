@@ -674,8 +674,9 @@ constexpr int kTcC = 128;          // pair width of the tensor-core route
 // and lo = bf16(y - hi), side by side in a row of 2 C_z (A = [hi | lo] [W1 |
 // W1]^T carries y to about 16 bits, so A's sign, the ReLU's decision, is
 // that of the fp32 y), and dP~ = dz_up + dM[row] / N as bf16, with z
-// rebuilt bf16-rounded as the forward rounds it.  With zt_up, dz_up is
-// Eq. 5's gp_b z~, formed here as the loss forms it.
+// rebuilt bf16-rounded as the forward rounds it, and the LayerNorm's mean
+// and rstd per cell for the LayerNorm backward.  With zt_up, dz_up is Eq.
+// 5's gp_b z~, formed here as the loss forms it.
 constexpr int kPrepThreads = 256;
 constexpr int kPrepCells = kPrepThreads / 16;   // cells per pass
 
@@ -685,7 +686,7 @@ bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const 
                 const int32_t* __restrict__ row_sample, int B, int64_t T, int64_t P,
                 const float* __restrict__ gamma, const float* __restrict__ beta, float eps,
                 const float* __restrict__ dM, const float* __restrict__ dz_up, const bf16* __restrict__ zt_up,
-                bf16* __restrict__ Y, bf16* __restrict__ dPt) {
+                bf16* __restrict__ Y, bf16* __restrict__ dPt, float2* __restrict__ stats) {
   const int lane = threadIdx.x & 31, q = threadIdx.x & 15, slot = threadIdx.x >> 4;
   __shared__ float gsh[kTcC], bsh[kTcC];
   if (threadIdx.x < kTcC) {
@@ -761,6 +762,7 @@ bwd_prep_kernel(const float* __restrict__ u, const float* __restrict__ v, const 
         const float rs = rsqrtf(s2 * (1.0f / kTcC) + eps);
         if (!ok[c]) continue;
         const int64_t p = p0 + j0 + c * kPrepCells + slot;
+        if (q == 0) stats[p] = make_float2(mean, rs);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t yw[2], lw[2], gw[2];
@@ -832,14 +834,15 @@ constexpr int kSumWarps = kSumThreads / 32;
 constexpr int kSumRows = 2;                                   // rows per copy group
 constexpr int kSumBufs = 3;                                   // copy groups in flight
 constexpr int kSumHalf = kSumTile * kTcC * 4;                 // 32 cells of fp32 features: 16 KB
-constexpr int kSumRowBytes = 2 * kSumHalf + 2 * kTcC * 4;     // dY, the upstream gradient, u[row], dM[row]
+constexpr int kSumStatBytes = 512;                             // the row's cells' (mean, rstd), from an even cell
+constexpr int kSumRowBytes = 2 * kSumHalf + 2 * kTcC * 4 + kSumStatBytes;   // dY, upstream, u[row], dM[row], stats
 constexpr size_t kSumSmem = (size_t)kSumBufs * kSumRows * kSumRowBytes + (size_t)kSumRows * kSumWarps * kTcC * 4 +
                             kSumBufs * sizeof(uint64_t);
 
 __global__ void __launch_bounds__(kSumThreads, 1)
 bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
                    const int32_t* __restrict__ cu, const int32_t* __restrict__ len, int B,
-                   const float* __restrict__ gamma, float eps, const float* __restrict__ dM,
+                   const float* __restrict__ gamma, const float2* __restrict__ stats, const float* __restrict__ dM,
                    const float* __restrict__ dz_up, const bf16* __restrict__ zt_up, const float* __restrict__ dY,
                    float* __restrict__ du_part, float* __restrict__ dv_part, float* __restrict__ dgamma,
                    float* __restrict__ dbeta, unsigned int* status) {
@@ -883,10 +886,21 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
   // copy group k: rows a_lo + 2k, a_lo + 2k + 1 into buffer k % 3
   auto issue = [&](int k) {
     const int buf = k % kSumBufs, a0 = a_lo + k * kSumRows, nr = min(kSumRows, a_hi - a0);
-    mbar_arrive_expect_tx(&full[buf], (uint32_t)nr * ((uint32_t)ncols * (kTcC * 4 + up_cell) + 2 * kTcC * 4));
+    // the stats copy starts at the even cell at or before the row's first
+    // (8-byte entries, 16-byte copies) and ends at an even cell count: one
+    // entry either side at most, inside the padded buffer
+    uint32_t tx = 0;
+    for (int r = 0; r < nr; ++r) {
+      const int64_t p = P0 + (int64_t)(a0 + r) * n + j0;
+      tx += (uint32_t)ncols * (kTcC * 4 + up_cell) + 2 * kTcC * 4 + (uint32_t)((((p + ncols + 1) & ~1LL) - (p & ~1LL)) * 8);
+    }
+    mbar_arrive_expect_tx(&full[buf], tx);
     for (int r = 0; r < nr; ++r) {
       const int64_t p = P0 + (int64_t)(a0 + r) * n + j0;
       uint8_t* dst = bufs + (size_t)(buf * kSumRows + r) * kSumRowBytes;
+      const int64_t s0 = p & ~1LL;
+      bulk_load(dst + 2 * kSumHalf + 2 * kTcC * 4, stats + s0, (uint32_t)((((p + ncols + 1) & ~1LL) - s0) * 8),
+                &full[buf]);
       bulk_load(dst + 2 * kSumHalf, u + (t0 + a0 + r) * kTcC, kTcC * 4, &full[buf]);
       bulk_load(dst + 2 * kSumHalf + kTcC * 4, dM + (t0 + a0 + r) * kTcC, kTcC * 4, &full[buf]);
       bulk_load(dst, dY + p * kTcC, (uint32_t)ncols * kTcC * 4, &full[buf]);
@@ -917,6 +931,8 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
         const uint8_t* sr = bufs + (size_t)(buf * kSumRows + r) * kSumRowBytes;
         const float* su = reinterpret_cast<const float*>(sr + 2 * kSumHalf);
         const float* sdm = su + kTcC;
+        const int64_t pr0 = P0 + (int64_t)(a0 + r) * n + j0;      // the row's first cell
+        const float2 st = reinterpret_cast<const float2*>(sdm + kTcC)[(pr0 & 1) + (cv ? slot : 0)];
         float dy[8], up[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) { dy[e] = 0.f; up[e] = 0.f; }
@@ -937,10 +953,10 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
             up[4] = u1.x; up[5] = u1.y; up[6] = u1.z; up[7] = u1.w;
           }
         }
-        // z rebuilt as the forward rounds it; its LayerNorm statistics over
-        // the 16 threads of the column.  Elementwise work in fp32 pairs; a
-        // column past the sample's end takes rstd = 1/N = 0, so its x-hat,
-        // dP~ and dz are exactly 0 (dy and up are 0 there already).
+        // z rebuilt as the forward rounds it, x-hat from its kept mean and
+        // rstd.  Elementwise work in fp32 pairs; a column past the sample's
+        // end takes rstd = 1/N = 0, so its x-hat, dP~ and dz are exactly 0
+        // (dy and up are 0 there already).
         float xh[8], gv[8], dx[8];
         {
           const float4 a0 = *reinterpret_cast<const float4*>(su + 4 * q);
@@ -964,28 +980,11 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
             fmul2(dy[i], dy[i + 1], ga[i], ga[i + 1], dx[i], dx[i + 1]);
           }
         }
-        float sa, sb;
-        fadd2(xh[0], xh[1], xh[2], xh[3], sa, sb);
-        fadd2(sa, sb, xh[4], xh[5], sa, sb);
-        fadd2(sa, sb, xh[6], xh[7], sa, sb);
-        float s1 = sa + sb;
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-        const float mean = s1 * (1.0f / kTcC);
-        sa = 0.f;
-        sb = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          fadd2(xh[i], xh[i + 1], -mean, -mean, xh[i], xh[i + 1]);
-          ffma2(xh[i], xh[i + 1], xh[i], xh[i + 1], sa, sb, sa, sb);
-        }
-        float s2 = sa + sb;
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-        const float rs = cv ? rsqrtf(s2 * (1.0f / kTcC) + eps) : 0.f;
+        const float mean = st.x, rs = cv ? st.y : 0.f;
         float m1a = 0.f, m1b = 0.f, m2a = 0.f, m2b = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
+          fadd2(xh[i], xh[i + 1], -mean, -mean, xh[i], xh[i + 1]);
           fmul2(xh[i], xh[i + 1], rs, rs, xh[i], xh[i + 1]);
           fadd2(m1a, m1b, dx[i], dx[i + 1], m1a, m1b);
           ffma2(dx[i], dx[i + 1], xh[i], xh[i + 1], m2a, m2b, m2a, m2b);
@@ -1109,7 +1108,7 @@ __global__ void twice_bf16_kernel(const bf16* __restrict__ in, int R, int Cc, bf
 // Byte offsets of the route's buffers in the workspace past the CUDA-core
 // route's (each 256-byte aligned).
 struct TcLayout {
-  size_t Y, dPt, H, dA, W1t, W2t, W1x2, du_part, dv_part, wg, end;
+  size_t Y, dPt, H, dA, stats, W1t, W2t, W1x2, du_part, dv_part, wg, end;
 };
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 TcLayout tc_layout(int64_t P, int64_t T, int C, int H) {
@@ -1119,6 +1118,7 @@ TcLayout tc_layout(int64_t P, int64_t T, int C, int H) {
   L.dPt = o; o = align256(o + (size_t)P * C * 2);
   L.H = o; o = align256(o + (size_t)P * H * 2);
   L.dA = o; o = align256(o + (size_t)P * H * 2);
+  L.stats = o; o = align256(o + (size_t)P * 8 + 16);   // one entry of slack for the 16-byte copies
   L.W1t = o; o = align256(o + (size_t)C * H * 2);
   L.W2t = o; o = align256(o + (size_t)C * H * 2);
   L.W1x2 = o; o = align256(o + (size_t)2 * C * H * 2);
@@ -1144,6 +1144,7 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
   bf16* W1t = reinterpret_cast<bf16*>(tcw + L.W1t);
   bf16* W2t = reinterpret_cast<bf16*>(tcw + L.W2t);
   bf16* W1x2 = reinterpret_cast<bf16*>(tcw + L.W1x2);
+  float2* stats = reinterpret_cast<float2*>(tcw + L.stats);
   float* du_part = reinterpret_cast<float*>(tcw + L.du_part);
   float* dv_part = reinterpret_cast<float*>(tcw + L.dv_part);
   void* wg = tcw + L.wg;
@@ -1153,7 +1154,7 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
   twice_bf16_kernel<<<gt, 256, 0, s>>>((const bf16*)q.W1, H, C, W1x2);       // [W1 | W1], [H, 2C]
   bwd_prep_kernel<<<(unsigned)min64(p->T, (int64_t)sm_count() * 16), kPrepThreads, 0, s>>>(
       q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->row_sample, p->B, p->T, P, q.gamma, q.beta, q.eps, q.dM,
-      q.dz_up, (const bf16*)q.zt_up, Y, dPt);
+      q.dz_up, (const bf16*)q.zt_up, Y, dPt, stats);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // H = ReLU([hi | lo] [W1 | W1]^T + b1) and dA = (dP~ W2) where H > 0, per tile in one
@@ -1169,7 +1170,7 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
       cudaSuccess)
     return e;
   bwd_ln_sums_kernel<<<(unsigned)items, kSumThreads, kSumSmem, s>>>(
-      q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, q.gamma, q.eps, q.dM, q.dz_up, (const bf16*)q.zt_up,
+      q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, q.gamma, stats, q.dM, q.dz_up, (const bf16*)q.zt_up,
       q.dz, du_part, dv_part, q.dgamma, q.dbeta, status);
   sums_finish_kernel<<<(unsigned)min64((p->T * C + kThreads - 1) / kThreads, (int64_t)sm_count() * 8), kThreads, 0,
                        s>>>(du_part, dv_part, p->pair_off, p->cu_seqlens, p->lengths, p->row_sample, p->T, q.du,
