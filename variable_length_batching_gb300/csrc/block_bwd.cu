@@ -186,75 +186,119 @@ eq5_finish_kernel(const double* __restrict__ partial, int nblocks, int64_t Trows
 
 // ------------------------------------------------------- the single rows side
 
+// Register-tiled fp32 products over the T single rows: a CTA computes a 64 x
+// 64 block of the output, each thread a 4 x 4 piece of it, from 16-deep
+// slices of both operands staged in shared memory (16 FMAs per two 16-byte
+// shared loads).
+constexpr int kGT = 64, kGK = 16;
+
 // Y[r, n] = R[r, n] + sum_k A[r, k] W[k, n] + sum_k A2[r, k] W2[k, n]
 // (A, A2 fp32 [rows, K]; W, W2 [K, N] row-major in the I/O dtype; R fp32 or
-// null; A2 and W2 may be null).  One CTA per 16 rows; its threads walk the
-// N columns.
+// null; A2 and W2 may be null).  Grid (ceil(N / 64), ceil(rows / 64)).
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 rowmm_kernel(const float* __restrict__ A, const T* __restrict__ W, const float* __restrict__ A2,
              const T* __restrict__ W2, const float* __restrict__ R, int64_t rows, int K, int N,
              float* __restrict__ Y) {
-  extern __shared__ float sa[];               // [16][K] of A, then [16][K] of A2
-  const int64_t r0 = (int64_t)blockIdx.x * 16;
-  const int nr = (int)min64(16, rows - r0);
-  for (int e = threadIdx.x; e < 16 * K; e += kThreads) {
-    const int rr = e / K, k = e % K;
-    sa[e] = rr < nr ? A[(r0 + rr) * K + k] : 0.f;
-    if (A2) sa[16 * K + e] = rr < nr ? A2[(r0 + rr) * K + k] : 0.f;
-  }
-  __syncthreads();
-  for (int n = threadIdx.x; n < N; n += kThreads) {
-    float acc[16];
+  __shared__ __align__(16) float as[kGK][kGT + 4];   // [k][row]
+  __shared__ __align__(16) float ws[kGK][kGT + 4];   // [k][col]
+  const int64_t r0 = (int64_t)blockIdx.y * kGT;
+  const int n0 = blockIdx.x * kGT;
+  const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;   // rows 4 tr .. 4 tr + 3, columns 4 tc ..
+  float acc[4][4];
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
-    for (int k = 0; k < K; ++k) {
-      const float w = to_f32(W[(int64_t)k * N + n]);
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) acc[rr] = fmaf(sa[rr * K + k], w, acc[rr]);
-    }
-    if (A2) {
-      for (int k = 0; k < K; ++k) {
-        const float w = to_f32(W2[(int64_t)k * N + n]);
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int pass = 0; pass < (A2 ? 2 : 1); ++pass) {
+    const float* Ap = pass ? A2 : A;
+    const T* Wp = pass ? W2 : W;
+    for (int k0 = 0; k0 < K; k0 += kGK) {
+      {   // A: 64 rows x 16 k, four consecutive k per thread, stored k-major
+        const int rr = threadIdx.x >> 2, kk = (threadIdx.x & 3) * 4;
+        const int64_t r = r0 + rr;
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) acc[rr] = fmaf(sa[16 * K + rr * K + k], w, acc[rr]);
+        for (int e = 0; e < 4; ++e) as[kk + e][rr] = (r < rows && k0 + kk + e < K) ? Ap[r * K + k0 + kk + e] : 0.f;
       }
+      {   // W: 16 k x 64 columns, four consecutive columns per thread
+        const int kk = threadIdx.x >> 4, cc = (threadIdx.x & 15) * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          ws[kk][cc + e] = (k0 + kk < K && n0 + cc + e < N) ? to_f32(Wp[(int64_t)(k0 + kk) * N + n0 + cc + e]) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < kGK; ++kk) {
+        const float4 a = *reinterpret_cast<const float4*>(&as[kk][4 * tr]);
+        const float4 w = *reinterpret_cast<const float4*>(&ws[kk][4 * tc]);
+        const float av[4] = {a.x, a.y, a.z, a.w}, wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], wv[j], acc[i][j]);
+      }
+      __syncthreads();
     }
-    for (int rr = 0; rr < nr; ++rr) Y[(r0 + rr) * N + n] = (R ? R[(r0 + rr) * N + n] : 0.f) + acc[rr];
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t r = r0 + 4 * tr + i;
+    if (r >= rows) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + 4 * tc + j;
+      if (n < N) Y[r * N + n] = (R ? R[r * N + n] : 0.f) + acc[i][j];
+    }
   }
 }
 
 // G[i, j] += sum_r A[r, i] B[r, j] over a range of the single rows (A fp32
-// [rows, M], B [rows, N] fp32 or I/O dtype): one CTA per 32 x 32 tile of G
-// and per range of rows, fp32 atomics into G.
+// [rows, M], B [rows, N] fp32 or I/O dtype): grid (ceil(M / 64), ceil(N /
+// 64), splits), one 64 x 64 block of G per CTA and range of rows, fp32
+// atomics into G.
 template <typename TB>
 __global__ void __launch_bounds__(kThreads)
 gram_kernel(const float* __restrict__ A, const TB* __restrict__ Bm, int64_t rows, int M, int N, int splits,
             float* __restrict__ G) {
-  __shared__ float ta[32][33], tb[32][33];
-  const int i0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  __shared__ __align__(16) float as[kGK][kGT + 4];   // [row][i]
+  __shared__ __align__(16) float bs[kGK][kGT + 4];   // [row][j]
+  const int i0 = blockIdx.x * kGT, j0 = blockIdx.y * kGT;
   const int64_t rlo = rows * blockIdx.z / splits, rhi = rows * (blockIdx.z + 1) / splits;
-  const int ti = threadIdx.x >> 3, tj = (threadIdx.x & 7) * 4;   // 32 x (8 x 4): four outputs per thread
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int64_t rb = rlo; rb < rhi; rb += 32) {
-    for (int e = threadIdx.x; e < 32 * 32; e += kThreads) {
-      const int rr = e >> 5, c = e & 31;
+  const int ti = threadIdx.x >> 4, tj = threadIdx.x & 15;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int64_t rb = rlo; rb < rhi; rb += kGK) {
+    {   // 16 rows x 64 columns of each operand, four consecutive columns per thread
+      const int rr = threadIdx.x >> 4, cc = (threadIdx.x & 15) * 4;
       const int64_t r = rb + rr;
-      ta[rr][c] = (r < rhi && i0 + c < M) ? A[r * M + i0 + c] : 0.f;
-      tb[rr][c] = (r < rhi && j0 + c < N) ? to_f32(Bm[r * N + j0 + c]) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        as[rr][cc + e] = (r < rhi && i0 + cc + e < M) ? A[r * M + i0 + cc + e] : 0.f;
+        bs[rr][cc + e] = (r < rhi && j0 + cc + e < N) ? to_f32(Bm[r * N + j0 + cc + e]) : 0.f;
+      }
     }
     __syncthreads();
-#pragma unroll 8
-    for (int rr = 0; rr < 32; ++rr) {
-      const float a = ta[rr][ti];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[q] = fmaf(a, tb[rr][tj + q], acc[q]);
+    for (int kk = 0; kk < kGK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&as[kk][4 * ti]);
+      const float4 b = *reinterpret_cast<const float4*>(&bs[kk][4 * tj]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if (i0 + ti < M && j0 + tj + q < N) atomicAdd(G + (int64_t)(i0 + ti) * N + j0 + tj + q, acc[q]);
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (i0 + 4 * ti + i < M && j0 + 4 * tj + j < N)
+        atomicAdd(G + (int64_t)(i0 + 4 * ti + i) * N + j0 + 4 * tj + j, acc[i][j]);
 }
 
 // out[j] += sum_r A[r, j] over a range of rows (fp32 atomics).
@@ -600,11 +644,10 @@ cudaError_t block_backward_t(const BlockBwd& q, unsigned int* status, cudaStream
   cudaError_t e;
   // dM = dX~ W_g ([T, C_s] x [C_s, C_z]); dW_g += dX~^T m; db_g += column sums of dX~
   if (Trows > 0) {
-    const unsigned g = (unsigned)((Trows + 15) / 16);
-    rowmm_kernel<T><<<g, kThreads, 16 * Cs * sizeof(float), s>>>(q.ds_out, (const T*)q.W_g, nullptr, nullptr,
-                                                                  nullptr, Trows, Cs, C, q.dM);
+    rowmm_kernel<T><<<dim3((C + kGT - 1) / kGT, (unsigned)((Trows + kGT - 1) / kGT)), kThreads, 0, s>>>(
+        q.ds_out, (const T*)q.W_g, nullptr, nullptr, nullptr, Trows, Cs, C, q.dM);
     const int splits = (int)min64(64, (Trows + 255) / 256);
-    gram_kernel<T><<<dim3((Cs + 31) / 32, (C + 31) / 32, splits), kThreads, 0, s>>>(q.ds_out, (const T*)q.m,
+    gram_kernel<T><<<dim3((Cs + kGT - 1) / kGT, (C + kGT - 1) / kGT, splits), kThreads, 0, s>>>(q.ds_out, (const T*)q.m,
                                                                                       Trows, Cs, C, splits, q.dW_g);
     colsum_kernel<<<dim3((Cs + kThreads - 1) / kThreads, splits), kThreads, 0, s>>>(q.ds_out, Trows, Cs, splits,
                                                                                      q.db_g);
@@ -636,13 +679,12 @@ cudaError_t block_backward_t(const BlockBwd& q, unsigned int* status, cudaStream
       pair_rowcol_sum_kernel<<<(unsigned)min64(Trows, 4096), kThreads, 2 * kThreads * sizeof(float), s>>>(
           q.dz, p->cu_seqlens, p->pair_off, p->lengths, p->row_sample, Trows, C, q.du, q.dv);
     const int splits = (int)min64(64, (Trows + 255) / 256);
-    gram_kernel<T><<<dim3((C + 31) / 32, (Cs + 31) / 32, splits), kThreads, 0, s>>>(q.du, (const T*)q.s, Trows, C,
+    gram_kernel<T><<<dim3((C + kGT - 1) / kGT, (Cs + kGT - 1) / kGT, splits), kThreads, 0, s>>>(q.du, (const T*)q.s, Trows, C,
                                                                                      Cs, splits, q.dW_a);
-    gram_kernel<T><<<dim3((C + 31) / 32, (Cs + 31) / 32, splits), kThreads, 0, s>>>(q.dv, (const T*)q.s, Trows, C,
+    gram_kernel<T><<<dim3((C + kGT - 1) / kGT, (Cs + kGT - 1) / kGT, splits), kThreads, 0, s>>>(q.dv, (const T*)q.s, Trows, C,
                                                                                      Cs, splits, q.dW_b);
-    const unsigned g = (unsigned)((Trows + 15) / 16);
-    rowmm_kernel<T><<<g, kThreads, 2 * 16 * C * sizeof(float), s>>>(q.du, (const T*)q.W_a, q.dv, (const T*)q.W_b,
-                                                                     q.ds_out, Trows, C, Cs, q.ds);
+    rowmm_kernel<T><<<dim3((Cs + kGT - 1) / kGT, (unsigned)((Trows + kGT - 1) / kGT)), kThreads, 0, s>>>(
+        q.du, (const T*)q.W_a, q.dv, (const T*)q.W_b, q.ds_out, Trows, C, Cs, q.ds);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
