@@ -110,11 +110,24 @@ eq5_partial_kernel(const T* __restrict__ s_out, const T* __restrict__ zt, const 
                    const int32_t* __restrict__ row_sample, int B, int64_t Trows, int64_t P, int C, int Cp,
                    double* __restrict__ partial, float* __restrict__ ds_out, float* __restrict__ dz) {
   __shared__ double red[2][kThreads / 32];
+  __shared__ double s_ab[2];
+  __shared__ float s_g[2];
   double ax = 0.0, ap = 0.0;
   for (int64_t r = blockIdx.x; r < Trows; r += gridDim.x) {
-    const int b = row_sample[r];
-    const double alpha = 1.0 + (double)b / B, beta = 1.5 - (double)b / (2.0 * B);
-    const float gx = (float)(2.0 * alpha / ((double)C * Trows)), gp = eq5_pair_scale(b, B, Cp, P);
+    // the row's weights and gradient scales, formed in double once per row
+    // (fp64 divisions are slow here; every thread used to form its own)
+    if (threadIdx.x == 0) {
+      const int b = row_sample[r];
+      const double alpha = 1.0 + (double)b / B, beta = 1.5 - (double)b / (2.0 * B);
+      s_ab[0] = alpha;
+      s_ab[1] = beta;
+      s_g[0] = (float)(2.0 * alpha / ((double)C * Trows));
+      s_g[1] = eq5_pair_scale(b, B, Cp, P);
+    }
+    __syncthreads();
+    const double alpha = s_ab[0], beta = s_ab[1];
+    const float gx = s_g[0], gp = s_g[1];
+    __syncthreads();                          // read before thread 0 writes the next row's
     float sx = 0.f;
     for (int k = threadIdx.x; k < C; k += kThreads) {
       const float x = to_f32(s_out[r * C + k]);
