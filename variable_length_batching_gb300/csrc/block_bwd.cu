@@ -207,7 +207,8 @@ constexpr int kGT = 64, kGK = 16;
 
 // Y[r, n] = R[r, n] + sum_k A[r, k] W[k, n] + sum_k A2[r, k] W2[k, n]
 // (A, A2 fp32 [rows, K]; W, W2 [K, N] row-major in the I/O dtype; R fp32 or
-// null; A2 and W2 may be null).  Grid (ceil(N / 64), ceil(rows / 64)).
+// null; A2 and W2 may be null).  Grid (ceil(rows / 64), ceil(N / 64)): the
+// rows on x, whose limit is 2^31 - 1 blocks.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 rowmm_kernel(const float* __restrict__ A, const T* __restrict__ W, const float* __restrict__ A2,
@@ -215,8 +216,8 @@ rowmm_kernel(const float* __restrict__ A, const T* __restrict__ W, const float* 
              float* __restrict__ Y) {
   __shared__ __align__(16) float as[kGK][kGT + 4];   // [k][row]
   __shared__ __align__(16) float ws[kGK][kGT + 4];   // [k][col]
-  const int64_t r0 = (int64_t)blockIdx.y * kGT;
-  const int n0 = blockIdx.x * kGT;
+  const int64_t r0 = (int64_t)blockIdx.x * kGT;
+  const int n0 = blockIdx.y * kGT;
   const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;   // rows 4 tr .. 4 tr + 3, columns 4 tc ..
   float acc[4][4];
 #pragma unroll
@@ -657,7 +658,7 @@ cudaError_t block_backward_t(const BlockBwd& q, unsigned int* status, cudaStream
   cudaError_t e;
   // dM = dX~ W_g ([T, C_s] x [C_s, C_z]); dW_g += dX~^T m; db_g += column sums of dX~
   if (Trows > 0) {
-    rowmm_kernel<T><<<dim3((C + kGT - 1) / kGT, (unsigned)((Trows + kGT - 1) / kGT)), kThreads, 0, s>>>(
+    rowmm_kernel<T><<<dim3((unsigned)((Trows + kGT - 1) / kGT), (C + kGT - 1) / kGT), kThreads, 0, s>>>(
         q.ds_out, (const T*)q.W_g, nullptr, nullptr, nullptr, Trows, Cs, C, q.dM);
     const int splits = (int)min64(64, (Trows + 255) / 256);
     gram_kernel<T><<<dim3((Cs + kGT - 1) / kGT, (C + kGT - 1) / kGT, splits), kThreads, 0, s>>>(q.ds_out, (const T*)q.m,
@@ -696,7 +697,7 @@ cudaError_t block_backward_t(const BlockBwd& q, unsigned int* status, cudaStream
                                                                                      Cs, splits, q.dW_a);
     gram_kernel<T><<<dim3((C + kGT - 1) / kGT, (Cs + kGT - 1) / kGT, splits), kThreads, 0, s>>>(q.dv, (const T*)q.s, Trows, C,
                                                                                      Cs, splits, q.dW_b);
-    rowmm_kernel<T><<<dim3((Cs + kGT - 1) / kGT, (unsigned)((Trows + kGT - 1) / kGT)), kThreads, 0, s>>>(
+    rowmm_kernel<T><<<dim3((unsigned)((Trows + kGT - 1) / kGT), (Cs + kGT - 1) / kGT), kThreads, 0, s>>>(
         q.du, (const T*)q.W_a, q.dv, (const T*)q.W_b, q.ds_out, Trows, C, Cs, q.ds);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
