@@ -145,3 +145,37 @@ def test_block_graph_loss_readback(mods):
     with pytest.raises(ValueError):
         graph.BlockGraph(wd, readback="z")
     nt.nt_device_status()
+
+
+def test_block_graph_shapes_change_in_flight(mods):
+    """Pipelined steps whose (B, T, P) change from one submission to the next
+    and back (each change drains the pipeline and captures anew; the input
+    slots are reallocated when B or T changes, kept when only the values
+    do): every step's z~ and s_out equal the eager calls' bit for bit."""
+    nt, graph = mods
+    cfg = wl.PAIRFORMER_BF16
+    base = wl.make_block_inputs(cfg, lengths=[37, 1, 0, 70], biases=True)
+    w = base.blocks[0]
+    g = lambda t: None if t is None else t.to(DEV).contiguous()
+    wd = SimpleNamespace(W_a=g(w.W_a), W_b=g(w.W_b), ln_gamma=g(w.ln_gamma), ln_beta=g(w.ln_beta), W1=g(w.W1),
+                         b1=g(w.b1), W2=g(w.W2), b2=g(w.b2), W_g=g(w.W_g), b_g=g(w.b_g))
+    shapes = [[37, 1, 0, 70], [37, 1, 0, 70], [5, 90, 33], [37, 1, 0, 70], [70, 1, 0, 37], [5, 90, 33], [5, 90, 33]]
+    inps = []
+    for i, lengths in enumerate(shapes):
+        x = wl.make_block_inputs(cfg, lengths=lengths, biases=True, seed=20 + i)
+        x.blocks = base.blocks
+        inps.append(x)
+    refs = [_eager(nt, x, wd) for x in inps]
+    runner = graph.BlockGraph(wd, slices=2, growth=2.0, depth=2)
+    tickets, got = [], []
+    for i, x in enumerate(inps):
+        tickets.append(runner.submit(torch.as_tensor(np.asarray(x.lengths, dtype=np.int32)).pin_memory(),
+                                     x.s.pin_memory()))
+        if i >= 1:
+            z_h, s_h = runner.wait(tickets[i - 1])
+            got.append((z_h.clone(), s_h.clone()))
+    z_h, s_h = runner.wait(tickets[-1])
+    got.append((z_h.clone(), s_h.clone()))
+    for i, ((z_h, s_h), (z_ref, s_ref)) in enumerate(zip(got, refs)):
+        assert torch.equal(z_h, z_ref) and torch.equal(s_h, s_ref), f"step {i} ({shapes[i]})"
+    nt.nt_device_status()

@@ -109,6 +109,7 @@ class BlockGraph:
         self.in_stream = torch.cuda.Stream(device=self.dev)
         self.key = None
         self.sets: List[_Set] = []
+        self.retired = {}        # ticket -> slot of a step submitted before a shape change, until waited
         self.inputs: List[_Inputs] = []
         self.in_key = None
         self.submitted = 0
@@ -166,8 +167,15 @@ class BlockGraph:
             inp.used = False
 
     def _setup(self, part, dtype):
-        """Output buffers for a new (B, T, P); graphs are captured on each slot's first use."""
+        """Output buffers for a new (B, T, P); graphs are captured on each slot's first use.
+        The old slots of steps not yet waited on keep their host results
+        (their device work has drained) until ``wait`` collects them."""
         self._drain()
+        for st in self.sets:
+            if st.ticket >= 0 and st.ticket >= self.submitted - self.depth:
+                self.retired[st.ticket] = st
+        for t in [t for t in self.retired if t < self.submitted - self.depth]:
+            del self.retired[t]
         P, T = part.P, part.T
         self.cuts = slice_cuts(P, self.slices, self.growth)
         need = _nt.nt_pair_broadcast_workspace_bytes_rect(T, T, self.C_z)
@@ -262,9 +270,12 @@ class BlockGraph:
         ``depth`` submissions later reuses them: (z~ of P x C_z, s_out of
         T x C_s) with readback "pair", (the Eq. 5 loss as a 1-element fp32
         tensor, s_out) with readback "loss"."""
-        if not self.sets or self.sets[ticket % self.depth].ticket != ticket:
+        if self.sets and self.sets[ticket % self.depth].ticket == ticket:
+            st = self.sets[ticket % self.depth]
+        elif ticket in self.retired:
+            st = self.retired.pop(ticket)
+        else:
             raise ValueError(f"step {ticket} is no longer held (depth {self.depth})")
-        st = self.sets[ticket % self.depth]
         st.done.synchronize()
         return (st.z_host if self.readback == "pair" else st.loss_host), st.s_out_host
 
