@@ -180,8 +180,9 @@ def test_rectangular_partition_refused(nt):
 
 def test_block_backward_near_uniform_sampled(nt):
     """The near-uniform B=16 batch itself (P = 8.6 M cells, the size the bench
-    times): the loss and backward of the whole batch on the GPU, and the
-    single-row gradient ds of its shortest sample against the oracle, which
+    times): the loss and backward of the whole batch on the GPU, through the
+    one-call entry and through the two calls (the same loss and ds bits), and
+    the single-row gradient ds of its shortest sample against the oracle, which
     needs that sample alone (ds of a sample's rows depends on its own cells;
     Eq. 5's weights and totals are the batch's)."""
     cfg = wl.NEAR_UNIFORM_BF16
@@ -190,11 +191,15 @@ def test_block_backward_near_uniform_sampled(nt):
     part = nt.nt_partition_build(torch.as_tensor(inp.lengths).to(DEV))
     s = inp.s.to(DEV)
     z, m, s_out = nt.block_forward(part, s, w)
-    _, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z)
+    # the one-call entry the bench times, then the two calls it must equal
+    l1, g1 = nt.nt_pair_block_loss_backward(part, s, w, m, s_out, z)
+    l2, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z)
     del z
     g = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
     torch.cuda.synchronize()
     nt.nt_device_status()
+    assert torch.equal(l1, l2)
+    assert torch.equal(g1["ds"], g["ds"])
     lengths = np.asarray(inp.lengths, dtype=np.int64)
     k = int(np.argmin(lengths))
     n = int(lengths[k])
@@ -208,6 +213,6 @@ def test_block_backward_near_uniform_sampled(nt):
     dX_up = 2.0 * alpha[k] * res.X_tilde / (C * T)
     dP_up = 2.0 * beta[k] * res.P_tilde / (Cp * P)
     ref_ds, _ = obwd.block_backward_sample(X, ow, dX_up, dP_up)
-    got = to_np(g["ds"][r0:r0 + n])
+    got = to_np(g1["ds"][r0:r0 + n])
     e = normwise_err(got, ref_ds, dtype="bf16")
     assert e <= TOL["bf16"], f"ds of sample {k} (N = {n}): {e:.3e}"
