@@ -655,10 +655,54 @@ def measure_block(nt, cfg, dev, stream, flush, steps, warmup, peaks):
     nb = len(run.ws)
     out = {"B": cfg.B, "T": run.T, "P": run.P, "blocks": nb, "block_ms": block_ms,
            "cells_per_s": nb * run.P / (block_ms * 1e-3), "steps": steps,
-           "kernels": block_kernels(run, per, peaks)}
+           "kernels": block_kernels(run, per, peaks),
+           "graph": measure_block_graph(nt, run, stream, flush, steps)}
     del run
     torch.cuda.empty_cache()
     return out
+
+
+def measure_block_graph(nt, run, stream, flush, steps):
+    """The block's calls (every stacked block's broadcast, transition and
+    reduce) captured once in a CUDA graph over a partition built beforehand,
+    and timed per replay with L2 flushed before each: the device time of the
+    calls with no host launch gaps between them (the partition build, which
+    reads its totals back to the host, is outside)."""
+    part = nt.nt_partition_build(run.lengths_d, T=run.s_d.shape[0])
+
+    def calls():
+        s_cur = run.s_d
+        for w, so in zip(run.ws, run.souts):
+            nt.nt_pair_broadcast(part, s_cur, s_cur, w.W_a, w.W_b, z=run.z, workspace=run.wsp)
+            nt.nt_pair_transition(part, run.z, w.ln_gamma, w.ln_beta, w.W1, w.b1, w.W2, w.b2, out=run.z)
+            nt.nt_pair_reduce(part, run.z, w.W_g, w.b_g, s_in=s_cur, m=run.m, s_out=so)
+            s_cur = so
+
+    with torch.cuda.stream(stream):
+        calls()                                   # lazy set-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            calls()
+        for i in range(3):
+            flush.fill_(float(i))
+            g.replay()
+        times = []
+        for i in range(steps):
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+    nt.nt_device_status(stream)
+    t = [a.elapsed_time(b) for a, b in times]
+    ms = float(np.mean(t))
+    del g
+    return {"block_ms": ms, "ms_p10_p50_p90": [float(x) for x in np.percentile(t, [10, 50, 90])],
+            "cells_per_s": len(run.ws) * run.P / (ms * 1e-3),
+            "note": "broadcast, transition and reduce replayed as one CUDA graph; partition built beforehand"}
 
 
 def run_e2e(nt, binp, dev, stream, args):
