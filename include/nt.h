@@ -606,6 +606,24 @@ nt_status nt_varlen_attn_bwd(nt_dtype dtype, const void* q, const void* k, const
  * checks: NT_ERR_DEVICE_CHECK).  NT_OK if nothing was flagged. */
 nt_status nt_device_status(void* stream);
 
+/* Self-test of the device-side failure reporting; computes nothing.  One
+ * CTA waits, through the same bounded mbarrier wait the tensor-core kernels
+ * use, on a barrier of its own that
+ *   mode 0: another warp completes after about delay_ns: the wait succeeds;
+ *   mode 1: nothing completes: the wait runs out after limit_ns, raises the
+ *           CTA's abort flag and sets the status word's timeout bit, so the
+ *           next nt_device_status returns NT_ERR_TIMEOUT (and clears it);
+ *   mode 2: nothing completes, but another warp raises the CTA's abort flag
+ *           after delay_ns: the wait gives up early without flagging, as a
+ *           CTA's other roles do once one role's wait has run out.
+ * d_result: device int64[2], 8-byte aligned, caller-owned; written with
+ * [0] = 1 if the wait succeeded, 0 if it gave up, and [1] = the wait's
+ * duration in ns.  limit_ns in (0, 2e9], delay_ns at most 2e9, else
+ * NT_ERR_INVALID (checked before anything is enqueued).  Asynchronous on
+ * `stream`; the CUDA context stays usable in every mode. */
+nt_status nt_selftest_bounded_wait(int32_t mode, uint64_t delay_ns, uint64_t limit_ns, int64_t* d_result,
+                                   void* stream);
+
 /* Static string naming a status code. */
 const char* nt_status_str(nt_status s);
 

@@ -134,6 +134,14 @@ def test_host_side_rejections(L):
     # a negative max length
     assert bw(1, fake, fake, fake, fake, fake, fake, fake, fake, 1, 64, 64, 64, -1, 1, 64, 0.125, 0, fake, fake,
               fake, fake, 1 << 20, None) == 1
+    # the wait self-test: bad mode, a limit of 0 or above 2 s, a delay above 2 s, NULL or misaligned result
+    sw = lib.nt_selftest_bounded_wait
+    assert sw(3, 0, 10**6, fake, None) == 1
+    assert sw(1, 0, 0, fake, None) == 1
+    assert sw(1, 0, 2 * 10**9 + 1, fake, None) == 1
+    assert sw(0, 2 * 10**9 + 1, 10**6, fake, None) == 1
+    assert sw(1, 0, 10**6, None, None) == 1
+    assert sw(1, 0, 10**6, ctypes.c_void_p(0x1004), None) == 1
     # SwiGLU without its value projection
     assert lib.nt_pair_transition_swiglu(P, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None,
                                          fake, None, None) == 1

@@ -52,6 +52,8 @@ unsigned int* status_word() {
   return g_status_ptr[dev];
 }
 
+constexpr uint64_t kSelftestMaxNs = 2000000000ull;   // the longest wait or delay of the self-test
+
 bool width_ok(nt_dtype dt, int64_t w) { return w > 0 && w % (dt == NT_BF16 ? 8 : 4) == 0; }
 bool dtype_ok(nt_dtype dt) { return dt == NT_F32 || dt == NT_BF16; }
 size_t esize(nt_dtype dt) { return dt == NT_BF16 ? 2 : 4; }
@@ -833,6 +835,21 @@ nt_status nt_pair_block_loss_backward(const nt_partition* part, nt_dtype dtype, 
   return block_backward_run(part, dtype, s, C_s, W_a, W_b, C_z, H_t, ln_gamma, ln_beta, ln_eps, W1, b1, W2, W_g, m,
                             dx, tc ? nullptr : dz, tc ? z_tilde : nullptr, ds, dW_a, dW_b, dgamma, dbeta, dW1, db1,
                             dW2, db2, dW_g, db_g, w + L.bwd, st_);
+}
+
+nt_status nt_selftest_bounded_wait(int32_t mode, uint64_t delay_ns, uint64_t limit_ns, int64_t* d_result,
+                                   void* stream) {
+  if (mode < 0 || mode > 2) return fail(NT_ERR_INVALID, "mode %d (0, 1 or 2)", mode);
+  if (limit_ns == 0 || limit_ns > kSelftestMaxNs || delay_ns > kSelftestMaxNs)
+    return fail(NT_ERR_INVALID, "limit_ns must be in (0, 2 s] and delay_ns at most 2 s");
+  if (!d_result) return fail(NT_ERR_INVALID, "NULL pointer");
+  if ((reinterpret_cast<uintptr_t>(d_result) & 7u) != 0) return fail(NT_ERR_INVALID, "d_result must be 8-byte aligned");
+  unsigned int* status = status_word();
+  if (!status) return fail(NT_ERR_CUDA, "device status word not available");
+  const cudaError_t e = launch_selftest_wait(mode, delay_ns, limit_ns, d_result, status,
+                                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return NT_OK;
 }
 
 nt_status nt_device_status(void* stream) {

@@ -322,5 +322,7 @@ bool attn_simt_supported(int d);
 cudaError_t launch_attn_simt(nt_dtype dt, const AttnProblem& p, unsigned int* status, cudaStream_t s);
 bool attn_tc_supported(nt_dtype dt, int d);
 cudaError_t launch_attn_tc(const AttnProblem& p, unsigned int* status, cudaStream_t s);
+cudaError_t launch_selftest_wait(int mode, uint64_t delay_ns, uint64_t limit_ns, int64_t* result,
+                                 unsigned int* status, cudaStream_t s);
 
 }  // namespace nt

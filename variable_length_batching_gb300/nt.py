@@ -78,6 +78,7 @@ SIGNATURES = {
     "nt_varlen_attn_bwd": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _I32,
                                   _F, _I32, _P, _P, _P, _P, _SZ, _P]),
     "nt_device_status": (_I32, [_P]),
+    "nt_selftest_bounded_wait": (_I32, [_I32, ctypes.c_uint64, ctypes.c_uint64, _P, _P]),
     "nt_status_str": (ctypes.c_char_p, [_I32]),
     "nt_last_error": (ctypes.c_char_p, []),
 }
@@ -589,6 +590,20 @@ def nt_device_status(stream=None) -> int:
     st = lib().nt_device_status(_stream(stream))
     _check(st, "nt_device_status")
     return st
+
+
+def nt_selftest_bounded_wait(mode: int, delay_ns: int, limit_ns: int, result: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """The device-side wait self-test (mode 0: completed after ``delay_ns``;
+    1: runs out after ``limit_ns`` and flags a timeout; 2: given up on the
+    CTA's abort flag after ``delay_ns``).  Returns the int64[2] device tensor
+    (succeeded, duration in ns) it writes asynchronously; nt_device_status
+    then reports what was flagged."""
+    if result is None:
+        result = torch.full((2,), -1, dtype=torch.int64, device="cuda")
+    st = lib().nt_selftest_bounded_wait(int(mode), int(delay_ns), int(limit_ns), _ptr(result), _stream(stream))
+    _check(st, "nt_selftest_bounded_wait")
+    return result
 
 
 def nt_pair_block_fused(part: Partition, s_left: torch.Tensor, s_right: torch.Tensor, w, W3=None, b3=None,
