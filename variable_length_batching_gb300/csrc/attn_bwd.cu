@@ -9,8 +9,8 @@
 // l, l + 32, ...; dot products are warp butterflies): D per query row, then
 // dQ walking the row's visible keys, then dK and dV walking the queries that
 // see each key.  No atomics: every output row has exactly one owner.  For
-// bf16 with d = 64, the D pass is followed by the tensor-core kernels
-// instead (attn_bwd_tc.cu).
+// bf16 with d = 64, the tensor-core kernels run instead (attn_bwd_tc.cu),
+// their dQ kernel forming D itself.
 #include <type_traits>
 
 #include "nt_common.cuh"
@@ -191,15 +191,13 @@ template <typename T, int D>
 cudaError_t launch_d(const AttnBwdProblem& p, float* Dbuf, unsigned int* status, cudaStream_t s) {
   const int64_t wq = p.T_q * p.H, wk = p.T_k * p.H;
   const unsigned gq = (unsigned)((wq + kWarps - 1) / kWarps), gk = (unsigned)((wk + kWarps - 1) / kWarps);
+  // the tensor-core route forms D in its dQ kernel
+  if (attn_bwd_tc_supported(std::is_same<T, bf16>::value ? NT_BF16 : NT_F32, D) && p.T_q > 0 && p.T_k > 0 &&
+      p.B > 0)
+    return launch_attn_bwd_tc(p, Dbuf, status, s);
   if (wq > 0)
     rowdot_kernel<T, D><<<(unsigned)((p.T_q + 7) / 8), 256, 0, s>>>((const T*)p.o, (const T*)p.d_o, p.T_q, p.H,
                                                                     Dbuf);
-  if (attn_bwd_tc_supported(std::is_same<T, bf16>::value ? NT_BF16 : NT_F32, D) && p.T_q > 0 && p.T_k > 0 &&
-      p.B > 0) {
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_attn_bwd_tc(p, Dbuf, status, s);
-  }
   if (wq > 0) {
     dq_kernel<T, D><<<gq, kWarps * 32, 0, s>>>((const T*)p.q, (const T*)p.k, (const T*)p.v, (const T*)p.d_o, p.lse,
                                              Dbuf, p.cu_q, p.cu_k, p.B, p.T_q, p.T_k, p.H, p.scale, p.causal,

@@ -3,17 +3,19 @@
 // packing", "What it is" / "How it works"; the causal and cross forms as in
 // the forward).  Per segment and head, with P rebuilt from the forward's
 // natural-log LSE (no running max: P = exp(scale s - lse) <= 1),
-//     dP = dO V^T,  dS = P * (dP - D),  D = rowsum(dO * O)   (D precomputed)
+//     dP = dO V^T,  dS = P * (dP - D),  D = rowsum(dO * O)
 //     dQ = scale dS K,   dK = scale dS^T Q,   dV = P^T dO.
 // Two kernels, so that every output row has one owner and no atomics:
 //
-// dQ kernel: one CTA per (segment, 128-query tile, head), walking the key
-// tiles of 64 the tile's queries see.
+// dQ kernel (first): one CTA per (segment, 128-query tile, head), walking
+// the key tiles of 64 the tile's queries see.  Its compute threads form D
+// of their query rows from O and dO while the first S / dP are computed, use
+// it, and write it out for the dK/dV kernel.
 //   S  = Q K_j^T, dP = dO V_j^T          (M=128, N=64, K=64)  -> TMEM
 //   dS -> bf16, written by the compute threads over dP's columns
 //   dQ += dS K_j                          (A from TMEM, K_j MN-major)
 //
-// dK/dV kernel: one CTA per (segment, 128-key tile, head), walking the query
+// dK/dV kernel (second): one CTA per (segment, 128-key tile, head), walking the query
 // tiles of 64 that see the tile's keys.  In the transposed frame (keys on
 // the TMEM lanes) the per-query LSE and D are column constants, staged in
 // shared memory by the producer warp beside each query tile.
@@ -47,6 +49,11 @@ constexpr uint32_t kOffAux = kOffRing + kStages * 2 * kSmallBytes;
 constexpr uint32_t kAuxBytes = 2 * kBN * 4;    // per stage: -lse (log2 units) and -D of 64 queries
 constexpr uint32_t kOffBar = kOffAux + kStages * kAuxBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256;
+// The dQ kernels stage no LSE/D; their O tile (128 rows, for D) sits where
+// the dK/dV kernels keep those, and their barrier block follows it.
+constexpr uint32_t kOffOQ = kOffAux;
+constexpr uint32_t kOffBarQ = kOffOQ + kBigBytes;
+constexpr uint32_t kSmemBytesQ = kOffBarQ + 256;
 constexpr uint32_t kTmemCols = 256;
 // S (or S^T) at 0, dP (or dP^T) at 64, accumulators at 128 (dQ or dV) and 192 (dK)
 constexpr uint32_t kColS = 0, kColP = 64, kColAcc0 = 128, kColAcc1 = 192;
@@ -67,6 +74,31 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 // [32 g, 32 g + 16) of the base.
 __device__ __forceinline__ uint32_t a_chunk(uint32_t base, int kk) {
   return base + 32u * (uint32_t)(kk >> 1) + 8u * (uint32_t)(kk & 1);
+}
+
+// D = rowsum(dO * O) of row r of the O and dO tiles (128-byte rows of 64
+// bf16, 16-byte chunks XOR-swizzled by row as TMA's 128-byte swizzle leaves
+// them), in the summation order of the D pass of the CUDA-core route: per
+// 8-element chunk two fp32 sums over alternate elements, added, then the
+// eight chunk sums pairwise.  So D does not depend on which route formed it.
+__device__ __forceinline__ float row_dot64(const uint8_t* o_tile, const uint8_t* do_tile, int r) {
+  float s[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int off = r * 128 + ((c ^ (r & 7)) << 4);
+    const uint4 a = *reinterpret_cast<const uint4*>(o_tile + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(do_tile + off);
+    const bf16* ea = reinterpret_cast<const bf16*>(&a);
+    const bf16* eb = reinterpret_cast<const bf16*>(&b);
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      acc0 = fmaf(__bfloat162float(eb[e]), __bfloat162float(ea[e]), acc0);
+      acc1 = fmaf(__bfloat162float(eb[e + 1]), __bfloat162float(ea[e + 1]), acc1);
+    }
+    s[c] = acc0 + acc1;
+  }
+  return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
 // The four MMAs of one M=128, N=64, K=64 product with both operands
@@ -215,7 +247,8 @@ template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 2)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const float* __restrict__ lse, const float* __restrict__ Dbuf, const int32_t* __restrict__ cu_q,
+                   const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ lse,
+                   float* __restrict__ Dbuf, const int32_t* __restrict__ cu_q,
                    const int32_t* __restrict__ cu_k, int B, int64_t T_q, int64_t T_k, int H, int QT,
                    float scale, bf16* __restrict__ dq, unsigned int* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -251,7 +284,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = smem_raw;
-  Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBar);
+  Bars& bar = *reinterpret_cast<Bars*>(smem + kOffBarQ);
   volatile int* abort_flag = &bar.abort;
   if (threadIdx.x == 0) init_bars(bar);
   if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
@@ -264,9 +297,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q); prefetch_tmap(&tm_do); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&bar.big_full, 2 * kBigBytes);
+      prefetch_tmap(&tm_o);
+      mbar_arrive_expect_tx(&bar.big_full, 3 * kBigBytes);
       tma_load_3d(smem + kOffBig0, &tm_q, &bar.big_full, 0, h, q0);
       tma_load_3d(smem + kOffBig1, &tm_do, &bar.big_full, 0, h, q0);
+      tma_load_3d(smem + kOffOQ, &tm_o, &bar.big_full, 0, h, q0);
       int issued = 0;
       for (int j = 0; j < nk; ++j) {
         const int st = j % kStages;
@@ -319,18 +354,22 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int64_t t = (int64_t)q0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
     const float scale_log2 = scale * kLog2e;
-    // rows past the segment, and rows that saw no key: P = 0 (lse -> +inf)
+    // D of the row from the O and dO tiles (both threads of a row form it;
+    // the first writes it for the dK/dV kernel); rows past the segment, and
+    // rows that saw no key: P = 0 (lse -> +inf)
+    bool ok = mbar_wait_warp(&bar.big_full, 0, abort_flag, status);
     float L = INFINITY, Dr = 0.f;
-    if (t < hi) {
-      const float l = lse[(int64_t)h * T_q + t], dv = Dbuf[(int64_t)h * T_q + t];
+    if (ok && t < hi) {
+      const float dv = row_dot64(smem + kOffOQ, smem + kOffBig1, r);
+      if (g == 0) Dbuf[(int64_t)h * T_q + t] = dv;
+      const float l = lse[(int64_t)h * T_q + t];
       if (l != -INFINITY) {
         L = l * kLog2e;
         Dr = dv;
       }
     }
     const float nL = -L, nD = -Dr;
-    bool ok = true;
-    for (int j = 0; j < nk; ++j) {
+    for (int j = 0; j < nk && ok; ++j) {
       if (!(ok = mbar_wait_warp(&bar.s_full, j & 1, abort_flag, status))) break;
       tc_fence_after();
       __syncwarp();
@@ -566,6 +605,7 @@ struct PBars {
   uint64_t big_full, big_empty;
   uint64_t full[kStages], empty[kStages], aux_full[kStages];
   uint64_t s_full, p_full, p_empty, acc_free;
+  uint64_t o_empty;                           // dQ: the compute threads have read D's rows
   uint64_t it_full[kQueue], it_empty[kQueue];
   uint64_t mma_done;
   BItem item[kQueue];
@@ -586,6 +626,7 @@ __device__ __forceinline__ void init_pbars(PBars& bar) {
   mbar_init(&bar.p_full, 256);
   mbar_init(&bar.p_empty, 1);
   mbar_init(&bar.acc_free, 256);
+  mbar_init(&bar.o_empty, 256);
   for (int i = 0; i < kQueue; ++i) {
     mbar_init(&bar.it_full[i], 1);
     mbar_init(&bar.it_empty[i], 9);            // the MMA warp and eight compute warps
@@ -685,7 +726,10 @@ __device__ __forceinline__ BItem shfl_bitem(BItem it) {
 // per-lane writes and the four-lanes-per-row reads free of bank conflicts.
 // Rows r >= nrows (past the segment) are not written.
 constexpr uint32_t kStgWarpBytes = 32 * 64;
-constexpr uint32_t kSmemBytesP = kSmemBytes + 8 * kStgWarpBytes;   // the persistent kernels
+constexpr uint32_t kSmemBytesP = kSmemBytes + 8 * kStgWarpBytes;   // the persistent dK/dV kernel
+constexpr uint32_t kSmemBytesQP = kSmemBytesQ + 8 * kStgWarpBytes; // the persistent dQ kernel
+// two CTAs per SM, each with the 1 KB the hardware reserves per CTA
+static_assert(2 * (kSmemBytesQP + 1024) <= 228 * 1024, "two persistent dQ CTAs per SM");
 __device__ __forceinline__ void staged_store_half32(uint8_t* stg, int lane, const float* v, float mul, bf16* dst0,
                                                     int64_t pitch, int nrows) {
 #pragma unroll
@@ -930,7 +974,8 @@ template <bool kCausal>
 __global__ void __launch_bounds__(kThreads, 2)
 attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                       const float* __restrict__ lse, const float* __restrict__ Dbuf,
+                       const __grid_constant__ CUtensorMap tm_o, const float* __restrict__ lse,
+                       float* __restrict__ Dbuf,
                        const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k, int B, int64_t T_q,
                        int64_t T_k, int H, int QT, float scale, bf16* __restrict__ dq, unsigned int* next,
                        unsigned int* status) {
@@ -941,7 +986,7 @@ attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_co
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = smem_raw;
-  PBars& bar = *reinterpret_cast<PBars*>(smem + kOffBar);
+  PBars& bar = *reinterpret_cast<PBars*>(smem + kOffBarQ);
   volatile int* abort_flag = &bar.abort;
   if (threadIdx.x == 0) init_pbars(bar);
   if (warp == 1) tmem_alloc(&bar.tmem_base, kTmemCols);
@@ -955,17 +1000,21 @@ attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     // ------------------------------------------------------------ producer and scheduler (lane 0)
     if (lane == 0) {
       prefetch_tmap(&tm_q); prefetch_tmap(&tm_do); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_o);
       int gt = 0, qc = 0, issued = 0;
       BItem cur = fetch_bitem<false, kCausal>(next, total, cu_q, cu_k, T_q, T_k, H, QT, abort_flag, status);
       bool ok = publish_bitem(bar, 0, cur, abort_flag, status);
       for (int n = 0; ok && cur.b >= 0; ++n) {
         if (cur.n > 0) {
-          // Q and dO of this item once the previous item's last S / dP are computed
+          // Q, dO and O of this item once the previous item's last S / dP are
+          // computed and its D has been read
           if (!(ok = mbar_wait(&bar.big_empty, (qc & 1) ^ 1, abort_flag, status))) break;
+          if (!(ok = mbar_wait(&bar.o_empty, (qc & 1) ^ 1, abort_flag, status))) break;
           const int q0 = cur.lo + cur.t * kBM;
-          mbar_arrive_expect_tx(&bar.big_full, 2 * kBigBytes);
+          mbar_arrive_expect_tx(&bar.big_full, 3 * kBigBytes);
           tma_load_3d(smem + kOffBig0, &tm_q, &bar.big_full, 0, cur.h, q0);
           tma_load_3d(smem + kOffBig1, &tm_do, &bar.big_full, 0, cur.h, q0);
+          tma_load_3d(smem + kOffOQ, &tm_o, &bar.big_full, 0, cur.h, q0);
           ++qc;
         }
         BItem nxt;
@@ -1038,8 +1087,8 @@ attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const int r = qd * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
     const float scale_log2 = scale * kLog2e;
-    uint8_t* stg = smem + kSmemBytes + (warp - 2) * kStgWarpBytes;   // this warp's output buffer
-    int gt = 0;
+    uint8_t* stg = smem + kSmemBytesQ + (warp - 2) * kStgWarpBytes;  // this warp's output buffer
+    int gt = 0, qc = 0;
     bool ok = true;
     BItem it;
     for (int n = 0; ok && (ok = take_bitem(bar, n, abort_flag, status, it)); ++n) {
@@ -1054,15 +1103,22 @@ attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         zero_rows32(lane, dq + off0, pitch, nrows);
         continue;
       }
+      // D of the row from the item's O and dO tiles, as in the per-item
+      // kernel, then the tiles may be reloaded as far as D is concerned;
       // rows past the segment, and rows that saw no key: P = 0 (-lse -> -inf)
+      if (!(ok = mbar_wait_warp(&bar.big_full, qc & 1, abort_flag, status))) break;
+      ++qc;
       float nL = -INFINITY, nD = 0.f;
       if (t < it.hi) {
-        const float l = lse[(int64_t)it.h * T_q + t], dvv = Dbuf[(int64_t)it.h * T_q + t];
+        const float dvv = row_dot64(smem + kOffOQ, smem + kOffBig1, r);
+        if (g == 0) Dbuf[(int64_t)it.h * T_q + t] = dvv;
+        const float l = lse[(int64_t)it.h * T_q + t];
         if (l != -INFINITY) {
           nL = -l * kLog2e;
           nD = -dvv;
         }
       }
+      mbar_arrive(&bar.o_empty);
       for (int j = 0; j < it.n; ++j, ++gt) {
         if (!(ok = mbar_wait_warp(&bar.s_full, gt & 1, abort_flag, status))) break;
         tc_fence_after();
@@ -1104,10 +1160,11 @@ bool make_map_thd(CUtensorMap* map, const void* ptr, int64_t T, int H, uint32_t 
 
 bool attn_bwd_tc_supported(nt_dtype dt, int d) { return dt == NT_BF16 && d == kD; }
 
-cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsigned int* status, cudaStream_t s) {
+cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, float* Dbuf, unsigned int* status, cudaStream_t s) {
   if (p.T_q == 0 || p.T_k == 0 || p.B == 0) return cudaErrorInvalidValue;   // the caller routes these
-  CUtensorMap q128, do128, k64, v64, k128, v128, q64, do64;
+  CUtensorMap q128, do128, o128, k64, v64, k128, v128, q64, do64;
   if (!make_map_thd(&q128, p.q, p.T_q, p.H, kBM) || !make_map_thd(&do128, p.d_o, p.T_q, p.H, kBM) ||
+      !make_map_thd(&o128, p.o, p.T_q, p.H, kBM) ||
       !make_map_thd(&k64, p.k, p.T_k, p.H, kBN) || !make_map_thd(&v64, p.v, p.T_k, p.H, kBN) ||
       !make_map_thd(&k128, p.k, p.T_k, p.H, kBM) || !make_map_thd(&v128, p.v, p.T_k, p.H, kBM) ||
       !make_map_thd(&q64, p.q, p.T_q, p.H, kBN) || !make_map_thd(&do64, p.d_o, p.T_q, p.H, kBN))
@@ -1132,6 +1189,22 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsig
     e = cudaMemsetAsync(counters, 0, 2 * sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;
   }
+  // the dQ kernel forms D, which the dK/dV kernel reads
+  if (pq) {
+    auto kq = p.causal ? attn_bwd_dq_persistent<true> : attn_bwd_dq_persistent<false>;
+    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesQP);
+    if (e != cudaSuccess) return e;
+    kq<<<(unsigned)min64(items_q, slots), kThreads, kSmemBytesQP, s>>>(q128, do128, k64, v64, o128, p.lse, Dbuf,
+                                                                       p.cu_q, p.cu_k, p.B, p.T_q, p.T_k, p.H, QT,
+                                                                       p.scale, (bf16*)p.dq, counters + 1, status);
+  } else {
+    auto kq = p.causal ? attn_bwd_dq_kernel<true> : attn_bwd_dq_kernel<false>;
+    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesQ);
+    if (e != cudaSuccess) return e;
+    kq<<<(unsigned)items_q, kThreads, kSmemBytesQ, s>>>(q128, do128, k64, v64, o128, p.lse, Dbuf, p.cu_q, p.cu_k,
+                                                        p.B, p.T_q, p.T_k, p.H, QT, p.scale, (bf16*)p.dq, status);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (pkv) {
     auto kkv = p.causal ? attn_bwd_dkv_persistent<true> : attn_bwd_dkv_persistent<false>;
     e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesP);
@@ -1146,21 +1219,6 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsig
     kkv<<<(unsigned)items_k, kThreads, kSmemBytes, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
                                                          p.T_q, p.T_k, p.H, KT, p.scale, (bf16*)p.dk, (bf16*)p.dv,
                                                          status);
-  }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (pq) {
-    auto kq = p.causal ? attn_bwd_dq_persistent<true> : attn_bwd_dq_persistent<false>;
-    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesP);
-    if (e != cudaSuccess) return e;
-    kq<<<(unsigned)min64(items_q, slots), kThreads, kSmemBytesP, s>>>(q128, do128, k64, v64, p.lse, Dbuf, p.cu_q,
-                                                                      p.cu_k, p.B, p.T_q, p.T_k, p.H, QT, p.scale,
-                                                                      (bf16*)p.dq, counters + 1, status);
-  } else {
-    auto kq = p.causal ? attn_bwd_dq_kernel<true> : attn_bwd_dq_kernel<false>;
-    e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    kq<<<(unsigned)items_q, kThreads, kSmemBytes, s>>>(q128, do128, k64, v64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
-                                                       p.T_q, p.T_k, p.H, QT, p.scale, (bf16*)p.dq, status);
   }
   return cudaGetLastError();
 }

@@ -244,7 +244,7 @@ cudaError_t launch_attn_bwd(nt_dtype dt, const AttnBwdProblem& p, float* Dbuf, u
 // The tensor-core kernels (dK/dV, then dQ) after Dbuf holds rowsum(dO * O);
 // T_q, T_k and B must be > 0.
 bool attn_bwd_tc_supported(nt_dtype dt, int d);
-cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, const float* Dbuf, unsigned int* status, cudaStream_t s);
+cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, float* Dbuf, unsigned int* status, cudaStream_t s);
 
 // The Eq. 5 loss ("DanLing NestedTensor" Appendix A.1) on the block's outputs
 // and, optionally, its gradients dX~ [T, C_s] and dP~ [P, C_z] (fp32).
