@@ -575,7 +575,7 @@ def measure_attn_backward(nt, dev, stream, flush, steps, peaks, ainp, q, k, v, c
     flops = 2.5 * aw["flops"]        # S recomputed, dV, dP, dQ, dK: 2.5 times the forward's flops
     return {"workload": ATTN_CFG.name, "ms": ms, "bound": "tensor", "achieved": flops / ms / 1e9,
             "unit": "TFLOP/s", "peak": peaks["bf16_tflops"], "frac": flops / ms / 1e9 / peaks["bf16_tflops"],
-            "flops": flops, "steps": steps, "call": "D pass + dK/dV kernel + dQ kernel"}
+            "flops": flops, "steps": steps, "call": "dQ kernel (forms D) + dK/dV kernel"}
 
 
 def backward_route(cfg):
