@@ -25,6 +25,10 @@
  *     biases fp32, all accumulation fp32.  NT_F32 -- every operand fp32.
  *   - Alignment: every pointer 16-byte aligned; feature widths multiples of
  *     8 (bf16) or 4 (fp32).  Otherwise NT_ERR_INVALID / NT_ERR_UNSUPPORTED.
+ *   - Empty batches: an array with no elements (the singles, m or s_out of a
+ *     batch with T = 0, the pair state of one with P = 0, a workspace of 0
+ *     bytes) may be passed as NULL; weights and parameters may not.  Such a
+ *     call writes what it has (e.g. zero parameter gradients, a loss of 0).
  *   - Asynchrony: calls enqueue work on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and return.  nt_partition_build (and its
  *     _rect and _with_rows forms) is the one call that synchronises the

@@ -216,3 +216,33 @@ def test_block_backward_near_uniform_sampled(nt):
     got = to_np(g1["ds"][r0:r0 + n])
     e = normwise_err(got, ref_ds, dtype="bf16")
     assert e <= TOL["bf16"], f"ds of sample {k} (N = {n}): {e:.3e}"
+
+
+@pytest.mark.parametrize("cfg", [wl.TINY_FP32, wl.PAIRFORMER_BF16])
+def test_empty_batch(nt, cfg):
+    """Samples that all have length 0 (T = P = 0): the forward calls, the
+    fused block, the loss and the backward through both entries accept the
+    empty tensors; Eq. 5's empty sums give a loss of 0 (the oracle's
+    reading), every parameter gradient is 0 and ds is empty."""
+    inp = wl.make_block_inputs(cfg, lengths=[0, 0], biases=True)
+    w = _dw(inp.blocks[0])
+    part = nt.nt_partition_build(torch.as_tensor(np.asarray(inp.lengths, dtype=np.int32)).to(DEV))
+    assert (part.T, part.P) == (0, 0)
+    s = inp.s.to(DEV)
+    assert s.shape[0] == 0
+    z, m, s_out = nt.block_forward(part, s, w)
+    assert z.shape == (0, cfg.C_z) and m.shape == (0, cfg.C_z) and s_out.shape == (0, cfg.C_s)
+    zf, mf, sf = nt.nt_pair_block_fused(part, s, s, w)
+    assert zf.shape == (0, cfg.C_z) and sf.shape == (0, cfg.C_s)
+    loss, ds_out, dz = nt.nt_pair_block_loss(part, s_out, z)
+    g = nt.nt_pair_block_backward(part, s, w, m, ds_out, dz)
+    l1, g1 = nt.nt_pair_block_loss_backward(part, s, w, m, s_out, z)
+    torch.cuda.synchronize()
+    assert nt.nt_device_status() == 0
+    ref_loss = obwd.eq5_loss(inp.lengths, np.zeros((0, cfg.C_s)), np.zeros((0, cfg.C_z)))
+    assert ref_loss == 0.0
+    assert float(loss.item()) == 0.0 and float(l1.item()) == 0.0
+    for grads in (g, g1):
+        assert grads["ds"].shape == (0, cfg.C_s)
+        for n in NAMES[1:]:
+            assert torch.count_nonzero(grads[n]).item() == 0, n

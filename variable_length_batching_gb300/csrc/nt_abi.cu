@@ -471,13 +471,15 @@ nt_status nt_pair_broadcast(const nt_partition* part, nt_dtype dtype, const void
   if (!width_ok(dtype, C_s) || !width_ok(dtype, C_z))
     return fail(NT_ERR_UNSUPPORTED, "C_s=%d, C_z=%d must be positive multiples of %d", C_s, C_z,
                 dtype == NT_BF16 ? 8 : 4);
-  if (!s_left || !s_right || !W_a || !W_b || !z || !workspace)
+  const int64_t T_cols = t_cols_of(part);
+  const size_t need = nt_pair_broadcast_workspace_bytes_rect(part->T, T_cols, C_z);
+  // an array of no elements may be NULL (an empty batch)
+  if (!W_a || !W_b || (part->T > 0 && !s_left) || (T_cols > 0 && !s_right) || (part->P > 0 && !z) ||
+      (need > 0 && !workspace))
     return fail(NT_ERR_INVALID, "NULL pointer");
   if (!aligned16(s_left) || !aligned16(s_right) || !aligned16(W_a) || !aligned16(W_b) ||
       !aligned16(z) || !aligned16(workspace))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
-  const int64_t T_cols = t_cols_of(part);
-  const size_t need = nt_pair_broadcast_workspace_bytes_rect(part->T, T_cols, C_z);
   if (workspace_bytes < need)
     return fail(NT_ERR_INVALID, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
   if (part->T == 0) return NT_OK;
@@ -524,8 +526,8 @@ nt_status nt_pair_reduce(const nt_partition* part, nt_dtype dtype, const void* z
   if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
   if (!width_ok(dtype, C_z)) return fail(NT_ERR_UNSUPPORTED, "C_z=%d", C_z);
   if (dtype == NT_BF16 && C_z > 1024) return fail(NT_ERR_UNSUPPORTED, "bf16 C_z=%d > 1024", C_z);
-  if (!z || !m) return fail(NT_ERR_INVALID, "NULL pointer");
-  if (W_g && (!s_out || !width_ok(dtype, C_s)))
+  if ((part->P > 0 && !z) || (part->T > 0 && !m)) return fail(NT_ERR_INVALID, "NULL pointer");
+  if (W_g && ((part->T > 0 && !s_out) || !width_ok(dtype, C_s)))
     return fail(NT_ERR_INVALID, "W_g given: s_out must be set and C_s=%d valid", C_s);
   if (!aligned16(z) || !aligned16(m) || !aligned16(W_g) || !aligned16(b_g) || !aligned16(s_in) ||
       !aligned16(s_out))
@@ -601,9 +603,13 @@ nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const vo
   if (!width_ok(dtype, C_s) || !width_ok(dtype, C_z) || !width_ok(dtype, H_t))
     return fail(NT_ERR_UNSUPPORTED, "C_s=%d, C_z=%d, H_t=%d must be positive multiples of %d", C_s, C_z, H_t,
                 dtype == NT_BF16 ? 8 : 4);
-  if (!s_left || !s_right || !W_a || !W_b || !ln_gamma || !ln_beta || !W1 || !W2 || !z_out || !m || !workspace)
+  // an array of no elements may be NULL (an empty batch)
+  const int64_t T_cols_f = t_cols_of(part);
+  if (!W_a || !W_b || !ln_gamma || !ln_beta || !W1 || !W2 || (part->T > 0 && (!s_left || !m)) ||
+      (T_cols_f > 0 && !s_right) || (part->P > 0 && !z_out) ||
+      (nt_pair_block_fused_workspace_bytes(part->T, T_cols_f, C_z) > 0 && !workspace))
     return fail(NT_ERR_INVALID, "NULL pointer");
-  if (W_g && !s_out) return fail(NT_ERR_INVALID, "W_g given: s_out must be set");
+  if (W_g && part->T > 0 && !s_out) return fail(NT_ERR_INVALID, "W_g given: s_out must be set");
   if (!aligned16(s_left) || !aligned16(s_right) || !aligned16(W_a) || !aligned16(W_b) || !aligned16(W1) ||
       !aligned16(W2) || !aligned16(W3) || !aligned16(z_out) || !aligned16(m) || !aligned16(workspace) ||
       !aligned16(W_g) || !aligned16(s_out) || !aligned16(ln_gamma) || !aligned16(ln_beta) || !aligned16(b1) ||
