@@ -248,7 +248,9 @@ nt_status nt_pair_broadcast_noalloc(const nt_partition* part, nt_dtype dtype, co
  *   W2 [C_z, H_t].  b2 [C_z] fp32 or NULL.
  * bf16 with C_z = 128 and H_t a multiple of 128 runs on the tcgen05 tensor
  * cores (hidden activations rounded to bf16 before the second GEMM); other
- * shapes and NT_F32 run on fp32 CUDA cores.  Asynchronous.
+ * shapes and NT_F32 run on fp32 CUDA cores.  Asynchronous.  At most
+ * 2^31 - 1025 cells per call (cell rows are 32-bit copy coordinates), else
+ * NT_ERR_OVERFLOW; the same bound holds for nt_pair_block_fused.
  */
 nt_status nt_pair_transition(const nt_partition* part, nt_dtype dtype, const void* z_in,
                              void* z_out, int32_t C_z, int32_t H_t, const float* ln_gamma,

@@ -134,6 +134,9 @@ def test_host_side_rejections(L):
     # a negative max length
     assert bw(1, fake, fake, fake, fake, fake, fake, fake, fake, 1, 64, 64, 64, -1, 1, 64, 0.125, 0, fake, fake,
               fake, fake, 1 << 20, None) == 1
+    # more cells than 32-bit copy coordinates reach
+    assert lib.nt_pair_transition_cells(2**31, 1, fake, fake, 128, 512, fake, fake, 1e-5, fake, None, None, None,
+                                        fake, None, None) == 3
     # the wait self-test: bad mode, a limit of 0 or above 2 s, a delay above 2 s, NULL or misaligned result
     sw = lib.nt_selftest_bounded_wait
     assert sw(3, 0, 10**6, fake, None) == 1

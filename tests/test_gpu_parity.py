@@ -273,6 +273,49 @@ def test_block_full_size_sampled(nt, cfg):
     nt.nt_device_status()
 
 
+def test_block_one_long_sample(nt):
+    """One 20,000-token sample beside three short ones (P = 400,000,010
+    cells, a 102 GB bf16 pair state): element offsets far past 2^31, a pair
+    row of 20,000 cells in the reduce, cell rows near the top of the 32-bit
+    copy coordinates' range still far off.  Sampled cells (among them the
+    first cells whose element offset passes 2^31 and 2^32) and rows against
+    the oracle; the fused block's sampled cells bit for bit against the
+    three calls', its m and s_out against the oracle."""
+    lengths = [20000, 1, 0, 3]
+    cfg = wl.PAIRFORMER_BF16
+    torch.cuda.empty_cache()
+    inp = wl.make_block_inputs(cfg, lengths=lengths, biases=True)
+    part = nt.nt_partition_build(dev_lengths(inp.lengths))
+    ref_part = opart.partition(inp.lengths)
+    assert part.P == ref_part.P == 400_000_010
+    w, ow = dev_weights(inp.blocks[0]), oracle_weights(inp.blocks[0])
+    s = inp.s.to(DEV)
+    z, m, s_out = nt.block_forward(part, s, w)
+    rng = np.random.default_rng(2)
+    edge = [(1 << 31) // cfg.C_z - 1, (1 << 31) // cfg.C_z, (1 << 32) // cfg.C_z]
+    cells = np.concatenate([rng.integers(0, ref_part.P, size=500), ref_part.pair_off[1:-1] - 1,
+                            ref_part.pair_off[:-1], [ref_part.P - 1], edge]).astype(np.int64)
+    idx = torch.as_tensor(cells, device=DEV)
+    got = z[idx].clone()
+    _, Pt = oblock.block_cells(inp.lengths, f64(inp.s), ow, cells)
+    assert normwise_err(to_np(got), Pt, dtype="bf16") <= TOL["bf16"]
+    rows = np.array([0, 12345, 19999, 20000, 20001, 20003], dtype=np.int64)
+    m_ref, s_ref = oblock.block_rows(inp.lengths, f64(inp.s), ow, rows)
+    ridx = torch.as_tensor(rows, device=DEV)
+    assert normwise_err(to_np(m[ridx]), m_ref, dtype="bf16") <= TOL["bf16"]
+    assert normwise_err(to_np(s_out[ridx]), s_ref, dtype="bf16") <= TOL["bf16"]
+    nt.nt_device_status()
+    del z
+    torch.cuda.empty_cache()
+    zf, mf, sf = nt.nt_pair_block_fused(part, s, s, w)
+    assert torch.equal(zf[idx], got)
+    assert normwise_err(to_np(mf[ridx]), m_ref, dtype="bf16") <= TOL["bf16"]
+    assert normwise_err(to_np(sf[ridx]), s_ref, dtype="bf16") <= TOL["bf16"]
+    nt.nt_device_status()
+    del zf
+    torch.cuda.empty_cache()
+
+
 def test_stacked_blocks_chain(nt):
     """Four blocks chained through the singles (the stacked workload's
     weights and width, lengths cut by 16): the library's chain against the

@@ -53,6 +53,7 @@ unsigned int* status_word() {
 }
 
 constexpr uint64_t kSelftestMaxNs = 2000000000ull;   // the longest wait or delay of the self-test
+constexpr int64_t kMaxCells = 0x7fffffffLL - 1024;     // pair cells a transition or fused call takes
 
 bool width_ok(nt_dtype dt, int64_t w) { return w > 0 && w % (dt == NT_BF16 ? 8 : 4) == 0; }
 bool dtype_ok(nt_dtype dt) { return dt == NT_F32 || dt == NT_BF16; }
@@ -120,6 +121,9 @@ nt_status transition_cells(int64_t P, nt_dtype dtype, const void* z_in, void* z_
   if (P < 0) return fail(NT_ERR_INVALID, "cell count %lld < 0", (long long)P);
   if (!dtype_ok(dtype)) return fail(NT_ERR_INVALID, "bad dtype %d", (int)dtype);
   if (P == 0) return NT_OK;                  // nothing to map (the pointers of empty tensors may be NULL)
+  // cell rows are 32-bit TMA coordinates (2^31 bf16 cells of 128 features
+  // would be 550 GB, beyond the device anyway)
+  if (P > kMaxCells) return fail(NT_ERR_OVERFLOW, "%lld cells: at most %lld", (long long)P, (long long)kMaxCells);
   if (!width_ok(dtype, C_z) || !width_ok(dtype, H_t))
     return fail(NT_ERR_UNSUPPORTED, "C_z=%d, H_t=%d must be positive multiples of %d", C_z, H_t,
                 dtype == NT_BF16 ? 8 : 4);
@@ -616,6 +620,8 @@ nt_status nt_pair_block_fused(const nt_partition* part, nt_dtype dtype, const vo
       !aligned16(b2) || !aligned16(b3) || !aligned16(b_g))
     return fail(NT_ERR_INVALID, "pointers must be 16-byte aligned");
   if (!(ln_eps >= 0.0f)) return fail(NT_ERR_INVALID, "ln_eps must be >= 0");
+  if (part->P > kMaxCells)
+    return fail(NT_ERR_OVERFLOW, "%lld cells: at most %lld", (long long)part->P, (long long)kMaxCells);
   const int64_t T_cols = t_cols_of(part);
   const size_t need = nt_pair_block_fused_workspace_bytes(part->T, T_cols, C_z);
   if (workspace_bytes < need)
