@@ -882,8 +882,8 @@ __device__ __forceinline__ int64_t sum_part_base(const int64_t* pair_off, const 
 // (an exchange that leaves each lane 4 of the row's 128 features), then
 // over the 16 warps in warp order through shared memory.  Fixed orders
 // throughout, so du and dv are reproducible.  dgamma += dY xhat and dbeta
-// += dY are reduced over the CTA in shared memory, then added with one
-// atomic per feature.  A copy wait that runs out flags the status word and
+// += dY are reduced over the CTA the same way (the warp's two columns, then
+// the warps in order), then added with one atomic per feature.  A copy wait that runs out flags the status word and
 // ends the CTA once the copies it issued have landed (bounded as well).
 constexpr int kSumThreads = 512;
 constexpr int kSumWarps = kSumThreads / 32;
@@ -894,6 +894,7 @@ constexpr int kSumStatBytes = 512;                             // the row's cell
 constexpr int kSumRowBytes = 2 * kSumHalf + 2 * kTcC * 4 + kSumStatBytes;   // dY, upstream, u[row], dM[row], stats
 constexpr size_t kSumSmem = (size_t)kSumBufs * kSumRows * kSumRowBytes + (size_t)kSumRows * kSumWarps * kTcC * 4 +
                             kSumBufs * sizeof(uint64_t);
+static_assert(kSumRows * kSumWarps * kTcC >= kSumWarps * 2 * kTcC, "the row-sum buffer holds the dgamma/dbeta tail");
 
 __global__ void __launch_bounds__(kSumThreads, 1)
 bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
@@ -906,7 +907,6 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
   uint8_t* bufs = sum_smem;                                                        // [buf][row][dY | up]
   float4* rp = reinterpret_cast<float4*>(sum_smem + (size_t)kSumBufs * kSumRows * kSumRowBytes);  // [row][warp][32]
   uint64_t* full = reinterpret_cast<uint64_t*>(rp + kSumRows * kSumWarps * (kTcC / 4));
-  __shared__ float red[2][kTcC];
   __shared__ float gs[kTcC];
   __shared__ int abort_flag;
   const int64_t g = blockIdx.x;
@@ -1103,18 +1103,30 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
     *reinterpret_cast<float4*>(o + 4 * q) = make_float4(cs[0], cs[1], cs[2], cs[3]);
     *reinterpret_cast<float4*>(o + 64 + 4 * q) = make_float4(cs[4], cs[5], cs[6], cs[7]);
   }
-  if (threadIdx.x < 2 * kTcC) red[threadIdx.x / kTcC][threadIdx.x % kTcC] = 0.f;
-  __syncthreads();
+  // dgamma and dbeta over the item: the warp's two columns first (lane bit
+  // 4), then the 16 warps in warp order through the row-sum buffer (free
+  // since the last group's barrier), then one atomic per feature
+  float* red = reinterpret_cast<float*>(rp);          // [warp][dgamma | dbeta][C]
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int f = 64 * (i >> 2) + 4 * q + (i & 3);
-    atomicAdd(&red[0][f], pg[i]);
-    atomicAdd(&red[1][f], pbt[i]);
+    pg[i] += __shfl_xor_sync(0xffffffffu, pg[i], 16);
+    pbt[i] += __shfl_xor_sync(0xffffffffu, pbt[i], 16);
+  }
+  if (!hi4) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int f = 64 * (i >> 2) + 4 * q + (i & 3);
+      red[(warp * 2) * kTcC + f] = pg[i];
+      red[(warp * 2 + 1) * kTcC + f] = pbt[i];
+    }
   }
   __syncthreads();
-  if (threadIdx.x < kTcC) {
-    atomicAdd(dgamma + threadIdx.x, red[0][threadIdx.x]);
-    atomicAdd(dbeta + threadIdx.x, red[1][threadIdx.x]);
+  if (threadIdx.x < 2 * kTcC) {
+    const int which = threadIdx.x / kTcC, f = threadIdx.x % kTcC;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSumWarps; ++w) acc += red[(w * 2 + which) * kTcC + f];
+    atomicAdd((which ? dbeta : dgamma) + f, acc);
   }
 }
 
