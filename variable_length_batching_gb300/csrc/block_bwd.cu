@@ -101,58 +101,86 @@ __device__ __forceinline__ float eq5_pair_scale(int b, int B, int Cp, int64_t P)
   return (float)(2.0 * beta / ((double)Cp * P));
 }
 
-// One CTA per group of pair rows: sum over its rows of alpha_b ||X~ row||^2
-// and of beta_b ||P~ row's cells||^2, in double, into partial[blockIdx];
-// optionally writes dX~ = 2 alpha_b X~ / (C T) and dP~ = 2 beta_b P~ / (C_p P).
-template <typename T>
+// Sum of alpha_b ||X~ row||^2 and of beta_b ||P~ row's cells||^2 over the
+// CTA's rows, in double, into partial[blockIdx]; optionally writes
+// dX~ = 2 alpha_b X~ / (C T) and dP~ = 2 beta_b P~ / (C_p P).  With the
+// cells (zt given) the CTA takes one pair row at a time: X~ row and cells.
+// Without them (the pair term then comes from the reduce, eq5_finish's extra
+// partials) one warp takes one single row: lane 0 forms the row's weight in
+// double, the row's squares are summed in fp32 by a fixed butterfly and
+// added once, weighted, so no row waits on a CTA barrier behind one thread's
+// fp64 divisions (which are slow here).
+constexpr int kLossWarps = kThreads / 32;
+template <typename T, bool kCells>
 __global__ void __launch_bounds__(kThreads)
 eq5_partial_kernel(const T* __restrict__ s_out, const T* __restrict__ zt, const int64_t* __restrict__ row_start,
                    const int32_t* __restrict__ row_sample, int B, int64_t Trows, int64_t P, int C, int Cp,
                    double* __restrict__ partial, float* __restrict__ ds_out, float* __restrict__ dz) {
-  __shared__ double red[2][kThreads / 32];
+  __shared__ double red[2][kLossWarps];
   __shared__ double s_ab[2];
   __shared__ float s_g[2];
   double ax = 0.0, ap = 0.0;
-  for (int64_t r = blockIdx.x; r < Trows; r += gridDim.x) {
-    // the row's weights and gradient scales, formed in double once per row
-    // (fp64 divisions are slow here; every thread used to form its own)
-    if (threadIdx.x == 0) {
-      const int b = row_sample[r];
-      const double alpha = 1.0 + (double)b / B, beta = 1.5 - (double)b / (2.0 * B);
-      s_ab[0] = alpha;
-      s_ab[1] = beta;
-      s_g[0] = (float)(2.0 * alpha / ((double)C * Trows));
-      s_g[1] = eq5_pair_scale(b, B, Cp, P);
-    }
-    __syncthreads();
-    const double alpha = s_ab[0], beta = s_ab[1];
-    const float gx = s_g[0], gp = s_g[1];
-    __syncthreads();                          // read before thread 0 writes the next row's
-    float sx = 0.f;
-    for (int k = threadIdx.x; k < C; k += kThreads) {
-      const float x = to_f32(s_out[r * C + k]);
-      sx += x * x;
-      if (ds_out) ds_out[r * C + k] = gx * x;
-    }
-    ax += alpha * sx;
-    // the row's cells: 16-byte loads (Cp is a multiple of 16 bytes' worth of
-    // elements, so every row starts on a 16-byte boundary); none without zt
-    // (the pair term then comes from the reduce, eq5_finish's extra partials)
-    constexpr int V = 16 / sizeof(T);
-    const int64_t c0 = row_start[r] * Cp, c1 = zt ? row_start[r + 1] * Cp : c0;
-    float sp = 0.f;
-    for (int64_t e = c0 + (int64_t)threadIdx.x * V; e < c1; e += (int64_t)kThreads * V) {
-      float x[V];
-      load_vec(zt + e, x);
-#pragma unroll
-      for (int i = 0; i < V; ++i) sp = fmaf(x[i], x[i], sp);
-      if (dz) {
-#pragma unroll
-        for (int i = 0; i < V; i += 4)
-          *reinterpret_cast<float4*>(dz + e + i) = make_float4(gp * x[i], gp * x[i + 1], gp * x[i + 2], gp * x[i + 3]);
+  if constexpr (!kCells) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t r = (int64_t)blockIdx.x * kLossWarps + warp; r < Trows; r += (int64_t)gridDim.x * kLossWarps) {
+      double alpha = 0.0;
+      float gx = 0.f;
+      if (lane == 0) {
+        alpha = 1.0 + (double)row_sample[r] / B;
+        gx = (float)(2.0 * alpha / ((double)C * Trows));
       }
+      gx = __shfl_sync(0xffffffffu, gx, 0);
+      float sx = 0.f;
+      for (int k = lane; k < C; k += 32) {
+        const float x = to_f32(s_out[r * C + k]);
+        sx = fmaf(x, x, sx);
+        if (ds_out) ds_out[r * C + k] = gx * x;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+      if (lane == 0) ax += alpha * (double)sx;
     }
-    ap += beta * sp;
+  } else {
+    for (int64_t r = blockIdx.x; r < Trows; r += gridDim.x) {
+      // the row's weights and gradient scales, formed in double once per row
+      if (threadIdx.x == 0) {
+        const int b = row_sample[r];
+        const double alpha = 1.0 + (double)b / B, beta = 1.5 - (double)b / (2.0 * B);
+        s_ab[0] = alpha;
+        s_ab[1] = beta;
+        s_g[0] = (float)(2.0 * alpha / ((double)C * Trows));
+        s_g[1] = eq5_pair_scale(b, B, Cp, P);
+      }
+      __syncthreads();
+      const double alpha = s_ab[0], beta = s_ab[1];
+      const float gx = s_g[0], gp = s_g[1];
+      __syncthreads();                          // read before thread 0 writes the next row's
+      float sx = 0.f;
+      for (int k = threadIdx.x; k < C; k += kThreads) {
+        const float x = to_f32(s_out[r * C + k]);
+        sx += x * x;
+        if (ds_out) ds_out[r * C + k] = gx * x;
+      }
+      ax += alpha * sx;
+      // the row's cells: 16-byte loads (Cp is a multiple of 16 bytes' worth
+      // of elements, so every row starts on a 16-byte boundary)
+      constexpr int V = 16 / sizeof(T);
+      const int64_t c0 = row_start[r] * Cp, c1 = row_start[r + 1] * Cp;
+      float sp = 0.f;
+      for (int64_t e = c0 + (int64_t)threadIdx.x * V; e < c1; e += (int64_t)kThreads * V) {
+        float x[V];
+        load_vec(zt + e, x);
+#pragma unroll
+        for (int i = 0; i < V; ++i) sp = fmaf(x[i], x[i], sp);
+        if (dz) {
+#pragma unroll
+          for (int i = 0; i < V; i += 4)
+            *reinterpret_cast<float4*>(dz + e + i) =
+                make_float4(gp * x[i], gp * x[i + 1], gp * x[i + 2], gp * x[i + 3]);
+        }
+      }
+      ap += beta * sp;
+    }
   }
   for (int o = 16; o > 0; o >>= 1) {
     ax += __shfl_xor_sync(0xffffffffu, ax, o);
@@ -637,8 +665,8 @@ trans_bwd_weights_kernel(CellArgs<T> a, int splits, float* __restrict__ dW1, flo
 template <typename T>
 cudaError_t eq5_loss_t(const nt_partition* p, const void* s_out, int C_s, const void* zt, int C_z, float* loss,
                        float* ds_out, float* dz, double* partial, int nblocks, cudaStream_t s) {
-  eq5_partial_kernel<T><<<nblocks, kThreads, 0, s>>>((const T*)s_out, (const T*)zt, p->row_start, p->row_sample,
-                                                     p->B, p->T, p->P, C_s, C_z, partial, ds_out, dz);
+  (zt ? eq5_partial_kernel<T, true> : eq5_partial_kernel<T, false>)<<<nblocks, kThreads, 0, s>>>(
+      (const T*)s_out, (const T*)zt, p->row_start, p->row_sample, p->B, p->T, p->P, C_s, C_z, partial, ds_out, dz);
   eq5_finish_kernel<<<1, kLossBlocks, 0, s>>>(partial, nblocks, p->T, p->P, C_s, C_z, loss);
   return cudaGetLastError();
 }
@@ -1279,12 +1307,13 @@ cudaError_t launch_eq5_loss_rows(nt_dtype dt, const nt_partition* p, const void*
   const int nblocks = (int)max64(1, min64(p->T, kLossBlocks));
   double* partial = static_cast<double*>(workspace);
   if (dt == NT_BF16)
-    eq5_partial_kernel<bf16><<<nblocks, kThreads, 0, s>>>((const bf16*)s_out, nullptr, p->row_start, p->row_sample,
-                                                         p->B, p->T, p->P, C_s, C_z, partial, nullptr, nullptr);
+    eq5_partial_kernel<bf16, false><<<nblocks, kThreads, 0, s>>>(
+        (const bf16*)s_out, nullptr, p->row_start, p->row_sample, p->B, p->T, p->P, C_s, C_z, partial, nullptr,
+        nullptr);
   else
-    eq5_partial_kernel<float><<<nblocks, kThreads, 0, s>>>((const float*)s_out, nullptr, p->row_start,
-                                                          p->row_sample, p->B, p->T, p->P, C_s, C_z, partial,
-                                                          nullptr, nullptr);
+    eq5_partial_kernel<float, false><<<nblocks, kThreads, 0, s>>>(
+        (const float*)s_out, nullptr, p->row_start, p->row_sample, p->B, p->T, p->P, C_s, C_z, partial, nullptr,
+        nullptr);
   eq5_finish_kernel<<<1, kLossBlocks, 0, s>>>(partial, nblocks, p->T, p->P, C_s, C_z, loss, pair_sq, npair);
   return cudaGetLastError();
 }
