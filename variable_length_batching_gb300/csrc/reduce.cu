@@ -36,6 +36,10 @@ reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ row_len,
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const int bs = row_sample[r];
     const int64_t n = row_len[bs];
+    // the row's Eq. 5 weight beta_b, formed in double before the row's loads
+    // so that the (slow) fp64 division overlaps them
+    double wrow = 0.0;
+    if (kSq && threadIdx.x == 0) wrow = 1.5 - (double)bs / (2.0 * B);
     const T* zr = z + row_start[r] * C_z + lane * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float sq = 0.f;
@@ -71,7 +75,7 @@ reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ row_len,
       for (int i = threadIdx.x; i < kThreads; i += 32) v += sqs[i];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (threadIdx.x == 0) cta_sq += (1.5 - (double)bs / (2.0 * B)) * (double)v;
+      if (threadIdx.x == 0) cta_sq += wrow * (double)v;
     }
     if (grp == 0) {
       float tot[8];
