@@ -20,7 +20,7 @@ constexpr int kThreads = 128;
 // the row's total over the CTA in fp32, the rows in double, into
 // sq_part[blockIdx.x].
 template <typename T, bool kSq>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 12 : 10)   // the kSq variants at the plain ones' occupancy
 reduce_kernel(const T* __restrict__ z, const int32_t* __restrict__ row_len,
               const int32_t* __restrict__ row_sample, const int64_t* __restrict__ row_start,
               int64_t rows, int C_z, T* __restrict__ m, double* __restrict__ sq_part, int B) {
