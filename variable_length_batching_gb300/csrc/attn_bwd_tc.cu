@@ -101,6 +101,14 @@ __device__ __forceinline__ float row_dot64(const uint8_t* o_tile, const uint8_t*
   return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
+// The dK/dV kernels start, by programmatic dependent launch, while the dQ
+// kernel (which forms D) is still running: they read D only after
+// griddepcontrol.wait, and every thread waits once more on its way out, so
+// that no dK/dV CTA, and hence the grid, completes before the dQ kernel has.
+struct WaitForPrimaryAtExit {
+  __device__ ~WaitForPrimaryAtExit() { pdl_wait(); }
+};
+
 // The four MMAs of one M=128, N=64, K=64 product with both operands
 // K-major in shared memory.
 __device__ __forceinline__ void mma_kmajor(uint32_t d, uint32_t a_base, uint32_t b_base, uint32_t idesc) {
@@ -291,6 +299,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();                               // the dK/dV kernel may start its set-up
   const uint32_t tmem = bar.tmem_base;
 
   if (warp == 0) {
@@ -410,6 +419,7 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const int32_t* __restrict__ cu_k, int B, int64_t T_q, int64_t T_k, int H, int KT,
                     float scale, bf16* __restrict__ dk, bf16* __restrict__ dv, unsigned int* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  WaitForPrimaryAtExit at_exit;
   const int64_t item = blockIdx.x;
   const int h = (int)(item % H);
   const int64_t rest = item / H;
@@ -472,7 +482,9 @@ attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       issued = i + 1;
       // -lse in log2 units (-inf where there is no query, or the query saw no
       // key, so that P = 0 there) and -D, one pair per query column; only the
-      // compute threads wait for these, not the S^T / dP^T MMAs
+      // compute threads wait for these, not the S^T / dP^T MMAs.  D is the dQ
+      // kernel's.
+      pdl_wait();
       float* aux = reinterpret_cast<float*>(smem + kOffAux + st * kAuxBytes);
       for (int c = lane; c < kBN; c += 32) {
         float nLc = -INFINITY, nDc = 0.f;
@@ -771,6 +783,7 @@ attn_bwd_dkv_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_c
                         int64_t T_k, int H, int KT, float scale, bf16* __restrict__ dk, bf16* __restrict__ dv,
                         unsigned int* next, unsigned int* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  WaitForPrimaryAtExit at_exit;
   if (smem_u32(smem_raw) & 1023) {
     if (threadIdx.x == 0) flag_device(status, kDevCheck);
     return;
@@ -842,6 +855,7 @@ attn_bwd_dkv_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_c
           }
         }
         if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        pdl_wait();                            // D is the dQ kernel's
         float* aux = reinterpret_cast<float*>(smem + kOffAux + st * kAuxBytes);
         for (int c = lane; c < kBN; c += 32) {
           float nLc = -INFINITY, nDc = 0.f;
@@ -993,6 +1007,7 @@ attn_bwd_dq_persistent(const __grid_constant__ CUtensorMap tm_q, const __grid_co
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();                               // the dK/dV kernel may start its set-up
   const uint32_t tmem = bar.tmem_base;
   const unsigned int total = (unsigned int)B * (unsigned int)QT * (unsigned int)H;
 
@@ -1209,16 +1224,18 @@ cudaError_t launch_attn_bwd_tc(const AttnBwdProblem& p, float* Dbuf, unsigned in
     auto kkv = p.causal ? attn_bwd_dkv_persistent<true> : attn_bwd_dkv_persistent<false>;
     e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytesP);
     if (e != cudaSuccess) return e;
-    kkv<<<(unsigned)min64(items_k, slots), kThreads, kSmemBytesP, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q,
-                                                                       p.cu_k, p.B, p.T_q, p.T_k, p.H, KT, p.scale,
-                                                                       (bf16*)p.dk, (bf16*)p.dv, counters, status);
+    e = launch_pdl(kkv, dim3((unsigned)min64(items_k, slots)), dim3(kThreads), kSmemBytesP, s, k128, v128, q64, do64,
+                   p.lse, (const float*)Dbuf, p.cu_q, p.cu_k, p.B, p.T_q, p.T_k, p.H, KT, p.scale, (bf16*)p.dk,
+                   (bf16*)p.dv, counters, status);
+    if (e != cudaSuccess) return e;
   } else {
     auto kkv = p.causal ? attn_bwd_dkv_kernel<true> : attn_bwd_dkv_kernel<false>;
     e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kkv<<<(unsigned)items_k, kThreads, kSmemBytes, s>>>(k128, v128, q64, do64, p.lse, Dbuf, p.cu_q, p.cu_k, p.B,
-                                                         p.T_q, p.T_k, p.H, KT, p.scale, (bf16*)p.dk, (bf16*)p.dv,
-                                                         status);
+    e = launch_pdl(kkv, dim3((unsigned)items_k), dim3(kThreads), kSmemBytes, s, k128, v128, q64, do64, p.lse,
+                   (const float*)Dbuf, p.cu_q, p.cu_k, p.B, p.T_q, p.T_k, p.H, KT, p.scale, (bf16*)p.dk,
+                   (bf16*)p.dv, status);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
