@@ -17,8 +17,9 @@
 // the result does not depend on timing.
 //
 // Warps: 0 = TMA producer (3-stage ring), 1 = TMEM owner and MMA issuer,
-// 2-3 = column sums of A from the staged tiles (CTAs with nt == 0); then
-// all four warps write the accumulator (one row per thread).
+// 2-3 = column sums of A from the staged tiles (each column by one of the
+// CTAs that read the tile); then all four warps write the accumulator (one
+// row per thread).
 #include "tc_ptx.cuh"
 
 namespace nt {
@@ -60,6 +61,7 @@ __device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr, uint32_t atom_by
   return d;
 }
 
+template <int kTpp>
 __global__ void __launch_bounds__(kThreads)
 wgrad_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, int64_t P, int M,
                 int N, int chunks_per_split, float* __restrict__ part, float* __restrict__ col_part,
@@ -73,7 +75,13 @@ wgrad_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
   const int64_t nchunks_all = (P + kBP - 1) / kBP;
   const int64_t c0 = (int64_t)sp * chunks_per_split;
   const int nch = (int)max64(0, min64((int64_t)chunks_per_split, nchunks_all - c0));
-  const bool sums = col_part != nullptr && nt == 0;
+  // Column sums of the A tile, shared by the N / 128 CTAs that read it: CTA
+  // nt takes column pairs [p_lo, p_hi) of the tile's 64, and each pair is
+  // summed by kTpp consecutive threads (a power of two), thread `sub` taking
+  // every kTpp-th cell; the pair's partials are added in sub order at the end.
+  const int NT = N / kBN;
+  const int p_lo = nt * 64 / NT, p_hi = (nt + 1) * 64 / NT, npairs = p_hi - p_lo;
+  const bool sums = col_part != nullptr && npairs > 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -93,7 +101,7 @@ wgrad_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
   pdl_wait();
   pdl_trigger();
 
-  float csum[2] = {0.f, 0.f};                   // column sums: columns 2t, 2t + 1 of the 128
+  float csum[2] = {0.f, 0.f};                   // this thread's share of its column pair's sums
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tmap(&ta); prefetch_tmap(&tb);
@@ -132,26 +140,46 @@ wgrad_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ 
       mma_commit(&bar.acc_full);
     }
   } else {
-    // column sums of the A tiles, columns 2t and 2t + 1 (one 32-bit word per cell)
+    // column sums of the A tiles (one 32-bit word, a column pair, per cell)
     const int t = threadIdx.x - 64;             // 0..63
+    const int pair = t / kTpp, sub = t % kTpp;
+    const bool mine = sums && pair < npairs;
+    const int col = 2 * (p_lo + pair);          // the pair's first column in the tile
     for (int k = 0; k < nch; ++k) {
       const int st = k % kStages;
       if (!mbar_wait_warp(&bar.full[st], (k / kStages) & 1, abort_flag, status)) break;
-      if (sums) {
+      if (mine) {
         const uint8_t* a = smem + st * kStageBytes;
-#pragma unroll 8
-        for (int r = 0; r < kBP; ++r) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(a + swz128_offset(r, 2 * t, kBP));
-          csum[0] += bf16lo(w);
-          csum[1] += bf16hi(w);
+        float e0 = 0.f, e1 = 0.f, o0 = 0.f, o1 = 0.f;   // two chains
+#pragma unroll
+        for (int i = 0; i < kBP / (2 * kTpp); ++i) {
+          const int r = sub + 2 * kTpp * i;
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(a + swz128_offset(r, col, kBP));
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(a + swz128_offset(r + kTpp, col, kBP));
+          e0 += bf16lo(w);
+          e1 += bf16hi(w);
+          o0 += bf16lo(x);
+          o1 += bf16hi(x);
         }
+        csum[0] += e0 + o0;
+        csum[1] += e1 + o1;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar.empty[st]);
     }
-    if (sums) {
-      col_part[(int64_t)sp * M + mt * kBM + 2 * t] = csum[0];
-      col_part[(int64_t)sp * M + mt * kBM + 2 * t + 1] = csum[1];
+    // the pair's kTpp partials in sub order (the pair's threads share a
+    // warp: kTpp is a power of two and pairs start at multiples of it)
+    float tot0 = csum[0], tot1 = csum[1];
+#pragma unroll
+    for (int j = 1; j < kTpp; ++j) {
+      const float a0 = __shfl_down_sync(0xffffffffu, csum[0], j);
+      const float a1 = __shfl_down_sync(0xffffffffu, csum[1], j);
+      tot0 += a0;
+      tot1 += a1;
+    }
+    if (mine && sub == 0) {
+      col_part[(int64_t)sp * M + mt * kBM + col] = tot0;
+      col_part[(int64_t)sp * M + mt * kBM + col + 1] = tot1;
     }
   }
 
@@ -237,10 +265,17 @@ cudaError_t launch_wgrad_tc(const void* A, int lda, const void* B, int ldb, int6
   const int cps = (int)((chunks + splits - 1) / splits);
   float* part = static_cast<float*>(workspace);
   float* col_part = colsum ? part + (int64_t)splits * M * N : nullptr;
-  cudaError_t e = cudaFuncSetAttribute(wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  // threads per column pair: the largest power of two that lets every CTA's
+  // share of the 64 pairs (at most ceil(64 / NT)) fit its 64 summing threads
+  const int NT = N / kBN, most = (64 + NT - 1) / NT;
+  int tpp = 1;
+  while (tpp < 32 && 2 * tpp * most <= 64) tpp *= 2;
+  auto kern = tpp >= 32 ? wgrad_tc_kernel<32> : tpp == 16 ? wgrad_tc_kernel<16> : tpp == 8 ? wgrad_tc_kernel<8>
+            : tpp == 4 ? wgrad_tc_kernel<4> : tpp == 2 ? wgrad_tc_kernel<2> : wgrad_tc_kernel<1>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(wgrad_tc_kernel, dim3(M / kBM, N / kBN, splits), dim3(kThreads), kSmemBytes, s, ta, tb, P, M, N,
-                 cps, part, col_part, status);
+  e = launch_pdl(kern, dim3(M / kBM, N / kBN, splits), dim3(kThreads), kSmemBytes, s, ta, tb, P, M, N, cps, part,
+                 col_part, status);
   if (e != cudaSuccess) return e;
   const int64_t work = (int64_t)M * N + (colsum ? M : 0);
   wgrad_finish_kernel<<<(unsigned)min64((work + 255) / 256, (int64_t)sm_count() * 8), 256, 0, s>>>(
