@@ -919,11 +919,25 @@ constexpr int kSumRows = 2;                                   // rows per copy g
 constexpr int kSumBufs = 3;                                   // copy groups in flight
 constexpr int kSumHalf = kSumTile * kTcC * 4;                 // 32 cells of fp32 features: 16 KB
 constexpr int kSumStatBytes = 512;                             // the row's cells' (mean, rstd), from an even cell
-constexpr int kSumRowBytes = 2 * kSumHalf + 2 * kTcC * 4 + kSumStatBytes;   // dY, upstream, u[row], dM[row], stats
-constexpr size_t kSumSmem = (size_t)kSumBufs * kSumRows * kSumRowBytes + (size_t)kSumRows * kSumWarps * kTcC * 4 +
-                            kSumBufs * sizeof(uint64_t);
+// Staging of one row: dY, the upstream gradient (bf16 z~ on the one-call
+// route, else fp32), u[row], dM[row], the statistics.  With the smaller bf16
+// upstream the row-sum buffer is double-buffered (one barrier per copy group
+// instead of two: group k + 1 writes the half that group k - 1's reduction
+// read before group k's barrier).
+template <bool kUpBf16>
+struct SumLayout {
+  static constexpr int kUpBytes = kUpBf16 ? kSumTile * kTcC * 2 : kSumHalf;
+  static constexpr int kOffUp = kSumHalf;
+  static constexpr int kOffU = kSumHalf + kUpBytes;
+  static constexpr int kRowBytes = kOffU + 2 * kTcC * 4 + kSumStatBytes;
+  static constexpr int kRp = kUpBf16 ? 2 : 1;                 // row-sum buffers
+  static constexpr size_t kRpBytes = (size_t)kSumRows * kSumWarps * kTcC * 4;
+  static constexpr size_t kSmem = (size_t)kSumBufs * kSumRows * kRowBytes + kRp * kRpBytes + kSumBufs * sizeof(uint64_t);
+};
 static_assert(kSumRows * kSumWarps * kTcC >= kSumWarps * 2 * kTcC, "the row-sum buffer holds the dgamma/dbeta tail");
+static_assert(SumLayout<true>::kSmem <= 227 * 1024 && SumLayout<false>::kSmem <= 227 * 1024, "staging fits");
 
+template <bool kUpBf16>
 __global__ void __launch_bounds__(kSumThreads, 1)
 bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, const int64_t* __restrict__ pair_off,
                    const int32_t* __restrict__ cu, const int32_t* __restrict__ len, int B,
@@ -933,8 +947,9 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
                    float* __restrict__ dbeta, unsigned int* status) {
   extern __shared__ __align__(128) uint8_t sum_smem[];
   uint8_t* bufs = sum_smem;                                                        // [buf][row][dY | up]
-  float4* rp = reinterpret_cast<float4*>(sum_smem + (size_t)kSumBufs * kSumRows * kSumRowBytes);  // [row][warp][32]
-  uint64_t* full = reinterpret_cast<uint64_t*>(rp + kSumRows * kSumWarps * (kTcC / 4));
+  using L = SumLayout<kUpBf16>;
+  float4* rp0 = reinterpret_cast<float4*>(sum_smem + (size_t)kSumBufs * kSumRows * L::kRowBytes);  // [row][warp][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sum_smem + (size_t)kSumBufs * kSumRows * L::kRowBytes + L::kRp * L::kRpBytes);
   __shared__ float gs[kTcC];
   __shared__ int abort_flag;
   const int64_t g = blockIdx.x;
@@ -981,15 +996,15 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
     mbar_arrive_expect_tx(&full[buf], tx);
     for (int r = 0; r < nr; ++r) {
       const int64_t p = P0 + (int64_t)(a0 + r) * n + j0;
-      uint8_t* dst = bufs + (size_t)(buf * kSumRows + r) * kSumRowBytes;
+      uint8_t* dst = bufs + (size_t)(buf * kSumRows + r) * L::kRowBytes;
       const int64_t s0 = p & ~1LL;
-      bulk_load(dst + 2 * kSumHalf + 2 * kTcC * 4, stats + s0, (uint32_t)((((p + ncols + 1) & ~1LL) - s0) * 8),
+      bulk_load(dst + L::kOffU + 2 * kTcC * 4, stats + s0, (uint32_t)((((p + ncols + 1) & ~1LL) - s0) * 8),
                 &full[buf]);
-      bulk_load(dst + 2 * kSumHalf, u + (t0 + a0 + r) * kTcC, kTcC * 4, &full[buf]);
-      bulk_load(dst + 2 * kSumHalf + kTcC * 4, dM + (t0 + a0 + r) * kTcC, kTcC * 4, &full[buf]);
+      bulk_load(dst + L::kOffU, u + (t0 + a0 + r) * kTcC, kTcC * 4, &full[buf]);
+      bulk_load(dst + L::kOffU + kTcC * 4, dM + (t0 + a0 + r) * kTcC, kTcC * 4, &full[buf]);
       bulk_load(dst, dY + p * kTcC, (uint32_t)ncols * kTcC * 4, &full[buf]);
-      if (zt_up) bulk_load(dst + kSumHalf, zt_up + p * kTcC, (uint32_t)ncols * up_cell, &full[buf]);
-      else if (dz_up) bulk_load(dst + kSumHalf, dz_up + p * kTcC, (uint32_t)ncols * up_cell, &full[buf]);
+      if (kUpBf16) bulk_load(dst + L::kOffUp, zt_up + p * kTcC, (uint32_t)ncols * up_cell, &full[buf]);
+      else if (dz_up) bulk_load(dst + L::kOffUp, dz_up + p * kTcC, (uint32_t)ncols * up_cell, &full[buf]);
     }
   };
   if (threadIdx.x == 0)
@@ -1009,11 +1024,12 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
   int k = 0;
   for (; k < ngroups; ++k) {
     const int buf = k % kSumBufs, a0 = a_lo + k * kSumRows, nr = min(kSumRows, a_hi - a0);
+    float4* rp = rp0 + (size_t)(k % L::kRp) * (L::kRpBytes / sizeof(float4));
     // warp-uniform: the row arithmetic below has full-warp shuffles
     if (mbar_wait_warp(&full[buf], (uint32_t)(k / kSumBufs) & 1, &abort_flag, status)) {
       for (int r = 0; r < nr; ++r) {
-        const uint8_t* sr = bufs + (size_t)(buf * kSumRows + r) * kSumRowBytes;
-        const float* su = reinterpret_cast<const float*>(sr + 2 * kSumHalf);
+        const uint8_t* sr = bufs + (size_t)(buf * kSumRows + r) * L::kRowBytes;
+        const float* su = reinterpret_cast<const float*>(sr + L::kOffU);
         const float* sdm = su + kTcC;
         const int64_t pr0 = P0 + (int64_t)(a0 + r) * n + j0;      // the row's first cell
         const float2 st = reinterpret_cast<const float2*>(sdm + kTcC)[(pr0 & 1) + (cv ? slot : 0)];
@@ -1025,14 +1041,14 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
           const float4 y1 = *reinterpret_cast<const float4*>(sr + slot * kTcC * 4 + 256 + 16 * q);
           dy[0] = y0.x; dy[1] = y0.y; dy[2] = y0.z; dy[3] = y0.w;
           dy[4] = y1.x; dy[5] = y1.y; dy[6] = y1.z; dy[7] = y1.w;
-          if (zt_up) {
-            const uint2 w0 = *reinterpret_cast<const uint2*>(sr + kSumHalf + slot * kTcC * 2 + 8 * q);
-            const uint2 w1 = *reinterpret_cast<const uint2*>(sr + kSumHalf + slot * kTcC * 2 + 128 + 8 * q);
+          if (kUpBf16) {
+            const uint2 w0 = *reinterpret_cast<const uint2*>(sr + L::kOffUp + slot * kTcC * 2 + 8 * q);
+            const uint2 w1 = *reinterpret_cast<const uint2*>(sr + L::kOffUp + slot * kTcC * 2 + 128 + 8 * q);
             up[0] = gp * bf16lo(w0.x); up[1] = gp * bf16hi(w0.x); up[2] = gp * bf16lo(w0.y); up[3] = gp * bf16hi(w0.y);
             up[4] = gp * bf16lo(w1.x); up[5] = gp * bf16hi(w1.x); up[6] = gp * bf16lo(w1.y); up[7] = gp * bf16hi(w1.y);
           } else if (dz_up) {
-            const float4 u0 = *reinterpret_cast<const float4*>(sr + kSumHalf + slot * kTcC * 4 + 16 * q);
-            const float4 u1 = *reinterpret_cast<const float4*>(sr + kSumHalf + slot * kTcC * 4 + 256 + 16 * q);
+            const float4 u0 = *reinterpret_cast<const float4*>(sr + L::kOffUp + slot * kTcC * 4 + 16 * q);
+            const float4 u1 = *reinterpret_cast<const float4*>(sr + L::kOffUp + slot * kTcC * 4 + 256 + 16 * q);
             up[0] = u0.x; up[1] = u0.y; up[2] = u0.z; up[3] = u0.w;
             up[4] = u1.x; up[5] = u1.y; up[6] = u1.z; up[7] = u1.w;
           }
@@ -1117,7 +1133,7 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
         du_part[(pb0 + (int64_t)cc * n + a0 + r) * kTcC + f] = acc;
       }
     }
-    __syncthreads();
+    if (L::kRp == 1) __syncthreads();        // single buffer: read before the next group writes it
   }
   if (abort_flag) {
     // let the copies still in flight land before the CTA's shared memory goes
@@ -1132,9 +1148,10 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
     *reinterpret_cast<float4*>(o + 64 + 4 * q) = make_float4(cs[4], cs[5], cs[6], cs[7]);
   }
   // dgamma and dbeta over the item: the warp's two columns first (lane bit
-  // 4), then the 16 warps in warp order through the row-sum buffer (free
-  // since the last group's barrier), then one atomic per feature
-  float* red = reinterpret_cast<float*>(rp);          // [warp][dgamma | dbeta][C]
+  // 4), then the 16 warps in warp order through the row-sum buffer (once
+  // the last group's reduction has read it), then one atomic per feature
+  if (L::kRp > 1) __syncthreads();
+  float* red = reinterpret_cast<float*>(rp0);         // [warp][dgamma | dbeta][C]
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     pg[i] += __shfl_xor_sync(0xffffffffu, pg[i], 16);
@@ -1262,10 +1279,12 @@ cudaError_t cells_backward_tc(const BlockBwd& q, uint8_t* tcw, unsigned int* sta
   // the LayerNorm backward and the broadcast's: du, dv (dz is not stored), dgamma, dbeta
   const int64_t items = P / 1024 + p->T / 16 + p->B;
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if ((e = cudaFuncSetAttribute(bwd_ln_sums_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem)) !=
-      cudaSuccess)
+  const bool up_bf16 = q.zt_up != nullptr;
+  auto sums = up_bf16 ? bwd_ln_sums_kernel<true> : bwd_ln_sums_kernel<false>;
+  const size_t sums_smem = up_bf16 ? SumLayout<true>::kSmem : SumLayout<false>::kSmem;
+  if ((e = cudaFuncSetAttribute(sums, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sums_smem)) != cudaSuccess)
     return e;
-  bwd_ln_sums_kernel<<<(unsigned)items, kSumThreads, kSumSmem, s>>>(
+  sums<<<(unsigned)items, kSumThreads, sums_smem, s>>>(
       q.u, q.v, p->pair_off, p->cu_seqlens, p->lengths, p->B, q.gamma, stats, q.dM, q.dz_up, (const bf16*)q.zt_up,
       q.dz, du_part, dv_part, q.dgamma, q.dbeta, status);
   sums_finish_kernel<<<(unsigned)min64((p->T * C + kThreads - 1) / kThreads, (int64_t)sm_count() * 8), kThreads, 0,
