@@ -348,9 +348,14 @@ __global__ void __launch_bounds__(kThreads)
 colsum_kernel(const float* __restrict__ A, int64_t rows, int N, int splits, float* __restrict__ out) {
   const int64_t rlo = rows * blockIdx.y / splits, rhi = rows * (blockIdx.y + 1) / splits;
   for (int j = blockIdx.x * kThreads + threadIdx.x; j < N; j += gridDim.x * kThreads) {
-    float acc = 0.f;
-    for (int64_t r = rlo; r < rhi; ++r) acc += A[r * N + j];
-    atomicAdd(out + j, acc);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};                 // four loads in flight
+    int64_t r = rlo;
+    for (; r + 4 <= rhi; r += 4) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += A[(r + i) * N + j];
+    }
+    for (; r < rhi; ++r) acc[0] += A[r * N + j];
+    atomicAdd(out + j, (acc[0] + acc[1]) + (acc[2] + acc[3]));
   }
 }
 
@@ -691,8 +696,11 @@ cudaError_t block_backward_t(const BlockBwd& q, unsigned int* status, cudaStream
     const int splits = (int)min64(64, (Trows + 255) / 256);
     gram_kernel<T><<<dim3((Cs + kGT - 1) / kGT, (C + kGT - 1) / kGT, splits), kThreads, 0, s>>>(q.ds_out, (const T*)q.m,
                                                                                       Trows, Cs, C, splits, q.dW_g);
-    colsum_kernel<<<dim3((Cs + kThreads - 1) / kThreads, splits), kThreads, 0, s>>>(q.ds_out, Trows, Cs, splits,
-                                                                                     q.db_g);
+    // the column sums in splits of about 32 rows: each thread's chain of
+    // dependent loads and adds stays short
+    const int csplits = (int)min64(1024, (Trows + 31) / 32);
+    colsum_kernel<<<dim3((Cs + kThreads - 1) / kThreads, csplits), kThreads, 0, s>>>(q.ds_out, Trows, Cs, csplits,
+                                                                                      q.db_g);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // the pair cells: dz, dgamma, dbeta, db2, then dW1, dW2, db1
