@@ -928,19 +928,21 @@ constexpr int kSumBufs = 3;                                   // copy groups in 
 constexpr int kSumHalf = kSumTile * kTcC * 4;                 // 32 cells of fp32 features: 16 KB
 constexpr int kSumStatBytes = 512;                             // the row's cells' (mean, rstd), from an even cell
 // Staging of one row: dY, the upstream gradient (bf16 z~ on the one-call
-// route, else fp32), u[row], dM[row], the statistics.  With the smaller bf16
-// upstream the row-sum buffer is double-buffered (one barrier per copy group
-// instead of two: group k + 1 writes the half that group k - 1's reduction
-// read before group k's barrier).
+// route, else fp32), u[row], dM[row], the statistics.  The row-sum buffer is
+// double-buffered (one barrier per copy group instead of two: group k + 1
+// writes the half that group k - 1's reduction read before group k's
+// barrier); with the larger fp32 upstream that leaves room for two copy
+// groups in flight instead of three.
 template <bool kUpBf16>
 struct SumLayout {
   static constexpr int kUpBytes = kUpBf16 ? kSumTile * kTcC * 2 : kSumHalf;
   static constexpr int kOffUp = kSumHalf;
   static constexpr int kOffU = kSumHalf + kUpBytes;
   static constexpr int kRowBytes = kOffU + 2 * kTcC * 4 + kSumStatBytes;
-  static constexpr int kRp = kUpBf16 ? 2 : 1;                 // row-sum buffers
+  static constexpr int kBufs = kUpBf16 ? kSumBufs : 2;       // copy groups in flight
+  static constexpr int kRp = 2;                               // row-sum buffers
   static constexpr size_t kRpBytes = (size_t)kSumRows * kSumWarps * kTcC * 4;
-  static constexpr size_t kSmem = (size_t)kSumBufs * kSumRows * kRowBytes + kRp * kRpBytes + kSumBufs * sizeof(uint64_t);
+  static constexpr size_t kSmem = (size_t)kBufs * kSumRows * kRowBytes + kRp * kRpBytes + kBufs * sizeof(uint64_t);
 };
 static_assert(kSumRows * kSumWarps * kTcC >= kSumWarps * 2 * kTcC, "the row-sum buffer holds the dgamma/dbeta tail");
 static_assert(SumLayout<true>::kSmem <= 227 * 1024 && SumLayout<false>::kSmem <= 227 * 1024, "staging fits");
@@ -956,8 +958,8 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
   extern __shared__ __align__(128) uint8_t sum_smem[];
   uint8_t* bufs = sum_smem;                                                        // [buf][row][dY | up]
   using L = SumLayout<kUpBf16>;
-  float4* rp0 = reinterpret_cast<float4*>(sum_smem + (size_t)kSumBufs * kSumRows * L::kRowBytes);  // [row][warp][32]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sum_smem + (size_t)kSumBufs * kSumRows * L::kRowBytes + L::kRp * L::kRpBytes);
+  float4* rp0 = reinterpret_cast<float4*>(sum_smem + (size_t)L::kBufs * kSumRows * L::kRowBytes);  // [row][warp][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sum_smem + (size_t)L::kBufs * kSumRows * L::kRowBytes + L::kRp * L::kRpBytes);
   __shared__ float gs[kTcC];
   __shared__ int abort_flag;
   const int64_t g = blockIdx.x;
@@ -984,7 +986,7 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
   const float gp = zt_up ? eq5_pair_scale(b, B, kTcC, pair_off[B]) : 0.f;
   const uint32_t up_cell = zt_up ? kTcC * 2 : (dz_up ? kTcC * 4 : 0);   // upstream bytes per cell
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSumBufs; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < L::kBufs; ++i) mbar_init(&full[i], 1);
     fence_mbar_init();
     abort_flag = 0;
   }
@@ -992,7 +994,7 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
   __syncthreads();
   // copy group k: rows a_lo + 2k, a_lo + 2k + 1 into buffer k % 3
   auto issue = [&](int k) {
-    const int buf = k % kSumBufs, a0 = a_lo + k * kSumRows, nr = min(kSumRows, a_hi - a0);
+    const int buf = k % L::kBufs, a0 = a_lo + k * kSumRows, nr = min(kSumRows, a_hi - a0);
     // the stats copy starts at the even cell at or before the row's first
     // (8-byte entries, 16-byte copies) and ends at an even cell count: one
     // entry either side at most, inside the padded buffer
@@ -1016,7 +1018,7 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
     }
   };
   if (threadIdx.x == 0)
-    for (int k = 0; k < min(kSumBufs, ngroups); ++k) issue(k);
+    for (int k = 0; k < min(L::kBufs, ngroups); ++k) issue(k);
   float vv[8];          // the column's v, features 4q.. and 64+4q..
   {
     const float* vcol = v + (t0 + (cv ? j : j0)) * kTcC;
@@ -1031,10 +1033,10 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
   const bool hi4 = (lane & 16) != 0;
   int k = 0;
   for (; k < ngroups; ++k) {
-    const int buf = k % kSumBufs, a0 = a_lo + k * kSumRows, nr = min(kSumRows, a_hi - a0);
+    const int buf = k % L::kBufs, a0 = a_lo + k * kSumRows, nr = min(kSumRows, a_hi - a0);
     float4* rp = rp0 + (size_t)(k % L::kRp) * (L::kRpBytes / sizeof(float4));
     // warp-uniform: the row arithmetic below has full-warp shuffles
-    if (mbar_wait_warp(&full[buf], (uint32_t)(k / kSumBufs) & 1, &abort_flag, status)) {
+    if (mbar_wait_warp(&full[buf], (uint32_t)(k / L::kBufs) & 1, &abort_flag, status)) {
       for (int r = 0; r < nr; ++r) {
         const uint8_t* sr = bufs + (size_t)(buf * kSumRows + r) * L::kRowBytes;
         const float* su = reinterpret_cast<const float*>(sr + L::kOffU);
@@ -1130,7 +1132,7 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
     }
     __syncthreads();
     if (abort_flag) break;   // read after the barrier: the same in every thread
-    if (threadIdx.x == 0 && k + kSumBufs < ngroups) issue(k + kSumBufs);   // buffer k % 3 has been read
+    if (threadIdx.x == 0 && k + L::kBufs < ngroups) issue(k + L::kBufs);   // buffer k % kBufs has been read
     {
       const int f = threadIdx.x & (kTcC - 1), r = threadIdx.x / kTcC;
       if (r < nr) {
@@ -1141,13 +1143,12 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
         du_part[(pb0 + (int64_t)cc * n + a0 + r) * kTcC + f] = acc;
       }
     }
-    if (L::kRp == 1) __syncthreads();        // single buffer: read before the next group writes it
   }
   if (abort_flag) {
     // let the copies still in flight land before the CTA's shared memory goes
     if (threadIdx.x == 0)
-      for (int k2 = k; k2 < min(k + kSumBufs, ngroups); ++k2)
-        mbar_wait(&full[k2 % kSumBufs], (uint32_t)(k2 / kSumBufs) & 1, nullptr, status);
+      for (int k2 = k; k2 < min(k + L::kBufs, ngroups); ++k2)
+        mbar_wait(&full[k2 % L::kBufs], (uint32_t)(k2 / L::kBufs) & 1, nullptr, status);
     return;
   }
   if (cv) {
@@ -1158,7 +1159,7 @@ bwd_ln_sums_kernel(const float* __restrict__ u, const float* __restrict__ v, con
   // dgamma and dbeta over the item: the warp's two columns first (lane bit
   // 4), then the 16 warps in warp order through the row-sum buffer (once
   // the last group's reduction has read it), then one atomic per feature
-  if (L::kRp > 1) __syncthreads();
+  __syncthreads();
   float* red = reinterpret_cast<float*>(rp0);         // [warp][dgamma | dbeta][C]
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
