@@ -252,35 +252,45 @@ rowmm_kernel(const float* __restrict__ A, const T* __restrict__ W, const float* 
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int pass = 0; pass < (A2 ? 2 : 1); ++pass) {
+  // steps of 16 k over one or two (A, W) pairs: A 64 rows x 16 k (four
+  // consecutive k per thread, stored k-major), W 16 k x 64 columns (four
+  // consecutive columns per thread); the next step's values are loaded into
+  // registers while the current step's products run
+  const int ksteps = (K + kGK - 1) / kGK, nsteps = (A2 ? 2 : 1) * ksteps;
+  const int ra = threadIdx.x >> 2, ka = (threadIdx.x & 3) * 4;
+  const int kw = threadIdx.x >> 4, cw = (threadIdx.x & 15) * 4;
+  float na[4], nw[4];
+  auto fetch = [&](int step) {
+    const int pass = step / ksteps, k0 = (step % ksteps) * kGK;
     const float* Ap = pass ? A2 : A;
     const T* Wp = pass ? W2 : W;
-    for (int k0 = 0; k0 < K; k0 += kGK) {
-      {   // A: 64 rows x 16 k, four consecutive k per thread, stored k-major
-        const int rr = threadIdx.x >> 2, kk = (threadIdx.x & 3) * 4;
-        const int64_t r = r0 + rr;
+    const int64_t r = r0 + ra;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) as[kk + e][rr] = (r < rows && k0 + kk + e < K) ? Ap[r * K + k0 + kk + e] : 0.f;
-      }
-      {   // W: 16 k x 64 columns, four consecutive columns per thread
-        const int kk = threadIdx.x >> 4, cc = (threadIdx.x & 15) * 4;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          ws[kk][cc + e] = (k0 + kk < K && n0 + cc + e < N) ? to_f32(Wp[(int64_t)(k0 + kk) * N + n0 + cc + e]) : 0.f;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int kk = 0; kk < kGK; ++kk) {
-        const float4 a = *reinterpret_cast<const float4*>(&as[kk][4 * tr]);
-        const float4 w = *reinterpret_cast<const float4*>(&ws[kk][4 * tc]);
-        const float av[4] = {a.x, a.y, a.z, a.w}, wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], wv[j], acc[i][j]);
-      }
-      __syncthreads();
+    for (int e = 0; e < 4; ++e) {
+      na[e] = (r < rows && k0 + ka + e < K) ? Ap[r * K + k0 + ka + e] : 0.f;
+      nw[e] = (k0 + kw < K && n0 + cw + e < N) ? to_f32(Wp[(int64_t)(k0 + kw) * N + n0 + cw + e]) : 0.f;
     }
+  };
+  fetch(0);
+  for (int step = 0; step < nsteps; ++step) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      as[ka + e][ra] = na[e];
+      ws[kw][cw + e] = nw[e];
+    }
+    __syncthreads();
+    if (step + 1 < nsteps) fetch(step + 1);
+#pragma unroll
+    for (int kk = 0; kk < kGK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&as[kk][4 * tr]);
+      const float4 w = *reinterpret_cast<const float4*>(&ws[kk][4 * tc]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], wv[j], acc[i][j]);
+    }
+    __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -312,17 +322,28 @@ gram_kernel(const float* __restrict__ A, const TB* __restrict__ Bm, int64_t rows
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int64_t rb = rlo; rb < rhi; rb += kGK) {
-    {   // 16 rows x 64 columns of each operand, four consecutive columns per thread
-      const int rr = threadIdx.x >> 4, cc = (threadIdx.x & 15) * 4;
-      const int64_t r = rb + rr;
+  // 16 rows x 64 columns of each operand per step, four consecutive columns
+  // per thread; the next step's values are loaded into registers while the
+  // current step's products run
+  const int rr = threadIdx.x >> 4, cc = (threadIdx.x & 15) * 4;
+  float na[4], nb[4];
+  auto fetch = [&](int64_t rb) {
+    const int64_t r = rb + rr;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        as[rr][cc + e] = (r < rhi && i0 + cc + e < M) ? A[r * M + i0 + cc + e] : 0.f;
-        bs[rr][cc + e] = (r < rhi && j0 + cc + e < N) ? to_f32(Bm[r * N + j0 + cc + e]) : 0.f;
-      }
+    for (int e = 0; e < 4; ++e) {
+      na[e] = (r < rhi && i0 + cc + e < M) ? A[r * M + i0 + cc + e] : 0.f;
+      nb[e] = (r < rhi && j0 + cc + e < N) ? to_f32(Bm[r * N + j0 + cc + e]) : 0.f;
+    }
+  };
+  if (rlo < rhi) fetch(rlo);
+  for (int64_t rb = rlo; rb < rhi; rb += kGK) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      as[rr][cc + e] = na[e];
+      bs[rr][cc + e] = nb[e];
     }
     __syncthreads();
+    if (rb + kGK < rhi) fetch(rb + kGK);
 #pragma unroll
     for (int kk = 0; kk < kGK; ++kk) {
       const float4 a = *reinterpret_cast<const float4*>(&as[kk][4 * ti]);
